@@ -1,0 +1,426 @@
+"""Benchmark of the joint attention forward + backward on GB300.
+
+A step is one pass of the whole path -- forward (RoPE table, fused
+RMSNorm+RoPE prologue, attention) and backward (Delta, dK/dV, dQ, RoPE/RMSNorm
+backward, gain-gradient fold) -- over one batch of the 1024^2 CFG-pair
+workload (B=2, 24 heads x 128, 4096 image + 256 text tokens, valid text
+lengths 87 and 193), synthetic seeded inputs. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   (the CPU oracle on a bounded sample)
+
+value = credited algorithmic TFLOP/s (valid keys only; backward credited at
+2.5x the forward) of the whole job. Under torchrun each rank runs its own
+replica of the workload (the path has no exchange step) and value sums the
+ranks' work over the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from invariant_mmdit_joint_gb300 import workloads as W  # noqa: E402
+
+METRIC = "joint-attn fwd+bwd TFLOP/s and % of BF16 tensor peak at 1024² (4096 img+256 txt)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+LAUNCHES_PER_STEP = 9  # fwd: table, prologue, attention; bwd: pre, dkdv, dq, norm/rope, 2 folds
+THROTTLE_BITS = {
+    0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+    0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+    0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    def __init__(self, gpu_index: int):
+        import tempfile
+        self.proc = None
+        fd, self.path = tempfile.mkstemp(suffix=".csv", prefix="rlk_clocks_")
+        os.close(fd)
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], None, set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 4:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx = float(parts[1])
+                    bits = int(parts[3], 16)
+                except ValueError:
+                    continue
+                for bit, name in THROTTLE_BITS.items():
+                    if bits & bit:
+                        reasons.add(name)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return None
+        loaded = [s for s in sm if s > 0]
+        return {"sm_mhz": statistics.median(loaded or sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons - {"gpu_idle"})}
+
+
+# ---------------------------------------------------------------- per-kernel bytes / flops
+def kernel_work(w: W.Workload):
+    """Algorithmic work per launch of each kernel: ("tensor", flops) or ("hbm", bytes)."""
+    fl = W.credited_flops(w)
+    G = fl["gemm"]
+    rows = w.B * w.H * w.S
+    D = W.HEAD_DIM
+    n_pos = (max(w.grid_h // 2, w.grid_w // 2) + w.T_txt) + max((w.grid_h + 1) // 2, (w.grid_w + 1) // 2)
+    return {
+        "rope_table": ("hbm", n_pos * 64 * 8),
+        # read Q, K (bf16), write qh, kh (bf16) and r (fp32) of both
+        "prologue": ("hbm", 4 * rows * D * 2 + 2 * rows * 4),
+        # QK^T and PV
+        "attn_fwd": ("tensor", 2 * G),
+        # read O, dO (bf16); write Delta (fp32)
+        "bwd_pre": ("hbm", 2 * rows * D * 2 + rows * 4),
+        # recomputed S^T, dV, dP^T, dK: four of the five credited backward GEMMs
+        "bwd_dkdv": ("tensor", 4 * G),
+        # dQ: the fifth credited GEMM (its recomputed S and dP are not credited)
+        "bwd_dq": ("tensor", 1 * G),
+        # read dqh, dkh (fp32), Q, K (bf16), r; write dQ, dK (bf16)
+        "norm_rope_bwd": ("hbm", 2 * rows * D * 4 + 2 * rows * D * 2 + 2 * rows * 4 + 2 * rows * D * 2),
+        "dg_fold": ("hbm", 2 * rows // 64 * D * 4 + w.B * w.H * 4 * D * 4),
+    }
+
+
+def load_traffic(source_hash: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on this exact source tree."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return {}
+    with open(path) as f:
+        t = json.load(f)
+    if t.get("source_hash") != source_hash:
+        return {}
+    return t.get("kernels", {})
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+
+    import invariant_mmdit_joint_gb300 as pkg
+    from invariant_mmdit_joint_gb300 import _build
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = W.WORKLOADS[args.workload]
+    batch = W.make_batch(w, seed=0)
+    flops = W.credited_flops(w)
+
+    def to_host(bits):
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory()
+
+    h_q, h_k, h_v, h_do = (to_host(batch[n]) for n in ("q", "k", "v", "do"))
+    h_g = torch.from_numpy(batch["gains"]).pin_memory()
+    q, k, v, do = (t.to(dev) for t in (h_q, h_k, h_v, h_do))
+    gains = h_g.to(dev)
+    vl = [int(x) for x in batch["valid_len"]]
+    ja = pkg.JointAttention(w.B, w.T_txt, w.grid_h, w.grid_w, w.H, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dgp = torch.empty((w.B, w.H, 4, W.HEAD_DIM), dtype=torch.float32, device=dev)
+    dg = torch.empty((4, W.HEAD_DIM), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ja.forward(q, k, v, gains, vl, out=out, lse=lse)
+        ja.backward(q, k, v, gains, vl, out, do, lse, dq=dq, dk=dk, dv=dv, dg_partial=dgp, dg=dg)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    pkg.rlk_joint_attn_check_status()
+
+    # ---- device-resident timed region (inputs in HBM; working set > L2) ----
+    pkg.rlk_kernel_timing(True)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = e0.elapsed_time(e1)
+    kern = {}
+    for name in pkg.KERNEL_IDS:
+        tot, n = pkg.rlk_kernel_timing_read(name)
+        kern[name] = (tot, n)
+    pkg.rlk_kernel_timing(False)
+    pkg.rlk_joint_attn_check_status()
+    ms_max = ms_total
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    ms_step = ms_max / args.steps
+    value = world * flops["fwd_bwd"] / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers ----
+    h_out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    h_dq, h_dk, h_dv = (torch.empty(q.shape, dtype=torch.bfloat16).pin_memory() for _ in range(3))
+    h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    h_dg = torch.empty(dg.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_do, h_g))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dq, h_dk, h_dv, h_lse, h_dg))
+
+    def e2e_step():
+        for dst, src in ((q, h_q), (k, h_k), (v, h_v), (do, h_do), (gains, h_g)):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in ((h_out, out), (h_dq, dq), (h_dk, dk), (h_dv, dv), (h_lse, lse), (h_dg, dg)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(3, min(args.steps, 20))
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = e0.elapsed_time(e1) / n_e2e
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    e2e_value = world * flops["fwd_bwd"] / (ms_e2e * 1e-3) / 1e12
+
+    # ---- roofline of the dominant kernel ----
+    peaks, peak_src = load_peaks()
+    work = kernel_work(w)
+    traffic = load_traffic(_build.source_hash())
+    total_kernel_ms = sum(t for t, _ in kern.values()) or 1.0
+    per_kernel = {}
+    for name, (tot, n) in kern.items():
+        if n == 0:
+            continue
+        avg_ms = tot / n
+        bound, units = work[name]
+        if bound == "tensor":
+            ach = units / (avg_ms * 1e-3) / 1e12
+            peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+            unit = "TFLOP/s"
+        else:
+            ach = units / (avg_ms * 1e-3) / 1e9
+            peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+            unit = "GB/s"
+        per_kernel[name] = {"bound": bound, "avg_ms": round(avg_ms, 4), "launches": n,
+                            "share": round(tot / total_kernel_ms, 4), "achieved": round(ach, 2),
+                            "peak": peak, "unit": unit, "frac": round(ach / peak, 4)}
+    dom = max(per_kernel, key=lambda k: per_kernel[k]["share"])
+    d = per_kernel[dom]
+    tr = traffic.get(dom)
+    roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
+                "unit": d["unit"], "frac": d["frac"], "traffic": tr,
+                "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if d['bound'] == 'tensor' else 'hbm_gbs'})",
+                "algorithmic_per_launch": work[dom][1]}
+    bf16_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    bf16_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+
+    clocks = clk.summary()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, batch, budget_s=args.cpu_seconds)
+    trace = pkg.rlk_joint_attn_trace()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 inputs, U(0.5,1.5) gains)",
+        "pct_of_bf16_peak": round(100.0 * value / world / bf16_peak, 2),
+        "pct_of_bf16_peak_basis": f"{peak_src} sustained {bf16_peak} TFLOP/s (burst {bf16_burst})",
+        "config": {**w.describe(), "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "credited_gflop_per_step": round(flops["fwd_bwd"] / 1e9, 2),
+                   "l2": "inputs larger than L2: q,k,v,dO, ctx and workspace total "
+                         f"{(4 * w.B * w.S * w.H * 128 * 2) / 1e6:.0f} MB + scratch > 129 MB L2"},
+        "roofline": roofline, "kernels": per_kernel,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clocks,
+        "backend": trace["backend"], "fingerprint": trace["fingerprint"],
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------- oracle arm
+def _oracle_sample(w, batch, rows_per_sample, n_samples, seed=0):
+    """Time the CPU oracle on (sample, head, query-row block) samples of w."""
+    from oracle import joint_attn as O
+    rng = np.random.default_rng(seed)
+    g = batch["gains"].astype(np.float64)
+    done_flops, t_total = 0.0, 0.0
+    for i in range(n_samples):
+        b = i % w.B
+        h = int(rng.integers(0, w.H))
+        r0 = int(rng.integers(0, max(1, w.S - rows_per_sample)))
+        rows = np.arange(r0, min(w.S, r0 + rows_per_sample))
+        Q = O.widen_bf16(batch["q"][b:b + 1, :, h:h + 1])
+        K = O.widen_bf16(batch["k"][b:b + 1, :, h:h + 1])
+        V = O.widen_bf16(batch["v"][b:b + 1, :, h:h + 1])
+        dO = O.widen_bf16(batch["do"][b:b + 1, :, h:h + 1])
+        t0 = time.perf_counter()
+        O.pair_rows_forward_backward(Q, K, V, g, dO, w.T_txt, w.grid_h, w.grid_w, batch["valid_len"][b],
+                                     0, 0, rows)
+        t_total += time.perf_counter() - t0
+        done_flops += 7 * 2.0 * W.HEAD_DIM * len(rows) * (w.T_img + int(batch["valid_len"][b]))
+    return done_flops, t_total
+
+
+def cpu_baseline(w, batch, budget_s=20.0):
+    """The oracle as it stands, on the host cores: full (sample, head) pairs of
+    the workload until about ``budget_s`` seconds of work are done."""
+    fl, t = _oracle_sample(w, batch, w.S, 1)
+    n = 1
+    while t < budget_s and n < 2 * w.B * w.H:
+        f2, t2 = _oracle_sample(w, batch, w.S, 1, seed=n)
+        fl += f2
+        t += t2
+        n += 1
+    return {"value": round(fl / t / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{n} full (sample, head) pairs of {w.name}, forward+backward, float64 numpy "
+                      f"(BLAS threads = host cores); credited flops of the sample / wall time"}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    w = W.WORKLOADS[args.workload]
+    batch = W.make_batch(w, seed=0)
+    # size each step so the whole run stays within about two minutes
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    f1, t1 = _oracle_sample(w, batch, 64, 1)
+    rows = int(max(16, min(w.S, 64 * per_step_budget / max(t1, 1e-3))))
+    for i in range(args.warmup):
+        _oracle_sample(w, batch, rows, 1, seed=1000 + i)
+    fl_tot, t_tot = 0.0, 0.0
+    for i in range(args.steps):
+        f, t = _oracle_sample(w, batch, rows, 1, seed=i)
+        fl_tot += f
+        t_tot += t
+    value = fl_tot / t_tot / 1e12
+    sample = (f"each step: forward+backward of {rows} consecutive query rows of one (sample, head) "
+              f"pair of {w.name} against all keys, float64 numpy oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * t_tot / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {**w.describe(), "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default="cfg1024")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "ours":
+        args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+/*
+ * rlk_joint_attn.h -- C ABI of the deterministic, batch-invariant joint
+ * attention of a Qwen-Image MMDiT block (forward and backward), with its
+ * QK-RMSNorm + three-axis RoPE prologue, for one NVIDIA GB300 (sm_103).
+ *
+ * What the operation is (sources are the RL-Kernel GitHub threads):
+ *   "[RFC][Qwen-Image][CUDA/ROCm] WS1/WS2 kernel roadmap ... #386",
+ *     Model contract table: 24 heads x 128; joint non-causal attention over
+ *     [text, image]; padded prompts need a key mask; learned-gain per-head
+ *     RMSNorm (eps 1e-6) on Q and K before RoPE; RoPE axes [16, 56, 56],
+ *     theta 10000, centred spatial indices, text offset max(H/2, W/2).
+ *     Numerical requirements: fixed reduction trees, FP32 accumulators, no
+ *     split-K / stream-K / split-KV / atomics, no TF32 or fast math, one
+ *     FP32->BF16 cast at the output, batch invariance, fail closed.
+ *     WS1 table rows qk_rmsnorm, multi_axis_rope, joint_attn_qk_gemm,
+ *     joint_attn_softmax, joint_attn_av_gemm, joint_attention_fused.
+ *   "[RFC] [Qwen-Image] WS1 Single-GPU Kernel List", Kernel table: the same
+ *     rows with "fwd + bwd"; rule 7 (trace records).
+ *
+ * Notation: B samples, H heads, D = 128, T_txt text tokens (the padded text
+ * length, equal for all samples), T_img = grid_h * grid_w image tokens,
+ * S = T_txt + T_img. Token n < T_txt is text token n; token T_txt + r*grid_w + c
+ * is image token (row r, column c). L_b = valid text length of sample b: text
+ * keys L_b <= n < T_txt are masked (padded prompt tokens).
+ *
+ * Per (sample b, head h), with x a row of Q or K:
+ *   qk_rmsnorm:      r = 1 / sqrt(mean_d(x_d^2) + eps);  y = x * r * g
+ *                    (g = the stream's gain: text rows use *_txt, image *_img)
+ *   multi_axis_rope: dims [0,16) follow the frame axis, [16,72) the row axis,
+ *                    [72,128) the column axis; pair (2j, 2j+1) of an axis
+ *                    block of width d_a turns by pos_a * theta^(-2j/d_a).
+ *                    Image token (r, c): pos = (0, r - ceil(gh/2), c - ceil(gw/2));
+ *                    text token t: pos = (o+t, o+t, o+t), o = max(gh/2, gw/2)
+ *                    (integer halves).
+ *   attention:       s_ij = qh_i . kh_j / sqrt(128) over valid keys j;
+ *                    P = softmax_j(s); O = P V; lse_i = log sum_j exp(s_ij).
+ *
+ * Layouts (all row-major, innermost index last):
+ *   q, k, v, out, dout, dq, dk, dv : bf16 [B, S, H, D]  (D contiguous, then H)
+ *   lse                            : fp32 [B, H, S]      (natural log)
+ *   gains                          : fp32 [D] each, four vectors
+ *   dg_partial                     : fp32 [B, H, 4, D]   slots (q_txt, k_txt, q_img, k_img)
+ *   dg                             : fp32 [4, D]         same slots
+ *   txt_valid_len                  : int32 [B], HOST memory, 0 <= L_b <= T_txt
+ *
+ * Ownership and streams: the caller owns and allocates every buffer (inputs,
+ * outputs, ctx, workspace) on the current CUDA device. The library never
+ * allocates or frees device memory and never synchronises, except in
+ * rlk_joint_attn_check_status(). Every call enqueues its kernels on `stream`
+ * (a cudaStream_t passed as void*; NULL = the legacy default stream) and
+ * returns as soon as they are enqueued. Host arrays are read before return.
+ *
+ * Errors: every entry point returns an rlk_status. On any validation error
+ * nothing is launched and no output is touched. Unsupported configurations
+ * fail closed with RLK_ERR_UNSUPPORTED; there is no fallback path.
+ *
+ * Determinism: each output tile is produced by exactly one CTA whose visit
+ * order over the other operand is fixed (text tiles from token 0, then image
+ * tiles from token T_txt, ascending; tiles with no valid key are skipped).
+ * Tile geometry depends on nothing but (T_txt, grid_h, grid_w), so a row's
+ * bytes are the same for any B, any batch position, any run, and whether or
+ * not lse is requested.
+ */
+#ifndef RLK_JOINT_ATTN_H
+#define RLK_JOINT_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rlk_status {
+    RLK_OK = 0,
+    RLK_ERR_INVALID_ARG = 1,   /* null pointer, bad size, L_b outside [0, T_txt] */
+    RLK_ERR_UNSUPPORTED = 2,   /* D != 128, axes != {16,56,56}, not sm_103, fast-math build */
+    RLK_ERR_ALIGNMENT = 3,     /* a device pointer not 16-byte aligned */
+    RLK_ERR_WORKSPACE = 4,     /* workspace smaller than rlk_joint_attn_bwd_workspace_bytes() */
+    RLK_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
+    RLK_ERR_DEVICE_TIMEOUT = 6 /* a bounded device-side wait gave up (see check_status) */
+} rlk_status;
+
+/* Largest batch one call accepts (valid lengths travel as kernel arguments). */
+#define RLK_MAX_BATCH 256
+
+typedef struct rlk_ja_shape {
+    int32_t B;        /* samples, 1 .. RLK_MAX_BATCH */
+    int32_t T_txt;    /* padded text length, >= 0 */
+    int32_t grid_h;   /* image token rows, >= 1 */
+    int32_t grid_w;   /* image token columns, >= 1 */
+    int32_t H;        /* heads, >= 1 */
+    int32_t D;        /* head dim; must be 128 */
+    float eps;        /* RMSNorm epsilon (the model uses 1e-6), > 0 */
+    float theta;      /* RoPE base (the model uses 10000), > 1 */
+    int32_t axes[3];  /* RoPE axis split; must be {16, 56, 56} */
+} rlk_ja_shape;
+
+/* Bytes of the forward context `ctx`: normed+rotated q and k (bf16
+ * [B, H, S, D] each), the RMSNorm factors r of q and k (fp32 [B, H, S] each)
+ * and the cos/sin table. The forward writes it; the backward reads it. Returns
+ * 0 for an invalid shape. */
+size_t rlk_joint_attn_ctx_bytes(const rlk_ja_shape* shape);
+
+/* Bytes of the backward scratch `workspace`: rowsum(dO * O) (fp32 [B, H, S]),
+ * the fp32 gradients of the rotated q and k ([B, H, S, D] each) and the
+ * per-chunk gain-gradient partials. Returns 0 for an invalid shape. */
+size_t rlk_joint_attn_bwd_workspace_bytes(const rlk_ja_shape* shape);
+
+/* Forward: rows qk_rmsnorm, multi_axis_rope, joint_attn_qk_gemm,
+ * joint_attn_softmax and joint_attn_av_gemm of the RFC's WS1 table, fused.
+ *   q, k, v         device bf16 [B, S, H, D], read only
+ *   g_q_txt ... g_k_img  device fp32 [D] each, read only
+ *   txt_valid_len   HOST int32 [B]
+ *   out             device bf16 [B, S, H, D], written (every row, padded
+ *                   text query rows included)
+ *   lse             device fp32 [B, H, S] or NULL (then not written; `out`
+ *                   bytes do not change)
+ *   ctx             device, rlk_joint_attn_ctx_bytes() bytes, written; keep
+ *                   it for the backward
+ * All device pointers must be 16-byte aligned. */
+rlk_status rlk_joint_attn_fwd(const rlk_ja_shape* shape,
+                              const void* q, const void* k, const void* v,
+                              const float* g_q_txt, const float* g_k_txt,
+                              const float* g_q_img, const float* g_k_img,
+                              const int32_t* txt_valid_len,
+                              void* out, float* lse, void* ctx, void* stream);
+
+/* Backward of the whole path: gradients of sum(out * dout).
+ *   q, k, v, gains, txt_valid_len  as in the forward (same values)
+ *   out, lse, ctx   what the forward wrote for these inputs (lse required)
+ *   dout            device bf16 [B, S, H, D]
+ *   dq, dk, dv      device bf16 [B, S, H, D], written; masked keys get 0
+ *   dg_partial      device fp32 [B, H, 4, D] or NULL: per (sample, head)
+ *                   gain gradients, each summed over one stream's tokens in
+ *                   a fixed order; these are batch invariant
+ *   dg              device fp32 [4, D], written: dg_partial summed over h
+ *                   ascending, then over b ascending
+ *   workspace       device scratch of >= rlk_joint_attn_bwd_workspace_bytes()
+ * Note: a padded text query row with nonzero dout feeds the key and value
+ * gradients of the valid keys, as the mathematics says. */
+rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape,
+                              const void* q, const void* k, const void* v,
+                              const float* g_q_txt, const float* g_k_txt,
+                              const float* g_q_img, const float* g_k_img,
+                              const int32_t* txt_valid_len,
+                              const void* out, const void* dout,
+                              const float* lse, const void* ctx,
+                              void* dq, void* dk, void* dv,
+                              float* dg_partial, float* dg,
+                              void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/* Synchronises `stream`, then reads and clears the device-side error word
+ * that bounded waits in the kernels set when they give up. Returns RLK_OK,
+ * RLK_ERR_DEVICE_TIMEOUT, or RLK_ERR_CUDA if the stream reported an error. */
+rlk_status rlk_joint_attn_check_status(void* stream);
+
+/* Runs, on the current device, a probe kernel compiled in each translation
+ * unit with that unit's flags: a subnormal product must survive, and
+ * division, square root and expf must keep IEEE / library accuracy. These
+ * all change under --use_fast_math (nvcc defines no macro for it in device
+ * code). Returns 1 if every unit is strict, 0 if not, -1 on a CUDA error.
+ * The first forward/backward call on a device runs it and fails closed with
+ * RLK_ERR_UNSUPPORTED if it returns 0.
+ * Source: PR #537 (adaln_mod_projection) review thread on the strict-math
+ * check, which replaced a macro test by a probe kernel. */
+int rlk_strict_math_compiled(void);
+
+typedef struct rlk_ja_trace {
+    char backend[32];          /* e.g. "sm_103a" + engine name */
+    char reduction_order[160]; /* how each sum is ordered */
+    char accumulator[16];      /* "fp32" */
+    int32_t split_k;           /* 0: no split-K / stream-K / split-KV */
+    int32_t atomics;           /* 0: no atomic accumulation */
+    int32_t tf32;              /* 0: TF32 off */
+    int32_t strict_math;       /* rlk_strict_math_compiled() at trace time */
+    int32_t block_q;           /* query rows per forward tile */
+    int32_t block_kv;          /* keys per forward tile */
+    char fingerprint[96];      /* source hash and build flags */
+} rlk_ja_trace;
+
+/* Fills the trace record of the WS1 kernel list's rule 7 (reduction order,
+ * accumulator precision, split-K state, TF32 state, kernel fingerprint,
+ * selected backend). */
+rlk_status rlk_joint_attn_trace(rlk_ja_trace* out);
+
+/* Human-readable text of a status code (static storage). */
+const char* rlk_strerror(int status);
+
+/* Kernel timing for benchmarks. kernel ids: 0 rope table, 1 prologue,
+ * 2 attention forward, 3 backward preprocess, 4 dK/dV, 5 dQ,
+ * 6 RoPE/RMSNorm backward, 7 gain-gradient fold.
+ * rlk_kernel_timing(1) makes later calls record a CUDA event pair around
+ * every launch (up to 4096 launches per kernel id); rlk_kernel_timing(0)
+ * stops and clears. rlk_kernel_timing_read() waits for the recorded events
+ * and returns the summed milliseconds and the launch count of one kernel id
+ * since the last clear. */
+rlk_status rlk_kernel_timing(int enable);
+rlk_status rlk_kernel_timing_read(int kernel_id, double* total_ms, int32_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RLK_JOINT_ATTN_H */

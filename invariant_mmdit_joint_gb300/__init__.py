@@ -1,0 +1,315 @@
+"""Deterministic, batch-invariant joint attention of a Qwen-Image MMDiT block
+(forward and backward, with the QK-RMSNorm + three-axis RoPE prologue) for one
+NVIDIA GB300.
+
+This module is a thin binding over the C ABI of ``librlk_joint_attn.so``
+(declared in ``include/rlk_joint_attn.h``): it marshals arguments and checks
+shapes so that no bad pointer reaches the library. Every step of the path runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback. If the
+library is missing, loading it raises.
+
+PyTorch is used only for device memory and streams.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+__all__ = [
+    "Shape", "RlkError", "lib", "library_path", "load_library",
+    "rlk_joint_attn_ctx_bytes", "rlk_joint_attn_bwd_workspace_bytes",
+    "rlk_joint_attn_fwd", "rlk_joint_attn_bwd", "rlk_joint_attn_check_status",
+    "rlk_strict_math_compiled", "rlk_joint_attn_trace", "rlk_strerror",
+    "rlk_kernel_timing", "rlk_kernel_timing_read", "JointAttention",
+    "EXPORTED_SYMBOLS", "KERNEL_IDS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_NAME = "librlk_joint_attn.so"
+HEAD_DIM = 128
+AXES = (16, 56, 56)
+MAX_BATCH = 256
+
+RLK_OK = 0
+STATUS_NAMES = {
+    0: "RLK_OK", 1: "RLK_ERR_INVALID_ARG", 2: "RLK_ERR_UNSUPPORTED", 3: "RLK_ERR_ALIGNMENT",
+    4: "RLK_ERR_WORKSPACE", 5: "RLK_ERR_CUDA", 6: "RLK_ERR_DEVICE_TIMEOUT",
+}
+KERNEL_IDS = {
+    "rope_table": 0, "prologue": 1, "attn_fwd": 2, "bwd_pre": 3,
+    "bwd_dkdv": 4, "bwd_dq": 5, "norm_rope_bwd": 6, "dg_fold": 7,
+}
+# Every symbol include/rlk_joint_attn.h declares.
+EXPORTED_SYMBOLS = (
+    "rlk_joint_attn_ctx_bytes", "rlk_joint_attn_bwd_workspace_bytes",
+    "rlk_joint_attn_fwd", "rlk_joint_attn_bwd", "rlk_joint_attn_check_status",
+    "rlk_strict_math_compiled", "rlk_joint_attn_trace", "rlk_strerror",
+    "rlk_kernel_timing", "rlk_kernel_timing_read",
+)
+
+
+class Shape(ctypes.Structure):
+    """rlk_ja_shape."""
+    _fields_ = [
+        ("B", ctypes.c_int32), ("T_txt", ctypes.c_int32), ("grid_h", ctypes.c_int32),
+        ("grid_w", ctypes.c_int32), ("H", ctypes.c_int32), ("D", ctypes.c_int32),
+        ("eps", ctypes.c_float), ("theta", ctypes.c_float), ("axes", ctypes.c_int32 * 3),
+    ]
+
+    @classmethod
+    def make(cls, B, T_txt, grid_h, grid_w, H, D=HEAD_DIM, eps=1e-6, theta=10000.0, axes=AXES):
+        s = cls()
+        s.B, s.T_txt, s.grid_h, s.grid_w, s.H, s.D = B, T_txt, grid_h, grid_w, H, D
+        s.eps, s.theta = eps, theta
+        s.axes[0], s.axes[1], s.axes[2] = axes
+        return s
+
+    @property
+    def S(self) -> int:
+        return self.T_txt + self.grid_h * self.grid_w
+
+
+class Trace(ctypes.Structure):
+    """rlk_ja_trace."""
+    _fields_ = [
+        ("backend", ctypes.c_char * 32), ("reduction_order", ctypes.c_char * 160),
+        ("accumulator", ctypes.c_char * 16), ("split_k", ctypes.c_int32),
+        ("atomics", ctypes.c_int32), ("tf32", ctypes.c_int32), ("strict_math", ctypes.c_int32),
+        ("block_q", ctypes.c_int32), ("block_kv", ctypes.c_int32),
+        ("fingerprint", ctypes.c_char * 96),
+    ]
+
+
+class RlkError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({_strerror(code)})")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, LIB_NAME)
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load a build of the library and declare its signatures."""
+    path = path or library_path()
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`. "
+            "There is no fallback implementation.")
+    L = ctypes.CDLL(path)
+    vp, sz, i32, f32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.POINTER(ctypes.c_float)
+    shp = ctypes.POINTER(Shape)
+    L.rlk_joint_attn_ctx_bytes.argtypes = [shp]
+    L.rlk_joint_attn_ctx_bytes.restype = sz
+    L.rlk_joint_attn_bwd_workspace_bytes.argtypes = [shp]
+    L.rlk_joint_attn_bwd_workspace_bytes.restype = sz
+    L.rlk_joint_attn_fwd.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_int32),
+                                     vp, vp, vp, vp]
+    L.rlk_joint_attn_fwd.restype = i32
+    L.rlk_joint_attn_bwd.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_int32),
+                                     vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.rlk_joint_attn_bwd.restype = i32
+    L.rlk_joint_attn_check_status.argtypes = [vp]
+    L.rlk_joint_attn_check_status.restype = i32
+    L.rlk_strict_math_compiled.argtypes = []
+    L.rlk_strict_math_compiled.restype = i32
+    L.rlk_joint_attn_trace.argtypes = [ctypes.POINTER(Trace)]
+    L.rlk_joint_attn_trace.restype = i32
+    L.rlk_strerror.argtypes = [i32]
+    L.rlk_strerror.restype = ctypes.c_char_p
+    L.rlk_kernel_timing.argtypes = [i32]
+    L.rlk_kernel_timing.restype = i32
+    L.rlk_kernel_timing_read.argtypes = [i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)]
+    L.rlk_kernel_timing_read.restype = i32
+    return L
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = load_library()
+    return _lib
+
+
+def _strerror(code: int) -> str:
+    try:
+        return lib().rlk_strerror(code).decode()
+    except Exception:  # the library itself failed to load
+        return "?"
+
+
+def _check(code: int, where: str) -> None:
+    if code != RLK_OK:
+        raise RlkError(code, where)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _lengths(valid_len: Sequence[int]):
+    vals = [int(x) for x in valid_len]
+    return (ctypes.c_int32 * max(1, len(vals)))(*vals)
+
+
+def rlk_joint_attn_ctx_bytes(shape: Shape) -> int:
+    return int(lib().rlk_joint_attn_ctx_bytes(ctypes.byref(shape)))
+
+
+def rlk_joint_attn_bwd_workspace_bytes(shape: Shape) -> int:
+    return int(lib().rlk_joint_attn_bwd_workspace_bytes(ctypes.byref(shape)))
+
+
+def rlk_joint_attn_fwd(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_valid_len,
+                       out, lse, ctx, stream=None) -> None:
+    """Enqueue the forward; tensors or raw device pointers (ints)."""
+    rc = lib().rlk_joint_attn_fwd(
+        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_q_txt), _ptr(g_k_txt),
+        _ptr(g_q_img), _ptr(g_k_img), _lengths(txt_valid_len), _ptr(out), _ptr(lse), _ptr(ctx),
+        _stream_handle(stream))
+    _check(rc, "rlk_joint_attn_fwd")
+
+
+def rlk_joint_attn_bwd(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_valid_len,
+                       out, dout, lse, ctx, dq, dk, dv, dg_partial, dg, workspace,
+                       workspace_bytes=None, stream=None) -> None:
+    """Enqueue the backward; tensors or raw device pointers (ints)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().rlk_joint_attn_bwd(
+        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_q_txt), _ptr(g_k_txt),
+        _ptr(g_q_img), _ptr(g_k_img), _lengths(txt_valid_len), _ptr(out), _ptr(dout), _ptr(lse),
+        _ptr(ctx), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg_partial), _ptr(dg), _ptr(workspace),
+        int(workspace_bytes), _stream_handle(stream))
+    _check(rc, "rlk_joint_attn_bwd")
+
+
+def rlk_joint_attn_check_status(stream=None) -> None:
+    _check(lib().rlk_joint_attn_check_status(_stream_handle(stream)), "rlk_joint_attn_check_status")
+
+
+def rlk_strict_math_compiled() -> int:
+    return int(lib().rlk_strict_math_compiled())
+
+
+def rlk_joint_attn_trace() -> dict:
+    t = Trace()
+    _check(lib().rlk_joint_attn_trace(ctypes.byref(t)), "rlk_joint_attn_trace")
+    return {f: (getattr(t, f).decode() if isinstance(getattr(t, f), bytes) else getattr(t, f))
+            for f, _ in Trace._fields_}
+
+
+def rlk_strerror(code: int) -> str:
+    return _strerror(code)
+
+
+def rlk_kernel_timing(enable: bool) -> None:
+    _check(lib().rlk_kernel_timing(1 if enable else 0), "rlk_kernel_timing")
+
+
+def rlk_kernel_timing_read(kernel: str | int) -> tuple[float, int]:
+    kid = KERNEL_IDS[kernel] if isinstance(kernel, str) else int(kernel)
+    ms, n = ctypes.c_double(), ctypes.c_int32()
+    _check(lib().rlk_kernel_timing_read(kid, ctypes.byref(ms), ctypes.byref(n)), "rlk_kernel_timing_read")
+    return ms.value, n.value
+
+
+class JointAttention:
+    """Buffers + calls for one geometry: allocates the caller-owned tensors
+    with PyTorch and passes them to the C ABI. Inputs are bf16 [B, S, H, 128]
+    CUDA tensors; gains a float32 [4, 128] tensor (q_txt, k_txt, q_img, k_img)."""
+
+    def __init__(self, B: int, T_txt: int, grid_h: int, grid_w: int, H: int, device="cuda",
+                 eps: float = 1e-6, theta: float = 10000.0):
+        import torch
+        self.shape = Shape.make(B, T_txt, grid_h, grid_w, H, eps=eps, theta=theta)
+        self.device = torch.device(device)
+        n_ctx = rlk_joint_attn_ctx_bytes(self.shape)
+        n_ws = rlk_joint_attn_bwd_workspace_bytes(self.shape)
+        if n_ctx == 0 or n_ws == 0:
+            raise RlkError(1, "JointAttention: invalid shape")
+        self.ctx = torch.empty(n_ctx, dtype=torch.uint8, device=self.device)
+        self.workspace = torch.empty(n_ws, dtype=torch.uint8, device=self.device)
+
+    def _check_inputs(self, *ts):
+        import torch
+        sh = self.shape
+        want = (sh.B, sh.S, sh.H, HEAD_DIM)
+        for t in ts:
+            if t.dtype != torch.bfloat16 or tuple(t.shape) != want or not t.is_contiguous() or t.device != self.device:
+                raise ValueError(f"expected contiguous bf16 {want} on {self.device}, got {t.dtype} "
+                                 f"{tuple(t.shape)} on {t.device}")
+
+    def _check_gains(self, gains):
+        import torch
+        if gains.dtype != torch.float32 or tuple(gains.shape) != (4, HEAD_DIM) or not gains.is_contiguous() \
+                or gains.device != self.device:
+            raise ValueError("gains must be a contiguous float32 [4, 128] tensor on the device")
+
+    def forward(self, q, k, v, gains, valid_len, out=None, lse=None, want_lse=True, stream=None):
+        import torch
+        self._check_inputs(q, k, v)
+        self._check_gains(gains)
+        if len(valid_len) != self.shape.B:
+            raise ValueError("one valid length per sample")
+        out = torch.empty_like(q) if out is None else out
+        if lse is None and want_lse:
+            lse = torch.empty((self.shape.B, self.shape.H, self.shape.S), dtype=torch.float32, device=self.device)
+        rlk_joint_attn_fwd(self.shape, q, k, v, gains[0], gains[1], gains[2], gains[3], valid_len,
+                           out, lse, self.ctx, stream)
+        return out, lse
+
+    def backward(self, q, k, v, gains, valid_len, out, dout, lse, dq=None, dk=None, dv=None,
+                 dg_partial=None, dg=None, stream=None):
+        import torch
+        self._check_inputs(q, k, v, out, dout)
+        self._check_gains(gains)
+        sh = self.shape
+        dq = torch.empty_like(q) if dq is None else dq
+        dk = torch.empty_like(k) if dk is None else dk
+        dv = torch.empty_like(v) if dv is None else dv
+        if dg_partial is None:
+            dg_partial = torch.empty((sh.B, sh.H, 4, HEAD_DIM), dtype=torch.float32, device=self.device)
+        if dg is None:
+            dg = torch.empty((4, HEAD_DIM), dtype=torch.float32, device=self.device)
+        rlk_joint_attn_bwd(sh, q, k, v, gains[0], gains[1], gains[2], gains[3], valid_len, out, dout,
+                           lse, self.ctx, dq, dk, dv, dg_partial, dg, self.workspace, stream=stream)
+        return dq, dk, dv, dg_partial, dg
+
+    def ctx_views(self):
+        """Views of the forward context: qh, kh bf16 [B, H, S, 128]; rq, rk fp32 [B, H, S].
+        The offsets follow the library's ctx layout (regions aligned to 256 bytes)."""
+        import torch
+        sh = self.shape
+        rows = sh.B * sh.H * sh.S
+
+        def up(x):
+            return (x + 255) // 256 * 256
+        o_kh = up(rows * HEAD_DIM * 2)
+        o_rq = up(o_kh + rows * HEAD_DIM * 2)
+        o_rk = up(o_rq + rows * 4)
+        c = self.ctx
+        qh = c[:rows * HEAD_DIM * 2].view(torch.bfloat16).view(sh.B, sh.H, sh.S, HEAD_DIM)
+        kh = c[o_kh:o_kh + rows * HEAD_DIM * 2].view(torch.bfloat16).view(sh.B, sh.H, sh.S, HEAD_DIM)
+        rq = c[o_rq:o_rq + rows * 4].view(torch.float32).view(sh.B, sh.H, sh.S)
+        rk = c[o_rk:o_rk + rows * 4].view(torch.float32).view(sh.B, sh.H, sh.S)
+        return qh, kh, rq, rk

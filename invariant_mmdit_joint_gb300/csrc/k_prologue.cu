@@ -1,0 +1,323 @@
+// HBM-bound kernels of the joint attention path (CUDA cores, FP32 math):
+//   rope_table      cos/sin of every (position, RoPE pair) the call needs
+//   prologue        qk_rmsnorm + multi_axis_rope of Q and K, one bf16 cast
+//   bwd_pre         Delta = rowsum(dO * O)
+//   norm_rope_bwd   inverse RoPE rotation + RMSNorm backward + per-chunk
+//                   gain-gradient partials
+//   dg_fold         fixed-order folds of the gain-gradient partials
+// Sources: RFC #386 "WS1/WS2 kernel roadmap", Model contract table (Q/K
+// preprocessing and RoPE rows) and WS1 table (qk_rmsnorm, multi_axis_rope);
+// "WS1 Single-GPU Kernel List", Kernel table (fwd + bwd for both rows) and
+// Acceptance ("multi-path gradient sums use a fixed order").
+#include "rlk_device.cuh"
+#include "rlk_internal.h"
+
+RLK_DEFINE_STRICT_PROBE(probe_prologue_tu)
+
+namespace rlk {
+namespace {
+
+constexpr int kRowThreads = 16;  // a half warp covers one 128-wide row, 8 dims per lane
+
+// ---------------------------------------------------------------- rope table
+// tab[(p - p_lo) * 64 + k] = (cos, sin) of p * theta^(-2j/d_a), where pair k
+// is pair j of axis a. Angles and cos/sin in FP64, rounded once to FP32.
+__global__ void rope_table_kernel(Geom g, float2* __restrict__ tab) {
+    int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= g.n_pos * kPairs) return;
+    int k = idx % kPairs;
+    int p = g.p_lo + idx / kPairs;
+    int a = pair_axis(k);
+    int j = a == 0 ? k : (a == 1 ? k - kAxis0Pairs : k - kAxis0Pairs - kAxis1Pairs);
+    double d_a = a == 0 ? 16.0 : 56.0;
+    double freq = pow((double)g.theta, -2.0 * (double)j / d_a);
+    double ang = (double)p * freq;
+    double s, c;
+    sincos(ang, &s, &c);
+    tab[idx] = make_float2((float)c, (float)s);
+}
+
+// ---------------------------------------------------------------- prologue
+// One half warp per (b, n, h) row; lane l owns dims [8l, 8l+8) = RoPE pairs
+// [4l, 4l+4). Sum of squares: each lane adds its 8 squares in order, then a
+// butterfly over the 16 lanes (xor 8, 4, 2, 1). r = 1 / sqrt(ss/128 + eps)
+// with IEEE sqrt and division. y = (x * r) * g; then each pair turns by its
+// angle; one round to bf16 at the output.
+__device__ __forceinline__ void norm_rope_row(const uint4 xv, const float* __restrict__ gain,
+                                              const float2* __restrict__ tab_row0,
+                                              const float2* __restrict__ tab_row1,
+                                              const float2* __restrict__ tab_row2, int lane16,
+                                              float eps, uint4& out, float& r_out) {
+    float x[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
+                  bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
+#pragma unroll
+    for (int m = 8; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+    float r = 1.0f / sqrtf(ss * (1.0f / 128.0f) + eps);
+    r_out = r;
+    const float4 g0 = __ldg(reinterpret_cast<const float4*>(gain) + 2 * lane16);
+    const float4 g1 = __ldg(reinterpret_cast<const float4*>(gain) + 2 * lane16 + 1);
+    const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int k = 4 * lane16 + i;
+        int a = pair_axis(k);
+        const float2 cs = (a == 0 ? tab_row0 : (a == 1 ? tab_row1 : tab_row2))[k];
+        float y0 = (x[2 * i] * r) * gv[2 * i];
+        float y1 = (x[2 * i + 1] * r) * gv[2 * i + 1];
+        float o0 = fmaf(y0, cs.x, -(y1 * cs.y));
+        float o1 = fmaf(y0, cs.y, y1 * cs.x);
+        o[i] = pack_bf16(o0, o1);
+    }
+    out = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void __launch_bounds__(256) prologue_kernel(
+    Geom g, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+    const float* __restrict__ gq_txt, const float* __restrict__ gk_txt,
+    const float* __restrict__ gq_img, const float* __restrict__ gk_img,
+    const float2* __restrict__ tab, uint16_t* __restrict__ qh, uint16_t* __restrict__ kh,
+    float* __restrict__ rq, float* __restrict__ rk) {
+    const long long rows = (long long)g.B * g.S * g.H;
+    const long long row_raw = (long long)blockIdx.x * (blockDim.x / kRowThreads) + threadIdx.x / kRowThreads;
+    const int lane16 = threadIdx.x % kRowThreads;
+    // A half warp past the end works on the last row and stores nothing, so
+    // that every lane of the warp reaches the shuffles.
+    const bool active = row_raw < rows;
+    const long long row = active ? row_raw : rows - 1;
+    const int h = (int)(row % g.H);
+    const long long bn = row / g.H;
+    const int n = (int)(bn % g.S);
+    const int b = (int)(bn / g.S);
+    const bool txt = n < g.T_txt;
+    const float2* t0 = tab + (size_t)(token_pos(g, n, 0) - g.p_lo) * kPairs;
+    const float2* t1 = tab + (size_t)(token_pos(g, n, 1) - g.p_lo) * kPairs;
+    const float2* t2 = tab + (size_t)(token_pos(g, n, 2) - g.p_lo) * kPairs;
+    const size_t src = (size_t)row * kHeadDim + 8 * lane16;
+    const size_t bh = (size_t)b * g.H + h;
+    const size_t dst = (bh * g.S + n) * kHeadDim + 8 * lane16;
+    const uint4 xq = __ldg(reinterpret_cast<const uint4*>(q + src));
+    const uint4 xk = __ldg(reinterpret_cast<const uint4*>(k + src));
+    uint4 oq, ok;
+    float r_q, r_k;
+    norm_rope_row(xq, txt ? gq_txt : gq_img, t0, t1, t2, lane16, g.eps, oq, r_q);
+    norm_rope_row(xk, txt ? gk_txt : gk_img, t0, t1, t2, lane16, g.eps, ok, r_k);
+    if (!active) return;
+    *reinterpret_cast<uint4*>(qh + dst) = oq;
+    *reinterpret_cast<uint4*>(kh + dst) = ok;
+    if (lane16 == 0) {
+        rq[bh * g.S + n] = r_q;
+        rk[bh * g.S + n] = r_k;
+    }
+}
+
+// ---------------------------------------------------------------- Delta
+// Delta[b,h,n] = sum_d dO * O in FP32: each lane adds its 8 products in
+// order, then a butterfly over the half warp.
+__global__ void __launch_bounds__(256) bwd_pre_kernel(Geom g, const uint16_t* __restrict__ o,
+                                                      const uint16_t* __restrict__ dout,
+                                                      float* __restrict__ delta) {
+    const long long rows = (long long)g.B * g.S * g.H;
+    const long long row_raw = (long long)blockIdx.x * (blockDim.x / kRowThreads) + threadIdx.x / kRowThreads;
+    const int lane16 = threadIdx.x % kRowThreads;
+    const bool active = row_raw < rows;
+    const long long row = active ? row_raw : rows - 1;
+    const int h = (int)(row % g.H);
+    const long long bn = row / g.H;
+    const int n = (int)(bn % g.S);
+    const int b = (int)(bn / g.S);
+    const size_t src = (size_t)row * kHeadDim + 8 * lane16;
+    const uint4 ov = __ldg(reinterpret_cast<const uint4*>(o + src));
+    const uint4 dv = __ldg(reinterpret_cast<const uint4*>(dout + src));
+    const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+    const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+    float acc = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc = fmaf(bf16_lo(dw[i]), bf16_lo(ow[i]), acc);
+        acc = fmaf(bf16_hi(dw[i]), bf16_hi(ow[i]), acc);
+    }
+#pragma unroll
+    for (int m = 8; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (active && lane16 == 0) delta[((size_t)b * g.H + h) * g.S + n] = acc;
+}
+
+// ---------------------------------------------------------------- norm/rope backward
+// CTA = (chunk of 64 tokens of one stream segment, h, b); warps 0-3 take Q
+// rows, warps 4-7 K rows, 16 consecutive rows each, in ascending order. Lane
+// l owns dims [4l, 4l+4) = pairs 2l, 2l+1. Per row:
+//   u  = R(-angle) * dyh          (inverse rotation)
+//   xh = x * r,  w = u * g,  c = (sum_d w_d xh_d) / 128   (lane order, then xor 16..1)
+//   dx = r * (w - xh * c)  -> bf16
+//   gain-gradient partial += u * xh (per lane, rows ascending)
+// The four warps of each operand are folded in warp order through shared
+// memory; chunk partials go to dg_chunks[b][h][q|k][chunk][128].
+constexpr int kNrbRowsPerWarp = kDgChunk / 4;
+
+__global__ void __launch_bounds__(256) norm_rope_bwd_kernel(
+    Geom g, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+    const float* __restrict__ gq_txt, const float* __restrict__ gk_txt,
+    const float* __restrict__ gq_img, const float* __restrict__ gk_img,
+    const float2* __restrict__ tab, const float* __restrict__ rq, const float* __restrict__ rk,
+    const float* __restrict__ dqh, const float* __restrict__ dkh, uint16_t* __restrict__ dq,
+    uint16_t* __restrict__ dk, float* __restrict__ dg_chunks) {
+    __shared__ float red[8][kHeadDim];
+    const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const bool is_k = warp >= 4;
+    const bool txt_chunk = chunk < g.n_dg_chunks_txt;
+    const int seg_start = txt_chunk ? chunk * kDgChunk : g.T_txt + (chunk - g.n_dg_chunks_txt) * kDgChunk;
+    const int seg_end = txt_chunk ? g.T_txt : g.S;
+    const float* gain = is_k ? (txt_chunk ? gk_txt : gk_img) : (txt_chunk ? gq_txt : gq_img);
+    const float* r_all = is_k ? rk : rq;
+    const float* dyh = is_k ? dkh : dqh;
+    const uint16_t* x_all = is_k ? k : q;
+    uint16_t* dx_all = is_k ? dk : dq;
+    const size_t bh = (size_t)b * g.H + h;
+    const float4 gv = __ldg(reinterpret_cast<const float4*>(gain) + lane);
+    const int k0 = 2 * lane, k1 = 2 * lane + 1;
+    const int ax = pair_axis(k0);  // both pairs of a lane share an axis
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int row0 = seg_start + (warp % 4) * kNrbRowsPerWarp;
+    for (int i = 0; i < kNrbRowsPerWarp; ++i) {
+        const int n = row0 + i;
+        if (n >= seg_end) break;
+        const float2* trow = tab + (size_t)(token_pos(g, n, ax) - g.p_lo) * kPairs;
+        const float2 c0 = trow[k0], c1 = trow[k1];
+        const float4 dy = *reinterpret_cast<const float4*>(dyh + (bh * g.S + n) * kHeadDim + 4 * lane);
+        const size_t xoff = (((size_t)b * g.S + n) * g.H + h) * kHeadDim + 4 * lane;
+        const uint2 xv = *reinterpret_cast<const uint2*>(x_all + xoff);
+        const float r = r_all[bh * g.S + n];
+        float u[4];
+        u[0] = fmaf(dy.x, c0.x, dy.y * c0.y);
+        u[1] = fmaf(dy.y, c0.x, -(dy.x * c0.y));
+        u[2] = fmaf(dy.z, c1.x, dy.w * c1.y);
+        u[3] = fmaf(dy.w, c1.x, -(dy.z * c1.y));
+        const float x[4] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y)};
+        const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
+        float xh[4], w[4];
+        float dot = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            xh[j] = x[j] * r;
+            w[j] = u[j] * gg[j];
+            dot = fmaf(w[j], xh[j], dot);
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
+        const float c = dot * (1.0f / 128.0f);
+        float dx[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            dx[j] = r * fmaf(-xh[j], c, w[j]);
+            acc[j] = fmaf(u[j], xh[j], acc[j]);
+        }
+        *reinterpret_cast<uint2*>(dx_all + xoff) = make_uint2(pack_bf16(dx[0], dx[1]), pack_bf16(dx[2], dx[3]));
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) red[warp][4 * lane + j] = acc[j];
+    __syncthreads();
+    if (threadIdx.x < 2 * kHeadDim) {
+        const int which = threadIdx.x / kHeadDim, d = threadIdx.x % kHeadDim;
+        const int w0 = 4 * which;
+        float s = red[w0][d];
+        s += red[w0 + 1][d];
+        s += red[w0 + 2][d];
+        s += red[w0 + 3][d];
+        const int nch = g.n_dg_chunks_txt + g.n_dg_chunks_img;
+        dg_chunks[((bh * 2 + which) * nch + chunk) * kHeadDim + d] = s;
+    }
+}
+
+// dg_partial[b,h,slot,d] = sum over that stream's chunks, ascending.
+// Slots: 0 q_txt, 1 k_txt, 2 q_img, 3 k_img.
+__global__ void dg_fold_bh_kernel(Geom g, const float* __restrict__ dg_chunks,
+                                  float* __restrict__ dg_partial) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= g.B * g.H * 4 * kHeadDim) return;
+    const int d = idx % kHeadDim;
+    const int slot = (idx / kHeadDim) % 4;
+    const size_t bh = idx / (4 * kHeadDim);
+    const int which = slot & 1;
+    const bool img = slot >= 2;
+    const int nch = g.n_dg_chunks_txt + g.n_dg_chunks_img;
+    const int c_begin = img ? g.n_dg_chunks_txt : 0;
+    const int c_end = img ? nch : g.n_dg_chunks_txt;
+    const float* src = dg_chunks + ((bh * 2 + which) * nch) * kHeadDim + d;
+    float s = 0.0f;
+    for (int c = c_begin; c < c_end; ++c) s += src[(size_t)c * kHeadDim];
+    dg_partial[idx] = s;
+}
+
+// dg[slot,d] = sum_b ( sum_h dg_partial[b,h,slot,d] ), both ascending.
+__global__ void dg_fold_total_kernel(Geom g, const float* __restrict__ dg_partial,
+                                     float* __restrict__ dg) {
+    const int idx = threadIdx.x;  // slot * 128 + d, 512 threads
+    float total = 0.0f;
+    for (int b = 0; b < g.B; ++b) {
+        float sb = 0.0f;
+        for (int h = 0; h < g.H; ++h) sb += dg_partial[((size_t)b * g.H + h) * 4 * kHeadDim + idx];
+        total += sb;
+    }
+    dg[idx] = total;
+}
+
+unsigned row_blocks(const Geom& g) {
+    const long long rows = (long long)g.B * g.S * g.H;
+    return (unsigned)((rows + 15) / 16);
+}
+
+}  // namespace
+
+cudaError_t launch_rope_table(const Geom& g, float2* tab, cudaStream_t s) {
+    const int n = g.n_pos * kPairs;
+    timing_begin(kKRopeTable, s);
+    rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(g, tab);
+    timing_end(kKRopeTable, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prologue(const Geom& g, const uint16_t* q, const uint16_t* k,
+                            const float* const gains[4], const float2* tab, uint16_t* qh,
+                            uint16_t* kh, float* rq, float* rk, cudaStream_t s) {
+    timing_begin(kKPrologue, s);
+    prologue_kernel<<<row_blocks(g), 256, 0, s>>>(g, q, k, gains[0], gains[1], gains[2], gains[3],
+                                                  tab, qh, kh, rq, rk);
+    timing_end(kKPrologue, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_pre(const Geom& g, const uint16_t* out, const uint16_t* dout, float* delta,
+                           cudaStream_t s) {
+    timing_begin(kKBwdPre, s);
+    bwd_pre_kernel<<<row_blocks(g), 256, 0, s>>>(g, out, dout, delta);
+    timing_end(kKBwdPre, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_norm_rope_bwd(const Geom& g, const uint16_t* q, const uint16_t* k,
+                                 const float* const gains[4], const float2* tab, const float* rq,
+                                 const float* rk, const float* dqh, const float* dkh, uint16_t* dq,
+                                 uint16_t* dk, float* dg_chunks, cudaStream_t s) {
+    dim3 grid(g.n_dg_chunks_txt + g.n_dg_chunks_img, g.H, g.B);
+    timing_begin(kKNormRopeBwd, s);
+    norm_rope_bwd_kernel<<<grid, 256, 0, s>>>(g, q, k, gains[0], gains[1], gains[2], gains[3], tab,
+                                              rq, rk, dqh, dkh, dq, dk, dg_chunks);
+    timing_end(kKNormRopeBwd, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dg_fold(const Geom& g, const float* dg_chunks, float* dg_partial, float* dg,
+                           cudaStream_t s) {
+    const int n = g.B * g.H * 4 * kHeadDim;
+    timing_begin(kKDgFold, s);
+    dg_fold_bh_kernel<<<(n + 255) / 256, 256, 0, s>>>(g, dg_chunks, dg_partial);
+    dg_fold_total_kernel<<<1, 4 * kHeadDim, 0, s>>>(g, dg_partial, dg);
+    timing_end(kKDgFold, s);
+    return cudaGetLastError();
+}
+
+}  // namespace rlk

@@ -1,0 +1,374 @@
+// Host side of the C ABI declared in include/rlk_joint_attn.h: argument
+// validation (fail closed, nothing launched on error), the layout of the
+// caller-owned ctx and workspace buffers, kernel sequencing, the device
+// status word, the trace record of the "WS1 Single-GPU Kernel List" (rule 7)
+// and launch timing for benchmarks.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "rlk_device.cuh"
+#include "rlk_internal.h"
+
+RLK_DEFINE_STRICT_PROBE(probe_host_tu)
+
+#ifndef RLK_SOURCE_HASH
+#define RLK_SOURCE_HASH "unknown"
+#endif
+#ifndef RLK_BUILD_FLAGS
+#define RLK_BUILD_FLAGS "unknown"
+#endif
+
+namespace rlk {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxDevices = 64;
+constexpr long long kMaxTokens = 1 << 20;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool shape_ok(const rlk_ja_shape* sh, rlk_status* why) {
+    if (sh == nullptr) { *why = RLK_ERR_INVALID_ARG; return false; }
+    if (sh->D != kHeadDim || sh->axes[0] != 16 || sh->axes[1] != 56 || sh->axes[2] != 56) {
+        *why = RLK_ERR_UNSUPPORTED;
+        return false;
+    }
+    if (sh->B < 1 || sh->B > RLK_MAX_BATCH || sh->T_txt < 0 || sh->grid_h < 1 || sh->grid_w < 1 ||
+        sh->H < 1 || sh->H > 4096 || !(sh->eps > 0.0f) || !std::isfinite(sh->eps) || !(sh->theta > 1.0f) ||
+        !std::isfinite(sh->theta)) {
+        *why = RLK_ERR_INVALID_ARG;
+        return false;
+    }
+    const long long t_img = (long long)sh->grid_h * sh->grid_w;
+    const long long s = t_img + sh->T_txt;
+    if (t_img > kMaxTokens || s > kMaxTokens || (long long)sh->B * sh->H * s * kHeadDim > (1LL << 40)) {
+        *why = RLK_ERR_INVALID_ARG;
+        return false;
+    }
+    return true;
+}
+
+Geom make_geom(const rlk_ja_shape* sh) {
+    Geom g{};
+    g.B = sh->B;
+    g.H = sh->H;
+    g.T_txt = sh->T_txt;
+    g.gh = sh->grid_h;
+    g.gw = sh->grid_w;
+    g.T_img = sh->grid_h * sh->grid_w;
+    g.S = g.T_txt + g.T_img;
+    g.txt_off = std::max(g.gh / 2, g.gw / 2);
+    g.ctr_h = (g.gh + 1) / 2;
+    g.ctr_w = (g.gw + 1) / 2;
+    const int p_lo = -std::max(g.ctr_h, g.ctr_w);
+    int p_hi = std::max(g.gh - 1 - g.ctr_h, g.gw - 1 - g.ctr_w);
+    p_hi = std::max(p_hi, 0);
+    if (g.T_txt > 0) p_hi = std::max(p_hi, g.txt_off + g.T_txt - 1);
+    g.p_lo = p_lo;
+    g.n_pos = p_hi - p_lo + 1;
+    g.eps = sh->eps;
+    g.theta = sh->theta;
+    g.n_dg_chunks_txt = (g.T_txt + kDgChunk - 1) / kDgChunk;
+    g.n_dg_chunks_img = (g.T_img + kDgChunk - 1) / kDgChunk;
+    return g;
+}
+
+struct CtxLayout {
+    size_t qh, kh, rq, rk, tab, total;
+};
+CtxLayout ctx_layout(const Geom& g) {
+    const size_t rows = (size_t)g.B * g.H * g.S;
+    CtxLayout l{};
+    l.qh = 0;
+    l.kh = align_up(l.qh + rows * kHeadDim * 2);
+    l.rq = align_up(l.kh + rows * kHeadDim * 2);
+    l.rk = align_up(l.rq + rows * 4);
+    l.tab = align_up(l.rk + rows * 4);
+    l.total = align_up(l.tab + (size_t)g.n_pos * kPairs * sizeof(float2));
+    return l;
+}
+
+struct WsLayout {
+    size_t delta, dqh, dkh, dgc, dgp, total;
+};
+WsLayout ws_layout(const Geom& g) {
+    const size_t rows = (size_t)g.B * g.H * g.S;
+    const size_t nch = (size_t)g.n_dg_chunks_txt + g.n_dg_chunks_img;
+    WsLayout l{};
+    l.delta = 0;
+    l.dqh = align_up(l.delta + rows * 4);
+    l.dkh = align_up(l.dqh + rows * kHeadDim * 4);
+    l.dgc = align_up(l.dkh + rows * kHeadDim * 4);
+    l.dgp = align_up(l.dgc + (size_t)g.B * g.H * 2 * nch * kHeadDim * 4);
+    l.total = align_up(l.dgp + (size_t)g.B * g.H * 4 * kHeadDim * 4);
+    return l;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Per-device one-time checks: compute capability 10.3 and strict math.
+std::mutex g_dev_mu;
+int g_dev_state[kMaxDevices];  // 0 unknown, 1 ok, 2 wrong arch, 3 fast math, 4 cuda error
+
+int strict_all_units() {
+    const int r[4] = {probe_host_tu(), probe_prologue_tu(), probe_fwd_tu(), probe_bwd_tu()};
+    for (int v : r)
+        if (v < 0) return -1;
+    for (int v : r)
+        if (v == 0) return 0;
+    return 1;
+}
+
+rlk_status device_ok() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RLK_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_dev_state[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            g_dev_state[dev] = 4;
+        } else if (major != 10 || minor != 3) {
+            g_dev_state[dev] = 2;
+        } else {
+            const int s = strict_all_units();
+            g_dev_state[dev] = s == 1 ? 1 : (s == 0 ? 3 : 4);
+        }
+    }
+    switch (g_dev_state[dev]) {
+        case 1: return RLK_OK;
+        case 2: case 3: return RLK_ERR_UNSUPPORTED;
+        default: return RLK_ERR_CUDA;
+    }
+}
+
+rlk_status common_checks(const rlk_ja_shape* sh, const int32_t* vl, Geom* g, ValidLen* v) {
+    rlk_status why = RLK_OK;
+    if (!shape_ok(sh, &why)) return why;
+    if (vl == nullptr) return RLK_ERR_INVALID_ARG;
+    for (int b = 0; b < sh->B; ++b)
+        if (vl[b] < 0 || vl[b] > sh->T_txt) return RLK_ERR_INVALID_ARG;
+    *g = make_geom(sh);
+    std::memset(v, 0, sizeof(*v));
+    for (int b = 0; b < sh->B; ++b) v->L[b] = vl[b];
+    return RLK_OK;
+}
+
+// ---- launch timing ----
+constexpr int kMaxTimed = 4096;
+struct Timing {
+    std::mutex mu;
+    bool on = false;
+    std::vector<cudaEvent_t> ev[kNumKernelIds];
+    int count[kNumKernelIds] = {};
+};
+Timing g_timing;
+
+}  // namespace
+
+void timing_begin(int id, cudaStream_t s) {
+    if (!g_timing.on) return;
+    std::lock_guard<std::mutex> lk(g_timing.mu);
+    const int i = g_timing.count[id];
+    if (i >= kMaxTimed) return;
+    auto& ev = g_timing.ev[id];
+    while ((int)ev.size() < 2 * i + 2) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return;
+        ev.push_back(e);
+    }
+    cudaEventRecord(ev[2 * i], s);
+}
+
+void timing_end(int id, cudaStream_t s) {
+    if (!g_timing.on) return;
+    std::lock_guard<std::mutex> lk(g_timing.mu);
+    const int i = g_timing.count[id];
+    if (i >= kMaxTimed || (int)g_timing.ev[id].size() < 2 * i + 2) return;
+    cudaEventRecord(g_timing.ev[id][2 * i + 1], s);
+    g_timing.count[id] = i + 1;
+}
+
+}  // namespace rlk
+
+using namespace rlk;
+
+extern "C" {
+
+size_t rlk_joint_attn_ctx_bytes(const rlk_ja_shape* shape) {
+    rlk_status why;
+    if (!shape_ok(shape, &why)) return 0;
+    return ctx_layout(make_geom(shape)).total;
+}
+
+size_t rlk_joint_attn_bwd_workspace_bytes(const rlk_ja_shape* shape) {
+    rlk_status why;
+    if (!shape_ok(shape, &why)) return 0;
+    return ws_layout(make_geom(shape)).total;
+}
+
+rlk_status rlk_joint_attn_fwd(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
+                              const float* g_q_txt, const float* g_k_txt, const float* g_q_img,
+                              const float* g_k_img, const int32_t* txt_valid_len, void* out, float* lse,
+                              void* ctx, void* stream) {
+    Geom g;
+    ValidLen vl;
+    rlk_status st = common_checks(shape, txt_valid_len, &g, &vl);
+    if (st != RLK_OK) return st;
+    const void* ptrs[] = {q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, out, ctx};
+    for (const void* p : ptrs)
+        if (p == nullptr) return RLK_ERR_INVALID_ARG;
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return RLK_ERR_ALIGNMENT;
+    if (lse != nullptr && !aligned16(lse)) return RLK_ERR_ALIGNMENT;
+    st = device_ok();
+    if (st != RLK_OK) return st;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const CtxLayout l = ctx_layout(g);
+    uint8_t* c = static_cast<uint8_t*>(ctx);
+    uint16_t* qh = reinterpret_cast<uint16_t*>(c + l.qh);
+    uint16_t* kh = reinterpret_cast<uint16_t*>(c + l.kh);
+    float* rq = reinterpret_cast<float*>(c + l.rq);
+    float* rk = reinterpret_cast<float*>(c + l.rk);
+    float2* tab = reinterpret_cast<float2*>(c + l.tab);
+    const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
+
+    if (launch_rope_table(g, tab, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_prologue(g, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), gains, tab, qh, kh,
+                        rq, rk, s) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    if (launch_attn_fwd(g, vl, qh, kh, static_cast<const uint16_t*>(v), static_cast<uint16_t*>(out), lse, s) !=
+        cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
+                              const float* g_q_txt, const float* g_k_txt, const float* g_q_img,
+                              const float* g_k_img, const int32_t* txt_valid_len, const void* out,
+                              const void* dout, const float* lse, const void* ctx, void* dq, void* dk, void* dv,
+                              float* dg_partial, float* dg, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+    Geom g;
+    ValidLen vl;
+    rlk_status st = common_checks(shape, txt_valid_len, &g, &vl);
+    if (st != RLK_OK) return st;
+    const void* ptrs[] = {q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, out, dout, lse, ctx, dq, dk, dv, dg,
+                          workspace};
+    for (const void* p : ptrs)
+        if (p == nullptr) return RLK_ERR_INVALID_ARG;
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return RLK_ERR_ALIGNMENT;
+    if (dg_partial != nullptr && !aligned16(dg_partial)) return RLK_ERR_ALIGNMENT;
+    const WsLayout w = ws_layout(g);
+    if (workspace_bytes < w.total) return RLK_ERR_WORKSPACE;
+    st = device_ok();
+    if (st != RLK_OK) return st;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const CtxLayout l = ctx_layout(g);
+    const uint8_t* c = static_cast<const uint8_t*>(ctx);
+    const uint16_t* qh = reinterpret_cast<const uint16_t*>(c + l.qh);
+    const uint16_t* kh = reinterpret_cast<const uint16_t*>(c + l.kh);
+    const float* rq = reinterpret_cast<const float*>(c + l.rq);
+    const float* rk = reinterpret_cast<const float*>(c + l.rk);
+    const float2* tab = reinterpret_cast<const float2*>(c + l.tab);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* delta = reinterpret_cast<float*>(ws + w.delta);
+    float* dqh = reinterpret_cast<float*>(ws + w.dqh);
+    float* dkh = reinterpret_cast<float*>(ws + w.dkh);
+    float* dgc = reinterpret_cast<float*>(ws + w.dgc);
+    float* dgp = dg_partial != nullptr ? dg_partial : reinterpret_cast<float*>(ws + w.dgp);
+    const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
+    const uint16_t* vv = static_cast<const uint16_t*>(v);
+    const uint16_t* dO = static_cast<const uint16_t*>(dout);
+
+    if (launch_bwd_pre(g, static_cast<const uint16_t*>(out), dO, delta, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_attn_bwd_dkdv(g, vl, qh, kh, vv, dO, lse, delta, static_cast<uint16_t*>(dv), dkh, s) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    if (launch_attn_bwd_dq(g, vl, qh, kh, vv, dO, lse, delta, dqh, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_norm_rope_bwd(g, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), gains, tab, rq,
+                             rk, dqh, dkh, static_cast<uint16_t*>(dq), static_cast<uint16_t*>(dk), dgc,
+                             s) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    if (launch_dg_fold(g, dgc, dgp, dg, s) != cudaSuccess) return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status rlk_joint_attn_check_status(void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RLK_ERR_CUDA;
+    const int a = read_and_clear_status_fwd(s);
+    const int b = read_and_clear_status_bwd(s);
+    if (a < 0 || b < 0) return RLK_ERR_CUDA;
+    if (a != 0 || b != 0) return RLK_ERR_DEVICE_TIMEOUT;
+    return RLK_OK;
+}
+
+int rlk_strict_math_compiled(void) { return strict_all_units(); }
+
+rlk_status rlk_joint_attn_trace(rlk_ja_trace* out) {
+    if (out == nullptr) return RLK_ERR_INVALID_ARG;
+    std::memset(out, 0, sizeof(*out));
+    std::snprintf(out->backend, sizeof(out->backend), "sm_103a/mma.sync.bf16");
+    std::snprintf(out->reduction_order, sizeof(out->reduction_order),
+                  "kv tiles: text from 0 then image from T_txt, ascending; dkdv: q tiles ascending; "
+                  "rows: lane order + xor butterfly; dg: chunks, h, b ascending");
+    std::snprintf(out->accumulator, sizeof(out->accumulator), "fp32");
+    out->split_k = 0;
+    out->atomics = 0;
+    out->tf32 = 0;
+    out->strict_math = strict_all_units();
+    out->block_q = kFwdBlockQ;
+    out->block_kv = kFwdBlockKV;
+    std::snprintf(out->fingerprint, sizeof(out->fingerprint), "%s %s", RLK_SOURCE_HASH, RLK_BUILD_FLAGS);
+    return RLK_OK;
+}
+
+const char* rlk_strerror(int status) {
+    switch (status) {
+        case RLK_OK: return "ok";
+        case RLK_ERR_INVALID_ARG: return "invalid argument";
+        case RLK_ERR_UNSUPPORTED: return "unsupported configuration (fails closed)";
+        case RLK_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+        case RLK_ERR_WORKSPACE: return "workspace too small";
+        case RLK_ERR_CUDA: return "CUDA error";
+        case RLK_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+rlk_status rlk_kernel_timing(int enable) {
+    std::lock_guard<std::mutex> lk(g_timing.mu);
+    g_timing.on = enable != 0;
+    for (int i = 0; i < kNumKernelIds; ++i) g_timing.count[i] = 0;
+    return RLK_OK;
+}
+
+rlk_status rlk_kernel_timing_read(int kernel_id, double* total_ms, int32_t* launches) {
+    if (kernel_id < 0 || kernel_id >= kNumKernelIds || total_ms == nullptr || launches == nullptr)
+        return RLK_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_timing.mu);
+    double sum = 0.0;
+    const int n = g_timing.count[kernel_id];
+    for (int i = 0; i < n; ++i) {
+        float ms = 0.0f;
+        if (cudaEventSynchronize(g_timing.ev[kernel_id][2 * i + 1]) != cudaSuccess) return RLK_ERR_CUDA;
+        if (cudaEventElapsedTime(&ms, g_timing.ev[kernel_id][2 * i], g_timing.ev[kernel_id][2 * i + 1]) !=
+            cudaSuccess)
+            return RLK_ERR_CUDA;
+        sum += ms;
+    }
+    *total_ms = sum;
+    *launches = n;
+    return RLK_OK;
+}
+
+}  // extern "C"

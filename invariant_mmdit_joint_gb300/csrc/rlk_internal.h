@@ -1,0 +1,100 @@
+// Internal host/device interface between the translation units of
+// librlk_joint_attn.so. Not part of the public ABI (include/rlk_joint_attn.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/rlk_joint_attn.h"
+
+namespace rlk {
+
+constexpr int kHeadDim = 128;
+constexpr int kPairs = kHeadDim / 2;       // RoPE pairs per head row
+constexpr int kAxis0Pairs = 8;             // frame axis: 16 dims
+constexpr int kAxis1Pairs = 28;            // row axis: 56 dims
+constexpr int kDgChunk = 64;               // tokens per gain-gradient chunk
+
+// Geometry of one call, derived from rlk_ja_shape on the host. Every kernel
+// receives it by value. Tile boundaries are functions of (T_txt, grid) only.
+struct Geom {
+    int B, H, S, T_txt, T_img, gh, gw;
+    int txt_off;        // o = max(gh/2, gw/2): position of text token 0
+    int ctr_h, ctr_w;   // ceil(gh/2), ceil(gw/2): image centring
+    int p_lo, n_pos;    // cos/sin table covers positions [p_lo, p_lo + n_pos)
+    float eps, theta;
+    int n_dg_chunks_txt, n_dg_chunks_img;
+};
+
+// Per-sample valid text lengths travel by value as a kernel argument.
+struct ValidLen {
+    int32_t L[RLK_MAX_BATCH];
+};
+
+// Position of token n on axis a (0 frame, 1 row, 2 column).
+__host__ __device__ inline int token_pos(const Geom& g, int n, int a) {
+    if (n < g.T_txt) return g.txt_off + n;
+    if (a == 0) return 0;
+    int i = n - g.T_txt;
+    int r = i / g.gw;
+    return a == 1 ? r - g.ctr_h : (i - r * g.gw) - g.ctr_w;
+}
+
+// Axis owning RoPE pair k (dims 2k, 2k+1) of a 128-wide head row.
+__host__ __device__ inline int pair_axis(int k) {
+    return k < kAxis0Pairs ? 0 : (k < kAxis0Pairs + kAxis1Pairs ? 1 : 2);
+}
+
+// Kernel ids used by the launch timing hooks (see rlk_kernel_timing()).
+enum KernelId {
+    kKRopeTable = 0, kKPrologue = 1, kKAttnFwd = 2, kKBwdPre = 3,
+    kKBwdDkDv = 4, kKBwdDq = 5, kKNormRopeBwd = 6, kKDgFold = 7, kNumKernelIds = 8
+};
+
+// Launch timing hooks (rlk_host.cu): bracket one launch with events.
+void timing_begin(int kernel_id, cudaStream_t s);
+void timing_end(int kernel_id, cudaStream_t s);
+
+// ---- launchers (each returns the cudaGetLastError() of its launch) ----
+// k_prologue.cu
+cudaError_t launch_rope_table(const Geom& g, float2* tab, cudaStream_t s);
+cudaError_t launch_prologue(const Geom& g, const uint16_t* q, const uint16_t* k,
+                            const float* const gains[4], const float2* tab,
+                            uint16_t* qh, uint16_t* kh, float* rq, float* rk,
+                            cudaStream_t s);
+cudaError_t launch_bwd_pre(const Geom& g, const uint16_t* out, const uint16_t* dout,
+                           float* delta, cudaStream_t s);
+cudaError_t launch_norm_rope_bwd(const Geom& g, const uint16_t* q, const uint16_t* k,
+                                 const float* const gains[4], const float2* tab,
+                                 const float* rq, const float* rk,
+                                 const float* dqh, const float* dkh,
+                                 uint16_t* dq, uint16_t* dk, float* dg_chunks,
+                                 cudaStream_t s);
+cudaError_t launch_dg_fold(const Geom& g, const float* dg_chunks, float* dg_partial,
+                           float* dg, cudaStream_t s);
+int probe_prologue_tu(void);
+
+// k_attn_fwd.cu
+cudaError_t launch_attn_fwd(const Geom& g, const ValidLen& vl, const uint16_t* qh,
+                            const uint16_t* kh, const uint16_t* v, uint16_t* out,
+                            float* lse, cudaStream_t s);
+int probe_fwd_tu(void);
+int read_and_clear_status_fwd(cudaStream_t s);
+
+// k_attn_bwd.cu
+cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16_t* qh,
+                                 const uint16_t* kh, const uint16_t* v,
+                                 const uint16_t* dout, const float* lse,
+                                 const float* delta, uint16_t* dv, float* dkh,
+                                 cudaStream_t s);
+cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t* qh,
+                               const uint16_t* kh, const uint16_t* v,
+                               const uint16_t* dout, const float* lse,
+                               const float* delta, float* dqh, cudaStream_t s);
+int probe_bwd_tu(void);
+int read_and_clear_status_bwd(cudaStream_t s);
+
+// Tile geometry of the attention kernels (reported by the trace record).
+extern const int kFwdBlockQ, kFwdBlockKV;
+
+}  // namespace rlk

@@ -291,3 +291,27 @@ def forward_rows(Q, K, V, g, T_txt, grid_h, grid_w, L, b, h, rows,
         outs.append(o[0])
         lses.append(lse[0])
     return np.array(outs), np.array(lses)
+
+
+def pair_rows_forward_backward(Q, K, V, g, dO, T_txt, grid_h, grid_w, L, b, h, rows,
+                               eps=EPS, theta=THETA, axes=AXES):
+    """Forward and backward of one (sample, head) restricted to the query rows
+    ``rows``: their O and lse, the gradient of sum(O[rows] * dO[rows]) with
+    respect to Q[rows], and that loss's gradient with respect to all of K and
+    V. With every row selected this is the full per-(sample, head) result.
+    (Used to time bounded samples of the oracle.)"""
+    S = Q.shape[1]
+    rows = np.asarray(rows)
+    ang = rope_angles(rope_positions(T_txt, grid_h, grid_w), axes, theta)
+    gq = token_gains(g, T_txt, S, "q")
+    gk = token_gains(g, T_txt, S, "k")
+    x_q, x_k = Q[b, rows, h], K[b, :, h]
+    yq, rq = rmsnorm(x_q, gq[rows], eps)
+    yk, rk = rmsnorm(x_k, gk, eps)
+    qh = rope_rotate(yq, ang[rows])
+    kh = rope_rotate(yk, ang)
+    o, lse, p = attention_forward(qh, kh, V[b, :, h], key_valid(T_txt, S, int(L)))
+    dqh, dkh, dv = attention_backward(qh, kh, V[b, :, h], p, dO[b, rows, h])
+    dxq, _ = rmsnorm_backward(x_q, rq, gq[rows], rope_rotate_back(dqh, ang[rows]))
+    dxk, _ = rmsnorm_backward(x_k, rk, gk, rope_rotate_back(dkh, ang))
+    return o, lse, dxq, dxk, dv

@@ -1,0 +1,134 @@
+"""CPU tests of the C ABI boundary: the library loads, exports every symbol
+the header declares, sizes its buffers as documented and fails closed on bad
+arguments before touching the GPU. No compute call is made here."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import invariant_mmdit_joint_gb300 as pkg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(pkg.library_path()):
+        from invariant_mmdit_joint_gb300 import _build
+        _build.build()
+    return pkg.lib()
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(HEADER_DIR):
+        if not f.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(rlk_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+def test_library_exports_every_declared_symbol(L):
+    declared = declared_functions()
+    assert declared, "no declarations found"
+    assert declared == set(pkg.EXPORTED_SYMBOLS)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_buffer_sizes_match_documented_layout(L):
+    s = pkg.Shape.make(2, 256, 64, 64, 24)
+    S, rows = 4352, 2 * 24 * 4352
+
+    def up(x):
+        return (x + 255) // 256 * 256
+    n_pos = (32 + 256 - 1) - (-32) + 1
+    ctx = up(up(up(up(rows * 256) + rows * 256) + rows * 4) + rows * 4) + n_pos * 64 * 8
+    assert pkg.rlk_joint_attn_ctx_bytes(s) == up(ctx)
+    nch = 256 // 64 + 4096 // 64
+    ws = up(up(up(up(rows * 4) + rows * 512) + rows * 512) + 2 * 24 * 2 * nch * 512) + 2 * 24 * 4 * 512
+    assert pkg.rlk_joint_attn_bwd_workspace_bytes(s) == up(ws)
+    assert S == s.S
+
+
+@pytest.mark.parametrize("mutate,code", [
+    (dict(D=64), 2), (dict(axes=(16, 48, 64)), 2), (dict(B=0), 1), (dict(B=257), 1),
+    (dict(grid_h=0), 1), (dict(H=0), 1), (dict(eps=0.0), 1), (dict(theta=1.0), 1), (dict(T_txt=-1), 1),
+])
+def test_invalid_shapes_fail_closed(L, mutate, code):
+    base = dict(B=1, T_txt=16, grid_h=8, grid_w=8, H=2)
+    args = {**base, **{k: v for k, v in mutate.items() if k in base}}
+    extra = {k: v for k, v in mutate.items() if k not in base}
+    s = pkg.Shape.make(**args, **extra)
+    assert pkg.rlk_joint_attn_ctx_bytes(s) == 0
+    fake = 1 << 20  # an aligned fake address: validation must stop before any use
+    rc = L.rlk_joint_attn_fwd(ctypes.byref(s), fake, fake, fake, fake, fake, fake, fake,
+                              (ctypes.c_int32 * 1)(0), fake, fake, fake, None)
+    assert rc == code
+
+
+def _fwd(L, s, vl, ptr=1 << 20, lse=1 << 20, **over):
+    p = dict(q=ptr, k=ptr, v=ptr, a=ptr, b=ptr, c=ptr, d=ptr, out=ptr, ctx=ptr)
+    p.update(over)
+    arr = (ctypes.c_int32 * len(vl))(*vl)
+    return L.rlk_joint_attn_fwd(ctypes.byref(s), p["q"], p["k"], p["v"], p["a"], p["b"], p["c"], p["d"],
+                                arr, p["out"], lse, p["ctx"], None)
+
+
+def test_argument_checks_fail_closed_without_a_gpu(L):
+    s = pkg.Shape.make(2, 16, 8, 8, 2)
+    assert _fwd(L, s, [3, 17]) == 1            # valid length beyond T_txt
+    assert _fwd(L, s, [-1, 3]) == 1            # negative valid length
+    assert _fwd(L, s, [3, 3], q=None) == 1     # null input
+    assert _fwd(L, s, [3, 3], ctx=None) == 1   # null ctx
+    assert _fwd(L, s, [3, 3], k=(1 << 20) + 8) == 3   # misaligned pointer
+    assert _fwd(L, s, [3, 3], lse=(1 << 20) + 4) == 3
+    # a well-formed call reaches the device check: with no GPU it reports a
+    # CUDA error -- it never falls back to another implementation
+    import torch
+    if not torch.cuda.is_available():
+        assert _fwd(L, s, [3, 3]) == 5
+
+
+def test_backward_checks_workspace_size(L):
+    s = pkg.Shape.make(1, 16, 8, 8, 2)
+    need = pkg.rlk_joint_attn_bwd_workspace_bytes(s)
+    p = 1 << 20
+    vl = (ctypes.c_int32 * 1)(4)
+    rc = L.rlk_joint_attn_bwd(ctypes.byref(s), p, p, p, p, p, p, p, vl, p, p, p, p, p, p, p, None, p, p,
+                              need - 1, None)
+    assert rc == 4
+    rc = L.rlk_joint_attn_bwd(ctypes.byref(s), p, p, p, p, p, p, p, vl, p, p, None, p, p, p, p, None, p, p,
+                              need, None)
+    assert rc == 1  # lse is required by the backward
+
+
+def test_strerror_and_trace(L):
+    assert pkg.rlk_strerror(0) == "ok"
+    assert "fails closed" in pkg.rlk_strerror(2)
+    t = pkg.rlk_joint_attn_trace()
+    assert t["split_k"] == 0 and t["atomics"] == 0 and t["tf32"] == 0
+    assert t["accumulator"] == "fp32"
+    assert t["backend"].startswith("sm_103a")
+    assert "fast_math" not in t["fingerprint"] and "-prec-div=true" in t["fingerprint"]
+
+
+def test_product_never_imports_the_oracle():
+    pkg_dir = os.path.join(ROOT, "invariant_mmdit_joint_gb300")
+    for dirpath, _, files in os.walk(pkg_dir):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", text, re.M), f
+                assert "oracle/" not in text, f
+
+
+def test_binding_rejects_missing_library(tmp_path):
+    with pytest.raises(ImportError):
+        pkg.load_library(str(tmp_path / "absent.so"))

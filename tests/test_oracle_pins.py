@@ -385,3 +385,16 @@ def test_planted_mistakes_are_caught():
     assert directional_fd_error(geom, Q, K, V, dO, g, backward=backward_mut, n_dir=1) > 1e-3
     # and the unmodified oracle passes the same pin on the same case
     assert directional_fd_error(geom, Q, K, V, dO, g, n_dir=1) < 1e-6
+
+
+def test_row_sample_equals_full_pair_when_all_rows_selected():
+    w, Q, K, V, dO, g, vl = _tiny()
+    o, lse = O.joint_attn_forward(Q, K, V, g, w.T_txt, w.grid_h, w.grid_w, vl)
+    dQ, dK, dV, _, _ = O.joint_attn_backward(Q, K, V, g, dO, w.T_txt, w.grid_h, w.grid_w, vl)
+    r = O.pair_rows_forward_backward(Q, K, V, g, dO, w.T_txt, w.grid_h, w.grid_w, vl[0], 0, 1, np.arange(w.S))
+    for a, ref in zip(r, (o[0, :, 1], lse[0, 1], dQ[0, :, 1], dK[0, :, 1], dV[0, :, 1])):
+        assert np.max(np.abs(a - ref)) <= 1e-12
+    # a row subset gives exactly the selected rows of the forward
+    rows = [0, 5, 40, 79]
+    r2 = O.pair_rows_forward_backward(Q, K, V, g, dO, w.T_txt, w.grid_h, w.grid_w, vl[0], 0, 1, rows)
+    assert np.max(np.abs(r2[0] - o[0, rows, 1])) <= 1e-12
