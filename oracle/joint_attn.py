@@ -31,6 +31,13 @@ fixed by the pages at all and are "parity unpinned" against the real model):
   * angles are formed in float64.                          [parity unpinned]
   * the key mask is a prefix valid length per sample over the text segment;
     padded query rows are computed like any other row.
+  * storage rounding (``store_bf16=True``): qk_rmsnorm and multi_axis_rope
+    are their own WS1 rows whose outputs are stored as bf16 ([RFC] Numerical
+    requirements: cast to bf16 at the declared kernel output boundary), and
+    the pages' CPU references round explicitly at storage. With the flag set
+    the normed, rotated q and k are rounded to bf16 before the attention; the
+    backward passes gradients through that rounding unchanged. With the flag
+    clear (the default) everything stays exact float64.
 """
 
 from __future__ import annotations
@@ -49,6 +56,13 @@ def widen_bf16(bits: np.ndarray) -> np.ndarray:
     """bfloat16 bit patterns (uint16) -> exact float64 values."""
     u = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
     return u.view(np.float32).astype(np.float64)
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 value, ties to even,
+    exactly (bfloat16 keeps 8 significant bits)."""
+    m, e = np.frexp(x)
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)
 
 
 # ---------------------------------------------------------------- positions
@@ -179,7 +193,7 @@ def attention_backward(qh, kh, v, p, do):
 
 
 # ---------------------------------------------------------------- full path
-def _pair_forward(Qbh, Kbh, Vbh, g, T_txt, grid_h, grid_w, L, eps, theta, axes):
+def _pair_forward(Qbh, Kbh, Vbh, g, T_txt, grid_h, grid_w, L, eps, theta, axes, store_bf16=False):
     S = Qbh.shape[0]
     ang = rope_angles(rope_positions(T_txt, grid_h, grid_w), axes, theta)
     gq = token_gains(g, T_txt, S, "q")
@@ -188,6 +202,8 @@ def _pair_forward(Qbh, Kbh, Vbh, g, T_txt, grid_h, grid_w, L, eps, theta, axes):
     yk, rk = rmsnorm(Kbh, gk, eps)
     qh = rope_rotate(yq, ang)
     kh = rope_rotate(yk, ang)
+    if store_bf16:
+        qh, kh = round_bf16(qh), round_bf16(kh)
     valid = key_valid(T_txt, S, L)
     o, lse, p = attention_forward(qh, kh, Vbh, valid)
     return dict(o=o, lse=lse, p=p, qh=qh, kh=kh, rq=rq, rk=rk, ang=ang,
@@ -195,7 +211,7 @@ def _pair_forward(Qbh, Kbh, Vbh, g, T_txt, grid_h, grid_w, L, eps, theta, axes):
 
 
 def joint_attn_forward(Q, K, V, g, T_txt, grid_h, grid_w, valid_len,
-                       eps=EPS, theta=THETA, axes=AXES, heads=None):
+                       eps=EPS, theta=THETA, axes=AXES, heads=None, store_bf16=False):
     """Forward of the whole path on float64 [B, S, H, D] inputs.
 
     g: float64 [4, D] gains (q_txt, k_txt, q_img, k_img); valid_len: [B].
@@ -209,14 +225,14 @@ def joint_attn_forward(Q, K, V, g, T_txt, grid_h, grid_w, valid_len,
     for b in range(B):
         for h in heads:
             f = _pair_forward(Q[b, :, h], K[b, :, h], V[b, :, h], g, T_txt,
-                              grid_h, grid_w, int(valid_len[b]), eps, theta, axes)
+                              grid_h, grid_w, int(valid_len[b]), eps, theta, axes, store_bf16)
             O[b, :, h] = f["o"]
             lse[b, h] = f["lse"]
     return O, lse
 
 
 def joint_attn_backward(Q, K, V, g, dO, T_txt, grid_h, grid_w, valid_len,
-                        eps=EPS, theta=THETA, axes=AXES, heads=None):
+                        eps=EPS, theta=THETA, axes=AXES, heads=None, store_bf16=False):
     """Backward of the whole path: gradients of sum(O * dO).
 
     Returns dQ, dK, dV [B, S, H, D], the per-(sample, head) gain-gradient
@@ -234,7 +250,7 @@ def joint_attn_backward(Q, K, V, g, dO, T_txt, grid_h, grid_w, valid_len,
         for h in heads:
             x_q, x_k = Q[b, :, h], K[b, :, h]
             f = _pair_forward(x_q, x_k, V[b, :, h], g, T_txt, grid_h, grid_w,
-                              int(valid_len[b]), eps, theta, axes)
+                              int(valid_len[b]), eps, theta, axes, store_bf16)
             dqh, dkh, dv = attention_backward(f["qh"], f["kh"], V[b, :, h],
                                               f["p"], dO[b, :, h])
             dyq = rope_rotate_back(dqh, f["ang"])
@@ -273,7 +289,7 @@ def prologue(Q, K, g, T_txt, grid_h, grid_w, eps=EPS, theta=THETA, axes=AXES):
 
 
 def forward_rows(Q, K, V, g, T_txt, grid_h, grid_w, L, b, h, rows,
-                 eps=EPS, theta=THETA, axes=AXES):
+                 eps=EPS, theta=THETA, axes=AXES, store_bf16=False):
     """O and lse of selected query rows of one (sample, head), computed one
     row at a time against all keys (for spot checks at full size)."""
     S = Q.shape[1]
@@ -282,11 +298,15 @@ def forward_rows(Q, K, V, g, T_txt, grid_h, grid_w, L, b, h, rows,
     gq = token_gains(g, T_txt, S, "q")
     yk, _ = rmsnorm(K[b, :, h], gk, eps)
     kh = rope_rotate(yk, ang)
+    if store_bf16:
+        kh = round_bf16(kh)
     valid = key_valid(T_txt, S, int(L))
     outs, lses = [], []
     for i in rows:
         yq, _ = rmsnorm(Q[b, i:i + 1, h], gq[i:i + 1], eps)
         qh = rope_rotate(yq, ang[i:i + 1])
+        if store_bf16:
+            qh = round_bf16(qh)
         o, lse, _ = attention_forward(qh, kh, V[b, :, h], valid)
         outs.append(o[0])
         lses.append(lse[0])

@@ -1,7 +1,11 @@
 """Shared helpers of the GPU tests: move seeded inputs to the device, run the
 path through the C ABI, and compare with the oracle at the declared
-tolerances (forward max abs <= 1e-2 and mean abs <= 1e-3, lse <= 1e-4
-relative, gradients relative L2 <= 1e-2)."""
+tolerances: forward max abs <= 1e-2 and mean abs <= 1e-3 for N(0,1) inputs
+(inputs drawn as sigma * N(0,1) scale both by sigma, since O is linear in
+V), lse <= 1e-4 relative, gradients relative L2 <= 1e-2. The oracle is run
+with the declared bf16 storage rounding of the normed, rotated q and k; the
+exact-float64 oracle is also checked, at the looser lse bound that rounding
+implies (PURE_LSE_REL)."""
 
 from __future__ import annotations
 
@@ -13,6 +17,9 @@ FWD_MAX_ABS = 1e-2
 FWD_MEAN_ABS = 1e-3
 LSE_REL = 1e-4
 GRAD_REL_L2 = 1e-2
+# bf16 storage of q and k alone moves lse by up to ~3e-4 relative at S = 80
+# and ~2e-4 at S = 4352 against exact float64 (measured with the oracle).
+PURE_LSE_REL = 1e-3
 
 
 def to_dev(bits: np.ndarray, dev):
@@ -47,12 +54,12 @@ def oracle_inputs(batch: dict):
     return Q, K, V, dO, batch["gains"].astype(np.float64)
 
 
-def assert_forward_close(out, lse, ref_o, ref_lse, where=""):
+def assert_forward_close(out, lse, ref_o, ref_lse, where="", scale=1.0, lse_rel=LSE_REL):
     err = np.abs(out - ref_o)
-    assert err.max() <= FWD_MAX_ABS, (where, "O max abs", err.max())
-    assert err.mean() <= FWD_MEAN_ABS, (where, "O mean abs", err.mean())
+    assert err.max() <= FWD_MAX_ABS * scale, (where, "O max abs", err.max())
+    assert err.mean() <= FWD_MEAN_ABS * scale, (where, "O mean abs", err.mean())
     rel = np.abs(lse - ref_lse) / np.abs(ref_lse)
-    assert rel.max() <= LSE_REL, (where, "lse rel", rel.max())
+    assert rel.max() <= lse_rel, (where, "lse rel", rel.max())
 
 
 def rel_l2(a, b) -> float:

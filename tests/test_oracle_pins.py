@@ -398,3 +398,31 @@ def test_row_sample_equals_full_pair_when_all_rows_selected():
     rows = [0, 5, 40, 79]
     r2 = O.pair_rows_forward_backward(Q, K, V, g, dO, w.T_txt, w.grid_h, w.grid_w, vl[0], 0, 1, rows)
     assert np.max(np.abs(r2[0] - o[0, rows, 1])) <= 1e-12
+
+
+def test_round_bf16_is_round_to_nearest_even():
+    torch = pytest.importorskip("torch")
+    x = np.random.default_rng(6).standard_normal(200000).astype(np.float32) * 7
+    # exact ties between two bf16 neighbours, both parities, and a carry
+    ties = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 255.5 / 128, 1.5 + 2 ** -8], np.float32)
+    x = np.concatenate([x, ties])
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.round_bf16(x.astype(np.float64))
+    assert np.array_equal(got, ref)
+    assert O.round_bf16(np.array([1 + 2 ** -8]))[0] == 1.0          # tie to even (down)
+    assert O.round_bf16(np.array([1 + 3 * 2 ** -8]))[0] == 1 + 2 ** -6  # tie to even (up)
+    assert O.round_bf16(np.array([255.5 / 128]))[0] == 2.0           # carry into the exponent
+
+
+def test_storage_rounding_only_rounds_q_and_k():
+    """With store_bf16 the forward equals the exact attention of the rounded
+    normed/rotated q and k; without it nothing is rounded."""
+    w, Q, K, V, dO, g, vl = _tiny()
+    qh, kh, _, _ = O.prologue(Q, K, g, w.T_txt, w.grid_h, w.grid_w)
+    o, lse = O.joint_attn_forward(Q, K, V, g, w.T_txt, w.grid_h, w.grid_w, vl, store_bf16=True)
+    valid = O.key_valid(w.T_txt, w.S, int(vl[0]))
+    for h in range(w.H):
+        ro, rl, _ = O.attention_forward(O.round_bf16(qh[0, h]), O.round_bf16(kh[0, h]), V[0, :, h], valid)
+        assert np.max(np.abs(o[0, :, h] - ro)) <= 1e-13 and np.max(np.abs(lse[0, h] - rl)) <= 1e-13
+    o2, lse2 = O.joint_attn_forward(Q, K, V, g, w.T_txt, w.grid_h, w.grid_w, vl)
+    assert 0 < np.max(np.abs(lse2 - lse)) < 1e-2
