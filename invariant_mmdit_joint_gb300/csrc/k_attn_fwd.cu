@@ -1,57 +1,98 @@
-// Joint attention forward: rows joint_attn_qk_gemm, joint_attn_softmax and
-// joint_attn_av_gemm of the RFC #386 WS1 table, fused
-// ("joint_attention_fused"), with an online softmax over key tiles.
+// Joint attention forward on the 5th-generation tensor cores (tcgen05):
+// rows joint_attn_qk_gemm, joint_attn_softmax and joint_attn_av_gemm of the
+// RFC #386 WS1 table fused ("joint_attention_fused"), with an online
+// softmax over key tiles.
 //
-// One CTA = one (query tile of 128 rows, head, sample). Query tiles are
-// segment aligned: text tiles start at token 0, image tiles at token T_txt,
-// so no tile straddles the two streams. Key tiles of 64 are visited in one
-// fixed order -- text tiles from key 0 (only those holding a valid key), then
-// image tiles from key T_txt -- so a row's result depends only on its own
-// sample's data, never on B, batch position, padding or the SM count. No
-// split-KV, no atomics. Scores, running max/sum and the O accumulator are
-// FP32; P enters the PV product as bf16 (round to nearest even); O is cast
-// to bf16 once, at the output.
+// One CTA = one (query tile of 128 rows, head, sample); 6 warps:
+//   warps 0-3  softmax: thread t owns query row t = TMEM lane t. Per key
+//              tile it reads S from TMEM, masks, keeps the running max m
+//              and sum l (FP32, log2 units), rescales O in TMEM when m grows,
+//              and writes P = exp2(s - m) as bf16 back into TMEM over S.
+//              Epilogue: O / l, one bf16 cast, and lse.
+//   warp 4     TMA producer: Q once, then K and V tiles (two stages).
+//   warp 5     MMA issuer (one thread) and TMEM owner:
+//              S_j = Q K_j^T  (A, B from shared memory, K-major),
+//              O  += P_j V_j  (A = P from tensor memory, B = V MN-major).
+// TMEM: S_0 cols [0,128), S_1 [128,256), O [256,384); P_j overwrites the
+// first 64 columns of S_j. S_{j+1} is computed while the softmax works on
+// S_j. Query tiles are segment aligned (text from token 0, image from token
+// T_txt); key tiles of 128 are visited in one fixed order (text tiles that
+// hold a valid key, then image tiles), so a row's bytes never depend on B,
+// its batch position, padding or the SM count. No split-KV, no atomics.
+// Every wait is bounded; a wait that gives up records RLK_ERR_DEVICE_TIMEOUT
+// in the status word and the CTA drains its copies and MMAs and exits.
 #include "rlk_device.cuh"
 #include "rlk_internal.h"
+#include "rlk_sm100.cuh"
+
+#include <cudaTypedefs.h>
 
 RLK_DEFINE_STRICT_PROBE(probe_fwd_tu)
 
 namespace rlk {
 
 const int kFwdBlockQ = 128;
-const int kFwdBlockKV = 64;
+const int kFwdBlockKV = 128;
 
 namespace {
 
-constexpr int kBM = 128;             // query rows per CTA
-constexpr int kBN = 64;              // keys per tile
-constexpr int kThreads = 256;        // 8 warps x 16 query rows
-constexpr int kTileBytesQ = kBM * 256;
-constexpr int kTileBytesKV = kBN * 256;
-constexpr int kSmemBytes = kTileBytesQ + 4 * kTileBytesKV;  // Q + 2 x (K, V)
-// exp(s / sqrt(128)) = exp2(s * kC); kC = log2(e) / sqrt(128)
-constexpr float kC = (float)(1.4426950408889634 * 0.08838834764831845);
+using namespace sm100;
+
+constexpr int kBM = 128, kBN = 128;
+constexpr int kThreads = 192;
+constexpr int kBoxBytes = 128 * 128;          // 128 rows x 64 bf16
+constexpr int kTileBytes = 2 * kBoxBytes;     // 128 rows x 128 bf16
+constexpr int kSmemQ = 0;
+constexpr int kSmemK = kTileBytes;            // 2 stages
+constexpr int kSmemV = 3 * kTileBytes;        // 2 stages
+constexpr int kSmemBytes = 5 * kTileBytes + 1024;  // + alignment slack
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr float kC = (float)(1.4426950408889634 * 0.08838834764831845);  // log2(e) / sqrt(128)
 constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ int g_status_fwd;
 
 struct FwdArgs {
+    CUtensorMap map_q;   // qh [B*H*S, 128] bf16, box 64 x 128
+    CUtensorMap map_k;   // kh [B*H*S, 128]
+    CUtensorMap map_v;   // v  [B, S, H, 128] as 4-D (d, h, n, b), box 64 x 1 x 128 x 1
     Geom g;
     ValidLen vl;
-    const uint16_t* qh;   // [B, H, S, D] normed + rotated q
-    const uint16_t* kh;   // [B, H, S, D]
-    const uint16_t* v;    // [B, S, H, D]
-    uint16_t* out;        // [B, S, H, D]
-    float* lse;           // [B, H, S] or null
+    uint16_t* out;       // [B, S, H, 128]
+    float* lse;          // [B, H, S] or null
 };
 
-__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdArgs a) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+struct TileInfo {
+    int k0, kend;
+};
+__device__ __forceinline__ TileInfo kv_tile(const Geom& g, int L, int nkt_txt, int j) {
+    TileInfo t;
+    if (j < nkt_txt) {
+        t.k0 = j * kBN;
+        t.kend = L;
+    } else {
+        t.k0 = g.T_txt + (j - nkt_txt) * kBN;
+        t.kend = g.S;
+    }
+    return t;
+}
+
+__device__ __forceinline__ void fail(volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicOr(&g_status_fwd, 1);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ FwdArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[13];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+
     const Geom& g = a.g;
     const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int gr = lane >> 2, gc = lane & 3;
-
     const int nqt_txt = (g.T_txt + kBM - 1) / kBM;
     const bool q_txt = qt < nqt_txt;
     const int q0 = q_txt ? qt * kBM : g.T_txt + (qt - nqt_txt) * kBM;
@@ -59,179 +100,303 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int L = a.vl.L[b];
     const int nkt_txt = (L + kBN - 1) / kBN;
     const int nkt = nkt_txt + (g.T_img + kBN - 1) / kBN;
-    const size_t bh = (size_t)b * g.H + h;
-    const uint16_t* qh = a.qh + bh * g.S * kHeadDim;
-    const uint16_t* kh = a.kh + bh * g.S * kHeadDim;
+    const int row_base = (b * g.H + h) * g.S;  // first row of this (b, h) in qh / kh
 
-    const uint32_t sQ = smem_u32(smem);
-    const uint32_t sK = sQ + kTileBytesQ;
-    const uint32_t sV = sK + 2 * kTileBytesKV;
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sQ = sbase + kSmemQ, sK = sbase + kSmemK, sV = sbase + kSmemV;
+    const uint32_t bar_q = smem_u32(&bars[0]);
+    const uint32_t bar_kf = smem_u32(&bars[1]);   // [2]
+    const uint32_t bar_vf = smem_u32(&bars[3]);   // [2]
+    const uint32_t bar_kve = smem_u32(&bars[5]);  // [2]
+    const uint32_t bar_sf = smem_u32(&bars[7]);   // [2]
+    const uint32_t bar_pf = smem_u32(&bars[9]);   // [2], one per S buffer
+    const uint32_t bar_od = smem_u32(&bars[11]);
+    const uint32_t bar_drain = smem_u32(&bars[12]);
 
-    for (int i = tid; i < kBM * 16; i += kThreads) {
-        const int r = i >> 4, c = i & 15, n = q0 + r;
-        const bool ok = n < q_end;
-        cp_async16(tile_addr(sQ, r, c), qh + (size_t)(ok ? n : 0) * kHeadDim + c * 8, ok);
+    if (tid == 0) {
+        abort_flag = 0;
+        mbar_init(bar_q, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar_kf + 8 * s, 1);
+            mbar_init(bar_vf + 8 * s, 1);
+            mbar_init(bar_kve + 8 * s, 1);
+            mbar_init(bar_sf + 8 * s, 1);
+            mbar_init(bar_pf + 8 * s, 128);
+        }
+        mbar_init(bar_od, 1);
+        mbar_init(bar_drain, 1);
+        fence_barrier_init();
     }
-    auto load_kv = [&](int t, int buf) {
-        const bool txt = t < nkt_txt;
-        const int k0 = txt ? t * kBN : g.T_txt + (t - nkt_txt) * kBN;
-        const int kend = txt ? L : g.S;
-        for (int i = tid; i < kBN * 16; i += kThreads) {
-            const int r = i >> 4, c = i & 15, n = k0 + r;
-            const bool ok = n < kend;
-            const int nn = ok ? n : 0;
-            cp_async16(tile_addr(sK + buf * kTileBytesKV, r, c), kh + (size_t)nn * kHeadDim + c * 8, ok);
-            cp_async16(tile_addr(sV + buf * kTileBytesKV, r, c),
-                       a.v + (((size_t)b * g.S + nn) * g.H + h) * kHeadDim + c * 8, ok);
-        }
-    };
-    load_kv(0, 0);
-    cp_async_commit();
+    if (warp == 5) {
+        tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
 
-    float o[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-    uint32_t qf[8][4];
-
-    for (int t = 0; t < nkt; ++t) {
-        if (t + 1 < nkt) load_kv(t + 1, (t + 1) & 1);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        if (t == 0) {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                ldsm_x4(tile_addr(sQ, 16 * warp + (lane & 15), 2 * ks + (lane >> 4)), qf[ks][0], qf[ks][1],
-                        qf[ks][2], qf[ks][3]);
-        }
-        const uint32_t kb = sK + (t & 1) * kTileBytesKV;
-        const uint32_t vb = sV + (t & 1) * kTileBytesKV;
-
-        // S = Q K^T for this warp's 16 rows x 64 keys
-        float s[8][4];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.0f;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t r0, r1, r2, r3;
-                ldsm_x4(tile_addr(kb, 16 * np + (lane & 7) + ((lane >> 4) << 3), 2 * ks + ((lane >> 3) & 1)), r0,
-                        r1, r2, r3);
-                mma_bf16(s[2 * np], qf[ks], r0, r1);
-                mma_bf16(s[2 * np + 1], qf[ks], r2, r3);
+    if (warp == 4) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tensormap(&a.map_q);
+            prefetch_tensormap(&a.map_k);
+            prefetch_tensormap(&a.map_v);
+            mbar_expect_tx(bar_q, kTileBytes);
+            tma_load_2d(sQ, &a.map_q, bar_q, 0, row_base + q0);
+            tma_load_2d(sQ + kBoxBytes, &a.map_q, bar_q, 64, row_base + q0);
+            int issued = 0;
+            for (int j = 0; j < nkt && !abort_flag; ++j) {
+                const int s = j & 1;
+                if (j >= 2 && !mbar_wait(bar_kve + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                    fail(&abort_flag);
+                    break;
+                }
+                const TileInfo t = kv_tile(g, L, nkt_txt, j);
+                const uint32_t dk = sK + s * kTileBytes, dv = sV + s * kTileBytes;
+                mbar_expect_tx(bar_kf + 8 * s, kTileBytes);
+                tma_load_2d(dk, &a.map_k, bar_kf + 8 * s, 0, row_base + t.k0);
+                tma_load_2d(dk + kBoxBytes, &a.map_k, bar_kf + 8 * s, 64, row_base + t.k0);
+                mbar_expect_tx(bar_vf + 8 * s, kTileBytes);
+                tma_load_4d(dv, &a.map_v, bar_vf + 8 * s, 0, h, t.k0, b);
+                tma_load_4d(dv + kBoxBytes, &a.map_v, bar_vf + 8 * s, 64, h, t.k0, b);
+                issued = j + 1;
+            }
+            // drain: the copies of the last (up to) two tiles and of Q have landed
+            const volatile int no_abort = 0;
+            mbar_wait(bar_q, 0, &no_abort, kWaitLimitNs);
+            for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) {
+                const int s = j & 1;
+                mbar_wait(bar_kf + 8 * s, (j >> 1) & 1, &no_abort, kWaitLimitNs);
+                mbar_wait(bar_vf + 8 * s, (j >> 1) & 1, &no_abort, kWaitLimitNs);
             }
         }
-
-        // mask, scale to log2 units, online softmax (rows gr and gr + 8)
-        const bool txt = t < nkt_txt;
-        const int k0 = txt ? t * kBN : g.T_txt + (t - nkt_txt) * kBN;
-        const int kend = txt ? L : g.S;
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+    } else if (warp == 5) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idesc_o = idesc_bf16(128, 128, false, true);
+            auto issue_s = [&](int j) {
+                const int s = j & 1;
+                const uint32_t dk = sK + s * kTileBytes;
+                const uint32_t d_tmem = tmem + (s ? kColS1 : kColS0);
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const bool ok = k0 + 8 * nt + 2 * gc + e < kend;
-                s[nt][e] = ok ? s[nt][e] * kC : -INFINITY;
-                s[nt][2 + e] = ok ? s[nt][2 + e] * kC : -INFINITY;
-                mx0 = fmaxf(mx0, s[nt][e]);
-                mx1 = fmaxf(mx1, s[nt][2 + e]);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                    mma_ss(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(dk + off, 16, 1024), idesc_s,
+                           kk > 0);
+                }
+                mma_commit(bar_sf + 8 * s);
+            };
+            bool ok = mbar_wait(bar_q, 0, &abort_flag, kWaitLimitNs) &&
+                      mbar_wait(bar_kf, 0, &abort_flag, kWaitLimitNs);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
             }
-        }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
-        float rs0 = 0.0f, rs1 = 0.0f;
+            for (int j = 0; ok && j < nkt; ++j) {
+                const int s = j & 1;
+                if (j + 1 < nkt) {
+                    const int s1 = (j + 1) & 1;
+                    if (!mbar_wait(bar_kf + 8 * s1, ((j + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_s(j + 1);
+                }
+                if (!mbar_wait(bar_pf + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs) ||
+                    !mbar_wait(bar_vf + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t p_tmem = tmem + (s ? kColS1 : kColS0);
+                const uint32_t dv = sV + s * kTileBytes;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                s[nt][e] = exp2f(s[nt][e] - mn0);
-                s[nt][2 + e] = exp2f(s[nt][2 + e] - mn1);
-                rs0 += s[nt][e];
-                rs1 += s[nt][2 + e];
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + kColO, p_tmem + kk * 8, sdesc_sw128(dv + kk * 2048, kBoxBytes, 1024), idesc_o,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar_od);
+                mma_commit(bar_kve + 8 * s);
             }
+            if (!ok) fail(&abort_flag);
+            // drain every MMA this thread issued before TMEM is released
+            mma_commit(bar_drain);
+            const volatile int no_abort = 0;
+            mbar_wait(bar_drain, 0, &no_abort, kWaitLimitNs);
         }
-        l0 = l0 * al0 + rs0;
-        l1 = l1 * al1 + rs1;
-#pragma unroll
-        for (int dt = 0; dt < 16; ++dt) {
-            o[dt][0] *= al0;
-            o[dt][1] *= al0;
-            o[dt][2] *= al1;
-            o[dt][3] *= al1;
-        }
-
-        // O += P V
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t pa[4] = {pack_bf16(s[2 * kk][0], s[2 * kk][1]), pack_bf16(s[2 * kk][2], s[2 * kk][3]),
-                                    pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]),
-                                    pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3])};
-#pragma unroll
-            for (int dp = 0; dp < 8; ++dp) {
-                uint32_t r0, r1, r2, r3;
-                ldsm_x4_t(tile_addr(vb, 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3), 2 * dp + (lane >> 4)), r0,
-                          r1, r2, r3);
-                mma_bf16(o[2 * dp], pa, r0, r1);
-                mma_bf16(o[2 * dp + 1], pa, r2, r3);
+    } else {
+        // ------------------------------------------------ softmax warps 0-3
+        // Barrier phases are consumed strictly in order (S_j, then PV_{j-1}
+        // once per tile), so no waiter ever falls two phases behind.
+        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+        const uint32_t o_tmem = tmem + lane_addr + kColO;
+        const int row = tid;
+        float m = -INFINITY, l = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < nkt; ++j) {
+            const int s = j & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_sf + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs))) {
+                ok = false;
+                break;
             }
+            tc_fence_after();
+            const uint32_t s_tmem = tmem + lane_addr + (s ? kColS1 : kColS0);
+            float x[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld32(s_tmem + 32 * c, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(r[i]);
+            }
+            const TileInfo t = kv_tile(g, L, nkt_txt, j);
+            const int nvalid = t.kend - t.k0;  // keys k0 + c with c < nvalid are valid
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                x[c] = c < nvalid ? x[c] * kC : -INFINITY;
+                mx = fmaxf(mx, x[c]);
+            }
+            const float m_new = fmaxf(m, mx);
+            const float alpha = exp2f(m - m_new);
+            if (j > 0) {
+                // PV_{j-1} has finished writing O
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_od, (j - 1) & 1, &abort_flag, kWaitLimitNs))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // rescale O when a row's max grew; the decision is warp-wide
+                // and rows whose max did not grow scale by exactly 1
+                if (__any_sync(0xffffffffu, m_new > m)) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(o_tmem + 32 * c, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(o_tmem + 32 * c, r);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            float rs = 0.0f;
+            uint32_t pa[32], pb[32];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float p0 = exp2f(x[2 * c] - m_new);
+                const float p1 = exp2f(x[2 * c + 1] - m_new);
+                rs += p0;
+                rs += p1;
+                if (c < 32) pa[c] = pack_bf16(p0, p1);
+                else pb[c - 32] = pack_bf16(p0, p1);
+            }
+            l = l * alpha + rs;
+            m = m_new;
+            tmem_st32(s_tmem, pa);
+            tmem_st32(s_tmem + 32, pb);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar_pf + 8 * s);
         }
-        __syncthreads();
+        if (ok && __all_sync(0xffffffffu, mbar_wait(bar_od, (nkt - 1) & 1, &abort_flag, kWaitLimitNs))) {
+            tc_fence_after();
+            const float inv = 1.0f / l;
+            const bool row_ok = q0 + row < q_end;
+            uint16_t* orow = a.out + (((size_t)b * g.S + q0 + row) * g.H + h) * kHeadDim;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld32(o_tmem + 32 * c, r);
+                tmem_ld_wait();
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = pack_bf16(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+                if (row_ok) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+                    dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+                }
+            }
+            if (row_ok && a.lse != nullptr)
+                a.lse[((size_t)b * g.H + h) * g.S + q0 + row] = (m + log2f(l)) * kLn2;
+        } else {
+            fail(&abort_flag);
+        }
     }
 
-    // epilogue: O / l, one bf16 cast, staged through this warp's Q rows
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const float inv0 = 1.0f / l0, inv1 = 1.0f / l1;
-    const int r_lo = 16 * warp + gr, r_hi = r_lo + 8;
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
-        const uint32_t lo = pack_bf16(o[dt][0] * inv0, o[dt][1] * inv0);
-        const uint32_t hi = pack_bf16(o[dt][2] * inv1, o[dt][3] * inv1);
-        asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(tile_addr(sQ, r_lo, dt) + 4 * gc), "r"(lo));
-        asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(tile_addr(sQ, r_hi, dt) + 4 * gc), "r"(hi));
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
     }
-    if (a.lse != nullptr && gc == 0) {
-        if (q0 + r_lo < q_end) a.lse[bh * g.S + q0 + r_lo] = (m0 + log2f(l0)) * kLn2;
-        if (q0 + r_hi < q_end) a.lse[bh * g.S + q0 + r_hi] = (m1 + log2f(l1)) * kLn2;
+}
+
+// ---------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     }
-    __syncwarp();
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int i = lane + 32 * it;
-        const int r = 16 * warp + (i >> 4), c = i & 15;
-        const int n = q0 + r;
-        if (n < q_end) {
-            uint4 v;
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
-                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                         : "r"(tile_addr(sQ, r, c)));
-            *reinterpret_cast<uint4*>(a.out + (((size_t)b * g.S + n) * g.H + h) * kHeadDim + c * 8) = v;
-        }
-    }
+    return fn;
+}
+
+bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows) {
+    auto enc = get_encode();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_bshd(CUtensorMap* m, const void* base, const Geom& g) {
+    auto enc = get_encode();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[4] = {128, (cuuint64_t)g.H, (cuuint64_t)g.S, (cuuint64_t)g.B};
+    cuuint64_t strides[3] = {256, (cuuint64_t)g.H * 256, (cuuint64_t)g.S * g.H * 256};
+    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
 cudaError_t launch_attn_fwd(const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
                             const uint16_t* v, uint16_t* out, float* lse, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    FwdArgs local;
+    const uint64_t rows = (uint64_t)g.B * g.H * g.S;
+    if (!encode_rows(&local.map_q, qh, rows) || !encode_rows(&local.map_k, kh, rows) ||
+        !encode_bshd(&local.map_v, v, g))
+        return cudaErrorInvalidValue;
+    local.g = g;
+    local.vl = vl;
+    local.out = out;
+    local.lse = lse;
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    FwdArgs args{g, vl, qh, kh, v, out, lse};
     const int nqt = (g.T_txt + kBM - 1) / kBM + (g.T_img + kBM - 1) / kBM;
     dim3 grid(nqt, g.H, g.B);
     timing_begin(kKAttnFwd, s);
-    attn_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(args);
+    attn_fwd_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(local);
     timing_end(kKAttnFwd, s);
     return cudaGetLastError();
 }

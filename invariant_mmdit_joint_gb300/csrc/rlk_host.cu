@@ -317,7 +317,7 @@ int rlk_strict_math_compiled(void) { return strict_all_units(); }
 rlk_status rlk_joint_attn_trace(rlk_ja_trace* out) {
     if (out == nullptr) return RLK_ERR_INVALID_ARG;
     std::memset(out, 0, sizeof(*out));
-    std::snprintf(out->backend, sizeof(out->backend), "sm_103a/mma.sync.bf16");
+    std::snprintf(out->backend, sizeof(out->backend), "sm_103a tcgen05/mma.sync");
     std::snprintf(out->reduction_order, sizeof(out->reduction_order),
                   "kv tiles: text from 0 then image from T_txt, ascending; dkdv: q tiles ascending; "
                   "rows: lane order + xor butterfly; dg: chunks, h, b ascending");

@@ -5,7 +5,7 @@ tolerances: forward max abs <= 1e-2 and mean abs <= 1e-3 for N(0,1) inputs
 V), lse <= 1e-4 relative, gradients relative L2 <= 1e-2. The oracle is run
 with the declared bf16 storage rounding of the normed, rotated q and k; the
 exact-float64 oracle is also checked, at the looser lse bound that rounding
-implies (PURE_LSE_REL)."""
+implies (PURE_LSE_ABS)."""
 
 from __future__ import annotations
 
@@ -17,9 +17,10 @@ FWD_MAX_ABS = 1e-2
 FWD_MEAN_ABS = 1e-3
 LSE_REL = 1e-4
 GRAD_REL_L2 = 1e-2
-# bf16 storage of q and k alone moves lse by up to ~3e-4 relative at S = 80
-# and ~2e-4 at S = 4352 against exact float64 (measured with the oracle).
-PURE_LSE_REL = 1e-3
+# bf16 storage of q and k alone moves lse against exact float64 by up to
+# ~1.5e-3 absolute at S = 80 and ~1.6e-3 at S = 4352 (measured with the
+# oracle); little averaging over keys (S = 6) gives ~2.5e-3.
+PURE_LSE_ABS = 5e-3
 
 
 def to_dev(bits: np.ndarray, dev):
@@ -54,12 +55,15 @@ def oracle_inputs(batch: dict):
     return Q, K, V, dO, batch["gains"].astype(np.float64)
 
 
-def assert_forward_close(out, lse, ref_o, ref_lse, where="", scale=1.0, lse_rel=LSE_REL):
+def assert_forward_close(out, lse, ref_o, ref_lse, where="", scale=1.0, lse_abs=None):
     err = np.abs(out - ref_o)
     assert err.max() <= FWD_MAX_ABS * scale, (where, "O max abs", err.max())
     assert err.mean() <= FWD_MEAN_ABS * scale, (where, "O mean abs", err.mean())
-    rel = np.abs(lse - ref_lse) / np.abs(ref_lse)
-    assert rel.max() <= lse_rel, (where, "lse rel", rel.max())
+    if lse_abs is None:
+        rel = np.abs(lse - ref_lse) / np.abs(ref_lse)
+        assert rel.max() <= LSE_REL, (where, "lse rel", rel.max())
+    else:
+        assert np.max(np.abs(lse - ref_lse)) <= lse_abs, (where, "lse abs", np.max(np.abs(lse - ref_lse)))
 
 
 def rel_l2(a, b) -> float:
