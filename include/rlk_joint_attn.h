@@ -126,6 +126,36 @@ rlk_status rlk_joint_attn_fwd(const rlk_ja_shape* shape,
                               const int32_t* txt_valid_len,
                               void* out, float* lse, void* ctx, void* stream);
 
+/* Size of the fixed device scratch used by rlk_joint_attn_fwd_noalloc():
+ * 64 MiB, enough for one 1024x1024 image with 24 heads and 256 text tokens
+ * (rlk_joint_attn_ctx_bytes() of that shape is about 54 MB). */
+#define RLK_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* Forward without any caller-provided scratch and without allocating.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot or may not allocate device memory on the call path (a plugin
+ * host that gives its plugins no workspace, a serving process whose memory
+ * pool owns the whole device, code that must not pay the synchronisation a
+ * cudaMalloc / cudaFree can bring).
+ * Arguments, layouts and results are those of rlk_joint_attn_fwd() minus
+ * `ctx`: the forward context lives in a file-scope device array of
+ * RLK_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
+ * the process exits. Nothing is allocated or freed.
+ *   - Shapes whose rlk_joint_attn_ctx_bytes() exceeds RLK_NOALLOC_SCRATCH_BYTES
+ *     return RLK_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device looks up the array's device address on that
+ *     (current) device; make that first call before any stream capture.
+ *   - All calls share the one array and keep the last call's contents, so
+ *     calls whose kernels overlap on the GPU (other streams, other host
+ *     threads) race: serialise them. The context is not kept for a backward:
+ *     this entry point serves forward-only (inference) use. */
+rlk_status rlk_joint_attn_fwd_noalloc(const rlk_ja_shape* shape,
+                                      const void* q, const void* k, const void* v,
+                                      const float* g_q_txt, const float* g_k_txt,
+                                      const float* g_q_img, const float* g_k_img,
+                                      const int32_t* txt_valid_len,
+                                      void* out, float* lse, void* stream);
+
 /* Backward of the whole path: gradients of sum(out * dout).
  *   q, k, v, gains, txt_valid_len  as in the forward (same values)
  *   out, lse, ctx   what the forward wrote for these inputs (lse required)

@@ -22,7 +22,7 @@ __all__ = [
     "rlk_joint_attn_ctx_bytes", "rlk_joint_attn_bwd_workspace_bytes",
     "rlk_joint_attn_fwd", "rlk_joint_attn_bwd", "rlk_joint_attn_check_status",
     "rlk_strict_math_compiled", "rlk_joint_attn_trace", "rlk_strerror",
-    "rlk_kernel_timing", "rlk_kernel_timing_read", "JointAttention",
+    "rlk_kernel_timing", "rlk_kernel_timing_read", "rlk_joint_attn_fwd_noalloc", "JointAttention",
     "EXPORTED_SYMBOLS", "KERNEL_IDS",
 ]
 
@@ -46,7 +46,7 @@ EXPORTED_SYMBOLS = (
     "rlk_joint_attn_ctx_bytes", "rlk_joint_attn_bwd_workspace_bytes",
     "rlk_joint_attn_fwd", "rlk_joint_attn_bwd", "rlk_joint_attn_check_status",
     "rlk_strict_math_compiled", "rlk_joint_attn_trace", "rlk_strerror",
-    "rlk_kernel_timing", "rlk_kernel_timing_read",
+    "rlk_kernel_timing", "rlk_kernel_timing_read", "rlk_joint_attn_fwd_noalloc",
 )
 
 
@@ -127,6 +127,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     L.rlk_kernel_timing.restype = i32
     L.rlk_kernel_timing_read.argtypes = [i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)]
     L.rlk_kernel_timing_read.restype = i32
+    L.rlk_joint_attn_fwd_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_int32),
+                                             vp, vp, vp]
+    L.rlk_joint_attn_fwd_noalloc.restype = i32
     return L
 
 
@@ -187,6 +190,17 @@ def rlk_joint_attn_fwd(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_v
         _ptr(g_q_img), _ptr(g_k_img), _lengths(txt_valid_len), _ptr(out), _ptr(lse), _ptr(ctx),
         _stream_handle(stream))
     _check(rc, "rlk_joint_attn_fwd")
+
+
+def rlk_joint_attn_fwd_noalloc(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_valid_len,
+                               out, lse, stream=None) -> None:
+    """Enqueue the forward with the library's built-in device scratch (for
+    callers that cannot allocate); forward-only, calls must not overlap."""
+    rc = lib().rlk_joint_attn_fwd_noalloc(
+        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_q_txt), _ptr(g_k_txt),
+        _ptr(g_q_img), _ptr(g_k_img), _lengths(txt_valid_len), _ptr(out), _ptr(lse),
+        _stream_handle(stream))
+    _check(rc, "rlk_joint_attn_fwd_noalloc")
 
 
 def rlk_joint_attn_bwd(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_valid_len,
