@@ -133,8 +133,8 @@ def kernel_work(w: W.Workload):
         "prologue": ("hbm", 4 * rows * D * 2 + 2 * rows * 4),
         # QK^T and PV
         "attn_fwd": ("tensor", 2 * G),
-        # read O, dO (bf16); write Delta (fp32)
-        "bwd_pre": ("hbm", 2 * rows * D * 2 + rows * 4),
+        # read O, dO (bf16) and lse; write Delta and lse2 (fp32)
+        "bwd_pre": ("hbm", 2 * rows * D * 2 + 3 * rows * 4),
         # recomputed S^T, dV, dP^T, dK: four of the five credited backward GEMMs
         "bwd_dkdv": ("tensor", 4 * G),
         # dQ: the fifth credited GEMM (its recomputed S and dP are not credited)

@@ -1,425 +1,609 @@
-// Joint attention backward (the "bwd" half of the WS1 attention rows of
-// RFC #386 and of the "WS1 Single-GPU Kernel List"): two atomic-free kernels.
+// Joint attention backward on the tcgen05 tensor cores (the "bwd" half of
+// the WS1 attention rows of RFC #386 and of the "WS1 Single-GPU Kernel
+// List"): two atomic-free kernels with the forward's warp roles.
 //
-//   dkdv: one CTA = (key tile of 128, head, sample). Walks every query tile of
-//         64 in one fixed ascending order (text tiles from token 0, then image
-//         tiles from token T_txt), recomputing P^T = exp(S^T - lse) and
-//         accumulating dV += P^T dO and dK += dS^T Q in FP32, with
-//         dS^T = P^T * (V dO^T - Delta).
+//   dkdv: one CTA = (key tile of 128, head, sample). Walks every query tile
+//         of 128 in one fixed ascending order (text tiles from token 0, then
+//         image tiles from token T_txt). Per query tile:
+//           S^T  = K Q^T, dP^T = V dO^T            (tcgen05, A and B in smem)
+//           P^T  = exp2(S^T * c - lse2), dS^T = P^T * (dP^T - Delta)
+//                                                  (4 warps, one key row each;
+//                                                   bf16 results into TMEM)
+//           dV  += P^T dO,  dK += dS^T Q           (tcgen05, A from TMEM)
 //   dq:   one CTA = (query tile of 128, head, sample). Walks the key tiles of
-//         64 in the forward's order, recomputing P and dP = dO V^T, and
-//         accumulates dQ += dS K in FP32. No atomics, no split.
-//
-// Every output element is produced by one CTA with a fixed reduction order,
-// so the bytes are independent of B, batch position and the SM count. P and
-// dS enter their products as bf16 (round to nearest even).
+//         128 in the forward's order: S = Q K^T, dP = dO V^T, dS as above,
+//         dQ += dS K.
+// Accumulators (dV, dK, dQ) stay in TMEM in FP32 for the whole CTA and are
+// written once. P and dS enter their products as bf16 (round to nearest
+// even). lse2 = lse * log2(e) and Delta = rowsum(dO * O) come from the
+// backward preprocess in a tile-padded layout (one 128-slot block per query
+// tile; slots past a segment hold lse2 = +inf and Delta = 0, so their P is
+// exactly 0). Every wait is bounded (RLK_ERR_DEVICE_TIMEOUT on give-up).
 #include "rlk_device.cuh"
 #include "rlk_internal.h"
+#include "rlk_sm100.cuh"
+
+#include <cudaTypedefs.h>
 
 RLK_DEFINE_STRICT_PROBE(probe_bwd_tu)
 
 namespace rlk {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr float kC = (float)(1.4426950408889634 * 0.08838834764831845);
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kScale = 0.08838834764831845f;  // 1 / sqrt(128)
+using namespace sm100;
+
+constexpr int kThreads = 192;
+constexpr int kBoxBytes = 128 * 128;       // 128 rows x 64 bf16
+constexpr int kTileBytes = 2 * kBoxBytes;  // 128 rows x 128 bf16
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr float kC = (float)(1.4426950408889634 * 0.08838834764831845);  // log2(e) / sqrt(128)
+constexpr float kScale = 0.08838834764831845f;                          // 1 / sqrt(128)
+constexpr uint32_t kIdescKK = idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescKM = idesc_bf16(128, 128, false, true);
 
 __device__ int g_status_bwd;
 
 struct BwdArgs {
+    CUtensorMap map_q;    // qh [B*H*S, 128]
+    CUtensorMap map_k;    // kh [B*H*S, 128]
+    CUtensorMap map_v;    // v  [B, S, H, 128] 4-D
+    CUtensorMap map_do;   // dO [B, S, H, 128] 4-D
     Geom g;
     ValidLen vl;
-    const uint16_t* qh;    // [B, H, S, D]
-    const uint16_t* kh;    // [B, H, S, D]
-    const uint16_t* v;     // [B, S, H, D]
-    const uint16_t* dout;  // [B, S, H, D]
-    const float* lse;      // [B, H, S]
-    const float* delta;    // [B, H, S]
-    uint16_t* dv;          // [B, S, H, D]
-    float* dkh;            // [B, H, S, D]
-    float* dqh;            // [B, H, S, D]
+    const float* lse2_p;  // [B, H, nq_pad]
+    const float* delta_p; // [B, H, nq_pad]
+    uint16_t* dv;         // [B, S, H, 128]
+    float* dkh;           // [B, H, S, 128]
+    float* dqh;           // [B, H, S, 128]
 };
 
-__device__ __forceinline__ size_t bshd(const Geom& g, int b, int n, int h) {
-    return (((size_t)b * g.S + n) * g.H + h) * kHeadDim;
+__device__ __forceinline__ void fail(volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicOr(&g_status_bwd, 1);
 }
 
-// ---------------------------------------------------------------- dK, dV
-constexpr int kKvBK = 128;  // keys per CTA (8 warps x 16)
-constexpr int kKvBQ = 64;   // queries per step
-constexpr int kKvSmem = 2 * kKvBK * 256 + 4 * kKvBQ * 256 + 4 * kKvBQ * 4;
+// K-major operand (rows x 128 bf16 as two 64-column boxes), k-step kk of 16
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
+    return sdesc_sw128(tile + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
+}
+// MN-major operand: the same tile read with its rows as the K dimension
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
+    return sdesc_sw128(tile + kk * 2048, kBoxBytes, 1024);
+}
 
-__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitLimitNs));
+}
+
+// Query tile i (segment aligned): first token and end of its segment.
+__device__ __forceinline__ void q_tile(const Geom& g, int i, int& q0, int& q_end) {
+    if (i < g.ntq_txt) {
+        q0 = i * 128;
+        q_end = g.T_txt;
+    } else {
+        q0 = g.T_txt + (i - g.ntq_txt) * 128;
+        q_end = g.S;
+    }
+}
+
+// ====================================================================== dK, dV
+constexpr int kKvSmemK = 0, kKvSmemV = kTileBytes, kKvSmemStage = 2 * kTileBytes;
+constexpr int kKvStageBytes = 2 * kTileBytes + 1024;  // Q, dO, lse2[128], delta[128]
+constexpr int kKvSmemBytes = kKvSmemStage + 2 * kKvStageBytes + 1024;
+constexpr uint32_t kColDV = 0, kColDK = 128, kColST = 256, kColDPT = 384;
+
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[10];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+
     const Geom& g = a.g;
     const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int gr = lane >> 2, gc = lane & 3;
-    const int nkt_txt = (g.T_txt + kKvBK - 1) / kKvBK;
-    const bool k_txt = kt < nkt_txt;
-    const int k0 = k_txt ? kt * kKvBK : g.T_txt + (kt - nkt_txt) * kKvBK;
+    const bool k_txt = kt < g.ntq_txt;
+    const int k0 = k_txt ? kt * 128 : g.T_txt + (kt - g.ntq_txt) * 128;
     const int seg_end = k_txt ? g.T_txt : g.S;
     const int L = a.vl.L[b];
     const int kvalid_end = k_txt ? L : g.S;
     const size_t bh = (size_t)b * g.H + h;
-    const uint16_t* qh = a.qh + bh * g.S * kHeadDim;
-    const uint16_t* kh = a.kh + bh * g.S * kHeadDim;
+    const int row_base = (int)(bh * g.S);
     float* dkh = a.dkh + bh * g.S * kHeadDim;
 
     if (k0 >= kvalid_end) {  // every key of the tile is masked: exact zeros
-        const int rows = min(kKvBK, seg_end - k0);
+        const int rows = min(128, seg_end - k0);
         for (int i = tid; i < rows * 16; i += kThreads) {
             const int r = i >> 4, c = i & 15;
-            *reinterpret_cast<uint4*>(a.dv + bshd(g, b, k0 + r, h) + c * 8) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(a.dv + (((size_t)b * g.S + k0 + r) * g.H + h) * kHeadDim + c * 8) =
+                make_uint4(0, 0, 0, 0);
             float4* dst = reinterpret_cast<float4*>(dkh + (size_t)(k0 + r) * kHeadDim + c * 8);
             dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
             dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         return;
     }
+    const int nq = g.ntq_txt + g.ntq_img;
 
-    const uint32_t sK = smem_u32(smem);
-    const uint32_t sV = sK + kKvBK * 256;
-    const uint32_t sQ = sV + kKvBK * 256;          // 2 buffers
-    const uint32_t sO = sQ + 2 * kKvBQ * 256;      // dO, 2 buffers
-    float* sStat = reinterpret_cast<float*>(smem + 2 * kKvBK * 256 + 4 * kKvBQ * 256);  // [2][lse2 | delta][64]
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sK = sbase + kKvSmemK, sV = sbase + kKvSmemV;
+    auto stage_q = [&](int s) { return sbase + kKvSmemStage + s * kKvStageBytes; };
+    auto stage_o = [&](int s) { return stage_q(s) + kTileBytes; };
+    auto stage_l = [&](int s) { return stage_q(s) + 2 * kTileBytes; };
+    const uint32_t bar_kv = smem_u32(&bars[0]);
+    const uint32_t bar_full = smem_u32(&bars[1]);   // [2]
+    const uint32_t bar_empty = smem_u32(&bars[3]);  // [2]
+    const uint32_t bar_s = smem_u32(&bars[5]);
+    const uint32_t bar_p = smem_u32(&bars[6]);
+    const uint32_t bar_done = smem_u32(&bars[7]);
+    const uint32_t bar_drain = smem_u32(&bars[8]);
 
-    for (int i = tid; i < kKvBK * 16; i += kThreads) {
-        const int r = i >> 4, c = i & 15, n = k0 + r;
-        const bool ok = n < kvalid_end;
-        const int nn = ok ? n : 0;
-        cp_async16(tile_addr(sK, r, c), kh + (size_t)nn * kHeadDim + c * 8, ok);
-        cp_async16(tile_addr(sV, r, c), a.v + bshd(g, b, nn, h) + c * 8, ok);
+    if (tid == 0) {
+        abort_flag = 0;
+        mbar_init(bar_kv, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_s, 1);
+        mbar_init(bar_p, 128);
+        mbar_init(bar_done, 1);
+        mbar_init(bar_drain, 1);
+        fence_barrier_init();
     }
-    const int nqt_txt = (g.T_txt + kKvBQ - 1) / kKvBQ;
-    const int nqt = nqt_txt + (g.T_img + kKvBQ - 1) / kKvBQ;
-    auto load_q = [&](int t, int buf) {
-        const bool txt = t < nqt_txt;
-        const int q0 = txt ? t * kKvBQ : g.T_txt + (t - nqt_txt) * kKvBQ;
-        const int qend = txt ? g.T_txt : g.S;
-        for (int i = tid; i < kKvBQ * 16; i += kThreads) {
-            const int r = i >> 4, c = i & 15, n = q0 + r;
-            const bool ok = n < qend;
-            const int nn = ok ? n : 0;
-            cp_async16(tile_addr(sQ + buf * kKvBQ * 256, r, c), qh + (size_t)nn * kHeadDim + c * 8, ok);
-            cp_async16(tile_addr(sO + buf * kKvBQ * 256, r, c), a.dout + bshd(g, b, nn, h) + c * 8, ok);
-        }
-        if (tid < kKvBQ) {
-            const int n = q0 + tid;
-            const bool ok = n < qend;
-            // rows outside the segment get lse = +inf, so their P is exactly 0
-            sStat[buf * 2 * kKvBQ + tid] = ok ? a.lse[bh * g.S + n] * kLog2e : INFINITY;
-            sStat[buf * 2 * kKvBQ + kKvBQ + tid] = ok ? a.delta[bh * g.S + n] : 0.0f;
-        }
-    };
-    load_q(0, 0);
-    cp_async_commit();
-
-    float dv[16][4], dk[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        dv[i][0] = dv[i][1] = dv[i][2] = dv[i][3] = 0.0f;
-        dk[i][0] = dk[i][1] = dk[i][2] = dk[i][3] = 0.0f;
+    if (warp == 5) {
+        tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+        tmem_relinquish();
     }
-    const bool kv0 = k0 + 16 * warp + gr < kvalid_end;
-    const bool kv1 = k0 + 16 * warp + gr + 8 < kvalid_end;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
 
-    for (int t = 0; t < nqt; ++t) {
-        if (t + 1 < nqt) load_q(t + 1, (t + 1) & 1);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        const uint32_t qb = sQ + (t & 1) * kKvBQ * 256;
-        const uint32_t ob = sO + (t & 1) * kKvBQ * 256;
-        const float* lse2 = sStat + (t & 1) * 2 * kKvBQ;
-        const float* dlt = lse2 + kKvBQ;
-
-        // S^T = K Q^T: 16 keys x 64 queries
-        float p[8][4];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) p[i][0] = p[i][1] = p[i][2] = p[i][3] = 0.0f;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t ka[4];
-            ldsm_x4(tile_addr(sK, 16 * warp + (lane & 15), 2 * ks + (lane >> 4)), ka[0], ka[1], ka[2], ka[3]);
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t r0, r1, r2, r3;
-                ldsm_x4(tile_addr(qb, 16 * np + (lane & 7) + ((lane >> 4) << 3), 2 * ks + ((lane >> 3) & 1)), r0,
-                        r1, r2, r3);
-                mma_bf16(p[2 * np], ka, r0, r1);
-                mma_bf16(p[2 * np + 1], ka, r2, r3);
+    if (warp == 4) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tensormap(&a.map_q);
+            prefetch_tensormap(&a.map_k);
+            prefetch_tensormap(&a.map_v);
+            prefetch_tensormap(&a.map_do);
+            mbar_expect_tx(bar_kv, 2 * kTileBytes);
+            tma_load_2d(sK, &a.map_k, bar_kv, 0, row_base + k0);
+            tma_load_2d(sK + kBoxBytes, &a.map_k, bar_kv, 64, row_base + k0);
+            tma_load_4d(sV, &a.map_v, bar_kv, 0, h, k0, b);
+            tma_load_4d(sV + kBoxBytes, &a.map_v, bar_kv, 64, h, k0, b);
+            int issued = 0;
+            for (int i = 0; i < nq && !abort_flag; ++i) {
+                const int s = i & 1;
+                if (i >= 2 && !mbar_wait(bar_empty + 8 * s, ((i >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                    fail(&abort_flag);
+                    break;
+                }
+                int q0, q_end;
+                q_tile(g, i, q0, q_end);
+                const uint32_t bf = bar_full + 8 * s;
+                mbar_expect_tx(bf, 2 * kTileBytes + 1024);
+                tma_load_2d(stage_q(s), &a.map_q, bf, 0, row_base + q0);
+                tma_load_2d(stage_q(s) + kBoxBytes, &a.map_q, bf, 64, row_base + q0);
+                tma_load_4d(stage_o(s), &a.map_do, bf, 0, h, q0, b);
+                tma_load_4d(stage_o(s) + kBoxBytes, &a.map_do, bf, 64, h, q0, b);
+                const size_t slot = bh * g.nq_pad + (size_t)i * 128;
+                bulk_load(stage_l(s), a.lse2_p + slot, 512, bf);
+                bulk_load(stage_l(s) + 512, a.delta_p + slot, 512, bf);
+                issued = i + 1;
             }
+            const volatile int no_abort = 0;
+            mbar_wait(bar_kv, 0, &no_abort, kWaitLimitNs);
+            for (int i = issued - 2 < 0 ? 0 : issued - 2; i < issued; ++i)
+                mbar_wait(bar_full + 8 * (i & 1), (i >> 1) & 1, &no_abort, kWaitLimitNs);
         }
-        // P^T = exp2(S^T * kC - lse2[query]); masked keys -> 0
+    } else if (warp == 5) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = mbar_wait(bar_kv, 0, &abort_flag, kWaitLimitNs);
+            for (int i = 0; ok && i < nq; ++i) {
+                const int s = i & 1;
+                if (!mbar_wait(bar_full + 8 * s, (i >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + kColST, desc_kmajor(sK, kk), desc_kmajor(stage_q(s), kk), kIdescKK, kk > 0);
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float l2 = lse2[8 * nt + 2 * gc + e];
-                p[nt][e] = kv0 ? exp2f(p[nt][e] * kC - l2) : 0.0f;
-                p[nt][2 + e] = kv1 ? exp2f(p[nt][2 + e] * kC - l2) : 0.0f;
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + kColDPT, desc_kmajor(sV, kk), desc_kmajor(stage_o(s), kk), kIdescKK, kk > 0);
+                mma_commit(bar_s);
+                if (!mbar_wait(bar_p, i & 1, &abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + kColDV, tmem + kColST + kk * 8, desc_mnmajor(stage_o(s), kk), kIdescKM,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + kColDK, tmem + kColDPT + kk * 8, desc_mnmajor(stage_q(s), kk), kIdescKM,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar_empty + 8 * s);
             }
+            if (ok)
+                mma_commit(bar_done);
+            else
+                fail(&abort_flag);
+            mma_commit(bar_drain);
+            const volatile int no_abort = 0;
+            mbar_wait(bar_drain, 0, &no_abort, kWaitLimitNs);
         }
-        // dV += P^T dO
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t pa[4] = {pack_bf16(p[2 * kk][0], p[2 * kk][1]), pack_bf16(p[2 * kk][2], p[2 * kk][3]),
-                                    pack_bf16(p[2 * kk + 1][0], p[2 * kk + 1][1]),
-                                    pack_bf16(p[2 * kk + 1][2], p[2 * kk + 1][3])};
-#pragma unroll
-            for (int dp = 0; dp < 8; ++dp) {
-                uint32_t r0, r1, r2, r3;
-                ldsm_x4_t(tile_addr(ob, 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3), 2 * dp + (lane >> 4)), r0,
-                          r1, r2, r3);
-                mma_bf16(dv[2 * dp], pa, r0, r1);
-                mma_bf16(dv[2 * dp + 1], pa, r2, r3);
+    } else {
+        // ------------------------------------------------ elementwise warps 0-3 (one key row each)
+        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+        const int kr = tid;
+        const bool kvalid = k0 + kr < kvalid_end;
+        bool ok = true;
+        for (int i = 0; i < nq; ++i) {
+            const int s = i & 1;
+            if (!warp_wait(bar_full + 8 * s, (i >> 1) & 1, &abort_flag) || !warp_wait(bar_s, i & 1, &abort_flag)) {
+                ok = false;
+                break;
             }
-        }
-        // dP^T = V dO^T
-        float ds[8][4];
+            tc_fence_after();
+            const float* l2 = reinterpret_cast<const float*>(smem_raw + (stage_l(s) - smem_u32(smem_raw)));
+            const float* dl = l2 + 128;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t rs[32], rd[32];
+                tmem_ld32(tmem + lane_addr + kColST + 32 * c, rs);
+                tmem_ld32(tmem + lane_addr + kColDPT + 32 * c, rd);
+                tmem_ld_wait();
+                uint32_t pp[16], pd[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ds[i][0] = ds[i][1] = ds[i][2] = ds[i][3] = 0.0f;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t va[4];
-            ldsm_x4(tile_addr(sV, 16 * warp + (lane & 15), 2 * ks + (lane >> 4)), va[0], va[1], va[2], va[3]);
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t r0, r1, r2, r3;
-                ldsm_x4(tile_addr(ob, 16 * np + (lane & 7) + ((lane >> 4) << 3), 2 * ks + ((lane >> 3) & 1)), r0,
-                        r1, r2, r3);
-                mma_bf16(ds[2 * np], va, r0, r1);
-                mma_bf16(ds[2 * np + 1], va, r2, r3);
+                for (int e = 0; e < 16; ++e) {
+                    const int q = 32 * c + 2 * e;
+                    float p0 = exp2f(fmaf(__uint_as_float(rs[2 * e]), kC, -l2[q]));
+                    float p1 = exp2f(fmaf(__uint_as_float(rs[2 * e + 1]), kC, -l2[q + 1]));
+                    if (!kvalid) p0 = p1 = 0.0f;
+                    const float d0 = p0 * (__uint_as_float(rd[2 * e]) - dl[q]);
+                    const float d1 = p1 * (__uint_as_float(rd[2 * e + 1]) - dl[q + 1]);
+                    pp[e] = pack_bf16(p0, p1);
+                    pd[e] = pack_bf16(d0, d1);
+                }
+                tmem_st16(tmem + lane_addr + kColST + 16 * c, pp);
+                tmem_st16(tmem + lane_addr + kColDPT + 16 * c, pd);
             }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar_p);
         }
-        // dS^T = P^T * (dP^T - Delta[query])
+        if (ok && warp_wait(bar_done, 0, &abort_flag)) {
+            tc_fence_after();
+            const int j = k0 + kr;
+            const bool row_ok = j < seg_end;
+            uint16_t* dvrow = a.dv + (((size_t)b * g.S + j) * g.H + h) * kHeadDim;
+            float* dkrow = dkh + (size_t)j * kHeadDim;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_addr + kColDV + 32 * c, r);
+                tmem_ld_wait();
+                uint32_t w[16];
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
+                for (int e = 0; e < 16; ++e)
+                    w[e] = kvalid ? pack_bf16(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])) : 0u;
+                if (row_ok) {
+                    uint4* dst = reinterpret_cast<uint4*>(dvrow + 32 * c);
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float d = dlt[8 * nt + 2 * gc + e];
-                ds[nt][e] = p[nt][e] * (ds[nt][e] - d);
-                ds[nt][2 + e] = p[nt][2 + e] * (ds[nt][2 + e] - d);
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+                }
+                tmem_ld32(tmem + lane_addr + kColDK + 32 * c, r);
+                tmem_ld_wait();
+                if (row_ok) {
+                    float4* dst = reinterpret_cast<float4*>(dkrow + 32 * c);
+#pragma unroll
+                    for (int v4 = 0; v4 < 8; ++v4) {
+                        float4 f;
+                        f.x = kvalid ? __uint_as_float(r[4 * v4]) * kScale : 0.0f;
+                        f.y = kvalid ? __uint_as_float(r[4 * v4 + 1]) * kScale : 0.0f;
+                        f.z = kvalid ? __uint_as_float(r[4 * v4 + 2]) * kScale : 0.0f;
+                        f.w = kvalid ? __uint_as_float(r[4 * v4 + 3]) * kScale : 0.0f;
+                        dst[v4] = f;
+                    }
+                }
             }
+        } else {
+            fail(&abort_flag);
         }
-        // dK += dS^T Q
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t sa[4] = {pack_bf16(ds[2 * kk][0], ds[2 * kk][1]), pack_bf16(ds[2 * kk][2], ds[2 * kk][3]),
-                                    pack_bf16(ds[2 * kk + 1][0], ds[2 * kk + 1][1]),
-                                    pack_bf16(ds[2 * kk + 1][2], ds[2 * kk + 1][3])};
-#pragma unroll
-            for (int dp = 0; dp < 8; ++dp) {
-                uint32_t r0, r1, r2, r3;
-                ldsm_x4_t(tile_addr(qb, 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3), 2 * dp + (lane >> 4)), r0,
-                          r1, r2, r3);
-                mma_bf16(dk[2 * dp], sa, r0, r1);
-                mma_bf16(dk[2 * dp + 1], sa, r2, r3);
-            }
-        }
-        __syncthreads();
     }
 
-    // epilogue: dV -> bf16 [B,S,H,D] (staged through the Q buffers); dkh -> fp32
-    const int r_lo = 16 * warp + gr, r_hi = r_lo + 8;
-    const uint32_t stage = sQ;  // 2 x 64 rows = 128 rows of 256 bytes
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
-        const uint32_t lo = kv0 ? pack_bf16(dv[dt][0], dv[dt][1]) : 0u;
-        const uint32_t hi = kv1 ? pack_bf16(dv[dt][2], dv[dt][3]) : 0u;
-        asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(tile_addr(stage, r_lo, dt) + 4 * gc), "r"(lo));
-        asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(tile_addr(stage, r_hi, dt) + 4 * gc), "r"(hi));
-        if (k0 + r_lo < seg_end) {
-            const float2 v = kv0 ? make_float2(dk[dt][0] * kScale, dk[dt][1] * kScale) : make_float2(0.f, 0.f);
-            *reinterpret_cast<float2*>(dkh + (size_t)(k0 + r_lo) * kHeadDim + 8 * dt + 2 * gc) = v;
-        }
-        if (k0 + r_hi < seg_end) {
-            const float2 v = kv1 ? make_float2(dk[dt][2] * kScale, dk[dt][3] * kScale) : make_float2(0.f, 0.f);
-            *reinterpret_cast<float2*>(dkh + (size_t)(k0 + r_hi) * kHeadDim + 8 * dt + 2 * gc) = v;
-        }
-    }
-    __syncwarp();
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int i = lane + 32 * it;
-        const int r = 16 * warp + (i >> 4), c = i & 15;
-        const int n = k0 + r;
-        if (n < seg_end) {
-            uint4 v;
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
-                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                         : "r"(tile_addr(stage, r, c)));
-            *reinterpret_cast<uint4*>(a.dv + bshd(g, b, n, h) + c * 8) = v;
-        }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
-// ---------------------------------------------------------------- dQ
-constexpr int kDqBQ = 128;  // query rows per CTA (8 warps x 16)
-constexpr int kDqBN = 64;   // keys per step
-constexpr int kDqSmem = 2 * kDqBQ * 256 + 4 * kDqBN * 256;
+// ====================================================================== dQ
+constexpr int kDqSmemQ = 0, kDqSmemO = kTileBytes, kDqSmemStage = 2 * kTileBytes;
+constexpr int kDqStageBytes = 2 * kTileBytes;  // K, V
+constexpr int kDqSmemBytes = kDqSmemStage + 2 * kDqStageBytes + 1024;
+constexpr uint32_t kColDQ = 0, kColS = 128, kColDP = 256;
 
-__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[10];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+
     const Geom& g = a.g;
     const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int gr = lane >> 2, gc = lane & 3;
-    const int nqt_txt = (g.T_txt + kDqBQ - 1) / kDqBQ;
-    const bool q_txt = qt < nqt_txt;
-    const int q0 = q_txt ? qt * kDqBQ : g.T_txt + (qt - nqt_txt) * kDqBQ;
-    const int q_end = q_txt ? g.T_txt : g.S;
+    int q0, q_end;
+    q_tile(g, qt, q0, q_end);
     const int L = a.vl.L[b];
-    const int nkt_txt = (L + kDqBN - 1) / kDqBN;
-    const int nkt = nkt_txt + (g.T_img + kDqBN - 1) / kDqBN;
+    const int nkt_txt = (L + 127) / 128;
+    const int nkt = nkt_txt + g.ntq_img;
     const size_t bh = (size_t)b * g.H + h;
-    const uint16_t* qh = a.qh + bh * g.S * kHeadDim;
-    const uint16_t* kh = a.kh + bh * g.S * kHeadDim;
+    const int row_base = (int)(bh * g.S);
 
-    const uint32_t sQ = smem_u32(smem);
-    const uint32_t sO = sQ + kDqBQ * 256;
-    const uint32_t sK = sO + kDqBQ * 256;          // 2 buffers
-    const uint32_t sV = sK + 2 * kDqBN * 256;      // 2 buffers
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sQ = sbase + kDqSmemQ, sO = sbase + kDqSmemO;
+    auto stage_k = [&](int s) { return sbase + kDqSmemStage + s * kDqStageBytes; };
+    auto stage_v = [&](int s) { return stage_k(s) + kTileBytes; };
+    const uint32_t bar_qo = smem_u32(&bars[0]);
+    const uint32_t bar_full = smem_u32(&bars[1]);   // [2]
+    const uint32_t bar_empty = smem_u32(&bars[3]);  // [2]
+    const uint32_t bar_s = smem_u32(&bars[5]);
+    const uint32_t bar_p = smem_u32(&bars[6]);
+    const uint32_t bar_done = smem_u32(&bars[7]);
+    const uint32_t bar_drain = smem_u32(&bars[8]);
 
-    for (int i = tid; i < kDqBQ * 16; i += kThreads) {
-        const int r = i >> 4, c = i & 15, n = q0 + r;
-        const bool ok = n < q_end;
-        const int nn = ok ? n : 0;
-        cp_async16(tile_addr(sQ, r, c), qh + (size_t)nn * kHeadDim + c * 8, ok);
-        cp_async16(tile_addr(sO, r, c), a.dout + bshd(g, b, nn, h) + c * 8, ok);
+    if (tid == 0) {
+        abort_flag = 0;
+        mbar_init(bar_qo, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_s, 1);
+        mbar_init(bar_p, 128);
+        mbar_init(bar_done, 1);
+        mbar_init(bar_drain, 1);
+        fence_barrier_init();
     }
-    auto load_kv = [&](int t, int buf) {
-        const bool txt = t < nkt_txt;
-        const int k0 = txt ? t * kDqBN : g.T_txt + (t - nkt_txt) * kDqBN;
-        const int kend = txt ? L : g.S;
-        for (int i = tid; i < kDqBN * 16; i += kThreads) {
-            const int r = i >> 4, c = i & 15, n = k0 + r;
-            const bool ok = n < kend;
-            const int nn = ok ? n : 0;
-            cp_async16(tile_addr(sK + buf * kDqBN * 256, r, c), kh + (size_t)nn * kHeadDim + c * 8, ok);
-            cp_async16(tile_addr(sV + buf * kDqBN * 256, r, c), a.v + bshd(g, b, nn, h) + c * 8, ok);
-        }
-    };
-    load_kv(0, 0);
-    cp_async_commit();
+    if (warp == 5) {
+        tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
 
-    const int r_lo = 16 * warp + gr, r_hi = r_lo + 8;
-    const bool ok_lo = q0 + r_lo < q_end, ok_hi = q0 + r_hi < q_end;
-    const float l2_lo = ok_lo ? a.lse[bh * g.S + q0 + r_lo] * kLog2e : 0.0f;
-    const float l2_hi = ok_hi ? a.lse[bh * g.S + q0 + r_hi] * kLog2e : 0.0f;
-    const float d_lo = ok_lo ? a.delta[bh * g.S + q0 + r_lo] : 0.0f;
-    const float d_hi = ok_hi ? a.delta[bh * g.S + q0 + r_hi] : 0.0f;
-
-    float dq[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) dq[i][0] = dq[i][1] = dq[i][2] = dq[i][3] = 0.0f;
-
-    for (int t = 0; t < nkt; ++t) {
-        if (t + 1 < nkt) load_kv(t + 1, (t + 1) & 1);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        const uint32_t kb = sK + (t & 1) * kDqBN * 256;
-        const uint32_t vb = sV + (t & 1) * kDqBN * 256;
-        const bool txt = t < nkt_txt;
-        const int k0 = txt ? t * kDqBN : g.T_txt + (t - nkt_txt) * kDqBN;
-        const int kend = txt ? L : g.S;
-
-        // S = Q K^T and dP = dO V^T, 16 rows x 64 keys each
-        float p[8][4], dp[8][4];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            p[i][0] = p[i][1] = p[i][2] = p[i][3] = 0.0f;
-            dp[i][0] = dp[i][1] = dp[i][2] = dp[i][3] = 0.0f;
-        }
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t qa[4], oa[4];
-            ldsm_x4(tile_addr(sQ, 16 * warp + (lane & 15), 2 * ks + (lane >> 4)), qa[0], qa[1], qa[2], qa[3]);
-            ldsm_x4(tile_addr(sO, 16 * warp + (lane & 15), 2 * ks + (lane >> 4)), oa[0], oa[1], oa[2], oa[3]);
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t r0, r1, r2, r3;
-                const int row = 16 * np + (lane & 7) + ((lane >> 4) << 3), ch = 2 * ks + ((lane >> 3) & 1);
-                ldsm_x4(tile_addr(kb, row, ch), r0, r1, r2, r3);
-                mma_bf16(p[2 * np], qa, r0, r1);
-                mma_bf16(p[2 * np + 1], qa, r2, r3);
-                ldsm_x4(tile_addr(vb, row, ch), r0, r1, r2, r3);
-                mma_bf16(dp[2 * np], oa, r0, r1);
-                mma_bf16(dp[2 * np + 1], oa, r2, r3);
+    if (warp == 4) {
+        if (lane == 0) {
+            prefetch_tensormap(&a.map_q);
+            prefetch_tensormap(&a.map_k);
+            prefetch_tensormap(&a.map_v);
+            prefetch_tensormap(&a.map_do);
+            mbar_expect_tx(bar_qo, 2 * kTileBytes);
+            tma_load_2d(sQ, &a.map_q, bar_qo, 0, row_base + q0);
+            tma_load_2d(sQ + kBoxBytes, &a.map_q, bar_qo, 64, row_base + q0);
+            tma_load_4d(sO, &a.map_do, bar_qo, 0, h, q0, b);
+            tma_load_4d(sO + kBoxBytes, &a.map_do, bar_qo, 64, h, q0, b);
+            int issued = 0;
+            for (int j = 0; j < nkt && !abort_flag; ++j) {
+                const int s = j & 1;
+                if (j >= 2 && !mbar_wait(bar_empty + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                    fail(&abort_flag);
+                    break;
+                }
+                const int kk0 = j < nkt_txt ? j * 128 : g.T_txt + (j - nkt_txt) * 128;
+                const uint32_t bf = bar_full + 8 * s;
+                mbar_expect_tx(bf, 2 * kTileBytes);
+                tma_load_2d(stage_k(s), &a.map_k, bf, 0, row_base + kk0);
+                tma_load_2d(stage_k(s) + kBoxBytes, &a.map_k, bf, 64, row_base + kk0);
+                tma_load_4d(stage_v(s), &a.map_v, bf, 0, h, kk0, b);
+                tma_load_4d(stage_v(s) + kBoxBytes, &a.map_v, bf, 64, h, kk0, b);
+                issued = j + 1;
             }
+            const volatile int no_abort = 0;
+            mbar_wait(bar_qo, 0, &no_abort, kWaitLimitNs);
+            for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
+                mbar_wait(bar_full + 8 * (j & 1), (j >> 1) & 1, &no_abort, kWaitLimitNs);
         }
-        // dS = P * (dP - Delta); masked keys -> 0
+    } else if (warp == 5) {
+        if (lane == 0) {
+            bool ok = mbar_wait(bar_qo, 0, &abort_flag, kWaitLimitNs);
+            for (int j = 0; ok && j < nkt; ++j) {
+                const int s = j & 1;
+                if (!mbar_wait(bar_full + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + kColS, desc_kmajor(sQ, kk), desc_kmajor(stage_k(s), kk), kIdescKK, kk > 0);
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const bool ok = k0 + 8 * nt + 2 * gc + e < kend;
-                const float p_lo = ok ? exp2f(p[nt][e] * kC - l2_lo) : 0.0f;
-                const float p_hi = ok ? exp2f(p[nt][2 + e] * kC - l2_hi) : 0.0f;
-                p[nt][e] = p_lo * (dp[nt][e] - d_lo);
-                p[nt][2 + e] = p_hi * (dp[nt][2 + e] - d_hi);
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + kColDP, desc_kmajor(sO, kk), desc_kmajor(stage_v(s), kk), kIdescKK, kk > 0);
+                mma_commit(bar_s);
+                if (!mbar_wait(bar_p, j & 1, &abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + kColDQ, tmem + kColS + kk * 8, desc_mnmajor(stage_k(s), kk), kIdescKM,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar_empty + 8 * s);
             }
+            if (ok)
+                mma_commit(bar_done);
+            else
+                fail(&abort_flag);
+            mma_commit(bar_drain);
+            const volatile int no_abort = 0;
+            mbar_wait(bar_drain, 0, &no_abort, kWaitLimitNs);
         }
-        // dQ += dS K
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t sa[4] = {pack_bf16(p[2 * kk][0], p[2 * kk][1]), pack_bf16(p[2 * kk][2], p[2 * kk][3]),
-                                    pack_bf16(p[2 * kk + 1][0], p[2 * kk + 1][1]),
-                                    pack_bf16(p[2 * kk + 1][2], p[2 * kk + 1][3])};
-#pragma unroll
-            for (int dd = 0; dd < 8; ++dd) {
-                uint32_t r0, r1, r2, r3;
-                ldsm_x4_t(tile_addr(kb, 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3), 2 * dd + (lane >> 4)), r0,
-                          r1, r2, r3);
-                mma_bf16(dq[2 * dd], sa, r0, r1);
-                mma_bf16(dq[2 * dd + 1], sa, r2, r3);
+    } else {
+        // ------------------------------------------------ elementwise warps 0-3 (one query row each)
+        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+        const int r = tid;
+        const size_t slot = bh * g.nq_pad + (size_t)qt * 128 + r;
+        const float l2 = a.lse2_p[slot];
+        const float dl = a.delta_p[slot];
+        bool ok = true;
+        for (int j = 0; j < nkt; ++j) {
+            if (!warp_wait(bar_s, j & 1, &abort_flag)) {
+                ok = false;
+                break;
             }
+            tc_fence_after();
+            const int kk0 = j < nkt_txt ? j * 128 : g.T_txt + (j - nkt_txt) * 128;
+            const int nvalid = (j < nkt_txt ? L : g.S) - kk0;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t rs[32], rd[32];
+                tmem_ld32(tmem + lane_addr + kColS + 32 * c, rs);
+                tmem_ld32(tmem + lane_addr + kColDP + 32 * c, rd);
+                tmem_ld_wait();
+                uint32_t pd[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int col = 32 * c + 2 * e;
+                    const float p0 = col < nvalid ? exp2f(fmaf(__uint_as_float(rs[2 * e]), kC, -l2)) : 0.0f;
+                    const float p1 = col + 1 < nvalid ? exp2f(fmaf(__uint_as_float(rs[2 * e + 1]), kC, -l2)) : 0.0f;
+                    pd[e] = pack_bf16(p0 * (__uint_as_float(rd[2 * e]) - dl), p1 * (__uint_as_float(rd[2 * e + 1]) - dl));
+                }
+                tmem_st16(tmem + lane_addr + kColS + 16 * c, pd);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar_p);
         }
-        __syncthreads();
+        if (ok && warp_wait(bar_done, 0, &abort_flag)) {
+            tc_fence_after();
+            const bool row_ok = q0 + r < q_end;
+            float* dqrow = a.dqh + (bh * g.S + q0 + r) * kHeadDim;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + lane_addr + kColDQ + 32 * c, rr);
+                tmem_ld_wait();
+                if (row_ok) {
+                    float4* dst = reinterpret_cast<float4*>(dqrow + 32 * c);
+#pragma unroll
+                    for (int v4 = 0; v4 < 8; ++v4)
+                        dst[v4] = make_float4(__uint_as_float(rr[4 * v4]) * kScale, __uint_as_float(rr[4 * v4 + 1]) * kScale,
+                                              __uint_as_float(rr[4 * v4 + 2]) * kScale,
+                                              __uint_as_float(rr[4 * v4 + 3]) * kScale);
+                }
+            }
+        } else {
+            fail(&abort_flag);
+        }
     }
 
-    float* dqh = a.dqh + bh * g.S * kHeadDim;
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
-        if (ok_lo)
-            *reinterpret_cast<float2*>(dqh + (size_t)(q0 + r_lo) * kHeadDim + 8 * dt + 2 * gc) =
-                make_float2(dq[dt][0] * kScale, dq[dt][1] * kScale);
-        if (ok_hi)
-            *reinterpret_cast<float2*>(dqh + (size_t)(q0 + r_hi) * kHeadDim + 8 * dt + 2 * gc) =
-                make_float2(dq[dt][2] * kScale, dq[dt][3] * kScale);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// ---------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows) {
+    auto enc = get_encode();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_bshd(CUtensorMap* m, const void* base, const Geom& g) {
+    auto enc = get_encode();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[4] = {128, (cuuint64_t)g.H, (cuuint64_t)g.S, (cuuint64_t)g.B};
+    cuuint64_t strides[3] = {256, (cuuint64_t)g.H * 256, (cuuint64_t)g.S * g.H * 256};
+    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_args(BwdArgs* a, const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
+               const uint16_t* v, const uint16_t* dout, const float* lse2_p, const float* delta_p) {
+    const uint64_t rows = (uint64_t)g.B * g.H * g.S;
+    if (!encode_rows(&a->map_q, qh, rows) || !encode_rows(&a->map_k, kh, rows) || !encode_bshd(&a->map_v, v, g) ||
+        !encode_bshd(&a->map_do, dout, g))
+        return false;
+    a->g = g;
+    a->vl = vl;
+    a->lse2_p = lse2_p;
+    a->delta_p = delta_p;
+    a->dv = nullptr;
+    a->dkh = nullptr;
+    a->dqh = nullptr;
+    return true;
 }
 
 }  // namespace
 
 cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
-                                 const uint16_t* v, const uint16_t* dout, const float* lse, const float* delta,
+                                 const uint16_t* v, const uint16_t* dout, const float* lse2_p, const float* delta_p,
                                  uint16_t* dv, float* dkh, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmem);
+    BwdArgs args;
+    if (!make_args(&args, g, vl, qh, kh, v, dout, lse2_p, delta_p)) return cudaErrorInvalidValue;
+    args.dv = dv;
+    args.dkh = dkh;
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmemBytes);
     if (e != cudaSuccess) return e;
-    BwdArgs args{g, vl, qh, kh, v, dout, lse, delta, dv, dkh, nullptr};
-    const int nkt = (g.T_txt + kKvBK - 1) / kKvBK + (g.T_img + kKvBK - 1) / kKvBK;
-    dim3 grid(nkt, g.H, g.B);
+    dim3 grid(g.ntq_txt + g.ntq_img, g.H, g.B);
     timing_begin(kKBwdDkDv, s);
-    attn_bwd_dkdv_kernel<<<grid, kThreads, kKvSmem, s>>>(args);
+    attn_bwd_dkdv_tc_kernel<<<grid, kThreads, kKvSmemBytes, s>>>(args);
     timing_end(kKBwdDkDv, s);
     return cudaGetLastError();
 }
 
 cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
-                               const uint16_t* v, const uint16_t* dout, const float* lse, const float* delta,
+                               const uint16_t* v, const uint16_t* dout, const float* lse2_p, const float* delta_p,
                                float* dqh, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmem);
+    BwdArgs args;
+    if (!make_args(&args, g, vl, qh, kh, v, dout, lse2_p, delta_p)) return cudaErrorInvalidValue;
+    args.dqh = dqh;
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmemBytes);
     if (e != cudaSuccess) return e;
-    BwdArgs args{g, vl, qh, kh, v, dout, lse, delta, nullptr, nullptr, dqh};
-    const int nqt = (g.T_txt + kDqBQ - 1) / kDqBQ + (g.T_img + kDqBQ - 1) / kDqBQ;
-    dim3 grid(nqt, g.H, g.B);
+    dim3 grid(g.ntq_txt + g.ntq_img, g.H, g.B);
     timing_begin(kKBwdDq, s);
-    attn_bwd_dq_kernel<<<grid, kThreads, kDqSmem, s>>>(args);
+    attn_bwd_dq_tc_kernel<<<grid, kThreads, kDqSmemBytes, s>>>(args);
     timing_end(kKBwdDq, s);
     return cudaGetLastError();
 }

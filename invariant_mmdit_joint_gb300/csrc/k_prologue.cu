@@ -1,7 +1,7 @@
 // HBM-bound kernels of the joint attention path (CUDA cores, FP32 math):
 //   rope_table      cos/sin of every (position, RoPE pair) the call needs
 //   prologue        qk_rmsnorm + multi_axis_rope of Q and K, one bf16 cast
-//   bwd_pre         Delta = rowsum(dO * O)
+//   bwd_pre         Delta = rowsum(dO * O) and lse2 = lse * log2(e), tile padded
 //   norm_rope_bwd   inverse RoPE rotation + RMSNorm backward + per-chunk
 //                   gain-gradient partials
 //   dg_fold         fixed-order folds of the gain-gradient partials
@@ -114,35 +114,47 @@ __global__ void __launch_bounds__(256) prologue_kernel(
     }
 }
 
-// ---------------------------------------------------------------- Delta
-// Delta[b,h,n] = sum_d dO * O in FP32: each lane adds its 8 products in
-// order, then a butterfly over the half warp.
+// ---------------------------------------------------------------- Delta, lse2
+// Backward preprocess in the tile-padded layout: slot r of (b, h) belongs to
+// query tile r / 128 (text tiles first, then image tiles) at offset r % 128.
+// A slot holding a token gets Delta = sum_d dO * O (each lane adds its 8
+// products in order, then a butterfly over the half warp) and
+// lse2 = lse * log2(e); a slot past its segment gets Delta = 0 and
+// lse2 = +inf, so the backward kernels see P = 0 there.
 __global__ void __launch_bounds__(256) bwd_pre_kernel(Geom g, const uint16_t* __restrict__ o,
                                                       const uint16_t* __restrict__ dout,
-                                                      float* __restrict__ delta) {
-    const long long rows = (long long)g.B * g.S * g.H;
-    const long long row_raw = (long long)blockIdx.x * (blockDim.x / kRowThreads) + threadIdx.x / kRowThreads;
+                                                      const float* __restrict__ lse, float* __restrict__ lse2_p,
+                                                      float* __restrict__ delta_p) {
+    const long long slots = (long long)g.B * g.H * g.nq_pad;
+    const long long slot_raw = (long long)blockIdx.x * (blockDim.x / kRowThreads) + threadIdx.x / kRowThreads;
     const int lane16 = threadIdx.x % kRowThreads;
-    const bool active = row_raw < rows;
-    const long long row = active ? row_raw : rows - 1;
-    const int h = (int)(row % g.H);
-    const long long bn = row / g.H;
-    const int n = (int)(bn % g.S);
-    const int b = (int)(bn / g.S);
-    const size_t src = (size_t)row * kHeadDim + 8 * lane16;
-    const uint4 ov = __ldg(reinterpret_cast<const uint4*>(o + src));
-    const uint4 dv = __ldg(reinterpret_cast<const uint4*>(dout + src));
-    const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
-    const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+    const bool active = slot_raw < slots;
+    const long long slot = active ? slot_raw : slots - 1;
+    const long long bh = slot / g.nq_pad;
+    const int r = (int)(slot % g.nq_pad);
+    const int t = r / 128, off = r % 128;
+    const int n = t < g.ntq_txt ? 128 * t + off : g.T_txt + 128 * (t - g.ntq_txt) + off;
+    const bool valid = t < g.ntq_txt ? n < g.T_txt : n < g.S;
+    const int b = (int)(bh / g.H), h = (int)(bh % g.H);
     float acc = 0.0f;
+    if (valid) {
+        const size_t src = (((size_t)b * g.S + n) * g.H + h) * kHeadDim + 8 * lane16;
+        const uint4 ov = __ldg(reinterpret_cast<const uint4*>(o + src));
+        const uint4 dv = __ldg(reinterpret_cast<const uint4*>(dout + src));
+        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+        const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        acc = fmaf(bf16_lo(dw[i]), bf16_lo(ow[i]), acc);
-        acc = fmaf(bf16_hi(dw[i]), bf16_hi(ow[i]), acc);
+        for (int i = 0; i < 4; ++i) {
+            acc = fmaf(bf16_lo(dw[i]), bf16_lo(ow[i]), acc);
+            acc = fmaf(bf16_hi(dw[i]), bf16_hi(ow[i]), acc);
+        }
     }
 #pragma unroll
     for (int m = 8; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-    if (active && lane16 == 0) delta[((size_t)b * g.H + h) * g.S + n] = acc;
+    if (active && lane16 == 0) {
+        delta_p[slot] = acc;
+        lse2_p[slot] = valid ? lse[bh * g.S + n] * 1.4426950408889634f : INFINITY;
+    }
 }
 
 // ---------------------------------------------------------------- norm/rope backward
@@ -290,10 +302,11 @@ cudaError_t launch_prologue(const Geom& g, const uint16_t* q, const uint16_t* k,
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_pre(const Geom& g, const uint16_t* out, const uint16_t* dout, float* delta,
-                           cudaStream_t s) {
+cudaError_t launch_bwd_pre(const Geom& g, const uint16_t* out, const uint16_t* dout, const float* lse,
+                           float* lse2_p, float* delta_p, cudaStream_t s) {
+    const long long slots = (long long)g.B * g.H * g.nq_pad;
     timing_begin(kKBwdPre, s);
-    bwd_pre_kernel<<<row_blocks(g), 256, 0, s>>>(g, out, dout, delta);
+    bwd_pre_kernel<<<(unsigned)((slots + 15) / 16), 256, 0, s>>>(g, out, dout, lse, lse2_p, delta_p);
     timing_end(kKBwdPre, s);
     return cudaGetLastError();
 }

@@ -76,6 +76,9 @@ Geom make_geom(const rlk_ja_shape* sh) {
     g.theta = sh->theta;
     g.n_dg_chunks_txt = (g.T_txt + kDgChunk - 1) / kDgChunk;
     g.n_dg_chunks_img = (g.T_img + kDgChunk - 1) / kDgChunk;
+    g.ntq_txt = (g.T_txt + 127) / 128;
+    g.ntq_img = (g.T_img + 127) / 128;
+    g.nq_pad = 128 * (g.ntq_txt + g.ntq_img);
     return g;
 }
 
@@ -95,14 +98,16 @@ CtxLayout ctx_layout(const Geom& g) {
 }
 
 struct WsLayout {
-    size_t delta, dqh, dkh, dgc, dgp, total;
+    size_t lse2, delta, dqh, dkh, dgc, dgp, total;
 };
 WsLayout ws_layout(const Geom& g) {
     const size_t rows = (size_t)g.B * g.H * g.S;
+    const size_t slots = (size_t)g.B * g.H * g.nq_pad;
     const size_t nch = (size_t)g.n_dg_chunks_txt + g.n_dg_chunks_img;
     WsLayout l{};
-    l.delta = 0;
-    l.dqh = align_up(l.delta + rows * 4);
+    l.lse2 = 0;
+    l.delta = align_up(l.lse2 + slots * 4);
+    l.dqh = align_up(l.delta + slots * 4);
     l.dkh = align_up(l.dqh + rows * kHeadDim * 4);
     l.dgc = align_up(l.dkh + rows * kHeadDim * 4);
     l.dgp = align_up(l.dgc + (size_t)g.B * g.H * 2 * nch * kHeadDim * 4);
@@ -281,7 +286,8 @@ rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape, const void* q, const vo
     const float* rk = reinterpret_cast<const float*>(c + l.rk);
     const float2* tab = reinterpret_cast<const float2*>(c + l.tab);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    float* delta = reinterpret_cast<float*>(ws + w.delta);
+    float* lse2_p = reinterpret_cast<float*>(ws + w.lse2);
+    float* delta_p = reinterpret_cast<float*>(ws + w.delta);
     float* dqh = reinterpret_cast<float*>(ws + w.dqh);
     float* dkh = reinterpret_cast<float*>(ws + w.dkh);
     float* dgc = reinterpret_cast<float*>(ws + w.dgc);
@@ -290,10 +296,12 @@ rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape, const void* q, const vo
     const uint16_t* vv = static_cast<const uint16_t*>(v);
     const uint16_t* dO = static_cast<const uint16_t*>(dout);
 
-    if (launch_bwd_pre(g, static_cast<const uint16_t*>(out), dO, delta, s) != cudaSuccess) return RLK_ERR_CUDA;
-    if (launch_attn_bwd_dkdv(g, vl, qh, kh, vv, dO, lse, delta, static_cast<uint16_t*>(dv), dkh, s) != cudaSuccess)
+    if (launch_bwd_pre(g, static_cast<const uint16_t*>(out), dO, lse, lse2_p, delta_p, s) != cudaSuccess)
         return RLK_ERR_CUDA;
-    if (launch_attn_bwd_dq(g, vl, qh, kh, vv, dO, lse, delta, dqh, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_attn_bwd_dkdv(g, vl, qh, kh, vv, dO, lse2_p, delta_p, static_cast<uint16_t*>(dv), dkh, s) !=
+        cudaSuccess)
+        return RLK_ERR_CUDA;
+    if (launch_attn_bwd_dq(g, vl, qh, kh, vv, dO, lse2_p, delta_p, dqh, s) != cudaSuccess) return RLK_ERR_CUDA;
     if (launch_norm_rope_bwd(g, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), gains, tab, rq,
                              rk, dqh, dkh, static_cast<uint16_t*>(dq), static_cast<uint16_t*>(dk), dgc,
                              s) != cudaSuccess)
@@ -317,9 +325,9 @@ int rlk_strict_math_compiled(void) { return strict_all_units(); }
 rlk_status rlk_joint_attn_trace(rlk_ja_trace* out) {
     if (out == nullptr) return RLK_ERR_INVALID_ARG;
     std::memset(out, 0, sizeof(*out));
-    std::snprintf(out->backend, sizeof(out->backend), "sm_103a tcgen05/mma.sync");
+    std::snprintf(out->backend, sizeof(out->backend), "sm_103a tcgen05");
     std::snprintf(out->reduction_order, sizeof(out->reduction_order),
-                  "kv tiles: text from 0 then image from T_txt, ascending; dkdv: q tiles ascending; "
+                  "tiles of 128: text from 0 then image from T_txt, ascending; dkdv: q tiles ascending; "
                   "rows: lane order + xor butterfly; dg: chunks, h, b ascending");
     std::snprintf(out->accumulator, sizeof(out->accumulator), "fp32");
     out->split_k = 0;

@@ -24,6 +24,10 @@ struct Geom {
     int p_lo, n_pos;    // cos/sin table covers positions [p_lo, p_lo + n_pos)
     float eps, theta;
     int n_dg_chunks_txt, n_dg_chunks_img;
+    // query / key tiles of 128, segment aligned: text tiles from token 0,
+    // image tiles from token T_txt; nq_pad = 128 * (ntq_txt + ntq_img) slots
+    // per (b, h) in the tile-padded layout of lse2 and Delta
+    int ntq_txt, ntq_img, nq_pad;
 };
 
 // Per-sample valid text lengths travel by value as a kernel argument.
@@ -63,7 +67,7 @@ cudaError_t launch_prologue(const Geom& g, const uint16_t* q, const uint16_t* k,
                             uint16_t* qh, uint16_t* kh, float* rq, float* rk,
                             cudaStream_t s);
 cudaError_t launch_bwd_pre(const Geom& g, const uint16_t* out, const uint16_t* dout,
-                           float* delta, cudaStream_t s);
+                           const float* lse, float* lse2_p, float* delta_p, cudaStream_t s);
 cudaError_t launch_norm_rope_bwd(const Geom& g, const uint16_t* q, const uint16_t* k,
                                  const float* const gains[4], const float2* tab,
                                  const float* rq, const float* rk,
@@ -84,13 +88,13 @@ int read_and_clear_status_fwd(cudaStream_t s);
 // k_attn_bwd.cu
 cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16_t* qh,
                                  const uint16_t* kh, const uint16_t* v,
-                                 const uint16_t* dout, const float* lse,
-                                 const float* delta, uint16_t* dv, float* dkh,
+                                 const uint16_t* dout, const float* lse2_p,
+                                 const float* delta_p, uint16_t* dv, float* dkh,
                                  cudaStream_t s);
 cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t* qh,
                                const uint16_t* kh, const uint16_t* v,
-                               const uint16_t* dout, const float* lse,
-                               const float* delta, float* dqh, cudaStream_t s);
+                               const uint16_t* dout, const float* lse2_p,
+                               const float* delta_p, float* dqh, cudaStream_t s);
 int probe_bwd_tu(void);
 int read_and_clear_status_bwd(cudaStream_t s);
 

@@ -52,7 +52,9 @@ def test_buffer_sizes_match_documented_layout(L):
     ctx = up(up(up(up(rows * 256) + rows * 256) + rows * 4) + rows * 4) + n_pos * 64 * 8
     assert pkg.rlk_joint_attn_ctx_bytes(s) == up(ctx)
     nch = 256 // 64 + 4096 // 64
-    ws = up(up(up(up(rows * 4) + rows * 512) + rows * 512) + 2 * 24 * 2 * nch * 512) + 2 * 24 * 4 * 512
+    slots = 2 * 24 * 128 * (256 // 128 + 4096 // 128)  # tile-padded lse2 and Delta
+    ws = up(up(up(up(up(slots * 4) + slots * 4) + rows * 512) + rows * 512) + 2 * 24 * 2 * nch * 512)
+    ws += 2 * 24 * 4 * 512
     assert pkg.rlk_joint_attn_bwd_workspace_bytes(s) == up(ws)
     assert S == s.S
 
