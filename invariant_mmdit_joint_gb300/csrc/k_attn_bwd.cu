@@ -32,7 +32,12 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 192;
+// warps 0-7: elementwise (warp w owns TMEM lane quarter w % 4 and the
+// column half w / 4 of each row); warp 8: TMA producer; warp 9: MMA issuer
+// and TMEM owner.
+constexpr int kThreads = 320;
+constexpr int kEwThreads = 256;
+constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr int kBoxBytes = 128 * 128;       // 128 rows x 64 bf16
 constexpr int kTileBytes = 2 * kBoxBytes;  // 128 rows x 128 bf16
 constexpr uint32_t kTmemCols = 512;
@@ -71,6 +76,12 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
     return sdesc_sw128(tile + kk * 2048, kBoxBytes, 1024);
 }
+
+// TMEM column of the bf16 A operand (P or dS) for k-step kk: the column
+// half h = kk / 4 of the 128 fp32 columns is rewritten in place as 32 packed
+// columns at the start of that half, so the two warps sharing a lane
+// quarter never overwrite each other's unread scores.
+__device__ __forceinline__ uint32_t a_col(int kk) { return (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8; }
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitLimitNs));
@@ -146,12 +157,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
             mbar_init(bar_empty + 8 * s, 1);
         }
         mbar_init(bar_s, 1);
-        mbar_init(bar_p, 128);
+        mbar_init(bar_p, kEwThreads);
         mbar_init(bar_done, 1);
         mbar_init(bar_drain, 1);
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -160,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
-    if (warp == 4) {
+    if (warp == kWarpTma) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tensormap(&a.map_q);
@@ -197,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
             for (int i = issued - 2 < 0 ? 0 : issued - 2; i < issued; ++i)
                 mbar_wait(bar_full + 8 * (i & 1), (i >> 1) & 1, &no_abort, kWaitLimitNs);
         }
-    } else if (warp == 5) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             bool ok = mbar_wait(bar_kv, 0, &abort_flag, kWaitLimitNs);
@@ -222,11 +233,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kColDV, tmem + kColST + kk * 8, desc_mnmajor(stage_o(s), kk), kIdescKM,
+                    mma_ts(tmem + kColDV, tmem + kColST + a_col(kk), desc_mnmajor(stage_o(s), kk), kIdescKM,
                            (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kColDK, tmem + kColDPT + kk * 8, desc_mnmajor(stage_q(s), kk), kIdescKM,
+                    mma_ts(tmem + kColDK, tmem + kColDPT + a_col(kk), desc_mnmajor(stage_q(s), kk), kIdescKM,
                            (i > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar_empty + 8 * s);
             }
@@ -239,9 +250,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
             mbar_wait(bar_drain, 0, &no_abort, kWaitLimitNs);
         }
     } else {
-        // ------------------------------------------------ elementwise warps 0-3 (one key row each)
-        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-        const int kr = tid;
+        // ------------------------------------------------ elementwise warps 0-7
+        // warp w: key rows 32 * (w % 4) + lane, query columns [64 h, 64 h + 64), h = w / 4
+        const int lq = warp & 3, half = warp >> 2;
+        const uint32_t lane_addr = (uint32_t)(lq * 32) << 16;
+        const int kr = lq * 32 + lane;
+        const int c0 = 64 * half;
         const bool kvalid = k0 + kr < kvalid_end;
         bool ok = true;
         for (int i = 0; i < nq; ++i) {
@@ -251,29 +265,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
                 break;
             }
             tc_fence_after();
-            const float* l2 = reinterpret_cast<const float*>(smem_raw + (stage_l(s) - smem_u32(smem_raw)));
+            const float* l2 = reinterpret_cast<const float*>(smem_raw + (stage_l(s) - smem_u32(smem_raw))) + c0;
             const float* dl = l2 + 128;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t rs[32], rd[32];
-                tmem_ld32(tmem + lane_addr + kColST + 32 * c, rs);
-                tmem_ld32(tmem + lane_addr + kColDPT + 32 * c, rd);
-                tmem_ld_wait();
-                uint32_t pp[16], pd[16];
+            uint32_t rs[2][32], rd[2][32];
+            tmem_ld32(tmem + lane_addr + kColST + c0, rs[0]);
+            tmem_ld32(tmem + lane_addr + kColST + c0 + 32, rs[1]);
+            tmem_ld32(tmem + lane_addr + kColDPT + c0, rd[0]);
+            tmem_ld32(tmem + lane_addr + kColDPT + c0 + 32, rd[1]);
+            tmem_ld_wait();
+            uint32_t pp[32], pd[32];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const int q = 32 * c + 2 * e;
-                    float p0 = exp2f(fmaf(__uint_as_float(rs[2 * e]), kC, -l2[q]));
-                    float p1 = exp2f(fmaf(__uint_as_float(rs[2 * e + 1]), kC, -l2[q + 1]));
-                    if (!kvalid) p0 = p1 = 0.0f;
-                    const float d0 = p0 * (__uint_as_float(rd[2 * e]) - dl[q]);
-                    const float d1 = p1 * (__uint_as_float(rd[2 * e + 1]) - dl[q + 1]);
-                    pp[e] = pack_bf16(p0, p1);
-                    pd[e] = pack_bf16(d0, d1);
+                    const int q = 32 * hh + 2 * e;
+                    float p0 = exp2f(fmaf(__uint_as_float(rs[hh][2 * e]), kC, -l2[q]));
+                    float p1 = exp2f(fmaf(__uint_as_float(rs[hh][2 * e + 1]), kC, -l2[q + 1]));
+                    p0 = kvalid ? p0 : 0.0f;
+                    p1 = kvalid ? p1 : 0.0f;
+                    const float d0 = p0 * (__uint_as_float(rd[hh][2 * e]) - dl[q]);
+                    const float d1 = p1 * (__uint_as_float(rd[hh][2 * e + 1]) - dl[q + 1]);
+                    pp[16 * hh + e] = pack_bf16(p0, p1);
+                    pd[16 * hh + e] = pack_bf16(d0, d1);
                 }
-                tmem_st16(tmem + lane_addr + kColST + 16 * c, pp);
-                tmem_st16(tmem + lane_addr + kColDPT + 16 * c, pd);
             }
+            tmem_st32(tmem + lane_addr + kColST + c0, pp);
+            tmem_st32(tmem + lane_addr + kColDPT + c0, pd);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_p);
@@ -285,24 +302,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
             uint16_t* dvrow = a.dv + (((size_t)b * g.S + j) * g.H + h) * kHeadDim;
             float* dkrow = dkh + (size_t)j * kHeadDim;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = c0; c < c0 + 64; c += 32) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_addr + kColDV + 32 * c, r);
+                tmem_ld32(tmem + lane_addr + kColDV + c, r);
                 tmem_ld_wait();
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     w[e] = kvalid ? pack_bf16(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])) : 0u;
                 if (row_ok) {
-                    uint4* dst = reinterpret_cast<uint4*>(dvrow + 32 * c);
+                    uint4* dst = reinterpret_cast<uint4*>(dvrow + c);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4)
                         dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
                 }
-                tmem_ld32(tmem + lane_addr + kColDK + 32 * c, r);
+                tmem_ld32(tmem + lane_addr + kColDK + c, r);
                 tmem_ld_wait();
                 if (row_ok) {
-                    float4* dst = reinterpret_cast<float4*>(dkrow + 32 * c);
+                    float4* dst = reinterpret_cast<float4*>(dkrow + c);
 #pragma unroll
                     for (int v4 = 0; v4 < 8; ++v4) {
                         float4 f;
@@ -321,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -370,12 +387,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
             mbar_init(bar_empty + 8 * s, 1);
         }
         mbar_init(bar_s, 1);
-        mbar_init(bar_p, 128);
+        mbar_init(bar_p, kEwThreads);
         mbar_init(bar_done, 1);
         mbar_init(bar_drain, 1);
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -384,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
-    if (warp == 4) {
+    if (warp == kWarpTma) {
         if (lane == 0) {
             prefetch_tensormap(&a.map_q);
             prefetch_tensormap(&a.map_k);
@@ -416,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
             for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
                 mbar_wait(bar_full + 8 * (j & 1), (j >> 1) & 1, &no_abort, kWaitLimitNs);
         }
-    } else if (warp == 5) {
+    } else if (warp == kWarpMma) {
         if (lane == 0) {
             bool ok = mbar_wait(bar_qo, 0, &abort_flag, kWaitLimitNs);
             for (int j = 0; ok && j < nkt; ++j) {
@@ -440,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kColDQ, tmem + kColS + kk * 8, desc_mnmajor(stage_k(s), kk), kIdescKM,
+                    mma_ts(tmem + kColDQ, tmem + kColS + a_col(kk), desc_mnmajor(stage_k(s), kk), kIdescKM,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar_empty + 8 * s);
             }
@@ -453,9 +470,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
             mbar_wait(bar_drain, 0, &no_abort, kWaitLimitNs);
         }
     } else {
-        // ------------------------------------------------ elementwise warps 0-3 (one query row each)
-        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-        const int r = tid;
+        // ------------------------------------------------ elementwise warps 0-7
+        // warp w: query rows 32 * (w % 4) + lane, key columns [64 h, 64 h + 64), h = w / 4
+        const int lq = warp & 3, half = warp >> 2;
+        const uint32_t lane_addr = (uint32_t)(lq * 32) << 16;
+        const int r = lq * 32 + lane;
+        const int c0 = 64 * half;
         const size_t slot = bh * g.nq_pad + (size_t)qt * 128 + r;
         const float l2 = a.lse2_p[slot];
         const float dl = a.delta_p[slot];
@@ -467,23 +487,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
             }
             tc_fence_after();
             const int kk0 = j < nkt_txt ? j * 128 : g.T_txt + (j - nkt_txt) * 128;
-            const int nvalid = (j < nkt_txt ? L : g.S) - kk0;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t rs[32], rd[32];
-                tmem_ld32(tmem + lane_addr + kColS + 32 * c, rs);
-                tmem_ld32(tmem + lane_addr + kColDP + 32 * c, rd);
-                tmem_ld_wait();
-                uint32_t pd[16];
+            const int nvalid = (j < nkt_txt ? L : g.S) - kk0 - c0;  // valid columns of this half
+            uint32_t rs[2][32], rd[2][32];
+            tmem_ld32(tmem + lane_addr + kColS + c0, rs[0]);
+            tmem_ld32(tmem + lane_addr + kColS + c0 + 32, rs[1]);
+            tmem_ld32(tmem + lane_addr + kColDP + c0, rd[0]);
+            tmem_ld32(tmem + lane_addr + kColDP + c0 + 32, rd[1]);
+            tmem_ld_wait();
+            uint32_t pd[32];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const int col = 32 * c + 2 * e;
-                    const float p0 = col < nvalid ? exp2f(fmaf(__uint_as_float(rs[2 * e]), kC, -l2)) : 0.0f;
-                    const float p1 = col + 1 < nvalid ? exp2f(fmaf(__uint_as_float(rs[2 * e + 1]), kC, -l2)) : 0.0f;
-                    pd[e] = pack_bf16(p0 * (__uint_as_float(rd[2 * e]) - dl), p1 * (__uint_as_float(rd[2 * e + 1]) - dl));
+                    const int col = 32 * hh + 2 * e;
+                    float p0 = exp2f(fmaf(__uint_as_float(rs[hh][2 * e]), kC, -l2));
+                    float p1 = exp2f(fmaf(__uint_as_float(rs[hh][2 * e + 1]), kC, -l2));
+                    p0 = col < nvalid ? p0 : 0.0f;
+                    p1 = col + 1 < nvalid ? p1 : 0.0f;
+                    pd[16 * hh + e] = pack_bf16(p0 * (__uint_as_float(rd[hh][2 * e]) - dl),
+                                                p1 * (__uint_as_float(rd[hh][2 * e + 1]) - dl));
                 }
-                tmem_st16(tmem + lane_addr + kColS + 16 * c, pd);
             }
+            tmem_st32(tmem + lane_addr + kColS + c0, pd);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_p);
@@ -493,12 +518,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
             const bool row_ok = q0 + r < q_end;
             float* dqrow = a.dqh + (bh * g.S + q0 + r) * kHeadDim;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = c0; c < c0 + 64; c += 32) {
                 uint32_t rr[32];
-                tmem_ld32(tmem + lane_addr + kColDQ + 32 * c, rr);
+                tmem_ld32(tmem + lane_addr + kColDQ + c, rr);
                 tmem_ld_wait();
                 if (row_ok) {
-                    float4* dst = reinterpret_cast<float4*>(dqrow + 32 * c);
+                    float4* dst = reinterpret_cast<float4*>(dqrow + c);
 #pragma unroll
                     for (int v4 = 0; v4 < 8; ++v4)
                         dst[v4] = make_float4(__uint_as_float(rr[4 * v4]) * kScale, __uint_as_float(rr[4 * v4 + 1]) * kScale,
@@ -513,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }

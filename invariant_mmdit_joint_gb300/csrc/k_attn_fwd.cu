@@ -243,24 +243,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             }
             tc_fence_after();
             const uint32_t s_tmem = tmem + lane_addr + (s ? kColS1 : kColS0);
+            uint32_t xr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + 32 * c, xr[c]);
+            tmem_ld_wait();
             float x[128];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(s_tmem + 32 * c, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(r[i]);
-            }
+            for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(xr[c >> 5][c & 31]);
             const TileInfo t = kv_tile(g, L, nkt_txt, j);
             const int nvalid = t.kend - t.k0;  // keys k0 + c with c < nvalid are valid
-            float mx = -INFINITY;
+            if (nvalid < 128) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                x[c] = c < nvalid ? x[c] * kC : -INFINITY;
-                mx = fmaxf(mx, x[c]);
+                for (int c = 0; c < 128; ++c) x[c] = c < nvalid ? x[c] : -INFINITY;
             }
-            const float m_new = fmaxf(m, mx);
+            // row max of the raw scores: eight interleaved partial maxima,
+            // then a fixed tree (max is exact in any order)
+            float mp[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mp[i] = x[i];
+#pragma unroll
+            for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
+            const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                   fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+            const float m_new = fmaxf(m, mx * kC);  // running max in log2 units
             const float alpha = exp2f(m - m_new);
             if (j > 0) {
                 // PV_{j-1} has finished writing O
@@ -284,17 +289,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                     tmem_st_wait();
                 }
             }
-            float rs = 0.0f;
+            // p = exp2(s * c - m); the row sum adds column c into partial
+            // c % 8, and the eight partials in a fixed tree
+            float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             uint32_t pa[32], pb[32];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                const float p0 = exp2f(x[2 * c] - m_new);
-                const float p1 = exp2f(x[2 * c + 1] - m_new);
-                rs += p0;
-                rs += p1;
+                const float p0 = exp2f(fmaf(x[2 * c], kC, -m_new));
+                const float p1 = exp2f(fmaf(x[2 * c + 1], kC, -m_new));
+                sp[(2 * c) & 7] += p0;
+                sp[(2 * c + 1) & 7] += p1;
                 if (c < 32) pa[c] = pack_bf16(p0, p1);
                 else pb[c - 32] = pack_bf16(p0, p1);
             }
+            const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
             l = l * alpha + rs;
             m = m_new;
             tmem_st32(s_tmem, pa);
