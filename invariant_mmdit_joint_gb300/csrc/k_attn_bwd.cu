@@ -12,7 +12,8 @@
 //           dV  += P^T dO,  dK += dS^T Q           (tcgen05, A from TMEM)
 //   dq:   one CTA = (query tile of 128, head, sample). Walks the key tiles of
 //         128 in the forward's order: S = Q K^T, dP = dO V^T, dS as above,
-//         dQ += dS K.
+//         dQ += dS K; the next tile's S and dP are computed while the
+//         elementwise warps work on the current one.
 // Accumulators (dV, dK, dQ) stay in TMEM in FP32 for the whole CTA and are
 // written once. P and dS enter their products as bf16 (round to nearest
 // even). lse2 = lse * log2(e) and Delta = rowsum(dO * O) come from the
@@ -77,6 +78,12 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
     return sdesc_sw128(tile + kk * 2048, kBoxBytes, 1024);
 }
 
+// TMEM column of the bf16 A operand (P or dS) for k-step kk: the column
+// half h = kk / 4 of the 128 fp32 columns is rewritten in place as 32 packed
+// columns at the start of that half, so the two warps sharing a lane
+// quarter never overwrite each other's unread scores.
+__device__ __forceinline__ uint32_t a_col(int kk) { return (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8; }
+
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitLimitNs));
 }
@@ -93,24 +100,14 @@ __device__ __forceinline__ void q_tile(const Geom& g, int i, int& q0, int& q_end
 }
 
 // ====================================================================== dK, dV
-// Each query tile is processed as two column halves h = 0, 1 (queries
-// [64h, 64h + 64) of the tile) with their own barriers: warps 0-3 take half
-// 0, warps 4-7 half 1. The MMA thread issues, per tile i,
-//   [P_0(i) ready] dV += P_0 dO_0, dK += dS_0 Q_0; S^T_0(i+1), dP^T_0(i+1)
-//   [P_1(i) ready] dV += P_1 dO_1, dK += dS_1 Q_1; S^T_1(i+1), dP^T_1(i+1)
-// so the tensor core works on one half while the warps of the other half
-// compute; the dV/dK reduction order (tiles ascending, half 0 then half 1)
-// is fixed.
 constexpr int kKvSmemK = 0, kKvSmemV = kTileBytes, kKvSmemStage = 2 * kTileBytes;
 constexpr int kKvStageBytes = 2 * kTileBytes + 1024;  // Q, dO, lse2[128], delta[128]
 constexpr int kKvSmemBytes = kKvSmemStage + 2 * kKvStageBytes + 1024;
-constexpr uint32_t kColDV = 0, kColDK = 128, kColST = 256, kColDPT = 384;  // S^T, dP^T: 64 columns per half
-constexpr uint32_t kIdescN64 = idesc_bf16(128, 64, false, false);
-constexpr int kHalfRowBytes = 64 * 128;  // byte offset of row 64 inside a 128-row swizzled box
+constexpr uint32_t kColDV = 0, kColDK = 128, kColST = 256, kColDPT = 384;
 
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[12];
+    __shared__ __align__(8) uint64_t bars[10];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
@@ -146,12 +143,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
     auto stage_o = [&](int s) { return stage_q(s) + kTileBytes; };
     auto stage_l = [&](int s) { return stage_q(s) + 2 * kTileBytes; };
     const uint32_t bar_kv = smem_u32(&bars[0]);
-    const uint32_t bar_full = smem_u32(&bars[1]);   // [2] stages
-    const uint32_t bar_empty = smem_u32(&bars[3]);  // [2] stages
-    const uint32_t bar_s = smem_u32(&bars[5]);      // [2] halves
-    const uint32_t bar_p = smem_u32(&bars[7]);      // [2] halves
-    const uint32_t bar_done = smem_u32(&bars[9]);
-    const uint32_t bar_drain = smem_u32(&bars[10]);
+    const uint32_t bar_full = smem_u32(&bars[1]);   // [2]
+    const uint32_t bar_empty = smem_u32(&bars[3]);  // [2]
+    const uint32_t bar_s = smem_u32(&bars[5]);
+    const uint32_t bar_p = smem_u32(&bars[6]);
+    const uint32_t bar_done = smem_u32(&bars[7]);
+    const uint32_t bar_drain = smem_u32(&bars[8]);
 
     if (tid == 0) {
         abort_flag = 0;
@@ -159,9 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
-            mbar_init(bar_s + 8 * s, 1);
-            mbar_init(bar_p + 8 * s, 128);
         }
+        mbar_init(bar_s, 1);
+        mbar_init(bar_p, kEwThreads);
         mbar_init(bar_done, 1);
         mbar_init(bar_drain, 1);
         fence_barrier_init();
@@ -215,65 +212,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
     } else if (warp == kWarpMma) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            // S^T_hf = K Q_hf^T and dP^T_hf = V dO_hf^T for query half hf of stage s
-            auto issue_scores = [&](int s, int hf) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kColST + 64 * hf, desc_kmajor(sK, kk),
-                           desc_kmajor(stage_q(s) + hf * kHalfRowBytes, kk), kIdescN64, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kColDPT + 64 * hf, desc_kmajor(sV, kk),
-                           desc_kmajor(stage_o(s) + hf * kHalfRowBytes, kk), kIdescN64, kk > 0);
-                mma_commit(bar_s + 8 * hf);
-            };
-            // dV += P_hf dO_hf, dK += dS_hf Q_hf: the 64 queries of the half
-            auto issue_grads = [&](int s, int hf, bool first) {
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const int kk = 4 * hf + k4;
-                    mma_ts(tmem + kColDV, tmem + kColST + 64 * hf + 8 * k4, desc_mnmajor(stage_o(s), kk), kIdescKM,
-                           (first && k4 == 0) ? 0u : 1u);
-                }
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const int kk = 4 * hf + k4;
-                    mma_ts(tmem + kColDK, tmem + kColDPT + 64 * hf + 8 * k4, desc_mnmajor(stage_q(s), kk),
-                           kIdescKM, (first && k4 == 0) ? 0u : 1u);
-                }
-            };
-            bool ok = mbar_wait(bar_kv, 0, &abort_flag, kWaitLimitNs) &&
-                      mbar_wait(bar_full, 0, &abort_flag, kWaitLimitNs);
-            if (ok) {
-                tc_fence_after();
-                issue_scores(0, 0);
-                issue_scores(0, 1);
-            }
+            bool ok = mbar_wait(bar_kv, 0, &abort_flag, kWaitLimitNs);
             for (int i = 0; ok && i < nq; ++i) {
-                const int s = i & 1, s1 = (i + 1) & 1;
-                const bool more = i + 1 < nq;
+                const int s = i & 1;
+                if (!mbar_wait(bar_full + 8 * s, (i >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + kColST, desc_kmajor(sK, kk), desc_kmajor(stage_q(s), kk), kIdescKK, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + kColDPT, desc_kmajor(sV, kk), desc_kmajor(stage_o(s), kk), kIdescKK, kk > 0);
+                mma_commit(bar_s);
                 if (!mbar_wait(bar_p, i & 1, &abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                issue_grads(s, 0, i == 0);
-                if (more) {
-                    if (!mbar_wait(bar_full + 8 * s1, ((i + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_scores(s1, 0);
-                }
-                if (!mbar_wait(bar_p + 8, i & 1, &abort_flag, kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                issue_grads(s, 1, false);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + kColDV, tmem + kColST + a_col(kk), desc_mnmajor(stage_o(s), kk), kIdescKM,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + kColDK, tmem + kColDPT + a_col(kk), desc_mnmajor(stage_q(s), kk), kIdescKM,
+                           (i > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar_empty + 8 * s);
-                if (more) issue_scores(s1, 1);
             }
             if (ok)
                 mma_commit(bar_done);
@@ -285,29 +252,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
         }
     } else {
         // ------------------------------------------------ elementwise warps 0-7
-        // warp w: key rows 32 * (w % 4) + lane, query half hf = w / 4
-        const int lq = warp & 3, hf = warp >> 2;
+        // warp w: key rows 32 * (w % 4) + lane, query columns [64 h, 64 h + 64), h = w / 4
+        const int lq = warp & 3, half = warp >> 2;
         const uint32_t lane_addr = (uint32_t)(lq * 32) << 16;
         const int kr = lq * 32 + lane;
+        const int c0 = 64 * half;
         const bool kvalid = k0 + kr < kvalid_end;
-        const uint32_t st_cols = tmem + lane_addr + kColST + 64 * hf;
-        const uint32_t dp_cols = tmem + lane_addr + kColDPT + 64 * hf;
         bool ok = true;
         for (int i = 0; i < nq; ++i) {
             const int s = i & 1;
-            if (!warp_wait(bar_full + 8 * s, (i >> 1) & 1, &abort_flag) ||
-                !warp_wait(bar_s + 8 * hf, i & 1, &abort_flag)) {
+            if (!warp_wait(bar_full + 8 * s, (i >> 1) & 1, &abort_flag) || !warp_wait(bar_s, i & 1, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t rs[2][32], rd[2][32];
-            tmem_ld32(st_cols, rs[0]);
-            tmem_ld32(st_cols + 32, rs[1]);
-            tmem_ld32(dp_cols, rd[0]);
-            tmem_ld32(dp_cols + 32, rd[1]);
-            const float4* l2v = reinterpret_cast<const float4*>(smem_raw + (stage_l(s) - smem_u32(smem_raw))) + 16 * hf;
+            const float4* l2v =
+                reinterpret_cast<const float4*>(smem_raw + (stage_l(s) - smem_u32(smem_raw))) + c0 / 4;
             const float4* dlv = l2v + 32;
+            uint32_t rs[2][32], rd[2][32];
+            tmem_ld32(tmem + lane_addr + kColST + c0, rs[0]);
+            tmem_ld32(tmem + lane_addr + kColST + c0 + 32, rs[1]);
+            tmem_ld32(tmem + lane_addr + kColDPT + c0, rd[0]);
+            tmem_ld32(tmem + lane_addr + kColDPT + c0 + 32, rd[1]);
             tmem_ld_wait();
             uint32_t pp[32], pd[32];
 #pragma unroll
@@ -331,11 +297,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
                     pd[16 * hh + 2 * e4 + 1] = pack_bf16(ds[2], ds[3]);
                 }
             }
-            tmem_st32(st_cols, pp);
-            tmem_st32(dp_cols, pd);
+            tmem_st32(tmem + lane_addr + kColST + c0, pp);
+            tmem_st32(tmem + lane_addr + kColDPT + c0, pd);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar_p + 8 * hf);
+            mbar_arrive(bar_p);
         }
         if (ok && warp_wait(bar_done, 0, &abort_flag)) {
             tc_fence_after();
@@ -344,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
             uint16_t* dvrow = a.dv + (((size_t)b * g.S + j) * g.H + h) * kHeadDim;
             float* dkrow = dkh + (size_t)j * kHeadDim;
 #pragma unroll 1
-            for (int c = 64 * hf; c < 64 * hf + 64; c += 32) {
+            for (int c = c0; c < c0 + 64; c += 32) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_addr + kColDV + c, r);
                 tmem_ld_wait();
@@ -387,16 +353,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
 }
 
 // ====================================================================== dQ
-// Each key tile is processed as two halves h = 0, 1 (keys [64h, 64h + 64))
-// with their own barriers, warps 0-3 on half 0 and warps 4-7 on half 1;
-// per tile j the MMA thread issues
-//   [dS_0(j) ready] dQ += dS_0 K_0; S_0(j+1), dP_0(j+1)
-//   [dS_1(j) ready] dQ += dS_1 K_1; S_1(j+1), dP_1(j+1)
-// (reduction order over keys fixed: tiles ascending, half 0 then half 1).
+// TMEM: R0, R1 (scores of alternate key tiles), dP, dQ. Per key tile j the
+// elementwise warps pull S_j and dP_j into registers and report "consumed";
+// the MMA thread then computes S_{j+1} into the other R region and dP_{j+1}
+// over dP while the warps form dS_j = P (dP - Delta) and write it (bf16) over
+// S_j; then dQ += dS_j K_j. Reduction order over keys: tiles ascending.
 constexpr int kDqSmemQ = 0, kDqSmemO = kTileBytes, kDqSmemStage = 2 * kTileBytes;
 constexpr int kDqStageBytes = 2 * kTileBytes;  // K, V
 constexpr int kDqSmemBytes = kDqSmemStage + 2 * kDqStageBytes + 1024;
-constexpr uint32_t kColDQ = 0, kColS = 128, kColDP = 256;  // S, dP: 64 columns per half
+constexpr uint32_t kColR0 = 0, kColR1 = 128, kColDP = 256, kColDQ = 384;
 
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -419,11 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
     const uint32_t sQ = sbase + kDqSmemQ, sO = sbase + kDqSmemO;
     auto stage_k = [&](int s) { return sbase + kDqSmemStage + s * kDqStageBytes; };
     auto stage_v = [&](int s) { return stage_k(s) + kTileBytes; };
+    auto col_r = [&](int j) { return (j & 1) ? kColR1 : kColR0; };
     const uint32_t bar_qo = smem_u32(&bars[0]);
     const uint32_t bar_full = smem_u32(&bars[1]);   // [2] stages
     const uint32_t bar_empty = smem_u32(&bars[3]);  // [2] stages
-    const uint32_t bar_s = smem_u32(&bars[5]);      // [2] halves
-    const uint32_t bar_p = smem_u32(&bars[7]);      // [2] halves
+    const uint32_t bar_s = smem_u32(&bars[5]);      // S_j, dP_j computed
+    const uint32_t bar_c = smem_u32(&bars[6]);      // S_j, dP_j read into registers
+    const uint32_t bar_p = smem_u32(&bars[7]);      // [2] by tile parity: dS_j written
     const uint32_t bar_done = smem_u32(&bars[9]);
     const uint32_t bar_drain = smem_u32(&bars[10]);
 
@@ -433,9 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
-            mbar_init(bar_s + 8 * s, 1);
-            mbar_init(bar_p + 8 * s, 128);
+            mbar_init(bar_p + 8 * s, kEwThreads);
         }
+        mbar_init(bar_s, 1);
+        mbar_init(bar_c, kEwThreads);
         mbar_init(bar_done, 1);
         mbar_init(bar_drain, 1);
         fence_barrier_init();
@@ -483,57 +451,44 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
         }
     } else if (warp == kWarpMma) {
         if (lane == 0) {
-            // S_hf = Q K_hf^T and dP_hf = dO V_hf^T for key half hf of stage s
-            auto issue_scores = [&](int s, int hf) {
+            // S_j = Q K_j^T into R(j), dP_j = dO V_j^T into dP
+            auto issue_scores = [&](int j) {
+                const int s = j & 1;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kColS + 64 * hf, desc_kmajor(sQ, kk),
-                           desc_kmajor(stage_k(s) + hf * kHalfRowBytes, kk), kIdescN64, kk > 0);
+                    mma_ss(tmem + col_r(j), desc_kmajor(sQ, kk), desc_kmajor(stage_k(s), kk), kIdescKK, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kColDP + 64 * hf, desc_kmajor(sO, kk),
-                           desc_kmajor(stage_v(s) + hf * kHalfRowBytes, kk), kIdescN64, kk > 0);
-                mma_commit(bar_s + 8 * hf);
-            };
-            // dQ += dS_hf K_hf over the 64 keys of the half
-            auto issue_grad = [&](int s, int hf, bool first) {
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4)
-                    mma_ts(tmem + kColDQ, tmem + kColS + 64 * hf + 8 * k4, desc_mnmajor(stage_k(s), 4 * hf + k4),
-                           kIdescKM, (first && k4 == 0) ? 0u : 1u);
+                    mma_ss(tmem + kColDP, desc_kmajor(sO, kk), desc_kmajor(stage_v(s), kk), kIdescKK, kk > 0);
+                mma_commit(bar_s);
             };
             bool ok = mbar_wait(bar_qo, 0, &abort_flag, kWaitLimitNs) &&
                       mbar_wait(bar_full, 0, &abort_flag, kWaitLimitNs);
             if (ok) {
                 tc_fence_after();
-                issue_scores(0, 0);
-                issue_scores(0, 1);
+                issue_scores(0);
             }
             for (int j = 0; ok && j < nkt; ++j) {
-                const int s = j & 1, s1 = (j + 1) & 1;
-                const bool more = j + 1 < nkt;
-                if (!mbar_wait(bar_p, j & 1, &abort_flag, kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                issue_grad(s, 0, j == 0);
-                if (more) {
-                    if (!mbar_wait(bar_full + 8 * s1, ((j + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                const int s = j & 1;
+                if (j + 1 < nkt) {
+                    if (!mbar_wait(bar_c, j & 1, &abort_flag, kWaitLimitNs) ||
+                        !mbar_wait(bar_full + 8 * ((j + 1) & 1), ((j + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    issue_scores(s1, 0);
+                    issue_scores(j + 1);
                 }
-                if (!mbar_wait(bar_p + 8, j & 1, &abort_flag, kWaitLimitNs)) {
+                if (!mbar_wait(bar_p + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                issue_grad(s, 1, false);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + kColDQ, tmem + col_r(j) + a_col(kk), desc_mnmajor(stage_k(s), kk), kIdescKM,
+                           (j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar_empty + 8 * s);
-                if (more) issue_scores(s1, 1);
             }
             if (ok)
                 mma_commit(bar_done);
@@ -545,55 +500,70 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
         }
     } else {
         // ------------------------------------------------ elementwise warps 0-7
-        // warp w: query rows 32 * (w % 4) + lane, key half hf = w / 4
+        // warp w: query rows 32 * (w % 4) + lane, key columns [64 hf, 64 hf + 64), hf = w / 4
         const int lq = warp & 3, hf = warp >> 2;
         const uint32_t lane_addr = (uint32_t)(lq * 32) << 16;
         const int r = lq * 32 + lane;
-        const uint32_t s_cols = tmem + lane_addr + kColS + 64 * hf;
-        const uint32_t dp_cols = tmem + lane_addr + kColDP + 64 * hf;
+        const int c0 = 64 * hf;
         const size_t slot = bh * g.nq_pad + (size_t)qt * 128 + r;
         const float l2 = a.lse2_p[slot];
         const float dl = a.delta_p[slot];
         bool ok = true;
         for (int j = 0; j < nkt; ++j) {
-            if (!warp_wait(bar_s + 8 * hf, j & 1, &abort_flag)) {
+            if (!warp_wait(bar_s, j & 1, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            const uint32_t s_cols = tmem + lane_addr + col_r(j) + c0;
             uint32_t rs[2][32], rd[2][32];
             tmem_ld32(s_cols, rs[0]);
             tmem_ld32(s_cols + 32, rs[1]);
-            tmem_ld32(dp_cols, rd[0]);
-            tmem_ld32(dp_cols + 32, rd[1]);
-            const int kk0 = j < nkt_txt ? j * 128 : g.T_txt + (j - nkt_txt) * 128;
-            const int nvalid = (j < nkt_txt ? L : g.S) - kk0 - 64 * hf;  // valid columns of this half
+            tmem_ld32(tmem + lane_addr + kColDP + c0, rd[0]);
+            tmem_ld32(tmem + lane_addr + kColDP + c0 + 32, rd[1]);
             tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(bar_c);  // S_j, dP_j are in registers: the MMA may overwrite dP
+            const int kk0 = j < nkt_txt ? j * 128 : g.T_txt + (j - nkt_txt) * 128;
+            const int nvalid = (j < nkt_txt ? L : g.S) - kk0 - c0;  // valid columns of this half
             uint32_t pd[32];
+            if (nvalid >= 64) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
+                for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int col = 32 * hh + 2 * e;
-                    float p0 = exp2f(fmaf(__uint_as_float(rs[hh][2 * e]), kC, -l2));
-                    float p1 = exp2f(fmaf(__uint_as_float(rs[hh][2 * e + 1]), kC, -l2));
-                    p0 = col < nvalid ? p0 : 0.0f;
-                    p1 = col + 1 < nvalid ? p1 : 0.0f;
-                    pd[16 * hh + e] = pack_bf16(p0 * (__uint_as_float(rd[hh][2 * e]) - dl),
-                                                p1 * (__uint_as_float(rd[hh][2 * e + 1]) - dl));
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = exp2f(fmaf(__uint_as_float(rs[hh][2 * e]), kC, -l2));
+                        const float p1 = exp2f(fmaf(__uint_as_float(rs[hh][2 * e + 1]), kC, -l2));
+                        pd[16 * hh + e] = pack_bf16(p0 * (__uint_as_float(rd[hh][2 * e]) - dl),
+                                                    p1 * (__uint_as_float(rd[hh][2 * e + 1]) - dl));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int col = 32 * hh + 2 * e;
+                        float p0 = exp2f(fmaf(__uint_as_float(rs[hh][2 * e]), kC, -l2));
+                        float p1 = exp2f(fmaf(__uint_as_float(rs[hh][2 * e + 1]), kC, -l2));
+                        p0 = col < nvalid ? p0 : 0.0f;
+                        p1 = col + 1 < nvalid ? p1 : 0.0f;
+                        pd[16 * hh + e] = pack_bf16(p0 * (__uint_as_float(rd[hh][2 * e]) - dl),
+                                                    p1 * (__uint_as_float(rd[hh][2 * e + 1]) - dl));
+                    }
                 }
             }
             tmem_st32(s_cols, pd);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar_p + 8 * hf);
+            mbar_arrive(bar_p + 8 * (j & 1));
         }
         if (ok && warp_wait(bar_done, 0, &abort_flag)) {
             tc_fence_after();
             const bool row_ok = q0 + r < q_end;
             float* dqrow = a.dqh + (bh * g.S + q0 + r) * kHeadDim;
 #pragma unroll 1
-            for (int c = 64 * hf; c < 64 * hf + 64; c += 32) {
+            for (int c = c0; c < c0 + 64; c += 32) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + lane_addr + kColDQ + c, rr);
                 tmem_ld_wait();
