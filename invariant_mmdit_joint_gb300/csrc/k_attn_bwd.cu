@@ -358,14 +358,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
 // the MMA thread then computes S_{j+1} into the other R region and dP_{j+1}
 // over dP while the warps form dS_j = P (dP - Delta) and write it (bf16) over
 // S_j; then dQ += dS_j K_j. Reduction order over keys: tiles ascending.
-constexpr int kDqSmemQ = 0, kDqSmemO = kTileBytes, kDqSmemStage = 2 * kTileBytes;
-constexpr int kDqStageBytes = 2 * kTileBytes;  // K, V
-constexpr int kDqSmemBytes = kDqSmemStage + 2 * kDqStageBytes + 1024;
+// K tiles live in a three-slot ring (each is read by S_j early and by the
+// dQ product late); V tiles, read only by dP_j, in a two-slot ring released
+// as soon as dP_j is done.
+constexpr int kDqSmemQ = 0, kDqSmemO = kTileBytes, kDqSmemK = 2 * kTileBytes;  // K: 3 slots
+constexpr int kDqSmemV = 5 * kTileBytes;                                           // V: 2 slots
+constexpr int kDqSmemBytes = 7 * kTileBytes + 1024;
 constexpr uint32_t kColR0 = 0, kColR1 = 128, kColDP = 256, kColDQ = 384;
 
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[12];
+    __shared__ __align__(8) uint64_t bars[17];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
@@ -382,24 +385,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
 
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sQ = sbase + kDqSmemQ, sO = sbase + kDqSmemO;
-    auto stage_k = [&](int s) { return sbase + kDqSmemStage + s * kDqStageBytes; };
-    auto stage_v = [&](int s) { return stage_k(s) + kTileBytes; };
+    auto slot_k = [&](int j) { return sbase + kDqSmemK + (j % 3) * kTileBytes; };
+    auto slot_v = [&](int j) { return sbase + kDqSmemV + (j & 1) * kTileBytes; };
     auto col_r = [&](int j) { return (j & 1) ? kColR1 : kColR0; };
     const uint32_t bar_qo = smem_u32(&bars[0]);
-    const uint32_t bar_full = smem_u32(&bars[1]);   // [2] stages
-    const uint32_t bar_empty = smem_u32(&bars[3]);  // [2] stages
-    const uint32_t bar_s = smem_u32(&bars[5]);      // S_j, dP_j computed
-    const uint32_t bar_c = smem_u32(&bars[6]);      // S_j, dP_j read into registers
-    const uint32_t bar_p = smem_u32(&bars[7]);      // [2] by tile parity: dS_j written
-    const uint32_t bar_done = smem_u32(&bars[9]);
-    const uint32_t bar_drain = smem_u32(&bars[10]);
+    const uint32_t bar_kf = smem_u32(&bars[1]);   // [3] K slot loaded
+    const uint32_t bar_ke = smem_u32(&bars[4]);   // [3] K slot free (dQ_j done)
+    const uint32_t bar_vf = smem_u32(&bars[7]);   // [2] V slot loaded
+    const uint32_t bar_ve = smem_u32(&bars[9]);   // [2] V slot free (dP_j done)
+    const uint32_t bar_s = smem_u32(&bars[11]);   // S_j, dP_j computed
+    const uint32_t bar_c = smem_u32(&bars[12]);   // S_j, dP_j read into registers
+    const uint32_t bar_p = smem_u32(&bars[13]);   // [2] by tile parity: dS_j written
+    const uint32_t bar_done = smem_u32(&bars[15]);
+    const uint32_t bar_drain = smem_u32(&bars[16]);
 
     if (tid == 0) {
         abort_flag = 0;
         mbar_init(bar_qo, 1);
+        for (int s = 0; s < 3; ++s) {
+            mbar_init(bar_kf + 8 * s, 1);
+            mbar_init(bar_ke + 8 * s, 1);
+        }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_vf + 8 * s, 1);
+            mbar_init(bar_ve + 8 * s, 1);
             mbar_init(bar_p + 8 * s, kEwThreads);
         }
         mbar_init(bar_s, 1);
@@ -428,42 +437,53 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
             tma_load_2d(sQ + kBoxBytes, &a.map_q, bar_qo, 64, row_base + q0);
             tma_load_4d(sO, &a.map_do, bar_qo, 0, h, q0, b);
             tma_load_4d(sO + kBoxBytes, &a.map_do, bar_qo, 64, h, q0, b);
-            int issued = 0;
+            int k_issued = 0, v_issued = 0;
             for (int j = 0; j < nkt && !abort_flag; ++j) {
-                const int s = j & 1;
-                if (j >= 2 && !mbar_wait(bar_empty + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                const int kk0 = j < nkt_txt ? j * 128 : g.T_txt + (j - nkt_txt) * 128;
+                const uint32_t kf = bar_kf + 8 * (j % 3), vf = bar_vf + 8 * (j & 1);
+                if (j >= 3 && !mbar_wait(bar_ke + 8 * (j % 3), ((j / 3) + 1) & 1, &abort_flag, kWaitLimitNs)) {
                     fail(&abort_flag);
                     break;
                 }
-                const int kk0 = j < nkt_txt ? j * 128 : g.T_txt + (j - nkt_txt) * 128;
-                const uint32_t bf = bar_full + 8 * s;
-                mbar_expect_tx(bf, 2 * kTileBytes);
-                tma_load_2d(stage_k(s), &a.map_k, bf, 0, row_base + kk0);
-                tma_load_2d(stage_k(s) + kBoxBytes, &a.map_k, bf, 64, row_base + kk0);
-                tma_load_4d(stage_v(s), &a.map_v, bf, 0, h, kk0, b);
-                tma_load_4d(stage_v(s) + kBoxBytes, &a.map_v, bf, 64, h, kk0, b);
-                issued = j + 1;
+                mbar_expect_tx(kf, kTileBytes);
+                tma_load_2d(slot_k(j), &a.map_k, kf, 0, row_base + kk0);
+                tma_load_2d(slot_k(j) + kBoxBytes, &a.map_k, kf, 64, row_base + kk0);
+                k_issued = j + 1;
+                if (j >= 2 && !mbar_wait(bar_ve + 8 * (j & 1), ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                    fail(&abort_flag);
+                    break;
+                }
+                mbar_expect_tx(vf, kTileBytes);
+                tma_load_4d(slot_v(j), &a.map_v, vf, 0, h, kk0, b);
+                tma_load_4d(slot_v(j) + kBoxBytes, &a.map_v, vf, 64, h, kk0, b);
+                v_issued = j + 1;
             }
             const volatile int no_abort = 0;
             mbar_wait(bar_qo, 0, &no_abort, kWaitLimitNs);
-            for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
-                mbar_wait(bar_full + 8 * (j & 1), (j >> 1) & 1, &no_abort, kWaitLimitNs);
+            for (int j = k_issued - 3 < 0 ? 0 : k_issued - 3; j < k_issued; ++j)
+                mbar_wait(bar_kf + 8 * (j % 3), (j / 3) & 1, &no_abort, kWaitLimitNs);
+            for (int j = v_issued - 2 < 0 ? 0 : v_issued - 2; j < v_issued; ++j)
+                mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1, &no_abort, kWaitLimitNs);
         }
     } else if (warp == kWarpMma) {
         if (lane == 0) {
             // S_j = Q K_j^T into R(j), dP_j = dO V_j^T into dP
+            // needs K_j and V_j landed
             auto issue_scores = [&](int j) {
-                const int s = j & 1;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + col_r(j), desc_kmajor(sQ, kk), desc_kmajor(stage_k(s), kk), kIdescKK, kk > 0);
+                    mma_ss(tmem + col_r(j), desc_kmajor(sQ, kk), desc_kmajor(slot_k(j), kk), kIdescKK, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kColDP, desc_kmajor(sO, kk), desc_kmajor(stage_v(s), kk), kIdescKK, kk > 0);
+                    mma_ss(tmem + kColDP, desc_kmajor(sO, kk), desc_kmajor(slot_v(j), kk), kIdescKK, kk > 0);
                 mma_commit(bar_s);
+                mma_commit(bar_ve + 8 * (j & 1));
             };
-            bool ok = mbar_wait(bar_qo, 0, &abort_flag, kWaitLimitNs) &&
-                      mbar_wait(bar_full, 0, &abort_flag, kWaitLimitNs);
+            auto wait_kv = [&](int j) {
+                return mbar_wait(bar_kf + 8 * (j % 3), (j / 3) & 1, &abort_flag, kWaitLimitNs) &&
+                       mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1, &abort_flag, kWaitLimitNs);
+            };
+            bool ok = mbar_wait(bar_qo, 0, &abort_flag, kWaitLimitNs) && wait_kv(0);
             if (ok) {
                 tc_fence_after();
                 issue_scores(0);
@@ -471,8 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
             for (int j = 0; ok && j < nkt; ++j) {
                 const int s = j & 1;
                 if (j + 1 < nkt) {
-                    if (!mbar_wait(bar_c, j & 1, &abort_flag, kWaitLimitNs) ||
-                        !mbar_wait(bar_full + 8 * ((j + 1) & 1), ((j + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                    if (!mbar_wait(bar_c, j & 1, &abort_flag, kWaitLimitNs) || !wait_kv(j + 1)) {
                         ok = false;
                         break;
                     }
@@ -486,9 +505,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kColDQ, tmem + col_r(j) + a_col(kk), desc_mnmajor(stage_k(s), kk), kIdescKM,
+                    mma_ts(tmem + kColDQ, tmem + col_r(j) + a_col(kk), desc_mnmajor(slot_k(j), kk), kIdescKM,
                            (j > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar_empty + 8 * s);
+                mma_commit(bar_ke + 8 * (j % 3));
             }
             if (ok)
                 mma_commit(bar_done);

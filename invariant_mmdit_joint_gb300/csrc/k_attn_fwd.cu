@@ -86,7 +86,7 @@ __device__ __forceinline__ void fail(volatile int* abort_flag) {
 
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ FwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[13];
+    __shared__ __align__(8) uint64_t bars[15];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
@@ -107,7 +107,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
     const uint32_t bar_q = smem_u32(&bars[0]);
     const uint32_t bar_kf = smem_u32(&bars[1]);   // [2]
     const uint32_t bar_vf = smem_u32(&bars[3]);   // [2]
-    const uint32_t bar_kve = smem_u32(&bars[5]);  // [2]
+    const uint32_t bar_ke = smem_u32(&bars[5]);   // [2] K slot free (S_j done)
+    const uint32_t bar_ve = smem_u32(&bars[13]);  // [2] V slot free (PV_j done)
     const uint32_t bar_sf = smem_u32(&bars[7]);   // [2]
     const uint32_t bar_pf = smem_u32(&bars[9]);   // [2], one per S buffer
     const uint32_t bar_od = smem_u32(&bars[11]);
@@ -119,7 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar_kf + 8 * s, 1);
             mbar_init(bar_vf + 8 * s, 1);
-            mbar_init(bar_kve + 8 * s, 1);
+            mbar_init(bar_ke + 8 * s, 1);
+            mbar_init(bar_ve + 8 * s, 1);
             mbar_init(bar_sf + 8 * s, 1);
             mbar_init(bar_pf + 8 * s, 128);
         }
@@ -145,10 +147,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             mbar_expect_tx(bar_q, kTileBytes);
             tma_load_2d(sQ, &a.map_q, bar_q, 0, row_base + q0);
             tma_load_2d(sQ + kBoxBytes, &a.map_q, bar_q, 64, row_base + q0);
-            int issued = 0;
+            int k_issued = 0, v_issued = 0;
             for (int j = 0; j < nkt && !abort_flag; ++j) {
                 const int s = j & 1;
-                if (j >= 2 && !mbar_wait(bar_kve + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                // K slots free up when S_j is done, V slots when PV_j is done,
+                // so the next K tile streams in while the softmax runs
+                if (j >= 2 && !mbar_wait(bar_ke + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
                     fail(&abort_flag);
                     break;
                 }
@@ -157,19 +161,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                 mbar_expect_tx(bar_kf + 8 * s, kTileBytes);
                 tma_load_2d(dk, &a.map_k, bar_kf + 8 * s, 0, row_base + t.k0);
                 tma_load_2d(dk + kBoxBytes, &a.map_k, bar_kf + 8 * s, 64, row_base + t.k0);
+                k_issued = j + 1;
+                if (j >= 2 && !mbar_wait(bar_ve + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                    fail(&abort_flag);
+                    break;
+                }
                 mbar_expect_tx(bar_vf + 8 * s, kTileBytes);
                 tma_load_4d(dv, &a.map_v, bar_vf + 8 * s, 0, h, t.k0, b);
                 tma_load_4d(dv + kBoxBytes, &a.map_v, bar_vf + 8 * s, 64, h, t.k0, b);
-                issued = j + 1;
+                v_issued = j + 1;
             }
-            // drain: the copies of the last (up to) two tiles and of Q have landed
+            // drain: the copies of Q and of the last (up to) two K and V tiles have landed
             const volatile int no_abort = 0;
             mbar_wait(bar_q, 0, &no_abort, kWaitLimitNs);
-            for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) {
-                const int s = j & 1;
-                mbar_wait(bar_kf + 8 * s, (j >> 1) & 1, &no_abort, kWaitLimitNs);
-                mbar_wait(bar_vf + 8 * s, (j >> 1) & 1, &no_abort, kWaitLimitNs);
-            }
+            for (int j = k_issued - 2 < 0 ? 0 : k_issued - 2; j < k_issued; ++j)
+                mbar_wait(bar_kf + 8 * (j & 1), (j >> 1) & 1, &no_abort, kWaitLimitNs);
+            for (int j = v_issued - 2 < 0 ? 0 : v_issued - 2; j < v_issued; ++j)
+                mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1, &no_abort, kWaitLimitNs);
         }
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer
@@ -187,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                            kk > 0);
                 }
                 mma_commit(bar_sf + 8 * s);
+                mma_commit(bar_ke + 8 * s);
             };
             bool ok = mbar_wait(bar_q, 0, &abort_flag, kWaitLimitNs) &&
                       mbar_wait(bar_kf, 0, &abort_flag, kWaitLimitNs);
@@ -218,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                     mma_ts(tmem + kColO, p_tmem + kk * 8, sdesc_sw128(dv + kk * 2048, kBoxBytes, 1024), idesc_o,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar_od);
-                mma_commit(bar_kve + 8 * s);
+                mma_commit(bar_ve + 8 * s);
             }
             if (!ok) fail(&abort_flag);
             // drain every MMA this thread issued before TMEM is released
