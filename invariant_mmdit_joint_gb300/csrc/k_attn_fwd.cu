@@ -3,19 +3,22 @@
 // RFC #386 WS1 table fused ("joint_attention_fused"), with an online
 // softmax over key tiles.
 //
-// One CTA = one (query tile of 128 rows, head, sample); 6 warps:
-//   warps 0-3  softmax: thread t owns query row t = TMEM lane t. Per key
-//              tile it reads S from TMEM, masks, keeps the running max m
-//              and sum l (FP32, log2 units), rescales O in TMEM when m grows,
-//              and writes P = exp2(s - m) as bf16 back into TMEM over S.
-//              Epilogue: O / l, one bf16 cast, and lse.
-//   warp 4     TMA producer: Q once, then K and V tiles (two stages).
-//   warp 5     MMA issuer (one thread) and TMEM owner:
-//              S_j = Q K_j^T  (A, B from shared memory, K-major),
-//              O  += P_j V_j  (A = P from tensor memory, B = V MN-major).
-// TMEM: S_0 cols [0,128), S_1 [128,256), O [256,384); P_j overwrites the
-// first 64 columns of S_j. S_{j+1} is computed while the softmax works on
-// S_j. Query tiles are segment aligned (text from token 0, image from token
+// One CTA = two query tiles A and B of 128 rows (the same head, sample and
+// stream segment) sharing every K/V tile; 10 warps:
+//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread t of a
+//              group owns query row t = TMEM lane t. Per key tile it reads
+//              S from TMEM (once for the row max, once for the exponentials),
+//              keeps the running max m and sum l (FP32, log2 units), rescales
+//              O in TMEM when m grows, and writes P = exp2(s - m) as bf16
+//              back over S. Epilogue: O / l, one bf16 cast, and lse.
+//   warp 8     TMA producer: Q tiles once, then K and V tiles (two slots
+//              each; a K slot frees when its S products are done, a V slot
+//              when its PV products are done).
+//   warp 9     MMA issuer (one thread) and TMEM owner, per key tile j:
+//              PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) -- while one group runs
+//              its softmax the tensor core works for the other.
+// TMEM: S_A [0,128), O_A [128,256), S_B [256,384), O_B [384,512).
+// Query tiles are segment aligned (text from token 0, image from token
 // T_txt); key tiles of 128 are visited in one fixed order (text tiles that
 // hold a valid key, then image tiles), so a row's bytes never depend on B,
 // its batch position, padding or the SM count. No split-KV, no atomics.
@@ -39,15 +42,15 @@ namespace {
 using namespace sm100;
 
 constexpr int kBM = 128, kBN = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr int kBoxBytes = 128 * 128;          // 128 rows x 64 bf16
 constexpr int kTileBytes = 2 * kBoxBytes;     // 128 rows x 128 bf16
-constexpr int kSmemQ = 0;
-constexpr int kSmemK = kTileBytes;            // 2 stages
-constexpr int kSmemV = 3 * kTileBytes;        // 2 stages
-constexpr int kSmemBytes = 5 * kTileBytes + 1024;  // + alignment slack
+constexpr int kSmemQ = 0;                     // Q_A, Q_B
+constexpr int kSmemK = 2 * kTileBytes;        // 2 slots
+constexpr int kSmemV = 4 * kTileBytes;        // 2 slots
+constexpr int kSmemBytes = 6 * kTileBytes + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kC = (float)(1.4426950408889634 * 0.08838834764831845);  // log2(e) / sqrt(128)
 constexpr float kLn2 = 0.6931471805599453f;
@@ -84,35 +87,44 @@ __device__ __forceinline__ void fail(volatile int* abort_flag) {
     atomicOr(&g_status_fwd, 1);
 }
 
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitLimitNs));
+}
+
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ FwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[15];
+    __shared__ __align__(8) uint64_t bars[16];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
     const Geom& g = a.g;
-    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int pt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nqt_txt = (g.T_txt + kBM - 1) / kBM;
-    const bool q_txt = qt < nqt_txt;
-    const int q0 = q_txt ? qt * kBM : g.T_txt + (qt - nqt_txt) * kBM;
+    // the CTA's pair of query tiles, inside one segment
+    const int np_txt = (g.ntq_txt + 1) / 2;
+    const bool q_txt = pt < np_txt;
+    const int first = q_txt ? 2 * pt : 2 * (pt - np_txt);          // tile index inside the segment
+    const int seg_tiles = q_txt ? g.ntq_txt : g.ntq_img;
+    const bool has_b = first + 1 < seg_tiles;
+    const int seg0 = q_txt ? 0 : g.T_txt;
     const int q_end = q_txt ? g.T_txt : g.S;
+    const int q0[2] = {seg0 + first * kBM, seg0 + (first + 1) * kBM};
     const int L = a.vl.L[b];
     const int nkt_txt = (L + kBN - 1) / kBN;
-    const int nkt = nkt_txt + (g.T_img + kBN - 1) / kBN;
+    const int nkt = nkt_txt + g.ntq_img;
     const int row_base = (b * g.H + h) * g.S;  // first row of this (b, h) in qh / kh
 
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sQ = sbase + kSmemQ, sK = sbase + kSmemK, sV = sbase + kSmemV;
     const uint32_t bar_q = smem_u32(&bars[0]);
-    const uint32_t bar_kf = smem_u32(&bars[1]);   // [2]
-    const uint32_t bar_vf = smem_u32(&bars[3]);   // [2]
-    const uint32_t bar_ke = smem_u32(&bars[5]);   // [2] K slot free (S_j done)
-    const uint32_t bar_ve = smem_u32(&bars[13]);  // [2] V slot free (PV_j done)
-    const uint32_t bar_sf = smem_u32(&bars[7]);   // [2]
-    const uint32_t bar_pf = smem_u32(&bars[9]);   // [2], one per S buffer
-    const uint32_t bar_od = smem_u32(&bars[11]);
-    const uint32_t bar_drain = smem_u32(&bars[12]);
+    const uint32_t bar_kf = smem_u32(&bars[1]);   // [2] K slot loaded
+    const uint32_t bar_vf = smem_u32(&bars[3]);   // [2] V slot loaded
+    const uint32_t bar_ke = smem_u32(&bars[5]);   // [2] K slot free (S_A, S_B done)
+    const uint32_t bar_ve = smem_u32(&bars[7]);   // [2] V slot free (PV_A, PV_B done)
+    const uint32_t bar_s = smem_u32(&bars[9]);    // [2] per Q tile: S ready
+    const uint32_t bar_p = smem_u32(&bars[11]);   // [2] per Q tile: P written
+    const uint32_t bar_o = smem_u32(&bars[13]);   // [2] per Q tile: PV done
+    const uint32_t bar_drain = smem_u32(&bars[15]);
 
     if (tid == 0) {
         abort_flag = 0;
@@ -122,14 +134,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             mbar_init(bar_vf + 8 * s, 1);
             mbar_init(bar_ke + 8 * s, 1);
             mbar_init(bar_ve + 8 * s, 1);
-            mbar_init(bar_sf + 8 * s, 1);
-            mbar_init(bar_pf + 8 * s, 128);
+            mbar_init(bar_s + 8 * s, 1);
+            mbar_init(bar_p + 8 * s, 128);
+            mbar_init(bar_o + 8 * s, 1);
         }
-        mbar_init(bar_od, 1);
         mbar_init(bar_drain, 1);
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -138,37 +150,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
-    if (warp == 4) {
+    if (warp == kWarpTma) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tensormap(&a.map_q);
             prefetch_tensormap(&a.map_k);
             prefetch_tensormap(&a.map_v);
-            mbar_expect_tx(bar_q, kTileBytes);
-            tma_load_2d(sQ, &a.map_q, bar_q, 0, row_base + q0);
-            tma_load_2d(sQ + kBoxBytes, &a.map_q, bar_q, 64, row_base + q0);
+            mbar_expect_tx(bar_q, (has_b ? 2 : 1) * kTileBytes);
+            for (int t = 0; t < (has_b ? 2 : 1); ++t) {
+                tma_load_2d(sQ + t * kTileBytes, &a.map_q, bar_q, 0, row_base + q0[t]);
+                tma_load_2d(sQ + t * kTileBytes + kBoxBytes, &a.map_q, bar_q, 64, row_base + q0[t]);
+            }
             int k_issued = 0, v_issued = 0;
             for (int j = 0; j < nkt && !abort_flag; ++j) {
                 const int s = j & 1;
-                // K slots free up when S_j is done, V slots when PV_j is done,
-                // so the next K tile streams in while the softmax runs
                 if (j >= 2 && !mbar_wait(bar_ke + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
                     fail(&abort_flag);
                     break;
                 }
-                const TileInfo t = kv_tile(g, L, nkt_txt, j);
+                const TileInfo ti = kv_tile(g, L, nkt_txt, j);
                 const uint32_t dk = sK + s * kTileBytes, dv = sV + s * kTileBytes;
                 mbar_expect_tx(bar_kf + 8 * s, kTileBytes);
-                tma_load_2d(dk, &a.map_k, bar_kf + 8 * s, 0, row_base + t.k0);
-                tma_load_2d(dk + kBoxBytes, &a.map_k, bar_kf + 8 * s, 64, row_base + t.k0);
+                tma_load_2d(dk, &a.map_k, bar_kf + 8 * s, 0, row_base + ti.k0);
+                tma_load_2d(dk + kBoxBytes, &a.map_k, bar_kf + 8 * s, 64, row_base + ti.k0);
                 k_issued = j + 1;
                 if (j >= 2 && !mbar_wait(bar_ve + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
                     fail(&abort_flag);
                     break;
                 }
                 mbar_expect_tx(bar_vf + 8 * s, kTileBytes);
-                tma_load_4d(dv, &a.map_v, bar_vf + 8 * s, 0, h, t.k0, b);
-                tma_load_4d(dv + kBoxBytes, &a.map_v, bar_vf + 8 * s, 64, h, t.k0, b);
+                tma_load_4d(dv, &a.map_v, bar_vf + 8 * s, 0, h, ti.k0, b);
+                tma_load_4d(dv + kBoxBytes, &a.map_v, bar_vf + 8 * s, 64, h, ti.k0, b);
                 v_issued = j + 1;
             }
             // drain: the copies of Q and of the last (up to) two K and V tiles have landed
@@ -179,55 +191,71 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             for (int j = v_issued - 2 < 0 ? 0 : v_issued - 2; j < v_issued; ++j)
                 mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1, &no_abort, kWaitLimitNs);
         }
-    } else if (warp == 5) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
             constexpr uint32_t idesc_o = idesc_bf16(128, 128, false, true);
-            auto issue_s = [&](int j) {
-                const int s = j & 1;
-                const uint32_t dk = sK + s * kTileBytes;
-                const uint32_t d_tmem = tmem + (s ? kColS1 : kColS0);
+            // S_t = Q_t K_j^T into TMEM [256 t, 256 t + 128)
+            auto issue_s = [&](int t, int j) {
+                const uint32_t dk = sK + (j & 1) * kTileBytes;
+                const uint32_t qt = sQ + t * kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                    mma_ss(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(dk + off, 16, 1024), idesc_s,
+                    mma_ss(tmem + 256 * t, sdesc_sw128(qt + off, 16, 1024), sdesc_sw128(dk + off, 16, 1024), idesc_s,
                            kk > 0);
                 }
-                mma_commit(bar_sf + 8 * s);
-                mma_commit(bar_ke + 8 * s);
+                mma_commit(bar_s + 8 * t);
+            };
+            // O_t += P_t V_j, P_t read from TMEM over S_t
+            auto issue_pv = [&](int t, int j) {
+                const uint32_t dv = sV + (j & 1) * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + 256 * t + 128, tmem + 256 * t + kk * 8, sdesc_sw128(dv + kk * 2048, kBoxBytes, 1024),
+                           idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar_o + 8 * t);
             };
             bool ok = mbar_wait(bar_q, 0, &abort_flag, kWaitLimitNs) &&
                       mbar_wait(bar_kf, 0, &abort_flag, kWaitLimitNs);
             if (ok) {
                 tc_fence_after();
-                issue_s(0);
+                issue_s(0, 0);
+                if (has_b) issue_s(1, 0);
+                mma_commit(bar_ke);
             }
             for (int j = 0; ok && j < nkt; ++j) {
-                const int s = j & 1;
-                if (j + 1 < nkt) {
-                    const int s1 = (j + 1) & 1;
-                    if (!mbar_wait(bar_kf + 8 * s1, ((j + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_s(j + 1);
-                }
-                if (!mbar_wait(bar_pf + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs) ||
+                const int s = j & 1, s1 = (j + 1) & 1;
+                const bool more = j + 1 < nkt;
+                if (!mbar_wait(bar_p, j & 1, &abort_flag, kWaitLimitNs) ||
                     !mbar_wait(bar_vf + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t p_tmem = tmem + (s ? kColS1 : kColS0);
-                const uint32_t dv = sV + s * kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kColO, p_tmem + kk * 8, sdesc_sw128(dv + kk * 2048, kBoxBytes, 1024), idesc_o,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar_od);
+                issue_pv(0, j);
+                if (more) {
+                    if (!mbar_wait(bar_kf + 8 * s1, ((j + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_s(0, j + 1);
+                }
+                if (has_b) {
+                    if (!mbar_wait(bar_p + 8, j & 1, &abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv(1, j);
+                }
                 mma_commit(bar_ve + 8 * s);
+                if (more) {
+                    if (has_b) issue_s(1, j + 1);
+                    mma_commit(bar_ke + 8 * s1);
+                }
             }
             if (!ok) fail(&abort_flag);
             // drain every MMA this thread issued before TMEM is released
@@ -235,50 +263,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             const volatile int no_abort = 0;
             mbar_wait(bar_drain, 0, &no_abort, kWaitLimitNs);
         }
-    } else {
-        // ------------------------------------------------ softmax warps 0-3
+    } else if (warp < 4 || has_b) {
+        // ------------------------------------------------ softmax warps (tile t = warp / 4)
         // Barrier phases are consumed strictly in order (S_j, then PV_{j-1}
         // once per tile), so no waiter ever falls two phases behind.
-        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-        const uint32_t o_tmem = tmem + lane_addr + kColO;
-        const int row = tid;
+        const int t = warp >> 2;
+        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t s_tmem = tmem + lane_addr + 256 * t;
+        const uint32_t o_tmem = s_tmem + 128;
+        const int row = (warp & 3) * 32 + lane;
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
         for (int j = 0; j < nkt; ++j) {
-            const int s = j & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar_sf + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs))) {
+            if (!warp_wait(bar_s + 8 * t, j & 1, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t s_tmem = tmem + lane_addr + (s ? kColS1 : kColS0);
-            uint32_t xr[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + 32 * c, xr[c]);
-            tmem_ld_wait();
-            float x[128];
-#pragma unroll
-            for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(xr[c >> 5][c & 31]);
-            const TileInfo t = kv_tile(g, L, nkt_txt, j);
-            const int nvalid = t.kend - t.k0;  // keys k0 + c with c < nvalid are valid
-            if (nvalid < 128) {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) x[c] = c < nvalid ? x[c] : -INFINITY;
-            }
-            // row max of the raw scores: eight interleaved partial maxima,
-            // then a fixed tree (max is exact in any order)
+            const TileInfo ti = kv_tile(g, L, nkt_txt, j);
+            const int nvalid = ti.kend - ti.k0;  // keys k0 + c with c < nvalid are valid
+            // pass 1: the row max of the raw scores (eight interleaved partial
+            // maxima, then a fixed tree; max is exact in any order)
             float mp[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mp[i] = x[i];
+            for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld32(s_tmem + 32 * c, r);
+                tmem_ld_wait();
 #pragma unroll
-            for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
+                for (int i = 0; i < 32; ++i) {
+                    const float x = (32 * c + i < nvalid) ? __uint_as_float(r[i]) : -INFINITY;
+                    mp[i & 7] = fmaxf(mp[i & 7], x);
+                }
+            }
             const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                    fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
             const float m_new = fmaxf(m, mx * kC);  // running max in log2 units
             const float alpha = exp2f(m - m_new);
             if (j > 0) {
                 // PV_{j-1} has finished writing O
-                if (!__all_sync(0xffffffffu, mbar_wait(bar_od, (j - 1) & 1, &abort_flag, kWaitLimitNs))) {
+                if (!warp_wait(bar_o + 8 * t, (j - 1) & 1, &abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -286,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                 // rescale O when a row's max grew; the decision is warp-wide
                 // and rows whose max did not grow scale by exactly 1
                 if (__any_sync(0xffffffffu, m_new > m)) {
-#pragma unroll
+#pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         uint32_t r[32];
                         tmem_ld32(o_tmem + 32 * c, r);
@@ -298,34 +324,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                     tmem_st_wait();
                 }
             }
-            // p = exp2(s * c - m); the row sum adds column c into partial
-            // c % 8, and the eight partials in a fixed tree
+            // pass 2: p = exp2(s * c - m), packed to bf16 over the first 64
+            // columns of S (chunk c lands on columns already read); the row
+            // sum adds column i of a chunk into partial i % 8, partials in a
+            // fixed tree
             float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            uint32_t pa[32], pb[32];
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld32(s_tmem + 32 * c, r);
+                tmem_ld_wait();
+                uint32_t pk[16];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float p0 = exp2f(fmaf(x[2 * c], kC, -m_new));
-                const float p1 = exp2f(fmaf(x[2 * c + 1], kC, -m_new));
-                sp[(2 * c) & 7] += p0;
-                sp[(2 * c + 1) & 7] += p1;
-                if (c < 32) pa[c] = pack_bf16(p0, p1);
-                else pb[c - 32] = pack_bf16(p0, p1);
+                for (int i = 0; i < 16; ++i) {
+                    const float x0 = (32 * c + 2 * i < nvalid) ? __uint_as_float(r[2 * i]) : -INFINITY;
+                    const float x1 = (32 * c + 2 * i + 1 < nvalid) ? __uint_as_float(r[2 * i + 1]) : -INFINITY;
+                    const float p0 = exp2f(fmaf(x0, kC, -m_new));
+                    const float p1 = exp2f(fmaf(x1, kC, -m_new));
+                    sp[(2 * i) & 7] += p0;
+                    sp[(2 * i + 1) & 7] += p1;
+                    pk[i] = pack_bf16(p0, p1);
+                }
+                tmem_st16(s_tmem + 16 * c, pk);
             }
             const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
             l = l * alpha + rs;
             m = m_new;
-            tmem_st32(s_tmem, pa);
-            tmem_st32(s_tmem + 32, pb);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar_pf + 8 * s);
+            mbar_arrive(bar_p + 8 * t);
         }
-        if (ok && __all_sync(0xffffffffu, mbar_wait(bar_od, (nkt - 1) & 1, &abort_flag, kWaitLimitNs))) {
+        if (ok && warp_wait(bar_o + 8 * t, (nkt - 1) & 1, &abort_flag)) {
             tc_fence_after();
             const float inv = 1.0f / l;
-            const bool row_ok = q0 + row < q_end;
-            uint16_t* orow = a.out + (((size_t)b * g.S + q0 + row) * g.H + h) * kHeadDim;
-#pragma unroll
+            const int n = q0[t] + row;
+            const bool row_ok = n < q_end;
+            uint16_t* orow = a.out + (((size_t)b * g.S + n) * g.H + h) * kHeadDim;
+#pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t r[32];
                 tmem_ld32(o_tmem + 32 * c, r);
@@ -342,8 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                     dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
                 }
             }
-            if (row_ok && a.lse != nullptr)
-                a.lse[((size_t)b * g.H + h) * g.S + q0 + row] = (m + log2f(l)) * kLn2;
+            if (row_ok && a.lse != nullptr) a.lse[((size_t)b * g.H + h) * g.S + n] = (m + log2f(l)) * kLn2;
         } else {
             fail(&abort_flag);
         }
@@ -351,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -410,8 +444,8 @@ cudaError_t launch_attn_fwd(const Geom& g, const ValidLen& vl, const uint16_t* q
     local.lse = lse;
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int nqt = (g.T_txt + kBM - 1) / kBM + (g.T_img + kBM - 1) / kBM;
-    dim3 grid(nqt, g.H, g.B);
+    const int npairs = (g.ntq_txt + 1) / 2 + (g.ntq_img + 1) / 2;
+    dim3 grid(npairs, g.H, g.B);
     timing_begin(kKAttnFwd, s);
     attn_fwd_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(local);
     timing_end(kKAttnFwd, s);
