@@ -7,8 +7,8 @@
 // stream segment) sharing every K/V tile; 10 warps:
 //   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread t of a
 //              group owns query row t = TMEM lane t. Per key tile it reads
-//              S from TMEM (once for the row max, once for the exponentials),
-//              keeps the running max m and sum l (FP32, log2 units), rescales
+//              the row of S from TMEM into registers, keeps the running max m
+//              and sum l (FP32, log2 units), rescales
 //              O in TMEM when m grows, and writes P = exp2(s - m) as bf16
 //              back over S. Epilogue: O / l, one bf16 cast, and lse.
 //   warp 8     TMA producer: Q tiles once, then K and V tiles (two slots
@@ -282,22 +282,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             tc_fence_after();
             const TileInfo ti = kv_tile(g, L, nkt_txt, j);
             const int nvalid = ti.kend - ti.k0;  // keys k0 + c with c < nvalid are valid
-            // pass 1: the row max of the raw scores (eight interleaved partial
-            // maxima, then a fixed tree; max is exact in any order)
+            // the row's 128 scores in one register array, loaded at once;
+            // the packed P later reuses its first 64 entries in place
+            uint32_t r[128];
+            tmem_ld32(s_tmem, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+            tmem_ld32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+            tmem_ld32(s_tmem + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
+            tmem_ld32(s_tmem + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+            tmem_ld_wait();
+            if (nvalid < 128) {
+#pragma unroll
+                for (int i = 0; i < 128; ++i) r[i] = i < nvalid ? r[i] : 0xff800000u;  // -inf
+            }
+            // row max of the raw scores: eight interleaved partial maxima,
+            // then a fixed tree (max is exact in any order)
             float mp[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(s_tmem + 32 * c, r);
-                tmem_ld_wait();
+            for (int i = 0; i < 8; ++i) mp[i] = __uint_as_float(r[i]);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float x = (32 * c + i < nvalid) ? __uint_as_float(r[i]) : -INFINITY;
-                    mp[i & 7] = fmaxf(mp[i & 7], x);
-                }
-            }
+            for (int i = 8; i < 128; ++i) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(r[i]));
             const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                    fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
             const float m_new = fmaxf(m, mx * kC);  // running max in log2 units
@@ -324,29 +327,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                     tmem_st_wait();
                 }
             }
-            // pass 2: p = exp2(s * c - m), packed to bf16 over the first 64
-            // columns of S (chunk c lands on columns already read); the row
-            // sum adds column i of a chunk into partial i % 8, partials in a
-            // fixed tree
+            // p = exp2(s * c - m), packed to bf16 into r[0..63] (pair i lands
+            // on an entry already read) and stored over the first 64 columns
+            // of S; the row sum adds column i into partial i % 8, partials in
+            // a fixed tree
             float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(s_tmem + 32 * c, r);
-                tmem_ld_wait();
-                uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float x0 = (32 * c + 2 * i < nvalid) ? __uint_as_float(r[2 * i]) : -INFINITY;
-                    const float x1 = (32 * c + 2 * i + 1 < nvalid) ? __uint_as_float(r[2 * i + 1]) : -INFINITY;
-                    const float p0 = exp2f(fmaf(x0, kC, -m_new));
-                    const float p1 = exp2f(fmaf(x1, kC, -m_new));
-                    sp[(2 * i) & 7] += p0;
-                    sp[(2 * i + 1) & 7] += p1;
-                    pk[i] = pack_bf16(p0, p1);
-                }
-                tmem_st16(s_tmem + 16 * c, pk);
+            for (int i = 0; i < 64; ++i) {
+                const float p0 = exp2f(fmaf(__uint_as_float(r[2 * i]), kC, -m_new));
+                const float p1 = exp2f(fmaf(__uint_as_float(r[2 * i + 1]), kC, -m_new));
+                sp[(2 * i) & 7] += p0;
+                sp[(2 * i + 1) & 7] += p1;
+                r[i] = pack_bf16(p0, p1);
             }
+            tmem_st32(s_tmem, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+            tmem_st32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
             const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
             l = l * alpha + rs;
             m = m_new;
