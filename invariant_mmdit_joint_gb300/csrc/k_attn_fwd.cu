@@ -7,10 +7,10 @@
 // stream segment) sharing every K/V tile; 10 warps:
 //   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread t of a
 //              group owns query row t = TMEM lane t. Per key tile it reads
-//              the row of S from TMEM into registers, keeps the running max m
-//              and sum l (FP32, log2 units), rescales
-//              O in TMEM when m grows, and writes P = exp2(s - m) as bf16
-//              back over S. Epilogue: O / l, one bf16 cast, and lse.
+//              the row of S from TMEM into registers, keeps a reference max m
+//              and the sum l (FP32, log2 units), writes P = exp2(s - m) as
+//              bf16 back over S and rescales O in TMEM when m moves (only
+//              when the row max has grown by more than 2^8). Epilogue: O / l, one bf16 cast, and lse.
 //   warp 8     TMA producer: Q tiles once, then K and V tiles (two slots
 //              each; a K slot frees when its S products are done, a V slot
 //              when its PV products are done).
@@ -303,34 +303,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             for (int i = 8; i < 128; ++i) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(r[i]));
             const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                    fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-            const float m_new = fmaxf(m, mx * kC);  // running max in log2 units
-            const float alpha = exp2f(m - m_new);
-            if (j > 0) {
-                // PV_{j-1} has finished writing O
-                if (!warp_wait(bar_o + 8 * t, (j - 1) & 1, &abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // rescale O when a row's max grew; the decision is warp-wide
-                // and rows whose max did not grow scale by exactly 1
-                if (__any_sync(0xffffffffu, m_new > m)) {
-#pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(o_tmem + 32 * c, r);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(o_tmem + 32 * c, r);
-                    }
-                    tmem_st_wait();
-                }
-            }
+            // Lazy rescaling: a row moves its reference max m only when the
+            // new max exceeds it by more than 8 (a factor 256), so rows
+            // rarely touch O; until then p = exp2(s c - m) <= 256, exact in
+            // the fp32 sums and within bf16 range. The decision depends only
+            // on the row's own scores, and O / l is the same softmax.
+            const float m_cand = fmaxf(m, mx * kC);  // log2 units
+            const bool move = m_cand > m + 8.0f;      // always true on the first tile
+            const float m_new = move ? m_cand : m;
+            const float alpha = move ? exp2f(m - m_new) : 1.0f;
             // p = exp2(s * c - m), packed to bf16 into r[0..63] (pair i lands
-            // on an entry already read) and stored over the first 64 columns
-            // of S; the row sum adds column i into partial i % 8, partials in
-            // a fixed tree
+            // on an entry already read); the row sum adds column i into
+            // partial i % 8, partials in a fixed tree
             float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
@@ -340,11 +324,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                 sp[(2 * i + 1) & 7] += p1;
                 r[i] = pack_bf16(p0, p1);
             }
-            tmem_st32(s_tmem, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-            tmem_st32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
             const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
             l = l * alpha + rs;
             m = m_new;
+            tmem_st32(s_tmem, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+            tmem_st32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+            if (j > 0) {
+                // PV_{j-1} has finished writing O
+                if (!warp_wait(bar_o + 8 * t, (j - 1) & 1, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // rescale O in the rows that moved their max; the decision is
+                // warp-wide and the other rows scale by exactly 1
+                if (__any_sync(0xffffffffu, move)) {
+                    uint32_t (&o32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[64]);
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        tmem_ld32(o_tmem + 32 * c, o32);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
+                        tmem_st32(o_tmem + 32 * c, o32);
+                    }
+                }
+            }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_p + 8 * t);
