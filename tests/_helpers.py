@@ -57,6 +57,11 @@ def oracle_inputs(batch: dict):
 
 def assert_forward_close(out, lse, ref_o, ref_lse, where="", scale=1.0, lse_abs=None):
     err = np.abs(out - ref_o)
+    if lse_abs is not None:
+        # against exact float64 the bf16 rounding of the stored q and k adds
+        # to the output rounding; with few keys |O| is large and the bf16
+        # output rounding alone reaches ~1e-3 mean: the bound doubles
+        scale = 2.0 * scale
     assert err.max() <= FWD_MAX_ABS * scale, (where, "O max abs", err.max())
     assert err.mean() <= FWD_MEAN_ABS * scale, (where, "O mean abs", err.mean())
     if lse_abs is None:
