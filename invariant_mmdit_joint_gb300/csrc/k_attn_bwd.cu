@@ -4,7 +4,8 @@
 //
 //   dkdv: one CTA = (key tile of 128, head, sample). Walks every query tile
 //         of 128 in one fixed ascending order (text tiles from token 0, then
-//         image tiles from token T_txt). Per query tile:
+//         image tiles from token T_txt). Per query tile (P^T is formed while
+//         dP^T computes, dS^T while dV computes):
 //           S^T  = K Q^T, dP^T = V dO^T            (tcgen05, A and B in smem)
 //           P^T  = exp2(S^T * c - lse2), dS^T = P^T * (dP^T - Delta)
 //                                                  (4 warps, one key row each;
@@ -107,7 +108,7 @@ constexpr uint32_t kColDV = 0, kColDK = 128, kColST = 256, kColDPT = 384;
 
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[10];
+    __shared__ __align__(8) uint64_t bars[12];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
@@ -145,8 +146,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
     const uint32_t bar_kv = smem_u32(&bars[0]);
     const uint32_t bar_full = smem_u32(&bars[1]);   // [2]
     const uint32_t bar_empty = smem_u32(&bars[3]);  // [2]
-    const uint32_t bar_s = smem_u32(&bars[5]);
-    const uint32_t bar_p = smem_u32(&bars[6]);
+    const uint32_t bar_st = smem_u32(&bars[5]);   // S^T_i computed
+    const uint32_t bar_dpt = smem_u32(&bars[6]);  // dP^T_i computed
+    const uint32_t bar_p = smem_u32(&bars[10]);   // P^T_i written (bf16)
+    const uint32_t bar_ds = smem_u32(&bars[11]);  // dS^T_i written (bf16)
     const uint32_t bar_done = smem_u32(&bars[7]);
     const uint32_t bar_drain = smem_u32(&bars[8]);
 
@@ -157,8 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
-        mbar_init(bar_s, 1);
+        mbar_init(bar_st, 1);
+        mbar_init(bar_dpt, 1);
         mbar_init(bar_p, kEwThreads);
+        mbar_init(bar_ds, kEwThreads);
         mbar_init(bar_done, 1);
         mbar_init(bar_drain, 1);
         fence_barrier_init();
@@ -223,10 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ss(tmem + kColST, desc_kmajor(sK, kk), desc_kmajor(stage_q(s), kk), kIdescKK, kk > 0);
+                mma_commit(bar_st);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ss(tmem + kColDPT, desc_kmajor(sV, kk), desc_kmajor(stage_o(s), kk), kIdescKK, kk > 0);
-                mma_commit(bar_s);
+                mma_commit(bar_dpt);
+                // dV needs only P (the warps form it while dP^T computes);
+                // dK needs dS (formed while dV computes)
                 if (!mbar_wait(bar_p, i & 1, &abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
@@ -236,6 +244,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tmem + kColDV, tmem + kColST + a_col(kk), desc_mnmajor(stage_o(s), kk), kIdescKM,
                            (i > 0 || kk > 0) ? 1u : 0u);
+                if (!mbar_wait(bar_ds, i & 1, &abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tmem + kColDK, tmem + kColDPT + a_col(kk), desc_mnmajor(stage_q(s), kk), kIdescKM,
@@ -261,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
         bool ok = true;
         for (int i = 0; i < nq; ++i) {
             const int s = i & 1;
-            if (!warp_wait(bar_full + 8 * s, (i >> 1) & 1, &abort_flag) || !warp_wait(bar_s, i & 1, &abort_flag)) {
+            if (!warp_wait(bar_full + 8 * s, (i >> 1) & 1, &abort_flag) || !warp_wait(bar_st, i & 1, &abort_flag)) {
                 ok = false;
                 break;
             }
@@ -269,39 +282,53 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
             const float4* l2v =
                 reinterpret_cast<const float4*>(smem_raw + (stage_l(s) - smem_u32(smem_raw))) + c0 / 4;
             const float4* dlv = l2v + 32;
-            uint32_t rs[2][32], rd[2][32];
-            tmem_ld32(tmem + lane_addr + kColST + c0, rs[0]);
-            tmem_ld32(tmem + lane_addr + kColST + c0 + 32, rs[1]);
-            tmem_ld32(tmem + lane_addr + kColDPT + c0, rd[0]);
-            tmem_ld32(tmem + lane_addr + kColDPT + c0 + 32, rd[1]);
+            // P^T = exp2(S^T * c - lse2[query]) (masked keys: 0), kept in fp32 for dS
+            uint32_t rs[64];
+            tmem_ld32(tmem + lane_addr + kColST + c0, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
+            tmem_ld32(tmem + lane_addr + kColST + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
             tmem_ld_wait();
-            uint32_t pp[32], pd[32];
+            float pf[64];
+            uint32_t pk[32];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
+            for (int e4 = 0; e4 < 16; ++e4) {
+                const float4 l4 = l2v[e4];
+                const float lq4[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4) {
-                    const float4 l4 = l2v[8 * hh + e4];
-                    const float4 d4 = dlv[8 * hh + e4];
-                    const float lq4[4] = {l4.x, l4.y, l4.z, l4.w};
-                    const float dq4[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float p[4], ds[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float pv = exp2f(fmaf(__uint_as_float(rs[hh][4 * e4 + u]), kC, -lq4[u]));
-                        p[u] = kvalid ? pv : 0.0f;
-                        ds[u] = p[u] * (__uint_as_float(rd[hh][4 * e4 + u]) - dq4[u]);
-                    }
-                    pp[16 * hh + 2 * e4] = pack_bf16(p[0], p[1]);
-                    pp[16 * hh + 2 * e4 + 1] = pack_bf16(p[2], p[3]);
-                    pd[16 * hh + 2 * e4] = pack_bf16(ds[0], ds[1]);
-                    pd[16 * hh + 2 * e4 + 1] = pack_bf16(ds[2], ds[3]);
+                for (int u = 0; u < 4; ++u) {
+                    const float pv = exp2f(fmaf(__uint_as_float(rs[4 * e4 + u]), kC, -lq4[u]));
+                    pf[4 * e4 + u] = kvalid ? pv : 0.0f;
                 }
+                pk[2 * e4] = pack_bf16(pf[4 * e4], pf[4 * e4 + 1]);
+                pk[2 * e4 + 1] = pack_bf16(pf[4 * e4 + 2], pf[4 * e4 + 3]);
             }
-            tmem_st32(tmem + lane_addr + kColST + c0, pp);
-            tmem_st32(tmem + lane_addr + kColDPT + c0, pd);
+            tmem_st32(tmem + lane_addr + kColST + c0, pk);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_p);
+            // dS^T = P^T * (dP^T - Delta[query])
+            if (!warp_wait(bar_dpt, i & 1, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t rd[64];
+            tmem_ld32(tmem + lane_addr + kColDPT + c0, *reinterpret_cast<uint32_t(*)[32]>(&rd[0]));
+            tmem_ld32(tmem + lane_addr + kColDPT + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rd[32]));
+            tmem_ld_wait();
+#pragma unroll
+            for (int e4 = 0; e4 < 16; ++e4) {
+                const float4 d4 = dlv[e4];
+                const float dq4[4] = {d4.x, d4.y, d4.z, d4.w};
+                float ds[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) ds[u] = pf[4 * e4 + u] * (__uint_as_float(rd[4 * e4 + u]) - dq4[u]);
+                pk[2 * e4] = pack_bf16(ds[0], ds[1]);
+                pk[2 * e4 + 1] = pack_bf16(ds[2], ds[3]);
+            }
+            tmem_st32(tmem + lane_addr + kColDPT + c0, pk);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar_ds);
         }
         if (ok && warp_wait(bar_done, 0, &abort_flag)) {
             tc_fence_after();
@@ -368,7 +395,7 @@ constexpr uint32_t kColR0 = 0, kColR1 = 128, kColDP = 256, kColDQ = 384;
 
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[17];
+    __shared__ __align__(8) uint64_t bars[19];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
@@ -393,8 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
     const uint32_t bar_ke = smem_u32(&bars[4]);   // [3] K slot free (dQ_j done)
     const uint32_t bar_vf = smem_u32(&bars[7]);   // [2] V slot loaded
     const uint32_t bar_ve = smem_u32(&bars[9]);   // [2] V slot free (dP_j done)
-    const uint32_t bar_s = smem_u32(&bars[11]);   // S_j, dP_j computed
-    const uint32_t bar_c = smem_u32(&bars[12]);   // S_j, dP_j read into registers
+    const uint32_t bar_sq = smem_u32(&bars[17]);  // [2] by tile parity: S_j computed
+    const uint32_t bar_dp = smem_u32(&bars[11]);  // dP_j computed
+    const uint32_t bar_c = smem_u32(&bars[12]);   // dP_j read into registers
     const uint32_t bar_p = smem_u32(&bars[13]);   // [2] by tile parity: dS_j written
     const uint32_t bar_done = smem_u32(&bars[15]);
     const uint32_t bar_drain = smem_u32(&bars[16]);
@@ -411,7 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
             mbar_init(bar_ve + 8 * s, 1);
             mbar_init(bar_p + 8 * s, kEwThreads);
         }
-        mbar_init(bar_s, 1);
+        mbar_init(bar_sq, 1);
+        mbar_init(bar_sq + 8, 1);
+        mbar_init(bar_dp, 1);
         mbar_init(bar_c, kEwThreads);
         mbar_init(bar_done, 1);
         mbar_init(bar_drain, 1);
@@ -468,15 +498,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
     } else if (warp == kWarpMma) {
         if (lane == 0) {
             // S_j = Q K_j^T into R(j), dP_j = dO V_j^T into dP
-            // needs K_j and V_j landed
-            auto issue_scores = [&](int j) {
+            // S_j = Q K_j^T into R(j) (needs K_j), dP_j = dO V_j^T (needs V_j)
+            auto issue_s = [&](int j) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ss(tmem + col_r(j), desc_kmajor(sQ, kk), desc_kmajor(slot_k(j), kk), kIdescKK, kk > 0);
+                mma_commit(bar_sq + 8 * (j & 1));
+            };
+            auto issue_dp = [&](int j) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ss(tmem + kColDP, desc_kmajor(sO, kk), desc_kmajor(slot_v(j), kk), kIdescKK, kk > 0);
-                mma_commit(bar_s);
+                mma_commit(bar_dp);
                 mma_commit(bar_ve + 8 * (j & 1));
             };
             auto wait_kv = [&](int j) {
@@ -486,17 +519,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
             bool ok = mbar_wait(bar_qo, 0, &abort_flag, kWaitLimitNs) && wait_kv(0);
             if (ok) {
                 tc_fence_after();
-                issue_scores(0);
+                issue_s(0);
+                issue_dp(0);
             }
             for (int j = 0; ok && j < nkt; ++j) {
                 const int s = j & 1;
                 if (j + 1 < nkt) {
-                    if (!mbar_wait(bar_c, j & 1, &abort_flag, kWaitLimitNs) || !wait_kv(j + 1)) {
+                    // S_{j+1} goes to the other R region; dP_{j+1} waits until
+                    // the warps hold dP_j in registers
+                    if (!wait_kv(j + 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    issue_scores(j + 1);
+                    issue_s(j + 1);
+                    if (!mbar_wait(bar_c, j & 1, &abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_dp(j + 1);
                 }
                 if (!mbar_wait(bar_p + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs)) {
                     ok = false;
@@ -529,49 +571,42 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
         const float dl = a.delta_p[slot];
         bool ok = true;
         for (int j = 0; j < nkt; ++j) {
-            if (!warp_wait(bar_s, j & 1, &abort_flag)) {
+            if (!warp_wait(bar_sq + 8 * (j & 1), (j >> 1) & 1, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t s_cols = tmem + lane_addr + col_r(j) + c0;
-            uint32_t rs[2][32], rd[2][32];
-            tmem_ld32(s_cols, rs[0]);
-            tmem_ld32(s_cols + 32, rs[1]);
-            tmem_ld32(tmem + lane_addr + kColDP + c0, rd[0]);
-            tmem_ld32(tmem + lane_addr + kColDP + c0 + 32, rd[1]);
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(bar_c);  // S_j, dP_j are in registers: the MMA may overwrite dP
             const int kk0 = j < nkt_txt ? j * 128 : g.T_txt + (j - nkt_txt) * 128;
             const int nvalid = (j < nkt_txt ? L : g.S) - kk0 - c0;  // valid columns of this half
-            uint32_t pd[32];
-            if (nvalid >= 64) {
+            // P = exp2(S * c - lse2) (masked keys: 0) while dP_j computes
+            uint32_t rs[64];
+            tmem_ld32(s_cols, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
+            tmem_ld32(s_cols + 32, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
+            tmem_ld_wait();
+            float pf[64];
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
+            for (int i = 0; i < 64; ++i) pf[i] = exp2f(fmaf(__uint_as_float(rs[i]), kC, -l2));
+            if (nvalid < 64) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float p0 = exp2f(fmaf(__uint_as_float(rs[hh][2 * e]), kC, -l2));
-                        const float p1 = exp2f(fmaf(__uint_as_float(rs[hh][2 * e + 1]), kC, -l2));
-                        pd[16 * hh + e] = pack_bf16(p0 * (__uint_as_float(rd[hh][2 * e]) - dl),
-                                                    p1 * (__uint_as_float(rd[hh][2 * e + 1]) - dl));
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int col = 32 * hh + 2 * e;
-                        float p0 = exp2f(fmaf(__uint_as_float(rs[hh][2 * e]), kC, -l2));
-                        float p1 = exp2f(fmaf(__uint_as_float(rs[hh][2 * e + 1]), kC, -l2));
-                        p0 = col < nvalid ? p0 : 0.0f;
-                        p1 = col + 1 < nvalid ? p1 : 0.0f;
-                        pd[16 * hh + e] = pack_bf16(p0 * (__uint_as_float(rd[hh][2 * e]) - dl),
-                                                    p1 * (__uint_as_float(rd[hh][2 * e + 1]) - dl));
-                    }
-                }
+                for (int i = 0; i < 64; ++i) pf[i] = i < nvalid ? pf[i] : 0.0f;
             }
+            if (!warp_wait(bar_dp, j & 1, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t rd[64];
+            tmem_ld32(tmem + lane_addr + kColDP + c0, *reinterpret_cast<uint32_t(*)[32]>(&rd[0]));
+            tmem_ld32(tmem + lane_addr + kColDP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rd[32]));
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(bar_c);  // dP_j is in registers: the MMA may overwrite dP
+            uint32_t pd[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                pd[i] = pack_bf16(pf[2 * i] * (__uint_as_float(rd[2 * i]) - dl),
+                                  pf[2 * i + 1] * (__uint_as_float(rd[2 * i + 1]) - dl));
             tmem_st32(s_cols, pd);
             tmem_st_wait();
             tc_fence_before();
