@@ -56,6 +56,24 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's value (timing is reported for the
+    slowest rank); the identity with one rank."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, world: int, ms_per_step_slowest: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own replica of the workload
+    (weak scaling, no data-path collective), timed by the slowest rank."""
+    return world * flops_per_step / (ms_per_step_slowest * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
@@ -224,14 +242,8 @@ def run_ours(args):
         kern[name] = (tot, n)
     pkg.rlk_kernel_timing(False)
     pkg.rlk_joint_attn_check_status()
-    ms_max = ms_total
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    ms_step = ms_max / args.steps
-    value = world * flops["fwd_bwd"] / (ms_step * 1e-3) / 1e12
+    ms_step = max_over_ranks(ms_total, world, dev) / args.steps
+    value = job_throughput(flops["fwd_bwd"], world, ms_step)
 
     # ---- end to end through the public API with host buffers ----
     h_out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
@@ -259,13 +271,8 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms_e2e = e0.elapsed_time(e1) / n_e2e
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
-    e2e_value = world * flops["fwd_bwd"] / (ms_e2e * 1e-3) / 1e12
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
+    e2e_value = job_throughput(flops["fwd_bwd"], world, ms_e2e)
 
     # ---- roofline of the dominant kernel ----
     peaks, peak_src = load_peaks()
