@@ -145,6 +145,10 @@ def kernel_work(w: W.Workload):
     rows = w.B * w.H * w.S
     D = W.HEAD_DIM
     n_pos = (max(w.grid_h // 2, w.grid_w // 2) + w.T_txt) + max((w.grid_h + 1) // 2, (w.grid_w + 1) // 2)
+    # bf16 dS^T tiles (128 x 128) the dK/dV kernel writes and the dQ kernel
+    # reads: every query tile against the key tiles holding a valid key
+    ntq_txt, ntq_img = -(-w.T_txt // 128), -(-w.T_img // 128)
+    ds_bytes = sum(w.H * (ntq_txt + ntq_img) * (-(-L // 128) + ntq_img) * 128 * 128 * 2 for L in w.valid_len)
     return {
         "rope_table": ("hbm", n_pos * 64 * 8),
         # read Q, K (bf16), write qh, kh (bf16) and r (fp32) of both
@@ -154,9 +158,11 @@ def kernel_work(w: W.Workload):
         # read O, dO (bf16) and lse; write Delta and lse2 (fp32)
         "bwd_pre": ("hbm", 2 * rows * D * 2 + 3 * rows * 4),
         # recomputed S^T, dV, dP^T, dK: four of the five credited backward GEMMs
+        # (it also writes the dS^T tiles, ds_bytes)
         "bwd_dkdv": ("tensor", 4 * G),
-        # dQ: the fifth credited GEMM (its recomputed S and dP are not credited)
-        "bwd_dq": ("tensor", 1 * G),
+        # dQ = dS K, the fifth GEMM, streams the dS^T tiles: read them and K
+        # once, write dqh (fp32)
+        "bwd_dq": ("hbm", ds_bytes + rows * D * 2 + rows * D * 4),
         # read dqh, dkh (fp32), Q, K (bf16), r; write dQ, dK (bf16)
         "norm_rope_bwd": ("hbm", 2 * rows * D * 4 + 2 * rows * D * 2 + 2 * rows * 4 + 2 * rows * D * 2),
         "dg_fold": ("hbm", 2 * rows // 64 * D * 4 + w.B * w.H * 4 * D * 4),

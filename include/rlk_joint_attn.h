@@ -102,9 +102,13 @@ typedef struct rlk_ja_shape {
  * 0 for an invalid shape. */
 size_t rlk_joint_attn_ctx_bytes(const rlk_ja_shape* shape);
 
-/* Bytes of the backward scratch `workspace`: rowsum(dO * O) (fp32 [B, H, S]),
- * the fp32 gradients of the rotated q and k ([B, H, S, D] each) and the
- * per-chunk gain-gradient partials. Returns 0 for an invalid shape. */
+/* Bytes of the backward scratch `workspace`: lse * log2(e) and
+ * rowsum(dO * O) (fp32, one 128-slot block per query tile of each (sample,
+ * head)), the fp32 gradients of the rotated q and k ([B, H, S, D] each), the
+ * per-chunk gain-gradient partials and the bf16 score gradients dS as 128 x
+ * 128 tiles (B * H * n_tiles^2 * 32 KiB, n_tiles = ceil(T_txt / 128) +
+ * ceil(grid_h * grid_w / 128); 1.8 GB for B = 2, H = 24 at 1024 x 1024).
+ * Returns 0 for an invalid shape. */
 size_t rlk_joint_attn_bwd_workspace_bytes(const rlk_ja_shape* shape);
 
 /* Forward: rows qk_rmsnorm, multi_axis_rope, joint_attn_qk_gemm,

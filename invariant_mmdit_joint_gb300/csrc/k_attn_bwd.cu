@@ -11,13 +11,13 @@
 //                                                  (4 warps, one key row each;
 //                                                   bf16 results into TMEM)
 //           dV  += P^T dO,  dK += dS^T Q           (tcgen05, A from TMEM)
-//   dq:   one CTA = (query tile of 128, head, sample). Walks the key tiles of
-//         128 in the forward's order: S = Q K^T, dP = dO V^T, dS as above,
-//         dQ += dS K; the next tile's S and dP are computed while the
-//         elementwise warps work on the current one.
-// Accumulators (dV, dK, dQ) stay in TMEM in FP32 for the whole CTA and are
+//         and stores the bf16 dS^T tile in the tensor cores' operand layout.
+//   dq:   persistent; one unit = (query tile of 128, head, sample):
+//         dQ += dS K over the key tiles in the forward's order, reading the
+//         dS^T tiles back, so S and dP are computed once, not twice.
+// Accumulators (dV, dK, dQ) stay in TMEM in FP32 for the whole unit and are
 // written once. P and dS enter their products as bf16 (round to nearest
-// even). lse2 = lse * log2(e) and Delta = rowsum(dO * O) come from the
+// even); dK and dQ use the same bf16 dS. lse2 = lse * log2(e) and Delta = rowsum(dO * O) come from the
 // backward preprocess in a tile-padded layout (one 128-slot block per query
 // tile; slots past a segment hold lse2 = +inf and Delta = 0, so their P is
 // exactly 0). Every wait is bounded (RLK_ERR_DEVICE_TIMEOUT on give-up).
@@ -63,6 +63,7 @@ struct BwdArgs {
     uint16_t* dv;         // [B, S, H, 128]
     float* dkh;           // [B, H, S, 128]
     float* dqh;           // [B, H, S, 128]
+    uint8_t* ds_tiles;    // [B, H, nq, nq] images of 32 KB (query tile major)
 };
 
 __device__ __forceinline__ void fail(volatile int* abort_flag) {
@@ -84,6 +85,19 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
 // columns at the start of that half, so the two warps sharing a lane
 // quarter never overwrite each other's unread scores.
 __device__ __forceinline__ uint32_t a_col(int kk) { return (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8; }
+
+// dS^T tile image (128 keys x 128 queries, bf16, 32 KB): the non-swizzled
+// MN-major operand layout of the tensor cores. Query chunk C (8 queries) is
+// a 2 KB block of 128 key rows of 16 bytes, so 8 consecutive keys of one
+// chunk form one 128-byte core matrix; chunks along MN are 2 KB apart,
+// 8-key groups along K 128 bytes apart.
+constexpr int kDsChunkBytes = 2048;
+__device__ __forceinline__ int ds_image_offset(int query, int key) {
+    return (query >> 3) * kDsChunkBytes + key * 16 + (query & 7) * 2;
+}
+__device__ __forceinline__ uint64_t desc_ds_image(uint32_t tile, int kk) {
+    return sdesc_noswizzle(tile + kk * 2 * 128, 128, kDsChunkBytes);
+}
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitLimitNs));
@@ -329,6 +343,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_ds);
+            // the same bf16 dS^T row into the (query tile i, key tile kt)
+            // image for the dQ product (see ds_image_offset): a warp's
+            // store of one query chunk covers 512 contiguous bytes
+            uint8_t* ds_img = a.ds_tiles + ((bh * nq + i) * nq + kt) * (size_t)kTileBytes + ds_image_offset(c0, kr);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(ds_img + c * kDsChunkBytes) =
+                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         }
         if (ok && warp_wait(bar_done, 0, &abort_flag)) {
             tc_fence_after();
@@ -380,75 +402,65 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
 }
 
 // ====================================================================== dQ
-// TMEM: R0, R1 (scores of alternate key tiles), dP, dQ. Per key tile j the
-// elementwise warps pull S_j and dP_j into registers and report "consumed";
-// the MMA thread then computes S_{j+1} into the other R region and dP_{j+1}
-// over dP while the warps form dS_j = P (dP - Delta) and write it (bf16) over
-// S_j; then dQ += dS_j K_j. Reduction order over keys: tiles ascending.
-// K tiles live in a three-slot ring (each is read by S_j early and by the
-// dQ product late); V tiles, read only by dP_j, in a two-slot ring released
-// as soon as dP_j is done.
-constexpr int kDqSmemQ = 0, kDqSmemO = kTileBytes, kDqSmemK = 2 * kTileBytes;  // K: 3 slots
-constexpr int kDqSmemV = 5 * kTileBytes;                                           // V: 2 slots
-constexpr int kDqSmemBytes = 7 * kTileBytes + 1024;
-constexpr uint32_t kColR0 = 0, kColR1 = 128, kColDP = 256, kColDQ = 384;
+// dQ_i = sum_j dS_ij K_j as a streaming tcgen05 GEMM over the bf16 dS^T
+// images the dK/dV kernel wrote (one 32 KB image per (query tile, key tile)
+// pair, query tile major, in the tensor cores' non-swizzled operand layout,
+// so one bulk copy stages it and it enters the product as an MN-major A). Persistent: CTA c takes the units (query tile, head, sample)
+// c, c + grid, ... in order; a unit sums its key tiles in the forward's
+// order into one of two TMEM accumulators, so the epilogue of one unit
+// overlaps the products of the next. No unit depends on which CTA runs it.
+constexpr int kDqThreads = 192;  // warps 0-3 epilogue, 4 copies, 5 MMA
+constexpr int kDqWarpTma = 4, kDqWarpMma = 5;
+constexpr int kDqStages = 3;
+constexpr int kDqStageBytes = 2 * kTileBytes;  // dS^T image, K tile
+constexpr int kDqSmemBytes = kDqStages * kDqStageBytes + 1024;
+constexpr uint32_t kDqTmemCols = 256;
+constexpr uint32_t kIdescMM = idesc_bf16(128, 128, true, true);
 
-__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a) {
+struct DqUnit {
+    int qt, h, b;
+};
+__device__ __forceinline__ DqUnit dq_unit(const Geom& g, int nq, int u) {
+    DqUnit r;
+    r.qt = u % nq;
+    r.h = (u / nq) % g.H;
+    r.b = u / (nq * g.H);
+    return r;
+}
+
+__global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[19];
+    __shared__ __align__(8) uint64_t bars[2 * kDqStages + 5];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
     const Geom& g = a.g;
-    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int q0, q_end;
-    q_tile(g, qt, q0, q_end);
-    const int L = a.vl.L[b];
-    const int nkt_txt = (L + 127) / 128;
-    const int nkt = nkt_txt + g.ntq_img;
-    const size_t bh = (size_t)b * g.H + h;
-    const int row_base = (int)(bh * g.S);
-
+    const int nq = g.ntq_txt + g.ntq_img;
+    const int n_units = nq * g.H * g.B;
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t sQ = sbase + kDqSmemQ, sO = sbase + kDqSmemO;
-    auto slot_k = [&](int j) { return sbase + kDqSmemK + (j % 3) * kTileBytes; };
-    auto slot_v = [&](int j) { return sbase + kDqSmemV + (j & 1) * kTileBytes; };
-    auto col_r = [&](int j) { return (j & 1) ? kColR1 : kColR0; };
-    const uint32_t bar_qo = smem_u32(&bars[0]);
-    const uint32_t bar_kf = smem_u32(&bars[1]);   // [3] K slot loaded
-    const uint32_t bar_ke = smem_u32(&bars[4]);   // [3] K slot free (dQ_j done)
-    const uint32_t bar_vf = smem_u32(&bars[7]);   // [2] V slot loaded
-    const uint32_t bar_ve = smem_u32(&bars[9]);   // [2] V slot free (dP_j done)
-    const uint32_t bar_sq = smem_u32(&bars[17]);  // [2] by tile parity: S_j computed
-    const uint32_t bar_dp = smem_u32(&bars[11]);  // dP_j computed
-    const uint32_t bar_c = smem_u32(&bars[12]);   // dP_j read into registers
-    const uint32_t bar_p = smem_u32(&bars[13]);   // [2] by tile parity: dS_j written
-    const uint32_t bar_done = smem_u32(&bars[15]);
-    const uint32_t bar_drain = smem_u32(&bars[16]);
+    auto stage = [&](int s) { return sbase + s * kDqStageBytes; };
+    const uint32_t bar_full = smem_u32(&bars[0]);                   // [3] stage loaded
+    const uint32_t bar_empty = smem_u32(&bars[kDqStages]);          // [3] stage consumed
+    const uint32_t bar_acc = smem_u32(&bars[2 * kDqStages]);        // [2] accumulator complete
+    const uint32_t bar_free = smem_u32(&bars[2 * kDqStages + 2]);   // [2] accumulator read out
+    const uint32_t bar_drain = smem_u32(&bars[2 * kDqStages + 4]);
 
     if (tid == 0) {
         abort_flag = 0;
-        mbar_init(bar_qo, 1);
-        for (int s = 0; s < 3; ++s) {
-            mbar_init(bar_kf + 8 * s, 1);
-            mbar_init(bar_ke + 8 * s, 1);
+        for (int s = 0; s < kDqStages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(bar_vf + 8 * s, 1);
-            mbar_init(bar_ve + 8 * s, 1);
-            mbar_init(bar_p + 8 * s, kEwThreads);
+            mbar_init(bar_acc + 8 * s, 1);
+            mbar_init(bar_free + 8 * s, 128);
         }
-        mbar_init(bar_sq, 1);
-        mbar_init(bar_sq + 8, 1);
-        mbar_init(bar_dp, 1);
-        mbar_init(bar_c, kEwThreads);
-        mbar_init(bar_done, 1);
         mbar_init(bar_drain, 1);
         fence_barrier_init();
     }
-    if (warp == kWarpMma) {
-        tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+    if (warp == kDqWarpMma) {
+        tmem_alloc(smem_u32(&tmem_slot), kDqTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -456,173 +468,101 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
-    if (warp == kWarpTma) {
+    if (warp == kDqWarpTma) {
+        // ------------------------------------------------ copies
         if (lane == 0) {
-            prefetch_tensormap(&a.map_q);
             prefetch_tensormap(&a.map_k);
-            prefetch_tensormap(&a.map_v);
-            prefetch_tensormap(&a.map_do);
-            mbar_expect_tx(bar_qo, 2 * kTileBytes);
-            tma_load_2d(sQ, &a.map_q, bar_qo, 0, row_base + q0);
-            tma_load_2d(sQ + kBoxBytes, &a.map_q, bar_qo, 64, row_base + q0);
-            tma_load_4d(sO, &a.map_do, bar_qo, 0, h, q0, b);
-            tma_load_4d(sO + kBoxBytes, &a.map_do, bar_qo, 64, h, q0, b);
-            int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < nkt && !abort_flag; ++j) {
-                const int kk0 = j < nkt_txt ? j * 128 : g.T_txt + (j - nkt_txt) * 128;
-                const uint32_t kf = bar_kf + 8 * (j % 3), vf = bar_vf + 8 * (j & 1);
-                if (j >= 3 && !mbar_wait(bar_ke + 8 * (j % 3), ((j / 3) + 1) & 1, &abort_flag, kWaitLimitNs)) {
-                    fail(&abort_flag);
-                    break;
+            int t = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < n_units && !abort_flag; u += gridDim.x) {
+                const DqUnit w = dq_unit(g, nq, u);
+                const int L = a.vl.L[w.b];
+                const int nkt_txt = (L + 127) / 128;
+                const int nkt = nkt_txt + g.ntq_img;
+                const size_t bh = (size_t)w.b * g.H + w.h;
+                const int row_base = (int)(bh * g.S);
+                const uint8_t* tiles = a.ds_tiles + (bh * nq + w.qt) * nq * (size_t)kTileBytes;
+                for (int j = 0; j < nkt; ++j, ++t) {
+                    const int s = t % kDqStages;
+                    if (t >= kDqStages &&
+                        !mbar_wait(bar_empty + 8 * s, ((t / kDqStages) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const int kt = j < nkt_txt ? j : g.ntq_txt + (j - nkt_txt);
+                    const int kk0 = j < nkt_txt ? j * 128 : g.T_txt + (j - nkt_txt) * 128;
+                    const uint32_t bf = bar_full + 8 * s;
+                    mbar_expect_tx(bf, kDqStageBytes);
+                    bulk_load(stage(s), tiles + (size_t)kt * kTileBytes, kTileBytes, bf);
+                    tma_load_2d(stage(s) + kTileBytes, &a.map_k, bf, 0, row_base + kk0);
+                    tma_load_2d(stage(s) + kTileBytes + kBoxBytes, &a.map_k, bf, 64, row_base + kk0);
                 }
-                mbar_expect_tx(kf, kTileBytes);
-                tma_load_2d(slot_k(j), &a.map_k, kf, 0, row_base + kk0);
-                tma_load_2d(slot_k(j) + kBoxBytes, &a.map_k, kf, 64, row_base + kk0);
-                k_issued = j + 1;
-                if (j >= 2 && !mbar_wait(bar_ve + 8 * (j & 1), ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
-                    fail(&abort_flag);
-                    break;
-                }
-                mbar_expect_tx(vf, kTileBytes);
-                tma_load_4d(slot_v(j), &a.map_v, vf, 0, h, kk0, b);
-                tma_load_4d(slot_v(j) + kBoxBytes, &a.map_v, vf, 64, h, kk0, b);
-                v_issued = j + 1;
             }
+            if (!ok) fail(&abort_flag);
             const volatile int no_abort = 0;
-            mbar_wait(bar_qo, 0, &no_abort, kWaitLimitNs);
-            for (int j = k_issued - 3 < 0 ? 0 : k_issued - 3; j < k_issued; ++j)
-                mbar_wait(bar_kf + 8 * (j % 3), (j / 3) & 1, &no_abort, kWaitLimitNs);
-            for (int j = v_issued - 2 < 0 ? 0 : v_issued - 2; j < v_issued; ++j)
-                mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1, &no_abort, kWaitLimitNs);
+            for (int tt = t - kDqStages < 0 ? 0 : t - kDqStages; tt < t; ++tt)
+                mbar_wait(bar_full + 8 * (tt % kDqStages), (tt / kDqStages) & 1, &no_abort, kWaitLimitNs);
         }
-    } else if (warp == kWarpMma) {
+    } else if (warp == kDqWarpMma) {
+        // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            // S_j = Q K_j^T into R(j), dP_j = dO V_j^T into dP
-            // S_j = Q K_j^T into R(j) (needs K_j), dP_j = dO V_j^T (needs V_j)
-            auto issue_s = [&](int j) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + col_r(j), desc_kmajor(sQ, kk), desc_kmajor(slot_k(j), kk), kIdescKK, kk > 0);
-                mma_commit(bar_sq + 8 * (j & 1));
-            };
-            auto issue_dp = [&](int j) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kColDP, desc_kmajor(sO, kk), desc_kmajor(slot_v(j), kk), kIdescKK, kk > 0);
-                mma_commit(bar_dp);
-                mma_commit(bar_ve + 8 * (j & 1));
-            };
-            auto wait_kv = [&](int j) {
-                return mbar_wait(bar_kf + 8 * (j % 3), (j / 3) & 1, &abort_flag, kWaitLimitNs) &&
-                       mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1, &abort_flag, kWaitLimitNs);
-            };
-            bool ok = mbar_wait(bar_qo, 0, &abort_flag, kWaitLimitNs) && wait_kv(0);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0);
-                issue_dp(0);
-            }
-            for (int j = 0; ok && j < nkt; ++j) {
-                const int s = j & 1;
-                if (j + 1 < nkt) {
-                    // S_{j+1} goes to the other R region; dP_{j+1} waits until
-                    // the warps hold dP_j in registers
-                    if (!wait_kv(j + 1)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_s(j + 1);
-                    if (!mbar_wait(bar_c, j & 1, &abort_flag, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_dp(j + 1);
-                }
-                if (!mbar_wait(bar_p + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+            int t = 0, n = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++n) {
+                const DqUnit w = dq_unit(g, nq, u);
+                const int nkt = (a.vl.L[w.b] + 127) / 128 + g.ntq_img;
+                const int buf = n & 1;
+                if (n >= 2 && !mbar_wait(bar_free + 8 * buf, ((n >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                for (int j = 0; j < nkt; ++j, ++t) {
+                    const int s = t % kDqStages;
+                    if (!mbar_wait(bar_full + 8 * s, (t / kDqStages) & 1, &abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kColDQ, tmem + col_r(j) + a_col(kk), desc_mnmajor(slot_k(j), kk), kIdescKM,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar_ke + 8 * (j % 3));
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tmem + 128 * buf, desc_ds_image(stage(s), kk), desc_mnmajor(stage(s) + kTileBytes, kk),
+                               kIdescMM, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar_empty + 8 * s);
+                }
+                if (ok) mma_commit(bar_acc + 8 * buf);
             }
-            if (ok)
-                mma_commit(bar_done);
-            else
-                fail(&abort_flag);
+            if (!ok) fail(&abort_flag);
             mma_commit(bar_drain);
             const volatile int no_abort = 0;
             mbar_wait(bar_drain, 0, &no_abort, kWaitLimitNs);
         }
     } else {
-        // ------------------------------------------------ elementwise warps 0-7
-        // warp w: query rows 32 * (w % 4) + lane, key columns [64 hf, 64 hf + 64), hf = w / 4
-        const int lq = warp & 3, hf = warp >> 2;
-        const uint32_t lane_addr = (uint32_t)(lq * 32) << 16;
-        const int r = lq * 32 + lane;
-        const int c0 = 64 * hf;
-        const size_t slot = bh * g.nq_pad + (size_t)qt * 128 + r;
-        const float l2 = a.lse2_p[slot];
-        const float dl = a.delta_p[slot];
+        // ------------------------------------------------ epilogue warps 0-3: query row 32 w + lane
+        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+        const int r = warp * 32 + lane;
+        int n = 0;
         bool ok = true;
-        for (int j = 0; j < nkt; ++j) {
-            if (!warp_wait(bar_sq + 8 * (j & 1), (j >> 1) & 1, &abort_flag)) {
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++n) {
+            const DqUnit w = dq_unit(g, nq, u);
+            const int buf = n & 1;
+            if (!warp_wait(bar_acc + 8 * buf, (n >> 1) & 1, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t s_cols = tmem + lane_addr + col_r(j) + c0;
-            const int kk0 = j < nkt_txt ? j * 128 : g.T_txt + (j - nkt_txt) * 128;
-            const int nvalid = (j < nkt_txt ? L : g.S) - kk0 - c0;  // valid columns of this half
-            // P = exp2(S * c - lse2) (masked keys: 0) while dP_j computes
-            uint32_t rs[64];
-            tmem_ld32(s_cols, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
-            tmem_ld32(s_cols + 32, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
-            tmem_ld_wait();
-            float pf[64];
-#pragma unroll
-            for (int i = 0; i < 64; ++i) pf[i] = exp2f(fmaf(__uint_as_float(rs[i]), kC, -l2));
-            if (nvalid < 64) {
-#pragma unroll
-                for (int i = 0; i < 64; ++i) pf[i] = i < nvalid ? pf[i] : 0.0f;
-            }
-            if (!warp_wait(bar_dp, j & 1, &abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t rd[64];
-            tmem_ld32(tmem + lane_addr + kColDP + c0, *reinterpret_cast<uint32_t(*)[32]>(&rd[0]));
-            tmem_ld32(tmem + lane_addr + kColDP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rd[32]));
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(bar_c);  // dP_j is in registers: the MMA may overwrite dP
-            uint32_t pd[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                pd[i] = pack_bf16(pf[2 * i] * (__uint_as_float(rd[2 * i]) - dl),
-                                  pf[2 * i + 1] * (__uint_as_float(rd[2 * i + 1]) - dl));
-            tmem_st32(s_cols, pd);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar_p + 8 * (j & 1));
-        }
-        if (ok && warp_wait(bar_done, 0, &abort_flag)) {
-            tc_fence_after();
+            int q0, q_end;
+            q_tile(g, w.qt, q0, q_end);
             const bool row_ok = q0 + r < q_end;
+            const size_t bh = (size_t)w.b * g.H + w.h;
             float* dqrow = a.dqh + (bh * g.S + q0 + r) * kHeadDim;
 #pragma unroll 1
-            for (int c = c0; c < c0 + 64; c += 32) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t rr[32];
-                tmem_ld32(tmem + lane_addr + kColDQ + c, rr);
+                tmem_ld32(tmem + lane_addr + 128 * buf + 32 * c, rr);
                 tmem_ld_wait();
                 if (row_ok) {
-                    float4* dst = reinterpret_cast<float4*>(dqrow + c);
+                    float4* dst = reinterpret_cast<float4*>(dqrow + 32 * c);
 #pragma unroll
                     for (int v4 = 0; v4 < 8; ++v4)
                         dst[v4] = make_float4(__uint_as_float(rr[4 * v4]) * kScale, __uint_as_float(rr[4 * v4 + 1]) * kScale,
@@ -630,16 +570,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_tc_kernel(const __gri
                                               __uint_as_float(rr[4 * v4 + 3]) * kScale);
                 }
             }
-        } else {
-            fail(&abort_flag);
+            tc_fence_before();
+            mbar_arrive(bar_free + 8 * buf);
         }
+        if (!ok) fail(&abort_flag);
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == kDqWarpMma) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, kDqTmemCols);
     }
 }
 
@@ -694,6 +635,7 @@ bool make_args(BwdArgs* a, const Geom& g, const ValidLen& vl, const uint16_t* qh
     a->dv = nullptr;
     a->dkh = nullptr;
     a->dqh = nullptr;
+    a->ds_tiles = nullptr;
     return true;
 }
 
@@ -701,11 +643,12 @@ bool make_args(BwdArgs* a, const Geom& g, const ValidLen& vl, const uint16_t* qh
 
 cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
                                  const uint16_t* v, const uint16_t* dout, const float* lse2_p, const float* delta_p,
-                                 uint16_t* dv, float* dkh, cudaStream_t s) {
+                                 uint16_t* dv, float* dkh, uint8_t* ds_tiles, cudaStream_t s) {
     BwdArgs args;
     if (!make_args(&args, g, vl, qh, kh, v, dout, lse2_p, delta_p)) return cudaErrorInvalidValue;
     args.dv = dv;
     args.dkh = dkh;
+    args.ds_tiles = ds_tiles;
     cudaError_t e =
         cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmemBytes);
     if (e != cudaSuccess) return e;
@@ -716,18 +659,24 @@ cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16
     return cudaGetLastError();
 }
 
-cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
-                               const uint16_t* v, const uint16_t* dout, const float* lse2_p, const float* delta_p,
+cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t* kh, const uint8_t* ds_tiles,
                                float* dqh, cudaStream_t s) {
     BwdArgs args;
-    if (!make_args(&args, g, vl, qh, kh, v, dout, lse2_p, delta_p)) return cudaErrorInvalidValue;
+    if (!encode_rows(&args.map_k, kh, (uint64_t)g.B * g.H * g.S)) return cudaErrorInvalidValue;
+    args.g = g;
+    args.vl = vl;
     args.dqh = dqh;
-    cudaError_t e =
-        cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmemBytes);
+    args.ds_tiles = const_cast<uint8_t*>(ds_tiles);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(g.ntq_txt + g.ntq_img, g.H, g.B);
+    const int n_units = (g.ntq_txt + g.ntq_img) * g.H * g.B;
+    const int grid = n_units < sms ? n_units : sms;
     timing_begin(kKBwdDq, s);
-    attn_bwd_dq_tc_kernel<<<grid, kThreads, kDqSmemBytes, s>>>(args);
+    attn_bwd_dq_tc_kernel<<<grid, kDqThreads, kDqSmemBytes, s>>>(args);
     timing_end(kKBwdDq, s);
     return cudaGetLastError();
 }

@@ -98,7 +98,7 @@ CtxLayout ctx_layout(const Geom& g) {
 }
 
 struct WsLayout {
-    size_t lse2, delta, dqh, dkh, dgc, dgp, total;
+    size_t lse2, delta, dqh, dkh, dgc, dgp, dst, total;
 };
 WsLayout ws_layout(const Geom& g) {
     const size_t rows = (size_t)g.B * g.H * g.S;
@@ -111,7 +111,10 @@ WsLayout ws_layout(const Geom& g) {
     l.dkh = align_up(l.dqh + rows * kHeadDim * 4);
     l.dgc = align_up(l.dkh + rows * kHeadDim * 4);
     l.dgp = align_up(l.dgc + (size_t)g.B * g.H * 2 * nch * kHeadDim * 4);
-    l.total = align_up(l.dgp + (size_t)g.B * g.H * 4 * kHeadDim * 4);
+    // bf16 dS^T tile images, one 32 KB image per (query tile, key tile)
+    const size_t ntiles = (size_t)g.ntq_txt + g.ntq_img;
+    l.dst = align_up(l.dgp + (size_t)g.B * g.H * 4 * kHeadDim * 4);
+    l.total = align_up(l.dst + (size_t)g.B * g.H * ntiles * ntiles * 32768);
     return l;
 }
 
@@ -298,10 +301,11 @@ rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape, const void* q, const vo
 
     if (launch_bwd_pre(g, static_cast<const uint16_t*>(out), dO, lse, lse2_p, delta_p, s) != cudaSuccess)
         return RLK_ERR_CUDA;
-    if (launch_attn_bwd_dkdv(g, vl, qh, kh, vv, dO, lse2_p, delta_p, static_cast<uint16_t*>(dv), dkh, s) !=
-        cudaSuccess)
+    uint8_t* ds_tiles = ws + w.dst;
+    if (launch_attn_bwd_dkdv(g, vl, qh, kh, vv, dO, lse2_p, delta_p, static_cast<uint16_t*>(dv), dkh, ds_tiles,
+                             s) != cudaSuccess)
         return RLK_ERR_CUDA;
-    if (launch_attn_bwd_dq(g, vl, qh, kh, vv, dO, lse2_p, delta_p, dqh, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_attn_bwd_dq(g, vl, kh, ds_tiles, dqh, s) != cudaSuccess) return RLK_ERR_CUDA;
     if (launch_norm_rope_bwd(g, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), gains, tab, rq,
                              rk, dqh, dkh, static_cast<uint16_t*>(dq), static_cast<uint16_t*>(dk), dgc,
                              s) != cudaSuccess)

@@ -90,11 +90,9 @@ cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16
                                  const uint16_t* kh, const uint16_t* v,
                                  const uint16_t* dout, const float* lse2_p,
                                  const float* delta_p, uint16_t* dv, float* dkh,
-                                 cudaStream_t s);
-cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t* qh,
-                               const uint16_t* kh, const uint16_t* v,
-                               const uint16_t* dout, const float* lse2_p,
-                               const float* delta_p, float* dqh, cudaStream_t s);
+                                 uint8_t* ds_tiles, cudaStream_t s);
+cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t* kh,
+                               const uint8_t* ds_tiles, float* dqh, cudaStream_t s);
 int probe_bwd_tu(void);
 int read_and_clear_status_bwd(cudaStream_t s);
 

@@ -183,5 +183,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// Shared-memory matrix descriptor for a non-swizzled operand built of 8 x
+// 16-byte core matrices (128 contiguous bytes each). For an MN-major operand
+// lbo is the byte stride between groups of 8 rows along K and sbo the stride
+// between core matrices along MN (checked on the GPU against a CPU product;
+// the opposite assignment gives wrong sums).
+__device__ __forceinline__ uint64_t sdesc_noswizzle(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version of this architecture; layout 0: no swizzle
+    return d;
+}
+
 }  // namespace sm100
 }  // namespace rlk

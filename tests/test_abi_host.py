@@ -54,7 +54,8 @@ def test_buffer_sizes_match_documented_layout(L):
     nch = 256 // 64 + 4096 // 64
     slots = 2 * 24 * 128 * (256 // 128 + 4096 // 128)  # tile-padded lse2 and Delta
     ws = up(up(up(up(up(slots * 4) + slots * 4) + rows * 512) + rows * 512) + 2 * 24 * 2 * nch * 512)
-    ws += 2 * 24 * 4 * 512
+    ws = up(ws + 2 * 24 * 4 * 512)
+    ws += 2 * 24 * 34 * 34 * 32768  # bf16 dS tiles, 128 x 128 per (query tile, key tile)
     assert pkg.rlk_joint_attn_bwd_workspace_bytes(s) == up(ws)
     assert S == s.S
 
