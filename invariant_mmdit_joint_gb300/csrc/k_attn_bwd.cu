@@ -4,11 +4,12 @@
 //
 //   dkdv: one CTA = (key tile of 128, head, sample). Walks every query tile
 //         of 128 in one fixed ascending order (text tiles from token 0, then
-//         image tiles from token T_txt). Per query tile (P^T is formed while
-//         dP^T computes, dS^T while dV computes):
+//         image tiles from token T_txt). Per query tile (dS^T is formed
+//         while dV computes, the next tile's P^T while dK computes):
 //           S^T  = K Q^T, dP^T = V dO^T            (tcgen05, A and B in smem)
 //           P^T  = exp2(S^T * c - lse2), dS^T = P^T * (dP^T - Delta)
-//                                                  (4 warps, one key row each;
+//                                                  (8 warps: key row = TMEM
+//                                                   lane, 64 queries each;
 //                                                   bf16 results into TMEM)
 //           dV  += P^T dO,  dK += dS^T Q           (tcgen05, A from TMEM)
 //         and stores the bf16 dS^T tile in the tensor cores' operand layout.
@@ -26,6 +27,7 @@
 #include "rlk_sm100.cuh"
 
 #include <cudaTypedefs.h>
+#include <string.h>
 
 RLK_DEFINE_STRICT_PROBE(probe_bwd_tu)
 
@@ -64,6 +66,10 @@ struct BwdArgs {
     float* dkh;           // [B, H, S, 128]
     float* dqh;           // [B, H, S, 128]
     uint8_t* ds_tiles;    // [B, H, nq, nq] images of 32 KB (query tile major)
+    // output maps per segment (0 text, 1 image) so a tile's rows past its
+    // segment are clipped: dV [B, S, H, 128] bf16, dkh [B*H, S, 128] fp32
+    CUtensorMap map_dv[2];
+    CUtensorMap map_dk[2];
 };
 
 __device__ __forceinline__ void fail(volatile int* abort_flag) {
@@ -231,24 +237,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
     } else if (warp == kWarpMma) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            bool ok = mbar_wait(bar_kv, 0, &abort_flag, kWaitLimitNs);
-            for (int i = 0; ok && i < nq; ++i) {
-                const int s = i & 1;
-                if (!mbar_wait(bar_full + 8 * s, (i >> 1) & 1, &abort_flag, kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+            // S^T_i = K Q_i^T into the S^T columns (needs stage i loaded)
+            auto issue_st = [&](int i) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kColST, desc_kmajor(sK, kk), desc_kmajor(stage_q(s), kk), kIdescKK, kk > 0);
+                    mma_ss(tmem + kColST, desc_kmajor(sK, kk), desc_kmajor(stage_q(i & 1), kk), kIdescKK, kk > 0);
                 mma_commit(bar_st);
+            };
+            bool ok = mbar_wait(bar_kv, 0, &abort_flag, kWaitLimitNs) &&
+                      mbar_wait(bar_full, 0, &abort_flag, kWaitLimitNs);
+            if (ok) {
+                tc_fence_after();
+                issue_st(0);
+            }
+            // Order per query tile i: dP^T_i, dV_i (after P^T_i), S^T_{i+1},
+            // dK_i (after dS^T_i). S^T_{i+1} overwrites the columns holding
+            // P^T_i, which dV_i, issued before it, has consumed; dP^T_{i+1}
+            // follows dK_i, the last reader of dS^T_i. So the warps form
+            // P^T_{i+1} while dK_i computes.
+            for (int i = 0; ok && i < nq; ++i) {
+                const int s = i & 1;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ss(tmem + kColDPT, desc_kmajor(sV, kk), desc_kmajor(stage_o(s), kk), kIdescKK, kk > 0);
                 mma_commit(bar_dpt);
-                // dV needs only P (the warps form it while dP^T computes);
-                // dK needs dS (formed while dV computes)
                 if (!mbar_wait(bar_p, i & 1, &abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
@@ -258,6 +270,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tmem + kColDV, tmem + kColST + a_col(kk), desc_mnmajor(stage_o(s), kk), kIdescKM,
                            (i > 0 || kk > 0) ? 1u : 0u);
+                if (i + 1 < nq) {
+                    if (!mbar_wait(bar_full + 8 * (s ^ 1), ((i + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_st(i + 1);
+                }
                 if (!mbar_wait(bar_ds, i & 1, &abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
@@ -309,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
                 const float lq4[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const float pv = exp2f(fmaf(__uint_as_float(rs[4 * e4 + u]), kC, -lq4[u]));
+                    const float pv = exp2_sfu(fmaf(__uint_as_float(rs[4 * e4 + u]), kC, -lq4[u]));
                     pf[4 * e4 + u] = kvalid ? pv : 0.0f;
                 }
                 pk[2 * e4] = pack_bf16(pf[4 * e4], pf[4 * e4 + 1]);
@@ -354,39 +374,53 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
         }
         if (ok && warp_wait(bar_done, 0, &abort_flag)) {
             tc_fence_after();
-            const int j = k0 + kr;
-            const bool row_ok = j < seg_end;
-            uint16_t* dvrow = a.dv + (((size_t)b * g.S + j) * g.H + h) * kHeadDim;
-            float* dkrow = dkh + (size_t)j * kHeadDim;
+            // Stage dV (bf16) and dK (fp32, times 1/sqrt(D)) in the K, V and
+            // first Q buffers (every product has finished) as six 128-row x
+            // 128-byte boxes in the 128-byte-swizzled layout of the output
+            // maps: dV boxes 0-1 (64 columns each), dK boxes 2-5 (32 columns
+            // each). One thread then stores the tile with TMA; the segment
+            // maps clip rows past the key's segment. Masked keys get zeros.
+            uint8_t* stg = smem_raw + (sbase - smem_u32(smem_raw));
+            const int sw = kr & 7;
 #pragma unroll 1
-            for (int c = c0; c < c0 + 64; c += 32) {
+            for (int c = 0; c < 64; c += 32) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_addr + kColDV + c, r);
+                tmem_ld32(tmem + lane_addr + kColDV + c0 + c, r);
                 tmem_ld_wait();
-                uint32_t w[16];
+                uint8_t* dvrow = stg + half * kBoxBytes + kr * 128;
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = kvalid ? pack_bf16(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])) : 0u;
-                if (row_ok) {
-                    uint4* dst = reinterpret_cast<uint4*>(dvrow + c);
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[4];
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = kvalid ? pack_bf16(__uint_as_float(r[8 * q + 2 * e]), __uint_as_float(r[8 * q + 2 * e + 1]))
+                                      : 0u;
+                    *reinterpret_cast<uint4*>(dvrow + ((((c >> 3) + q) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                tmem_ld32(tmem + lane_addr + kColDK + c, r);
+                tmem_ld32(tmem + lane_addr + kColDK + c0 + c, r);
                 tmem_ld_wait();
-                if (row_ok) {
-                    float4* dst = reinterpret_cast<float4*>(dkrow + c);
+                uint8_t* dkrow = stg + (2 + ((c0 + c) >> 5)) * kBoxBytes + kr * 128;
 #pragma unroll
-                    for (int v4 = 0; v4 < 8; ++v4) {
-                        float4 f;
-                        f.x = kvalid ? __uint_as_float(r[4 * v4]) * kScale : 0.0f;
-                        f.y = kvalid ? __uint_as_float(r[4 * v4 + 1]) * kScale : 0.0f;
-                        f.z = kvalid ? __uint_as_float(r[4 * v4 + 2]) * kScale : 0.0f;
-                        f.w = kvalid ? __uint_as_float(r[4 * v4 + 3]) * kScale : 0.0f;
-                        dst[v4] = f;
-                    }
+                for (int q = 0; q < 8; ++q) {
+                    float4 f;
+                    f.x = kvalid ? __uint_as_float(r[4 * q]) * kScale : 0.0f;
+                    f.y = kvalid ? __uint_as_float(r[4 * q + 1]) * kScale : 0.0f;
+                    f.z = kvalid ? __uint_as_float(r[4 * q + 2]) * kScale : 0.0f;
+                    f.w = kvalid ? __uint_as_float(r[4 * q + 3]) * kScale : 0.0f;
+                    *reinterpret_cast<float4*>(dkrow + ((q ^ sw) << 4)) = f;
                 }
+            }
+            fence_proxy_async_smem();
+            named_barrier_sync(1, kEwThreads);
+            if (tid == 0) {
+                const int seg = k_txt ? 0 : 1;
+                const int srow = k_txt ? k0 : k0 - g.T_txt;
+                tma_store_4d(&a.map_dv[seg], sbase, 0, h, srow, b);
+                tma_store_4d(&a.map_dv[seg], sbase + kBoxBytes, 64, h, srow, b);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) tma_store_3d(&a.map_dk[seg], sbase + (2 + q) * kBoxBytes, 32 * q, srow, (int)bh);
+                bulk_commit_group();
+                bulk_wait_read_all();
             }
         } else {
             fail(&abort_flag);
@@ -622,6 +656,43 @@ bool encode_bshd(CUtensorMap* m, const void* base, const Geom& g) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Segment views for the stores: seg 0 = text rows [0, T_txt), seg 1 = image
+// rows [T_txt, S); a box reaching past the segment is clipped there.
+bool encode_bshd_segment(CUtensorMap* m, const uint16_t* base, const Geom& g, int seg) {
+    const int rows = seg == 0 ? g.T_txt : g.T_img;
+    if (rows == 0) {
+        memset(m, 0, sizeof(*m));  // no tile of this segment exists
+        return true;
+    }
+    auto enc = get_encode();
+    if (enc == nullptr) return false;
+    const uint16_t* p = base + (seg == 0 ? 0 : (size_t)g.T_txt * g.H * kHeadDim);
+    cuuint64_t dims[4] = {128, (cuuint64_t)g.H, (cuuint64_t)rows, (cuuint64_t)g.B};
+    cuuint64_t strides[3] = {256, (cuuint64_t)g.H * 256, (cuuint64_t)g.S * g.H * 256};
+    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(p), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool encode_bhsd_f32_segment(CUtensorMap* m, const float* base, const Geom& g, int seg) {
+    const int rows = seg == 0 ? g.T_txt : g.T_img;
+    if (rows == 0) {
+        memset(m, 0, sizeof(*m));
+        return true;
+    }
+    auto enc = get_encode();
+    if (enc == nullptr) return false;
+    const float* p = base + (seg == 0 ? 0 : (size_t)g.T_txt * kHeadDim);
+    cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)g.B * g.H};
+    cuuint64_t strides[2] = {512, (cuuint64_t)g.S * 512};
+    cuuint32_t box[3] = {32, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(p), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_args(BwdArgs* a, const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
                const uint16_t* v, const uint16_t* dout, const float* lse2_p, const float* delta_p) {
     const uint64_t rows = (uint64_t)g.B * g.H * g.S;
@@ -649,6 +720,9 @@ cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16
     args.dv = dv;
     args.dkh = dkh;
     args.ds_tiles = ds_tiles;
+    for (int seg = 0; seg < 2; ++seg)
+        if (!encode_bshd_segment(&args.map_dv[seg], dv, g, seg) || !encode_bhsd_f32_segment(&args.map_dk[seg], dkh, g, seg))
+            return cudaErrorInvalidValue;
     cudaError_t e =
         cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmemBytes);
     if (e != cudaSuccess) return e;

@@ -20,6 +20,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&p);
 }
 
+// ------------------------------------------------------------ exp2
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32): relative error
+// about 2^-22, results below 2^-126 flush to 0, 2^-inf = 0. Used only for
+// softmax numerators, which are rounded to bf16 (2^-9 relative) before their
+// products or summed into row sums of at least 1, so neither the error nor
+// the flush is visible. A fixed hardware instruction: the same bits on every
+// run and in every batch composition.
+__device__ __forceinline__ float exp2_sfu(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ------------------------------------------------------------ shared memory
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
