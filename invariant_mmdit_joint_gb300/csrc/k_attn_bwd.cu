@@ -37,9 +37,9 @@ namespace {
 using namespace sm100;
 
 // warps 0-7: elementwise (warp w owns TMEM lane quarter w % 4 and the
-// column half w / 4 of each row); warp 8: TMA producer; warp 9: MMA issuer
-// and TMEM owner.
-constexpr int kThreads = 320;
+// column half w / 4 of each row); warp 8: TMA producer; warps 9 and 10: MMA
+// issuers of two independent chains (warp 9 owns TMEM).
+constexpr int kThreads = 352;
 constexpr int kEwThreads = 256;
 constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr int kBoxBytes = 128 * 128;       // 128 rows x 64 bf16
@@ -128,7 +128,7 @@ constexpr uint32_t kColDV = 0, kColDK = 128, kColST = 256, kColDPT = 384;
 
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[12];
+    __shared__ __align__(8) uint64_t bars[12];  // bars[9]: second issuer's drain
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
@@ -178,14 +178,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
         mbar_init(bar_kv, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 2);  // one commit per issuer
         }
         mbar_init(bar_st, 1);
         mbar_init(bar_dpt, 1);
         mbar_init(bar_p, kEwThreads);
         mbar_init(bar_ds, kEwThreads);
-        mbar_init(bar_done, 1);
+        mbar_init(bar_done, 2);
         mbar_init(bar_drain, 1);
+        mbar_init(smem_u32(&bars[9]), 1);
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
@@ -234,68 +235,86 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
             for (int i = issued - 2 < 0 ? 0 : issued - 2; i < issued; ++i)
                 mbar_wait(bar_full + 8 * (i & 1), (i >> 1) & 1, &no_abort, kWaitLimitNs);
         }
-    } else if (warp == kWarpMma) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+        // ------------------------------------------------ MMA issuers
+        // Two independent chains, one issuing thread each, so that one keeps
+        // the tensor pipe fed while the other waits on a barrier:
+        //   warp 9:  S^T_0; per query tile i: dV_i (after P^T_i), then
+        //            S^T_{i+1} (after stage i+1 lands). S^T_{i+1} overwrites
+        //            the columns holding P^T_i, which dV_i, issued before it
+        //            on the same thread, has consumed.
+        //   warp 10: per query tile i: dP^T_i, then dK_i (after dS^T_i).
+        //            dP^T_{i+1} overwrites dS^T_i after dK_i, likewise.
+        // The two write disjoint TMEM columns; a stage frees when both have
+        // issued their last product reading it.
         if (lane == 0) {
-            // S^T_i = K Q_i^T into the S^T columns (needs stage i loaded)
+            const bool chain_p = warp == kWarpMma;
+            const uint32_t bar_my_drain = chain_p ? bar_drain : smem_u32(&bars[9]);
             auto issue_st = [&](int i) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ss(tmem + kColST, desc_kmajor(sK, kk), desc_kmajor(stage_q(i & 1), kk), kIdescKK, kk > 0);
                 mma_commit(bar_st);
             };
-            bool ok = mbar_wait(bar_kv, 0, &abort_flag, kWaitLimitNs) &&
-                      mbar_wait(bar_full, 0, &abort_flag, kWaitLimitNs);
-            if (ok) {
-                tc_fence_after();
-                issue_st(0);
-            }
-            // Order per query tile i: dP^T_i, dV_i (after P^T_i), S^T_{i+1},
-            // dK_i (after dS^T_i). S^T_{i+1} overwrites the columns holding
-            // P^T_i, which dV_i, issued before it, has consumed; dP^T_{i+1}
-            // follows dK_i, the last reader of dS^T_i. So the warps form
-            // P^T_{i+1} while dK_i computes.
-            for (int i = 0; ok && i < nq; ++i) {
-                const int s = i & 1;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kColDPT, desc_kmajor(sV, kk), desc_kmajor(stage_o(s), kk), kIdescKK, kk > 0);
-                mma_commit(bar_dpt);
-                if (!mbar_wait(bar_p, i & 1, &abort_flag, kWaitLimitNs)) {
-                    ok = false;
-                    break;
+            bool ok = mbar_wait(bar_kv, 0, &abort_flag, kWaitLimitNs);
+            if (chain_p) {
+                ok = ok && mbar_wait(bar_full, 0, &abort_flag, kWaitLimitNs);
+                if (ok) {
+                    tc_fence_after();
+                    issue_st(0);
                 }
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kColDV, tmem + kColST + a_col(kk), desc_mnmajor(stage_o(s), kk), kIdescKM,
-                           (i > 0 || kk > 0) ? 1u : 0u);
-                if (i + 1 < nq) {
-                    if (!mbar_wait(bar_full + 8 * (s ^ 1), ((i + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                for (int i = 0; ok && i < nq; ++i) {
+                    const int s = i & 1;
+                    if (!mbar_wait(bar_p, i & 1, &abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    issue_st(i + 1);
-                }
-                if (!mbar_wait(bar_ds, i & 1, &abort_flag, kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kColDK, tmem + kColDPT + a_col(kk), desc_mnmajor(stage_q(s), kk), kIdescKM,
-                           (i > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar_empty + 8 * s);
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tmem + kColDV, tmem + kColST + a_col(kk), desc_mnmajor(stage_o(s), kk), kIdescKM,
+                               (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar_empty + 8 * s);
+                    if (i + 1 < nq) {
+                        if (!mbar_wait(bar_full + 8 * (s ^ 1), ((i + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_st(i + 1);
+                    }
+                }
+            } else {
+                for (int i = 0; ok && i < nq; ++i) {
+                    const int s = i & 1;
+                    if (!mbar_wait(bar_full + 8 * s, (i >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tmem + kColDPT, desc_kmajor(sV, kk), desc_kmajor(stage_o(s), kk), kIdescKK, kk > 0);
+                    mma_commit(bar_dpt);
+                    if (!mbar_wait(bar_ds, i & 1, &abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tmem + kColDK, tmem + kColDPT + a_col(kk), desc_mnmajor(stage_q(s), kk), kIdescKM,
+                               (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar_empty + 8 * s);
+                }
             }
             if (ok)
                 mma_commit(bar_done);
             else
                 fail(&abort_flag);
-            mma_commit(bar_drain);
+            mma_commit(bar_my_drain);
             const volatile int no_abort = 0;
-            mbar_wait(bar_drain, 0, &no_abort, kWaitLimitNs);
+            mbar_wait(bar_my_drain, 0, &no_abort, kWaitLimitNs);
         }
     } else {
         // ------------------------------------------------ elementwise warps 0-7

@@ -225,26 +225,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                 if (has_b) issue_s(1, 0);
                 mma_commit(bar_ke);
             }
+            // Two wait points per key tile: a dependent barrier wait stalls
+            // the issuing thread for ~100 cycles while the tensor pipe, which
+            // buffers little, runs dry, so everything a pair of blocks needs
+            // is checked at once (non-blocking tests, one branch), with
+            // bounded blocking waits only when a check fails.
             for (int j = 0; ok && j < nkt; ++j) {
                 const int s = j & 1, s1 = (j + 1) & 1;
                 const bool more = j + 1 < nkt;
-                if (!mbar_wait(bar_p, j & 1, &abort_flag, kWaitLimitNs) ||
-                    !mbar_wait(bar_vf + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                // PV_A(j) needs P_A(j) and V(j); S_A(j+1) needs K(j+1)
+                const uint32_t kf_bar = bar_kf + 8 * s1, kf_par = ((j + 1) >> 1) & 1;
+                uint32_t r = mbar_test(bar_p, j & 1) & mbar_test(bar_vf + 8 * s, (j >> 1) & 1);
+                if (more) r &= mbar_test(kf_bar, kf_par);
+                if (!r && !(mbar_wait(bar_p, j & 1, &abort_flag, kWaitLimitNs) &&
+                            mbar_wait(bar_vf + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs) &&
+                            (!more || mbar_wait(kf_bar, kf_par, &abort_flag, kWaitLimitNs)))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 issue_pv(0, j);
-                if (more) {
-                    if (!mbar_wait(bar_kf + 8 * s1, ((j + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_s(0, j + 1);
-                }
+                if (more) issue_s(0, j + 1);
                 if (has_b) {
-                    if (!mbar_wait(bar_p + 8, j & 1, &abort_flag, kWaitLimitNs)) {
+                    // PV_B(j) needs P_B(j); S_B(j+1) reads the K(j+1) checked above
+                    if (!mbar_test(bar_p + 8, j & 1) && !mbar_wait(bar_p + 8, j & 1, &abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
