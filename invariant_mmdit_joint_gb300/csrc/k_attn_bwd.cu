@@ -25,9 +25,8 @@
 #include "rlk_device.cuh"
 #include "rlk_internal.h"
 #include "rlk_sm100.cuh"
+#include "rlk_tmap.h"
 
-#include <cudaTypedefs.h>
-#include <string.h>
 
 RLK_DEFINE_STRICT_PROBE(probe_bwd_tu)
 
@@ -638,85 +637,11 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc_kernel(const __g
 }
 
 // ---------------------------------------------------------------- tensor maps
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
-        cudaDriverEntryPointQueryResult q;
-        void* p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows) {
-    auto enc = get_encode();
-    if (enc == nullptr) return false;
-    cuuint64_t dims[2] = {128, rows};
-    cuuint64_t strides[1] = {256};
-    cuuint32_t box[2] = {64, 128};
-    cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool encode_bshd(CUtensorMap* m, const void* base, const Geom& g) {
-    auto enc = get_encode();
-    if (enc == nullptr) return false;
-    cuuint64_t dims[4] = {128, (cuuint64_t)g.H, (cuuint64_t)g.S, (cuuint64_t)g.B};
-    cuuint64_t strides[3] = {256, (cuuint64_t)g.H * 256, (cuuint64_t)g.S * g.H * 256};
-    cuuint32_t box[4] = {64, 1, 128, 1};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Segment views for the stores: seg 0 = text rows [0, T_txt), seg 1 = image
-// rows [T_txt, S); a box reaching past the segment is clipped there.
-bool encode_bshd_segment(CUtensorMap* m, const uint16_t* base, const Geom& g, int seg) {
-    const int rows = seg == 0 ? g.T_txt : g.T_img;
-    if (rows == 0) {
-        memset(m, 0, sizeof(*m));  // no tile of this segment exists
-        return true;
-    }
-    auto enc = get_encode();
-    if (enc == nullptr) return false;
-    const uint16_t* p = base + (seg == 0 ? 0 : (size_t)g.T_txt * g.H * kHeadDim);
-    cuuint64_t dims[4] = {128, (cuuint64_t)g.H, (cuuint64_t)rows, (cuuint64_t)g.B};
-    cuuint64_t strides[3] = {256, (cuuint64_t)g.H * 256, (cuuint64_t)g.S * g.H * 256};
-    cuuint32_t box[4] = {64, 1, 128, 1};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(p), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-bool encode_bhsd_f32_segment(CUtensorMap* m, const float* base, const Geom& g, int seg) {
-    const int rows = seg == 0 ? g.T_txt : g.T_img;
-    if (rows == 0) {
-        memset(m, 0, sizeof(*m));
-        return true;
-    }
-    auto enc = get_encode();
-    if (enc == nullptr) return false;
-    const float* p = base + (seg == 0 ? 0 : (size_t)g.T_txt * kHeadDim);
-    cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)g.B * g.H};
-    cuuint64_t strides[2] = {512, (cuuint64_t)g.S * 512};
-    cuuint32_t box[3] = {32, 128, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(p), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool make_args(BwdArgs* a, const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
                const uint16_t* v, const uint16_t* dout, const float* lse2_p, const float* delta_p) {
     const uint64_t rows = (uint64_t)g.B * g.H * g.S;
-    if (!encode_rows(&a->map_q, qh, rows) || !encode_rows(&a->map_k, kh, rows) || !encode_bshd(&a->map_v, v, g) ||
-        !encode_bshd(&a->map_do, dout, g))
+    if (!tmap::rows_bf16(&a->map_q, qh, rows) || !tmap::rows_bf16(&a->map_k, kh, rows) ||
+        !tmap::bshd_bf16(&a->map_v, v, g) || !tmap::bshd_bf16(&a->map_do, dout, g))
         return false;
     a->g = g;
     a->vl = vl;
@@ -740,7 +665,7 @@ cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16
     args.dkh = dkh;
     args.ds_tiles = ds_tiles;
     for (int seg = 0; seg < 2; ++seg)
-        if (!encode_bshd_segment(&args.map_dv[seg], dv, g, seg) || !encode_bhsd_f32_segment(&args.map_dk[seg], dkh, g, seg))
+        if (!tmap::bshd_bf16(&args.map_dv[seg], dv, g, seg) || !tmap::bhsd_f32_segment(&args.map_dk[seg], dkh, g, seg))
             return cudaErrorInvalidValue;
     cudaError_t e =
         cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmemBytes);
@@ -755,7 +680,7 @@ cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16
 cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t* kh, const uint8_t* ds_tiles,
                                float* dqh, cudaStream_t s) {
     BwdArgs args;
-    if (!encode_rows(&args.map_k, kh, (uint64_t)g.B * g.H * g.S)) return cudaErrorInvalidValue;
+    if (!tmap::rows_bf16(&args.map_k, kh, (uint64_t)g.B * g.H * g.S)) return cudaErrorInvalidValue;
     args.g = g;
     args.vl = vl;
     args.dqh = dqh;

@@ -27,8 +27,8 @@
 #include "rlk_device.cuh"
 #include "rlk_internal.h"
 #include "rlk_sm100.cuh"
+#include "rlk_tmap.h"
 
-#include <cudaTypedefs.h>
 
 RLK_DEFINE_STRICT_PROBE(probe_fwd_tu)
 
@@ -65,6 +65,7 @@ struct FwdArgs {
     ValidLen vl;
     uint16_t* out;       // [B, S, H, 128]
     float* lse;          // [B, H, S] or null
+    CUtensorMap map_o[2];  // out per segment (0 text, 1 image): rows past a segment are clipped
 };
 
 struct TileInfo {
@@ -360,28 +361,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
         }
         if (ok && warp_wait(bar_o + 8 * t, (nkt - 1) & 1, &abort_flag)) {
             tc_fence_after();
+            // O / l as bf16 into this tile's Q buffer (its last S product has
+            // finished) as two 128-row x 128-byte boxes in the 128-byte
+            // swizzle; one thread of the group then stores the tile with
+            // TMA, the segment map clipping rows past the segment.
             const float inv = 1.0f / l;
             const int n = q0[t] + row;
-            const bool row_ok = n < q_end;
-            uint16_t* orow = a.out + (((size_t)b * g.S + n) * g.H + h) * kHeadDim;
+            const uint32_t stg_u32 = sQ + t * kTileBytes;
+            uint8_t* stg = smem_raw + (stg_u32 - smem_u32(smem_raw));
+            const int sw = row & 7;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t r[32];
                 tmem_ld32(o_tmem + 32 * c, r);
                 tmem_ld_wait();
-                uint32_t w[16];
+                uint8_t* orow = stg + (c >> 1) * kBoxBytes + row * 128;
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    w[i] = pack_bf16(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-                if (row_ok) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-                    dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = pack_bf16(__uint_as_float(r[8 * q + 2 * e]) * inv, __uint_as_float(r[8 * q + 2 * e + 1]) * inv);
+                    *reinterpret_cast<uint4*>(orow + ((((c & 1) * 4 + q) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
-            if (row_ok && a.lse != nullptr) a.lse[((size_t)b * g.H + h) * g.S + n] = (m + log2f(l)) * kLn2;
+            fence_proxy_async_smem();
+            named_barrier_sync(1 + t, 128);
+            if ((warp & 3) == 0 && lane == 0) {
+                const int seg = q_txt ? 0 : 1;
+                const int srow = q0[t] - seg0;
+                tma_store_4d(&a.map_o[seg], stg_u32, 0, h, srow, b);
+                tma_store_4d(&a.map_o[seg], stg_u32 + kBoxBytes, 64, h, srow, b);
+                bulk_commit_group();
+                bulk_wait_read_all();
+            }
+            if (n < q_end && a.lse != nullptr) a.lse[((size_t)b * g.H + h) * g.S + n] = (m + log2f(l)) * kLn2;
         } else {
             fail(&abort_flag);
         }
@@ -395,52 +409,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
     }
 }
 
-// ---------------------------------------------------------------- tensor maps
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
-        cudaDriverEntryPointQueryResult q;
-        void* p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows) {
-    auto enc = get_encode();
-    if (enc == nullptr) return false;
-    cuuint64_t dims[2] = {128, rows};
-    cuuint64_t strides[1] = {256};
-    cuuint32_t box[2] = {64, 128};
-    cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool encode_bshd(CUtensorMap* m, const void* base, const Geom& g) {
-    auto enc = get_encode();
-    if (enc == nullptr) return false;
-    cuuint64_t dims[4] = {128, (cuuint64_t)g.H, (cuuint64_t)g.S, (cuuint64_t)g.B};
-    cuuint64_t strides[3] = {256, (cuuint64_t)g.H * 256, (cuuint64_t)g.S * g.H * 256};
-    cuuint32_t box[4] = {64, 1, 128, 1};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_attn_fwd(const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
                             const uint16_t* v, uint16_t* out, float* lse, cudaStream_t s) {
     FwdArgs local;
     const uint64_t rows = (uint64_t)g.B * g.H * g.S;
-    if (!encode_rows(&local.map_q, qh, rows) || !encode_rows(&local.map_k, kh, rows) ||
-        !encode_bshd(&local.map_v, v, g))
+    if (!tmap::rows_bf16(&local.map_q, qh, rows) || !tmap::rows_bf16(&local.map_k, kh, rows) ||
+        !tmap::bshd_bf16(&local.map_v, v, g) || !tmap::bshd_bf16(&local.map_o[0], out, g, 0) ||
+        !tmap::bshd_bf16(&local.map_o[1], out, g, 1))
         return cudaErrorInvalidValue;
     local.g = g;
     local.vl = vl;
