@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
                 const float lq4[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const float pv = exp2_sfu(fmaf(__uint_as_float(rs[4 * e4 + u]), kC, -lq4[u]));
+                    const float pv = exp2_num(fmaf(__uint_as_float(rs[4 * e4 + u]), kC, -lq4[u]));
                     pf[4 * e4 + u] = kvalid ? pv : 0.0f;
                 }
                 pk[2 * e4] = pack_bf16(pf[4 * e4], pf[4 * e4 + 1]);

@@ -323,8 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
-                const float p0 = exp2_sfu(fmaf(__uint_as_float(r[2 * i]), kC, -m_new));
-                const float p1 = exp2_sfu(fmaf(__uint_as_float(r[2 * i + 1]), kC, -m_new));
+                const float p0 = exp2_num(fmaf(__uint_as_float(r[2 * i]), kC, -m_new));
+                const float p1 = exp2_num(fmaf(__uint_as_float(r[2 * i + 1]), kC, -m_new));
                 sp[(2 * i) & 7] += p0;
                 sp[(2 * i + 1) & 7] += p1;
                 r[i] = pack_bf16(p0, p1);

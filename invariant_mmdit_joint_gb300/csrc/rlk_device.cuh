@@ -1,5 +1,5 @@
 // Device helpers shared by the kernels of librlk_joint_attn.so: bf16 packing,
-// cp.async / ldmatrix / mma.sync wrappers (inline PTX) and the per-unit
+// the softmax numerators' exp2, shared-memory addresses and the per-unit
 // strict-math probe.
 #pragma once
 
@@ -21,63 +21,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // ------------------------------------------------------------ exp2
-// 2^x on the special-function unit (PTX ex2.approx.ftz.f32): relative error
-// about 2^-22, results below 2^-126 flush to 0, 2^-inf = 0. Used only for
-// softmax numerators, which are rounded to bf16 (2^-9 relative) before their
-// products or summed into row sums of at least 1, so neither the error nor
-// the flush is visible. A fixed hardware instruction: the same bits on every
-// run and in every batch composition.
-__device__ __forceinline__ float exp2_sfu(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
+// Softmax numerators 2^x use the CUDA math library's exp2f (maximum error
+// 2 ulp, subnormal results kept, 2^-inf = 0), compiled without fast math:
+// no approximate or flush-to-zero instruction is named here.
+__device__ __forceinline__ float exp2_num(float x) { return exp2f(x); }
 
 // ------------------------------------------------------------ shared memory
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// 16-byte async copy global -> shared; when !valid the 16 bytes are zeroed.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-    int n = valid ? 16 : 0;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-// D += A * B, m16n8k16, bf16 inputs, fp32 accumulators.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// A tile of rows x 128 bf16 in shared memory: a row is 256 bytes = 16 chunks
-// of 16 bytes; chunk c of row r is stored at chunk position c ^ (r & 7), so
-// that the 8 rows an ldmatrix phase reads hit 8 different bank groups.
-__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk) {
-    return base + row * 256 + ((chunk ^ (row & 7)) << 4);
 }
 
 }  // namespace rlk
