@@ -185,6 +185,75 @@ rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape,
                               void* workspace, size_t workspace_bytes,
                               void* stream);
 
+/* ---------------------------------------------------------------------------
+ * The path's operators one at a time. The RFC's WS1 table lists
+ * qk_rmsnorm, multi_axis_rope, joint_attn_qk_gemm, joint_attn_softmax and
+ * joint_attn_av_gemm as separate rows and requires joint_attention_fused to
+ * be a byte-equal fusion of the three attention operators; the WS1
+ * Single-GPU Kernel List says the fusion "must match their composition byte
+ * for byte". The four calls below, chained as
+ *     rlk_qk_norm_rope -> rlk_joint_attn_qk_gemm -> rlk_joint_attn_softmax
+ *                      -> rlk_joint_attn_av_gemm
+ * produce `out` and `lse` bytes identical to rlk_joint_attn_fwd() on the same
+ * inputs, for every shape, batch composition and run.
+ *
+ * Intermediate layouts (n_tiles = ceil(T_txt/128) + ceil(grid_h*grid_w/128);
+ * column block t holds key tile t: text tiles from token 0, then image tiles
+ * from token T_txt, 128 keys each):
+ *   scores  fp32 [B, H, S, n_tiles * 128]  raw q^ . k^ (the 1/sqrt(128)
+ *           scale is applied inside the softmax, folded with log2(e) into
+ *           the exponent's one rounding, exactly as the fused kernel does)
+ *   P       bf16 [B, H, S, n_tiles * 128]  exp(s_ij - m_i(t)) where m_i(t)
+ *           is row i's running reference maximum when key tile t is visited
+ *   alpha   fp32 [B, H, S, n_tiles]        factor by which the running O and
+ *           row sum are rescaled at key tile t (1 when the reference stays)
+ *   l       fp32 [B, H, S]                 final row sum, so that
+ *           O_i = sum_t (prod_{t' > t} alpha_i(t')) P_i(t) V(t) / l_i
+ *   lse     fp32 [B, H, S]                 natural-log logsumexp
+ * Column blocks of text tiles past ceil(L_b/128) are not written; inside a
+ * visited block, masked key columns (and columns past the key's segment)
+ * hold -inf in `scores` and exactly 0 in P, so every written byte depends
+ * only on the sample's own inputs. Sizes come from
+ * rlk_joint_attn_unfused_bytes(). Pointer rules, errors and streams are those
+ * of the fused calls: every device pointer 16-byte aligned, validation errors
+ * launch nothing. */
+#define RLK_UNFUSED_SCORES 0
+#define RLK_UNFUSED_P 1
+#define RLK_UNFUSED_ALPHA 2
+#define RLK_UNFUSED_ROWS 3 /* one of l or lse */
+
+/* Bytes of one intermediate (`which` = RLK_UNFUSED_*); 0 for an invalid
+ * shape or `which`. 3.6 GB of scores for B = 2, H = 24 at 1024 x 1024. */
+size_t rlk_joint_attn_unfused_bytes(const rlk_ja_shape* shape, int which);
+
+/* Rows qk_rmsnorm + multi_axis_rope: writes the normed, rotated q^ and k^
+ * (bf16), their RMSNorm factors and the cos/sin table into `ctx`
+ * (rlk_joint_attn_ctx_bytes() bytes), exactly as rlk_joint_attn_fwd() does
+ * before its attention. Inputs as in rlk_joint_attn_fwd(). */
+rlk_status rlk_qk_norm_rope(const rlk_ja_shape* shape, const void* q, const void* k,
+                            const float* g_q_txt, const float* g_k_txt,
+                            const float* g_q_img, const float* g_k_img,
+                            void* ctx, void* stream);
+
+/* Row joint_attn_qk_gemm: scores = q^ k^T for every key tile holding a valid
+ * key, read from `ctx` as written by rlk_qk_norm_rope() or the forward. */
+rlk_status rlk_joint_attn_qk_gemm(const rlk_ja_shape* shape, const void* ctx,
+                                  const int32_t* txt_valid_len, float* scores,
+                                  void* stream);
+
+/* Row joint_attn_softmax: masked online softmax of `scores` over the key
+ * tiles in the fixed order; writes P, alpha, l and (if non-NULL) lse. */
+rlk_status rlk_joint_attn_softmax(const rlk_ja_shape* shape, const float* scores,
+                                  const int32_t* txt_valid_len, void* p,
+                                  float* alpha, float* l, float* lse, void* stream);
+
+/* Row joint_attn_av_gemm: out = O / l from P, alpha and l (above) and
+ * v (bf16 [B, S, H, D]); out bf16 [B, S, H, D], every row written. */
+rlk_status rlk_joint_attn_av_gemm(const rlk_ja_shape* shape, const void* p,
+                                  const float* alpha, const float* l, const void* v,
+                                  const int32_t* txt_valid_len, void* out,
+                                  void* stream);
+
 /* Synchronises `stream`, then reads and clears the device-side error word
  * that bounded waits in the kernels set when they give up. Returns RLK_OK,
  * RLK_ERR_DEVICE_TIMEOUT, or RLK_ERR_CUDA if the stream reported an error. */
@@ -224,7 +293,8 @@ const char* rlk_strerror(int status);
 
 /* Kernel timing for benchmarks. kernel ids: 0 rope table, 1 prologue,
  * 2 attention forward, 3 backward preprocess, 4 dK/dV, 5 dQ,
- * 6 RoPE/RMSNorm backward, 7 gain-gradient fold.
+ * 6 RoPE/RMSNorm backward, 7 gain-gradient fold, 8 qk_gemm, 9 softmax,
+ * 10 av_gemm.
  * rlk_kernel_timing(1) makes later calls record a CUDA event pair around
  * every launch (up to 4096 launches per kernel id); rlk_kernel_timing(0)
  * stops and clears. rlk_kernel_timing_read() waits for the recorded events

@@ -22,7 +22,9 @@ __all__ = [
     "rlk_joint_attn_ctx_bytes", "rlk_joint_attn_bwd_workspace_bytes",
     "rlk_joint_attn_fwd", "rlk_joint_attn_bwd", "rlk_joint_attn_check_status",
     "rlk_strict_math_compiled", "rlk_joint_attn_trace", "rlk_strerror",
-    "rlk_kernel_timing", "rlk_kernel_timing_read", "rlk_joint_attn_fwd_noalloc", "JointAttention",
+    "rlk_kernel_timing", "rlk_kernel_timing_read", "rlk_joint_attn_fwd_noalloc",
+    "rlk_joint_attn_unfused_bytes", "rlk_qk_norm_rope", "rlk_joint_attn_qk_gemm",
+    "rlk_joint_attn_softmax", "rlk_joint_attn_av_gemm", "UNFUSED", "JointAttention",
     "EXPORTED_SYMBOLS", "KERNEL_IDS",
 ]
 
@@ -40,13 +42,18 @@ STATUS_NAMES = {
 KERNEL_IDS = {
     "rope_table": 0, "prologue": 1, "attn_fwd": 2, "bwd_pre": 3,
     "bwd_dkdv": 4, "bwd_dq": 5, "norm_rope_bwd": 6, "dg_fold": 7,
+    "qk_gemm": 8, "softmax": 9, "av_gemm": 10,
 }
+# which intermediate rlk_joint_attn_unfused_bytes() sizes
+UNFUSED = {"scores": 0, "p": 1, "alpha": 2, "rows": 3}
 # Every symbol include/rlk_joint_attn.h declares.
 EXPORTED_SYMBOLS = (
     "rlk_joint_attn_ctx_bytes", "rlk_joint_attn_bwd_workspace_bytes",
     "rlk_joint_attn_fwd", "rlk_joint_attn_bwd", "rlk_joint_attn_check_status",
     "rlk_strict_math_compiled", "rlk_joint_attn_trace", "rlk_strerror",
     "rlk_kernel_timing", "rlk_kernel_timing_read", "rlk_joint_attn_fwd_noalloc",
+    "rlk_joint_attn_unfused_bytes", "rlk_qk_norm_rope", "rlk_joint_attn_qk_gemm",
+    "rlk_joint_attn_softmax", "rlk_joint_attn_av_gemm",
 )
 
 
@@ -130,6 +137,17 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     L.rlk_joint_attn_fwd_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_int32),
                                              vp, vp, vp]
     L.rlk_joint_attn_fwd_noalloc.restype = i32
+    L.rlk_joint_attn_unfused_bytes.argtypes = [shp, i32]
+    L.rlk_joint_attn_unfused_bytes.restype = sz
+    L.rlk_qk_norm_rope.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.rlk_qk_norm_rope.restype = i32
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    L.rlk_joint_attn_qk_gemm.argtypes = [shp, vp, i32p, vp, vp]
+    L.rlk_joint_attn_qk_gemm.restype = i32
+    L.rlk_joint_attn_softmax.argtypes = [shp, vp, i32p, vp, vp, vp, vp, vp]
+    L.rlk_joint_attn_softmax.restype = i32
+    L.rlk_joint_attn_av_gemm.argtypes = [shp, vp, vp, vp, vp, i32p, vp, vp]
+    L.rlk_joint_attn_av_gemm.restype = i32
     return L
 
 
@@ -215,6 +233,36 @@ def rlk_joint_attn_bwd(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_v
         _ptr(ctx), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg_partial), _ptr(dg), _ptr(workspace),
         int(workspace_bytes), _stream_handle(stream))
     _check(rc, "rlk_joint_attn_bwd")
+
+
+def rlk_joint_attn_unfused_bytes(shape: Shape, which: str | int) -> int:
+    w = UNFUSED[which] if isinstance(which, str) else int(which)
+    return int(lib().rlk_joint_attn_unfused_bytes(ctypes.byref(shape), w))
+
+
+def rlk_qk_norm_rope(shape, q, k, g_q_txt, g_k_txt, g_q_img, g_k_img, ctx, stream=None) -> None:
+    """Enqueue qk_rmsnorm + multi_axis_rope into ctx."""
+    rc = lib().rlk_qk_norm_rope(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(g_q_txt), _ptr(g_k_txt),
+                                _ptr(g_q_img), _ptr(g_k_img), _ptr(ctx), _stream_handle(stream))
+    _check(rc, "rlk_qk_norm_rope")
+
+
+def rlk_joint_attn_qk_gemm(shape, ctx, txt_valid_len, scores, stream=None) -> None:
+    rc = lib().rlk_joint_attn_qk_gemm(ctypes.byref(shape), _ptr(ctx), _lengths(txt_valid_len), _ptr(scores),
+                                      _stream_handle(stream))
+    _check(rc, "rlk_joint_attn_qk_gemm")
+
+
+def rlk_joint_attn_softmax(shape, scores, txt_valid_len, p, alpha, l, lse, stream=None) -> None:
+    rc = lib().rlk_joint_attn_softmax(ctypes.byref(shape), _ptr(scores), _lengths(txt_valid_len), _ptr(p),
+                                      _ptr(alpha), _ptr(l), _ptr(lse), _stream_handle(stream))
+    _check(rc, "rlk_joint_attn_softmax")
+
+
+def rlk_joint_attn_av_gemm(shape, p, alpha, l, v, txt_valid_len, out, stream=None) -> None:
+    rc = lib().rlk_joint_attn_av_gemm(ctypes.byref(shape), _ptr(p), _ptr(alpha), _ptr(l), _ptr(v),
+                                      _lengths(txt_valid_len), _ptr(out), _stream_handle(stream))
+    _check(rc, "rlk_joint_attn_av_gemm")
 
 
 def rlk_joint_attn_check_status(stream=None) -> None:
@@ -308,6 +356,32 @@ class JointAttention:
         rlk_joint_attn_bwd(sh, q, k, v, gains[0], gains[1], gains[2], gains[3], valid_len, out, dout,
                            lse, self.ctx, dq, dk, dv, dg_partial, dg, self.workspace, stream=stream)
         return dq, dk, dv, dg_partial, dg
+
+    def forward_unfused(self, q, k, v, gains, valid_len, stream=None):
+        """The forward as the four standalone operators (qk_rmsnorm +
+        multi_axis_rope, joint_attn_qk_gemm, joint_attn_softmax,
+        joint_attn_av_gemm) with materialised intermediates. Returns a dict
+        with out, lse and the intermediates scores [B, H, S, n_tiles*128]
+        fp32, p (same shape, bf16), alpha [B, H, S, n_tiles] fp32 and l."""
+        import torch
+        self._check_inputs(q, k, v)
+        self._check_gains(gains)
+        if len(valid_len) != self.shape.B:
+            raise ValueError("one valid length per sample")
+        sh = self.shape
+        n_tiles = -(-sh.T_txt // 128) + -(-(sh.grid_h * sh.grid_w) // 128)
+        dev = self.device
+        scores = torch.empty((sh.B, sh.H, sh.S, n_tiles * 128), dtype=torch.float32, device=dev)
+        p = torch.empty((sh.B, sh.H, sh.S, n_tiles * 128), dtype=torch.bfloat16, device=dev)
+        alpha = torch.empty((sh.B, sh.H, sh.S, n_tiles), dtype=torch.float32, device=dev)
+        l = torch.empty((sh.B, sh.H, sh.S), dtype=torch.float32, device=dev)
+        lse = torch.empty((sh.B, sh.H, sh.S), dtype=torch.float32, device=dev)
+        out = torch.empty_like(q)
+        rlk_qk_norm_rope(sh, q, k, gains[0], gains[1], gains[2], gains[3], self.ctx, stream)
+        rlk_joint_attn_qk_gemm(sh, self.ctx, valid_len, scores, stream)
+        rlk_joint_attn_softmax(sh, scores, valid_len, p, alpha, l, lse, stream)
+        rlk_joint_attn_av_gemm(sh, p, alpha, l, v, valid_len, out, stream)
+        return {"out": out, "lse": lse, "l": l, "scores": scores, "p": p, "alpha": alpha}
 
     def ctx_views(self):
         """Views of the forward context: qh, kh bf16 [B, H, S, 128]; rq, rk fp32 [B, H, S].

@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                 r[i] = pack_bf16(p0, p1);
             }
             const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-            l = l * alpha + rs;
+            l = fmaf(l, alpha, rs);  // one rounding, as the standalone softmax operator
             m = m_new;
             tmem_st32(s_tmem, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
             tmem_st32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));

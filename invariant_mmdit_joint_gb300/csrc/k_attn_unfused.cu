@@ -1,0 +1,598 @@
+// The three attention operators of the RFC #386 WS1 table on their own --
+// joint_attn_qk_gemm, joint_attn_softmax and joint_attn_av_gemm -- whose
+// composition reproduces the fused forward (joint_attention_fused,
+// k_attn_fwd.cu) byte for byte, as the table's joint_attention_fused row
+// ("byte-equal fusion of the three attention operators") and the WS1
+// Single-GPU Kernel List ("must match their composition byte for byte")
+// require.
+//
+// Byte equality holds because each operator performs the fused kernel's
+// arithmetic in the fused kernel's order:
+//   qk_gemm   the same tcgen05 SS products (128 x 128 x 16, 128-byte-swizzled
+//             K-major q^ and k^ tiles, k-steps 0..7 in order) into TMEM, read
+//             out as raw FP32 scores s = q^ . k^ (-inf for masked keys,
+//             which the fused kernel also sets to -inf). The 1/sqrt(128) scale is
+//             not applied here: the fused kernel folds it, with log2(e),
+//             into the one rounding of the softmax argument
+//             fmaf(s, log2(e)/sqrt(128), -m), and so does the softmax
+//             operator.
+//   softmax   per query row, key tiles in the fused order (text tiles that
+//             hold a valid key, then image tiles): the same masking, lazy
+//             reference max (moves only past a 2^8 growth), exp2f
+//             numerators, eight-way partial row sums and fixed sum tree; it
+//             writes P (bf16, relative to the row's reference max at that
+//             tile), the rescale factor alpha of every tile, the final row
+//             sum l and lse.
+//   av_gemm   the same tcgen05 TS products O += P V (P in TMEM as the A
+//             operand, V tiles MN-major in shared memory), O rescaled in
+//             TMEM by alpha before each tile's product, then O * (1 / l)
+//             rounded once to bf16.
+// The intermediates are materialised in caller-owned buffers:
+//   scores  fp32 [B, H, S, n_tiles * 128]   column block t = key tile t
+//   P       bf16 [B, H, S, n_tiles * 128]   (text tiles t < ceil(T_txt/128),
+//   alpha   fp32 [B, H, S, n_tiles]          then image tiles)
+//   l, lse  fp32 [B, H, S]
+// Blocks of text tiles with no valid key are not written; inside a visited
+// block the columns of masked keys hold -inf (scores) and exactly 0 (P).
+// Each query row is written by its own segment's tile. Every wait is
+// bounded (RLK_ERR_DEVICE_TIMEOUT).
+#include "rlk_device.cuh"
+#include "rlk_internal.h"
+#include "rlk_sm100.cuh"
+#include "rlk_tmap.h"
+
+RLK_DEFINE_STRICT_PROBE(probe_unfused_tu)
+
+namespace rlk {
+namespace {
+
+using namespace sm100;
+
+constexpr int kBoxBytes = 128 * 128;       // 128 rows x 64 bf16
+constexpr int kTileBytes = 2 * kBoxBytes;  // 128 rows x 128 bf16
+constexpr uint32_t kTmemCols = 256;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr float kC = (float)(1.4426950408889634 * 0.08838834764831845);  // log2(e) / sqrt(128)
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescO = idesc_bf16(128, 128, false, true);
+constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-5 one query row per thread
+constexpr int kWarpTma = 0, kWarpMma = 1;
+
+__device__ int g_status_unf;
+
+__device__ __forceinline__ void fail(volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicOr(&g_status_unf, 1);
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitLimitNs));
+}
+
+// Key tile j of the fused order for a sample with L valid text keys: its
+// column block in the materialised layout and its key range [k0, kend) of
+// valid keys.
+struct KeyTile {
+    int blk, k0, kend;
+};
+__device__ __forceinline__ KeyTile key_tile(const Geom& g, int L, int j) {
+    const int nkt_txt = (L + 127) / 128;
+    KeyTile t;
+    if (j < nkt_txt) {
+        t.blk = j;
+        t.k0 = j * 128;
+        t.kend = L;
+    } else {
+        t.blk = g.ntq_txt + (j - nkt_txt);
+        t.k0 = g.T_txt + (j - nkt_txt) * 128;
+        t.kend = g.S;
+    }
+    return t;
+}
+__device__ __forceinline__ int n_key_tiles(const Geom& g, int L) { return (L + 127) / 128 + g.ntq_img; }
+
+// Query tile qt (segment aligned): first token and end of its segment.
+__device__ __forceinline__ void query_tile(const Geom& g, int qt, int& q0, int& q_end) {
+    if (qt < g.ntq_txt) {
+        q0 = qt * 128;
+        q_end = g.T_txt;
+    } else {
+        q0 = g.T_txt + (qt - g.ntq_txt) * 128;
+        q_end = g.S;
+    }
+}
+
+// ====================================================================== qk_gemm
+struct QkArgs {
+    CUtensorMap map_q;  // qh [B*H*S, 128] bf16
+    CUtensorMap map_k;  // kh [B*H*S, 128] bf16
+    Geom g;
+    ValidLen vl;
+    float* scores;      // [B, H, S, ncols]
+    int ncols;
+};
+
+constexpr int kQkSmemBytes = 3 * kTileBytes + 1024;  // Q, two K slots
+
+__global__ void __launch_bounds__(kThreads, 1) qk_gemm_kernel(const __grid_constant__ QkArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[10];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+
+    const Geom& g = a.g;
+    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int q0, q_end;
+    query_tile(g, qt, q0, q_end);
+    const int L = a.vl.L[b];
+    const int nkt = n_key_tiles(g, L);
+    const size_t bh = (size_t)b * g.H + h;
+    const int row_base = (int)(bh * g.S);
+
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sQ = sbase, sK = sbase + kTileBytes;
+    const uint32_t bar_q = smem_u32(&bars[0]);
+    const uint32_t bar_kf = smem_u32(&bars[1]);  // [2] K slot loaded
+    const uint32_t bar_ke = smem_u32(&bars[3]);  // [2] K slot free (its product done)
+    const uint32_t bar_s = smem_u32(&bars[5]);   // [2] score buffer written
+    const uint32_t bar_se = smem_u32(&bars[7]);  // [2] score buffer read out
+    const uint32_t bar_drain = smem_u32(&bars[9]);
+
+    if (tid == 0) {
+        abort_flag = 0;
+        mbar_init(bar_q, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar_kf + 8 * s, 1);
+            mbar_init(bar_ke + 8 * s, 1);
+            mbar_init(bar_s + 8 * s, 1);
+            mbar_init(bar_se + 8 * s, 128);
+        }
+        mbar_init(bar_drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == kWarpTma) {
+        if (lane == 0) {
+            prefetch_tensormap(&a.map_q);
+            prefetch_tensormap(&a.map_k);
+            mbar_expect_tx(bar_q, kTileBytes);
+            tma_load_2d(sQ, &a.map_q, bar_q, 0, row_base + q0);
+            tma_load_2d(sQ + kBoxBytes, &a.map_q, bar_q, 64, row_base + q0);
+            int issued = 0;
+            for (int j = 0; j < nkt && !abort_flag; ++j) {
+                const int s = j & 1;
+                if (j >= 2 && !mbar_wait(bar_ke + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                    fail(&abort_flag);
+                    break;
+                }
+                const KeyTile kt = key_tile(g, L, j);
+                mbar_expect_tx(bar_kf + 8 * s, kTileBytes);
+                tma_load_2d(sK + s * kTileBytes, &a.map_k, bar_kf + 8 * s, 0, row_base + kt.k0);
+                tma_load_2d(sK + s * kTileBytes + kBoxBytes, &a.map_k, bar_kf + 8 * s, 64, row_base + kt.k0);
+                issued = j + 1;
+            }
+            const volatile int no_abort = 0;
+            mbar_wait(bar_q, 0, &no_abort, kWaitLimitNs);
+            for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
+                mbar_wait(bar_kf + 8 * (j & 1), (j >> 1) & 1, &no_abort, kWaitLimitNs);
+        }
+    } else if (warp == kWarpMma) {
+        if (lane == 0) {
+            bool ok = mbar_wait(bar_q, 0, &abort_flag, kWaitLimitNs);
+            for (int j = 0; ok && j < nkt; ++j) {
+                const int s = j & 1;
+                ok = mbar_wait(bar_kf + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs) &&
+                     (j < 2 || mbar_wait(bar_se + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t dk = sK + s * kTileBytes;
+                // the fused forward's score product, k-steps in the same order
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                    mma_ss(tmem + 128 * s, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(dk + off, 16, 1024), kIdescS,
+                           kk > 0);
+                }
+                mma_commit(bar_s + 8 * s);
+                mma_commit(bar_ke + 8 * s);
+            }
+            if (!ok) fail(&abort_flag);
+            mma_commit(bar_drain);
+            const volatile int no_abort = 0;
+            mbar_wait(bar_drain, 0, &no_abort, kWaitLimitNs);
+        }
+    } else {
+        // one query row per thread: TMEM lane quarter warp % 4
+        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+        const int row = (warp & 3) * 32 + lane;
+        const int n = q0 + row;
+        float* srow = a.scores + ((bh * g.S + n) * (size_t)a.ncols);
+        bool ok = true;
+        for (int j = 0; j < nkt; ++j) {
+            const int s = j & 1;
+            if (!warp_wait(bar_s + 8 * s, (j >> 1) & 1, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t r[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                tmem_ld32(tmem + lane_addr + 128 * s + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c]));
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(bar_se + 8 * s);
+            const KeyTile kt = key_tile(g, L, j);
+            const int nvalid = kt.kend - kt.k0;  // masked keys (and keys past the segment) score -inf
+            if (nvalid < 128) {
+#pragma unroll
+                for (int i = 0; i < 128; ++i) r[i] = i < nvalid ? r[i] : 0xff800000u;
+            }
+            if (n < q_end) {
+                float4* dst = reinterpret_cast<float4*>(srow + (size_t)kt.blk * 128);
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    dst[c] = make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
+                                         __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
+            }
+        }
+        if (!ok) fail(&abort_flag);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ====================================================================== softmax
+// One thread per query row (128 per CTA = one query tile); the row's scores
+// of one key tile are read with 16-byte loads into registers, exactly the
+// values the fused kernel reads from TMEM, and go through the fused kernel's
+// steps: mask, row max, lazy reference max, exp2f numerators, partial sums.
+struct SmArgs {
+    Geom g;
+    ValidLen vl;
+    const float* scores;  // [B, H, S, ncols]
+    uint32_t* p;          // bf16 pairs [B, H, S, ncols / 2]
+    float* alpha;         // [B, H, S, nblk]
+    float* l;             // [B, H, S]
+    float* lse;           // [B, H, S] or null
+    int ncols, nblk;
+};
+
+__global__ void __launch_bounds__(128) softmax_kernel(const __grid_constant__ SmArgs a) {
+    const Geom& g = a.g;
+    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    int q0, q_end;
+    query_tile(g, qt, q0, q_end);
+    const int n = q0 + (int)threadIdx.x;
+    if (n >= q_end) return;
+    const int L = a.vl.L[b];
+    const int nkt = n_key_tiles(g, L);
+    const size_t rowi = ((size_t)b * g.H + h) * g.S + n;
+    const float* srow = a.scores + rowi * a.ncols;
+    uint32_t* prow = a.p + rowi * (a.ncols / 2);
+    float* arow = a.alpha + rowi * a.nblk;
+    float m = -INFINITY, l = 0.0f;
+    for (int j = 0; j < nkt; ++j) {
+        const KeyTile kt = key_tile(g, L, j);
+        const int nvalid = kt.kend - kt.k0;
+        uint32_t r[128];
+        const uint4* src = reinterpret_cast<const uint4*>(srow + (size_t)kt.blk * 128);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const uint4 v = src[c];
+            r[4 * c] = v.x;
+            r[4 * c + 1] = v.y;
+            r[4 * c + 2] = v.z;
+            r[4 * c + 3] = v.w;
+        }
+        if (nvalid < 128) {
+#pragma unroll
+            for (int i = 0; i < 128; ++i) r[i] = i < nvalid ? r[i] : 0xff800000u;  // -inf
+        }
+        float mp[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mp[i] = __uint_as_float(r[i]);
+#pragma unroll
+        for (int i = 8; i < 128; ++i) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(r[i]));
+        const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        const float m_cand = fmaxf(m, mx * kC);
+        const bool move = m_cand > m + 8.0f;
+        const float m_new = move ? m_cand : m;
+        const float alpha = move ? exp2f(m - m_new) : 1.0f;
+        float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+            const float p0 = exp2_num(fmaf(__uint_as_float(r[2 * i]), kC, -m_new));
+            const float p1 = exp2_num(fmaf(__uint_as_float(r[2 * i + 1]), kC, -m_new));
+            sp[(2 * i) & 7] += p0;
+            sp[(2 * i + 1) & 7] += p1;
+            r[i] = pack_bf16(p0, p1);
+        }
+        const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+        l = fmaf(l, alpha, rs);
+        m = m_new;
+        uint4* dst = reinterpret_cast<uint4*>(prow + (size_t)kt.blk * 64);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) dst[c] = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+        arow[kt.blk] = alpha;
+    }
+    a.l[rowi] = l;
+    if (a.lse != nullptr) a.lse[rowi] = (m + log2f(l)) * kLn2;
+}
+
+// ====================================================================== av_gemm
+// One CTA = one query tile. TMEM: O [0, 128), P [128, 192) (64 columns of
+// bf16 pairs: pair i of a row in column 128 + i, the fused kernel's packed
+// layout, so k-step kk reads columns 128 + 8 kk .. 128 + 8 kk + 7).
+// Per key tile j of the fused order the row threads load their P row block
+// and alpha, wait for the previous product, rescale O by alpha (only in
+// warps where a row's alpha differs from 1, as the fused kernel does; the
+// other rows scale by exactly 1), store P into TMEM and signal the MMA
+// thread, which issues O += P V.
+struct AvArgs {
+    CUtensorMap map_v;     // v [B, S, H, 128] as 4-D
+    Geom g;
+    ValidLen vl;
+    const uint32_t* p;     // bf16 pairs [B, H, S, ncols / 2]
+    const float* alpha;    // [B, H, S, nblk]
+    const float* l;        // [B, H, S]
+    uint16_t* out;         // [B, S, H, 128]
+    int ncols, nblk;
+};
+
+// two V slots; sized like qk_gemm so that at most two CTAs (2 x 256 TMEM
+// columns) share an SM
+constexpr int kAvSmemBytes = 3 * kTileBytes + 1024;
+
+__global__ void __launch_bounds__(kThreads, 1) av_gemm_kernel(const __grid_constant__ AvArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[8];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+
+    const Geom& g = a.g;
+    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int q0, q_end;
+    query_tile(g, qt, q0, q_end);
+    const int L = a.vl.L[b];
+    const int nkt = n_key_tiles(g, L);
+    const size_t bh = (size_t)b * g.H + h;
+
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sV = sbase;
+    const uint32_t bar_vf = smem_u32(&bars[0]);  // [2] V slot loaded
+    const uint32_t bar_ve = smem_u32(&bars[2]);  // [2] V slot free
+    const uint32_t bar_p = smem_u32(&bars[4]);   // P stored and O rescaled (128 row threads)
+    const uint32_t bar_o = smem_u32(&bars[5]);   // product of tile j done (O updated, P read)
+    const uint32_t bar_drain = smem_u32(&bars[6]);
+
+    if (tid == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar_vf + 8 * s, 1);
+            mbar_init(bar_ve + 8 * s, 1);
+        }
+        mbar_init(bar_p, 128);
+        mbar_init(bar_o, 1);
+        mbar_init(bar_drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == kWarpTma) {
+        if (lane == 0) {
+            prefetch_tensormap(&a.map_v);
+            int issued = 0;
+            for (int j = 0; j < nkt && !abort_flag; ++j) {
+                const int s = j & 1;
+                if (j >= 2 && !mbar_wait(bar_ve + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                    fail(&abort_flag);
+                    break;
+                }
+                const KeyTile kt = key_tile(g, L, j);
+                mbar_expect_tx(bar_vf + 8 * s, kTileBytes);
+                tma_load_4d(sV + s * kTileBytes, &a.map_v, bar_vf + 8 * s, 0, h, kt.k0, b);
+                tma_load_4d(sV + s * kTileBytes + kBoxBytes, &a.map_v, bar_vf + 8 * s, 64, h, kt.k0, b);
+                issued = j + 1;
+            }
+            const volatile int no_abort = 0;
+            for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
+                mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1, &no_abort, kWaitLimitNs);
+        }
+    } else if (warp == kWarpMma) {
+        if (lane == 0) {
+            bool ok = true;
+            for (int j = 0; ok && j < nkt; ++j) {
+                const int s = j & 1;
+                ok = mbar_wait(bar_p, j & 1, &abort_flag, kWaitLimitNs) &&
+                     mbar_wait(bar_vf + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs);
+                if (!ok) break;
+                tc_fence_after();
+                // the fused forward's PV product: A = P from TMEM, B = V MN-major
+                const uint32_t dv = sV + s * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem, tmem + 128 + kk * 8, sdesc_sw128(dv + kk * 2048, kBoxBytes, 1024), kIdescO,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar_o);
+                mma_commit(bar_ve + 8 * s);
+            }
+            if (!ok) fail(&abort_flag);
+            mma_commit(bar_drain);
+            const volatile int no_abort = 0;
+            mbar_wait(bar_drain, 0, &no_abort, kWaitLimitNs);
+        }
+    } else {
+        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+        const int row = (warp & 3) * 32 + lane;
+        const int n = q0 + row;
+        const bool in_seg = n < q_end;
+        const size_t rowi = bh * g.S + (in_seg ? n : q0);
+        const uint4* prow = reinterpret_cast<const uint4*>(a.p + rowi * (a.ncols / 2));
+        bool ok = true;
+        for (int j = 0; j < nkt; ++j) {
+            const KeyTile kt = key_tile(g, L, j);
+            uint32_t pr[64];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const uint4 v = in_seg ? prow[kt.blk * 16 + c] : make_uint4(0u, 0u, 0u, 0u);
+                pr[4 * c] = v.x;
+                pr[4 * c + 1] = v.y;
+                pr[4 * c + 2] = v.z;
+                pr[4 * c + 3] = v.w;
+            }
+            const float alpha = in_seg ? a.alpha[rowi * a.nblk + kt.blk] : 1.0f;
+            if (j > 0) {
+                // the product of tile j - 1 has finished writing O and reading P
+                if (!warp_wait(bar_o, (j - 1) & 1, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+                    uint32_t o32[32];
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        tmem_ld32(tmem + lane_addr + 32 * c, o32);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
+                        tmem_st32(tmem + lane_addr + 32 * c, o32);
+                    }
+                }
+            }
+            tmem_st32(tmem + lane_addr + 128, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
+            tmem_st32(tmem + lane_addr + 160, *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar_p);
+        }
+        if (ok && warp_wait(bar_o, (nkt - 1) & 1, &abort_flag)) {
+            tc_fence_after();
+            // the TMEM loads are warp-collective; only rows inside the
+            // segment store
+            const float inv = 1.0f / a.l[rowi];
+            uint4* orow = reinterpret_cast<uint4*>(a.out + (((size_t)b * g.S + (in_seg ? n : q0)) * g.H + h) * kHeadDim);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_addr + 32 * c, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = pack_bf16(__uint_as_float(r[8 * q + 2 * e]) * inv,
+                                         __uint_as_float(r[8 * q + 2 * e + 1]) * inv);
+                    if (in_seg) orow[4 * c + q] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+        } else {
+            fail(&abort_flag);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_qk_gemm(const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh, float* scores,
+                           cudaStream_t s) {
+    QkArgs a;
+    const uint64_t rows = (uint64_t)g.B * g.H * g.S;
+    if (!tmap::rows_bf16(&a.map_q, qh, rows) || !tmap::rows_bf16(&a.map_k, kh, rows)) return cudaErrorInvalidValue;
+    a.g = g;
+    a.vl = vl;
+    a.scores = scores;
+    a.ncols = 128 * (g.ntq_txt + g.ntq_img);
+    cudaError_t e = cudaFuncSetAttribute(qk_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkSmemBytes);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(g.ntq_txt + g.ntq_img, g.H, g.B);
+    timing_begin(kKQkGemm, s);
+    qk_gemm_kernel<<<grid, kThreads, kQkSmemBytes, s>>>(a);
+    timing_end(kKQkGemm, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_softmax(const Geom& g, const ValidLen& vl, const float* scores, uint16_t* p, float* alpha,
+                           float* l, float* lse, cudaStream_t s) {
+    SmArgs a;
+    a.g = g;
+    a.vl = vl;
+    a.scores = scores;
+    a.p = reinterpret_cast<uint32_t*>(p);
+    a.alpha = alpha;
+    a.l = l;
+    a.lse = lse;
+    a.nblk = g.ntq_txt + g.ntq_img;
+    a.ncols = 128 * a.nblk;
+    const dim3 grid(a.nblk, g.H, g.B);
+    timing_begin(kKSoftmax, s);
+    softmax_kernel<<<grid, 128, 0, s>>>(a);
+    timing_end(kKSoftmax, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_av_gemm(const Geom& g, const ValidLen& vl, const uint16_t* p, const float* alpha, const float* l,
+                           const uint16_t* v, uint16_t* out, cudaStream_t s) {
+    AvArgs a;
+    if (!tmap::bshd_bf16(&a.map_v, v, g)) return cudaErrorInvalidValue;
+    a.g = g;
+    a.vl = vl;
+    a.p = reinterpret_cast<const uint32_t*>(p);
+    a.alpha = alpha;
+    a.l = l;
+    a.out = out;
+    a.nblk = g.ntq_txt + g.ntq_img;
+    a.ncols = 128 * a.nblk;
+    cudaError_t e = cudaFuncSetAttribute(av_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAvSmemBytes);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(a.nblk, g.H, g.B);
+    timing_begin(kKAvGemm, s);
+    av_gemm_kernel<<<grid, kThreads, kAvSmemBytes, s>>>(a);
+    timing_end(kKAvGemm, s);
+    return cudaGetLastError();
+}
+
+int read_and_clear_status_unfused(cudaStream_t s) {
+    int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_status_unf, sizeof(int), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return -1;
+    if (cudaMemcpyToSymbolAsync(g_status_unf, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return -1;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return -1;
+    return v;
+}
+
+}  // namespace rlk

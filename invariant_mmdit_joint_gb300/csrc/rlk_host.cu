@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <vector>
 
@@ -125,7 +126,7 @@ std::mutex g_dev_mu;
 int g_dev_state[kMaxDevices];  // 0 unknown, 1 ok, 2 wrong arch, 3 fast math, 4 cuda error
 
 int strict_all_units() {
-    const int r[4] = {probe_host_tu(), probe_prologue_tu(), probe_fwd_tu(), probe_bwd_tu()};
+    const int r[5] = {probe_host_tu(), probe_prologue_tu(), probe_fwd_tu(), probe_bwd_tu(), probe_unfused_tu()};
     for (int v : r)
         if (v < 0) return -1;
     for (int v : r)
@@ -165,6 +166,46 @@ rlk_status common_checks(const rlk_ja_shape* sh, const int32_t* vl, Geom* g, Val
     *g = make_geom(sh);
     std::memset(v, 0, sizeof(*v));
     for (int b = 0; b < sh->B; ++b) v->L[b] = vl[b];
+    return RLK_OK;
+}
+
+// Rows qk_rmsnorm + multi_axis_rope: cos/sin table and normed, rotated q^, k^
+// (with the RMSNorm factors) into ctx.
+rlk_status run_prologue(const Geom& g, const void* q, const void* k, const float* const gains[4], void* ctx,
+                        cudaStream_t s) {
+    const CtxLayout l = ctx_layout(g);
+    uint8_t* c = static_cast<uint8_t*>(ctx);
+    float2* tab = reinterpret_cast<float2*>(c + l.tab);
+    if (launch_rope_table(g, tab, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_prologue(g, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), gains, tab,
+                        reinterpret_cast<uint16_t*>(c + l.qh), reinterpret_cast<uint16_t*>(c + l.kh),
+                        reinterpret_cast<float*>(c + l.rq), reinterpret_cast<float*>(c + l.rk), s) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+// Sizes of the standalone operators' intermediates.
+size_t unfused_bytes(const Geom& g, int which) {
+    const size_t rows = (size_t)g.B * g.H * g.S;
+    const size_t nblk = (size_t)g.ntq_txt + g.ntq_img;
+    switch (which) {
+        case RLK_UNFUSED_SCORES: return rows * nblk * 128 * 4;
+        case RLK_UNFUSED_P: return rows * nblk * 128 * 2;
+        case RLK_UNFUSED_ALPHA: return rows * nblk * 4;
+        case RLK_UNFUSED_ROWS: return rows * 4;
+        default: return 0;
+    }
+}
+
+// Common argument checks of the standalone entry points: valid shape and
+// lengths, non-null and 16-byte-aligned device pointers, a supported device.
+rlk_status check_ptrs(std::initializer_list<const void*> required, std::initializer_list<const void*> optional) {
+    for (const void* p : required)
+        if (p == nullptr) return RLK_ERR_INVALID_ARG;
+    for (const void* p : required)
+        if (!aligned16(p)) return RLK_ERR_ALIGNMENT;
+    for (const void* p : optional)
+        if (p != nullptr && !aligned16(p)) return RLK_ERR_ALIGNMENT;
     return RLK_OK;
 }
 
@@ -241,17 +282,12 @@ rlk_status rlk_joint_attn_fwd(const rlk_ja_shape* shape, const void* q, const vo
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const CtxLayout l = ctx_layout(g);
     uint8_t* c = static_cast<uint8_t*>(ctx);
-    uint16_t* qh = reinterpret_cast<uint16_t*>(c + l.qh);
-    uint16_t* kh = reinterpret_cast<uint16_t*>(c + l.kh);
-    float* rq = reinterpret_cast<float*>(c + l.rq);
-    float* rk = reinterpret_cast<float*>(c + l.rk);
-    float2* tab = reinterpret_cast<float2*>(c + l.tab);
+    const uint16_t* qh = reinterpret_cast<const uint16_t*>(c + l.qh);
+    const uint16_t* kh = reinterpret_cast<const uint16_t*>(c + l.kh);
     const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
 
-    if (launch_rope_table(g, tab, s) != cudaSuccess) return RLK_ERR_CUDA;
-    if (launch_prologue(g, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), gains, tab, qh, kh,
-                        rq, rk, s) != cudaSuccess)
-        return RLK_ERR_CUDA;
+    st = run_prologue(g, q, k, gains, ctx, s);
+    if (st != RLK_OK) return st;
     if (launch_attn_fwd(g, vl, qh, kh, static_cast<const uint16_t*>(v), static_cast<uint16_t*>(out), lse, s) !=
         cudaSuccess)
         return RLK_ERR_CUDA;
@@ -314,13 +350,84 @@ rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape, const void* q, const vo
     return RLK_OK;
 }
 
+size_t rlk_joint_attn_unfused_bytes(const rlk_ja_shape* shape, int which) {
+    rlk_status why;
+    if (!shape_ok(shape, &why)) return 0;
+    return unfused_bytes(make_geom(shape), which);
+}
+
+rlk_status rlk_qk_norm_rope(const rlk_ja_shape* shape, const void* q, const void* k, const float* g_q_txt,
+                            const float* g_k_txt, const float* g_q_img, const float* g_k_img, void* ctx,
+                            void* stream) {
+    rlk_status why = RLK_OK;
+    if (!shape_ok(shape, &why)) return why;
+    rlk_status st = check_ptrs({q, k, g_q_txt, g_k_txt, g_q_img, g_k_img, ctx}, {});
+    if (st != RLK_OK) return st;
+    st = device_ok();
+    if (st != RLK_OK) return st;
+    const Geom g = make_geom(shape);
+    const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
+    return run_prologue(g, q, k, gains, ctx, static_cast<cudaStream_t>(stream));
+}
+
+rlk_status rlk_joint_attn_qk_gemm(const rlk_ja_shape* shape, const void* ctx, const int32_t* txt_valid_len,
+                                  float* scores, void* stream) {
+    Geom g;
+    ValidLen vl;
+    rlk_status st = common_checks(shape, txt_valid_len, &g, &vl);
+    if (st != RLK_OK) return st;
+    st = check_ptrs({ctx, scores}, {});
+    if (st != RLK_OK) return st;
+    st = device_ok();
+    if (st != RLK_OK) return st;
+    const CtxLayout l = ctx_layout(g);
+    const uint8_t* c = static_cast<const uint8_t*>(ctx);
+    if (launch_qk_gemm(g, vl, reinterpret_cast<const uint16_t*>(c + l.qh), reinterpret_cast<const uint16_t*>(c + l.kh),
+                       scores, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status rlk_joint_attn_softmax(const rlk_ja_shape* shape, const float* scores, const int32_t* txt_valid_len,
+                                  void* p, float* alpha, float* l, float* lse, void* stream) {
+    Geom g;
+    ValidLen vl;
+    rlk_status st = common_checks(shape, txt_valid_len, &g, &vl);
+    if (st != RLK_OK) return st;
+    st = check_ptrs({scores, p, alpha, l}, {lse});
+    if (st != RLK_OK) return st;
+    st = device_ok();
+    if (st != RLK_OK) return st;
+    if (launch_softmax(g, vl, scores, static_cast<uint16_t*>(p), alpha, l, lse, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status rlk_joint_attn_av_gemm(const rlk_ja_shape* shape, const void* p, const float* alpha, const float* l,
+                                  const void* v, const int32_t* txt_valid_len, void* out, void* stream) {
+    Geom g;
+    ValidLen vl;
+    rlk_status st = common_checks(shape, txt_valid_len, &g, &vl);
+    if (st != RLK_OK) return st;
+    st = check_ptrs({p, alpha, l, v, out}, {});
+    if (st != RLK_OK) return st;
+    st = device_ok();
+    if (st != RLK_OK) return st;
+    if (launch_av_gemm(g, vl, static_cast<const uint16_t*>(p), alpha, l, static_cast<const uint16_t*>(v),
+                       static_cast<uint16_t*>(out), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
 rlk_status rlk_joint_attn_check_status(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return RLK_ERR_CUDA;
     const int a = read_and_clear_status_fwd(s);
     const int b = read_and_clear_status_bwd(s);
-    if (a < 0 || b < 0) return RLK_ERR_CUDA;
-    if (a != 0 || b != 0) return RLK_ERR_DEVICE_TIMEOUT;
+    const int c = read_and_clear_status_unfused(s);
+    if (a < 0 || b < 0 || c < 0) return RLK_ERR_CUDA;
+    if (a != 0 || b != 0 || c != 0) return RLK_ERR_DEVICE_TIMEOUT;
     return RLK_OK;
 }
 

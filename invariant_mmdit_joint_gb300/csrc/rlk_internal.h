@@ -52,7 +52,8 @@ __host__ __device__ inline int pair_axis(int k) {
 // Kernel ids used by the launch timing hooks (see rlk_kernel_timing()).
 enum KernelId {
     kKRopeTable = 0, kKPrologue = 1, kKAttnFwd = 2, kKBwdPre = 3,
-    kKBwdDkDv = 4, kKBwdDq = 5, kKNormRopeBwd = 6, kKDgFold = 7, kNumKernelIds = 8
+    kKBwdDkDv = 4, kKBwdDq = 5, kKNormRopeBwd = 6, kKDgFold = 7,
+    kKQkGemm = 8, kKSoftmax = 9, kKAvGemm = 10, kNumKernelIds = 11
 };
 
 // Launch timing hooks (rlk_host.cu): bracket one launch with events.
@@ -95,6 +96,17 @@ cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t
                                const uint8_t* ds_tiles, float* dqh, cudaStream_t s);
 int probe_bwd_tu(void);
 int read_and_clear_status_bwd(cudaStream_t s);
+
+// k_attn_unfused.cu: the standalone joint_attn_qk_gemm, joint_attn_softmax
+// and joint_attn_av_gemm operators (layouts in that file's header)
+cudaError_t launch_qk_gemm(const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
+                           float* scores, cudaStream_t s);
+cudaError_t launch_softmax(const Geom& g, const ValidLen& vl, const float* scores, uint16_t* p,
+                           float* alpha, float* l, float* lse, cudaStream_t s);
+cudaError_t launch_av_gemm(const Geom& g, const ValidLen& vl, const uint16_t* p, const float* alpha,
+                           const float* l, const uint16_t* v, uint16_t* out, cudaStream_t s);
+int probe_unfused_tu(void);
+int read_and_clear_status_unfused(cudaStream_t s);
 
 // Tile geometry of the attention kernels (reported by the trace record).
 extern const int kFwdBlockQ, kFwdBlockKV;

@@ -135,3 +135,38 @@ def test_product_never_imports_the_oracle():
 def test_binding_rejects_missing_library(tmp_path):
     with pytest.raises(ImportError):
         pkg.load_library(str(tmp_path / "absent.so"))
+
+
+def test_unfused_intermediate_sizes(L):
+    s = pkg.Shape.make(2, 256, 64, 64, 24)
+    rows, n_tiles = 2 * 24 * 4352, 2 + 32
+    assert pkg.rlk_joint_attn_unfused_bytes(s, "scores") == rows * n_tiles * 128 * 4
+    assert pkg.rlk_joint_attn_unfused_bytes(s, "p") == rows * n_tiles * 128 * 2
+    assert pkg.rlk_joint_attn_unfused_bytes(s, "alpha") == rows * n_tiles * 4
+    assert pkg.rlk_joint_attn_unfused_bytes(s, "rows") == rows * 4
+    assert L.rlk_joint_attn_unfused_bytes(ctypes.byref(s), 7) == 0
+    # a ragged image side: ceil(83 * 83 / 128) = 54 image tiles, 2 text tiles
+    s2 = pkg.Shape.make(4, 256, 83, 83, 24)
+    assert pkg.rlk_joint_attn_unfused_bytes(s2, "alpha") == 4 * 24 * (256 + 83 * 83) * 56 * 4
+    bad = pkg.Shape.make(1, 16, 8, 8, 2, D=64)
+    assert pkg.rlk_joint_attn_unfused_bytes(bad, "scores") == 0
+
+
+def test_unfused_operators_fail_closed_without_a_gpu(L):
+    s = pkg.Shape.make(2, 16, 8, 8, 2)
+    p = 1 << 20
+    vl = (ctypes.c_int32 * 2)(3, 3)
+    bad_vl = (ctypes.c_int32 * 2)(3, 17)
+    assert L.rlk_qk_norm_rope(ctypes.byref(s), p, p, p, p, p, None, p, None) == 1
+    assert L.rlk_qk_norm_rope(ctypes.byref(s), p, p + 8, p, p, p, p, p, None) == 3
+    assert L.rlk_joint_attn_qk_gemm(ctypes.byref(s), p, bad_vl, p, None) == 1
+    assert L.rlk_joint_attn_qk_gemm(ctypes.byref(s), p, vl, None, None) == 1
+    assert L.rlk_joint_attn_softmax(ctypes.byref(s), p, vl, p, p, None, None, None) == 1   # l required
+    assert L.rlk_joint_attn_softmax(ctypes.byref(s), p, vl, p, p, p, p + 4, None) == 3     # lse misaligned
+    assert L.rlk_joint_attn_av_gemm(ctypes.byref(s), p, p, p, None, vl, p, None) == 1      # v required
+    assert L.rlk_joint_attn_av_gemm(ctypes.byref(s), p, p, p, p, None, p, None) == 1      # lengths required
+    bad = pkg.Shape.make(1, 16, 8, 8, 2, D=64)
+    assert L.rlk_joint_attn_qk_gemm(ctypes.byref(bad), p, vl, p, None) == 2
+    import torch
+    if not torch.cuda.is_available():
+        assert L.rlk_joint_attn_softmax(ctypes.byref(s), p, vl, p, p, p, None, None) == 5
