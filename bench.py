@@ -169,6 +169,57 @@ def kernel_work(w: W.Workload):
     }
 
 
+def unfused_work(w: W.Workload):
+    """Algorithmic HBM bytes per launch of the standalone operators: each
+    reads its inputs once and writes its outputs once; the intermediates
+    cover the key tiles each sample visits."""
+    rows = w.B * w.H * w.S
+    D = W.HEAD_DIM
+    ntq_img = -(-w.T_img // 128)
+    blocks = sum(w.H * w.S * (-(-L // 128) + ntq_img) for L in w.valid_len)  # (row, key tile) pairs
+    scores, p, alpha = blocks * 128 * 4, blocks * 128 * 2, blocks * 4
+    return {
+        "qk_gemm": 2 * rows * D * 2 + scores,
+        "softmax": scores + p + alpha + 2 * rows * 4,
+        "av_gemm": p + alpha + rows * 4 + 2 * rows * D * 2,
+    }
+
+
+def measure_unfused(pkg, ja, w, q, k, v, gains, vl, fused_out, fused_ms, peaks, n_steps):
+    """The forward as the four standalone operators (prologue, qk_gemm,
+    softmax, av_gemm): time per forward, byte equality with the fused
+    forward's output on the same inputs, and each operator's HBM rate."""
+    import torch
+    stream = torch.cuda.current_stream()
+    u = ja.forward_unfused(q, k, v, gains, vl)  # warm-up; allocates the intermediates once
+    torch.cuda.synchronize()
+    byte_equal = bool(torch.equal(u["out"].view(torch.int16), fused_out.view(torch.int16)))
+    del u
+    pkg.rlk_kernel_timing(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n_steps):
+        ja.forward_unfused(q, k, v, gains, vl)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n_steps
+    work = unfused_work(w)
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    ops = {}
+    for name in ("qk_gemm", "softmax", "av_gemm"):
+        tot, n = pkg.rlk_kernel_timing_read(name)
+        if n:
+            avg = tot / n
+            gbs = work[name] / (avg * 1e-3) / 1e9
+            ops[name] = {"avg_ms": round(avg, 4), "algorithmic_bytes": work[name], "achieved": round(gbs, 1),
+                         "unit": "GB/s", "frac": round(gbs / hbm, 4)}
+    pkg.rlk_kernel_timing(False)
+    return {"ms_per_forward": round(ms, 4), "fused_forward_ms": round(fused_ms, 4),
+            "byte_equal_to_fused": byte_equal, "steps": n_steps, "operators": ops,
+            "peak": f"hbm_gbs {hbm}"}
+
+
 def load_traffic(source_hash: str):
     """dram bytes per launch from the committed ncu summary, if it was taken
     on this exact source tree."""
@@ -313,6 +364,10 @@ def run_ours(args):
     bf16_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
 
     clocks = clk.summary()
+    unfused = None
+    if not args.no_unfused:
+        fwd_ms = sum(per_kernel[n]["avg_ms"] for n in ("rope_table", "prologue", "attn_fwd") if n in per_kernel)
+        unfused = measure_unfused(pkg, ja, w, q, k, v, gains, vl, out, fwd_ms, peaks, max(3, min(args.steps, 10)))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -333,7 +388,7 @@ def run_ours(args):
                    "credited_gflop_per_step": round(flops["fwd_bwd"] / 1e9, 2),
                    "l2": "inputs larger than L2: q,k,v,dO, ctx and workspace total "
                          f"{(4 * w.B * w.S * w.H * 128 * 2) / 1e6:.0f} MB + scratch > 129 MB L2"},
-        "roofline": roofline, "kernels": per_kernel,
+        "roofline": roofline, "kernels": per_kernel, "unfused_forward": unfused,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e},
@@ -426,6 +481,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default="cfg1024")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-unfused", action="store_true",
+                    help="skip timing the forward as the four standalone operators")
     args = ap.parse_args()
     if args.impl == "ours":
         args.warmup = max(3, args.warmup)
