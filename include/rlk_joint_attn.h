@@ -288,6 +288,52 @@ typedef struct rlk_ja_trace {
  * selected backend). */
 rlk_status rlk_joint_attn_trace(rlk_ja_trace* out);
 
+/* ---------------------------------------------------------------------------
+ * Operator trace: one record per call. The RFC's Foundation table asks for
+ * an operator trace that records the requested and actual backend, kernel
+ * identity, arithmetic policy and fallback state (qwenimage_operator_trace);
+ * the WS1 kernel list's rule 7 asks trace records to carry the reduction
+ * order, accumulator precision, Split-K / Stream-K state, TF32 state, kernel
+ * fingerprint and selected backend, and says there is no silent fallback.
+ * While tracing is on, every entry point that can launch work (the fused
+ * forward and backward, the allocation-free forward, and the standalone
+ * operators) appends one record when it returns, including calls refused
+ * during validation (status != RLK_OK, no kernel listed, actual backend
+ * "none"). The kernels listed are the ones the call enqueued, in launch
+ * order. Records live in a ring of RLK_OP_TRACE_CAP entries in host memory;
+ * the oldest is dropped first. Thread safe; nested calls (the allocation-free
+ * forward calling the regular one) produce one record. */
+#define RLK_OP_TRACE_CAP 256
+#define RLK_OP_TRACE_MAX_KERNELS 8
+
+typedef struct rlk_op_record {
+    uint64_t seq;                  /* 1, 2, ... since tracing was last enabled */
+    char op[48];                   /* WS1 row(s) the call computes */
+    char entry_point[40];          /* the C ABI function called */
+    char requested_backend[24];    /* "cuda": the library's only backend */
+    char actual_backend[24];       /* "sm_103a tcgen05", or "none" if nothing ran */
+    int32_t status;                /* rlk_status returned */
+    int32_t fallback;              /* 0: there is no fallback path */
+    int32_t split_k;               /* 0: no Split-K / Stream-K / split-KV */
+    int32_t atomics;               /* 0: no atomic accumulation */
+    int32_t tf32;                  /* 0: TF32 off */
+    int32_t n_kernels;             /* kernels enqueued (<= RLK_OP_TRACE_MAX_KERNELS) */
+    char kernels[RLK_OP_TRACE_MAX_KERNELS][32];
+    char kernel_fingerprint[96];   /* source hash of the library and its build flags */
+    char accumulator[16];          /* "fp32" */
+    char arithmetic_policy[192];   /* operand/accumulate/cast/transcendental policy */
+    char reduction_order[160];
+    int32_t B, H, T_txt, grid_h, grid_w;  /* the call's geometry (0 if the shape was null) */
+} rlk_op_record;
+
+/* Turns the operator trace on (1) or off (0); either way clears the log. */
+rlk_status rlk_op_trace_enable(int enable);
+/* Records currently kept (0 .. RLK_OP_TRACE_CAP). */
+int32_t rlk_op_trace_count(void);
+/* Copies record i (0 = oldest kept) into *out; RLK_ERR_INVALID_ARG if i is
+ * out of range or out is NULL. */
+rlk_status rlk_op_trace_read(int32_t i, rlk_op_record* out);
+
 /* Human-readable text of a status code (static storage). */
 const char* rlk_strerror(int status);
 

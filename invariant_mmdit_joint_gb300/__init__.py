@@ -25,6 +25,7 @@ __all__ = [
     "rlk_kernel_timing", "rlk_kernel_timing_read", "rlk_joint_attn_fwd_noalloc",
     "rlk_joint_attn_unfused_bytes", "rlk_qk_norm_rope", "rlk_joint_attn_qk_gemm",
     "rlk_joint_attn_softmax", "rlk_joint_attn_av_gemm", "UNFUSED", "JointAttention",
+    "rlk_op_trace_enable", "rlk_op_trace_count", "rlk_op_trace_read", "op_trace", "OP_TRACE_CAP",
     "EXPORTED_SYMBOLS", "KERNEL_IDS",
 ]
 
@@ -54,7 +55,10 @@ EXPORTED_SYMBOLS = (
     "rlk_kernel_timing", "rlk_kernel_timing_read", "rlk_joint_attn_fwd_noalloc",
     "rlk_joint_attn_unfused_bytes", "rlk_qk_norm_rope", "rlk_joint_attn_qk_gemm",
     "rlk_joint_attn_softmax", "rlk_joint_attn_av_gemm",
+    "rlk_op_trace_enable", "rlk_op_trace_count", "rlk_op_trace_read",
 )
+OP_TRACE_CAP = 256
+OP_TRACE_MAX_KERNELS = 8
 
 
 class Shape(ctypes.Structure):
@@ -93,6 +97,32 @@ class RlkError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
         super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({_strerror(code)})")
+
+
+class OpRecord(ctypes.Structure):
+    """rlk_op_record: one operator-trace record."""
+    _fields_ = [
+        ("seq", ctypes.c_uint64), ("op", ctypes.c_char * 48), ("entry_point", ctypes.c_char * 40),
+        ("requested_backend", ctypes.c_char * 24), ("actual_backend", ctypes.c_char * 24),
+        ("status", ctypes.c_int32), ("fallback", ctypes.c_int32), ("split_k", ctypes.c_int32),
+        ("atomics", ctypes.c_int32), ("tf32", ctypes.c_int32), ("n_kernels", ctypes.c_int32),
+        ("kernels", (ctypes.c_char * 32) * OP_TRACE_MAX_KERNELS), ("kernel_fingerprint", ctypes.c_char * 96),
+        ("accumulator", ctypes.c_char * 16), ("arithmetic_policy", ctypes.c_char * 192),
+        ("reduction_order", ctypes.c_char * 160), ("B", ctypes.c_int32), ("H", ctypes.c_int32),
+        ("T_txt", ctypes.c_int32), ("grid_h", ctypes.c_int32), ("grid_w", ctypes.c_int32),
+    ]
+
+    def to_dict(self) -> dict:
+        d = {}
+        for f, _ in self._fields_:
+            v = getattr(self, f)
+            if f == "kernels":
+                d[f] = [v[i].value.decode() for i in range(self.n_kernels)]
+            elif isinstance(v, bytes):
+                d[f] = v.decode()
+            else:
+                d[f] = v
+        return d
 
 
 _lib = None
@@ -148,6 +178,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     L.rlk_joint_attn_softmax.restype = i32
     L.rlk_joint_attn_av_gemm.argtypes = [shp, vp, vp, vp, vp, i32p, vp, vp]
     L.rlk_joint_attn_av_gemm.restype = i32
+    L.rlk_op_trace_enable.argtypes = [i32]
+    L.rlk_op_trace_enable.restype = i32
+    L.rlk_op_trace_count.argtypes = []
+    L.rlk_op_trace_count.restype = ctypes.c_int32
+    L.rlk_op_trace_read.argtypes = [ctypes.c_int32, ctypes.POINTER(OpRecord)]
+    L.rlk_op_trace_read.restype = i32
     return L
 
 
@@ -263,6 +299,39 @@ def rlk_joint_attn_av_gemm(shape, p, alpha, l, v, txt_valid_len, out, stream=Non
     rc = lib().rlk_joint_attn_av_gemm(ctypes.byref(shape), _ptr(p), _ptr(alpha), _ptr(l), _ptr(v),
                                       _lengths(txt_valid_len), _ptr(out), _stream_handle(stream))
     _check(rc, "rlk_joint_attn_av_gemm")
+
+
+def rlk_op_trace_enable(enable: bool) -> None:
+    _check(lib().rlk_op_trace_enable(1 if enable else 0), "rlk_op_trace_enable")
+
+
+def rlk_op_trace_count() -> int:
+    return int(lib().rlk_op_trace_count())
+
+
+def rlk_op_trace_read() -> list[dict]:
+    """Every record kept, oldest first, as dicts."""
+    out = []
+    for i in range(rlk_op_trace_count()):
+        r = OpRecord()
+        _check(lib().rlk_op_trace_read(i, ctypes.byref(r)), "rlk_op_trace_read")
+        out.append(r.to_dict())
+    return out
+
+
+class op_trace:
+    """Context manager: records every library call made inside it.
+    ``with op_trace() as t: ...``; afterwards ``t.records`` holds the records."""
+
+    def __enter__(self):
+        rlk_op_trace_enable(True)
+        self.records = []
+        return self
+
+    def __exit__(self, *exc):
+        self.records = rlk_op_trace_read()
+        rlk_op_trace_enable(False)
+        return False
 
 
 def rlk_joint_attn_check_status(stream=None) -> None:

@@ -48,13 +48,10 @@ rlk_status scratch_address(void** out) {
     return RLK_OK;
 }
 
-}  // namespace
-
-extern "C" rlk_status rlk_joint_attn_fwd_noalloc(const rlk_ja_shape* shape, const void* q, const void* k,
-                                                 const void* v, const float* g_q_txt, const float* g_k_txt,
-                                                 const float* g_q_img, const float* g_k_img,
-                                                 const int32_t* txt_valid_len, void* out, float* lse,
-                                                 void* stream) {
+rlk_status fwd_noalloc_impl(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
+                            const float* g_q_txt, const float* g_k_txt, const float* g_q_img,
+                            const float* g_k_img, const int32_t* txt_valid_len, void* out, float* lse,
+                            void* stream) {
     const size_t need = rlk_joint_attn_ctx_bytes(shape);
     if (need == 0) {
         // an invalid shape: let the regular entry point report why, without
@@ -68,4 +65,18 @@ extern "C" rlk_status rlk_joint_attn_fwd_noalloc(const rlk_ja_shape* shape, cons
     if (st != RLK_OK) return st;
     return rlk_joint_attn_fwd(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_valid_len, out, lse, scratch,
                               stream);
+}
+
+}  // namespace
+
+// One operator-trace record per call (the nested regular forward adds its
+// kernels to it).
+extern "C" rlk_status rlk_joint_attn_fwd_noalloc(const rlk_ja_shape* shape, const void* q, const void* k,
+                                                 const void* v, const float* g_q_txt, const float* g_k_txt,
+                                                 const float* g_q_img, const float* g_k_img,
+                                                 const int32_t* txt_valid_len, void* out, float* lse,
+                                                 void* stream) {
+    rlk::OpScope sc(rlk::kOpFwdNoalloc, shape);
+    return sc.finish(fwd_noalloc_impl(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_valid_len, out, lse,
+                                      stream));
 }

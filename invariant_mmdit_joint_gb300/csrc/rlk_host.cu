@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -219,9 +220,117 @@ struct Timing {
 };
 Timing g_timing;
 
+// ---- operator trace ----
+struct OpInfo {
+    const char* op;
+    const char* entry;
+    const char* policy;
+    const char* order;
+};
+constexpr const char* kFwdPolicy =
+    "bf16 q^ k^ v and bf16 P operands, fp32 TMEM accumulators, scores*log2(e)/sqrt(128) in one fmaf, "
+    "exp2f numerators, lazy max (2^8), IEEE div/sqrt, one bf16 cast of O; no TF32, no fast math";
+constexpr const char* kFwdOrder =
+    "key tiles of 128: text tiles with a valid key, then image tiles, ascending; row sums: 8 partials "
+    "by column mod 8, fixed tree";
+const OpInfo kOps[] = {
+    {"qk_rmsnorm+multi_axis_rope+joint_attention_fused", "rlk_joint_attn_fwd", kFwdPolicy, kFwdOrder},
+    {"joint_attention_fused backward", "rlk_joint_attn_bwd",
+     "bf16 operands with P and dS rounded to bf16, fp32 TMEM accumulators, exp2f numerators, dK and dQ "
+     "from the same bf16 dS, one bf16 cast of dQ dK dV; no TF32, no fast math",
+     "dK/dV: query tiles ascending; dQ: key tiles in the forward order; dg: 64-token chunks, then h, "
+     "then b ascending"},
+    {"qk_rmsnorm+multi_axis_rope+joint_attention_fused", "rlk_joint_attn_fwd_noalloc", kFwdPolicy, kFwdOrder},
+    {"qk_rmsnorm+multi_axis_rope", "rlk_qk_norm_rope",
+     "fp32 math, r = 1/sqrt(mean(x^2)+eps) with IEEE sqrt and division, fp32 cos/sin from fp64 angles, "
+     "one bf16 cast of q^ k^",
+     "sum of squares: 8 per lane in order, then xor butterfly 8,4,2,1"},
+    {"joint_attn_qk_gemm", "rlk_joint_attn_qk_gemm",
+     "bf16 q^ k^ operands, fp32 TMEM accumulators, raw scores stored fp32, -inf at masked keys",
+     "k-steps of 16 in order; key tiles in the fused order"},
+    {"joint_attn_softmax", "rlk_joint_attn_softmax", kFwdPolicy, kFwdOrder},
+    {"joint_attn_av_gemm", "rlk_joint_attn_av_gemm",
+     "bf16 P and v operands, fp32 TMEM accumulator rescaled by alpha per tile, O*(1/l), one bf16 cast",
+     "key tiles in the fused order; k-steps of 16 in order"},
+};
+const char* const kKernelNames[kNumKernelIds] = {
+    "rope_table_kernel", "prologue_kernel", "attn_fwd_tc_kernel", "bwd_pre_kernel",
+    "attn_bwd_dkdv_tc_kernel", "attn_bwd_dq_tc_kernel", "norm_rope_bwd_kernel", "dg_fold_kernels",
+    "qk_gemm_kernel", "softmax_kernel", "av_gemm_kernel"};
+
+struct OpLog {
+    std::mutex mu;
+    std::atomic<bool> on{false};
+    std::vector<rlk_op_record> ring;
+    int head = 0, count = 0;
+    uint64_t seq = 0;
+};
+OpLog g_op;
+thread_local int t_op_depth = 0;
+thread_local bool t_op_open = false;
+thread_local rlk_op_record t_op_rec;
+
+void copy_str(char* dst, size_t n, const char* src) { std::snprintf(dst, n, "%s", src); }
+
+void op_trace_kernel(int id) {
+    if (!t_op_open || id < 0 || id >= kNumKernelIds) return;
+    if (t_op_rec.n_kernels < RLK_OP_TRACE_MAX_KERNELS)
+        copy_str(t_op_rec.kernels[t_op_rec.n_kernels++], sizeof(t_op_rec.kernels[0]), kKernelNames[id]);
+    copy_str(t_op_rec.actual_backend, sizeof(t_op_rec.actual_backend), "sm_103a tcgen05");
+}
+
 }  // namespace
 
+OpScope::OpScope(OpKind kind, const rlk_ja_shape* sh) {
+    if (t_op_depth++ > 0 || !g_op.on.load()) return;
+    owner_ = true;
+    t_op_open = true;
+    rlk_op_record& r = t_op_rec;
+    std::memset(&r, 0, sizeof(r));
+    const OpInfo& info = kOps[kind];
+    copy_str(r.op, sizeof(r.op), info.op);
+    copy_str(r.entry_point, sizeof(r.entry_point), info.entry);
+    copy_str(r.requested_backend, sizeof(r.requested_backend), "cuda");
+    copy_str(r.actual_backend, sizeof(r.actual_backend), "none");
+    std::snprintf(r.kernel_fingerprint, sizeof(r.kernel_fingerprint), "%s %s", RLK_SOURCE_HASH, RLK_BUILD_FLAGS);
+    copy_str(r.accumulator, sizeof(r.accumulator), "fp32");
+    copy_str(r.arithmetic_policy, sizeof(r.arithmetic_policy), info.policy);
+    copy_str(r.reduction_order, sizeof(r.reduction_order), info.order);
+    if (sh != nullptr) {
+        r.B = sh->B;
+        r.H = sh->H;
+        r.T_txt = sh->T_txt;
+        r.grid_h = sh->grid_h;
+        r.grid_w = sh->grid_w;
+    }
+}
+
+rlk_status OpScope::finish(rlk_status st) {
+    if (owner_ && !done_) {
+        t_op_rec.status = st;
+        std::lock_guard<std::mutex> lk(g_op.mu);
+        if (g_op.on.load()) {
+            if ((int)g_op.ring.size() < RLK_OP_TRACE_CAP) g_op.ring.resize(RLK_OP_TRACE_CAP);
+            t_op_rec.seq = ++g_op.seq;
+            g_op.ring[(g_op.head + g_op.count) % RLK_OP_TRACE_CAP] = t_op_rec;
+            if (g_op.count < RLK_OP_TRACE_CAP)
+                ++g_op.count;
+            else
+                g_op.head = (g_op.head + 1) % RLK_OP_TRACE_CAP;
+        }
+        t_op_open = false;
+    }
+    done_ = true;
+    return st;
+}
+
+OpScope::~OpScope() {
+    if (owner_ && !done_) t_op_open = false;
+    --t_op_depth;
+}
+
 void timing_begin(int id, cudaStream_t s) {
+    op_trace_kernel(id);
     if (!g_timing.on) return;
     std::lock_guard<std::mutex> lk(g_timing.mu);
     const int i = g_timing.count[id];
@@ -262,7 +371,7 @@ size_t rlk_joint_attn_bwd_workspace_bytes(const rlk_ja_shape* shape) {
     return ws_layout(make_geom(shape)).total;
 }
 
-rlk_status rlk_joint_attn_fwd(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
+static rlk_status rlk_joint_attn_fwd_impl(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
                               const float* g_q_txt, const float* g_k_txt, const float* g_q_img,
                               const float* g_k_img, const int32_t* txt_valid_len, void* out, float* lse,
                               void* ctx, void* stream) {
@@ -294,7 +403,16 @@ rlk_status rlk_joint_attn_fwd(const rlk_ja_shape* shape, const void* q, const vo
     return RLK_OK;
 }
 
-rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
+rlk_status rlk_joint_attn_fwd(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
+                              const float* g_q_txt, const float* g_k_txt, const float* g_q_img,
+                              const float* g_k_img, const int32_t* txt_valid_len, void* out, float* lse,
+                              void* ctx, void* stream) {
+    OpScope sc(kOpFwd, shape);
+    return sc.finish(rlk_joint_attn_fwd_impl(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_valid_len,
+                                             out, lse, ctx, stream));
+}
+
+static rlk_status rlk_joint_attn_bwd_impl(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
                               const float* g_q_txt, const float* g_k_txt, const float* g_q_img,
                               const float* g_k_img, const int32_t* txt_valid_len, const void* out,
                               const void* dout, const float* lse, const void* ctx, void* dq, void* dk, void* dv,
@@ -350,13 +468,25 @@ rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape, const void* q, const vo
     return RLK_OK;
 }
 
+rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
+                              const float* g_q_txt, const float* g_k_txt, const float* g_q_img,
+                              const float* g_k_img, const int32_t* txt_valid_len, const void* out,
+                              const void* dout, const float* lse, const void* ctx, void* dq, void* dk, void* dv,
+                              float* dg_partial, float* dg, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+    OpScope sc(kOpBwd, shape);
+    return sc.finish(rlk_joint_attn_bwd_impl(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_valid_len,
+                                             out, dout, lse, ctx, dq, dk, dv, dg_partial, dg, workspace,
+                                             workspace_bytes, stream));
+}
+
 size_t rlk_joint_attn_unfused_bytes(const rlk_ja_shape* shape, int which) {
     rlk_status why;
     if (!shape_ok(shape, &why)) return 0;
     return unfused_bytes(make_geom(shape), which);
 }
 
-rlk_status rlk_qk_norm_rope(const rlk_ja_shape* shape, const void* q, const void* k, const float* g_q_txt,
+static rlk_status rlk_qk_norm_rope_impl(const rlk_ja_shape* shape, const void* q, const void* k, const float* g_q_txt,
                             const float* g_k_txt, const float* g_q_img, const float* g_k_img, void* ctx,
                             void* stream) {
     rlk_status why = RLK_OK;
@@ -370,7 +500,14 @@ rlk_status rlk_qk_norm_rope(const rlk_ja_shape* shape, const void* q, const void
     return run_prologue(g, q, k, gains, ctx, static_cast<cudaStream_t>(stream));
 }
 
-rlk_status rlk_joint_attn_qk_gemm(const rlk_ja_shape* shape, const void* ctx, const int32_t* txt_valid_len,
+rlk_status rlk_qk_norm_rope(const rlk_ja_shape* shape, const void* q, const void* k, const float* g_q_txt,
+                            const float* g_k_txt, const float* g_q_img, const float* g_k_img, void* ctx,
+                            void* stream) {
+    OpScope sc(kOpNormRope, shape);
+    return sc.finish(rlk_qk_norm_rope_impl(shape, q, k, g_q_txt, g_k_txt, g_q_img, g_k_img, ctx, stream));
+}
+
+static rlk_status rlk_joint_attn_qk_gemm_impl(const rlk_ja_shape* shape, const void* ctx, const int32_t* txt_valid_len,
                                   float* scores, void* stream) {
     Geom g;
     ValidLen vl;
@@ -388,7 +525,13 @@ rlk_status rlk_joint_attn_qk_gemm(const rlk_ja_shape* shape, const void* ctx, co
     return RLK_OK;
 }
 
-rlk_status rlk_joint_attn_softmax(const rlk_ja_shape* shape, const float* scores, const int32_t* txt_valid_len,
+rlk_status rlk_joint_attn_qk_gemm(const rlk_ja_shape* shape, const void* ctx, const int32_t* txt_valid_len,
+                                  float* scores, void* stream) {
+    OpScope sc(kOpQkGemm, shape);
+    return sc.finish(rlk_joint_attn_qk_gemm_impl(shape, ctx, txt_valid_len, scores, stream));
+}
+
+static rlk_status rlk_joint_attn_softmax_impl(const rlk_ja_shape* shape, const float* scores, const int32_t* txt_valid_len,
                                   void* p, float* alpha, float* l, float* lse, void* stream) {
     Geom g;
     ValidLen vl;
@@ -404,7 +547,13 @@ rlk_status rlk_joint_attn_softmax(const rlk_ja_shape* shape, const float* scores
     return RLK_OK;
 }
 
-rlk_status rlk_joint_attn_av_gemm(const rlk_ja_shape* shape, const void* p, const float* alpha, const float* l,
+rlk_status rlk_joint_attn_softmax(const rlk_ja_shape* shape, const float* scores, const int32_t* txt_valid_len,
+                                  void* p, float* alpha, float* l, float* lse, void* stream) {
+    OpScope sc(kOpSoftmax, shape);
+    return sc.finish(rlk_joint_attn_softmax_impl(shape, scores, txt_valid_len, p, alpha, l, lse, stream));
+}
+
+static rlk_status rlk_joint_attn_av_gemm_impl(const rlk_ja_shape* shape, const void* p, const float* alpha, const float* l,
                                   const void* v, const int32_t* txt_valid_len, void* out, void* stream) {
     Geom g;
     ValidLen vl;
@@ -418,6 +567,12 @@ rlk_status rlk_joint_attn_av_gemm(const rlk_ja_shape* shape, const void* p, cons
                        static_cast<uint16_t*>(out), static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return RLK_ERR_CUDA;
     return RLK_OK;
+}
+
+rlk_status rlk_joint_attn_av_gemm(const rlk_ja_shape* shape, const void* p, const float* alpha, const float* l,
+                                  const void* v, const int32_t* txt_valid_len, void* out, void* stream) {
+    OpScope sc(kOpAvGemm, shape);
+    return sc.finish(rlk_joint_attn_av_gemm_impl(shape, p, alpha, l, v, txt_valid_len, out, stream));
 }
 
 rlk_status rlk_joint_attn_check_status(void* stream) {
@@ -448,6 +603,27 @@ rlk_status rlk_joint_attn_trace(rlk_ja_trace* out) {
     out->block_q = kFwdBlockQ;
     out->block_kv = kFwdBlockKV;
     std::snprintf(out->fingerprint, sizeof(out->fingerprint), "%s %s", RLK_SOURCE_HASH, RLK_BUILD_FLAGS);
+    return RLK_OK;
+}
+
+rlk_status rlk_op_trace_enable(int enable) {
+    std::lock_guard<std::mutex> lk(g_op.mu);
+    g_op.on.store(enable != 0);
+    g_op.head = g_op.count = 0;
+    g_op.seq = 0;
+    return RLK_OK;
+}
+
+int32_t rlk_op_trace_count(void) {
+    std::lock_guard<std::mutex> lk(g_op.mu);
+    return g_op.count;
+}
+
+rlk_status rlk_op_trace_read(int32_t i, rlk_op_record* out) {
+    if (out == nullptr) return RLK_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_op.mu);
+    if (i < 0 || i >= g_op.count) return RLK_ERR_INVALID_ARG;
+    *out = g_op.ring[(g_op.head + i) % RLK_OP_TRACE_CAP];
     return RLK_OK;
 }
 

@@ -57,8 +57,24 @@ enum KernelId {
 };
 
 // Launch timing hooks (rlk_host.cu): bracket one launch with events.
+// timing_begin also adds the kernel to the open operator-trace record.
 void timing_begin(int kernel_id, cudaStream_t s);
 void timing_end(int kernel_id, cudaStream_t s);
+
+// Operator trace (rlk_host.cu). Every C ABI entry point that can launch work
+// opens a scope; the outermost scope of a thread owns one record, which the
+// launches inside it fill and finish() appends to the log.
+enum OpKind { kOpFwd = 0, kOpBwd, kOpFwdNoalloc, kOpNormRope, kOpQkGemm, kOpSoftmax, kOpAvGemm };
+class OpScope {
+   public:
+    OpScope(OpKind kind, const rlk_ja_shape* shape);
+    ~OpScope();
+    rlk_status finish(rlk_status st);
+
+   private:
+    bool owner_ = false;
+    bool done_ = false;
+};
 
 // ---- launchers (each returns the cudaGetLastError() of its launch) ----
 // k_prologue.cu

@@ -170,3 +170,102 @@ def test_unfused_operators_fail_closed_without_a_gpu(L):
     import torch
     if not torch.cuda.is_available():
         assert L.rlk_joint_attn_softmax(ctypes.byref(s), p, vl, p, p, p, None, None) == 5
+
+
+def test_op_trace_records_refused_calls(L):
+    s = pkg.Shape.make(2, 16, 8, 8, 2)
+    p = 1 << 20
+    vl = (ctypes.c_int32 * 2)(3, 5)
+    bad_vl = (ctypes.c_int32 * 2)(3, 17)
+    pkg.rlk_op_trace_enable(True)
+    try:
+        assert L.rlk_joint_attn_qk_gemm(ctypes.byref(s), p, bad_vl, p, None) == 1
+        assert L.rlk_joint_attn_softmax(ctypes.byref(s), p, vl, p, p, None, None, None) == 1
+        assert L.rlk_joint_attn_av_gemm(ctypes.byref(s), p, p, p, p, vl, p + 8, None) == 3
+        assert L.rlk_qk_norm_rope(None, p, p, p, p, p, p, p, None) == 1
+        assert _fwd(L, s, [3, 3], q=None) == 1
+        big = pkg.Shape.make(2, 256, 64, 64, 24)  # context beyond the fixed scratch
+        assert L.rlk_joint_attn_fwd_noalloc(ctypes.byref(big), p, p, p, p, p, p, p, vl, p, p, None) == 4
+        recs = pkg.rlk_op_trace_read()
+    finally:
+        pkg.rlk_op_trace_enable(False)
+    assert [r["entry_point"] for r in recs] == [
+        "rlk_joint_attn_qk_gemm", "rlk_joint_attn_softmax", "rlk_joint_attn_av_gemm", "rlk_qk_norm_rope",
+        "rlk_joint_attn_fwd", "rlk_joint_attn_fwd_noalloc"]
+    assert [r["status"] for r in recs] == [1, 1, 3, 1, 1, 4]
+    assert [r["seq"] for r in recs] == [1, 2, 3, 4, 5, 6]
+    for r in recs:
+        # nothing was enqueued and there is no other path to fall back to
+        assert r["actual_backend"] == "none" and r["kernels"] == [] and r["fallback"] == 0
+        assert r["requested_backend"] == "cuda"
+        assert r["split_k"] == 0 and r["atomics"] == 0 and r["tf32"] == 0 and r["accumulator"] == "fp32"
+        assert "-prec-div=true" in r["kernel_fingerprint"] and r["reduction_order"] and r["arithmetic_policy"]
+    assert recs[0]["op"] == "joint_attn_qk_gemm" and (recs[0]["B"], recs[0]["T_txt"]) == (2, 16)
+    assert recs[3]["B"] == 0  # no shape given
+    assert recs[5]["B"] == 2 and recs[5]["grid_h"] == 64
+    assert "no fast math" in recs[4]["arithmetic_policy"]
+    # off: nothing is recorded, and enabling clears the log
+    assert _fwd(L, s, [3, 3], q=None) == 1
+    assert pkg.rlk_op_trace_count() == 0
+
+
+def test_op_trace_ring_keeps_the_newest_records(L):
+    s = pkg.Shape.make(1, 16, 8, 8, 2)
+    bad = (ctypes.c_int32 * 1)(99)
+    n = pkg.OP_TRACE_CAP + 44
+    with pkg.op_trace() as t:
+        for _ in range(n):
+            assert L.rlk_joint_attn_qk_gemm(ctypes.byref(s), 1 << 20, bad, 1 << 20, None) == 1
+    assert len(t.records) == pkg.OP_TRACE_CAP
+    assert t.records[0]["seq"] == n - pkg.OP_TRACE_CAP + 1 and t.records[-1]["seq"] == n
+    rec = pkg.OpRecord()
+    pkg.rlk_op_trace_enable(True)
+    try:
+        assert L.rlk_op_trace_read(0, ctypes.byref(rec)) == 1   # empty log
+        assert L.rlk_op_trace_read(-1, ctypes.byref(rec)) == 1
+        assert L.rlk_op_trace_read(0, None) == 1
+    finally:
+        pkg.rlk_op_trace_enable(False)
+
+
+def test_op_trace_is_whole_per_call_across_threads(L):
+    import threading
+    s = pkg.Shape.make(1, 16, 8, 8, 2)
+    p = 1 << 20
+
+    def worker(kind):
+        vl = (ctypes.c_int32 * 1)(99)
+        for _ in range(50):
+            if kind == 0:
+                L.rlk_joint_attn_qk_gemm(ctypes.byref(s), p, vl, p, None)
+            else:
+                L.rlk_joint_attn_av_gemm(ctypes.byref(s), p, p, p, p, vl, p, None)
+
+    with pkg.op_trace() as t:
+        ths = [threading.Thread(target=worker, args=(i % 2,)) for i in range(4)]
+        for th in ths:
+            th.start()
+        for th in ths:
+            th.join()
+    assert len(t.records) == 200
+    assert sorted(r["seq"] for r in t.records) == list(range(1, 201))
+    for r in t.records:
+        assert r["op"] == r["entry_point"].replace("rlk_", "") and r["status"] == 1
+
+
+def test_op_record_layout_matches_the_header(tmp_path):
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "rlk_joint_attn.h"\n'
+        'int main(void) { printf("%zu %zu %zu %zu\\n", sizeof(rlk_op_record), offsetof(rlk_op_record, kernels), '
+        'offsetof(rlk_op_record, arithmetic_policy), offsetof(rlk_op_record, grid_w)); return 0; }\n')
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", HEADER_DIR, str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    R = pkg.OpRecord
+    assert got == [ctypes.sizeof(R), R.kernels.offset, R.arithmetic_policy.offset, R.grid_w.offset]
