@@ -289,6 +289,38 @@ typedef struct rlk_ja_trace {
 rlk_status rlk_joint_attn_trace(rlk_ja_trace* out);
 
 /* ---------------------------------------------------------------------------
+ * The fused forward over one key shard, for ring-ordered sequence
+ * parallelism. The RFC's WS2 table asks sp_attention_ring for a "fixed
+ * global block and partial-state merge order", and its numerical
+ * requirements ask strict replay and topology invariance to keep byte
+ * equality. Here the global blocks are the forward's own key tiles (column
+ * block t = key tile t: text tiles from token 0, then image tiles from token
+ * T_txt, 128 keys each; n_tiles = ceil(T_txt/128) + ceil(grid_h*grid_w/128)),
+ * and the partial state -- per query row the running reference maximum m,
+ * the row sum l and the unnormalised output O -- is handed from shard to
+ * shard in ascending block order. Any split of [0, n_tiles) into shards
+ * [b_0 = 0, b_1), [b_1, b_2), ..., [b_k, n_tiles), run in that order, gives
+ * `out` and `lse` bytes identical to rlk_joint_attn_fwd() (one GPU emulates
+ * what ranks holding consecutive key shards would do).
+ *   ctx           as written by rlk_qk_norm_rope() or the forward
+ *   v             device bf16 [B, S, H, D]
+ *   blk_begin, blk_end   the shard, 0 <= blk_begin < blk_end <= n_tiles
+ *   state_in      the previous shard's state_out; NULL iff blk_begin == 0
+ *   state_out     rlk_joint_attn_state_bytes() bytes; NULL iff this is the
+ *                 last shard (blk_end == n_tiles). It may equal state_in.
+ *   out, lse      written by the last shard only (out required there, lse
+ *                 optional); NULL for the others
+ * The state is opaque: fp32 m (log2 units) [B, H, S], l [B, H, S], then
+ * O [B, H, S, D]. Text blocks past a sample's valid keys are skipped as in
+ * the fused forward; a shard with no valid key for a sample passes its
+ * state through. */
+size_t rlk_joint_attn_state_bytes(const rlk_ja_shape* shape);
+rlk_status rlk_joint_attn_fwd_shard(const rlk_ja_shape* shape, const void* ctx, const void* v,
+                                    const int32_t* txt_valid_len, int32_t blk_begin,
+                                    int32_t blk_end, const float* state_in, float* state_out,
+                                    void* out, float* lse, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Operator trace: one record per call. The RFC's Foundation table asks for
  * an operator trace that records the requested and actual backend, kernel
  * identity, arithmetic policy and fallback state (qwenimage_operator_trace);
@@ -296,8 +328,8 @@ rlk_status rlk_joint_attn_trace(rlk_ja_trace* out);
  * order, accumulator precision, Split-K / Stream-K state, TF32 state, kernel
  * fingerprint and selected backend, and says there is no silent fallback.
  * While tracing is on, every entry point that can launch work (the fused
- * forward and backward, the allocation-free forward, and the standalone
- * operators) appends one record when it returns, including calls refused
+ * forward and backward, the allocation-free forward, the key-shard forward
+ * and the standalone operators) appends one record when it returns, including calls refused
  * during validation (status != RLK_OK, no kernel listed, actual backend
  * "none"). The kernels listed are the ones the call enqueued, in launch
  * order. Records live in a ring of RLK_OP_TRACE_CAP entries in host memory;
@@ -340,7 +372,7 @@ const char* rlk_strerror(int status);
 /* Kernel timing for benchmarks. kernel ids: 0 rope table, 1 prologue,
  * 2 attention forward, 3 backward preprocess, 4 dK/dV, 5 dQ,
  * 6 RoPE/RMSNorm backward, 7 gain-gradient fold, 8 qk_gemm, 9 softmax,
- * 10 av_gemm.
+ * 10 av_gemm, 11 forward key shard.
  * rlk_kernel_timing(1) makes later calls record a CUDA event pair around
  * every launch (up to 4096 launches per kernel id); rlk_kernel_timing(0)
  * stops and clears. rlk_kernel_timing_read() waits for the recorded events

@@ -26,6 +26,7 @@ __all__ = [
     "rlk_joint_attn_unfused_bytes", "rlk_qk_norm_rope", "rlk_joint_attn_qk_gemm",
     "rlk_joint_attn_softmax", "rlk_joint_attn_av_gemm", "UNFUSED", "JointAttention",
     "rlk_op_trace_enable", "rlk_op_trace_count", "rlk_op_trace_read", "op_trace", "OP_TRACE_CAP",
+    "rlk_joint_attn_state_bytes", "rlk_joint_attn_fwd_shard",
     "EXPORTED_SYMBOLS", "KERNEL_IDS",
 ]
 
@@ -43,7 +44,7 @@ STATUS_NAMES = {
 KERNEL_IDS = {
     "rope_table": 0, "prologue": 1, "attn_fwd": 2, "bwd_pre": 3,
     "bwd_dkdv": 4, "bwd_dq": 5, "norm_rope_bwd": 6, "dg_fold": 7,
-    "qk_gemm": 8, "softmax": 9, "av_gemm": 10,
+    "qk_gemm": 8, "softmax": 9, "av_gemm": 10, "attn_fwd_shard": 11,
 }
 # which intermediate rlk_joint_attn_unfused_bytes() sizes
 UNFUSED = {"scores": 0, "p": 1, "alpha": 2, "rows": 3}
@@ -56,6 +57,7 @@ EXPORTED_SYMBOLS = (
     "rlk_joint_attn_unfused_bytes", "rlk_qk_norm_rope", "rlk_joint_attn_qk_gemm",
     "rlk_joint_attn_softmax", "rlk_joint_attn_av_gemm",
     "rlk_op_trace_enable", "rlk_op_trace_count", "rlk_op_trace_read",
+    "rlk_joint_attn_state_bytes", "rlk_joint_attn_fwd_shard",
 )
 OP_TRACE_CAP = 256
 OP_TRACE_MAX_KERNELS = 8
@@ -178,6 +180,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     L.rlk_joint_attn_softmax.restype = i32
     L.rlk_joint_attn_av_gemm.argtypes = [shp, vp, vp, vp, vp, i32p, vp, vp]
     L.rlk_joint_attn_av_gemm.restype = i32
+    L.rlk_joint_attn_state_bytes.argtypes = [shp]
+    L.rlk_joint_attn_state_bytes.restype = sz
+    L.rlk_joint_attn_fwd_shard.argtypes = [shp, vp, vp, i32p, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp, vp]
+    L.rlk_joint_attn_fwd_shard.restype = i32
     L.rlk_op_trace_enable.argtypes = [i32]
     L.rlk_op_trace_enable.restype = i32
     L.rlk_op_trace_count.argtypes = []
@@ -299,6 +305,20 @@ def rlk_joint_attn_av_gemm(shape, p, alpha, l, v, txt_valid_len, out, stream=Non
     rc = lib().rlk_joint_attn_av_gemm(ctypes.byref(shape), _ptr(p), _ptr(alpha), _ptr(l), _ptr(v),
                                       _lengths(txt_valid_len), _ptr(out), _stream_handle(stream))
     _check(rc, "rlk_joint_attn_av_gemm")
+
+
+def rlk_joint_attn_state_bytes(shape: Shape) -> int:
+    return int(lib().rlk_joint_attn_state_bytes(ctypes.byref(shape)))
+
+
+def rlk_joint_attn_fwd_shard(shape, ctx, v, txt_valid_len, blk_begin, blk_end, state_in, state_out, out, lse,
+                             stream=None) -> None:
+    """Enqueue the forward over key column blocks [blk_begin, blk_end),
+    handing the online-softmax state on (see the header)."""
+    rc = lib().rlk_joint_attn_fwd_shard(ctypes.byref(shape), _ptr(ctx), _ptr(v), _lengths(txt_valid_len),
+                                        int(blk_begin), int(blk_end), _ptr(state_in), _ptr(state_out), _ptr(out),
+                                        _ptr(lse), _stream_handle(stream))
+    _check(rc, "rlk_joint_attn_fwd_shard")
 
 
 def rlk_op_trace_enable(enable: bool) -> None:
@@ -451,6 +471,32 @@ class JointAttention:
         rlk_joint_attn_softmax(sh, scores, valid_len, p, alpha, l, lse, stream)
         rlk_joint_attn_av_gemm(sh, p, alpha, l, v, valid_len, out, stream)
         return {"out": out, "lse": lse, "l": l, "scores": scores, "p": p, "alpha": alpha}
+
+    def n_key_blocks(self) -> int:
+        sh = self.shape
+        return -(-sh.T_txt // 128) + -(-(sh.grid_h * sh.grid_w) // 128)
+
+    def forward_sharded(self, q, k, v, gains, valid_len, bounds, stream=None):
+        """The forward run as consecutive key shards handing the softmax
+        state on (ring order). ``bounds`` are the shard boundaries inside
+        (0, n_key_blocks()), ascending. Returns out and lse."""
+        import torch
+        self._check_inputs(q, k, v)
+        self._check_gains(gains)
+        sh = self.shape
+        edges = [0] + [int(x) for x in bounds] + [self.n_key_blocks()]
+        out = torch.empty_like(q)
+        lse = torch.empty((sh.B, sh.H, sh.S), dtype=torch.float32, device=self.device)
+        n_state = rlk_joint_attn_state_bytes(sh) // 4
+        states = [torch.empty(n_state, dtype=torch.float32, device=self.device) for _ in range(2)]
+        rlk_qk_norm_rope(sh, q, k, gains[0], gains[1], gains[2], gains[3], self.ctx, stream)
+        for i in range(len(edges) - 1):
+            last = i == len(edges) - 2
+            st_in = None if i == 0 else states[(i - 1) % 2]
+            st_out = None if last else states[i % 2]
+            rlk_joint_attn_fwd_shard(sh, self.ctx, v, valid_len, edges[i], edges[i + 1], st_in, st_out,
+                                     out if last else None, lse if last else None, stream)
+        return out, lse
 
     def ctx_views(self):
         """Views of the forward context: qh, kh bf16 [B, H, S, 128]; rq, rk fp32 [B, H, S].

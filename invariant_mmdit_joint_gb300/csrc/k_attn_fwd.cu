@@ -66,6 +66,18 @@ struct FwdArgs {
     uint16_t* out;       // [B, S, H, 128]
     float* lse;          // [B, H, S] or null
     CUtensorMap map_o[2];  // out per segment (0 text, 1 image): rows past a segment are clipped
+    // key shard (kShard launches): column blocks [blk_begin, blk_end) of the
+    // fused order, the online-softmax state handed in by the previous shard
+    // (null for the first) and handed on to the next one (null for the
+    // last, which writes out and lse instead). State per query row: m (log2
+    // units) and l fp32 [B, H, S], O fp32 [B, H, S, 128] (not yet divided by l).
+    int blk_begin, blk_end;
+    const float* st_in_m;
+    const float* st_in_l;
+    const float* st_in_o;
+    float* st_out_m;
+    float* st_out_l;
+    float* st_out_o;
 };
 
 struct TileInfo {
@@ -92,6 +104,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitLimitNs));
 }
 
+template <bool kShard>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ FwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[16];
@@ -112,8 +125,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
     const int q0[2] = {seg0 + first * kBM, seg0 + (first + 1) * kBM};
     const int L = a.vl.L[b];
     const int nkt_txt = (L + kBN - 1) / kBN;
-    const int nkt = nkt_txt + g.ntq_img;
+    const int nkt_all = nkt_txt + g.ntq_img;
+    // tiles j0 .. j0 + nkt - 1 of the fused order run here; the loops below
+    // count j locally (barrier phases, buffer slots) and name the tile j0 + j
+    int j0 = 0, nkt = nkt_all;
+    if (kShard) {
+        auto fused_index = [&](int blk) { return blk < g.ntq_txt ? min(blk, nkt_txt) : nkt_txt + (blk - g.ntq_txt); };
+        j0 = fused_index(a.blk_begin);
+        nkt = fused_index(a.blk_end) - j0;
+    }
+    const bool last_shard = !kShard || j0 + nkt == nkt_all;
     const int row_base = (b * g.H + h) * g.S;  // first row of this (b, h) in qh / kh
+    if (kShard && nkt == 0) {
+        // no tile of this shard holds a valid key of this sample: the state
+        // passes through unchanged (or starts empty)
+        const size_t bh = (size_t)b * g.H + h;
+        for (int i = threadIdx.x; i < 2 * kBM; i += kThreads) {
+            const int n = q0[i >> 7] + (i & 127);
+            if (!(i < kBM || has_b) || n >= q_end) continue;
+            const size_t rowi = bh * g.S + n;
+            const bool have = a.st_in_m != nullptr && j0 > 0;
+            a.st_out_m[rowi] = have ? a.st_in_m[rowi] : -INFINITY;
+            a.st_out_l[rowi] = have ? a.st_in_l[rowi] : 0.0f;
+            for (int d = 0; d < kHeadDim; ++d)
+                a.st_out_o[rowi * kHeadDim + d] = have ? a.st_in_o[rowi * kHeadDim + d] : 0.0f;
+        }
+        return;
+    }
 
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sQ = sbase + kSmemQ, sK = sbase + kSmemK, sV = sbase + kSmemV;
@@ -169,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                     fail(&abort_flag);
                     break;
                 }
-                const TileInfo ti = kv_tile(g, L, nkt_txt, j);
+                const TileInfo ti = kv_tile(g, L, nkt_txt, j0 + j);
                 const uint32_t dk = sK + s * kTileBytes, dv = sV + s * kTileBytes;
                 mbar_expect_tx(bar_kf + 8 * s, kTileBytes);
                 tma_load_2d(dk, &a.map_k, bar_kf + 8 * s, 0, row_base + ti.k0);
@@ -215,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tmem + 256 * t + 128, tmem + 256 * t + kk * 8, sdesc_sw128(dv + kk * 2048, kBoxBytes, 1024),
-                           idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                           idesc_o, (j0 + j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar_o + 8 * t);
             };
             bool ok = mbar_wait(bar_q, 0, &abort_flag, kWaitLimitNs) &&
@@ -278,6 +316,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
         const uint32_t o_tmem = s_tmem + 128;
         const int row = (warp & 3) * 32 + lane;
         float m = -INFINITY, l = 0.0f;
+        // this row's slot in a shard state (rows past the segment read a
+        // valid row and write nothing)
+        const size_t rowi = ((size_t)b * g.H + h) * g.S + min(q0[t] + row, q_end - 1);
+        if (kShard && j0 > 0) {
+            m = a.st_in_m[rowi];
+            l = a.st_in_l[rowi];
+        }
         bool ok = true;
         for (int j = 0; j < nkt; ++j) {
             if (!warp_wait(bar_s + 8 * t, j & 1, &abort_flag)) {
@@ -285,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                 break;
             }
             tc_fence_after();
-            const TileInfo ti = kv_tile(g, L, nkt_txt, j);
+            const TileInfo ti = kv_tile(g, L, nkt_txt, j0 + j);
             const int nvalid = ti.kend - ti.k0;  // keys k0 + c with c < nvalid are valid
             // the row's 128 scores in one register array, loaded at once;
             // the packed P later reuses its first 64 entries in place
@@ -354,12 +399,51 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                         tmem_st32(o_tmem + 32 * c, o32);
                     }
                 }
+            } else if (kShard && j0 > 0) {
+                // first tile of a later shard: O is the previous shard's,
+                // scaled by alpha as above (alpha is exactly 1 in rows whose
+                // reference max stays, so those keep their bits)
+                uint32_t (&o32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[64]);
+                const float4* oin = reinterpret_cast<const float4*>(a.st_in_o + rowi * kHeadDim);
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 x = oin[8 * c + i];
+                        o32[4 * i] = __float_as_uint(x.x * alpha);
+                        o32[4 * i + 1] = __float_as_uint(x.y * alpha);
+                        o32[4 * i + 2] = __float_as_uint(x.z * alpha);
+                        o32[4 * i + 3] = __float_as_uint(x.w * alpha);
+                    }
+                    tmem_st32(o_tmem + 32 * c, o32);
+                }
             }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_p + 8 * t);
         }
-        if (ok && warp_wait(bar_o + 8 * t, (nkt - 1) & 1, &abort_flag)) {
+        if (ok && !last_shard && warp_wait(bar_o + 8 * t, (nkt - 1) & 1, &abort_flag)) {
+            tc_fence_after();
+            // hand the state on: m, l and O (not divided by l), fp32
+            const bool mine = q0[t] + row < q_end;
+            if (mine) {
+                a.st_out_m[rowi] = m;
+                a.st_out_l[rowi] = l;
+            }
+            float4* oout = reinterpret_cast<float4*>(a.st_out_o + rowi * kHeadDim);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld32(o_tmem + 32 * c, r);
+                tmem_ld_wait();
+                if (mine) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        oout[8 * c + i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                      __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                }
+            }
+        } else if (ok && last_shard && warp_wait(bar_o + 8 * t, (nkt - 1) & 1, &abort_flag)) {
             tc_fence_after();
             // O / l as bf16 into this tile's Q buffer (its last S product has
             // finished) as two 128-row x 128-byte boxes in the 128-byte
@@ -423,13 +507,57 @@ cudaError_t launch_attn_fwd(const Geom& g, const ValidLen& vl, const uint16_t* q
     local.vl = vl;
     local.out = out;
     local.lse = lse;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    local.blk_begin = 0;
+    local.blk_end = g.ntq_txt + g.ntq_img;
+    local.st_in_m = local.st_in_l = local.st_in_o = nullptr;
+    local.st_out_m = local.st_out_l = local.st_out_o = nullptr;
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
     if (e != cudaSuccess) return e;
     const int npairs = (g.ntq_txt + 1) / 2 + (g.ntq_img + 1) / 2;
     dim3 grid(npairs, g.H, g.B);
     timing_begin(kKAttnFwd, s);
-    attn_fwd_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(local);
+    attn_fwd_tc_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(local);
     timing_end(kKAttnFwd, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_fwd_shard(const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
+                                  const uint16_t* v, int blk_begin, int blk_end, const float* state_in,
+                                  float* state_out, uint16_t* out, float* lse, cudaStream_t s) {
+    FwdArgs local;
+    const uint64_t rows = (uint64_t)g.B * g.H * g.S;
+    if (!tmap::rows_bf16(&local.map_q, qh, rows) || !tmap::rows_bf16(&local.map_k, kh, rows) ||
+        !tmap::bshd_bf16(&local.map_v, v, g))
+        return cudaErrorInvalidValue;
+    // only the last shard writes out (its maps are unused elsewhere)
+    if (out != nullptr) {
+        if (!tmap::bshd_bf16(&local.map_o[0], out, g, 0) || !tmap::bshd_bf16(&local.map_o[1], out, g, 1))
+            return cudaErrorInvalidValue;
+    } else {
+        memset(local.map_o, 0, sizeof(local.map_o));
+    }
+    local.g = g;
+    local.vl = vl;
+    local.out = out;
+    local.lse = lse;
+    local.blk_begin = blk_begin;
+    local.blk_end = blk_end;
+    // state layout: m [rows], l [rows], O [rows, 128]
+    local.st_in_m = state_in;
+    local.st_in_l = state_in != nullptr ? state_in + rows : nullptr;
+    local.st_in_o = state_in != nullptr ? state_in + 2 * rows : nullptr;
+    local.st_out_m = state_out;
+    local.st_out_l = state_out != nullptr ? state_out + rows : nullptr;
+    local.st_out_o = state_out != nullptr ? state_out + 2 * rows : nullptr;
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int npairs = (g.ntq_txt + 1) / 2 + (g.ntq_img + 1) / 2;
+    dim3 grid(npairs, g.H, g.B);
+    timing_begin(kKAttnFwdShard, s);
+    attn_fwd_tc_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(local);
+    timing_end(kKAttnFwdShard, s);
     return cudaGetLastError();
 }
 

@@ -252,11 +252,14 @@ const OpInfo kOps[] = {
     {"joint_attn_av_gemm", "rlk_joint_attn_av_gemm",
      "bf16 P and v operands, fp32 TMEM accumulator rescaled by alpha per tile, O*(1/l), one bf16 cast",
      "key tiles in the fused order; k-steps of 16 in order"},
+    {"joint_attention_fused key shard", "rlk_joint_attn_fwd_shard", kFwdPolicy,
+     "key tiles of 128 in the fused order, shards in ascending block order, the online-softmax state "
+     "handed from shard to shard"},
 };
 const char* const kKernelNames[kNumKernelIds] = {
     "rope_table_kernel", "prologue_kernel", "attn_fwd_tc_kernel", "bwd_pre_kernel",
     "attn_bwd_dkdv_tc_kernel", "attn_bwd_dq_tc_kernel", "norm_rope_bwd_kernel", "dg_fold_kernels",
-    "qk_gemm_kernel", "softmax_kernel", "av_gemm_kernel"};
+    "qk_gemm_kernel", "softmax_kernel", "av_gemm_kernel", "attn_fwd_tc_kernel<shard>"};
 
 struct OpLog {
     std::mutex mu;
@@ -573,6 +576,51 @@ rlk_status rlk_joint_attn_av_gemm(const rlk_ja_shape* shape, const void* p, cons
                                   const void* v, const int32_t* txt_valid_len, void* out, void* stream) {
     OpScope sc(kOpAvGemm, shape);
     return sc.finish(rlk_joint_attn_av_gemm_impl(shape, p, alpha, l, v, txt_valid_len, out, stream));
+}
+
+size_t rlk_joint_attn_state_bytes(const rlk_ja_shape* shape) {
+    rlk_status why;
+    if (!shape_ok(shape, &why)) return 0;
+    const Geom g = make_geom(shape);
+    return (size_t)g.B * g.H * g.S * (2 + kHeadDim) * sizeof(float);
+}
+
+static rlk_status rlk_joint_attn_fwd_shard_impl(const rlk_ja_shape* shape, const void* ctx, const void* v,
+                                                const int32_t* txt_valid_len, int32_t blk_begin, int32_t blk_end,
+                                                const float* state_in, float* state_out, void* out, float* lse,
+                                                void* stream) {
+    Geom g;
+    ValidLen vl;
+    rlk_status st = common_checks(shape, txt_valid_len, &g, &vl);
+    if (st != RLK_OK) return st;
+    const int nblk = g.ntq_txt + g.ntq_img;
+    if (blk_begin < 0 || blk_end > nblk || blk_begin >= blk_end) return RLK_ERR_INVALID_ARG;
+    const bool first = blk_begin == 0, last = blk_end == nblk;
+    // the state comes in unless this is the first shard and goes on unless
+    // it is the last, which writes out (and lse if given)
+    if ((state_in == nullptr) != first || (state_out == nullptr) != last || (out == nullptr) != !last ||
+        (lse != nullptr && !last))
+        return RLK_ERR_INVALID_ARG;
+    st = check_ptrs({ctx, v}, {state_in, state_out, out, lse});
+    if (st != RLK_OK) return st;
+    st = device_ok();
+    if (st != RLK_OK) return st;
+    const CtxLayout l = ctx_layout(g);
+    const uint8_t* c = static_cast<const uint8_t*>(ctx);
+    if (launch_attn_fwd_shard(g, vl, reinterpret_cast<const uint16_t*>(c + l.qh),
+                              reinterpret_cast<const uint16_t*>(c + l.kh), static_cast<const uint16_t*>(v), blk_begin,
+                              blk_end, state_in, state_out, static_cast<uint16_t*>(out), lse,
+                              static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status rlk_joint_attn_fwd_shard(const rlk_ja_shape* shape, const void* ctx, const void* v,
+                                    const int32_t* txt_valid_len, int32_t blk_begin, int32_t blk_end,
+                                    const float* state_in, float* state_out, void* out, float* lse, void* stream) {
+    OpScope sc(kOpFwdShard, shape);
+    return sc.finish(rlk_joint_attn_fwd_shard_impl(shape, ctx, v, txt_valid_len, blk_begin, blk_end, state_in,
+                                                   state_out, out, lse, stream));
 }
 
 rlk_status rlk_joint_attn_check_status(void* stream) {

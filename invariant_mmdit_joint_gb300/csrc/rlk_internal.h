@@ -53,7 +53,7 @@ __host__ __device__ inline int pair_axis(int k) {
 enum KernelId {
     kKRopeTable = 0, kKPrologue = 1, kKAttnFwd = 2, kKBwdPre = 3,
     kKBwdDkDv = 4, kKBwdDq = 5, kKNormRopeBwd = 6, kKDgFold = 7,
-    kKQkGemm = 8, kKSoftmax = 9, kKAvGemm = 10, kNumKernelIds = 11
+    kKQkGemm = 8, kKSoftmax = 9, kKAvGemm = 10, kKAttnFwdShard = 11, kNumKernelIds = 12
 };
 
 // Launch timing hooks (rlk_host.cu): bracket one launch with events.
@@ -64,7 +64,7 @@ void timing_end(int kernel_id, cudaStream_t s);
 // Operator trace (rlk_host.cu). Every C ABI entry point that can launch work
 // opens a scope; the outermost scope of a thread owns one record, which the
 // launches inside it fill and finish() appends to the log.
-enum OpKind { kOpFwd = 0, kOpBwd, kOpFwdNoalloc, kOpNormRope, kOpQkGemm, kOpSoftmax, kOpAvGemm };
+enum OpKind { kOpFwd = 0, kOpBwd, kOpFwdNoalloc, kOpNormRope, kOpQkGemm, kOpSoftmax, kOpAvGemm, kOpFwdShard };
 class OpScope {
    public:
     OpScope(OpKind kind, const rlk_ja_shape* shape);
@@ -99,6 +99,13 @@ int probe_prologue_tu(void);
 cudaError_t launch_attn_fwd(const Geom& g, const ValidLen& vl, const uint16_t* qh,
                             const uint16_t* kh, const uint16_t* v, uint16_t* out,
                             float* lse, cudaStream_t s);
+// One key shard of the forward: column blocks [blk_begin, blk_end) of the
+// fused order, with the online-softmax state passed from and to the
+// neighbouring shards (state: m, l fp32 [rows] then O fp32 [rows, 128]).
+cudaError_t launch_attn_fwd_shard(const Geom& g, const ValidLen& vl, const uint16_t* qh,
+                                  const uint16_t* kh, const uint16_t* v, int blk_begin, int blk_end,
+                                  const float* state_in, float* state_out, uint16_t* out, float* lse,
+                                  cudaStream_t s);
 int probe_fwd_tu(void);
 int read_and_clear_status_fwd(cudaStream_t s);
 

@@ -269,3 +269,25 @@ def test_op_record_layout_matches_the_header(tmp_path):
     got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
     R = pkg.OpRecord
     assert got == [ctypes.sizeof(R), R.kernels.offset, R.arithmetic_policy.offset, R.grid_w.offset]
+
+
+def test_key_shard_forward_fails_closed(L):
+    s = pkg.Shape.make(2, 200, 13, 21, 2)  # 2 text + 3 image key blocks
+    assert pkg.rlk_joint_attn_state_bytes(s) == 2 * 2 * (200 + 273) * (2 + 128) * 4
+    p = 1 << 20
+    vl = (ctypes.c_int32 * 2)(3, 150)
+
+    def shard(b0, b1, st_in=p, st_out=p, out=None, lse=None, ctx=p, lens=vl):
+        return L.rlk_joint_attn_fwd_shard(ctypes.byref(s), ctx, p, lens, b0, b1, st_in, st_out, out, lse, None)
+    assert shard(2, 2) == 1                       # empty shard
+    assert shard(3, 6, st_out=None, out=p) == 1   # past the last block
+    assert shard(0, 2) == 1                       # the first shard takes no state
+    assert shard(1, 3, st_in=None) == 1           # a later shard needs one
+    assert shard(1, 5, st_out=p, out=p) == 1      # the last shard hands no state on...
+    assert shard(1, 5, st_out=None) == 1          # ...and writes out
+    assert shard(1, 3, lse=p) == 1                # only the last shard writes lse
+    assert shard(1, 3, st_out=p + 4) == 3         # misaligned state
+    assert shard(1, 3, lens=(ctypes.c_int32 * 2)(3, 201)) == 1
+    import torch
+    if not torch.cuda.is_available():
+        assert shard(0, 2, st_in=None) == 5 and shard(2, 5, st_out=None, out=p, lse=p) == 5
