@@ -39,15 +39,15 @@ __global__ void rope_table_kernel(Geom g, float2* __restrict__ tab) {
 
 // ---------------------------------------------------------------- prologue
 // One half warp per (b, n, h) row; lane l owns dims [8l, 8l+8) = RoPE pairs
-// [4l, 4l+4). Sum of squares: each lane adds its 8 squares in order, then a
-// butterfly over the 16 lanes (xor 8, 4, 2, 1). r = 1 / sqrt(ss/128 + eps)
-// with IEEE sqrt and division. y = (x * r) * g; then each pair turns by its
-// angle; one round to bf16 at the output.
+// [4l, 4l+4), which all lie on one axis (the axis blocks start at pairs 0,
+// 8 and 36, multiples of 4), so a lane reads its four (cos, sin) from one
+// table row with two 16-byte loads. Sum of squares: each lane adds its 8
+// squares in order, then a butterfly over the 16 lanes (xor 8, 4, 2, 1).
+// r = 1 / sqrt(ss/128 + eps) with IEEE sqrt and division. y = (x * r) * g;
+// then each pair turns by its angle; one round to bf16 at the output.
 __device__ __forceinline__ void norm_rope_row(const uint4 xv, const float* __restrict__ gain,
-                                              const float2* __restrict__ tab_row0,
-                                              const float2* __restrict__ tab_row1,
-                                              const float2* __restrict__ tab_row2, int lane16,
-                                              float eps, uint4& out, float& r_out) {
+                                              const float2* __restrict__ tab_row, int lane16, float eps,
+                                              uint4& out, float& r_out) {
     float x[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
                   bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
     float ss = 0.0f;
@@ -60,20 +60,26 @@ __device__ __forceinline__ void norm_rope_row(const uint4 xv, const float* __res
     const float4 g0 = __ldg(reinterpret_cast<const float4*>(gain) + 2 * lane16);
     const float4 g1 = __ldg(reinterpret_cast<const float4*>(gain) + 2 * lane16 + 1);
     const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const float4 t0 = __ldg(reinterpret_cast<const float4*>(tab_row + 4 * lane16));
+    const float4 t1 = __ldg(reinterpret_cast<const float4*>(tab_row + 4 * lane16) + 1);
+    const float2 cs[4] = {make_float2(t0.x, t0.y), make_float2(t0.z, t0.w), make_float2(t1.x, t1.y),
+                          make_float2(t1.z, t1.w)};
     uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        int k = 4 * lane16 + i;
-        int a = pair_axis(k);
-        const float2 cs = (a == 0 ? tab_row0 : (a == 1 ? tab_row1 : tab_row2))[k];
         float y0 = (x[2 * i] * r) * gv[2 * i];
         float y1 = (x[2 * i + 1] * r) * gv[2 * i + 1];
-        float o0 = fmaf(y0, cs.x, -(y1 * cs.y));
-        float o1 = fmaf(y0, cs.y, y1 * cs.x);
+        float o0 = fmaf(y0, cs[i].x, -(y1 * cs[i].y));
+        float o1 = fmaf(y0, cs[i].y, y1 * cs[i].x);
         o[i] = pack_bf16(o0, o1);
     }
     out = make_uint4(o[0], o[1], o[2], o[3]);
 }
+
+// A CTA of 256 threads covers 32 rows: half warp w takes rows base + w and
+// base + 16 + w (the two half warps of a warp read 512 contiguous bytes);
+// all four 16-byte input loads of a lane are issued before any arithmetic.
+constexpr int kPrologueRowsPerCta = 32;
 
 __global__ void __launch_bounds__(256) prologue_kernel(
     Geom g, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
@@ -82,35 +88,44 @@ __global__ void __launch_bounds__(256) prologue_kernel(
     const float2* __restrict__ tab, uint16_t* __restrict__ qh, uint16_t* __restrict__ kh,
     float* __restrict__ rq, float* __restrict__ rk) {
     const long long rows = (long long)g.B * g.S * g.H;
-    const long long row_raw = (long long)blockIdx.x * (blockDim.x / kRowThreads) + threadIdx.x / kRowThreads;
     const int lane16 = threadIdx.x % kRowThreads;
-    // A half warp past the end works on the last row and stores nothing, so
-    // that every lane of the warp reaches the shuffles.
-    const bool active = row_raw < rows;
-    const long long row = active ? row_raw : rows - 1;
-    const int h = (int)(row % g.H);
-    const long long bn = row / g.H;
-    const int n = (int)(bn % g.S);
-    const int b = (int)(bn / g.S);
-    const bool txt = n < g.T_txt;
-    const float2* t0 = tab + (size_t)(token_pos(g, n, 0) - g.p_lo) * kPairs;
-    const float2* t1 = tab + (size_t)(token_pos(g, n, 1) - g.p_lo) * kPairs;
-    const float2* t2 = tab + (size_t)(token_pos(g, n, 2) - g.p_lo) * kPairs;
-    const size_t src = (size_t)row * kHeadDim + 8 * lane16;
-    const size_t bh = (size_t)b * g.H + h;
-    const size_t dst = (bh * g.S + n) * kHeadDim + 8 * lane16;
-    const uint4 xq = __ldg(reinterpret_cast<const uint4*>(q + src));
-    const uint4 xk = __ldg(reinterpret_cast<const uint4*>(k + src));
-    uint4 oq, ok;
-    float r_q, r_k;
-    norm_rope_row(xq, txt ? gq_txt : gq_img, t0, t1, t2, lane16, g.eps, oq, r_q);
-    norm_rope_row(xk, txt ? gk_txt : gk_img, t0, t1, t2, lane16, g.eps, ok, r_k);
-    if (!active) return;
-    *reinterpret_cast<uint4*>(qh + dst) = oq;
-    *reinterpret_cast<uint4*>(kh + dst) = ok;
-    if (lane16 == 0) {
-        rq[bh * g.S + n] = r_q;
-        rk[bh * g.S + n] = r_k;
+    const int axis = pair_axis(4 * lane16);
+    const long long base = (long long)blockIdx.x * kPrologueRowsPerCta + threadIdx.x / kRowThreads;
+    uint4 xq[2], xk[2];
+    long long row[2];
+    bool active[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        // a half warp past the end works on the last row and stores
+        // nothing, so that every lane of the warp reaches the shuffles
+        const long long rr = base + 16 * u;
+        active[u] = rr < rows;
+        row[u] = active[u] ? rr : rows - 1;
+        const size_t src = (size_t)row[u] * kHeadDim + 8 * lane16;
+        xq[u] = __ldg(reinterpret_cast<const uint4*>(q + src));
+        xk[u] = __ldg(reinterpret_cast<const uint4*>(k + src));
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int h = (int)(row[u] % g.H);
+        const long long bn = row[u] / g.H;
+        const int n = (int)(bn % g.S);
+        const int b = (int)(bn / g.S);
+        const bool txt = n < g.T_txt;
+        const float2* trow = tab + (size_t)(token_pos(g, n, axis) - g.p_lo) * kPairs;
+        uint4 oq, ok;
+        float r_q, r_k;
+        norm_rope_row(xq[u], txt ? gq_txt : gq_img, trow, lane16, g.eps, oq, r_q);
+        norm_rope_row(xk[u], txt ? gk_txt : gk_img, trow, lane16, g.eps, ok, r_k);
+        if (!active[u]) continue;
+        const size_t bh = (size_t)b * g.H + h;
+        const size_t dst = (bh * g.S + n) * kHeadDim + 8 * lane16;
+        *reinterpret_cast<uint4*>(qh + dst) = oq;
+        *reinterpret_cast<uint4*>(kh + dst) = ok;
+        if (lane16 == 0) {
+            rq[bh * g.S + n] = r_q;
+            rk[bh * g.S + n] = r_k;
+        }
     }
 }
 
@@ -279,7 +294,7 @@ __global__ void dg_fold_total_kernel(Geom g, const float* __restrict__ dg_partia
 
 unsigned row_blocks(const Geom& g) {
     const long long rows = (long long)g.B * g.S * g.H;
-    return (unsigned)((rows + 15) / 16);
+    return (unsigned)((rows + kPrologueRowsPerCta - 1) / kPrologueRowsPerCta);
 }
 
 }  // namespace
