@@ -254,6 +254,41 @@ rlk_status rlk_joint_attn_av_gemm(const rlk_ja_shape* shape, const void* p,
                                   const int32_t* txt_valid_len, void* out,
                                   void* stream);
 
+/* ---------------------------------------------------------------------------
+ * The same forward and backward with the text and image streams in separate
+ * buffers, so a caller whose per-stream projections produce them apart (the
+ * RFC's Streams row: text and image keep separate weights; its WS1 rows
+ * qkv_bias_gemm and attn_out_bias_gemm run per stream) needs no
+ * concatenation copy before the attention or split copy after it.
+ * Every activation is a pair: *_txt bf16 [B, T_txt, H, D] and *_img bf16
+ * [B, grid_h * grid_w, H, D], each densely packed. *_img must be non-NULL;
+ * *_txt may be NULL only when T_txt == 0. All other arguments, the results
+ * and their bytes are exactly those of rlk_joint_attn_fwd() /
+ * rlk_joint_attn_bwd() on the concatenation [text, image]. */
+rlk_status rlk_joint_attn_fwd_streams(const rlk_ja_shape* shape,
+                                      const void* q_txt, const void* q_img,
+                                      const void* k_txt, const void* k_img,
+                                      const void* v_txt, const void* v_img,
+                                      const float* g_q_txt, const float* g_k_txt,
+                                      const float* g_q_img, const float* g_k_img,
+                                      const int32_t* txt_valid_len,
+                                      void* out_txt, void* out_img, float* lse, void* ctx,
+                                      void* stream);
+rlk_status rlk_joint_attn_bwd_streams(const rlk_ja_shape* shape,
+                                      const void* q_txt, const void* q_img,
+                                      const void* k_txt, const void* k_img,
+                                      const void* v_txt, const void* v_img,
+                                      const float* g_q_txt, const float* g_k_txt,
+                                      const float* g_q_img, const float* g_k_img,
+                                      const int32_t* txt_valid_len,
+                                      const void* out_txt, const void* out_img,
+                                      const void* dout_txt, const void* dout_img,
+                                      const float* lse, const void* ctx,
+                                      void* dq_txt, void* dq_img, void* dk_txt, void* dk_img,
+                                      void* dv_txt, void* dv_img,
+                                      float* dg_partial, float* dg,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device-side error word
  * that bounded waits in the kernels set when they give up. Returns RLK_OK,
  * RLK_ERR_DEVICE_TIMEOUT, or RLK_ERR_CUDA if the stream reported an error. */
@@ -328,8 +363,9 @@ rlk_status rlk_joint_attn_fwd_shard(const rlk_ja_shape* shape, const void* ctx, 
  * order, accumulator precision, Split-K / Stream-K state, TF32 state, kernel
  * fingerprint and selected backend, and says there is no silent fallback.
  * While tracing is on, every entry point that can launch work (the fused
- * forward and backward, the allocation-free forward, the key-shard forward
- * and the standalone operators) appends one record when it returns, including calls refused
+ * forward and backward with concatenated or separate streams, the
+ * allocation-free forward, the key-shard forward and the standalone
+ * operators) appends one record when it returns, including calls refused
  * during validation (status != RLK_OK, no kernel listed, actual backend
  * "none"). The kernels listed are the ones the call enqueued, in launch
  * order. Records live in a ring of RLK_OP_TRACE_CAP entries in host memory;

@@ -26,7 +26,8 @@ __all__ = [
     "rlk_joint_attn_unfused_bytes", "rlk_qk_norm_rope", "rlk_joint_attn_qk_gemm",
     "rlk_joint_attn_softmax", "rlk_joint_attn_av_gemm", "UNFUSED", "JointAttention",
     "rlk_op_trace_enable", "rlk_op_trace_count", "rlk_op_trace_read", "op_trace", "OP_TRACE_CAP",
-    "rlk_joint_attn_state_bytes", "rlk_joint_attn_fwd_shard",
+    "rlk_joint_attn_state_bytes", "rlk_joint_attn_fwd_shard", "rlk_joint_attn_fwd_streams",
+    "rlk_joint_attn_bwd_streams",
     "EXPORTED_SYMBOLS", "KERNEL_IDS",
 ]
 
@@ -58,6 +59,7 @@ EXPORTED_SYMBOLS = (
     "rlk_joint_attn_softmax", "rlk_joint_attn_av_gemm",
     "rlk_op_trace_enable", "rlk_op_trace_count", "rlk_op_trace_read",
     "rlk_joint_attn_state_bytes", "rlk_joint_attn_fwd_shard",
+    "rlk_joint_attn_fwd_streams", "rlk_joint_attn_bwd_streams",
 )
 OP_TRACE_CAP = 256
 OP_TRACE_MAX_KERNELS = 8
@@ -184,6 +186,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     L.rlk_joint_attn_state_bytes.restype = sz
     L.rlk_joint_attn_fwd_shard.argtypes = [shp, vp, vp, i32p, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp, vp]
     L.rlk_joint_attn_fwd_shard.restype = i32
+    L.rlk_joint_attn_fwd_streams.argtypes = [shp] + [vp] * 10 + [i32p] + [vp] * 5
+    L.rlk_joint_attn_fwd_streams.restype = i32
+    L.rlk_joint_attn_bwd_streams.argtypes = [shp] + [vp] * 10 + [i32p] + [vp] * 14 + [sz, vp]
+    L.rlk_joint_attn_bwd_streams.restype = i32
     L.rlk_op_trace_enable.argtypes = [i32]
     L.rlk_op_trace_enable.restype = i32
     L.rlk_op_trace_count.argtypes = []
@@ -319,6 +325,31 @@ def rlk_joint_attn_fwd_shard(shape, ctx, v, txt_valid_len, blk_begin, blk_end, s
                                         int(blk_begin), int(blk_end), _ptr(state_in), _ptr(state_out), _ptr(out),
                                         _ptr(lse), _stream_handle(stream))
     _check(rc, "rlk_joint_attn_fwd_shard")
+
+
+def rlk_joint_attn_fwd_streams(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_valid_len, out, lse, ctx,
+                               stream=None) -> None:
+    """Forward on separate streams: q, k, v and out are (text, image) pairs
+    of tensors or device pointers (the text one may be None if T_txt == 0)."""
+    args = [_ptr(x) for pair in (q, k, v) for x in pair]
+    rc = lib().rlk_joint_attn_fwd_streams(
+        ctypes.byref(shape), *args, _ptr(g_q_txt), _ptr(g_k_txt), _ptr(g_q_img), _ptr(g_k_img),
+        _lengths(txt_valid_len), _ptr(out[0]), _ptr(out[1]), _ptr(lse), _ptr(ctx), _stream_handle(stream))
+    _check(rc, "rlk_joint_attn_fwd_streams")
+
+
+def rlk_joint_attn_bwd_streams(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_valid_len, out, dout, lse,
+                               ctx, dq, dk, dv, dg_partial, dg, workspace, workspace_bytes=None, stream=None) -> None:
+    """Backward on separate streams; activations as (text, image) pairs."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    ins = [_ptr(x) for pair in (q, k, v) for x in pair]
+    rc = lib().rlk_joint_attn_bwd_streams(
+        ctypes.byref(shape), *ins, _ptr(g_q_txt), _ptr(g_k_txt), _ptr(g_q_img), _ptr(g_k_img),
+        _lengths(txt_valid_len), _ptr(out[0]), _ptr(out[1]), _ptr(dout[0]), _ptr(dout[1]), _ptr(lse), _ptr(ctx),
+        _ptr(dq[0]), _ptr(dq[1]), _ptr(dk[0]), _ptr(dk[1]), _ptr(dv[0]), _ptr(dv[1]), _ptr(dg_partial), _ptr(dg),
+        _ptr(workspace), int(workspace_bytes), _stream_handle(stream))
+    _check(rc, "rlk_joint_attn_bwd_streams")
 
 
 def rlk_op_trace_enable(enable: bool) -> None:
@@ -471,6 +502,31 @@ class JointAttention:
         rlk_joint_attn_softmax(sh, scores, valid_len, p, alpha, l, lse, stream)
         rlk_joint_attn_av_gemm(sh, p, alpha, l, v, valid_len, out, stream)
         return {"out": out, "lse": lse, "l": l, "scores": scores, "p": p, "alpha": alpha}
+
+    def forward_streams(self, q, k, v, gains, valid_len, stream=None):
+        """Forward on separate text/image tensors: q, k, v are (txt, img)
+        pairs, txt [B, T_txt, H, 128] and img [B, grid_h*grid_w, H, 128]
+        bf16. Returns ((out_txt, out_img), lse)."""
+        import torch
+        sh = self.shape
+        out = tuple(None if x is None else torch.empty_like(x) for x in q)
+        lse = torch.empty((sh.B, sh.H, sh.S), dtype=torch.float32, device=self.device)
+        rlk_joint_attn_fwd_streams(sh, q, k, v, gains[0], gains[1], gains[2], gains[3], valid_len, out, lse,
+                                   self.ctx, stream)
+        return out, lse
+
+    def backward_streams(self, q, k, v, gains, valid_len, out, dout, lse, stream=None):
+        """Backward on separate text/image tensors (pairs as in
+        forward_streams). Returns dq, dk, dv pairs, dg_partial and dg."""
+        import torch
+        sh = self.shape
+        like = lambda pair: tuple(None if x is None else torch.empty_like(x) for x in pair)  # noqa: E731
+        dq, dk, dv = like(q), like(k), like(v)
+        dgp = torch.empty((sh.B, sh.H, 4, HEAD_DIM), dtype=torch.float32, device=self.device)
+        dg = torch.empty((4, HEAD_DIM), dtype=torch.float32, device=self.device)
+        rlk_joint_attn_bwd_streams(sh, q, k, v, gains[0], gains[1], gains[2], gains[3], valid_len, out, dout, lse,
+                                   self.ctx, dq, dk, dv, dgp, dg, self.workspace, stream=stream)
+        return dq, dk, dv, dgp, dg
 
     def n_key_blocks(self) -> int:
         sh = self.shape

@@ -55,13 +55,13 @@ __device__ int g_status_bwd;
 struct BwdArgs {
     CUtensorMap map_q;    // qh [B*H*S, 128]
     CUtensorMap map_k;    // kh [B*H*S, 128]
-    CUtensorMap map_v;    // v  [B, S, H, 128] 4-D
-    CUtensorMap map_do;   // dO [B, S, H, 128] 4-D
+    CUtensorMap map_v[2];   // v per segment (0 text, 1 image), 4-D (d, h, token, b)
+    CUtensorMap map_do[2];  // dO per segment
     Geom g;
     ValidLen vl;
     const float* lse2_p;  // [B, H, nq_pad]
     const float* delta_p; // [B, H, nq_pad]
-    uint16_t* dv;         // [B, S, H, 128]
+    SegBf16 dv;           // [B, S, H, 128] (text rows, image rows)
     float* dkh;           // [B, H, S, 128]
     float* dqh;           // [B, H, S, 128]
     uint8_t* ds_tiles;    // [B, H, nq, nq] images of 32 KB (query tile major)
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
         const int rows = min(128, seg_end - k0);
         for (int i = tid; i < rows * 16; i += kThreads) {
             const int r = i >> 4, c = i & 15;
-            *reinterpret_cast<uint4*>(a.dv + (((size_t)b * g.S + k0 + r) * g.H + h) * kHeadDim + c * 8) =
+            *reinterpret_cast<uint4*>(seg_row(a.dv, g, b, k0 + r, h) + c * 8) =
                 make_uint4(0, 0, 0, 0);
             float4* dst = reinterpret_cast<float4*>(dkh + (size_t)(k0 + r) * kHeadDim + c * 8);
             dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -202,13 +202,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
         if (lane == 0) {
             prefetch_tensormap(&a.map_q);
             prefetch_tensormap(&a.map_k);
-            prefetch_tensormap(&a.map_v);
-            prefetch_tensormap(&a.map_do);
+            prefetch_tensormap(&a.map_v[0]);
+            prefetch_tensormap(&a.map_v[1]);
+            prefetch_tensormap(&a.map_do[0]);
+            prefetch_tensormap(&a.map_do[1]);
             mbar_expect_tx(bar_kv, 2 * kTileBytes);
             tma_load_2d(sK, &a.map_k, bar_kv, 0, row_base + k0);
             tma_load_2d(sK + kBoxBytes, &a.map_k, bar_kv, 64, row_base + k0);
-            tma_load_4d(sV, &a.map_v, bar_kv, 0, h, k0, b);
-            tma_load_4d(sV + kBoxBytes, &a.map_v, bar_kv, 64, h, k0, b);
+            // tiles never straddle the streams: rows counted from the segment start
+            const int vseg = k_txt ? 0 : 1, vrow = k_txt ? k0 : k0 - g.T_txt;
+            tma_load_4d(sV, &a.map_v[vseg], bar_kv, 0, h, vrow, b);
+            tma_load_4d(sV + kBoxBytes, &a.map_v[vseg], bar_kv, 64, h, vrow, b);
             int issued = 0;
             for (int i = 0; i < nq && !abort_flag; ++i) {
                 const int s = i & 1;
@@ -222,8 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
                 mbar_expect_tx(bf, 2 * kTileBytes + 1024);
                 tma_load_2d(stage_q(s), &a.map_q, bf, 0, row_base + q0);
                 tma_load_2d(stage_q(s) + kBoxBytes, &a.map_q, bf, 64, row_base + q0);
-                tma_load_4d(stage_o(s), &a.map_do, bf, 0, h, q0, b);
-                tma_load_4d(stage_o(s) + kBoxBytes, &a.map_do, bf, 64, h, q0, b);
+                const int oseg = i < g.ntq_txt ? 0 : 1, orow = oseg ? q0 - g.T_txt : q0;
+                tma_load_4d(stage_o(s), &a.map_do[oseg], bf, 0, h, orow, b);
+                tma_load_4d(stage_o(s) + kBoxBytes, &a.map_do[oseg], bf, 64, h, orow, b);
                 const size_t slot = bh * g.nq_pad + (size_t)i * 128;
                 bulk_load(stage_l(s), a.lse2_p + slot, 512, bf);
                 bulk_load(stage_l(s) + 512, a.delta_p + slot, 512, bf);
@@ -638,16 +643,18 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc_kernel(const __g
 
 // ---------------------------------------------------------------- tensor maps
 bool make_args(BwdArgs* a, const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
-               const uint16_t* v, const uint16_t* dout, const float* lse2_p, const float* delta_p) {
+               const SegBf16& v, const SegBf16& dout, const float* lse2_p, const float* delta_p) {
     const uint64_t rows = (uint64_t)g.B * g.H * g.S;
-    if (!tmap::rows_bf16(&a->map_q, qh, rows) || !tmap::rows_bf16(&a->map_k, kh, rows) ||
-        !tmap::bshd_bf16(&a->map_v, v, g) || !tmap::bshd_bf16(&a->map_do, dout, g))
+    if (!tmap::rows_bf16(&a->map_q, qh, rows) || !tmap::rows_bf16(&a->map_k, kh, rows))
         return false;
+    for (int seg = 0; seg < 2; ++seg)
+        if (!tmap::seg_bf16(&a->map_v[seg], v, g, seg) || !tmap::seg_bf16(&a->map_do[seg], dout, g, seg))
+            return false;
     a->g = g;
     a->vl = vl;
     a->lse2_p = lse2_p;
     a->delta_p = delta_p;
-    a->dv = nullptr;
+    a->dv = SegBf16{{nullptr, nullptr}, {0, 0}};
     a->dkh = nullptr;
     a->dqh = nullptr;
     a->ds_tiles = nullptr;
@@ -657,15 +664,15 @@ bool make_args(BwdArgs* a, const Geom& g, const ValidLen& vl, const uint16_t* qh
 }  // namespace
 
 cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
-                                 const uint16_t* v, const uint16_t* dout, const float* lse2_p, const float* delta_p,
-                                 uint16_t* dv, float* dkh, uint8_t* ds_tiles, cudaStream_t s) {
+                                 const SegBf16& v, const SegBf16& dout, const float* lse2_p, const float* delta_p,
+                                 const SegBf16& dv, float* dkh, uint8_t* ds_tiles, cudaStream_t s) {
     BwdArgs args;
     if (!make_args(&args, g, vl, qh, kh, v, dout, lse2_p, delta_p)) return cudaErrorInvalidValue;
     args.dv = dv;
     args.dkh = dkh;
     args.ds_tiles = ds_tiles;
     for (int seg = 0; seg < 2; ++seg)
-        if (!tmap::bshd_bf16(&args.map_dv[seg], dv, g, seg) || !tmap::bhsd_f32_segment(&args.map_dk[seg], dkh, g, seg))
+        if (!tmap::seg_bf16(&args.map_dv[seg], dv, g, seg) || !tmap::bhsd_f32_segment(&args.map_dk[seg], dkh, g, seg))
             return cudaErrorInvalidValue;
     cudaError_t e =
         cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmemBytes);

@@ -60,10 +60,9 @@ __device__ int g_status_fwd;
 struct FwdArgs {
     CUtensorMap map_q;   // qh [B*H*S, 128] bf16, box 64 x 128
     CUtensorMap map_k;   // kh [B*H*S, 128]
-    CUtensorMap map_v;   // v  [B, S, H, 128] as 4-D (d, h, n, b), box 64 x 1 x 128 x 1
+    CUtensorMap map_v[2];  // v per segment (0 text, 1 image) as 4-D (d, h, token, b), box 64 x 1 x 128 x 1
     Geom g;
     ValidLen vl;
-    uint16_t* out;       // [B, S, H, 128]
     float* lse;          // [B, H, S] or null
     CUtensorMap map_o[2];  // out per segment (0 text, 1 image): rows past a segment are clipped
     // key shard (kShard launches): column blocks [blk_begin, blk_end) of the
@@ -194,7 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
         if (lane == 0) {
             prefetch_tensormap(&a.map_q);
             prefetch_tensormap(&a.map_k);
-            prefetch_tensormap(&a.map_v);
+            prefetch_tensormap(&a.map_v[0]);
+            prefetch_tensormap(&a.map_v[1]);
             mbar_expect_tx(bar_q, (has_b ? 2 : 1) * kTileBytes);
             for (int t = 0; t < (has_b ? 2 : 1); ++t) {
                 tma_load_2d(sQ + t * kTileBytes, &a.map_q, bar_q, 0, row_base + q0[t]);
@@ -218,8 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                     break;
                 }
                 mbar_expect_tx(bar_vf + 8 * s, kTileBytes);
-                tma_load_4d(dv, &a.map_v, bar_vf + 8 * s, 0, h, ti.k0, b);
-                tma_load_4d(dv + kBoxBytes, &a.map_v, bar_vf + 8 * s, 64, h, ti.k0, b);
+                // key tiles never straddle the streams: V comes from the
+                // tile's own segment, rows counted from the segment start
+                const int vseg = ti.k0 < g.T_txt ? 0 : 1;
+                const int vrow = vseg ? ti.k0 - g.T_txt : ti.k0;
+                tma_load_4d(dv, &a.map_v[vseg], bar_vf + 8 * s, 0, h, vrow, b);
+                tma_load_4d(dv + kBoxBytes, &a.map_v[vseg], bar_vf + 8 * s, 64, h, vrow, b);
                 v_issued = j + 1;
             }
             // drain: the copies of Q and of the last (up to) two K and V tiles have landed
@@ -496,16 +500,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
 }  // namespace
 
 cudaError_t launch_attn_fwd(const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
-                            const uint16_t* v, uint16_t* out, float* lse, cudaStream_t s) {
+                            const SegBf16& v, const SegBf16& out, float* lse, cudaStream_t s) {
     FwdArgs local;
     const uint64_t rows = (uint64_t)g.B * g.H * g.S;
     if (!tmap::rows_bf16(&local.map_q, qh, rows) || !tmap::rows_bf16(&local.map_k, kh, rows) ||
-        !tmap::bshd_bf16(&local.map_v, v, g) || !tmap::bshd_bf16(&local.map_o[0], out, g, 0) ||
-        !tmap::bshd_bf16(&local.map_o[1], out, g, 1))
+        !tmap::seg_bf16(&local.map_v[0], v, g, 0) || !tmap::seg_bf16(&local.map_v[1], v, g, 1) ||
+        !tmap::seg_bf16(&local.map_o[0], out, g, 0) || !tmap::seg_bf16(&local.map_o[1], out, g, 1))
         return cudaErrorInvalidValue;
     local.g = g;
     local.vl = vl;
-    local.out = out;
     local.lse = lse;
     local.blk_begin = 0;
     local.blk_end = g.ntq_txt + g.ntq_img;
@@ -523,23 +526,22 @@ cudaError_t launch_attn_fwd(const Geom& g, const ValidLen& vl, const uint16_t* q
 }
 
 cudaError_t launch_attn_fwd_shard(const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
-                                  const uint16_t* v, int blk_begin, int blk_end, const float* state_in,
-                                  float* state_out, uint16_t* out, float* lse, cudaStream_t s) {
+                                  const SegBf16& v, int blk_begin, int blk_end, const float* state_in,
+                                  float* state_out, const SegBf16* out, float* lse, cudaStream_t s) {
     FwdArgs local;
     const uint64_t rows = (uint64_t)g.B * g.H * g.S;
     if (!tmap::rows_bf16(&local.map_q, qh, rows) || !tmap::rows_bf16(&local.map_k, kh, rows) ||
-        !tmap::bshd_bf16(&local.map_v, v, g))
+        !tmap::seg_bf16(&local.map_v[0], v, g, 0) || !tmap::seg_bf16(&local.map_v[1], v, g, 1))
         return cudaErrorInvalidValue;
     // only the last shard writes out (its maps are unused elsewhere)
     if (out != nullptr) {
-        if (!tmap::bshd_bf16(&local.map_o[0], out, g, 0) || !tmap::bshd_bf16(&local.map_o[1], out, g, 1))
+        if (!tmap::seg_bf16(&local.map_o[0], *out, g, 0) || !tmap::seg_bf16(&local.map_o[1], *out, g, 1))
             return cudaErrorInvalidValue;
     } else {
         memset(local.map_o, 0, sizeof(local.map_o));
     }
     local.g = g;
     local.vl = vl;
-    local.out = out;
     local.lse = lse;
     local.blk_begin = blk_begin;
     local.blk_end = blk_end;

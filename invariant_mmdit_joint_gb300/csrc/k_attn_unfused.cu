@@ -346,13 +346,13 @@ __global__ void __launch_bounds__(128) softmax_kernel(const __grid_constant__ Sm
 // other rows scale by exactly 1), store P into TMEM and signal the MMA
 // thread, which issues O += P V.
 struct AvArgs {
-    CUtensorMap map_v;     // v [B, S, H, 128] as 4-D
+    CUtensorMap map_v[2];  // v per segment (0 text, 1 image) as 4-D (d, h, token, b)
     Geom g;
     ValidLen vl;
     const uint32_t* p;     // bf16 pairs [B, H, S, ncols / 2]
     const float* alpha;    // [B, H, S, nblk]
     const float* l;        // [B, H, S]
-    uint16_t* out;         // [B, S, H, 128]
+    SegBf16 out;           // [B, S, H, 128] (text rows, image rows)
     int ncols, nblk;
 };
 
@@ -405,7 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1) av_gemm_kernel(const __grid_const
 
     if (warp == kWarpTma) {
         if (lane == 0) {
-            prefetch_tensormap(&a.map_v);
+            prefetch_tensormap(&a.map_v[0]);
+            prefetch_tensormap(&a.map_v[1]);
             int issued = 0;
             for (int j = 0; j < nkt && !abort_flag; ++j) {
                 const int s = j & 1;
@@ -415,8 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1) av_gemm_kernel(const __grid_const
                 }
                 const KeyTile kt = key_tile(g, L, j);
                 mbar_expect_tx(bar_vf + 8 * s, kTileBytes);
-                tma_load_4d(sV + s * kTileBytes, &a.map_v, bar_vf + 8 * s, 0, h, kt.k0, b);
-                tma_load_4d(sV + s * kTileBytes + kBoxBytes, &a.map_v, bar_vf + 8 * s, 64, h, kt.k0, b);
+                const int vseg = kt.k0 < g.T_txt ? 0 : 1, vrow = vseg ? kt.k0 - g.T_txt : kt.k0;
+                tma_load_4d(sV + s * kTileBytes, &a.map_v[vseg], bar_vf + 8 * s, 0, h, vrow, b);
+                tma_load_4d(sV + s * kTileBytes + kBoxBytes, &a.map_v[vseg], bar_vf + 8 * s, 64, h, vrow, b);
                 issued = j + 1;
             }
             const volatile int no_abort = 0;
@@ -496,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) av_gemm_kernel(const __grid_const
             // the TMEM loads are warp-collective; only rows inside the
             // segment store
             const float inv = 1.0f / a.l[rowi];
-            uint4* orow = reinterpret_cast<uint4*>(a.out + (((size_t)b * g.S + (in_seg ? n : q0)) * g.H + h) * kHeadDim);
+            uint4* orow = reinterpret_cast<uint4*>(seg_row(a.out, g, b, in_seg ? n : q0, h));
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t r[32];
@@ -565,9 +567,9 @@ cudaError_t launch_softmax(const Geom& g, const ValidLen& vl, const float* score
 }
 
 cudaError_t launch_av_gemm(const Geom& g, const ValidLen& vl, const uint16_t* p, const float* alpha, const float* l,
-                           const uint16_t* v, uint16_t* out, cudaStream_t s) {
+                           const SegBf16& v, const SegBf16& out, cudaStream_t s) {
     AvArgs a;
-    if (!tmap::bshd_bf16(&a.map_v, v, g)) return cudaErrorInvalidValue;
+    if (!tmap::seg_bf16(&a.map_v[0], v, g, 0) || !tmap::seg_bf16(&a.map_v[1], v, g, 1)) return cudaErrorInvalidValue;
     a.g = g;
     a.vl = vl;
     a.p = reinterpret_cast<const uint32_t*>(p);

@@ -82,7 +82,7 @@ __device__ __forceinline__ void norm_rope_row(const uint4 xv, const float* __res
 constexpr int kPrologueRowsPerCta = 32;
 
 __global__ void __launch_bounds__(256) prologue_kernel(
-    Geom g, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+    Geom g, const SegBf16 q, const SegBf16 k,
     const float* __restrict__ gq_txt, const float* __restrict__ gk_txt,
     const float* __restrict__ gq_img, const float* __restrict__ gk_img,
     const float2* __restrict__ tab, uint16_t* __restrict__ qh, uint16_t* __restrict__ kh,
@@ -92,25 +92,26 @@ __global__ void __launch_bounds__(256) prologue_kernel(
     const int axis = pair_axis(4 * lane16);
     const long long base = (long long)blockIdx.x * kPrologueRowsPerCta + threadIdx.x / kRowThreads;
     uint4 xq[2], xk[2];
-    long long row[2];
+    int hh[2], nn[2], bb[2];
     bool active[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         // a half warp past the end works on the last row and stores
-        // nothing, so that every lane of the warp reaches the shuffles
+        // nothing, so that every lane of the warp reaches the shuffles;
+        // rows are enumerated as (b, n, h) of [B, S, H]
         const long long rr = base + 16 * u;
         active[u] = rr < rows;
-        row[u] = active[u] ? rr : rows - 1;
-        const size_t src = (size_t)row[u] * kHeadDim + 8 * lane16;
-        xq[u] = __ldg(reinterpret_cast<const uint4*>(q + src));
-        xk[u] = __ldg(reinterpret_cast<const uint4*>(k + src));
+        const long long row = active[u] ? rr : rows - 1;
+        hh[u] = (int)(row % g.H);
+        const long long bn = row / g.H;
+        nn[u] = (int)(bn % g.S);
+        bb[u] = (int)(bn / g.S);
+        xq[u] = __ldg(reinterpret_cast<const uint4*>(seg_row(q, g, bb[u], nn[u], hh[u]) + 8 * lane16));
+        xk[u] = __ldg(reinterpret_cast<const uint4*>(seg_row(k, g, bb[u], nn[u], hh[u]) + 8 * lane16));
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-        const int h = (int)(row[u] % g.H);
-        const long long bn = row[u] / g.H;
-        const int n = (int)(bn % g.S);
-        const int b = (int)(bn / g.S);
+        const int h = hh[u], n = nn[u], b = bb[u];
         const bool txt = n < g.T_txt;
         const float2* trow = tab + (size_t)(token_pos(g, n, axis) - g.p_lo) * kPairs;
         uint4 oq, ok;
@@ -136,8 +137,7 @@ __global__ void __launch_bounds__(256) prologue_kernel(
 // products in order, then a butterfly over the half warp) and
 // lse2 = lse * log2(e); a slot past its segment gets Delta = 0 and
 // lse2 = +inf, so the backward kernels see P = 0 there.
-__global__ void __launch_bounds__(256) bwd_pre_kernel(Geom g, const uint16_t* __restrict__ o,
-                                                      const uint16_t* __restrict__ dout,
+__global__ void __launch_bounds__(256) bwd_pre_kernel(Geom g, const SegBf16 o, const SegBf16 dout,
                                                       const float* __restrict__ lse, float* __restrict__ lse2_p,
                                                       float* __restrict__ delta_p) {
     const long long slots = (long long)g.B * g.H * g.nq_pad;
@@ -153,9 +153,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(Geom g, const uint16_t* __
     const int b = (int)(bh / g.H), h = (int)(bh % g.H);
     float acc = 0.0f;
     if (valid) {
-        const size_t src = (((size_t)b * g.S + n) * g.H + h) * kHeadDim + 8 * lane16;
-        const uint4 ov = __ldg(reinterpret_cast<const uint4*>(o + src));
-        const uint4 dv = __ldg(reinterpret_cast<const uint4*>(dout + src));
+        const uint4 ov = __ldg(reinterpret_cast<const uint4*>(seg_row(o, g, b, n, h) + 8 * lane16));
+        const uint4 dv = __ldg(reinterpret_cast<const uint4*>(seg_row(dout, g, b, n, h) + 8 * lane16));
         const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
         const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
@@ -185,12 +184,12 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(Geom g, const uint16_t* __
 constexpr int kNrbRowsPerWarp = kDgChunk / 4;
 
 __global__ void __launch_bounds__(256) norm_rope_bwd_kernel(
-    Geom g, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+    Geom g, const SegBf16 q, const SegBf16 k,
     const float* __restrict__ gq_txt, const float* __restrict__ gk_txt,
     const float* __restrict__ gq_img, const float* __restrict__ gk_img,
     const float2* __restrict__ tab, const float* __restrict__ rq, const float* __restrict__ rk,
-    const float* __restrict__ dqh, const float* __restrict__ dkh, uint16_t* __restrict__ dq,
-    uint16_t* __restrict__ dk, float* __restrict__ dg_chunks) {
+    const float* __restrict__ dqh, const float* __restrict__ dkh, const SegBf16 dq,
+    const SegBf16 dk, float* __restrict__ dg_chunks) {
     __shared__ float red[8][kHeadDim];
     const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -201,8 +200,8 @@ __global__ void __launch_bounds__(256) norm_rope_bwd_kernel(
     const float* gain = is_k ? (txt_chunk ? gk_txt : gk_img) : (txt_chunk ? gq_txt : gq_img);
     const float* r_all = is_k ? rk : rq;
     const float* dyh = is_k ? dkh : dqh;
-    const uint16_t* x_all = is_k ? k : q;
-    uint16_t* dx_all = is_k ? dk : dq;
+    const SegBf16 x_all = is_k ? k : q;
+    const SegBf16 dx_all = is_k ? dk : dq;
     const size_t bh = (size_t)b * g.H + h;
     const float4 gv = __ldg(reinterpret_cast<const float4*>(gain) + lane);
     const int k0 = 2 * lane, k1 = 2 * lane + 1;
@@ -215,8 +214,7 @@ __global__ void __launch_bounds__(256) norm_rope_bwd_kernel(
         const float2* trow = tab + (size_t)(token_pos(g, n, ax) - g.p_lo) * kPairs;
         const float2 c0 = trow[k0], c1 = trow[k1];
         const float4 dy = *reinterpret_cast<const float4*>(dyh + (bh * g.S + n) * kHeadDim + 4 * lane);
-        const size_t xoff = (((size_t)b * g.S + n) * g.H + h) * kHeadDim + 4 * lane;
-        const uint2 xv = *reinterpret_cast<const uint2*>(x_all + xoff);
+        const uint2 xv = *reinterpret_cast<const uint2*>(seg_row(x_all, g, b, n, h) + 4 * lane);
         const float r = r_all[bh * g.S + n];
         float u[4];
         u[0] = fmaf(dy.x, c0.x, dy.y * c0.y);
@@ -242,7 +240,8 @@ __global__ void __launch_bounds__(256) norm_rope_bwd_kernel(
             dx[j] = r * fmaf(-xh[j], c, w[j]);
             acc[j] = fmaf(u[j], xh[j], acc[j]);
         }
-        *reinterpret_cast<uint2*>(dx_all + xoff) = make_uint2(pack_bf16(dx[0], dx[1]), pack_bf16(dx[2], dx[3]));
+        *reinterpret_cast<uint2*>(seg_row(dx_all, g, b, n, h) + 4 * lane) =
+            make_uint2(pack_bf16(dx[0], dx[1]), pack_bf16(dx[2], dx[3]));
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) red[warp][4 * lane + j] = acc[j];
@@ -307,7 +306,7 @@ cudaError_t launch_rope_table(const Geom& g, float2* tab, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_prologue(const Geom& g, const uint16_t* q, const uint16_t* k,
+cudaError_t launch_prologue(const Geom& g, const SegBf16& q, const SegBf16& k,
                             const float* const gains[4], const float2* tab, uint16_t* qh,
                             uint16_t* kh, float* rq, float* rk, cudaStream_t s) {
     timing_begin(kKPrologue, s);
@@ -317,7 +316,7 @@ cudaError_t launch_prologue(const Geom& g, const uint16_t* q, const uint16_t* k,
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_pre(const Geom& g, const uint16_t* out, const uint16_t* dout, const float* lse,
+cudaError_t launch_bwd_pre(const Geom& g, const SegBf16& out, const SegBf16& dout, const float* lse,
                            float* lse2_p, float* delta_p, cudaStream_t s) {
     const long long slots = (long long)g.B * g.H * g.nq_pad;
     timing_begin(kKBwdPre, s);
@@ -326,10 +325,10 @@ cudaError_t launch_bwd_pre(const Geom& g, const uint16_t* out, const uint16_t* d
     return cudaGetLastError();
 }
 
-cudaError_t launch_norm_rope_bwd(const Geom& g, const uint16_t* q, const uint16_t* k,
+cudaError_t launch_norm_rope_bwd(const Geom& g, const SegBf16& q, const SegBf16& k,
                                  const float* const gains[4], const float2* tab, const float* rq,
-                                 const float* rk, const float* dqh, const float* dkh, uint16_t* dq,
-                                 uint16_t* dk, float* dg_chunks, cudaStream_t s) {
+                                 const float* rk, const float* dqh, const float* dkh, const SegBf16& dq,
+                                 const SegBf16& dk, float* dg_chunks, cudaStream_t s) {
     dim3 grid(g.n_dg_chunks_txt + g.n_dg_chunks_img, g.H, g.B);
     timing_begin(kKNormRopeBwd, s);
     norm_rope_bwd_kernel<<<grid, 256, 0, s>>>(g, q, k, gains[0], gains[1], gains[2], gains[3], tab,

@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstring>
 #include <initializer_list>
+#include <utility>
 #include <mutex>
 #include <vector>
 
@@ -172,20 +173,38 @@ rlk_status common_checks(const rlk_ja_shape* sh, const int32_t* vl, Geom* g, Val
 
 // Rows qk_rmsnorm + multi_axis_rope: cos/sin table and normed, rotated q^, k^
 // (with the RMSNorm factors) into ctx.
-rlk_status run_prologue(const Geom& g, const void* q, const void* k, const float* const gains[4], void* ctx,
+rlk_status run_prologue(const Geom& g, const SegBf16& q, const SegBf16& k, const float* const gains[4], void* ctx,
                         cudaStream_t s) {
     const CtxLayout l = ctx_layout(g);
     uint8_t* c = static_cast<uint8_t*>(ctx);
     float2* tab = reinterpret_cast<float2*>(c + l.tab);
     if (launch_rope_table(g, tab, s) != cudaSuccess) return RLK_ERR_CUDA;
-    if (launch_prologue(g, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), gains, tab,
-                        reinterpret_cast<uint16_t*>(c + l.qh), reinterpret_cast<uint16_t*>(c + l.kh),
-                        reinterpret_cast<float*>(c + l.rq), reinterpret_cast<float*>(c + l.rk), s) != cudaSuccess)
+    if (launch_prologue(g, q, k, gains, tab, reinterpret_cast<uint16_t*>(c + l.qh),
+                        reinterpret_cast<uint16_t*>(c + l.kh), reinterpret_cast<float*>(c + l.rq),
+                        reinterpret_cast<float*>(c + l.rk), s) != cudaSuccess)
         return RLK_ERR_CUDA;
     return RLK_OK;
 }
 
-// Sizes of the standalone operators' intermediates.
+// The forward and backward on segmented activations (arguments checked).
+rlk_status fwd_core(const Geom& g, const ValidLen& vl, const SegBf16& q, const SegBf16& k, const SegBf16& v,
+                    const float* const gains[4], const SegBf16& out, float* lse, void* ctx, cudaStream_t s) {
+    const CtxLayout l = ctx_layout(g);
+    const uint8_t* c = static_cast<const uint8_t*>(ctx);
+    const rlk_status st = run_prologue(g, q, k, gains, ctx, s);
+    if (st != RLK_OK) return st;
+    if (launch_attn_fwd(g, vl, reinterpret_cast<const uint16_t*>(c + l.qh), reinterpret_cast<const uint16_t*>(c + l.kh),
+                        v, out, lse, s) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status bwd_core(const Geom& g, const ValidLen& vl, const SegBf16& q, const SegBf16& k, const SegBf16& v,
+                    const float* const gains[4], const SegBf16& out, const SegBf16& dout, const float* lse,
+                    const void* ctx, const SegBf16& dq, const SegBf16& dk, const SegBf16& dv, float* dg_partial,
+                    float* dg, void* workspace, cudaStream_t s);
+
+// Sizes of the standalone operators' intermediates.// Sizes of the standalone operators' intermediates.
 size_t unfused_bytes(const Geom& g, int which) {
     const size_t rows = (size_t)g.B * g.H * g.S;
     const size_t nblk = (size_t)g.ntq_txt + g.ntq_img;
@@ -255,6 +274,12 @@ const OpInfo kOps[] = {
     {"joint_attention_fused key shard", "rlk_joint_attn_fwd_shard", kFwdPolicy,
      "key tiles of 128 in the fused order, shards in ascending block order, the online-softmax state "
      "handed from shard to shard"},
+    {"qk_rmsnorm+multi_axis_rope+joint_attention_fused", "rlk_joint_attn_fwd_streams", kFwdPolicy, kFwdOrder},
+    {"joint_attention_fused backward", "rlk_joint_attn_bwd_streams",
+     "bf16 operands with P and dS rounded to bf16, fp32 TMEM accumulators, exp2f numerators, dK and dQ "
+     "from the same bf16 dS, one bf16 cast of dQ dK dV; no TF32, no fast math",
+     "dK/dV: query tiles ascending; dQ: key tiles in the forward order; dg: 64-token chunks, then h, "
+     "then b ascending"},
 };
 const char* const kKernelNames[kNumKernelIds] = {
     "rope_table_kernel", "prologue_kernel", "attn_fwd_tc_kernel", "bwd_pre_kernel",
@@ -358,6 +383,41 @@ void timing_end(int id, cudaStream_t s) {
 
 }  // namespace rlk
 
+
+namespace rlk {
+namespace {
+rlk_status bwd_core(const Geom& g, const ValidLen& vl, const SegBf16& q, const SegBf16& k, const SegBf16& v,
+                    const float* const gains[4], const SegBf16& out, const SegBf16& dout, const float* lse,
+                    const void* ctx, const SegBf16& dq, const SegBf16& dk, const SegBf16& dv, float* dg_partial,
+                    float* dg, void* workspace, cudaStream_t s) {
+    const CtxLayout l = ctx_layout(g);
+    const WsLayout w = ws_layout(g);
+    const uint8_t* c = static_cast<const uint8_t*>(ctx);
+    const uint16_t* qh = reinterpret_cast<const uint16_t*>(c + l.qh);
+    const uint16_t* kh = reinterpret_cast<const uint16_t*>(c + l.kh);
+    const float* rq = reinterpret_cast<const float*>(c + l.rq);
+    const float* rk = reinterpret_cast<const float*>(c + l.rk);
+    const float2* tab = reinterpret_cast<const float2*>(c + l.tab);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* lse2_p = reinterpret_cast<float*>(ws + w.lse2);
+    float* delta_p = reinterpret_cast<float*>(ws + w.delta);
+    float* dqh = reinterpret_cast<float*>(ws + w.dqh);
+    float* dkh = reinterpret_cast<float*>(ws + w.dkh);
+    float* dgc = reinterpret_cast<float*>(ws + w.dgc);
+    float* dgp = dg_partial != nullptr ? dg_partial : reinterpret_cast<float*>(ws + w.dgp);
+    uint8_t* ds_tiles = ws + w.dst;
+    if (launch_bwd_pre(g, out, dout, lse, lse2_p, delta_p, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_attn_bwd_dkdv(g, vl, qh, kh, v, dout, lse2_p, delta_p, dv, dkh, ds_tiles, s) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    if (launch_attn_bwd_dq(g, vl, kh, ds_tiles, dqh, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_norm_rope_bwd(g, q, k, gains, tab, rq, rk, dqh, dkh, dq, dk, dgc, s) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    if (launch_dg_fold(g, dgc, dgp, dg, s) != cudaSuccess) return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+}  // namespace
+}  // namespace rlk
+
 using namespace rlk;
 
 extern "C" {
@@ -391,19 +451,9 @@ static rlk_status rlk_joint_attn_fwd_impl(const rlk_ja_shape* shape, const void*
     st = device_ok();
     if (st != RLK_OK) return st;
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const CtxLayout l = ctx_layout(g);
-    uint8_t* c = static_cast<uint8_t*>(ctx);
-    const uint16_t* qh = reinterpret_cast<const uint16_t*>(c + l.qh);
-    const uint16_t* kh = reinterpret_cast<const uint16_t*>(c + l.kh);
     const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
-
-    st = run_prologue(g, q, k, gains, ctx, s);
-    if (st != RLK_OK) return st;
-    if (launch_attn_fwd(g, vl, qh, kh, static_cast<const uint16_t*>(v), static_cast<uint16_t*>(out), lse, s) !=
-        cudaSuccess)
-        return RLK_ERR_CUDA;
-    return RLK_OK;
+    return fwd_core(g, vl, seg_concat(q, g), seg_concat(k, g), seg_concat(v, g), gains, seg_concat(out, g), lse, ctx,
+                    static_cast<cudaStream_t>(stream));
 }
 
 rlk_status rlk_joint_attn_fwd(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
@@ -437,38 +487,10 @@ static rlk_status rlk_joint_attn_bwd_impl(const rlk_ja_shape* shape, const void*
     st = device_ok();
     if (st != RLK_OK) return st;
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const CtxLayout l = ctx_layout(g);
-    const uint8_t* c = static_cast<const uint8_t*>(ctx);
-    const uint16_t* qh = reinterpret_cast<const uint16_t*>(c + l.qh);
-    const uint16_t* kh = reinterpret_cast<const uint16_t*>(c + l.kh);
-    const float* rq = reinterpret_cast<const float*>(c + l.rq);
-    const float* rk = reinterpret_cast<const float*>(c + l.rk);
-    const float2* tab = reinterpret_cast<const float2*>(c + l.tab);
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    float* lse2_p = reinterpret_cast<float*>(ws + w.lse2);
-    float* delta_p = reinterpret_cast<float*>(ws + w.delta);
-    float* dqh = reinterpret_cast<float*>(ws + w.dqh);
-    float* dkh = reinterpret_cast<float*>(ws + w.dkh);
-    float* dgc = reinterpret_cast<float*>(ws + w.dgc);
-    float* dgp = dg_partial != nullptr ? dg_partial : reinterpret_cast<float*>(ws + w.dgp);
     const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
-    const uint16_t* vv = static_cast<const uint16_t*>(v);
-    const uint16_t* dO = static_cast<const uint16_t*>(dout);
-
-    if (launch_bwd_pre(g, static_cast<const uint16_t*>(out), dO, lse, lse2_p, delta_p, s) != cudaSuccess)
-        return RLK_ERR_CUDA;
-    uint8_t* ds_tiles = ws + w.dst;
-    if (launch_attn_bwd_dkdv(g, vl, qh, kh, vv, dO, lse2_p, delta_p, static_cast<uint16_t*>(dv), dkh, ds_tiles,
-                             s) != cudaSuccess)
-        return RLK_ERR_CUDA;
-    if (launch_attn_bwd_dq(g, vl, kh, ds_tiles, dqh, s) != cudaSuccess) return RLK_ERR_CUDA;
-    if (launch_norm_rope_bwd(g, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), gains, tab, rq,
-                             rk, dqh, dkh, static_cast<uint16_t*>(dq), static_cast<uint16_t*>(dk), dgc,
-                             s) != cudaSuccess)
-        return RLK_ERR_CUDA;
-    if (launch_dg_fold(g, dgc, dgp, dg, s) != cudaSuccess) return RLK_ERR_CUDA;
-    return RLK_OK;
+    return bwd_core(g, vl, seg_concat(q, g), seg_concat(k, g), seg_concat(v, g), gains, seg_concat(out, g),
+                    seg_concat(dout, g), lse, ctx, seg_concat(dq, g), seg_concat(dk, g), seg_concat(dv, g), dg_partial,
+                    dg, workspace, static_cast<cudaStream_t>(stream));
 }
 
 rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
@@ -481,6 +503,89 @@ rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape, const void* q, const vo
     return sc.finish(rlk_joint_attn_bwd_impl(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_valid_len,
                                              out, dout, lse, ctx, dq, dk, dv, dg_partial, dg, workspace,
                                              workspace_bytes, stream));
+}
+
+// Separate text and image buffers: an image pointer is required, a text
+// pointer only when T_txt > 0; all 16-byte aligned.
+static rlk_status check_pairs(const Geom& g, std::initializer_list<std::pair<const void*, const void*>> pairs) {
+    for (const auto& pr : pairs) {
+        if (pr.second == nullptr || (g.T_txt > 0 && pr.first == nullptr)) return RLK_ERR_INVALID_ARG;
+        if (!aligned16(pr.second) || (pr.first != nullptr && !aligned16(pr.first))) return RLK_ERR_ALIGNMENT;
+    }
+    return RLK_OK;
+}
+
+static rlk_status rlk_joint_attn_fwd_streams_impl(const rlk_ja_shape* shape, const void* q_txt, const void* q_img,
+                                                  const void* k_txt, const void* k_img, const void* v_txt,
+                                                  const void* v_img, const float* g_q_txt, const float* g_k_txt,
+                                                  const float* g_q_img, const float* g_k_img,
+                                                  const int32_t* txt_valid_len, void* out_txt, void* out_img,
+                                                  float* lse, void* ctx, void* stream) {
+    Geom g;
+    ValidLen vl;
+    rlk_status st = common_checks(shape, txt_valid_len, &g, &vl);
+    if (st != RLK_OK) return st;
+    st = check_pairs(g, {{q_txt, q_img}, {k_txt, k_img}, {v_txt, v_img}, {out_txt, out_img}});
+    if (st != RLK_OK) return st;
+    st = check_ptrs({g_q_txt, g_k_txt, g_q_img, g_k_img, ctx}, {lse});
+    if (st != RLK_OK) return st;
+    st = device_ok();
+    if (st != RLK_OK) return st;
+    const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
+    return fwd_core(g, vl, seg_split(q_txt, q_img, g), seg_split(k_txt, k_img, g), seg_split(v_txt, v_img, g), gains,
+                    seg_split(out_txt, out_img, g), lse, ctx, static_cast<cudaStream_t>(stream));
+}
+
+rlk_status rlk_joint_attn_fwd_streams(const rlk_ja_shape* shape, const void* q_txt, const void* q_img,
+                                      const void* k_txt, const void* k_img, const void* v_txt, const void* v_img,
+                                      const float* g_q_txt, const float* g_k_txt, const float* g_q_img,
+                                      const float* g_k_img, const int32_t* txt_valid_len, void* out_txt,
+                                      void* out_img, float* lse, void* ctx, void* stream) {
+    OpScope sc(kOpFwdStreams, shape);
+    return sc.finish(rlk_joint_attn_fwd_streams_impl(shape, q_txt, q_img, k_txt, k_img, v_txt, v_img, g_q_txt,
+                                                     g_k_txt, g_q_img, g_k_img, txt_valid_len, out_txt, out_img,
+                                                     lse, ctx, stream));
+}
+
+static rlk_status rlk_joint_attn_bwd_streams_impl(
+    const rlk_ja_shape* shape, const void* q_txt, const void* q_img, const void* k_txt, const void* k_img,
+    const void* v_txt, const void* v_img, const float* g_q_txt, const float* g_k_txt, const float* g_q_img,
+    const float* g_k_img, const int32_t* txt_valid_len, const void* out_txt, const void* out_img,
+    const void* dout_txt, const void* dout_img, const float* lse, const void* ctx, void* dq_txt, void* dq_img,
+    void* dk_txt, void* dk_img, void* dv_txt, void* dv_img, float* dg_partial, float* dg, void* workspace,
+    size_t workspace_bytes, void* stream) {
+    Geom g;
+    ValidLen vl;
+    rlk_status st = common_checks(shape, txt_valid_len, &g, &vl);
+    if (st != RLK_OK) return st;
+    st = check_pairs(g, {{q_txt, q_img}, {k_txt, k_img}, {v_txt, v_img}, {out_txt, out_img}, {dout_txt, dout_img},
+                         {dq_txt, dq_img}, {dk_txt, dk_img}, {dv_txt, dv_img}});
+    if (st != RLK_OK) return st;
+    st = check_ptrs({g_q_txt, g_k_txt, g_q_img, g_k_img, lse, ctx, dg, workspace}, {dg_partial});
+    if (st != RLK_OK) return st;
+    if (workspace_bytes < ws_layout(g).total) return RLK_ERR_WORKSPACE;
+    st = device_ok();
+    if (st != RLK_OK) return st;
+    const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
+    return bwd_core(g, vl, seg_split(q_txt, q_img, g), seg_split(k_txt, k_img, g), seg_split(v_txt, v_img, g), gains,
+                    seg_split(out_txt, out_img, g), seg_split(dout_txt, dout_img, g), lse, ctx,
+                    seg_split(dq_txt, dq_img, g), seg_split(dk_txt, dk_img, g), seg_split(dv_txt, dv_img, g),
+                    dg_partial, dg, workspace, static_cast<cudaStream_t>(stream));
+}
+
+rlk_status rlk_joint_attn_bwd_streams(const rlk_ja_shape* shape, const void* q_txt, const void* q_img,
+                                      const void* k_txt, const void* k_img, const void* v_txt, const void* v_img,
+                                      const float* g_q_txt, const float* g_k_txt, const float* g_q_img,
+                                      const float* g_k_img, const int32_t* txt_valid_len, const void* out_txt,
+                                      const void* out_img, const void* dout_txt, const void* dout_img,
+                                      const float* lse, const void* ctx, void* dq_txt, void* dq_img, void* dk_txt,
+                                      void* dk_img, void* dv_txt, void* dv_img, float* dg_partial, float* dg,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+    OpScope sc(kOpBwdStreams, shape);
+    return sc.finish(rlk_joint_attn_bwd_streams_impl(
+        shape, q_txt, q_img, k_txt, k_img, v_txt, v_img, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_valid_len, out_txt,
+        out_img, dout_txt, dout_img, lse, ctx, dq_txt, dq_img, dk_txt, dk_img, dv_txt, dv_img, dg_partial, dg,
+        workspace, workspace_bytes, stream));
 }
 
 size_t rlk_joint_attn_unfused_bytes(const rlk_ja_shape* shape, int which) {
@@ -500,7 +605,7 @@ static rlk_status rlk_qk_norm_rope_impl(const rlk_ja_shape* shape, const void* q
     if (st != RLK_OK) return st;
     const Geom g = make_geom(shape);
     const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
-    return run_prologue(g, q, k, gains, ctx, static_cast<cudaStream_t>(stream));
+    return run_prologue(g, seg_concat(q, g), seg_concat(k, g), gains, ctx, static_cast<cudaStream_t>(stream));
 }
 
 rlk_status rlk_qk_norm_rope(const rlk_ja_shape* shape, const void* q, const void* k, const float* g_q_txt,
@@ -566,8 +671,8 @@ static rlk_status rlk_joint_attn_av_gemm_impl(const rlk_ja_shape* shape, const v
     if (st != RLK_OK) return st;
     st = device_ok();
     if (st != RLK_OK) return st;
-    if (launch_av_gemm(g, vl, static_cast<const uint16_t*>(p), alpha, l, static_cast<const uint16_t*>(v),
-                       static_cast<uint16_t*>(out), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (launch_av_gemm(g, vl, static_cast<const uint16_t*>(p), alpha, l, seg_concat(v, g), seg_concat(out, g),
+                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return RLK_ERR_CUDA;
     return RLK_OK;
 }
@@ -607,9 +712,10 @@ static rlk_status rlk_joint_attn_fwd_shard_impl(const rlk_ja_shape* shape, const
     if (st != RLK_OK) return st;
     const CtxLayout l = ctx_layout(g);
     const uint8_t* c = static_cast<const uint8_t*>(ctx);
+    const SegBf16 out_seg = seg_concat(out, g);
     if (launch_attn_fwd_shard(g, vl, reinterpret_cast<const uint16_t*>(c + l.qh),
-                              reinterpret_cast<const uint16_t*>(c + l.kh), static_cast<const uint16_t*>(v), blk_begin,
-                              blk_end, state_in, state_out, static_cast<uint16_t*>(out), lse,
+                              reinterpret_cast<const uint16_t*>(c + l.kh), seg_concat(v, g), blk_begin, blk_end,
+                              state_in, state_out, out != nullptr ? &out_seg : nullptr, lse,
                               static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return RLK_ERR_CUDA;
     return RLK_OK;

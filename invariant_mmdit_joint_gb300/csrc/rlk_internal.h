@@ -35,6 +35,16 @@ struct ValidLen {
     int32_t L[RLK_MAX_BATCH];
 };
 
+// A bf16 activation of shape [B, tokens, H, 128] given as its text rows and
+// its image rows, each with its own batch stride in tokens: either one
+// concatenated tensor (text then image; both strides S) or two separate
+// tensors [B, T_txt, H, 128] and [B, T_img, H, 128] (strides T_txt, T_img),
+// so a caller holding the two streams apart needs no concatenation copy.
+struct SegBf16 {
+    uint16_t* p[2];         // element 0 of the text rows / of the image rows
+    long long bstride[2];   // tokens from sample b to sample b + 1
+};
+
 // Position of token n on axis a (0 frame, 1 row, 2 column).
 __host__ __device__ inline int token_pos(const Geom& g, int n, int a) {
     if (n < g.T_txt) return g.txt_off + n;
@@ -42,6 +52,32 @@ __host__ __device__ inline int token_pos(const Geom& g, int n, int a) {
     int i = n - g.T_txt;
     int r = i / g.gw;
     return a == 1 ? r - g.ctr_h : (i - r * g.gw) - g.ctr_w;
+}
+
+// Address of (b, token n, head h, dim 0) in its segment's buffer.
+__host__ __device__ inline uint16_t* seg_row(const SegBf16& t, const Geom& g, int b, int n, int h) {
+    const int seg = n < g.T_txt ? 0 : 1;
+    const long long nn = seg == 0 ? n : n - g.T_txt;
+    return t.p[seg] + (((long long)b * t.bstride[seg] + nn) * g.H + h) * kHeadDim;
+}
+
+// The two segment views of one concatenated [B, S, H, 128] tensor, and of
+// two separate stream tensors.
+inline SegBf16 seg_concat(const void* base, const Geom& g) {
+    SegBf16 t;
+    uint16_t* p = static_cast<uint16_t*>(const_cast<void*>(base));
+    t.p[0] = p;
+    t.p[1] = p + (size_t)g.T_txt * g.H * kHeadDim;
+    t.bstride[0] = t.bstride[1] = g.S;
+    return t;
+}
+inline SegBf16 seg_split(const void* txt, const void* img, const Geom& g) {
+    SegBf16 t;
+    t.p[0] = static_cast<uint16_t*>(const_cast<void*>(txt));
+    t.p[1] = static_cast<uint16_t*>(const_cast<void*>(img));
+    t.bstride[0] = g.T_txt;
+    t.bstride[1] = g.T_img;
+    return t;
 }
 
 // Axis owning RoPE pair k (dims 2k, 2k+1) of a 128-wide head row.
@@ -64,7 +100,10 @@ void timing_end(int kernel_id, cudaStream_t s);
 // Operator trace (rlk_host.cu). Every C ABI entry point that can launch work
 // opens a scope; the outermost scope of a thread owns one record, which the
 // launches inside it fill and finish() appends to the log.
-enum OpKind { kOpFwd = 0, kOpBwd, kOpFwdNoalloc, kOpNormRope, kOpQkGemm, kOpSoftmax, kOpAvGemm, kOpFwdShard };
+enum OpKind {
+    kOpFwd = 0, kOpBwd, kOpFwdNoalloc, kOpNormRope, kOpQkGemm, kOpSoftmax, kOpAvGemm, kOpFwdShard,
+    kOpFwdStreams, kOpBwdStreams
+};
 class OpScope {
    public:
     OpScope(OpKind kind, const rlk_ja_shape* shape);
@@ -79,17 +118,17 @@ class OpScope {
 // ---- launchers (each returns the cudaGetLastError() of its launch) ----
 // k_prologue.cu
 cudaError_t launch_rope_table(const Geom& g, float2* tab, cudaStream_t s);
-cudaError_t launch_prologue(const Geom& g, const uint16_t* q, const uint16_t* k,
+cudaError_t launch_prologue(const Geom& g, const SegBf16& q, const SegBf16& k,
                             const float* const gains[4], const float2* tab,
                             uint16_t* qh, uint16_t* kh, float* rq, float* rk,
                             cudaStream_t s);
-cudaError_t launch_bwd_pre(const Geom& g, const uint16_t* out, const uint16_t* dout,
+cudaError_t launch_bwd_pre(const Geom& g, const SegBf16& out, const SegBf16& dout,
                            const float* lse, float* lse2_p, float* delta_p, cudaStream_t s);
-cudaError_t launch_norm_rope_bwd(const Geom& g, const uint16_t* q, const uint16_t* k,
+cudaError_t launch_norm_rope_bwd(const Geom& g, const SegBf16& q, const SegBf16& k,
                                  const float* const gains[4], const float2* tab,
                                  const float* rq, const float* rk,
                                  const float* dqh, const float* dkh,
-                                 uint16_t* dq, uint16_t* dk, float* dg_chunks,
+                                 const SegBf16& dq, const SegBf16& dk, float* dg_chunks,
                                  cudaStream_t s);
 cudaError_t launch_dg_fold(const Geom& g, const float* dg_chunks, float* dg_partial,
                            float* dg, cudaStream_t s);
@@ -97,23 +136,24 @@ int probe_prologue_tu(void);
 
 // k_attn_fwd.cu
 cudaError_t launch_attn_fwd(const Geom& g, const ValidLen& vl, const uint16_t* qh,
-                            const uint16_t* kh, const uint16_t* v, uint16_t* out,
+                            const uint16_t* kh, const SegBf16& v, const SegBf16& out,
                             float* lse, cudaStream_t s);
 // One key shard of the forward: column blocks [blk_begin, blk_end) of the
 // fused order, with the online-softmax state passed from and to the
-// neighbouring shards (state: m, l fp32 [rows] then O fp32 [rows, 128]).
+// neighbouring shards (state: m, l fp32 [rows] then O fp32 [rows, 128]);
+// out is null except for the last shard.
 cudaError_t launch_attn_fwd_shard(const Geom& g, const ValidLen& vl, const uint16_t* qh,
-                                  const uint16_t* kh, const uint16_t* v, int blk_begin, int blk_end,
-                                  const float* state_in, float* state_out, uint16_t* out, float* lse,
-                                  cudaStream_t s);
+                                  const uint16_t* kh, const SegBf16& v, int blk_begin, int blk_end,
+                                  const float* state_in, float* state_out, const SegBf16* out,
+                                  float* lse, cudaStream_t s);
 int probe_fwd_tu(void);
 int read_and_clear_status_fwd(cudaStream_t s);
 
 // k_attn_bwd.cu
 cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16_t* qh,
-                                 const uint16_t* kh, const uint16_t* v,
-                                 const uint16_t* dout, const float* lse2_p,
-                                 const float* delta_p, uint16_t* dv, float* dkh,
+                                 const uint16_t* kh, const SegBf16& v,
+                                 const SegBf16& dout, const float* lse2_p,
+                                 const float* delta_p, const SegBf16& dv, float* dkh,
                                  uint8_t* ds_tiles, cudaStream_t s);
 cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t* kh,
                                const uint8_t* ds_tiles, float* dqh, cudaStream_t s);
@@ -127,7 +167,7 @@ cudaError_t launch_qk_gemm(const Geom& g, const ValidLen& vl, const uint16_t* qh
 cudaError_t launch_softmax(const Geom& g, const ValidLen& vl, const float* scores, uint16_t* p,
                            float* alpha, float* l, float* lse, cudaStream_t s);
 cudaError_t launch_av_gemm(const Geom& g, const ValidLen& vl, const uint16_t* p, const float* alpha,
-                           const float* l, const uint16_t* v, uint16_t* out, cudaStream_t s);
+                           const float* l, const SegBf16& v, const SegBf16& out, cudaStream_t s);
 int probe_unfused_tu(void);
 int read_and_clear_status_unfused(cudaStream_t s);
 

@@ -291,3 +291,33 @@ def test_key_shard_forward_fails_closed(L):
     import torch
     if not torch.cuda.is_available():
         assert shard(0, 2, st_in=None) == 5 and shard(2, 5, st_out=None, out=p, lse=p) == 5
+
+
+def test_stream_pair_calls_fail_closed(L):
+    s = pkg.Shape.make(2, 16, 8, 8, 2)
+    p = 1 << 20
+    vl = (ctypes.c_int32 * 2)(3, 5)
+
+    def fwd(qt=p, qi=p, vt=p, ot=p, oi=p, lse=p, shape=s, lens=vl):
+        return L.rlk_joint_attn_fwd_streams(ctypes.byref(shape), qt, qi, p, p, vt, p, p, p, p, p, lens, ot, oi, lse,
+                                            p, None)
+    assert fwd(qi=None) == 1          # the image buffer is required
+    assert fwd(qt=None) == 1          # the text buffer too, when T_txt > 0
+    assert fwd(oi=p + 8) == 3
+    assert fwd(vt=p + 2) == 3
+    assert fwd(lse=p + 4) == 3
+    assert fwd(lens=(ctypes.c_int32 * 2)(3, 17)) == 1
+    no_text = pkg.Shape.make(2, 0, 8, 8, 2)
+    zero = (ctypes.c_int32 * 2)(0, 0)
+    ws = pkg.rlk_joint_attn_bwd_workspace_bytes(s)
+
+    def bwd(wsb=ws, dvt=p):
+        return L.rlk_joint_attn_bwd_streams(ctypes.byref(s), p, p, p, p, p, p, p, p, p, p, vl, p, p, p, p, p, p,
+                                            p, p, p, p, dvt, p, None, p, p, wsb, None)
+    assert bwd(wsb=ws - 1) == 4
+    assert bwd(dvt=None) == 1
+    import torch
+    if not torch.cuda.is_available():
+        # well formed (text buffers may be absent without text) up to the device check
+        assert fwd(qt=None, vt=None, ot=None, shape=no_text, lens=zero) != 1
+        assert fwd() == 5 and bwd() == 5
