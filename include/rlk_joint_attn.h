@@ -289,6 +289,41 @@ rlk_status rlk_joint_attn_bwd_streams(const rlk_ja_shape* shape,
                                       float* dg_partial, float* dg,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * The attention's adjacent producer: row qkv_bias_gemm of the RFC's WS1
+ * table ("per-stream packed QKV + bias"; the WS1 kernel list: 3072 ->
+ * 3 x 3072 + bias, one weight set per stream), with qk_rmsnorm and
+ * multi_axis_rope fused into its epilogue.
+ *   x_txt, x_img   bf16 [B, T_txt, C] and [B, grid_h*grid_w, C], C = H * 128
+ *   w_txt, w_img   bf16 [3C, C]: output feature rows (the nn.Linear layout),
+ *                  Q features first (head-major: feature h*128 + d), then K, V
+ *   b_txt, b_img   bf16 [3C]
+ * Q, K, V = bf16(x w^T + b) per stream (fp32 accumulation in a fixed order,
+ * one rounding). With `ctx` non-NULL the epilogue also writes the context
+ * rlk_joint_attn_fwd() would write for these Q, K (the normed, rotated q^
+ * and k^, the RMSNorm factors and the cos/sin table), byte for byte what
+ * rlk_qk_norm_rope() gives on the stored Q, K; the gains are then required,
+ * and the pre-norm Q and K are stored only if their buffers are given
+ * (a backward needs them). With `ctx` NULL, Q and K are required and the
+ * gains ignored. V is always stored. Outputs q_*, k_*, v_* are bf16
+ * [B, T_s, H, 128]; a *_txt pointer may be NULL only when T_txt == 0. */
+rlk_status rlk_qkv_bias_gemm(const rlk_ja_shape* shape,
+                             const void* x_txt, const void* x_img,
+                             const void* w_txt, const void* w_img,
+                             const void* b_txt, const void* b_img,
+                             const float* g_q_txt, const float* g_k_txt,
+                             const float* g_q_img, const float* g_k_img, void* ctx,
+                             void* q_txt, void* q_img, void* k_txt, void* k_img,
+                             void* v_txt, void* v_img, void* stream);
+
+/* The forward's attention from a context already holding q^ and k^ (written
+ * by rlk_qkv_bias_gemm(), rlk_qk_norm_rope() or the forward): out and lse
+ * are those of rlk_joint_attn_fwd_streams() on the same inputs. */
+rlk_status rlk_joint_attn_fwd_ctx(const rlk_ja_shape* shape, const void* ctx,
+                                  const void* v_txt, const void* v_img,
+                                  const int32_t* txt_valid_len,
+                                  void* out_txt, void* out_img, float* lse, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device-side error word
  * that bounded waits in the kernels set when they give up. Returns RLK_OK,
  * RLK_ERR_DEVICE_TIMEOUT, or RLK_ERR_CUDA if the stream reported an error. */
@@ -364,8 +399,9 @@ rlk_status rlk_joint_attn_fwd_shard(const rlk_ja_shape* shape, const void* ctx, 
  * fingerprint and selected backend, and says there is no silent fallback.
  * While tracing is on, every entry point that can launch work (the fused
  * forward and backward with concatenated or separate streams, the
- * allocation-free forward, the key-shard forward and the standalone
- * operators) appends one record when it returns, including calls refused
+ * allocation-free forward, the key-shard and from-context forwards, the
+ * QKV projection and the standalone operators) appends one record when it
+ * returns, including calls refused
  * during validation (status != RLK_OK, no kernel listed, actual backend
  * "none"). The kernels listed are the ones the call enqueued, in launch
  * order. Records live in a ring of RLK_OP_TRACE_CAP entries in host memory;
@@ -408,7 +444,7 @@ const char* rlk_strerror(int status);
 /* Kernel timing for benchmarks. kernel ids: 0 rope table, 1 prologue,
  * 2 attention forward, 3 backward preprocess, 4 dK/dV, 5 dQ,
  * 6 RoPE/RMSNorm backward, 7 gain-gradient fold, 8 qk_gemm, 9 softmax,
- * 10 av_gemm, 11 forward key shard.
+ * 10 av_gemm, 11 forward key shard, 12 qkv_bias_gemm.
  * rlk_kernel_timing(1) makes later calls record a CUDA event pair around
  * every launch (up to 4096 launches per kernel id); rlk_kernel_timing(0)
  * stops and clears. rlk_kernel_timing_read() waits for the recorded events

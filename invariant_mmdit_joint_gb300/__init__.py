@@ -27,7 +27,7 @@ __all__ = [
     "rlk_joint_attn_softmax", "rlk_joint_attn_av_gemm", "UNFUSED", "JointAttention",
     "rlk_op_trace_enable", "rlk_op_trace_count", "rlk_op_trace_read", "op_trace", "OP_TRACE_CAP",
     "rlk_joint_attn_state_bytes", "rlk_joint_attn_fwd_shard", "rlk_joint_attn_fwd_streams",
-    "rlk_joint_attn_bwd_streams",
+    "rlk_joint_attn_bwd_streams", "rlk_qkv_bias_gemm", "rlk_joint_attn_fwd_ctx",
     "EXPORTED_SYMBOLS", "KERNEL_IDS",
 ]
 
@@ -45,7 +45,7 @@ STATUS_NAMES = {
 KERNEL_IDS = {
     "rope_table": 0, "prologue": 1, "attn_fwd": 2, "bwd_pre": 3,
     "bwd_dkdv": 4, "bwd_dq": 5, "norm_rope_bwd": 6, "dg_fold": 7,
-    "qk_gemm": 8, "softmax": 9, "av_gemm": 10, "attn_fwd_shard": 11,
+    "qk_gemm": 8, "softmax": 9, "av_gemm": 10, "attn_fwd_shard": 11, "qkv_gemm": 12,
 }
 # which intermediate rlk_joint_attn_unfused_bytes() sizes
 UNFUSED = {"scores": 0, "p": 1, "alpha": 2, "rows": 3}
@@ -59,7 +59,8 @@ EXPORTED_SYMBOLS = (
     "rlk_joint_attn_softmax", "rlk_joint_attn_av_gemm",
     "rlk_op_trace_enable", "rlk_op_trace_count", "rlk_op_trace_read",
     "rlk_joint_attn_state_bytes", "rlk_joint_attn_fwd_shard",
-    "rlk_joint_attn_fwd_streams", "rlk_joint_attn_bwd_streams",
+    "rlk_joint_attn_fwd_streams", "rlk_joint_attn_bwd_streams", "rlk_qkv_bias_gemm",
+    "rlk_joint_attn_fwd_ctx",
 )
 OP_TRACE_CAP = 256
 OP_TRACE_MAX_KERNELS = 8
@@ -190,6 +191,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     L.rlk_joint_attn_fwd_streams.restype = i32
     L.rlk_joint_attn_bwd_streams.argtypes = [shp] + [vp] * 10 + [i32p] + [vp] * 14 + [sz, vp]
     L.rlk_joint_attn_bwd_streams.restype = i32
+    L.rlk_qkv_bias_gemm.argtypes = [shp] + [vp] * 18
+    L.rlk_qkv_bias_gemm.restype = i32
+    L.rlk_joint_attn_fwd_ctx.argtypes = [shp, vp, vp, vp, i32p, vp, vp, vp, vp]
+    L.rlk_joint_attn_fwd_ctx.restype = i32
     L.rlk_op_trace_enable.argtypes = [i32]
     L.rlk_op_trace_enable.restype = i32
     L.rlk_op_trace_count.argtypes = []
@@ -350,6 +355,26 @@ def rlk_joint_attn_bwd_streams(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_im
         _ptr(dq[0]), _ptr(dq[1]), _ptr(dk[0]), _ptr(dk[1]), _ptr(dv[0]), _ptr(dv[1]), _ptr(dg_partial), _ptr(dg),
         _ptr(workspace), int(workspace_bytes), _stream_handle(stream))
     _check(rc, "rlk_joint_attn_bwd_streams")
+
+
+def rlk_qkv_bias_gemm(shape, x, w, b, gains, ctx, q, k, v, stream=None) -> None:
+    """Per-stream QKV projection; x, w, b, q, k, v are (text, image) pairs
+    (q, k may be (None, None) when ctx is given); gains a [4, 128] tensor or
+    None (plain mode, ctx None)."""
+    g = [None] * 4 if gains is None else [gains[0], gains[1], gains[2], gains[3]]
+    rc = lib().rlk_qkv_bias_gemm(
+        ctypes.byref(shape), _ptr(x[0]), _ptr(x[1]), _ptr(w[0]), _ptr(w[1]), _ptr(b[0]), _ptr(b[1]),
+        *[_ptr(t) for t in g], _ptr(ctx), _ptr(q[0]), _ptr(q[1]), _ptr(k[0]), _ptr(k[1]), _ptr(v[0]), _ptr(v[1]),
+        _stream_handle(stream))
+    _check(rc, "rlk_qkv_bias_gemm")
+
+
+def rlk_joint_attn_fwd_ctx(shape, ctx, v, txt_valid_len, out, lse, stream=None) -> None:
+    """Attention from a prepared context; v and out are (text, image) pairs."""
+    rc = lib().rlk_joint_attn_fwd_ctx(ctypes.byref(shape), _ptr(ctx), _ptr(v[0]), _ptr(v[1]),
+                                      _lengths(txt_valid_len), _ptr(out[0]), _ptr(out[1]), _ptr(lse),
+                                      _stream_handle(stream))
+    _check(rc, "rlk_joint_attn_fwd_ctx")
 
 
 def rlk_op_trace_enable(enable: bool) -> None:

@@ -55,7 +55,7 @@ __device__ __forceinline__ void norm_rope_row(const uint4 xv, const float* __res
     for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
 #pragma unroll
     for (int m = 8; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-    float r = 1.0f / sqrtf(ss * (1.0f / 128.0f) + eps);
+    float r = 1.0f / sqrtf(fmaf(ss, 1.0f / 128.0f, eps));
     r_out = r;
     const float4 g0 = __ldg(reinterpret_cast<const float4*>(gain) + 2 * lane16);
     const float4 g1 = __ldg(reinterpret_cast<const float4*>(gain) + 2 * lane16 + 1);
@@ -81,7 +81,7 @@ __device__ __forceinline__ void norm_rope_row(const uint4 xv, const float* __res
 // all four 16-byte input loads of a lane are issued before any arithmetic.
 constexpr int kPrologueRowsPerCta = 32;
 
-__global__ void __launch_bounds__(256) prologue_kernel(
+__global__ void __launch_bounds__(256, 4) prologue_kernel(
     Geom g, const SegBf16 q, const SegBf16 k,
     const float* __restrict__ gq_txt, const float* __restrict__ gk_txt,
     const float* __restrict__ gq_img, const float* __restrict__ gk_img,
@@ -106,8 +106,14 @@ __global__ void __launch_bounds__(256) prologue_kernel(
         const long long bn = row / g.H;
         nn[u] = (int)(bn % g.S);
         bb[u] = (int)(bn / g.S);
-        xq[u] = __ldg(reinterpret_cast<const uint4*>(seg_row(q, g, bb[u], nn[u], hh[u]) + 8 * lane16));
-        xk[u] = __ldg(reinterpret_cast<const uint4*>(seg_row(k, g, bb[u], nn[u], hh[u]) + 8 * lane16));
+        // q and k share their segment strides (both calls pass them alike),
+        // so one offset addresses both
+        const bool img = nn[u] >= g.T_txt;
+        const long long off =
+            (((long long)bb[u] * (img ? q.bstride[1] : q.bstride[0]) + (img ? nn[u] - g.T_txt : nn[u])) * g.H +
+             hh[u]) * kHeadDim + 8 * lane16;
+        xq[u] = __ldg(reinterpret_cast<const uint4*>((img ? q.p[1] : q.p[0]) + off));
+        xk[u] = __ldg(reinterpret_cast<const uint4*>((img ? k.p[1] : k.p[0]) + off));
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -200,21 +206,33 @@ __global__ void __launch_bounds__(256) norm_rope_bwd_kernel(
     const float* gain = is_k ? (txt_chunk ? gk_txt : gk_img) : (txt_chunk ? gq_txt : gq_img);
     const float* r_all = is_k ? rk : rq;
     const float* dyh = is_k ? dkh : dqh;
-    const SegBf16 x_all = is_k ? k : q;
-    const SegBf16 dx_all = is_k ? dk : dq;
+
     const size_t bh = (size_t)b * g.H + h;
     const float4 gv = __ldg(reinterpret_cast<const float4*>(gain) + lane);
     const int k0 = 2 * lane, k1 = 2 * lane + 1;
     const int ax = pair_axis(k0);  // both pairs of a lane share an axis
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const int row0 = seg_start + (warp % 4) * kNrbRowsPerWarp;
+    // the chunk lies in one segment of one sample: consecutive tokens are
+    // H * 128 elements apart in either layout. (Pointers are selected one by
+    // one: a reference to a parameter chosen at run time would put the
+    // parameters in local memory.)
+    const int sg = txt_chunk ? 0 : 1;
+    const uint16_t* x_seg = is_k ? (sg ? k.p[1] : k.p[0]) : (sg ? q.p[1] : q.p[0]);
+    uint16_t* dx_seg = is_k ? (sg ? dk.p[1] : dk.p[0]) : (sg ? dq.p[1] : dq.p[0]);
+    const long long x_bs = is_k ? (sg ? k.bstride[1] : k.bstride[0]) : (sg ? q.bstride[1] : q.bstride[0]);
+    const long long dx_bs = is_k ? (sg ? dk.bstride[1] : dk.bstride[0]) : (sg ? dq.bstride[1] : dq.bstride[0]);
+    const long long n0 = min(row0, seg_end - 1) - (sg ? g.T_txt : 0);  // token of row0 inside its segment
+    const uint16_t* x_row0 = x_seg + (((long long)b * x_bs + n0) * g.H + h) * kHeadDim + 4 * lane;
+    uint16_t* dx_row0 = dx_seg + (((long long)b * dx_bs + n0) * g.H + h) * kHeadDim + 4 * lane;
+    const size_t token_stride = (size_t)g.H * kHeadDim;
     for (int i = 0; i < kNrbRowsPerWarp; ++i) {
         const int n = row0 + i;
         if (n >= seg_end) break;
         const float2* trow = tab + (size_t)(token_pos(g, n, ax) - g.p_lo) * kPairs;
         const float2 c0 = trow[k0], c1 = trow[k1];
         const float4 dy = *reinterpret_cast<const float4*>(dyh + (bh * g.S + n) * kHeadDim + 4 * lane);
-        const uint2 xv = *reinterpret_cast<const uint2*>(seg_row(x_all, g, b, n, h) + 4 * lane);
+        const uint2 xv = *reinterpret_cast<const uint2*>(x_row0 + i * token_stride);
         const float r = r_all[bh * g.S + n];
         float u[4];
         u[0] = fmaf(dy.x, c0.x, dy.y * c0.y);
@@ -240,8 +258,7 @@ __global__ void __launch_bounds__(256) norm_rope_bwd_kernel(
             dx[j] = r * fmaf(-xh[j], c, w[j]);
             acc[j] = fmaf(u[j], xh[j], acc[j]);
         }
-        *reinterpret_cast<uint2*>(seg_row(dx_all, g, b, n, h) + 4 * lane) =
-            make_uint2(pack_bf16(dx[0], dx[1]), pack_bf16(dx[2], dx[3]));
+        *reinterpret_cast<uint2*>(dx_row0 + i * token_stride) = make_uint2(pack_bf16(dx[0], dx[1]), pack_bf16(dx[2], dx[3]));
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) red[warp][4 * lane + j] = acc[j];

@@ -128,7 +128,8 @@ std::mutex g_dev_mu;
 int g_dev_state[kMaxDevices];  // 0 unknown, 1 ok, 2 wrong arch, 3 fast math, 4 cuda error
 
 int strict_all_units() {
-    const int r[5] = {probe_host_tu(), probe_prologue_tu(), probe_fwd_tu(), probe_bwd_tu(), probe_unfused_tu()};
+    const int r[6] = {probe_host_tu(), probe_prologue_tu(), probe_fwd_tu(), probe_bwd_tu(), probe_unfused_tu(),
+                      probe_qkv_tu()};
     for (int v : r)
         if (v < 0) return -1;
     for (int v : r)
@@ -280,11 +281,16 @@ const OpInfo kOps[] = {
      "from the same bf16 dS, one bf16 cast of dQ dK dV; no TF32, no fast math",
      "dK/dV: query tiles ascending; dQ: key tiles in the forward order; dg: 64-token chunks, then h, "
      "then b ascending"},
+    {"qkv_bias_gemm(+qk_rmsnorm+multi_axis_rope)", "rlk_qkv_bias_gemm",
+     "bf16 X W operands, fp32 TMEM accumulators, + bf16 bias, one bf16 rounding of Q K V; the fused epilogue "
+     "then runs the prologue arithmetic (IEEE sqrt and division)",
+     "K in ascending steps of 64 (16 per MMA); no split-K; norm: 16 partials of 8 then a fixed tree"},
+    {"joint_attention_fused (from context)", "rlk_joint_attn_fwd_ctx", kFwdPolicy, kFwdOrder},
 };
 const char* const kKernelNames[kNumKernelIds] = {
     "rope_table_kernel", "prologue_kernel", "attn_fwd_tc_kernel", "bwd_pre_kernel",
     "attn_bwd_dkdv_tc_kernel", "attn_bwd_dq_tc_kernel", "norm_rope_bwd_kernel", "dg_fold_kernels",
-    "qk_gemm_kernel", "softmax_kernel", "av_gemm_kernel", "attn_fwd_tc_kernel<shard>"};
+    "qk_gemm_kernel", "softmax_kernel", "av_gemm_kernel", "attn_fwd_tc_kernel<shard>", "qkv_gemm_kernel"};
 
 struct OpLog {
     std::mutex mu;
@@ -588,6 +594,94 @@ rlk_status rlk_joint_attn_bwd_streams(const rlk_ja_shape* shape, const void* q_t
         workspace, workspace_bytes, stream));
 }
 
+static rlk_status rlk_qkv_bias_gemm_impl(const rlk_ja_shape* shape, const void* x_txt, const void* x_img,
+                                         const void* w_txt, const void* w_img, const void* b_txt, const void* b_img,
+                                         const float* g_q_txt, const float* g_k_txt, const float* g_q_img,
+                                         const float* g_k_img, void* ctx, void* q_txt, void* q_img, void* k_txt,
+                                         void* k_img, void* v_txt, void* v_img, void* stream) {
+    rlk_status why = RLK_OK;
+    if (!shape_ok(shape, &why)) return why;
+    const Geom g = make_geom(shape);
+    const bool fused = ctx != nullptr;
+    // inputs and V are required; Q and K outputs are required without a
+    // context and optional with one (a stream pair, or neither)
+    rlk_status st = check_pairs(g, {{x_txt, x_img}, {w_txt, w_img}, {b_txt, b_img}, {v_txt, v_img}});
+    if (st != RLK_OK) return st;
+    const bool store_q = q_img != nullptr || q_txt != nullptr;
+    const bool store_k = k_img != nullptr || k_txt != nullptr;
+    if (!fused && (!store_q || !store_k)) return RLK_ERR_INVALID_ARG;
+    if (store_q && (st = check_pairs(g, {{q_txt, q_img}})) != RLK_OK) return st;
+    if (store_k && (st = check_pairs(g, {{k_txt, k_img}})) != RLK_OK) return st;
+    if (fused && (st = check_ptrs({g_q_txt, g_k_txt, g_q_img, g_k_img, ctx}, {})) != RLK_OK) return st;
+    st = device_ok();
+    if (st != RLK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint16_t* x[2] = {static_cast<const uint16_t*>(x_txt), static_cast<const uint16_t*>(x_img)};
+    const uint16_t* w[2] = {static_cast<const uint16_t*>(w_txt), static_cast<const uint16_t*>(w_img)};
+    const uint16_t* bias[2] = {static_cast<const uint16_t*>(b_txt), static_cast<const uint16_t*>(b_img)};
+    const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
+    uint16_t *qh = nullptr, *kh = nullptr;
+    float *rq = nullptr, *rk = nullptr;
+    const float2* tab = nullptr;
+    if (fused) {
+        const CtxLayout l = ctx_layout(g);
+        uint8_t* c = static_cast<uint8_t*>(ctx);
+        qh = reinterpret_cast<uint16_t*>(c + l.qh);
+        kh = reinterpret_cast<uint16_t*>(c + l.kh);
+        rq = reinterpret_cast<float*>(c + l.rq);
+        rk = reinterpret_cast<float*>(c + l.rk);
+        float2* t = reinterpret_cast<float2*>(c + l.tab);
+        if (launch_rope_table(g, t, s) != cudaSuccess) return RLK_ERR_CUDA;
+        tab = t;
+    }
+    const SegBf16 none = seg_split(nullptr, nullptr, g);
+    if (launch_qkv_gemm(g, x, w, bias, gains, qh, kh, rq, rk, tab, store_q ? seg_split(q_txt, q_img, g) : none,
+                        store_k ? seg_split(k_txt, k_img, g) : none, seg_split(v_txt, v_img, g), store_q, store_k,
+                        s) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status rlk_qkv_bias_gemm(const rlk_ja_shape* shape, const void* x_txt, const void* x_img, const void* w_txt,
+                             const void* w_img, const void* b_txt, const void* b_img, const float* g_q_txt,
+                             const float* g_k_txt, const float* g_q_img, const float* g_k_img, void* ctx,
+                             void* q_txt, void* q_img, void* k_txt, void* k_img, void* v_txt, void* v_img,
+                             void* stream) {
+    OpScope sc(kOpQkvGemm, shape);
+    return sc.finish(rlk_qkv_bias_gemm_impl(shape, x_txt, x_img, w_txt, w_img, b_txt, b_img, g_q_txt, g_k_txt,
+                                            g_q_img, g_k_img, ctx, q_txt, q_img, k_txt, k_img, v_txt, v_img, stream));
+}
+
+static rlk_status rlk_joint_attn_fwd_ctx_impl(const rlk_ja_shape* shape, const void* ctx, const void* v_txt,
+                                             const void* v_img, const int32_t* txt_valid_len, void* out_txt,
+                                             void* out_img, float* lse, void* stream) {
+    Geom g;
+    ValidLen vl;
+    rlk_status st = common_checks(shape, txt_valid_len, &g, &vl);
+    if (st != RLK_OK) return st;
+    st = check_pairs(g, {{v_txt, v_img}, {out_txt, out_img}});
+    if (st != RLK_OK) return st;
+    st = check_ptrs({ctx}, {lse});
+    if (st != RLK_OK) return st;
+    st = device_ok();
+    if (st != RLK_OK) return st;
+    const CtxLayout l = ctx_layout(g);
+    const uint8_t* c = static_cast<const uint8_t*>(ctx);
+    if (launch_attn_fwd(g, vl, reinterpret_cast<const uint16_t*>(c + l.qh), reinterpret_cast<const uint16_t*>(c + l.kh),
+                        seg_split(v_txt, v_img, g), seg_split(out_txt, out_img, g), lse,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status rlk_joint_attn_fwd_ctx(const rlk_ja_shape* shape, const void* ctx, const void* v_txt, const void* v_img,
+                                  const int32_t* txt_valid_len, void* out_txt, void* out_img, float* lse,
+                                  void* stream) {
+    OpScope sc(kOpFwdCtx, shape);
+    return sc.finish(rlk_joint_attn_fwd_ctx_impl(shape, ctx, v_txt, v_img, txt_valid_len, out_txt, out_img, lse,
+                                                 stream));
+}
+
 size_t rlk_joint_attn_unfused_bytes(const rlk_ja_shape* shape, int which) {
     rlk_status why;
     if (!shape_ok(shape, &why)) return 0;
@@ -735,8 +829,9 @@ rlk_status rlk_joint_attn_check_status(void* stream) {
     const int a = read_and_clear_status_fwd(s);
     const int b = read_and_clear_status_bwd(s);
     const int c = read_and_clear_status_unfused(s);
-    if (a < 0 || b < 0 || c < 0) return RLK_ERR_CUDA;
-    if (a != 0 || b != 0 || c != 0) return RLK_ERR_DEVICE_TIMEOUT;
+    const int d = read_and_clear_status_qkv(s);
+    if (a < 0 || b < 0 || c < 0 || d < 0) return RLK_ERR_CUDA;
+    if (a != 0 || b != 0 || c != 0 || d != 0) return RLK_ERR_DEVICE_TIMEOUT;
     return RLK_OK;
 }
 

@@ -55,10 +55,14 @@ __host__ __device__ inline int token_pos(const Geom& g, int n, int a) {
 }
 
 // Address of (b, token n, head h, dim 0) in its segment's buffer.
+// (Selects on constant indices, not t.p[seg]: a runtime index into a kernel
+// parameter's array would make the compiler copy it to local memory.)
 __host__ __device__ inline uint16_t* seg_row(const SegBf16& t, const Geom& g, int b, int n, int h) {
-    const int seg = n < g.T_txt ? 0 : 1;
-    const long long nn = seg == 0 ? n : n - g.T_txt;
-    return t.p[seg] + (((long long)b * t.bstride[seg] + nn) * g.H + h) * kHeadDim;
+    const bool img = n >= g.T_txt;
+    uint16_t* const base = img ? t.p[1] : t.p[0];
+    const long long bs = img ? t.bstride[1] : t.bstride[0];
+    const long long nn = img ? n - g.T_txt : n;
+    return base + (((long long)b * bs + nn) * g.H + h) * kHeadDim;
 }
 
 // The two segment views of one concatenated [B, S, H, 128] tensor, and of
@@ -89,7 +93,7 @@ __host__ __device__ inline int pair_axis(int k) {
 enum KernelId {
     kKRopeTable = 0, kKPrologue = 1, kKAttnFwd = 2, kKBwdPre = 3,
     kKBwdDkDv = 4, kKBwdDq = 5, kKNormRopeBwd = 6, kKDgFold = 7,
-    kKQkGemm = 8, kKSoftmax = 9, kKAvGemm = 10, kKAttnFwdShard = 11, kNumKernelIds = 12
+    kKQkGemm = 8, kKSoftmax = 9, kKAvGemm = 10, kKAttnFwdShard = 11, kKQkvGemm = 12, kNumKernelIds = 13
 };
 
 // Launch timing hooks (rlk_host.cu): bracket one launch with events.
@@ -102,7 +106,7 @@ void timing_end(int kernel_id, cudaStream_t s);
 // launches inside it fill and finish() appends to the log.
 enum OpKind {
     kOpFwd = 0, kOpBwd, kOpFwdNoalloc, kOpNormRope, kOpQkGemm, kOpSoftmax, kOpAvGemm, kOpFwdShard,
-    kOpFwdStreams, kOpBwdStreams
+    kOpFwdStreams, kOpBwdStreams, kOpQkvGemm, kOpFwdCtx
 };
 class OpScope {
    public:
@@ -170,6 +174,17 @@ cudaError_t launch_av_gemm(const Geom& g, const ValidLen& vl, const uint16_t* p,
                            const float* l, const SegBf16& v, const SegBf16& out, cudaStream_t s);
 int probe_unfused_tu(void);
 int read_and_clear_status_unfused(cudaStream_t s);
+
+// k_qkv_gemm.cu: per-stream QKV projection Y = X W^T + b (both streams in
+// one launch), stored as bf16; with qh != null the epilogue also runs
+// qk_rmsnorm + multi_axis_rope into the context (q^, k^, r) from the table
+// tab, and writes the pre-norm Q / K only if store_q / store_k.
+cudaError_t launch_qkv_gemm(const Geom& g, const uint16_t* const x[2], const uint16_t* const w[2],
+                            const uint16_t* const bias[2], const float* const gains[4], uint16_t* qh,
+                            uint16_t* kh, float* rq, float* rk, const float2* tab, const SegBf16& q,
+                            const SegBf16& k, const SegBf16& v, bool store_q, bool store_k, cudaStream_t s);
+int probe_qkv_tu(void);
+int read_and_clear_status_qkv(cudaStream_t s);
 
 // Tile geometry of the attention kernels (reported by the trace record).
 extern const int kFwdBlockQ, kFwdBlockKV;

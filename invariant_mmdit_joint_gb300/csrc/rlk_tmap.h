@@ -45,6 +45,14 @@ inline bool rows_bf16(CUtensorMap* m, const void* base, uint64_t rows) {
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box);
 }
 
+// bf16 row-major [rows, cols] (cols a multiple of 64), box 64 x box_rows
+inline bool mat_bf16(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows) {
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box);
+}
+
 // bf16 [B, S, H, 128] as 4-D (d, h, token, b), box 64 x 1 x 128 x 1; seg
 // -1 = all S tokens, 0 = the text rows [0, T_txt), 1 = the image rows
 // [T_txt, S) (a box reaching past the segment is clipped there). A

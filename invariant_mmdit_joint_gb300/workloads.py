@@ -157,3 +157,28 @@ def credited_flops(w: Workload, valid_len: Sequence[int] | None = None,
     vl = list(w.valid_len) if valid_len is None else list(valid_len)
     gemm = sum(2.0 * D * w.S * (w.T_img + L) for L in vl) * w.H
     return {"gemm": gemm, "fwd": 2 * gemm, "bwd": 5 * gemm, "fwd_bwd": 7 * gemm}
+
+
+QKV_STREAM = 1_000_081
+
+
+def make_qkv_inputs(w: Workload, seed: int) -> dict:
+    """Seeded inputs of the per-stream QKV projection (bf16 bits, uint16):
+    activations x_txt [B, T_txt, C] and x_img [B, T_img, C] ~ N(0, 1),
+    weights w_txt, w_img [3C, C] ~ N(0, 1/C) (the usual initial scale, so
+    the projections are O(1)) and biases b_txt, b_img [3C] ~ N(0, 0.02^2),
+    C = H * D, all drawn from ``default_rng([seed, QKV_STREAM])``."""
+    C = w.H * HEAD_DIM
+    rng = np.random.default_rng([seed, QKV_STREAM])
+    out = {}
+    for s, T in (("txt", w.T_txt), ("img", w.T_img)):
+        out["x_" + s] = f32_to_bf16_bits(rng.standard_normal((w.B, T, C), dtype=np.float32))
+        out["w_" + s] = f32_to_bf16_bits(rng.standard_normal((3 * C, C), dtype=np.float32) / np.float32(np.sqrt(C)))
+        out["b_" + s] = f32_to_bf16_bits(rng.standard_normal(3 * C, dtype=np.float32) * np.float32(0.02))
+    return out
+
+
+def qkv_flops(w: Workload) -> float:
+    """FLOPs of the two streams' projections: 2 * tokens * 3C * C."""
+    C = w.H * HEAD_DIM
+    return 2.0 * w.B * w.S * 3 * C * C

@@ -266,6 +266,22 @@ def joint_attn_backward(Q, K, V, g, dO, T_txt, grid_h, grid_w, valid_len,
     return dQ, dK, dV, dgp, dg
 
 
+def qkv_projection(X, W, b):
+    """[RFC] WS1 row qkv_bias_gemm ("per-stream packed QKV + bias"; [KL]
+    3072 -> 3 x 3072 + bias, one weight set per stream) for one stream, in
+    float64: Y = X W^T + b.
+
+    X [B, T, C] with C = H * 128; W [3C, C], rows are output features in the
+    nn.Linear layout: the Q features first (feature h * 128 + d is head h,
+    dim d), then K, then V; b [3C]. Returns Q, K, V as [B, T, H, 128].
+    """
+    B, T, C = X.shape
+    H = C // D_HEAD
+    Y = X @ W.T + b
+    parts = (Y[..., :C], Y[..., C:2 * C], Y[..., 2 * C:])
+    return tuple(p.reshape(B, T, H, D_HEAD) for p in parts)
+
+
 def prologue(Q, K, g, T_txt, grid_h, grid_w, eps=EPS, theta=THETA, axes=AXES):
     """qk_rmsnorm followed by multi_axis_rope on [B, S, H, D] inputs.
 

@@ -321,3 +321,23 @@ def test_stream_pair_calls_fail_closed(L):
         # well formed (text buffers may be absent without text) up to the device check
         assert fwd(qt=None, vt=None, ot=None, shape=no_text, lens=zero) != 1
         assert fwd() == 5 and bwd() == 5
+
+
+def test_qkv_projection_and_context_forward_fail_closed(L):
+    s = pkg.Shape.make(2, 16, 8, 8, 2)
+    p = 1 << 20
+    vl = (ctypes.c_int32 * 2)(3, 5)
+
+    def qkv(ctx=None, q=(p, p), k=(p, p), x_img=p, b_txt=p, gq=p):
+        return L.rlk_qkv_bias_gemm(ctypes.byref(s), p, x_img, p, p, b_txt, p, gq, p, p, p, ctx, q[0], q[1], k[0],
+                                   k[1], p, p, None)
+    assert qkv(x_img=None) == 1                       # inputs required
+    assert qkv(b_txt=p + 2) == 3                      # misaligned bias
+    assert qkv(q=(None, None)) == 1                   # plain mode needs Q and K
+    assert qkv(q=(None, p)) == 1                      # a text buffer is needed when T_txt > 0
+    assert qkv(ctx=p, gq=None) == 1                   # the fused epilogue needs the gains
+    assert L.rlk_joint_attn_fwd_ctx(ctypes.byref(s), None, p, p, vl, p, p, p, None) == 1
+    assert L.rlk_joint_attn_fwd_ctx(ctypes.byref(s), p, p, p, vl, p, p + 8, p, None) == 3
+    import torch
+    if not torch.cuda.is_available():
+        assert qkv() == 5 and qkv(ctx=p, q=(None, None), k=(None, None)) == 5

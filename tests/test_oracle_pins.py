@@ -426,3 +426,52 @@ def test_storage_rounding_only_rounds_q_and_k():
         assert np.max(np.abs(o[0, :, h] - ro)) <= 1e-13 and np.max(np.abs(lse[0, h] - rl)) <= 1e-13
     o2, lse2 = O.joint_attn_forward(Q, K, V, g, w.T_txt, w.grid_h, w.grid_w, vl)
     assert 0 < np.max(np.abs(lse2 - lse)) < 1e-2
+
+
+# ---------------------------------------------------------------- qkv_bias_gemm
+def _brute_qkv(X, W, b):
+    """Every output feature as a plain Python sum, for tiny sizes."""
+    B, T, C = X.shape
+    out = np.zeros((B, T, 3 * C))
+    for bb in range(B):
+        for t in range(T):
+            for o in range(3 * C):
+                acc = 0.0
+                for c in range(C):
+                    acc += float(X[bb, t, c]) * float(W[o, c])
+                out[bb, t, o] = acc + float(b[o])
+    return out
+
+
+def test_qkv_projection_matches_brute_force():
+    rng = np.random.default_rng(7)
+    B, T, C = 2, 3, 128
+    X = rng.standard_normal((B, T, C))
+    W = rng.standard_normal((3 * C, C))
+    b = rng.standard_normal(3 * C)
+    Q, K, V = O.qkv_projection(X, W, b)
+    Y = _brute_qkv(X, W, b)
+    for i, part in enumerate((Q, K, V)):
+        assert part.shape == (B, T, 1, 128)
+        assert np.allclose(part.reshape(B, T, C), Y[..., i * C:(i + 1) * C], rtol=0, atol=1e-11)
+
+
+def test_qkv_projection_exact_on_integers_and_identity_blocks():
+    rng = np.random.default_rng(8)
+    B, T, H = 1, 5, 2
+    C = H * 128
+    X = rng.integers(-4, 5, (B, T, C)).astype(np.float64)
+    b = rng.integers(-3, 4, 3 * C).astype(np.float64)
+    # W = [I; 2I; -I]: Q = X + b_q, K = 2X + b_k, V = -X + b_v, head-major
+    I = np.eye(C)
+    Q, K, V = O.qkv_projection(X, np.concatenate([I, 2 * I, -I]), b)
+    assert np.array_equal(Q.reshape(B, T, C), X + b[:C])
+    assert np.array_equal(K.reshape(B, T, C), 2 * X + b[C:2 * C])
+    assert np.array_equal(V.reshape(B, T, C), -X + b[2 * C:])
+    # feature h * 128 + d is head h, dim d
+    assert np.array_equal(Q[0, :, 1, 5], X[0, :, 128 + 5] + b[128 + 5])
+    # integer operands: the general product is exact in float64
+    W = rng.integers(-3, 4, (3 * C, C)).astype(np.float64)
+    Q, K, V = O.qkv_projection(X, W, b)
+    Y = np.einsum("btc,oc->bto", X.astype(np.int64), W.astype(np.int64)) + b.astype(np.int64)
+    assert np.array_equal(V.reshape(B, T, C), Y[..., 2 * C:].astype(np.float64))
