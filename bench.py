@@ -250,9 +250,18 @@ def measure_qkv(pkg, w, peaks, n_steps):
         kc = k[1] if k[0] is None else torch.cat(k, dim=1)
         pkg.rlk_qk_norm_rope(shape, qc, kc, gains[0], gains[1], gains[2], gains[3], ja.ctx)
 
+    C = w.H * W.HEAD_DIM
+    o = tuple(None if t is None else t.view(w.B, -1, w.H, W.HEAD_DIM) for t in x)
+    wo = tuple(t[:C].contiguous() for t in wt)
+    bo = tuple(t[:C].contiguous() for t in b)
+    y = tuple(None if t is None else torch.empty_like(t) for t in x)
+
+    def out_proj():
+        pkg.rlk_attn_out_bias_gemm(shape, o, wo, bo, y)
+
     res = {}
     stream = torch.cuda.current_stream()
-    for name, fn in (("fused", fused), ("plain_then_prologue", plain_then_prologue)):
+    for name, fn in (("fused", fused), ("plain_then_prologue", plain_then_prologue), ("out_proj", out_proj)):
         for _ in range(3):
             fn()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -270,7 +279,10 @@ def measure_qkv(pkg, w, peaks, n_steps):
     return {"op": "qkv_bias_gemm + qk_rmsnorm + multi_axis_rope (both streams)", "gflop": round(flops / 1e9, 2),
             "ms_fused": round(res["fused"], 4), "ms_plain_then_prologue": round(res["plain_then_prologue"], 4),
             "achieved": round(tf, 1), "unit": "TFLOP/s", "peak": peak, "frac": round(tf / peak, 4),
-            "peak_source": "bf16_tflops (burst: the projection is timed alone)", "steps": n_steps}
+            "peak_source": "bf16_tflops (burst: the projection is timed alone)", "steps": n_steps,
+            "attn_out_bias_gemm": {"gflop": round(flops / 3e9, 2), "ms": round(res["out_proj"], 4),
+                                   "achieved": round(flops / 3 / (res["out_proj"] * 1e-3) / 1e12, 1),
+                                   "frac": round(flops / 3 / (res["out_proj"] * 1e-3) / 1e12 / peak, 4)}}
 
 
 def load_traffic(source_hash: str):

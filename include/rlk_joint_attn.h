@@ -324,6 +324,21 @@ rlk_status rlk_joint_attn_fwd_ctx(const rlk_ja_shape* shape, const void* ctx,
                                   const int32_t* txt_valid_len,
                                   void* out_txt, void* out_img, float* lse, void* stream);
 
+/* The attention's adjacent consumer: row attn_out_bias_gemm of the RFC's
+ * WS1 table (per-stream attention output projection 3072 -> 3072 + bias).
+ *   o_txt, o_img   bf16 [B, T_txt, H, 128] and [B, grid_h*grid_w, H, 128]
+ *                  (the forward's separate-stream output, read as [B, T_s, C])
+ *   w_txt, w_img   bf16 [C, C] (nn.Linear layout: output feature rows)
+ *   b_txt, b_img   bf16 [C]
+ *   y_txt, y_img   bf16 [B, T_s, C], written: bf16(o w^T + b), fp32
+ *                  accumulation over the input features in a fixed order.
+ * A *_txt pointer may be NULL only when T_txt == 0. */
+rlk_status rlk_attn_out_bias_gemm(const rlk_ja_shape* shape,
+                                  const void* o_txt, const void* o_img,
+                                  const void* w_txt, const void* w_img,
+                                  const void* b_txt, const void* b_img,
+                                  void* y_txt, void* y_img, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device-side error word
  * that bounded waits in the kernels set when they give up. Returns RLK_OK,
  * RLK_ERR_DEVICE_TIMEOUT, or RLK_ERR_CUDA if the stream reported an error. */
@@ -400,8 +415,8 @@ rlk_status rlk_joint_attn_fwd_shard(const rlk_ja_shape* shape, const void* ctx, 
  * While tracing is on, every entry point that can launch work (the fused
  * forward and backward with concatenated or separate streams, the
  * allocation-free forward, the key-shard and from-context forwards, the
- * QKV projection and the standalone operators) appends one record when it
- * returns, including calls refused
+ * QKV and output projections and the standalone operators) appends one
+ * record when it returns, including calls refused
  * during validation (status != RLK_OK, no kernel listed, actual backend
  * "none"). The kernels listed are the ones the call enqueued, in launch
  * order. Records live in a ring of RLK_OP_TRACE_CAP entries in host memory;
@@ -444,7 +459,7 @@ const char* rlk_strerror(int status);
 /* Kernel timing for benchmarks. kernel ids: 0 rope table, 1 prologue,
  * 2 attention forward, 3 backward preprocess, 4 dK/dV, 5 dQ,
  * 6 RoPE/RMSNorm backward, 7 gain-gradient fold, 8 qk_gemm, 9 softmax,
- * 10 av_gemm, 11 forward key shard, 12 qkv_bias_gemm.
+ * 10 av_gemm, 11 forward key shard, 12 qkv_bias_gemm, 13 attn_out_bias_gemm.
  * rlk_kernel_timing(1) makes later calls record a CUDA event pair around
  * every launch (up to 4096 launches per kernel id); rlk_kernel_timing(0)
  * stops and clears. rlk_kernel_timing_read() waits for the recorded events

@@ -28,6 +28,7 @@ __all__ = [
     "rlk_op_trace_enable", "rlk_op_trace_count", "rlk_op_trace_read", "op_trace", "OP_TRACE_CAP",
     "rlk_joint_attn_state_bytes", "rlk_joint_attn_fwd_shard", "rlk_joint_attn_fwd_streams",
     "rlk_joint_attn_bwd_streams", "rlk_qkv_bias_gemm", "rlk_joint_attn_fwd_ctx",
+    "rlk_attn_out_bias_gemm",
     "EXPORTED_SYMBOLS", "KERNEL_IDS",
 ]
 
@@ -45,7 +46,7 @@ STATUS_NAMES = {
 KERNEL_IDS = {
     "rope_table": 0, "prologue": 1, "attn_fwd": 2, "bwd_pre": 3,
     "bwd_dkdv": 4, "bwd_dq": 5, "norm_rope_bwd": 6, "dg_fold": 7,
-    "qk_gemm": 8, "softmax": 9, "av_gemm": 10, "attn_fwd_shard": 11, "qkv_gemm": 12,
+    "qk_gemm": 8, "softmax": 9, "av_gemm": 10, "attn_fwd_shard": 11, "qkv_gemm": 12, "out_gemm": 13,
 }
 # which intermediate rlk_joint_attn_unfused_bytes() sizes
 UNFUSED = {"scores": 0, "p": 1, "alpha": 2, "rows": 3}
@@ -60,7 +61,7 @@ EXPORTED_SYMBOLS = (
     "rlk_op_trace_enable", "rlk_op_trace_count", "rlk_op_trace_read",
     "rlk_joint_attn_state_bytes", "rlk_joint_attn_fwd_shard",
     "rlk_joint_attn_fwd_streams", "rlk_joint_attn_bwd_streams", "rlk_qkv_bias_gemm",
-    "rlk_joint_attn_fwd_ctx",
+    "rlk_joint_attn_fwd_ctx", "rlk_attn_out_bias_gemm",
 )
 OP_TRACE_CAP = 256
 OP_TRACE_MAX_KERNELS = 8
@@ -195,6 +196,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     L.rlk_qkv_bias_gemm.restype = i32
     L.rlk_joint_attn_fwd_ctx.argtypes = [shp, vp, vp, vp, i32p, vp, vp, vp, vp]
     L.rlk_joint_attn_fwd_ctx.restype = i32
+    L.rlk_attn_out_bias_gemm.argtypes = [shp] + [vp] * 9
+    L.rlk_attn_out_bias_gemm.restype = i32
     L.rlk_op_trace_enable.argtypes = [i32]
     L.rlk_op_trace_enable.restype = i32
     L.rlk_op_trace_count.argtypes = []
@@ -375,6 +378,13 @@ def rlk_joint_attn_fwd_ctx(shape, ctx, v, txt_valid_len, out, lse, stream=None) 
                                       _lengths(txt_valid_len), _ptr(out[0]), _ptr(out[1]), _ptr(lse),
                                       _stream_handle(stream))
     _check(rc, "rlk_joint_attn_fwd_ctx")
+
+
+def rlk_attn_out_bias_gemm(shape, o, w, b, y, stream=None) -> None:
+    """Per-stream output projection; o, w, b, y are (text, image) pairs."""
+    rc = lib().rlk_attn_out_bias_gemm(ctypes.byref(shape), _ptr(o[0]), _ptr(o[1]), _ptr(w[0]), _ptr(w[1]),
+                                      _ptr(b[0]), _ptr(b[1]), _ptr(y[0]), _ptr(y[1]), _stream_handle(stream))
+    _check(rc, "rlk_attn_out_bias_gemm")
 
 
 def rlk_op_trace_enable(enable: bool) -> None:

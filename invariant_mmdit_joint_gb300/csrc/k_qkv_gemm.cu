@@ -64,9 +64,11 @@ struct QkvArgs {
     const uint16_t* bias[2];
     const float* gain[2][2];  // [stream][0 q, 1 k]
     Geom g;
-    int C;                  // H * 128
+    int C;                  // H * 128 (the input features)
+    int ncols;              // output features: 3C (QKV) or C (output projection)
+    bool out_proj;          // every column is one plain output, stored to v
     int m_tiles[2];         // ceil(B * T_s / 128)
-    int n_tiles;            // ceil(3C / 256)
+    int n_tiles;            // ceil(ncols / 256)
     // fused mode (qh != null): q^, k^ [B*H*S, 128] and r [B*H*S] into the
     // context, the cos/sin table read from it; q, k optional pre-norm copies
     uint16_t* qh;
@@ -269,8 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1) qkv_gemm_kernel(const __grid_cons
 #pragma unroll 1
             for (int hl = 0; hl < 2; ++hl) {
                 const int col0 = tl.n0 + 128 * hl;
-                if (col0 >= 3 * a.C) break;             // past the last head (odd H): warp-uniform
-                const int part = col0 / a.C;            // 0 Q, 1 K, 2 V
+                if (col0 >= a.ncols) break;             // past the last head (odd H): warp-uniform
+                // 0 Q, 1 K, 2 V (the output projection stores like V)
+                const int part = a.out_proj ? 2 : col0 / a.C;
                 const int head = (col0 % a.C) / 128;
                 float x[128];
                 __syncwarp();  // the TMEM loads are warp-collective
@@ -329,19 +332,20 @@ __global__ void __launch_bounds__(kThreads, 1) qkv_gemm_kernel(const __grid_cons
 
 }  // namespace
 
-cudaError_t launch_qkv_gemm(const Geom& g, const uint16_t* const x[2], const uint16_t* const w[2],
-                            const uint16_t* const bias[2], const float* const gains[4], uint16_t* qh, uint16_t* kh,
-                            float* rq, float* rk, const float2* tab, const SegBf16& q, const SegBf16& k,
-                            const SegBf16& v, bool store_q, bool store_k, cudaStream_t s) {
+cudaError_t launch_proj_gemm(const Geom& g, bool out_proj, const uint16_t* const x[2], const uint16_t* const w[2],
+                             const uint16_t* const bias[2], const float* const gains[4], uint16_t* qh, uint16_t* kh,
+                             float* rq, float* rk, const float2* tab, const SegBf16& q, const SegBf16& k,
+                             const SegBf16& v, bool store_q, bool store_k, cudaStream_t s) {
     QkvArgs a;
     const int C = g.H * kHeadDim;
+    const int ncols = out_proj ? C : 3 * C;
     const long long rows[2] = {(long long)g.B * g.T_txt, (long long)g.B * g.T_img};
     for (int st = 0; st < 2; ++st) {
         if (rows[st] == 0) {
             memset(&a.map_x[st], 0, sizeof(a.map_x[st]));
             memset(&a.map_w[st], 0, sizeof(a.map_w[st]));
         } else if (!tmap::mat_bf16(&a.map_x[st], x[st], rows[st], C, kBM) ||
-                   !tmap::mat_bf16(&a.map_w[st], w[st], 3LL * C, C, kBN)) {
+                   !tmap::mat_bf16(&a.map_w[st], w[st], ncols, C, kBN)) {
             return cudaErrorInvalidValue;
         }
         a.bias[st] = bias[st];
@@ -353,7 +357,9 @@ cudaError_t launch_qkv_gemm(const Geom& g, const uint16_t* const x[2], const uin
     a.gain[1][1] = gains[3];  // k image
     a.g = g;
     a.C = C;
-    a.n_tiles = (3 * C + kBN - 1) / kBN;
+    a.ncols = ncols;
+    a.out_proj = out_proj;
+    a.n_tiles = (ncols + kBN - 1) / kBN;
     a.qh = qh;
     a.kh = kh;
     a.rq = rq;
@@ -372,9 +378,10 @@ cudaError_t launch_qkv_gemm(const Geom& g, const uint16_t* const x[2], const uin
     const int tiles = (a.m_tiles[0] + a.m_tiles[1]) * a.n_tiles;
     const int grid = tiles < sms ? tiles : sms;
     if (grid == 0) return cudaSuccess;
-    timing_begin(kKQkvGemm, s);
+    const int kid = out_proj ? kKOutGemm : kKQkvGemm;
+    timing_begin(kid, s);
     qkv_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
-    timing_end(kKQkvGemm, s);
+    timing_end(kid, s);
     return cudaGetLastError();
 }
 

@@ -286,11 +286,15 @@ const OpInfo kOps[] = {
      "then runs the prologue arithmetic (IEEE sqrt and division)",
      "K in ascending steps of 64 (16 per MMA); no split-K; norm: 16 partials of 8 then a fixed tree"},
     {"joint_attention_fused (from context)", "rlk_joint_attn_fwd_ctx", kFwdPolicy, kFwdOrder},
+    {"attn_out_bias_gemm", "rlk_attn_out_bias_gemm",
+     "bf16 O W operands, fp32 TMEM accumulators, + bf16 bias, one bf16 rounding of the output",
+     "K in ascending steps of 64 (16 per MMA); no split-K"},
 };
 const char* const kKernelNames[kNumKernelIds] = {
     "rope_table_kernel", "prologue_kernel", "attn_fwd_tc_kernel", "bwd_pre_kernel",
     "attn_bwd_dkdv_tc_kernel", "attn_bwd_dq_tc_kernel", "norm_rope_bwd_kernel", "dg_fold_kernels",
-    "qk_gemm_kernel", "softmax_kernel", "av_gemm_kernel", "attn_fwd_tc_kernel<shard>", "qkv_gemm_kernel"};
+    "qk_gemm_kernel", "softmax_kernel", "av_gemm_kernel", "attn_fwd_tc_kernel<shard>", "qkv_gemm_kernel",
+    "qkv_gemm_kernel<out_proj>"};
 
 struct OpLog {
     std::mutex mu;
@@ -635,7 +639,7 @@ static rlk_status rlk_qkv_bias_gemm_impl(const rlk_ja_shape* shape, const void* 
         tab = t;
     }
     const SegBf16 none = seg_split(nullptr, nullptr, g);
-    if (launch_qkv_gemm(g, x, w, bias, gains, qh, kh, rq, rk, tab, store_q ? seg_split(q_txt, q_img, g) : none,
+    if (launch_proj_gemm(g, false, x, w, bias, gains, qh, kh, rq, rk, tab, store_q ? seg_split(q_txt, q_img, g) : none,
                         store_k ? seg_split(k_txt, k_img, g) : none, seg_split(v_txt, v_img, g), store_q, store_k,
                         s) != cudaSuccess)
         return RLK_ERR_CUDA;
@@ -680,6 +684,35 @@ rlk_status rlk_joint_attn_fwd_ctx(const rlk_ja_shape* shape, const void* ctx, co
     OpScope sc(kOpFwdCtx, shape);
     return sc.finish(rlk_joint_attn_fwd_ctx_impl(shape, ctx, v_txt, v_img, txt_valid_len, out_txt, out_img, lse,
                                                  stream));
+}
+
+static rlk_status rlk_attn_out_bias_gemm_impl(const rlk_ja_shape* shape, const void* o_txt, const void* o_img,
+                                              const void* w_txt, const void* w_img, const void* b_txt,
+                                              const void* b_img, void* y_txt, void* y_img, void* stream) {
+    rlk_status why = RLK_OK;
+    if (!shape_ok(shape, &why)) return why;
+    const Geom g = make_geom(shape);
+    rlk_status st = check_pairs(g, {{o_txt, o_img}, {w_txt, w_img}, {b_txt, b_img}, {y_txt, y_img}});
+    if (st != RLK_OK) return st;
+    st = device_ok();
+    if (st != RLK_OK) return st;
+    const uint16_t* x[2] = {static_cast<const uint16_t*>(o_txt), static_cast<const uint16_t*>(o_img)};
+    const uint16_t* w[2] = {static_cast<const uint16_t*>(w_txt), static_cast<const uint16_t*>(w_img)};
+    const uint16_t* bias[2] = {static_cast<const uint16_t*>(b_txt), static_cast<const uint16_t*>(b_img)};
+    const float* gains[4] = {nullptr, nullptr, nullptr, nullptr};
+    const SegBf16 none = seg_split(nullptr, nullptr, g);
+    if (launch_proj_gemm(g, true, x, w, bias, gains, nullptr, nullptr, nullptr, nullptr, nullptr, none, none,
+                         seg_split(y_txt, y_img, g), false, false, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status rlk_attn_out_bias_gemm(const rlk_ja_shape* shape, const void* o_txt, const void* o_img, const void* w_txt,
+                                  const void* w_img, const void* b_txt, const void* b_img, void* y_txt, void* y_img,
+                                  void* stream) {
+    OpScope sc(kOpOutGemm, shape);
+    return sc.finish(
+        rlk_attn_out_bias_gemm_impl(shape, o_txt, o_img, w_txt, w_img, b_txt, b_img, y_txt, y_img, stream));
 }
 
 size_t rlk_joint_attn_unfused_bytes(const rlk_ja_shape* shape, int which) {

@@ -93,7 +93,7 @@ __host__ __device__ inline int pair_axis(int k) {
 enum KernelId {
     kKRopeTable = 0, kKPrologue = 1, kKAttnFwd = 2, kKBwdPre = 3,
     kKBwdDkDv = 4, kKBwdDq = 5, kKNormRopeBwd = 6, kKDgFold = 7,
-    kKQkGemm = 8, kKSoftmax = 9, kKAvGemm = 10, kKAttnFwdShard = 11, kKQkvGemm = 12, kNumKernelIds = 13
+    kKQkGemm = 8, kKSoftmax = 9, kKAvGemm = 10, kKAttnFwdShard = 11, kKQkvGemm = 12, kKOutGemm = 13, kNumKernelIds = 14
 };
 
 // Launch timing hooks (rlk_host.cu): bracket one launch with events.
@@ -106,7 +106,7 @@ void timing_end(int kernel_id, cudaStream_t s);
 // launches inside it fill and finish() appends to the log.
 enum OpKind {
     kOpFwd = 0, kOpBwd, kOpFwdNoalloc, kOpNormRope, kOpQkGemm, kOpSoftmax, kOpAvGemm, kOpFwdShard,
-    kOpFwdStreams, kOpBwdStreams, kOpQkvGemm, kOpFwdCtx
+    kOpFwdStreams, kOpBwdStreams, kOpQkvGemm, kOpFwdCtx, kOpOutGemm
 };
 class OpScope {
    public:
@@ -175,14 +175,16 @@ cudaError_t launch_av_gemm(const Geom& g, const ValidLen& vl, const uint16_t* p,
 int probe_unfused_tu(void);
 int read_and_clear_status_unfused(cudaStream_t s);
 
-// k_qkv_gemm.cu: per-stream QKV projection Y = X W^T + b (both streams in
-// one launch), stored as bf16; with qh != null the epilogue also runs
-// qk_rmsnorm + multi_axis_rope into the context (q^, k^, r) from the table
-// tab, and writes the pre-norm Q / K only if store_q / store_k.
-cudaError_t launch_qkv_gemm(const Geom& g, const uint16_t* const x[2], const uint16_t* const w[2],
-                            const uint16_t* const bias[2], const float* const gains[4], uint16_t* qh,
-                            uint16_t* kh, float* rq, float* rk, const float2* tab, const SegBf16& q,
-                            const SegBf16& k, const SegBf16& v, bool store_q, bool store_k, cudaStream_t s);
+// k_qkv_gemm.cu: per-stream projection Y = X W^T + b (both streams in one
+// launch), stored as bf16. QKV (out_proj false): W is [3C, C]; with
+// qh != null the epilogue also runs qk_rmsnorm + multi_axis_rope into the
+// context (q^, k^, r) from the table tab, and writes the pre-norm Q / K only
+// if store_q / store_k. Output projection (out_proj true): W is [C, C] and
+// every column goes to v.
+cudaError_t launch_proj_gemm(const Geom& g, bool out_proj, const uint16_t* const x[2], const uint16_t* const w[2],
+                             const uint16_t* const bias[2], const float* const gains[4], uint16_t* qh,
+                             uint16_t* kh, float* rq, float* rk, const float2* tab, const SegBf16& q,
+                             const SegBf16& k, const SegBf16& v, bool store_q, bool store_k, cudaStream_t s);
 int probe_qkv_tu(void);
 int read_and_clear_status_qkv(cudaStream_t s);
 

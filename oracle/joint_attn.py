@@ -282,6 +282,15 @@ def qkv_projection(X, W, b):
     return tuple(p.reshape(B, T, H, D_HEAD) for p in parts)
 
 
+def attn_out_projection(O_s, W, b):
+    """[RFC] WS1 row attn_out_bias_gemm ("per-stream attention output
+    projection"; [KL] 3072 -> 3072 + bias) for one stream, in float64:
+    Y = O W^T + b with O [B, T, H, 128] read as [B, T, C], W [C, C] (output
+    feature rows), b [C]. Returns Y [B, T, C]."""
+    B, T, H, D = O_s.shape
+    return O_s.reshape(B, T, H * D) @ W.T + b
+
+
 def prologue(Q, K, g, T_txt, grid_h, grid_w, eps=EPS, theta=THETA, axes=AXES):
     """qk_rmsnorm followed by multi_axis_rope on [B, S, H, D] inputs.
 

@@ -341,3 +341,15 @@ def test_qkv_projection_and_context_forward_fail_closed(L):
     import torch
     if not torch.cuda.is_available():
         assert qkv() == 5 and qkv(ctx=p, q=(None, None), k=(None, None)) == 5
+
+
+def test_output_projection_fails_closed(L):
+    s = pkg.Shape.make(2, 16, 8, 8, 2)
+    p = 1 << 20
+    assert L.rlk_attn_out_bias_gemm(ctypes.byref(s), p, None, p, p, p, p, p, p, None) == 1
+    assert L.rlk_attn_out_bias_gemm(ctypes.byref(s), None, p, p, p, p, p, p, p, None) == 1
+    assert L.rlk_attn_out_bias_gemm(ctypes.byref(s), p, p, p, p, p, p, p + 2, p, None) == 3
+    no_text = pkg.Shape.make(2, 0, 8, 8, 2)
+    import torch
+    if not torch.cuda.is_available():
+        assert L.rlk_attn_out_bias_gemm(ctypes.byref(no_text), None, p, None, p, None, p, None, p, None) == 5

@@ -162,3 +162,38 @@ def test_full_size_projection_on_sampled_rows(dev):
         for got_pair, ref, sa in zip((q, k, v), exact, sum_abs):
             g = Hh.f64(got_pair[si].reshape(w.B * T, w.H, 128)[rows])
             assert np.all(np.abs(g - ref[0]) <= 2.0 ** -8 * np.abs(ref[0]) + 2.0 ** -16 * sa[0]), s
+
+
+@pytest.mark.parametrize("w", CASES + [W.CFG1024], ids=lambda w: w.name)
+def test_output_projection_matches_oracle(w, dev):
+    """attn_out_bias_gemm on separate stream buffers (seeded inputs: the
+    activations x stand in for the attention output, the first C rows of the
+    QKV weights and biases for the projection's)."""
+    import torch
+    from oracle import joint_attn as O
+    d, x, wt, b, _ = _inputs(w, 55, dev)
+    C = w.H * 128
+    shape = pkg.Shape.make(w.B, w.T_txt, w.grid_h, w.grid_w, w.H)
+    o = tuple(None if t is None else t.view(w.B, -1, w.H, 128) for t in x)
+    wo = tuple(t[:C].contiguous() for t in wt)
+    bo = tuple(t[:C].contiguous() for t in b)
+    y = tuple(None if t is None else torch.empty_like(t) for t in x)
+    pkg.rlk_attn_out_bias_gemm(shape, o, wo, bo, y)
+    torch.cuda.synchronize()
+    pkg.rlk_joint_attn_check_status()
+    rng = np.random.default_rng(6)
+    for si, s in enumerate(("txt", "img")):
+        if y[si] is None:
+            continue
+        T = w.T_txt if si == 0 else w.T_img
+        rows = np.arange(w.B * T)
+        if rows.size > 64:  # full size: sampled rows
+            rows = np.array(sorted(set(rng.integers(0, rows.size, 24).tolist()) | {0, rows.size - 1}))
+        X = O.widen_bf16(d["x_" + s]).reshape(w.B * T, w.H, 128)[rows][None]
+        Wm = O.widen_bf16(d["w_" + s])[:C]
+        bias = O.widen_bf16(d["b_" + s])[:C]
+        ref = O.attn_out_projection(X, Wm, bias)[0]
+        sa = O.attn_out_projection(np.abs(X), np.abs(Wm), np.abs(bias))[0]
+        g = Hh.f64(y[si].reshape(w.B * T, C)[torch.from_numpy(rows).to(dev)])
+        assert np.all(np.abs(g - ref) <= 2.0 ** -8 * np.abs(ref) + 2.0 ** -16 * sa), (w.name, s)
+        assert np.mean(g == O.round_bf16(ref)) > 0.99, (w.name, s)

@@ -475,3 +475,23 @@ def test_qkv_projection_exact_on_integers_and_identity_blocks():
     Q, K, V = O.qkv_projection(X, W, b)
     Y = np.einsum("btc,oc->bto", X.astype(np.int64), W.astype(np.int64)) + b.astype(np.int64)
     assert np.array_equal(V.reshape(B, T, C), Y[..., 2 * C:].astype(np.float64))
+
+
+def test_attn_out_projection_matches_brute_force_and_identity():
+    rng = np.random.default_rng(9)
+    B, T, H = 2, 3, 1
+    C = H * 128
+    O_s = rng.standard_normal((B, T, H, 128))
+    W = rng.standard_normal((C, C))
+    b = rng.standard_normal(C)
+    Y = O.attn_out_projection(O_s, W, b)
+    for bb in range(B):
+        for t in range(T):
+            for o in (0, 17, C - 1):
+                ref = sum(float(O_s[bb, t, 0, c]) * float(W[o, c]) for c in range(C)) + float(b[o])
+                assert abs(Y[bb, t, o] - ref) <= 1e-11
+    # W = permutation: output feature o reads input feature perm[o]
+    perm = rng.permutation(C)
+    P = np.eye(C)[perm]
+    Y = O.attn_out_projection(O_s, P, np.zeros(C))
+    assert np.array_equal(Y, O_s.reshape(B, T, C)[..., perm])
