@@ -36,11 +36,13 @@ namespace {
 using namespace sm100;
 
 // warps 0-7: elementwise (warp w owns TMEM lane quarter w % 4 and the
-// column half w / 4 of each row); warp 8: TMA producer; warps 9 and 10: MMA
-// issuers of two independent chains (warp 9 owns TMEM).
-constexpr int kThreads = 352;
-constexpr int kEwThreads = 256;
-constexpr int kWarpTma = 8, kWarpMma = 9;
+// column half w / 4 of each row; kEwWarps below); warp 8: TMA producer;
+// warps 9 and 10: MMA issuers of two independent chains (warp 9 owns TMEM).
+constexpr int kEwWarps = 8;                       // elementwise warps (16 measured 3% slower)
+constexpr int kEwThreads = 32 * kEwWarps;
+constexpr int kThreads = kEwThreads + 96;         // + TMA producer + two MMA issuers
+constexpr int kWarpTma = kEwWarps, kWarpMma = kEwWarps + 1;
+constexpr int kGroupCols = 128 / (kEwWarps / 4);  // query columns per elementwise warp
 constexpr int kBoxBytes = 128 * 128;       // 128 rows x 64 bf16
 constexpr int kTileBytes = 2 * kBoxBytes;  // 128 rows x 128 bf16
 constexpr uint32_t kTmemCols = 512;
@@ -89,7 +91,16 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
 // half h = kk / 4 of the 128 fp32 columns is rewritten in place as 32 packed
 // columns at the start of that half, so the two warps sharing a lane
 // quarter never overwrite each other's unread scores.
-__device__ __forceinline__ uint32_t a_col(int kk) { return (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8; }
+__device__ __forceinline__ uint32_t a_col(int kk) {
+    return (16 * kk / kGroupCols) * kGroupCols + (16 * kk % kGroupCols) / 2;
+}
+// A warp's packed bf16 pairs of its columns, kGroupCols / 2 TMEM columns.
+__device__ __forceinline__ void tmem_st_packed(uint32_t taddr, const uint32_t (&r)[kGroupCols / 2]) {
+    if constexpr (kGroupCols == 64)
+        tmem_st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(&r[0]));
+    else
+        tmem_st16(taddr, *reinterpret_cast<const uint32_t(*)[16]>(&r[0]));
+}
 
 // dS^T tile image (128 keys x 128 queries, bf16, 32 KB): the non-swizzled
 // MN-major operand layout of the tensor cores. Query chunk C (8 queries) is
@@ -321,12 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
             mbar_wait(bar_my_drain, 0, &no_abort, kWaitLimitNs);
         }
     } else {
-        // ------------------------------------------------ elementwise warps 0-7
-        // warp w: key rows 32 * (w % 4) + lane, query columns [64 h, 64 h + 64), h = w / 4
-        const int lq = warp & 3, half = warp >> 2;
+        // ------------------------------------------------ elementwise warps
+        // warp w: key rows 32 * (w % 4) + lane, query columns
+        // [kGroupCols * grp, kGroupCols * (grp + 1)), grp = w / 4. No row
+        // reduction: every element of P^T and dS^T is the thread's own.
+        const int lq = warp & 3, grp = warp >> 2;
         const uint32_t lane_addr = (uint32_t)(lq * 32) << 16;
         const int kr = lq * 32 + lane;
-        const int c0 = 64 * half;
+        const int c0 = kGroupCols * grp;
         const bool kvalid = k0 + kr < kvalid_end;
         bool ok = true;
         for (int i = 0; i < nq; ++i) {
@@ -340,14 +353,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
                 reinterpret_cast<const float4*>(smem_raw + (stage_l(s) - smem_u32(smem_raw))) + c0 / 4;
             const float4* dlv = l2v + 32;
             // P^T = exp2(S^T * c - lse2[query]) (masked keys: 0), kept in fp32 for dS
-            uint32_t rs[64];
-            tmem_ld32(tmem + lane_addr + kColST + c0, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
-            tmem_ld32(tmem + lane_addr + kColST + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
-            tmem_ld_wait();
-            float pf[64];
-            uint32_t pk[32];
+            uint32_t rs[kGroupCols];
 #pragma unroll
-            for (int e4 = 0; e4 < 16; ++e4) {
+            for (int c = 0; c < kGroupCols; c += 32)
+                tmem_ld32(tmem + lane_addr + kColST + c0 + c, *reinterpret_cast<uint32_t(*)[32]>(&rs[c]));
+            tmem_ld_wait();
+            float pf[kGroupCols];
+            uint32_t pk[kGroupCols / 2];
+#pragma unroll
+            for (int e4 = 0; e4 < kGroupCols / 4; ++e4) {
                 const float4 l4 = l2v[e4];
                 const float lq4[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
@@ -358,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
                 pk[2 * e4] = pack_bf16(pf[4 * e4], pf[4 * e4 + 1]);
                 pk[2 * e4 + 1] = pack_bf16(pf[4 * e4 + 2], pf[4 * e4 + 3]);
             }
-            tmem_st32(tmem + lane_addr + kColST + c0, pk);
+            tmem_st_packed(tmem + lane_addr + kColST + c0, pk);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_p);
@@ -368,12 +382,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
                 break;
             }
             tc_fence_after();
-            uint32_t rd[64];
-            tmem_ld32(tmem + lane_addr + kColDPT + c0, *reinterpret_cast<uint32_t(*)[32]>(&rd[0]));
-            tmem_ld32(tmem + lane_addr + kColDPT + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rd[32]));
+            uint32_t rd[kGroupCols];
+#pragma unroll
+            for (int c = 0; c < kGroupCols; c += 32)
+                tmem_ld32(tmem + lane_addr + kColDPT + c0 + c, *reinterpret_cast<uint32_t(*)[32]>(&rd[c]));
             tmem_ld_wait();
 #pragma unroll
-            for (int e4 = 0; e4 < 16; ++e4) {
+            for (int e4 = 0; e4 < kGroupCols / 4; ++e4) {
                 const float4 d4 = dlv[e4];
                 const float dq4[4] = {d4.x, d4.y, d4.z, d4.w};
                 float ds[4];
@@ -382,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
                 pk[2 * e4] = pack_bf16(ds[0], ds[1]);
                 pk[2 * e4 + 1] = pack_bf16(ds[2], ds[3]);
             }
-            tmem_st32(tmem + lane_addr + kColDPT + c0, pk);
+            tmem_st_packed(tmem + lane_addr + kColDPT + c0, pk);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_ds);
@@ -391,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
             // store of one query chunk covers 512 contiguous bytes
             uint8_t* ds_img = a.ds_tiles + ((bh * nq + i) * nq + kt) * (size_t)kTileBytes + ds_image_offset(c0, kr);
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
+            for (int c = 0; c < kGroupCols / 8; ++c)
                 *reinterpret_cast<uint4*>(ds_img + c * kDsChunkBytes) =
                     make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         }
@@ -406,11 +421,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
             uint8_t* stg = smem_raw + (sbase - smem_u32(smem_raw));
             const int sw = kr & 7;
 #pragma unroll 1
-            for (int c = 0; c < 64; c += 32) {
+            for (int c = 0; c < kGroupCols; c += 32) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_addr + kColDV + c0 + c, r);
                 tmem_ld_wait();
-                uint8_t* dvrow = stg + half * kBoxBytes + kr * 128;
+                // dV box (c0 + c) / 64, 16-byte chunks from ((c0 + c) % 64) / 8
+                uint8_t* dvrow = stg + ((c0 + c) >> 6) * kBoxBytes + kr * 128;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint32_t w[4];
@@ -418,7 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
                     for (int e = 0; e < 4; ++e)
                         w[e] = kvalid ? pack_bf16(__uint_as_float(r[8 * q + 2 * e]), __uint_as_float(r[8 * q + 2 * e + 1]))
                                       : 0u;
-                    *reinterpret_cast<uint4*>(dvrow + ((((c >> 3) + q) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(dvrow + (((((c0 + c) & 63) >> 3) + q) ^ sw) * 16) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
                 }
                 tmem_ld32(tmem + lane_addr + kColDK + c0 + c, r);
                 tmem_ld_wait();
