@@ -9,6 +9,8 @@
 // preprocessing and RoPE rows) and WS1 table (qk_rmsnorm, multi_axis_rope);
 // "WS1 Single-GPU Kernel List", Kernel table (fwd + bwd for both rows) and
 // Acceptance ("multi-path gradient sums use a fixed order").
+#include <cmath>
+
 #include "rlk_device.cuh"
 #include "rlk_internal.h"
 
@@ -20,18 +22,19 @@ namespace {
 constexpr int kRowThreads = 16;  // a half warp covers one 128-wide row, 8 dims per lane
 
 // ---------------------------------------------------------------- rope table
-// tab[(p - p_lo) * 64 + k] = (cos, sin) of p * theta^(-2j/d_a), where pair k
-// is pair j of axis a. Angles and cos/sin in FP64, rounded once to FP32.
-__global__ void rope_table_kernel(Geom g, float2* __restrict__ tab) {
+// tab[(p - p_lo) * 64 + k] = (cos, sin) of p * freq[k], freq[k] =
+// theta^(-2j/d_a) for pair k = pair j of axis a (computed once on the host in
+// FP64). Angles and cos/sin in FP64, rounded once to FP32.
+struct PairFreqs {
+    double f[kPairs];
+};
+
+__global__ void rope_table_kernel(Geom g, const PairFreqs fr, float2* __restrict__ tab) {
     int idx = blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= g.n_pos * kPairs) return;
     int k = idx % kPairs;
     int p = g.p_lo + idx / kPairs;
-    int a = pair_axis(k);
-    int j = a == 0 ? k : (a == 1 ? k - kAxis0Pairs : k - kAxis0Pairs - kAxis1Pairs);
-    double d_a = a == 0 ? 16.0 : 56.0;
-    double freq = pow((double)g.theta, -2.0 * (double)j / d_a);
-    double ang = (double)p * freq;
+    double ang = (double)p * fr.f[k];
     double s, c;
     sincos(ang, &s, &c);
     tab[idx] = make_float2((float)c, (float)s);
@@ -317,8 +320,15 @@ unsigned row_blocks(const Geom& g) {
 
 cudaError_t launch_rope_table(const Geom& g, float2* tab, cudaStream_t s) {
     const int n = g.n_pos * kPairs;
+    PairFreqs fr;
+    for (int k = 0; k < kPairs; ++k) {
+        const int a = pair_axis(k);
+        const int j = a == 0 ? k : (a == 1 ? k - kAxis0Pairs : k - kAxis0Pairs - kAxis1Pairs);
+        const double d_a = a == 0 ? 16.0 : 56.0;
+        fr.f[k] = std::pow((double)g.theta, -2.0 * (double)j / d_a);
+    }
     timing_begin(kKRopeTable, s);
-    rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(g, tab);
+    rope_table_kernel<<<(n + 127) / 128, 128, 0, s>>>(g, fr, tab);
     timing_end(kKRopeTable, s);
     return cudaGetLastError();
 }
