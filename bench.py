@@ -34,7 +34,7 @@ from invariant_mmdit_joint_gb300 import workloads as W  # noqa: E402
 
 METRIC = "joint-attn fwd+bwd TFLOP/s and % of BF16 tensor peak at 1024² (4096 img+256 txt)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-LAUNCHES_PER_STEP = 9  # fwd: table, prologue, attention; bwd: pre, dkdv, dq, norm/rope, 2 folds
+LAUNCHES_PER_STEP = 9  # fwd: table, prologue, attention; bwd: pre, dkdv, dq, key norm/rope, 2 folds
 THROTTLE_BITS = {
     0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
     0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
@@ -161,11 +161,14 @@ def kernel_work(w: W.Workload):
         # (it also writes the dS^T tiles, ds_bytes)
         "bwd_dkdv": ("tensor", 4 * G),
         # dQ = dS K, the fifth GEMM, streams the dS^T tiles: read them and K
-        # once, write dqh (fp32)
-        "bwd_dq": ("hbm", ds_bytes + rows * D * 2 + rows * D * 4),
-        # read dqh, dkh (fp32), Q, K (bf16), r; write dQ, dK (bf16)
-        "norm_rope_bwd": ("hbm", 2 * rows * D * 4 + 2 * rows * D * 2 + 2 * rows * 4 + 2 * rows * D * 2),
-        "dg_fold": ("hbm", 2 * rows // 64 * D * 4 + w.B * w.H * 4 * D * 4),
+        # once; its epilogue runs the RoPE / RMSNorm backward of the query
+        # rows from TMEM: read q (bf16) and rq, write dQ (bf16) and the q
+        # gain-gradient partials (one per 32-row quarter of a tile)
+        "bwd_dq": ("hbm", ds_bytes + rows * D * 2 + rows * D * 2 + rows * 4 + rows * D * 2 + rows // 32 * D * 4),
+        # read dk^ (fp32), k (bf16), rk; write dK (bf16) and the k partials
+        "norm_rope_bwd_k": ("hbm", rows * D * 4 + rows * D * 2 + rows * 4 + rows * D * 2 + rows // 32 * D * 4),
+        # read both operands' tile partials, write the (b, h) folds
+        "dg_fold": ("hbm", 2 * rows // 32 * D * 4 + w.B * w.H * 4 * D * 4),
     }
 
 

@@ -104,8 +104,9 @@ size_t rlk_joint_attn_ctx_bytes(const rlk_ja_shape* shape);
 
 /* Bytes of the backward scratch `workspace`: lse * log2(e) and
  * rowsum(dO * O) (fp32, one 128-slot block per query tile of each (sample,
- * head)), the fp32 gradients of the rotated q and k ([B, H, S, D] each), the
- * per-chunk gain-gradient partials and the bf16 score gradients dS as 128 x
+ * head)), the fp32 gradient of the rotated k ([B, H, S, D]), the
+ * gain-gradient partials (fp32 [B, H, 2, n_tiles, 4, D]: q and k, per
+ * 128-token tile and 32-row quarter) and the bf16 score gradients dS as 128 x
  * 128 tiles (B * H * n_tiles^2 * 32 KiB, n_tiles = ceil(T_txt / 128) +
  * ceil(grid_h * grid_w / 128); 1.8 GB for B = 2, H = 24 at 1024 x 1024).
  * Returns 0 for an invalid shape. */
@@ -458,7 +459,8 @@ const char* rlk_strerror(int status);
 
 /* Kernel timing for benchmarks. kernel ids: 0 rope table, 1 prologue,
  * 2 attention forward, 3 backward preprocess, 4 dK/dV, 5 dQ,
- * 6 RoPE/RMSNorm backward, 7 gain-gradient fold, 8 qk_gemm, 9 softmax,
+ * 6 RoPE/RMSNorm backward of the keys (the queries' runs inside dQ),
+ * 7 gain-gradient fold, 8 qk_gemm, 9 softmax,
  * 10 av_gemm, 11 forward key shard, 12 qkv_bias_gemm, 13 attn_out_bias_gemm.
  * rlk_kernel_timing(1) makes later calls record a CUDA event pair around
  * every launch (up to 4096 launches per kernel id); rlk_kernel_timing(0)

@@ -45,7 +45,7 @@ STATUS_NAMES = {
 }
 KERNEL_IDS = {
     "rope_table": 0, "prologue": 1, "attn_fwd": 2, "bwd_pre": 3,
-    "bwd_dkdv": 4, "bwd_dq": 5, "norm_rope_bwd": 6, "dg_fold": 7,
+    "bwd_dkdv": 4, "bwd_dq": 5, "norm_rope_bwd_k": 6, "dg_fold": 7,
     "qk_gemm": 8, "softmax": 9, "av_gemm": 10, "attn_fwd_shard": 11, "qkv_gemm": 12, "out_gemm": 13,
 }
 # which intermediate rlk_joint_attn_unfused_bytes() sizes

@@ -24,6 +24,7 @@
 // exactly 0). Every wait is bounded (RLK_ERR_DEVICE_TIMEOUT on give-up).
 #include "rlk_device.cuh"
 #include "rlk_internal.h"
+#include "rlk_normrope_bwd.cuh"
 #include "rlk_sm100.cuh"
 #include "rlk_tmap.h"
 
@@ -64,13 +65,22 @@ struct BwdArgs {
     const float* lse2_p;  // [B, H, nq_pad]
     const float* delta_p; // [B, H, nq_pad]
     SegBf16 dv;           // [B, S, H, 128] (text rows, image rows)
-    float* dkh;           // [B, H, S, 128]
-    float* dqh;           // [B, H, S, 128]
     uint8_t* ds_tiles;    // [B, H, nq, nq] images of 32 KB (query tile major)
     // output maps per segment (0 text, 1 image) so a tile's rows past its
-    // segment are clipped: dV [B, S, H, 128] bf16, dkh [B*H, S, 128] fp32
+    // segment are clipped: dV [B, S, H, 128] bf16, dk^ [B*H, S, 128] fp32
     CUtensorMap map_dv[2];
     CUtensorMap map_dk[2];
+    float* dkh;  // dk^ = dK of the rotated, normalised keys / sqrt(128), fp32 [B, H, S, 128]
+    // the RoPE / RMSNorm backward of the query rows in the dQ epilogue:
+    // input q (bf16 [B, S, H, 128]), its RMSNorm factors rq [B, H, S], the
+    // gains (q_txt, k_txt, q_img, k_img), the cos/sin table; outputs dQ and
+    // the q gain-gradient partials of every (b, h, 128-token tile, 32-row
+    // quarter) in dgt [B, H, 2 (q, k), n_tiles, 4, 128]
+    SegBf16 q_in, dq_out;
+    const float* rq;
+    const float* gains[4];
+    const float2* tab;
+    float* dgt;
 };
 
 __device__ __forceinline__ void fail(volatile int* abort_flag) {
@@ -152,21 +162,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
     const int kvalid_end = k_txt ? L : g.S;
     const size_t bh = (size_t)b * g.H + h;
     const int row_base = (int)(bh * g.S);
+    const int nq = g.ntq_txt + g.ntq_img;
+
     float* dkh = a.dkh + bh * g.S * kHeadDim;
 
     if (k0 >= kvalid_end) {  // every key of the tile is masked: exact zeros
         const int rows = min(128, seg_end - k0);
         for (int i = tid; i < rows * 16; i += kThreads) {
             const int r = i >> 4, c = i & 15;
-            *reinterpret_cast<uint4*>(seg_row(a.dv, g, b, k0 + r, h) + c * 8) =
-                make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(seg_row(a.dv, g, b, k0 + r, h) + c * 8) = make_uint4(0, 0, 0, 0);
             float4* dst = reinterpret_cast<float4*>(dkh + (size_t)(k0 + r) * kHeadDim + c * 8);
             dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
             dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         return;
     }
-    const int nq = g.ntq_txt + g.ntq_img;
 
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sK = sbase + kKvSmemK, sV = sbase + kKvSmemV;
@@ -613,6 +623,10 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc_kernel(const __g
         }
     } else {
         // ------------------------------------------------ epilogue warps 0-3: query row 32 w + lane
+        // Per unit: the RoPE / RMSNorm backward of the tile's query rows
+        // from dq^ = acc / sqrt(128) (TMEM): bf16 dQ rows and this warp's
+        // partial of the tile's q gain gradient (its 32 rows summed by a
+        // transposing butterfly), stored for the fold.
         const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
         const int r = warp * 32 + lane;
         int n = 0;
@@ -628,22 +642,20 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc_kernel(const __g
             int q0, q_end;
             q_tile(g, w.qt, q0, q_end);
             const bool row_ok = q0 + r < q_end;
+            const int tok = row_ok ? q0 + r : q0;  // rows past the segment read a valid row, store nothing
             const size_t bh = (size_t)w.b * g.H + w.h;
-            float* dqrow = a.dqh + (bh * g.S + q0 + r) * kHeadDim;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t rr[32];
-                tmem_ld32(tmem + lane_addr + 128 * buf + 32 * c, rr);
+            const uint32_t acc_addr = tmem + lane_addr + 128 * buf;
+            auto dq_chunk = [&](int c, float (&dy)[32]) {
+                uint32_t acc[32];
+                tmem_ld32(acc_addr + 32 * c, acc);
                 tmem_ld_wait();
-                if (row_ok) {
-                    float4* dst = reinterpret_cast<float4*>(dqrow + 32 * c);
 #pragma unroll
-                    for (int v4 = 0; v4 < 8; ++v4)
-                        dst[v4] = make_float4(__uint_as_float(rr[4 * v4]) * kScale, __uint_as_float(rr[4 * v4 + 1]) * kScale,
-                                              __uint_as_float(rr[4 * v4 + 2]) * kScale,
-                                              __uint_as_float(rr[4 * v4 + 3]) * kScale);
-                }
-            }
+                for (int i = 0; i < 32; ++i) dy[i] = row_ok ? __uint_as_float(acc[i]) * kScale : 0.0f;
+            };
+            nrb_row(dq_chunk, row_ok, reinterpret_cast<const uint4*>(seg_row(a.q_in, g, w.b, tok, w.h)),
+                    a.rq[bh * g.S + tok], w.qt < g.ntq_txt ? a.gains[0] : a.gains[2], tab_rows(a.tab, g, tok),
+                    reinterpret_cast<uint4*>(seg_row(a.dq_out, g, w.b, tok, w.h)),
+                    a.dgt + ((bh * 2 * nq + w.qt) * 4 + warp) * kHeadDim, lane);
             tc_fence_before();
             mbar_arrive(bar_free + 8 * buf);
         }
@@ -673,9 +685,17 @@ bool make_args(BwdArgs* a, const Geom& g, const ValidLen& vl, const uint16_t* qh
     a->delta_p = delta_p;
     a->dv = SegBf16{{nullptr, nullptr}, {0, 0}};
     a->dkh = nullptr;
-    a->dqh = nullptr;
     a->ds_tiles = nullptr;
     return true;
+}
+
+void set_norm_rope_io(BwdArgs* a, const NormRopeBwdIo& nr) {
+    a->q_in = nr.q;
+    a->dq_out = nr.dq;
+    a->rq = nr.rq;
+    for (int i = 0; i < 4; ++i) a->gains[i] = nr.gains[i];
+    a->tab = nr.tab;
+    a->dgt = nr.dgt;
 }
 
 }  // namespace
@@ -702,13 +722,13 @@ cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16
 }
 
 cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t* kh, const uint8_t* ds_tiles,
-                               float* dqh, cudaStream_t s) {
+                               const NormRopeBwdIo& nr, cudaStream_t s) {
     BwdArgs args;
     if (!tmap::rows_bf16(&args.map_k, kh, (uint64_t)g.B * g.H * g.S)) return cudaErrorInvalidValue;
     args.g = g;
     args.vl = vl;
-    args.dqh = dqh;
     args.ds_tiles = const_cast<uint8_t*>(ds_tiles);
+    set_norm_rope_io(&args, nr);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -2,8 +2,9 @@
 //   rope_table      cos/sin of every (position, RoPE pair) the call needs
 //   prologue        qk_rmsnorm + multi_axis_rope of Q and K, one bf16 cast
 //   bwd_pre         Delta = rowsum(dO * O) and lse2 = lse * log2(e), tile padded
-//   norm_rope_bwd   inverse RoPE rotation + RMSNorm backward + per-chunk
-//                   gain-gradient partials
+//   norm_rope_bwd_k inverse RoPE rotation + RMSNorm backward of the keys and
+//                   their gain-gradient partials (the queries' runs in the
+//                   dQ kernel's epilogue)
 //   dg_fold         fixed-order folds of the gain-gradient partials
 // Sources: RFC #386 "WS1/WS2 kernel roadmap", Model contract table (Q/K
 // preprocessing and RoPE rows) and WS1 table (qk_rmsnorm, multi_axis_rope);
@@ -180,108 +181,120 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(Geom g, const SegBf16 o, c
     }
 }
 
-// ---------------------------------------------------------------- norm/rope backward
-// CTA = (chunk of 64 tokens of one stream segment, h, b); warps 0-3 take Q
-// rows, warps 4-7 K rows, 16 consecutive rows each, in ascending order. Lane
-// l owns dims [4l, 4l+4) = pairs 2l, 2l+1. Per row:
-//   u  = R(-angle) * dyh          (inverse rotation)
-//   xh = x * r,  w = u * g,  c = (sum_d w_d xh_d) / 128   (lane order, then xor 16..1)
-//   dx = r * (w - xh * c)  -> bf16
+// ---------------------------------------------------------------- key-side norm/rope backward
+// (The query side runs in the dQ kernel's epilogue, from its accumulator.)
+// CTA = (128-token tile of one stream segment, h, b); warp w takes rows
+// 16 w .. 16 w + 15 of the tile in ascending order. Lane l owns dims
+// [4l, 4l+4) = pairs 2l, 2l+1. Per row:
+//   u  = R(-angle) * dk^          (inverse rotation)
+//   xh = k * r,  w = u * g,  c = (sum_d w_d xh_d) / 128   (lane order, then xor 16..1)
+//   dK = r * (w - xh * c)  -> bf16
 //   gain-gradient partial += u * xh (per lane, rows ascending)
-// The four warps of each operand are folded in warp order through shared
-// memory; chunk partials go to dg_chunks[b][h][q|k][chunk][128].
-constexpr int kNrbRowsPerWarp = kDgChunk / 4;
+// Warps 2j and 2j + 1 add (in that order) into the tile's quarter j,
+// dgt[b][h][1][tile][j][128]: the layout the dQ epilogue fills for q.
+constexpr int kNrbRowsPerWarp = 16;
+constexpr int kNrbGroup = 4;
 
-__global__ void __launch_bounds__(256) norm_rope_bwd_kernel(
-    Geom g, const SegBf16 q, const SegBf16 k,
-    const float* __restrict__ gq_txt, const float* __restrict__ gk_txt,
-    const float* __restrict__ gq_img, const float* __restrict__ gk_img,
-    const float2* __restrict__ tab, const float* __restrict__ rq, const float* __restrict__ rk,
-    const float* __restrict__ dqh, const float* __restrict__ dkh, const SegBf16 dq,
-    const SegBf16 dk, float* __restrict__ dg_chunks) {
+__global__ void __launch_bounds__(256) norm_rope_bwd_k_kernel(
+    Geom g, const SegBf16 k, const float* __restrict__ gk_txt, const float* __restrict__ gk_img,
+    const float2* __restrict__ tab, const float* __restrict__ rk, const float* __restrict__ dkh, const SegBf16 dk,
+    float* __restrict__ dgt) {
     __shared__ float red[8][kHeadDim];
-    const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const bool is_k = warp >= 4;
-    const bool txt_chunk = chunk < g.n_dg_chunks_txt;
-    const int seg_start = txt_chunk ? chunk * kDgChunk : g.T_txt + (chunk - g.n_dg_chunks_txt) * kDgChunk;
-    const int seg_end = txt_chunk ? g.T_txt : g.S;
-    const float* gain = is_k ? (txt_chunk ? gk_txt : gk_img) : (txt_chunk ? gq_txt : gq_img);
-    const float* r_all = is_k ? rk : rq;
-    const float* dyh = is_k ? dkh : dqh;
-
+    const bool txt = tile < g.ntq_txt;
+    const int t0 = txt ? tile * 128 : g.T_txt + (tile - g.ntq_txt) * 128;
+    const int seg_end = txt ? g.T_txt : g.S;
     const size_t bh = (size_t)b * g.H + h;
-    const float4 gv = __ldg(reinterpret_cast<const float4*>(gain) + lane);
+    const float4 gv = __ldg(reinterpret_cast<const float4*>(txt ? gk_txt : gk_img) + lane);
     const int k0 = 2 * lane, k1 = 2 * lane + 1;
     const int ax = pair_axis(k0);  // both pairs of a lane share an axis
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const int row0 = seg_start + (warp % 4) * kNrbRowsPerWarp;
-    // the chunk lies in one segment of one sample: consecutive tokens are
+    const int row0 = t0 + warp * kNrbRowsPerWarp;
+    // the tile lies in one segment of one sample: consecutive tokens are
     // H * 128 elements apart in either layout. (Pointers are selected one by
     // one: a reference to a parameter chosen at run time would put the
     // parameters in local memory.)
-    const int sg = txt_chunk ? 0 : 1;
-    const uint16_t* x_seg = is_k ? (sg ? k.p[1] : k.p[0]) : (sg ? q.p[1] : q.p[0]);
-    uint16_t* dx_seg = is_k ? (sg ? dk.p[1] : dk.p[0]) : (sg ? dq.p[1] : dq.p[0]);
-    const long long x_bs = is_k ? (sg ? k.bstride[1] : k.bstride[0]) : (sg ? q.bstride[1] : q.bstride[0]);
-    const long long dx_bs = is_k ? (sg ? dk.bstride[1] : dk.bstride[0]) : (sg ? dq.bstride[1] : dq.bstride[0]);
-    const long long n0 = min(row0, seg_end - 1) - (sg ? g.T_txt : 0);  // token of row0 inside its segment
+    const int sg = txt ? 0 : 1;
+    const uint16_t* x_seg = sg ? k.p[1] : k.p[0];
+    uint16_t* dx_seg = sg ? dk.p[1] : dk.p[0];
+    const long long x_bs = sg ? k.bstride[1] : k.bstride[0];
+    const long long dx_bs = sg ? dk.bstride[1] : dk.bstride[0];
+    const int row0c = min(row0, seg_end - 1);  // row0, or the segment's last row when the warp has none
+    const long long n0 = row0c - (sg ? g.T_txt : 0);  // token of row0c inside its segment
     const uint16_t* x_row0 = x_seg + (((long long)b * x_bs + n0) * g.H + h) * kHeadDim + 4 * lane;
     uint16_t* dx_row0 = dx_seg + (((long long)b * dx_bs + n0) * g.H + h) * kHeadDim + 4 * lane;
     const size_t token_stride = (size_t)g.H * kHeadDim;
-    for (int i = 0; i < kNrbRowsPerWarp; ++i) {
-        const int n = row0 + i;
-        if (n >= seg_end) break;
-        const float2* trow = tab + (size_t)(token_pos(g, n, ax) - g.p_lo) * kPairs;
-        const float2 c0 = trow[k0], c1 = trow[k1];
-        const float4 dy = *reinterpret_cast<const float4*>(dyh + (bh * g.S + n) * kHeadDim + 4 * lane);
-        const uint2 xv = *reinterpret_cast<const uint2*>(x_row0 + i * token_stride);
-        const float r = r_all[bh * g.S + n];
-        float u[4];
-        u[0] = fmaf(dy.x, c0.x, dy.y * c0.y);
-        u[1] = fmaf(dy.y, c0.x, -(dy.x * c0.y));
-        u[2] = fmaf(dy.z, c1.x, dy.w * c1.y);
-        u[3] = fmaf(dy.w, c1.x, -(dy.z * c1.y));
-        const float x[4] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y)};
-        const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
-        float xh[4], w[4];
-        float dot = 0.0f;
+    // rows in groups of kNrbGroup: every load of a group is issued before
+    // its arithmetic, so a warp keeps several rows in flight
+    for (int i0 = 0; i0 < kNrbRowsPerWarp; i0 += kNrbGroup) {
+        float4 dyv[kNrbGroup];
+        uint2 xv[kNrbGroup];
+        float rv[kNrbGroup];
+        float2 c0v[kNrbGroup], c1v[kNrbGroup];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            xh[j] = x[j] * r;
-            w[j] = u[j] * gg[j];
-            dot = fmaf(w[j], xh[j], dot);
+        for (int j = 0; j < kNrbGroup; ++j) {
+            const int n = min(row0 + i0 + j, seg_end - 1);  // rows past the segment: a valid row, not stored
+            const float2* trow = tab + (size_t)(token_pos(g, n, ax) - g.p_lo) * kPairs;
+            c0v[j] = __ldg(trow + k0);
+            c1v[j] = __ldg(trow + k1);
+            dyv[j] = __ldg(reinterpret_cast<const float4*>(dkh + (bh * g.S + n) * kHeadDim + 4 * lane));
+            xv[j] = __ldg(reinterpret_cast<const uint2*>(x_row0 + (size_t)(n - row0c) * token_stride));
+            rv[j] = __ldg(rk + bh * g.S + n);
         }
 #pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
-        const float c = dot * (1.0f / 128.0f);
-        float dx[4];
+        for (int j = 0; j < kNrbGroup; ++j) {
+            const int i = i0 + j;
+            if (row0 + i >= seg_end) break;
+            const float4 dy = dyv[j];
+            const float2 c0 = c0v[j], c1 = c1v[j];
+            const float r = rv[j];
+            float u[4];
+            u[0] = fmaf(dy.x, c0.x, dy.y * c0.y);
+            u[1] = fmaf(dy.y, c0.x, -(dy.x * c0.y));
+            u[2] = fmaf(dy.z, c1.x, dy.w * c1.y);
+            u[3] = fmaf(dy.w, c1.x, -(dy.z * c1.y));
+            const float x[4] = {bf16_lo(xv[j].x), bf16_hi(xv[j].x), bf16_lo(xv[j].y), bf16_hi(xv[j].y)};
+            const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
+            float xh[4], w[4];
+            float dot = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            dx[j] = r * fmaf(-xh[j], c, w[j]);
-            acc[j] = fmaf(u[j], xh[j], acc[j]);
+            for (int e = 0; e < 4; ++e) {
+                xh[e] = x[e] * r;
+                w[e] = u[e] * gg[e];
+                dot = fmaf(w[e], xh[e], dot);
+            }
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
+            const float c = dot * (1.0f / 128.0f);
+            float dx[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                dx[e] = r * fmaf(-xh[e], c, w[e]);
+                acc[e] = fmaf(u[e], xh[e], acc[e]);
+            }
+            *reinterpret_cast<uint2*>(dx_row0 + (size_t)i * token_stride) =
+                make_uint2(pack_bf16(dx[0], dx[1]), pack_bf16(dx[2], dx[3]));
         }
-        *reinterpret_cast<uint2*>(dx_row0 + i * token_stride) = make_uint2(pack_bf16(dx[0], dx[1]), pack_bf16(dx[2], dx[3]));
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) red[warp][4 * lane + j] = acc[j];
     __syncthreads();
-    if (threadIdx.x < 2 * kHeadDim) {
-        const int which = threadIdx.x / kHeadDim, d = threadIdx.x % kHeadDim;
-        const int w0 = 4 * which;
-        float s = red[w0][d];
-        s += red[w0 + 1][d];
-        s += red[w0 + 2][d];
-        s += red[w0 + 3][d];
-        const int nch = g.n_dg_chunks_txt + g.n_dg_chunks_img;
-        dg_chunks[((bh * 2 + which) * nch + chunk) * kHeadDim + d] = s;
+    const int nt = g.ntq_txt + g.ntq_img;
+    float* part = dgt + ((bh * 2 + 1) * nt + tile) * 4 * kHeadDim;
+    for (int i = threadIdx.x; i < 4 * kHeadDim; i += blockDim.x) {
+        const int j = i / kHeadDim, d = i % kHeadDim;
+        part[i] = red[2 * j][d] + red[2 * j + 1][d];
     }
 }
 
-// dg_partial[b,h,slot,d] = sum over that stream's chunks, ascending.
+// ---------------------------------------------------------------- gain-gradient folds
+// The dQ kernel's epilogue (q) and norm_rope_bwd_k (k) leave one partial per (b, h, q|k, 128-token
+// tile, 32-row quarter, dim): dgt[b][h][q|k][tile][quarter][128].
+// dg_partial[b,h,slot,d] = sum over that stream's tiles, ascending, of
+// ((quarter 0 + quarter 1) + (quarter 2 + quarter 3)).
 // Slots: 0 q_txt, 1 k_txt, 2 q_img, 3 k_img.
-__global__ void dg_fold_bh_kernel(Geom g, const float* __restrict__ dg_chunks,
-                                  float* __restrict__ dg_partial) {
+__global__ void dg_fold_bh_kernel(Geom g, const float* __restrict__ dgt, float* __restrict__ dg_partial) {
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= g.B * g.H * 4 * kHeadDim) return;
     const int d = idx % kHeadDim;
@@ -289,12 +302,16 @@ __global__ void dg_fold_bh_kernel(Geom g, const float* __restrict__ dg_chunks,
     const size_t bh = idx / (4 * kHeadDim);
     const int which = slot & 1;
     const bool img = slot >= 2;
-    const int nch = g.n_dg_chunks_txt + g.n_dg_chunks_img;
-    const int c_begin = img ? g.n_dg_chunks_txt : 0;
-    const int c_end = img ? nch : g.n_dg_chunks_txt;
-    const float* src = dg_chunks + ((bh * 2 + which) * nch) * kHeadDim + d;
+    const int nt = g.ntq_txt + g.ntq_img;
+    const int t_begin = img ? g.ntq_txt : 0;
+    const int t_end = img ? nt : g.ntq_txt;
+    const float* src = dgt + ((bh * 2 + which) * nt) * 4 * kHeadDim + d;
     float s = 0.0f;
-    for (int c = c_begin; c < c_end; ++c) s += src[(size_t)c * kHeadDim];
+#pragma unroll 8
+    for (int t = t_begin; t < t_end; ++t) {  // unrolled so the loads of 8 tiles are in flight together
+        const float* p = src + (size_t)t * 4 * kHeadDim;
+        s += (p[0] + p[kHeadDim]) + (p[2 * kHeadDim] + p[3 * kHeadDim]);
+    }
     dg_partial[idx] = s;
 }
 
@@ -352,23 +369,21 @@ cudaError_t launch_bwd_pre(const Geom& g, const SegBf16& out, const SegBf16& dou
     return cudaGetLastError();
 }
 
-cudaError_t launch_norm_rope_bwd(const Geom& g, const SegBf16& q, const SegBf16& k,
-                                 const float* const gains[4], const float2* tab, const float* rq,
-                                 const float* rk, const float* dqh, const float* dkh, const SegBf16& dq,
-                                 const SegBf16& dk, float* dg_chunks, cudaStream_t s) {
-    dim3 grid(g.n_dg_chunks_txt + g.n_dg_chunks_img, g.H, g.B);
+cudaError_t launch_norm_rope_bwd_k(const Geom& g, const SegBf16& k, const float* gk_txt, const float* gk_img,
+                                   const float2* tab, const float* rk, const float* dkh, const SegBf16& dk,
+                                   float* dgt, cudaStream_t s) {
+    dim3 grid(g.ntq_txt + g.ntq_img, g.H, g.B);
     timing_begin(kKNormRopeBwd, s);
-    norm_rope_bwd_kernel<<<grid, 256, 0, s>>>(g, q, k, gains[0], gains[1], gains[2], gains[3], tab,
-                                              rq, rk, dqh, dkh, dq, dk, dg_chunks);
+    norm_rope_bwd_k_kernel<<<grid, 256, 0, s>>>(g, k, gk_txt, gk_img, tab, rk, dkh, dk, dgt);
     timing_end(kKNormRopeBwd, s);
     return cudaGetLastError();
 }
 
-cudaError_t launch_dg_fold(const Geom& g, const float* dg_chunks, float* dg_partial, float* dg,
+cudaError_t launch_dg_fold(const Geom& g, const float* dgt, float* dg_partial, float* dg,
                            cudaStream_t s) {
     const int n = g.B * g.H * 4 * kHeadDim;
     timing_begin(kKDgFold, s);
-    dg_fold_bh_kernel<<<(n + 255) / 256, 256, 0, s>>>(g, dg_chunks, dg_partial);
+    dg_fold_bh_kernel<<<(n + 255) / 256, 256, 0, s>>>(g, dgt, dg_partial);
     dg_fold_total_kernel<<<1, 4 * kHeadDim, 0, s>>>(g, dg_partial, dg);
     timing_end(kKDgFold, s);
     return cudaGetLastError();

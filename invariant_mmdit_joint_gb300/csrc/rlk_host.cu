@@ -77,8 +77,6 @@ Geom make_geom(const rlk_ja_shape* sh) {
     g.n_pos = p_hi - p_lo + 1;
     g.eps = sh->eps;
     g.theta = sh->theta;
-    g.n_dg_chunks_txt = (g.T_txt + kDgChunk - 1) / kDgChunk;
-    g.n_dg_chunks_img = (g.T_img + kDgChunk - 1) / kDgChunk;
     g.ntq_txt = (g.T_txt + 127) / 128;
     g.ntq_img = (g.T_img + 127) / 128;
     g.nq_pad = 128 * (g.ntq_txt + g.ntq_img);
@@ -101,21 +99,21 @@ CtxLayout ctx_layout(const Geom& g) {
 }
 
 struct WsLayout {
-    size_t lse2, delta, dqh, dkh, dgc, dgp, dst, total;
+    size_t lse2, delta, dkh, dgt, dgp, dst, total;
 };
 WsLayout ws_layout(const Geom& g) {
     const size_t rows = (size_t)g.B * g.H * g.S;
     const size_t slots = (size_t)g.B * g.H * g.nq_pad;
-    const size_t nch = (size_t)g.n_dg_chunks_txt + g.n_dg_chunks_img;
+    const size_t ntiles = (size_t)g.ntq_txt + g.ntq_img;
     WsLayout l{};
     l.lse2 = 0;
     l.delta = align_up(l.lse2 + slots * 4);
-    l.dqh = align_up(l.delta + slots * 4);
-    l.dkh = align_up(l.dqh + rows * kHeadDim * 4);
-    l.dgc = align_up(l.dkh + rows * kHeadDim * 4);
-    l.dgp = align_up(l.dgc + (size_t)g.B * g.H * 2 * nch * kHeadDim * 4);
+    // dk^ (fp32 [B, H, S, 128]), from the dK/dV kernel to norm_rope_bwd_k
+    l.dkh = align_up(l.delta + slots * 4);
+    // gain-gradient partials [B, H, 2, n_tiles, 4, 128] and their per-(b, h) folds
+    l.dgt = align_up(l.dkh + rows * kHeadDim * 4);
+    l.dgp = align_up(l.dgt + (size_t)g.B * g.H * 2 * ntiles * 4 * kHeadDim * 4);
     // bf16 dS^T tile images, one 32 KB image per (query tile, key tile)
-    const size_t ntiles = (size_t)g.ntq_txt + g.ntq_img;
     l.dst = align_up(l.dgp + (size_t)g.B * g.H * 4 * kHeadDim * 4);
     l.total = align_up(l.dst + (size_t)g.B * g.H * ntiles * ntiles * 32768);
     return l;
@@ -292,7 +290,7 @@ const OpInfo kOps[] = {
 };
 const char* const kKernelNames[kNumKernelIds] = {
     "rope_table_kernel", "prologue_kernel", "attn_fwd_tc_kernel", "bwd_pre_kernel",
-    "attn_bwd_dkdv_tc_kernel", "attn_bwd_dq_tc_kernel", "norm_rope_bwd_kernel", "dg_fold_kernels",
+    "attn_bwd_dkdv_tc_kernel", "attn_bwd_dq_tc_kernel", "norm_rope_bwd_k_kernel", "dg_fold_kernels",
     "qk_gemm_kernel", "softmax_kernel", "av_gemm_kernel", "attn_fwd_tc_kernel<shard>", "qkv_gemm_kernel",
     "qkv_gemm_kernel<out_proj>"};
 
@@ -411,18 +409,18 @@ rlk_status bwd_core(const Geom& g, const ValidLen& vl, const SegBf16& q, const S
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     float* lse2_p = reinterpret_cast<float*>(ws + w.lse2);
     float* delta_p = reinterpret_cast<float*>(ws + w.delta);
-    float* dqh = reinterpret_cast<float*>(ws + w.dqh);
     float* dkh = reinterpret_cast<float*>(ws + w.dkh);
-    float* dgc = reinterpret_cast<float*>(ws + w.dgc);
+    float* dgt = reinterpret_cast<float*>(ws + w.dgt);
     float* dgp = dg_partial != nullptr ? dg_partial : reinterpret_cast<float*>(ws + w.dgp);
     uint8_t* ds_tiles = ws + w.dst;
+    const NormRopeBwdIo nr{q, dq, rq, {gains[0], gains[1], gains[2], gains[3]}, tab, dgt};
     if (launch_bwd_pre(g, out, dout, lse, lse2_p, delta_p, s) != cudaSuccess) return RLK_ERR_CUDA;
     if (launch_attn_bwd_dkdv(g, vl, qh, kh, v, dout, lse2_p, delta_p, dv, dkh, ds_tiles, s) != cudaSuccess)
         return RLK_ERR_CUDA;
-    if (launch_attn_bwd_dq(g, vl, kh, ds_tiles, dqh, s) != cudaSuccess) return RLK_ERR_CUDA;
-    if (launch_norm_rope_bwd(g, q, k, gains, tab, rq, rk, dqh, dkh, dq, dk, dgc, s) != cudaSuccess)
+    if (launch_attn_bwd_dq(g, vl, kh, ds_tiles, nr, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_norm_rope_bwd_k(g, k, gains[1], gains[3], tab, rk, dkh, dk, dgt, s) != cudaSuccess)
         return RLK_ERR_CUDA;
-    if (launch_dg_fold(g, dgc, dgp, dg, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_dg_fold(g, dgt, dgp, dg, s) != cudaSuccess) return RLK_ERR_CUDA;
     return RLK_OK;
 }
 }  // namespace

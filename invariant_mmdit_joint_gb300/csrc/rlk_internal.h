@@ -13,7 +13,6 @@ constexpr int kHeadDim = 128;
 constexpr int kPairs = kHeadDim / 2;       // RoPE pairs per head row
 constexpr int kAxis0Pairs = 8;             // frame axis: 16 dims
 constexpr int kAxis1Pairs = 28;            // row axis: 56 dims
-constexpr int kDgChunk = 64;               // tokens per gain-gradient chunk
 
 // Geometry of one call, derived from rlk_ja_shape on the host. Every kernel
 // receives it by value. Tile boundaries are functions of (T_txt, grid) only.
@@ -23,7 +22,6 @@ struct Geom {
     int ctr_h, ctr_w;   // ceil(gh/2), ceil(gw/2): image centring
     int p_lo, n_pos;    // cos/sin table covers positions [p_lo, p_lo + n_pos)
     float eps, theta;
-    int n_dg_chunks_txt, n_dg_chunks_img;
     // query / key tiles of 128, segment aligned: text tiles from token 0,
     // image tiles from token T_txt; nq_pad = 128 * (ntq_txt + ntq_img) slots
     // per (b, h) in the tile-padded layout of lse2 and Delta
@@ -128,13 +126,11 @@ cudaError_t launch_prologue(const Geom& g, const SegBf16& q, const SegBf16& k,
                             cudaStream_t s);
 cudaError_t launch_bwd_pre(const Geom& g, const SegBf16& out, const SegBf16& dout,
                            const float* lse, float* lse2_p, float* delta_p, cudaStream_t s);
-cudaError_t launch_norm_rope_bwd(const Geom& g, const SegBf16& q, const SegBf16& k,
-                                 const float* const gains[4], const float2* tab,
-                                 const float* rq, const float* rk,
-                                 const float* dqh, const float* dkh,
-                                 const SegBf16& dq, const SegBf16& dk, float* dg_chunks,
-                                 cudaStream_t s);
-cudaError_t launch_dg_fold(const Geom& g, const float* dg_chunks, float* dg_partial,
+// dK from dk^ (fp32 [B, H, S, 128]) and the k gain-gradient partials into dgt
+cudaError_t launch_norm_rope_bwd_k(const Geom& g, const SegBf16& k, const float* gk_txt, const float* gk_img,
+                                   const float2* tab, const float* rk, const float* dkh, const SegBf16& dk,
+                                   float* dgt, cudaStream_t s);
+cudaError_t launch_dg_fold(const Geom& g, const float* dgt, float* dg_partial,
                            float* dg, cudaStream_t s);
 int probe_prologue_tu(void);
 
@@ -154,13 +150,28 @@ int probe_fwd_tu(void);
 int read_and_clear_status_fwd(cudaStream_t s);
 
 // k_attn_bwd.cu
+// What the RoPE / RMSNorm backward of the query rows (in the dQ kernel's
+// epilogue) reads and writes: the pre-norm q (bf16 [B, S, H, 128] per
+// segment), its RMSNorm factors rq [B, H, S], the gains (q_txt, k_txt,
+// q_img, k_img), the cos/sin table; dQ (bf16, per segment) and the q half
+// of the gain-gradient partials dgt [B, H, 2 (q, k), n_tiles, 4 (32-row
+// quarters), 128].
+struct NormRopeBwdIo {
+    SegBf16 q, dq;
+    const float* rq;
+    const float* gains[4];
+    const float2* tab;
+    float* dgt;
+};
+// dkh: dk^ (the gradient of the rotated, normalised keys, times 1/sqrt(128)),
+// fp32 [B, H, S, 128], written by dkdv and read by norm_rope_bwd_k.
 cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16_t* qh,
                                  const uint16_t* kh, const SegBf16& v,
                                  const SegBf16& dout, const float* lse2_p,
                                  const float* delta_p, const SegBf16& dv, float* dkh,
                                  uint8_t* ds_tiles, cudaStream_t s);
 cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t* kh,
-                               const uint8_t* ds_tiles, float* dqh, cudaStream_t s);
+                               const uint8_t* ds_tiles, const NormRopeBwdIo& nr, cudaStream_t s);
 int probe_bwd_tu(void);
 int read_and_clear_status_bwd(cudaStream_t s);
 

@@ -51,9 +51,10 @@ def test_buffer_sizes_match_documented_layout(L):
     n_pos = (32 + 256 - 1) - (-32) + 1
     ctx = up(up(up(up(rows * 256) + rows * 256) + rows * 4) + rows * 4) + n_pos * 64 * 8
     assert pkg.rlk_joint_attn_ctx_bytes(s) == up(ctx)
-    nch = 256 // 64 + 4096 // 64
-    slots = 2 * 24 * 128 * (256 // 128 + 4096 // 128)  # tile-padded lse2 and Delta
-    ws = up(up(up(up(up(slots * 4) + slots * 4) + rows * 512) + rows * 512) + 2 * 24 * 2 * nch * 512)
+    nt = 256 // 128 + 4096 // 128
+    slots = 2 * 24 * 128 * nt  # tile-padded lse2 and Delta
+    # dk^ (fp32), gain-gradient partials per (b, h, q|k, tile, 32-row quarter), then per (b, h)
+    ws = up(up(up(up(slots * 4) + slots * 4) + rows * 512) + 2 * 24 * 2 * nt * 4 * 512)
     ws = up(ws + 2 * 24 * 4 * 512)
     ws += 2 * 24 * 34 * 34 * 32768  # bf16 dS tiles, 128 x 128 per (query tile, key tile)
     assert pkg.rlk_joint_attn_bwd_workspace_bytes(s) == up(ws)

@@ -11,7 +11,7 @@ from tests import _helpers as Hh
 pytestmark = pytest.mark.gpu
 
 FWD = ["rope_table_kernel", "prologue_kernel", "attn_fwd_tc_kernel"]
-BWD = ["bwd_pre_kernel", "attn_bwd_dkdv_tc_kernel", "attn_bwd_dq_tc_kernel", "norm_rope_bwd_kernel",
+BWD = ["bwd_pre_kernel", "attn_bwd_dkdv_tc_kernel", "attn_bwd_dq_tc_kernel", "norm_rope_bwd_k_kernel",
        "dg_fold_kernels"]
 
 
