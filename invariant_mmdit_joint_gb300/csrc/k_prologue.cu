@@ -146,7 +146,9 @@ __global__ void __launch_bounds__(256, 4) prologue_kernel(
 // A slot holding a token gets Delta = sum_d dO * O (each lane adds its 8
 // products in order, then a butterfly over the half warp) and
 // lse2 = lse * log2(e); a slot past its segment gets Delta = 0 and
-// lse2 = +inf, so the backward kernels see P = 0 there.
+// lse2 = +inf, so the backward kernels see P = 0 there. One half warp per
+// slot, slots in order (enumerating them in the inputs' memory order instead
+// measured 35 us against 30).
 __global__ void __launch_bounds__(256) bwd_pre_kernel(Geom g, const SegBf16 o, const SegBf16 dout,
                                                       const float* __restrict__ lse, float* __restrict__ lse2_p,
                                                       float* __restrict__ delta_p) {
@@ -183,23 +185,24 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(Geom g, const SegBf16 o, c
 
 // ---------------------------------------------------------------- key-side norm/rope backward
 // (The query side runs in the dQ kernel's epilogue, from its accumulator.)
-// CTA = (128-token tile of one stream segment, h, b); warp w takes rows
-// 16 w .. 16 w + 15 of the tile in ascending order. Lane l owns dims
+// CTA = (128-token tile of one stream segment, h, b), 128 threads; warp w
+// takes rows 32 w .. 32 w + 31 of the tile in ascending order (the whole
+// grid is resident at once at the 1024^2 shapes). Lane l owns dims
 // [4l, 4l+4) = pairs 2l, 2l+1. Per row:
 //   u  = R(-angle) * dk^          (inverse rotation)
 //   xh = k * r,  w = u * g,  c = (sum_d w_d xh_d) / 128   (lane order, then xor 16..1)
 //   dK = r * (w - xh * c)  -> bf16
 //   gain-gradient partial += u * xh (per lane, rows ascending)
-// Warps 2j and 2j + 1 add (in that order) into the tile's quarter j,
-// dgt[b][h][1][tile][j][128]: the layout the dQ epilogue fills for q.
-constexpr int kNrbRowsPerWarp = 16;
+// Warp w's partial is the tile's quarter w, dgt[b][h][1][tile][w][128]: the
+// layout the dQ epilogue fills for q.
+constexpr int kNrbWarps = 4;
+constexpr int kNrbRowsPerWarp = 32;
 constexpr int kNrbGroup = 4;
 
-__global__ void __launch_bounds__(256) norm_rope_bwd_k_kernel(
+__global__ void __launch_bounds__(kNrbWarps * 32) norm_rope_bwd_k_kernel(
     Geom g, const SegBf16 k, const float* __restrict__ gk_txt, const float* __restrict__ gk_img,
     const float2* __restrict__ tab, const float* __restrict__ rk, const float* __restrict__ dkh, const SegBf16 dk,
     float* __restrict__ dgt) {
-    __shared__ float red[8][kHeadDim];
     const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const bool txt = tile < g.ntq_txt;
@@ -277,15 +280,9 @@ __global__ void __launch_bounds__(256) norm_rope_bwd_k_kernel(
                 make_uint2(pack_bf16(dx[0], dx[1]), pack_bf16(dx[2], dx[3]));
         }
     }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) red[warp][4 * lane + j] = acc[j];
-    __syncthreads();
     const int nt = g.ntq_txt + g.ntq_img;
-    float* part = dgt + ((bh * 2 + 1) * nt + tile) * 4 * kHeadDim;
-    for (int i = threadIdx.x; i < 4 * kHeadDim; i += blockDim.x) {
-        const int j = i / kHeadDim, d = i % kHeadDim;
-        part[i] = red[2 * j][d] + red[2 * j + 1][d];
-    }
+    float* part = dgt + (((bh * 2 + 1) * nt + tile) * 4 + warp) * kHeadDim;
+    *reinterpret_cast<float4*>(part + 4 * lane) = make_float4(acc[0], acc[1], acc[2], acc[3]);
 }
 
 // ---------------------------------------------------------------- gain-gradient folds
@@ -322,6 +319,7 @@ __global__ void dg_fold_total_kernel(Geom g, const float* __restrict__ dg_partia
     float total = 0.0f;
     for (int b = 0; b < g.B; ++b) {
         float sb = 0.0f;
+#pragma unroll 8
         for (int h = 0; h < g.H; ++h) sb += dg_partial[((size_t)b * g.H + h) * 4 * kHeadDim + idx];
         total += sb;
     }
@@ -374,7 +372,7 @@ cudaError_t launch_norm_rope_bwd_k(const Geom& g, const SegBf16& k, const float*
                                    float* dgt, cudaStream_t s) {
     dim3 grid(g.ntq_txt + g.ntq_img, g.H, g.B);
     timing_begin(kKNormRopeBwd, s);
-    norm_rope_bwd_k_kernel<<<grid, 256, 0, s>>>(g, k, gk_txt, gk_img, tab, rk, dkh, dk, dgt);
+    norm_rope_bwd_k_kernel<<<grid, kNrbWarps * 32, 0, s>>>(g, k, gk_txt, gk_img, tab, rk, dkh, dk, dgt);
     timing_end(kKNormRopeBwd, s);
     return cudaGetLastError();
 }
