@@ -49,9 +49,8 @@ __global__ void rope_table_kernel(Geom g, const PairFreqs fr, float2* __restrict
 // squares in order, then a butterfly over the 16 lanes (xor 8, 4, 2, 1).
 // r = 1 / sqrt(ss/128 + eps) with IEEE sqrt and division. y = (x * r) * g;
 // then each pair turns by its angle; one round to bf16 at the output.
-__device__ __forceinline__ void norm_rope_row(const uint4 xv, const float* __restrict__ gain,
-                                              const float2* __restrict__ tab_row, int lane16, float eps,
-                                              uint4& out, float& r_out) {
+__device__ __forceinline__ void norm_rope_row(const uint4 xv, const float* gain, const float4 t0, const float4 t1,
+                                              int lane16, float eps, uint4& out, float& r_out) {
     float x[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
                   bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
     float ss = 0.0f;
@@ -61,11 +60,9 @@ __device__ __forceinline__ void norm_rope_row(const uint4 xv, const float* __res
     for (int m = 8; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
     float r = 1.0f / sqrtf(fmaf(ss, 1.0f / 128.0f, eps));
     r_out = r;
-    const float4 g0 = __ldg(reinterpret_cast<const float4*>(gain) + 2 * lane16);
-    const float4 g1 = __ldg(reinterpret_cast<const float4*>(gain) + 2 * lane16 + 1);
+    const float4 g0 = reinterpret_cast<const float4*>(gain)[2 * lane16];
+    const float4 g1 = reinterpret_cast<const float4*>(gain)[2 * lane16 + 1];
     const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-    const float4 t0 = __ldg(reinterpret_cast<const float4*>(tab_row + 4 * lane16));
-    const float4 t1 = __ldg(reinterpret_cast<const float4*>(tab_row + 4 * lane16) + 1);
     const float2 cs[4] = {make_float2(t0.x, t0.y), make_float2(t0.z, t0.w), make_float2(t1.x, t1.y),
                           make_float2(t1.z, t1.w)};
     uint32_t o[4];
@@ -81,8 +78,10 @@ __device__ __forceinline__ void norm_rope_row(const uint4 xv, const float* __res
 }
 
 // A CTA of 256 threads covers 32 rows: half warp w takes rows base + w and
-// base + 16 + w (the two half warps of a warp read 512 contiguous bytes);
-// all four 16-byte input loads of a lane are issued before any arithmetic.
+// base + 16 + w (the two half warps of a warp read 512 contiguous bytes).
+// Every global load of a lane (q, k and the (cos, sin) table row of both
+// rows) is issued before any arithmetic; the four gain vectors are staged
+// in shared memory first.
 constexpr int kPrologueRowsPerCta = 32;
 
 __global__ void __launch_bounds__(256, 4) prologue_kernel(
@@ -91,11 +90,20 @@ __global__ void __launch_bounds__(256, 4) prologue_kernel(
     const float* __restrict__ gq_img, const float* __restrict__ gk_img,
     const float2* __restrict__ tab, uint16_t* __restrict__ qh, uint16_t* __restrict__ kh,
     float* __restrict__ rq, float* __restrict__ rk) {
+    __shared__ __align__(16) float gs[4][kHeadDim];  // q_txt, k_txt, q_img, k_img
+    {
+        const int i = threadIdx.x;  // 256 threads, 512 gains
+        const float* src0 = i < kHeadDim ? gq_txt : gk_txt;
+        const float* src1 = i < kHeadDim ? gq_img : gk_img;
+        gs[i / kHeadDim][i % kHeadDim] = __ldg(src0 + i % kHeadDim);
+        gs[2 + i / kHeadDim][i % kHeadDim] = __ldg(src1 + i % kHeadDim);
+    }
     const long long rows = (long long)g.B * g.S * g.H;
     const int lane16 = threadIdx.x % kRowThreads;
     const int axis = pair_axis(4 * lane16);
     const long long base = (long long)blockIdx.x * kPrologueRowsPerCta + threadIdx.x / kRowThreads;
     uint4 xq[2], xk[2];
+    float4 ta[2], tb[2];
     int hh[2], nn[2], bb[2];
     bool active[2];
 #pragma unroll
@@ -118,16 +126,21 @@ __global__ void __launch_bounds__(256, 4) prologue_kernel(
              hh[u]) * kHeadDim + 8 * lane16;
         xq[u] = __ldg(reinterpret_cast<const uint4*>((img ? q.p[1] : q.p[0]) + off));
         xk[u] = __ldg(reinterpret_cast<const uint4*>((img ? k.p[1] : k.p[0]) + off));
+        // lane l's four (cos, sin) pairs: two 16-byte loads from one table row
+        const float4* trow =
+            reinterpret_cast<const float4*>(tab + (size_t)(token_pos(g, nn[u], axis) - g.p_lo) * kPairs + 4 * lane16);
+        ta[u] = __ldg(trow);
+        tb[u] = __ldg(trow + 1);
     }
+    __syncthreads();  // gains staged
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         const int h = hh[u], n = nn[u], b = bb[u];
         const bool txt = n < g.T_txt;
-        const float2* trow = tab + (size_t)(token_pos(g, n, axis) - g.p_lo) * kPairs;
         uint4 oq, ok;
         float r_q, r_k;
-        norm_rope_row(xq[u], txt ? gq_txt : gq_img, trow, lane16, g.eps, oq, r_q);
-        norm_rope_row(xk[u], txt ? gk_txt : gk_img, trow, lane16, g.eps, ok, r_k);
+        norm_rope_row(xq[u], gs[txt ? 0 : 2], ta[u], tb[u], lane16, g.eps, oq, r_q);
+        norm_rope_row(xk[u], gs[txt ? 1 : 3], ta[u], tb[u], lane16, g.eps, ok, r_k);
         if (!active[u]) continue;
         const size_t bh = (size_t)b * g.H + h;
         const size_t dst = (bh * g.S + n) * kHeadDim + 8 * lane16;
@@ -164,6 +177,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(Geom g, const SegBf16 o, c
     const bool valid = t < g.ntq_txt ? n < g.T_txt : n < g.S;
     const int b = (int)(bh / g.H), h = (int)(bh % g.H);
     float acc = 0.0f;
+    // lse is loaded with the rows, not after the reduction
+    const float lse_n = valid && lane16 == 0 ? __ldg(lse + bh * g.S + n) : 0.0f;
     if (valid) {
         const uint4 ov = __ldg(reinterpret_cast<const uint4*>(seg_row(o, g, b, n, h) + 8 * lane16));
         const uint4 dv = __ldg(reinterpret_cast<const uint4*>(seg_row(dout, g, b, n, h) + 8 * lane16));
@@ -179,15 +194,16 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(Geom g, const SegBf16 o, c
     for (int m = 8; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
     if (active && lane16 == 0) {
         delta_p[slot] = acc;
-        lse2_p[slot] = valid ? lse[bh * g.S + n] * 1.4426950408889634f : INFINITY;
+        lse2_p[slot] = valid ? lse_n * 1.4426950408889634f : INFINITY;
     }
 }
 
 // ---------------------------------------------------------------- key-side norm/rope backward
 // (The query side runs in the dQ kernel's epilogue, from its accumulator.)
 // CTA = (128-token tile of one stream segment, h, b), 128 threads; warp w
-// takes rows 32 w .. 32 w + 31 of the tile in ascending order (the whole
-// grid is resident at once at the 1024^2 shapes). Lane l owns dims
+// takes rows 32 w .. 32 w + 31 of the tile in ascending order, loading four
+// rows at a time (measured against 256-thread CTAs of 16 rows per warp, and
+// against groups of 2 or 8 rows or a cap of 64 registers: all slower). Lane l owns dims
 // [4l, 4l+4) = pairs 2l, 2l+1. Per row:
 //   u  = R(-angle) * dk^          (inverse rotation)
 //   xh = k * r,  w = u * g,  c = (sum_d w_d xh_d) / 128   (lane order, then xor 16..1)
