@@ -84,6 +84,9 @@ typedef enum rlk_status {
 /* Largest batch one call accepts (valid lengths travel as kernel arguments). */
 #define RLK_MAX_BATCH 256
 
+/* Shape limits (otherwise RLK_ERR_INVALID_ARG): T_txt + grid_h * grid_w
+ * <= 2^20 tokens, and B * H * 128 * (ceil(T_txt / 128) + ceil(grid_h *
+ * grid_w / 128)) < 2^31 rows (q alone would then exceed 512 GB). */
 typedef struct rlk_ja_shape {
     int32_t B;        /* samples, 1 .. RLK_MAX_BATCH */
     int32_t T_txt;    /* padded text length, >= 0 */

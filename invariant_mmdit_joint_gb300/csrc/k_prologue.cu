@@ -98,10 +98,15 @@ __global__ void __launch_bounds__(256, 4) prologue_kernel(
         gs[i / kHeadDim][i % kHeadDim] = __ldg(src0 + i % kHeadDim);
         gs[2 + i / kHeadDim][i % kHeadDim] = __ldg(src1 + i % kHeadDim);
     }
-    const long long rows = (long long)g.B * g.S * g.H;
+    // rows (b, n, h) of [B, S, H] in 32-bit arithmetic (B * S * H rows of
+    // 256 bytes fit far below 2^31); the CTA's first row is divided out once,
+    // each thread's row follows from it by carrying, not by division
+    const int rows = g.B * g.S * g.H;
     const int lane16 = threadIdx.x % kRowThreads;
     const int axis = pair_axis(4 * lane16);
-    const long long base = (long long)blockIdx.x * kPrologueRowsPerCta + threadIdx.x / kRowThreads;
+    const int base = (int)blockIdx.x * kPrologueRowsPerCta;
+    const int bn0 = base / g.H, h0 = base - bn0 * g.H;
+    const int b0 = bn0 / g.S, n0 = bn0 - b0 * g.S;
     uint4 xq[2], xk[2];
     float4 ta[2], tb[2];
     int hh[2], nn[2], bb[2];
@@ -109,15 +114,25 @@ __global__ void __launch_bounds__(256, 4) prologue_kernel(
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         // a half warp past the end works on the last row and stores
-        // nothing, so that every lane of the warp reaches the shuffles;
-        // rows are enumerated as (b, n, h) of [B, S, H]
-        const long long rr = base + 16 * u;
-        active[u] = rr < rows;
-        const long long row = active[u] ? rr : rows - 1;
-        hh[u] = (int)(row % g.H);
-        const long long bn = row / g.H;
-        nn[u] = (int)(bn % g.S);
-        bb[u] = (int)(bn / g.S);
+        // nothing, so that every lane of the warp reaches the shuffles
+        const int ro = (int)(threadIdx.x / kRowThreads) + 16 * u;  // row offset in the CTA
+        active[u] = base + ro < rows;
+        int h = h0 + ro, n = n0, b = b0;
+        while (h >= g.H) {
+            h -= g.H;
+            if (++n == g.S) {
+                n = 0;
+                ++b;
+            }
+        }
+        if (!active[u]) {
+            h = g.H - 1;
+            n = g.S - 1;
+            b = g.B - 1;
+        }
+        hh[u] = h;
+        nn[u] = n;
+        bb[u] = b;
         // q and k share their segment strides (both calls pass them alike),
         // so one offset addresses both
         const bool img = nn[u] >= g.T_txt;
@@ -165,17 +180,32 @@ __global__ void __launch_bounds__(256, 4) prologue_kernel(
 __global__ void __launch_bounds__(256) bwd_pre_kernel(Geom g, const SegBf16 o, const SegBf16 dout,
                                                       const float* __restrict__ lse, float* __restrict__ lse2_p,
                                                       float* __restrict__ delta_p) {
-    const long long slots = (long long)g.B * g.H * g.nq_pad;
-    const long long slot_raw = (long long)blockIdx.x * (blockDim.x / kRowThreads) + threadIdx.x / kRowThreads;
+    // 32-bit slots (the host caps B * H * nq_pad below 2^31); the CTA's first
+    // slot is divided out once and each half warp's follows by carrying
+    const int slots = g.B * g.H * g.nq_pad;
+    const int base = (int)blockIdx.x * (int)(blockDim.x / kRowThreads);
+    const int w = (int)(threadIdx.x / kRowThreads);
     const int lane16 = threadIdx.x % kRowThreads;
-    const bool active = slot_raw < slots;
-    const long long slot = active ? slot_raw : slots - 1;
-    const long long bh = slot / g.nq_pad;
-    const int r = (int)(slot % g.nq_pad);
-    const int t = r / 128, off = r % 128;
+    const bool active = base + w < slots;
+    const int bh0 = base / g.nq_pad;
+    int r = base - bh0 * g.nq_pad + w, b = bh0 / g.H, h = bh0 - (bh0 / g.H) * g.H;
+    if (r >= g.nq_pad) {  // at most one carry: 16 slots per CTA, nq_pad >= 128
+        r -= g.nq_pad;
+        if (++h == g.H) {
+            h = 0;
+            ++b;
+        }
+    }
+    if (!active) {  // the last slot: loads stay in bounds, nothing is stored
+        r = g.nq_pad - 1;
+        h = g.H - 1;
+        b = g.B - 1;
+    }
+    const size_t bh = (size_t)b * g.H + h;
+    const size_t slot = bh * g.nq_pad + r;
+    const int t = r >> 7, off = r & 127;
     const int n = t < g.ntq_txt ? 128 * t + off : g.T_txt + 128 * (t - g.ntq_txt) + off;
     const bool valid = t < g.ntq_txt ? n < g.T_txt : n < g.S;
-    const int b = (int)(bh / g.H), h = (int)(bh % g.H);
     float acc = 0.0f;
     // lse is loaded with the rows, not after the reduction
     const float lse_n = valid && lane16 == 0 ? __ldg(lse + bh * g.S + n) : 0.0f;
@@ -343,7 +373,7 @@ __global__ void dg_fold_total_kernel(Geom g, const float* __restrict__ dg_partia
 }
 
 unsigned row_blocks(const Geom& g) {
-    const long long rows = (long long)g.B * g.S * g.H;
+    const int rows = g.B * g.S * g.H;
     return (unsigned)((rows + kPrologueRowsPerCta - 1) / kPrologueRowsPerCta);
 }
 
@@ -376,7 +406,7 @@ cudaError_t launch_prologue(const Geom& g, const SegBf16& q, const SegBf16& k,
 
 cudaError_t launch_bwd_pre(const Geom& g, const SegBf16& out, const SegBf16& dout, const float* lse,
                            float* lse2_p, float* delta_p, cudaStream_t s) {
-    const long long slots = (long long)g.B * g.H * g.nq_pad;
+    const long long slots = (long long)g.B * g.H * g.nq_pad;  // < 2^31 (shape limit)
     timing_begin(kKBwdPre, s);
     bwd_pre_kernel<<<(unsigned)((slots + 15) / 16), 256, 0, s>>>(g, out, dout, lse, lse2_p, delta_p);
     timing_end(kKBwdPre, s);

@@ -50,7 +50,9 @@ bool shape_ok(const rlk_ja_shape* sh, rlk_status* why) {
     }
     const long long t_img = (long long)sh->grid_h * sh->grid_w;
     const long long s = t_img + sh->T_txt;
-    if (t_img > kMaxTokens || s > kMaxTokens || (long long)sh->B * sh->H * s * kHeadDim > (1LL << 40)) {
+    // rows (b, h, tile-padded token) are indexed in 32 bits on the device
+    const long long s_pad = 128 * ((sh->T_txt + 127) / 128 + (t_img + 127) / 128);
+    if (t_img > kMaxTokens || s > kMaxTokens || (long long)sh->B * sh->H * s_pad >= (1LL << 31)) {
         *why = RLK_ERR_INVALID_ARG;
         return false;
     }

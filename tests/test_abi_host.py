@@ -77,6 +77,16 @@ def test_invalid_shapes_fail_closed(L, mutate, code):
     assert rc == code
 
 
+def test_row_count_limit(L):
+    """B * H * (tile-padded S) must stay below 2^31 rows (the device indexes
+    rows in 32 bits); a shape just under the limit is accepted."""
+    rows_per_bh = 128 * (2 + 32)  # 256 text + 64 x 64 image tokens in tiles of 128
+    ok = pkg.Shape.make(B=256, T_txt=256, grid_h=64, grid_w=64, H=1900)
+    assert 256 * 1900 * rows_per_bh < 2 ** 31 and pkg.rlk_joint_attn_ctx_bytes(ok) > 0
+    bad = pkg.Shape.make(B=256, T_txt=256, grid_h=64, grid_w=64, H=1928)
+    assert 256 * 1928 * rows_per_bh >= 2 ** 31 and pkg.rlk_joint_attn_ctx_bytes(bad) == 0
+
+
 def _fwd(L, s, vl, ptr=1 << 20, lse=1 << 20, **over):
     p = dict(q=ptr, k=ptr, v=ptr, a=ptr, b=ptr, c=ptr, d=ptr, out=ptr, ctx=ptr)
     p.update(over)
