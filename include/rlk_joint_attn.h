@@ -50,6 +50,13 @@
  * (a cudaStream_t passed as void*; NULL = the legacy default stream) and
  * returns as soon as they are enqueued. Host arrays are read before return.
  *
+ * CUDA graphs: every entry point may be captured into a CUDA graph (stream
+ * capture), and a replay performs the same arithmetic as the eager call, so
+ * it gives the same bytes. Host arrays (txt_valid_len) and the tensor maps are
+ * taken by value at capture time. The first call on a device runs one-time
+ * checks that launch and synchronise; called inside a capture it returns
+ * RLK_ERR_UNSUPPORTED instead, so make one eager call first.
+ *
  * Errors: every entry point returns an rlk_status. On any validation error
  * nothing is launched and no output is touched. Unsupported configurations
  * fail closed with RLK_ERR_UNSUPPORTED; there is no fallback path.

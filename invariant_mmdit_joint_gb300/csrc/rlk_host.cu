@@ -137,11 +137,19 @@ int strict_all_units() {
     return 1;
 }
 
-rlk_status device_ok() {
+// The first call on a device runs the probes, which launch and synchronise:
+// inside a stream capture that would break the caller's capture, so such a
+// call fails closed instead (one eager call first makes later calls
+// capturable).
+rlk_status device_ok(void* stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RLK_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_dev_mu);
     if (g_dev_state[dev] == 0) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs) != cudaSuccess ||
+            cs != cudaStreamCaptureStatusNone)
+            return RLK_ERR_UNSUPPORTED;
         int major = 0, minor = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
@@ -458,7 +466,7 @@ static rlk_status rlk_joint_attn_fwd_impl(const rlk_ja_shape* shape, const void*
     for (const void* p : ptrs)
         if (!aligned16(p)) return RLK_ERR_ALIGNMENT;
     if (lse != nullptr && !aligned16(lse)) return RLK_ERR_ALIGNMENT;
-    st = device_ok();
+    st = device_ok(stream);
     if (st != RLK_OK) return st;
 
     const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
@@ -494,7 +502,7 @@ static rlk_status rlk_joint_attn_bwd_impl(const rlk_ja_shape* shape, const void*
     if (dg_partial != nullptr && !aligned16(dg_partial)) return RLK_ERR_ALIGNMENT;
     const WsLayout w = ws_layout(g);
     if (workspace_bytes < w.total) return RLK_ERR_WORKSPACE;
-    st = device_ok();
+    st = device_ok(stream);
     if (st != RLK_OK) return st;
 
     const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
@@ -539,7 +547,7 @@ static rlk_status rlk_joint_attn_fwd_streams_impl(const rlk_ja_shape* shape, con
     if (st != RLK_OK) return st;
     st = check_ptrs({g_q_txt, g_k_txt, g_q_img, g_k_img, ctx}, {lse});
     if (st != RLK_OK) return st;
-    st = device_ok();
+    st = device_ok(stream);
     if (st != RLK_OK) return st;
     const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
     return fwd_core(g, vl, seg_split(q_txt, q_img, g), seg_split(k_txt, k_img, g), seg_split(v_txt, v_img, g), gains,
@@ -574,7 +582,7 @@ static rlk_status rlk_joint_attn_bwd_streams_impl(
     st = check_ptrs({g_q_txt, g_k_txt, g_q_img, g_k_img, lse, ctx, dg, workspace}, {dg_partial});
     if (st != RLK_OK) return st;
     if (workspace_bytes < ws_layout(g).total) return RLK_ERR_WORKSPACE;
-    st = device_ok();
+    st = device_ok(stream);
     if (st != RLK_OK) return st;
     const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
     return bwd_core(g, vl, seg_split(q_txt, q_img, g), seg_split(k_txt, k_img, g), seg_split(v_txt, v_img, g), gains,
@@ -617,7 +625,7 @@ static rlk_status rlk_qkv_bias_gemm_impl(const rlk_ja_shape* shape, const void* 
     if (store_q && (st = check_pairs(g, {{q_txt, q_img}})) != RLK_OK) return st;
     if (store_k && (st = check_pairs(g, {{k_txt, k_img}})) != RLK_OK) return st;
     if (fused && (st = check_ptrs({g_q_txt, g_k_txt, g_q_img, g_k_img, ctx}, {})) != RLK_OK) return st;
-    st = device_ok();
+    st = device_ok(stream);
     if (st != RLK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint16_t* x[2] = {static_cast<const uint16_t*>(x_txt), static_cast<const uint16_t*>(x_img)};
@@ -667,7 +675,7 @@ static rlk_status rlk_joint_attn_fwd_ctx_impl(const rlk_ja_shape* shape, const v
     if (st != RLK_OK) return st;
     st = check_ptrs({ctx}, {lse});
     if (st != RLK_OK) return st;
-    st = device_ok();
+    st = device_ok(stream);
     if (st != RLK_OK) return st;
     const CtxLayout l = ctx_layout(g);
     const uint8_t* c = static_cast<const uint8_t*>(ctx);
@@ -694,7 +702,7 @@ static rlk_status rlk_attn_out_bias_gemm_impl(const rlk_ja_shape* shape, const v
     const Geom g = make_geom(shape);
     rlk_status st = check_pairs(g, {{o_txt, o_img}, {w_txt, w_img}, {b_txt, b_img}, {y_txt, y_img}});
     if (st != RLK_OK) return st;
-    st = device_ok();
+    st = device_ok(stream);
     if (st != RLK_OK) return st;
     const uint16_t* x[2] = {static_cast<const uint16_t*>(o_txt), static_cast<const uint16_t*>(o_img)};
     const uint16_t* w[2] = {static_cast<const uint16_t*>(w_txt), static_cast<const uint16_t*>(w_img)};
@@ -728,7 +736,7 @@ static rlk_status rlk_qk_norm_rope_impl(const rlk_ja_shape* shape, const void* q
     if (!shape_ok(shape, &why)) return why;
     rlk_status st = check_ptrs({q, k, g_q_txt, g_k_txt, g_q_img, g_k_img, ctx}, {});
     if (st != RLK_OK) return st;
-    st = device_ok();
+    st = device_ok(stream);
     if (st != RLK_OK) return st;
     const Geom g = make_geom(shape);
     const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
@@ -750,7 +758,7 @@ static rlk_status rlk_joint_attn_qk_gemm_impl(const rlk_ja_shape* shape, const v
     if (st != RLK_OK) return st;
     st = check_ptrs({ctx, scores}, {});
     if (st != RLK_OK) return st;
-    st = device_ok();
+    st = device_ok(stream);
     if (st != RLK_OK) return st;
     const CtxLayout l = ctx_layout(g);
     const uint8_t* c = static_cast<const uint8_t*>(ctx);
@@ -774,7 +782,7 @@ static rlk_status rlk_joint_attn_softmax_impl(const rlk_ja_shape* shape, const f
     if (st != RLK_OK) return st;
     st = check_ptrs({scores, p, alpha, l}, {lse});
     if (st != RLK_OK) return st;
-    st = device_ok();
+    st = device_ok(stream);
     if (st != RLK_OK) return st;
     if (launch_softmax(g, vl, scores, static_cast<uint16_t*>(p), alpha, l, lse, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
@@ -796,7 +804,7 @@ static rlk_status rlk_joint_attn_av_gemm_impl(const rlk_ja_shape* shape, const v
     if (st != RLK_OK) return st;
     st = check_ptrs({p, alpha, l, v, out}, {});
     if (st != RLK_OK) return st;
-    st = device_ok();
+    st = device_ok(stream);
     if (st != RLK_OK) return st;
     if (launch_av_gemm(g, vl, static_cast<const uint16_t*>(p), alpha, l, seg_concat(v, g), seg_concat(out, g),
                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -835,7 +843,7 @@ static rlk_status rlk_joint_attn_fwd_shard_impl(const rlk_ja_shape* shape, const
         return RLK_ERR_INVALID_ARG;
     st = check_ptrs({ctx, v}, {state_in, state_out, out, lse});
     if (st != RLK_OK) return st;
-    st = device_ok();
+    st = device_ok(stream);
     if (st != RLK_OK) return st;
     const CtxLayout l = ctx_layout(g);
     const uint8_t* c = static_cast<const uint8_t*>(ctx);
