@@ -492,10 +492,11 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
-    e0.record(stream)
-    e2e_pipelined(n_e2e, e0)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as e2e_clk:
+        e0.record(stream)
+        e2e_pipelined(n_e2e, e0)
+        e1.record(stream)
+        torch.cuda.synchronize()
     barrier()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
     e2e_value = job_throughput(flops["fwd_bwd"], world, ms_e2e)
@@ -571,7 +572,7 @@ def run_ours(args):
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                 "pipelined": "step i's compute overlaps step i+1's H2D and step i-1's D2H (3 streams, "
-                             "double-buffered device buffers)"},
+                             "double-buffered device buffers)", "clocks": e2e_clk.summary()},
         "e2e_serial": {"value": round(e2e_serial_value, 2), "unit": "TFLOP/s",
                        "ms_per_step": round(ms_e2e_serial, 4)},
         "ms_per_step_instrumented": round(ms_instrumented, 4),
