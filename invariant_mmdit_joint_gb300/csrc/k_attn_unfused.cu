@@ -111,9 +111,13 @@ struct QkArgs {
     ValidLen vl;
     float* scores;      // [B, H, S, ncols]
     int ncols;
+    CUtensorMap map_s[2];  // scores per segment (text, image rows), fp32 boxes of 32 x 32
 };
 
-constexpr int kQkSmemBytes = 3 * kTileBytes + 1024;  // Q, two K slots
+// Q, two K slots, and the epilogue's staging: per epilogue warp its 32 rows
+// as four 32-column boxes of 4 KB in the 128-byte-swizzled layout of map_s
+constexpr int kQkStageBytes = 4 * 4 * 4096;
+constexpr int kQkSmemBytes = 3 * kTileBytes + kQkStageBytes + 1024;
 
 __global__ void __launch_bounds__(kThreads, 1) qk_gemm_kernel(const __grid_constant__ QkArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -212,11 +216,18 @@ __global__ void __launch_bounds__(kThreads, 1) qk_gemm_kernel(const __grid_const
             mbar_wait(bar_drain, 0, &no_abort, kWaitLimitNs);
         }
     } else {
-        // one query row per thread: TMEM lane quarter warp % 4
-        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
-        const int row = (warp & 3) * 32 + lane;
-        const int n = q0 + row;
-        float* srow = a.scores + ((bh * g.S + n) * (size_t)a.ncols);
+        // one query row per thread: TMEM lane quarter warp % 4. The warp
+        // stages its 32 rows of a key tile as four 32 x 32 fp32 boxes and its
+        // lane 0 stores them with TMA; the segment maps clip rows past the
+        // query's segment.
+        const int wq = warp & 3;
+        const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+        const uint32_t stage = sbase + 3 * kTileBytes + wq * (4 * 4096);
+        uint8_t* stage_p = smem_raw + (stage - smem_u32(smem_raw));
+        const int seg = qt < g.ntq_txt ? 0 : 1;
+        const int srow = (seg ? q0 - g.T_txt : q0) + 32 * wq;  // the warp's first row in its segment
+        const int sw = lane & 7;
+        if (lane == 0) prefetch_tensormap(&a.map_s[seg]);
         bool ok = true;
         for (int j = 0; j < nkt; ++j) {
             const int s = j & 1;
@@ -238,14 +249,28 @@ __global__ void __launch_bounds__(kThreads, 1) qk_gemm_kernel(const __grid_const
 #pragma unroll
                 for (int i = 0; i < 128; ++i) r[i] = i < nvalid ? r[i] : 0xff800000u;
             }
-            if (n < q_end) {
-                float4* dst = reinterpret_cast<float4*>(srow + (size_t)kt.blk * 128);
+            // the staging of the previous key tile has been read by its stores
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    dst[c] = make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
-                                         __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
+            for (int c = 0; c < 4; ++c) {
+                uint8_t* rowp = stage_p + c * 4096 + lane * 128;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<float4*>(rowp + ((k ^ sw) << 4)) =
+                        make_float4(__uint_as_float(r[32 * c + 4 * k]), __uint_as_float(r[32 * c + 4 * k + 1]),
+                                    __uint_as_float(r[32 * c + 4 * k + 2]), __uint_as_float(r[32 * c + 4 * k + 3]));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tma_store_3d(&a.map_s[seg], stage + c * 4096, kt.blk * 128 + 32 * c, srow, (int)bh);
+                bulk_commit_group();
             }
         }
+        if (lane == 0) bulk_wait_read_all();  // the staging must outlive the stores' reads
+        __syncwarp();
         if (!ok) fail(&abort_flag);
     }
 
@@ -538,6 +563,8 @@ cudaError_t launch_qk_gemm(const Geom& g, const ValidLen& vl, const uint16_t* qh
     a.vl = vl;
     a.scores = scores;
     a.ncols = 128 * (g.ntq_txt + g.ntq_img);
+    for (int seg = 0; seg < 2; ++seg)
+        if (!tmap::scores_f32_segment(&a.map_s[seg], scores, g, a.ncols, seg)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(qk_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkSmemBytes);
     if (e != cudaSuccess) return e;
     const dim3 grid(g.ntq_txt + g.ntq_img, g.H, g.B);

@@ -100,5 +100,21 @@ inline bool bhsd_f32_segment(CUtensorMap* m, const float* base, const Geom& g, i
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p, dims, strides, box);
 }
 
+// fp32 scores [B*H, S, ncols] per segment (0 text, 1 image rows) as 3-D
+// (col, row in the segment, b*H + h), box 32 x 32 x 1: a box reaching past
+// the segment is clipped there.
+inline bool scores_f32_segment(CUtensorMap* m, const float* base, const Geom& g, int ncols, int seg) {
+    const int rows = seg == 0 ? g.T_txt : g.T_img;
+    if (rows == 0) {
+        memset(m, 0, sizeof(*m));
+        return true;
+    }
+    const float* p = base + (seg == 0 ? 0 : (size_t)g.T_txt * ncols);
+    const cuuint64_t dims[3] = {(cuuint64_t)ncols, (cuuint64_t)rows, (cuuint64_t)g.B * g.H};
+    const cuuint64_t strides[2] = {(cuuint64_t)ncols * 4, (cuuint64_t)g.S * ncols * 4};
+    const cuuint32_t box[3] = {32, 32, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p, dims, strides, box);
+}
+
 }  // namespace tmap
 }  // namespace rlk
