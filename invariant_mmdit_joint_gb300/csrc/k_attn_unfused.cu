@@ -283,47 +283,108 @@ __global__ void __launch_bounds__(kThreads, 1) qk_gemm_kernel(const __grid_const
 }
 
 // ====================================================================== softmax
-// One thread per query row (128 per CTA = one query tile); the row's scores
-// of one key tile are read with 16-byte loads into registers, exactly the
-// values the fused kernel reads from TMEM, and go through the fused kernel's
-// steps: mask, row max, lazy reference max, exp2f numerators, partial sums.
+// One warp per 32 query rows (a CTA of one warp; four per query tile), one
+// row per lane, the key tiles in the fused order. Lane 0 loads the warp's
+// 32 x 128 fp32 scores of the next key tile by TMA into the other of two
+// shared-memory slots (four 32 x 32 boxes, 128-byte swizzled) while the
+// lanes work on the current one; each lane reads its row back from the slot,
+// exactly the values the fused kernel reads from TMEM, and goes through the
+// fused kernel's steps: mask, row max, lazy reference max, exp2f numerators,
+// partial sums. P is staged as two 64 x 32 bf16 boxes and stored by TMA
+// through per-segment maps, which clip rows past the query's segment.
 struct SmArgs {
+    CUtensorMap map_sc;    // scores [B*H*S, ncols] fp32, box 32 x 32
+    CUtensorMap map_p[2];  // P per segment (text, image rows) [B*H, rows, ncols] bf16, box 64 x 32 x 1
     Geom g;
     ValidLen vl;
-    const float* scores;  // [B, H, S, ncols]
-    uint32_t* p;          // bf16 pairs [B, H, S, ncols / 2]
-    float* alpha;         // [B, H, S, nblk]
-    float* l;             // [B, H, S]
-    float* lse;           // [B, H, S] or null
+    float* alpha;          // [B, H, S, nblk]
+    float* l;              // [B, H, S]
+    float* lse;            // [B, H, S] or null
     int ncols, nblk;
 };
 
-__global__ void __launch_bounds__(128) softmax_kernel(const __grid_constant__ SmArgs a) {
+constexpr int kSmSlotBytes = 4 * 4096;                          // 32 rows x 128 fp32
+constexpr int kSmStageBytes = 2 * 4096;                         // 32 rows x 128 bf16
+constexpr int kSmSmemBytes = 2 * kSmSlotBytes + kSmStageBytes + 1024;
+
+__global__ void __launch_bounds__(32) softmax_kernel(const __grid_constant__ SmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[2];  // score slot s loaded
+    __shared__ volatile int abort_flag;
+
     const Geom& g = a.g;
-    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int wq = (int)blockIdx.x & 3, qt = (int)blockIdx.x >> 2, h = blockIdx.y, b = blockIdx.z;
+    const int lane = threadIdx.x;
     int q0, q_end;
     query_tile(g, qt, q0, q_end);
-    const int n = q0 + (int)threadIdx.x;
-    if (n >= q_end) return;
+    const int r0 = q0 + 32 * wq;  // the warp's first row
+    if (r0 >= q_end) return;      // the whole warp lies past the segment
+    const int n = r0 + lane;
+    const bool row_ok = n < q_end;
     const int L = a.vl.L[b];
     const int nkt = n_key_tiles(g, L);
-    const size_t rowi = ((size_t)b * g.H + h) * g.S + n;
-    const float* srow = a.scores + rowi * a.ncols;
-    uint32_t* prow = a.p + rowi * (a.ncols / 2);
-    float* arow = a.alpha + rowi * a.nblk;
+    const size_t bh = (size_t)b * g.H + h;
+    const size_t rowi = bh * g.S + n;
+    const int seg = qt < g.ntq_txt ? 0 : 1;
+    const int srow = seg ? r0 - g.T_txt : r0;  // the warp's first row in its segment
+
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    auto slot = [&](int s) { return sbase + s * kSmSlotBytes; };
+    const uint32_t stage = sbase + 2 * kSmSlotBytes;
+    const uint8_t* base_p = smem_raw + (sbase - smem_u32(smem_raw));
+    uint8_t* stage_p = smem_raw + (stage - smem_u32(smem_raw));
+    const uint32_t bar = smem_u32(&bars[0]);
+    const int sw = lane & 7;
+    if (lane == 0) {
+        abort_flag = 0;
+        mbar_init(bar, 1);
+        mbar_init(bar + 8, 1);
+        fence_barrier_init();
+        prefetch_tensormap(&a.map_sc);
+        prefetch_tensormap(&a.map_p[seg]);
+    }
+    __syncwarp();
+    auto issue = [&](int j) {  // lane 0: key tile j's scores into slot j & 1
+        const KeyTile kt = key_tile(g, L, j);
+        const uint32_t bs = bar + 8 * (j & 1);
+        mbar_expect_tx(bs, kSmSlotBytes);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            tma_load_2d(slot(j & 1) + c * 4096, &a.map_sc, bs, kt.blk * 128 + 32 * c, (int)(bh * g.S) + r0);
+    };
+    int issued = 0;  // key tiles whose loads lane 0 has issued
+    if (lane == 0) {
+        issue(0);
+        issued = 1;
+    }
     float m = -INFINITY, l = 0.0f;
+    bool ok = true;
     for (int j = 0; j < nkt; ++j) {
+        const int s = j & 1;
+        // the other slot was read out by every lane in the previous tile
+        __syncwarp();
+        if (lane == 0 && j + 1 < nkt) {
+            issue(j + 1);
+            issued = j + 2;
+        }
+        if (!warp_wait(bar + 8 * s, (j >> 1) & 1, &abort_flag)) {
+            ok = false;
+            break;
+        }
         const KeyTile kt = key_tile(g, L, j);
         const int nvalid = kt.kend - kt.k0;
         uint32_t r[128];
-        const uint4* src = reinterpret_cast<const uint4*>(srow + (size_t)kt.blk * 128);
+        const uint8_t* rowp = base_p + s * kSmSlotBytes + lane * 128;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            const uint4 v = src[c];
-            r[4 * c] = v.x;
-            r[4 * c + 1] = v.y;
-            r[4 * c + 2] = v.z;
-            r[4 * c + 3] = v.w;
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint4 v = *reinterpret_cast<const uint4*>(rowp + c * 4096 + ((k ^ sw) << 4));
+                r[32 * c + 4 * k] = v.x;
+                r[32 * c + 4 * k + 1] = v.y;
+                r[32 * c + 4 * k + 2] = v.z;
+                r[32 * c + 4 * k + 3] = v.w;
+            }
         }
         if (nvalid < 128) {
 #pragma unroll
@@ -352,13 +413,40 @@ __global__ void __launch_bounds__(128) softmax_kernel(const __grid_constant__ Sm
         const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
         l = fmaf(l, alpha, rs);
         m = m_new;
-        uint4* dst = reinterpret_cast<uint4*>(prow + (size_t)kt.blk * 64);
+        // P: the previous tile's stores have read the staging
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
 #pragma unroll
-        for (int c = 0; c < 16; ++c) dst[c] = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
-        arow[kt.blk] = alpha;
+        for (int c = 0; c < 2; ++c) {
+            uint8_t* prow = stage_p + c * 4096 + lane * 128;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<uint4*>(prow + ((k ^ sw) << 4)) =
+                    make_uint4(r[32 * c + 4 * k], r[32 * c + 4 * k + 1], r[32 * c + 4 * k + 2], r[32 * c + 4 * k + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) tma_store_3d(&a.map_p[seg], stage + c * 4096, kt.blk * 128 + 64 * c, srow, (int)bh);
+            bulk_commit_group();
+        }
+        if (row_ok) a.alpha[rowi * a.nblk + kt.blk] = alpha;
     }
-    a.l[rowi] = l;
-    if (a.lse != nullptr) a.lse[rowi] = (m + log2f(l)) * kLn2;
+    if (!ok) {
+        if (lane == 0) fail(&abort_flag);
+    } else if (row_ok) {
+        a.l[rowi] = l;
+        if (a.lse != nullptr) a.lse[rowi] = (m + log2f(l)) * kLn2;
+    }
+    // the slots' loads in flight and the staging's stores finish before exit
+    if (lane == 0) {
+        const volatile int no_abort = 0;
+        for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
+            mbar_wait(bar + 8 * (j & 1), (j >> 1) & 1, &no_abort, kWaitLimitNs);
+        bulk_wait_read_all();
+    }
+    __syncwarp();
 }
 
 // ====================================================================== av_gemm
@@ -579,16 +667,19 @@ cudaError_t launch_softmax(const Geom& g, const ValidLen& vl, const float* score
     SmArgs a;
     a.g = g;
     a.vl = vl;
-    a.scores = scores;
-    a.p = reinterpret_cast<uint32_t*>(p);
     a.alpha = alpha;
     a.l = l;
     a.lse = lse;
     a.nblk = g.ntq_txt + g.ntq_img;
     a.ncols = 128 * a.nblk;
-    const dim3 grid(a.nblk, g.H, g.B);
+    if (!tmap::mat_f32(&a.map_sc, scores, (long long)g.B * g.H * g.S, a.ncols, 32, 32)) return cudaErrorInvalidValue;
+    for (int seg = 0; seg < 2; ++seg)
+        if (!tmap::p_bf16_segment(&a.map_p[seg], p, g, a.ncols, seg)) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(softmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmSmemBytes);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(4 * a.nblk, g.H, g.B);
     timing_begin(kKSoftmax, s);
-    softmax_kernel<<<grid, 128, 0, s>>>(a);
+    softmax_kernel<<<grid, 32, kSmSmemBytes, s>>>(a);
     timing_end(kKSoftmax, s);
     return cudaGetLastError();
 }

@@ -116,5 +116,27 @@ inline bool scores_f32_segment(CUtensorMap* m, const float* base, const Geom& g,
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p, dims, strides, box);
 }
 
+// fp32 row-major [rows, cols] (cols a multiple of 32), box box_cols x box_rows
+inline bool mat_f32(CUtensorMap* m, const float* base, long long rows, int cols, int box_cols, int box_rows) {
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box);
+}
+
+// bf16 P [B*H, S, ncols] per segment (as scores_f32_segment), box 64 x 32 x 1
+inline bool p_bf16_segment(CUtensorMap* m, const void* base, const Geom& g, int ncols, int seg) {
+    const int rows = seg == 0 ? g.T_txt : g.T_img;
+    if (rows == 0) {
+        memset(m, 0, sizeof(*m));
+        return true;
+    }
+    const uint16_t* p = static_cast<const uint16_t*>(base) + (seg == 0 ? 0 : (size_t)g.T_txt * ncols);
+    const cuuint64_t dims[3] = {(cuuint64_t)ncols, (cuuint64_t)rows, (cuuint64_t)g.B * g.H};
+    const cuuint64_t strides[2] = {(cuuint64_t)ncols * 2, (cuuint64_t)g.S * ncols * 2};
+    const cuuint32_t box[3] = {64, 32, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p, dims, strides, box);
+}
+
 }  // namespace tmap
 }  // namespace rlk
