@@ -450,32 +450,31 @@ __global__ void __launch_bounds__(32) softmax_kernel(const __grid_constant__ SmA
 }
 
 // ====================================================================== av_gemm
-// One CTA = one query tile. TMEM: O [0, 128), P [128, 192) (64 columns of
-// bf16 pairs: pair i of a row in column 128 + i, the fused kernel's packed
-// layout, so k-step kk reads columns 128 + 8 kk .. 128 + 8 kk + 7).
-// Per key tile j of the fused order the row threads load their P row block
-// and alpha, wait for the previous product, rescale O by alpha (only in
-// warps where a row's alpha differs from 1, as the fused kernel does; the
-// other rows scale by exactly 1), store P into TMEM and signal the MMA
-// thread, which issues O += P V.
+// One CTA = one query tile. TMEM: O [0, 128). Per key tile j of the fused
+// order the copy warp loads V_j and the tile's P block (128 rows x 128 bf16,
+// two 128-byte-swizzled boxes) by TMA into a stage of a three-stage ring;
+// the row threads load alpha, wait for the previous product, rescale O by
+// alpha (only in warps where a row's alpha differs from 1, as the fused
+// kernel does; the other rows scale by exactly 1) and signal the MMA thread,
+// which issues O += P V with P as the K-major A operand from shared memory.
 struct AvArgs {
     CUtensorMap map_v[2];  // v per segment (0 text, 1 image) as 4-D (d, h, token, b)
+    CUtensorMap map_p;     // P bf16 [B*H*S, ncols], box 64 x 128
     Geom g;
     ValidLen vl;
-    const uint32_t* p;     // bf16 pairs [B, H, S, ncols / 2]
     const float* alpha;    // [B, H, S, nblk]
     const float* l;        // [B, H, S]
     SegBf16 out;           // [B, S, H, 128] (text rows, image rows)
     int ncols, nblk;
 };
 
-// two V slots; sized like qk_gemm so that at most two CTAs (2 x 256 TMEM
-// columns) share an SM
-constexpr int kAvSmemBytes = 3 * kTileBytes + 1024;
+constexpr int kAvStages = 3;
+constexpr int kAvStageBytes = 2 * kTileBytes;  // V tile, P block
+constexpr int kAvSmemBytes = kAvStages * kAvStageBytes + 1024;
 
 __global__ void __launch_bounds__(kThreads, 1) av_gemm_kernel(const __grid_constant__ AvArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[8];
+    __shared__ __align__(8) uint64_t bars[2 * kAvStages + 3];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
@@ -489,18 +488,19 @@ __global__ void __launch_bounds__(kThreads, 1) av_gemm_kernel(const __grid_const
     const size_t bh = (size_t)b * g.H + h;
 
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t sV = sbase;
-    const uint32_t bar_vf = smem_u32(&bars[0]);  // [2] V slot loaded
-    const uint32_t bar_ve = smem_u32(&bars[2]);  // [2] V slot free
-    const uint32_t bar_p = smem_u32(&bars[4]);   // P stored and O rescaled (128 row threads)
-    const uint32_t bar_o = smem_u32(&bars[5]);   // product of tile j done (O updated, P read)
-    const uint32_t bar_drain = smem_u32(&bars[6]);
+    auto stage_v = [&](int s) { return sbase + s * kAvStageBytes; };
+    auto stage_p = [&](int s) { return sbase + s * kAvStageBytes + kTileBytes; };
+    const uint32_t bar_full = smem_u32(&bars[0]);           // [kAvStages] V and P loaded
+    const uint32_t bar_empty = smem_u32(&bars[kAvStages]);  // [kAvStages] stage's product done
+    const uint32_t bar_p = smem_u32(&bars[2 * kAvStages]);      // O rescaled (128 row threads)
+    const uint32_t bar_o = smem_u32(&bars[2 * kAvStages + 1]);  // product of tile j done (O updated)
+    const uint32_t bar_drain = smem_u32(&bars[2 * kAvStages + 2]);
 
     if (tid == 0) {
         abort_flag = 0;
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar_vf + 8 * s, 1);
-            mbar_init(bar_ve + 8 * s, 1);
+        for (int s = 0; s < kAvStages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
         }
         mbar_init(bar_p, 128);
         mbar_init(bar_o, 1);
@@ -520,41 +520,48 @@ __global__ void __launch_bounds__(kThreads, 1) av_gemm_kernel(const __grid_const
         if (lane == 0) {
             prefetch_tensormap(&a.map_v[0]);
             prefetch_tensormap(&a.map_v[1]);
+            prefetch_tensormap(&a.map_p);
+            const int prow = (int)(bh * g.S) + q0;  // the tile's first row of P
             int issued = 0;
             for (int j = 0; j < nkt && !abort_flag; ++j) {
-                const int s = j & 1;
-                if (j >= 2 && !mbar_wait(bar_ve + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                const int s = j % kAvStages;
+                if (j >= kAvStages &&
+                    !mbar_wait(bar_empty + 8 * s, ((j / kAvStages) + 1) & 1, &abort_flag, kWaitLimitNs)) {
                     fail(&abort_flag);
                     break;
                 }
                 const KeyTile kt = key_tile(g, L, j);
-                mbar_expect_tx(bar_vf + 8 * s, kTileBytes);
+                const uint32_t bf = bar_full + 8 * s;
+                mbar_expect_tx(bf, kAvStageBytes);
                 const int vseg = kt.k0 < g.T_txt ? 0 : 1, vrow = vseg ? kt.k0 - g.T_txt : kt.k0;
-                tma_load_4d(sV + s * kTileBytes, &a.map_v[vseg], bar_vf + 8 * s, 0, h, vrow, b);
-                tma_load_4d(sV + s * kTileBytes + kBoxBytes, &a.map_v[vseg], bar_vf + 8 * s, 64, h, vrow, b);
+                tma_load_4d(stage_v(s), &a.map_v[vseg], bf, 0, h, vrow, b);
+                tma_load_4d(stage_v(s) + kBoxBytes, &a.map_v[vseg], bf, 64, h, vrow, b);
+                tma_load_2d(stage_p(s), &a.map_p, bf, kt.blk * 128, prow);
+                tma_load_2d(stage_p(s) + kBoxBytes, &a.map_p, bf, kt.blk * 128 + 64, prow);
                 issued = j + 1;
             }
             const volatile int no_abort = 0;
-            for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
-                mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1, &no_abort, kWaitLimitNs);
+            for (int j = issued - kAvStages < 0 ? 0 : issued - kAvStages; j < issued; ++j)
+                mbar_wait(bar_full + 8 * (j % kAvStages), (j / kAvStages) & 1, &no_abort, kWaitLimitNs);
         }
     } else if (warp == kWarpMma) {
         if (lane == 0) {
             bool ok = true;
             for (int j = 0; ok && j < nkt; ++j) {
-                const int s = j & 1;
+                const int s = j % kAvStages;
                 ok = mbar_wait(bar_p, j & 1, &abort_flag, kWaitLimitNs) &&
-                     mbar_wait(bar_vf + 8 * s, (j >> 1) & 1, &abort_flag, kWaitLimitNs);
+                     mbar_wait(bar_full + 8 * s, (j / kAvStages) & 1, &abort_flag, kWaitLimitNs);
                 if (!ok) break;
                 tc_fence_after();
-                // the fused forward's PV product: A = P from TMEM, B = V MN-major
-                const uint32_t dv = sV + s * kTileBytes;
+                // the fused forward's PV product: A = P (K-major, here from
+                // shared memory), B = V MN-major, k-steps in the same order
+                const uint32_t dv = stage_v(s), dp = stage_p(s);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem, tmem + 128 + kk * 8, sdesc_sw128(dv + kk * 2048, kBoxBytes, 1024), kIdescO,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_ss(tmem, sdesc_sw128(dp + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                           sdesc_sw128(dv + kk * 2048, kBoxBytes, 1024), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar_o);
-                mma_commit(bar_ve + 8 * s);
+                mma_commit(bar_empty + 8 * s);
             }
             if (!ok) fail(&abort_flag);
             mma_commit(bar_drain);
@@ -567,22 +574,12 @@ __global__ void __launch_bounds__(kThreads, 1) av_gemm_kernel(const __grid_const
         const int n = q0 + row;
         const bool in_seg = n < q_end;
         const size_t rowi = bh * g.S + (in_seg ? n : q0);
-        const uint4* prow = reinterpret_cast<const uint4*>(a.p + rowi * (a.ncols / 2));
         bool ok = true;
         for (int j = 0; j < nkt; ++j) {
             const KeyTile kt = key_tile(g, L, j);
-            uint32_t pr[64];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint4 v = in_seg ? prow[kt.blk * 16 + c] : make_uint4(0u, 0u, 0u, 0u);
-                pr[4 * c] = v.x;
-                pr[4 * c + 1] = v.y;
-                pr[4 * c + 2] = v.z;
-                pr[4 * c + 3] = v.w;
-            }
             const float alpha = in_seg ? a.alpha[rowi * a.nblk + kt.blk] : 1.0f;
             if (j > 0) {
-                // the product of tile j - 1 has finished writing O and reading P
+                // the product of tile j - 1 has finished writing O
                 if (!warp_wait(bar_o, (j - 1) & 1, &abort_flag)) {
                     ok = false;
                     break;
@@ -598,11 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1) av_gemm_kernel(const __grid_const
                         for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
                         tmem_st32(tmem + lane_addr + 32 * c, o32);
                     }
+                    tmem_st_wait();
                 }
             }
-            tmem_st32(tmem + lane_addr + 128, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
-            tmem_st32(tmem + lane_addr + 160, *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
-            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_p);
         }
@@ -690,12 +685,12 @@ cudaError_t launch_av_gemm(const Geom& g, const ValidLen& vl, const uint16_t* p,
     if (!tmap::seg_bf16(&a.map_v[0], v, g, 0) || !tmap::seg_bf16(&a.map_v[1], v, g, 1)) return cudaErrorInvalidValue;
     a.g = g;
     a.vl = vl;
-    a.p = reinterpret_cast<const uint32_t*>(p);
     a.alpha = alpha;
     a.l = l;
     a.out = out;
     a.nblk = g.ntq_txt + g.ntq_img;
     a.ncols = 128 * a.nblk;
+    if (!tmap::mat_bf16(&a.map_p, p, (long long)g.B * g.H * g.S, a.ncols, 128)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(av_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAvSmemBytes);
     if (e != cudaSuccess) return e;
     const dim3 grid(a.nblk, g.H, g.B);
