@@ -14,11 +14,15 @@
 
 #include "rlk_device.cuh"
 #include "rlk_internal.h"
+#include "rlk_sm100.cuh"
+#include "rlk_tmap.h"
 
 RLK_DEFINE_STRICT_PROBE(probe_prologue_tu)
 
 namespace rlk {
 namespace {
+
+using namespace sm100;
 
 constexpr int kRowThreads = 16;  // a half warp covers one 128-wide row, 8 dims per lane
 
@@ -171,61 +175,93 @@ __global__ void __launch_bounds__(256, 4) prologue_kernel(
 // ---------------------------------------------------------------- Delta, lse2
 // Backward preprocess in the tile-padded layout: slot r of (b, h) belongs to
 // query tile r / 128 (text tiles first, then image tiles) at offset r % 128.
-// A slot holding a token gets Delta = sum_d dO * O (each lane adds its 8
-// products in order, then a butterfly over the half warp) and
-// lse2 = lse * log2(e); a slot past its segment gets Delta = 0 and
-// lse2 = +inf, so the backward kernels see P = 0 there. One half warp per
-// slot, slots in order (enumerating them in the inputs' memory order instead
-// measured 35 us against 30).
-__global__ void __launch_bounds__(256) bwd_pre_kernel(Geom g, const SegBf16 o, const SegBf16 dout,
-                                                      const float* __restrict__ lse, float* __restrict__ lse2_p,
-                                                      float* __restrict__ delta_p) {
-    // 32-bit slots (the host caps B * H * nq_pad below 2^31); the CTA's first
-    // slot is divided out once and each half warp's follows by carrying
-    const int slots = g.B * g.H * g.nq_pad;
-    const int base = (int)blockIdx.x * (int)(blockDim.x / kRowThreads);
-    const int w = (int)(threadIdx.x / kRowThreads);
-    const int lane16 = threadIdx.x % kRowThreads;
-    const bool active = base + w < slots;
-    const int bh0 = base / g.nq_pad;
-    int r = base - bh0 * g.nq_pad + w, b = bh0 / g.H, h = bh0 - (bh0 / g.H) * g.H;
-    if (r >= g.nq_pad) {  // at most one carry: 16 slots per CTA, nq_pad >= 128
-        r -= g.nq_pad;
-        if (++h == g.H) {
-            h = 0;
-            ++b;
+// A slot holding a token gets Delta = sum_d dO * O and lse2 = lse * log2(e);
+// a slot past its segment gets Delta = 0 and lse2 = +inf, so the backward
+// kernels see P = 0 there. One warp (a CTA) per 32 consecutive slots of one
+// (b, h), a slot per lane: the warp's 32 tokens of o and dout arrive by TMA
+// as 128-byte-swizzled boxes of 64 dims x 32 tokens (tokens past the segment
+// read zeros), and each lane sums its row in the order of a half warp
+// holding 8 dims per lane: 16 partials of 8 products each in order, then the
+// butterfly tree xor 8, 4, 2, 1.
+__device__ int g_status_pro;
+constexpr uint64_t kProWaitLimitNs = 2000000000ull;
+
+struct PreArgs {
+    CUtensorMap map_o[2];   // o per segment (text, image rows), box 64 x 1 x 32 x 1
+    CUtensorMap map_do[2];  // dout likewise
+    Geom g;
+    const float* lse;
+    float* lse2_p;
+    float* delta_p;
+};
+constexpr int kPreSmemBytes = 4 * 4096 + 1024;  // o, dout: two boxes each
+
+__global__ void __launch_bounds__(32) bwd_pre_kernel(const __grid_constant__ PreArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_s;
+    __shared__ volatile int abort_flag;
+    const Geom& g = a.g;
+    const int lane = threadIdx.x;
+    const int bh = (int)blockIdx.x, r0 = 32 * (int)blockIdx.y;
+    const int b = bh / g.H, h = bh - b * g.H;
+    const int t = r0 >> 7;
+    const int seg = t < g.ntq_txt ? 0 : 1;
+    const int n_seg0 = seg ? 128 * (t - g.ntq_txt) + (r0 & 127) : r0;  // first token, counted in its segment
+    const int seg_len = seg ? g.T_img : g.T_txt;
+    const size_t slot = (size_t)bh * g.nq_pad + r0 + lane;
+    const bool valid = n_seg0 + lane < seg_len;
+    const int n = (seg ? g.T_txt : 0) + n_seg0 + lane;
+    if (n_seg0 >= seg_len) {  // all 32 slots lie past the segment
+        a.delta_p[slot] = 0.0f;
+        a.lse2_p[slot] = INFINITY;
+        return;
+    }
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint8_t* sp = smem_raw + (sbase - smem_u32(smem_raw));
+    const uint32_t bar = smem_u32(&bar_s);
+    if (lane == 0) {
+        abort_flag = 0;
+        mbar_init(bar, 1);
+        fence_barrier_init();
+        mbar_expect_tx(bar, 4 * 4096);
+        tma_load_4d(sbase, &a.map_o[seg], bar, 0, h, n_seg0, b);
+        tma_load_4d(sbase + 4096, &a.map_o[seg], bar, 64, h, n_seg0, b);
+        tma_load_4d(sbase + 8192, &a.map_do[seg], bar, 0, h, n_seg0, b);
+        tma_load_4d(sbase + 12288, &a.map_do[seg], bar, 64, h, n_seg0, b);
+    }
+    const float lse_n = valid ? __ldg(a.lse + (size_t)bh * g.S + n) : 0.0f;
+    __syncwarp();
+    if (!__all_sync(0xffffffffu, mbar_wait(bar, 0, &abort_flag, kProWaitLimitNs))) {
+        if (lane == 0) atomicOr(&g_status_pro, 1);
+        return;
+    }
+    const int sw = lane & 7;
+    float s16[16];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // dims 64 c + 8 k .. + 7: one half-warp lane's share
+            const uint4 ov = *reinterpret_cast<const uint4*>(sp + c * 4096 + lane * 128 + ((k ^ sw) << 4));
+            const uint4 dv = *reinterpret_cast<const uint4*>(sp + 8192 + c * 4096 + lane * 128 + ((k ^ sw) << 4));
+            const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+            const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+            float acc = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc = fmaf(bf16_lo(dw[i]), bf16_lo(ow[i]), acc);
+                acc = fmaf(bf16_hi(dw[i]), bf16_hi(ow[i]), acc);
+            }
+            s16[8 * c + k] = acc;
         }
     }
-    if (!active) {  // the last slot: loads stay in bounds, nothing is stored
-        r = g.nq_pad - 1;
-        h = g.H - 1;
-        b = g.B - 1;
-    }
-    const size_t bh = (size_t)b * g.H + h;
-    const size_t slot = bh * g.nq_pad + r;
-    const int t = r >> 7, off = r & 127;
-    const int n = t < g.ntq_txt ? 128 * t + off : g.T_txt + 128 * (t - g.ntq_txt) + off;
-    const bool valid = t < g.ntq_txt ? n < g.T_txt : n < g.S;
-    float acc = 0.0f;
-    // lse is loaded with the rows, not after the reduction
-    const float lse_n = valid && lane16 == 0 ? __ldg(lse + bh * g.S + n) : 0.0f;
-    if (valid) {
-        const uint4 ov = __ldg(reinterpret_cast<const uint4*>(seg_row(o, g, b, n, h) + 8 * lane16));
-        const uint4 dv = __ldg(reinterpret_cast<const uint4*>(seg_row(dout, g, b, n, h) + 8 * lane16));
-        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
-        const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+    float t8[8], t4[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            acc = fmaf(bf16_lo(dw[i]), bf16_lo(ow[i]), acc);
-            acc = fmaf(bf16_hi(dw[i]), bf16_hi(ow[i]), acc);
-        }
-    }
+    for (int i = 0; i < 8; ++i) t8[i] = s16[i] + s16[i + 8];
 #pragma unroll
-    for (int m = 8; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-    if (active && lane16 == 0) {
-        delta_p[slot] = acc;
-        lse2_p[slot] = valid ? lse_n * 1.4426950408889634f : INFINITY;
-    }
+    for (int i = 0; i < 4; ++i) t4[i] = t8[i] + t8[i + 4];
+    const float delta = (t4[0] + t4[2]) + (t4[1] + t4[3]);
+    a.delta_p[slot] = valid ? delta : 0.0f;
+    a.lse2_p[slot] = valid ? lse_n * 1.4426950408889634f : INFINITY;
 }
 
 // ---------------------------------------------------------------- key-side norm/rope backward
@@ -406,9 +442,17 @@ cudaError_t launch_prologue(const Geom& g, const SegBf16& q, const SegBf16& k,
 
 cudaError_t launch_bwd_pre(const Geom& g, const SegBf16& out, const SegBf16& dout, const float* lse,
                            float* lse2_p, float* delta_p, cudaStream_t s) {
-    const long long slots = (long long)g.B * g.H * g.nq_pad;  // < 2^31 (shape limit)
+    PreArgs a;
+    for (int seg = 0; seg < 2; ++seg)
+        if (!tmap::seg_bf16(&a.map_o[seg], out, g, seg, 32) || !tmap::seg_bf16(&a.map_do[seg], dout, g, seg, 32))
+            return cudaErrorInvalidValue;
+    a.g = g;
+    a.lse = lse;
+    a.lse2_p = lse2_p;
+    a.delta_p = delta_p;
+    const dim3 grid((unsigned)(g.B * g.H), (unsigned)(g.nq_pad / 32));
     timing_begin(kKBwdPre, s);
-    bwd_pre_kernel<<<(unsigned)((slots + 15) / 16), 256, 0, s>>>(g, out, dout, lse, lse2_p, delta_p);
+    bwd_pre_kernel<<<grid, 32, kPreSmemBytes, s>>>(a);
     timing_end(kKBwdPre, s);
     return cudaGetLastError();
 }
@@ -431,6 +475,16 @@ cudaError_t launch_dg_fold(const Geom& g, const float* dgt, float* dg_partial, f
     dg_fold_total_kernel<<<1, 4 * kHeadDim, 0, s>>>(g, dg_partial, dg);
     timing_end(kKDgFold, s);
     return cudaGetLastError();
+}
+
+int read_and_clear_status_prologue(cudaStream_t s) {
+    int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_status_pro, sizeof(int), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return -1;
+    if (cudaMemcpyToSymbolAsync(g_status_pro, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return -1;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return -1;
+    return v;
 }
 
 }  // namespace rlk

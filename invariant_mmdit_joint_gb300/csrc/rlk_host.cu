@@ -871,8 +871,9 @@ rlk_status rlk_joint_attn_check_status(void* stream) {
     const int b = read_and_clear_status_bwd(s);
     const int c = read_and_clear_status_unfused(s);
     const int d = read_and_clear_status_qkv(s);
-    if (a < 0 || b < 0 || c < 0 || d < 0) return RLK_ERR_CUDA;
-    if (a != 0 || b != 0 || c != 0 || d != 0) return RLK_ERR_DEVICE_TIMEOUT;
+    const int e = read_and_clear_status_prologue(s);
+    if (a < 0 || b < 0 || c < 0 || d < 0 || e < 0) return RLK_ERR_CUDA;
+    if (a != 0 || b != 0 || c != 0 || d != 0 || e != 0) return RLK_ERR_DEVICE_TIMEOUT;
     return RLK_OK;
 }
 
@@ -884,7 +885,7 @@ rlk_status rlk_joint_attn_trace(rlk_ja_trace* out) {
     std::snprintf(out->backend, sizeof(out->backend), "sm_103a tcgen05");
     std::snprintf(out->reduction_order, sizeof(out->reduction_order),
                   "tiles of 128: text from 0 then image from T_txt, ascending; dkdv: q tiles ascending; "
-                  "rows: lane order + xor butterfly; dg: chunks, h, b ascending");
+                  "rows: lane order + xor butterfly; dg: 32-row quarters, (q0+q1)+(q2+q3), tiles, h, b ascending");
     std::snprintf(out->accumulator, sizeof(out->accumulator), "fp32");
     out->split_k = 0;
     out->atomics = 0;

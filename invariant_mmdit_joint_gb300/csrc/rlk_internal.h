@@ -133,6 +133,7 @@ cudaError_t launch_norm_rope_bwd_k(const Geom& g, const SegBf16& k, const float*
 cudaError_t launch_dg_fold(const Geom& g, const float* dgt, float* dg_partial,
                            float* dg, cudaStream_t s);
 int probe_prologue_tu(void);
+int read_and_clear_status_prologue(cudaStream_t s);
 
 // k_attn_fwd.cu
 cudaError_t launch_attn_fwd(const Geom& g, const ValidLen& vl, const uint16_t* qh,

@@ -71,10 +71,10 @@ inline bool bshd_bf16(CUtensorMap* m, const void* base, const Geom& g, int seg =
 }
 
 // One segment (0 text, 1 image) of a segmented bf16 activation as a 4-D
-// map (d, h, token in the segment, b), box 64 x 1 x 128 x 1: a box reaching
+// map (d, h, token in the segment, b), box 64 x 1 x box_rows x 1: a box reaching
 // past the segment is clipped there (loads read zeros, stores are dropped).
 // A segment with no rows gets a zeroed map that no kernel uses.
-inline bool seg_bf16(CUtensorMap* m, const SegBf16& t, const Geom& g, int seg) {
+inline bool seg_bf16(CUtensorMap* m, const SegBf16& t, const Geom& g, int seg, int box_rows = 128) {
     const int rows = seg == 0 ? g.T_txt : g.T_img;
     if (rows == 0) {
         memset(m, 0, sizeof(*m));
@@ -82,7 +82,7 @@ inline bool seg_bf16(CUtensorMap* m, const SegBf16& t, const Geom& g, int seg) {
     }
     const cuuint64_t dims[4] = {128, (cuuint64_t)g.H, (cuuint64_t)rows, (cuuint64_t)g.B};
     const cuuint64_t strides[3] = {256, (cuuint64_t)g.H * 256, (cuuint64_t)t.bstride[seg] * g.H * 256};
-    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t.p[seg], dims, strides, box);
 }
 
