@@ -504,8 +504,11 @@ constexpr uint32_t kIdescMM = idesc_bf16(128, 128, true, true);
 struct DqUnit {
     int qt, h, b;
 };
+// Units run from the last (sample, head) down: the dK/dV kernel's last CTAs
+// wrote those dS^T images, some still in L2 (317.0 -> 313.6 us measured).
 __device__ __forceinline__ DqUnit dq_unit(const Geom& g, int nq, int u) {
     DqUnit r;
+    u = nq * g.H * g.B - 1 - u;
     r.qt = u % nq;
     r.h = (u / nq) % g.H;
     r.b = u / (nq * g.H);
