@@ -355,6 +355,15 @@ rlk_status rlk_attn_out_bias_gemm(const rlk_ja_shape* shape,
  * RLK_ERR_DEVICE_TIMEOUT, or RLK_ERR_CUDA if the stream reported an error. */
 rlk_status rlk_joint_attn_check_status(void* stream);
 
+/* Self-test of the failure path: enqueues on `stream` one warp that waits,
+ * through the same bounded mbarrier wait the kernels use, on a barrier that
+ * nothing completes. After limit_ms (1 .. 2000) it gives up and records the
+ * failure in the device status word, so the next
+ * rlk_joint_attn_check_status() returns RLK_ERR_DEVICE_TIMEOUT (and clears
+ * it); nothing faults and the context stays usable. RLK_ERR_INVALID_ARG
+ * for a limit out of range. */
+rlk_status rlk_selftest_wait_timeout(int32_t limit_ms, void* stream);
+
 /* Runs, on the current device, a probe kernel compiled in each translation
  * unit with that unit's flags: a subnormal product must survive, and
  * division, square root and expf must keep IEEE / library accuracy. These

@@ -28,7 +28,7 @@ __all__ = [
     "rlk_op_trace_enable", "rlk_op_trace_count", "rlk_op_trace_read", "op_trace", "OP_TRACE_CAP",
     "rlk_joint_attn_state_bytes", "rlk_joint_attn_fwd_shard", "rlk_joint_attn_fwd_streams",
     "rlk_joint_attn_bwd_streams", "rlk_qkv_bias_gemm", "rlk_joint_attn_fwd_ctx",
-    "rlk_attn_out_bias_gemm",
+    "rlk_attn_out_bias_gemm", "rlk_selftest_wait_timeout",
     "EXPORTED_SYMBOLS", "KERNEL_IDS",
 ]
 
@@ -61,7 +61,7 @@ EXPORTED_SYMBOLS = (
     "rlk_op_trace_enable", "rlk_op_trace_count", "rlk_op_trace_read",
     "rlk_joint_attn_state_bytes", "rlk_joint_attn_fwd_shard",
     "rlk_joint_attn_fwd_streams", "rlk_joint_attn_bwd_streams", "rlk_qkv_bias_gemm",
-    "rlk_joint_attn_fwd_ctx", "rlk_attn_out_bias_gemm",
+    "rlk_joint_attn_fwd_ctx", "rlk_attn_out_bias_gemm", "rlk_selftest_wait_timeout",
 )
 OP_TRACE_CAP = 256
 OP_TRACE_MAX_KERNELS = 8
@@ -162,6 +162,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     L.rlk_joint_attn_check_status.restype = i32
     L.rlk_strict_math_compiled.argtypes = []
     L.rlk_strict_math_compiled.restype = i32
+    L.rlk_selftest_wait_timeout.argtypes = [i32, vp]
+    L.rlk_selftest_wait_timeout.restype = i32
     L.rlk_joint_attn_trace.argtypes = [ctypes.POINTER(Trace)]
     L.rlk_joint_attn_trace.restype = i32
     L.rlk_strerror.argtypes = [i32]
@@ -426,6 +428,13 @@ def rlk_joint_attn_check_status(stream=None) -> None:
 
 def rlk_strict_math_compiled() -> int:
     return int(lib().rlk_strict_math_compiled())
+
+
+def rlk_selftest_wait_timeout(limit_ms: int, stream=None) -> None:
+    """Enqueue one warp whose bounded wait on a barrier nothing completes
+    gives up after limit_ms: the next rlk_joint_attn_check_status() raises
+    RlkError(RLK_ERR_DEVICE_TIMEOUT)."""
+    _check(lib().rlk_selftest_wait_timeout(int(limit_ms), _stream_handle(stream)), "rlk_selftest_wait_timeout")
 
 
 def rlk_joint_attn_trace() -> dict:

@@ -413,7 +413,29 @@ unsigned row_blocks(const Geom& g) {
     return (unsigned)((rows + kPrologueRowsPerCta - 1) / kPrologueRowsPerCta);
 }
 
+// The failure path's self-test: one warp waits on an mbarrier that nothing
+// completes; the bounded wait gives up after limit_ns and records the
+// failure like every kernel's wait does.
+__global__ void wait_timeout_probe_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar_s;
+    __shared__ volatile int abort_flag;
+    const uint32_t bar = smem_u32(&bar_s);
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    if (!__all_sync(0xffffffffu, mbar_wait(bar, 0, &abort_flag, limit_ns)) && threadIdx.x == 0)
+        atomicOr(&g_status_pro, 1);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout_probe(int limit_ms, cudaStream_t s) {
+    wait_timeout_probe_kernel<<<1, 32, 0, s>>>((uint64_t)limit_ms * 1000000ull);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_rope_table(const Geom& g, float2* tab, cudaStream_t s) {
     const int n = g.n_pos * kPairs;

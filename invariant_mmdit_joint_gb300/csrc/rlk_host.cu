@@ -879,6 +879,12 @@ rlk_status rlk_joint_attn_check_status(void* stream) {
 
 int rlk_strict_math_compiled(void) { return strict_all_units(); }
 
+rlk_status rlk_selftest_wait_timeout(int32_t limit_ms, void* stream) {
+    if (limit_ms < 1 || limit_ms > 2000) return RLK_ERR_INVALID_ARG;
+    return launch_wait_timeout_probe(limit_ms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? RLK_OK
+                                                                                                  : RLK_ERR_CUDA;
+}
+
 rlk_status rlk_joint_attn_trace(rlk_ja_trace* out) {
     if (out == nullptr) return RLK_ERR_INVALID_ARG;
     std::memset(out, 0, sizeof(*out));

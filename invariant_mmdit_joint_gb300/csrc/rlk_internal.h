@@ -134,6 +134,8 @@ cudaError_t launch_dg_fold(const Geom& g, const float* dgt, float* dg_partial,
                            float* dg, cudaStream_t s);
 int probe_prologue_tu(void);
 int read_and_clear_status_prologue(cudaStream_t s);
+// one warp whose bounded wait on a barrier nothing completes gives up after limit_ms
+cudaError_t launch_wait_timeout_probe(int limit_ms, cudaStream_t s);
 
 // k_attn_fwd.cu
 cudaError_t launch_attn_fwd(const Geom& g, const ValidLen& vl, const uint16_t* qh,
