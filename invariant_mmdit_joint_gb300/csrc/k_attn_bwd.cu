@@ -370,17 +370,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
             tmem_ld_wait();
             float pf[kGroupCols];
             uint32_t pk[kGroupCols / 2];
+            if (kvalid) {  // the row's key is valid for the whole CTA: no per-element select
 #pragma unroll
-            for (int e4 = 0; e4 < kGroupCols / 4; ++e4) {
-                const float4 l4 = l2v[e4];
-                const float lq4[4] = {l4.x, l4.y, l4.z, l4.w};
+                for (int e4 = 0; e4 < kGroupCols / 4; ++e4) {
+                    const float4 l4 = l2v[e4];
+                    const float lq4[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float pv = exp2_num(fmaf(__uint_as_float(rs[4 * e4 + u]), kC, -lq4[u]));
-                    pf[4 * e4 + u] = kvalid ? pv : 0.0f;
+                    for (int u = 0; u < 4; ++u)
+                        pf[4 * e4 + u] = exp2_num(fmaf(__uint_as_float(rs[4 * e4 + u]), kC, -lq4[u]));
+                    pk[2 * e4] = pack_bf16(pf[4 * e4], pf[4 * e4 + 1]);
+                    pk[2 * e4 + 1] = pack_bf16(pf[4 * e4 + 2], pf[4 * e4 + 3]);
                 }
-                pk[2 * e4] = pack_bf16(pf[4 * e4], pf[4 * e4 + 1]);
-                pk[2 * e4 + 1] = pack_bf16(pf[4 * e4 + 2], pf[4 * e4 + 3]);
+            } else {  // a masked key: P = 0
+#pragma unroll
+                for (int e = 0; e < kGroupCols; ++e) pf[e] = 0.0f;
+#pragma unroll
+                for (int e = 0; e < kGroupCols / 2; ++e) pk[e] = 0u;
             }
             tmem_st_packed(tmem + lane_addr + kColST + c0, pk);
             tmem_st_wait();
