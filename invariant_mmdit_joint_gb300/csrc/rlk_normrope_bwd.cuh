@@ -1,14 +1,16 @@
 // Backward of rows multi_axis_rope and qk_rmsnorm for one head row held by
-// one thread, in 32-dim chunks, for the epilogue of the dQ kernel (RFC #386 WS1 rows qk_rmsnorm / multi_axis_rope, "fwd + bwd" in the
-// WS1 Single-GPU Kernel List):
+// one thread, in 32-dim chunks, for the epilogue of the dQ kernel (RFC #386
+// WS1 rows qk_rmsnorm / multi_axis_rope, "fwd + bwd" in the WS1 Single-GPU
+// Kernel List):
 //   u  = R(-angle) dy                       inverse rotation of each pair
 //   xh = x r,  w = u g,  c = (sum_d w_d xh_d) / 128
 //   dx = r (w - xh c)                       one bf16 rounding
 //   gain gradient contribution  u_d xh_d
-// The sum over d uses the fixed tree of the reference layout in which lane l
-// of a warp holds dims 4l .. 4l+3: each lane's four products in order, then
-// the butterfly xor 16, 8, 4, 2, 1 (fp32 addition is commutative, so every
-// lane of that butterfly ends with the value lane_tree() forms).
+// The sum over d uses the fixed tree of norm_rope_bwd_k's layout, in which
+// lane l of a warp holds dims 4l .. 4l+3: each lane's four products in order,
+// then the butterfly xor 16, 8, 4, 2, 1 (fp32 addition is commutative, so
+// every lane of that butterfly ends with the value lane_tree() forms). Query
+// and key rows therefore round identically whichever kernel forms them.
 #pragma once
 
 #include "rlk_device.cuh"
@@ -53,7 +55,7 @@ __device__ __forceinline__ void nrb_chunk(int c, const float (&dy)[32], const fl
     }
 }
 
-// The 8 lane partials of a chunk (lanes 8 c .. 8 c + 7 of the reference
+// The 8 lane partials of a chunk (lanes 8 c .. 8 c + 7 of norm_rope_bwd_k's
 // layout): four products each, in order.
 __device__ __forceinline__ void nrb_partials(const float (&w)[32], const float (&xh)[32], float* s8) {
 #pragma unroll
