@@ -1,0 +1,35 @@
+"""bench.py's reference arm on CPU (the oracle on a bounded sample of the
+tiny workload): its one JSON line carries the keys the benchmark contract
+names, with the e2e and cpu_baseline objects describing this run."""
+
+import io
+import json
+import os
+import sys
+from contextlib import redirect_stdout
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_line_has_the_contract_keys():
+    sys.path.insert(0, ROOT)
+    import bench
+    args = type("A", (), dict(steps=2, warmup=1, workload="tiny"))()
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_reference(args)
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["n_gpus"] == 1
+    assert (d["steps"], d["warmup"]) == (2, 1)
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
+    assert d["config"]["workload"] == "tiny"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    e2e = d["e2e"]
+    assert (e2e["value"], e2e["unit"]) == (d["value"], d["unit"])
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
