@@ -13,6 +13,16 @@ value = credited algorithmic TFLOP/s (valid keys only; backward credited at
 2.5x the forward) of the whole job. Under torchrun each rank runs its own
 replica of the workload (the path has no exchange step) and value sums the
 ranks' work over the slowest rank's time.
+
+Timed regions, each of K steps after W warm-up steps, inputs resident in HBM
+and larger than L2:
+  value, ms_per_step        the API calls as a caller makes them
+  kernels, roofline         the same with a CUDA event pair around every
+                            launch (ms_per_step_instrumented)
+  graph                     the step captured once into a CUDA graph, replayed
+  e2e (e2e_serial)          with each step's inputs copied from pinned host
+                            memory and its results read back, pipelined over
+                            three streams (serial on one stream)
 """
 
 from __future__ import annotations
