@@ -24,6 +24,8 @@
 // its batch position, padding or the SM count. No split-KV, no atomics.
 // Every wait is bounded; a wait that gives up records RLK_ERR_DEVICE_TIMEOUT
 // in the status word and the CTA drains its copies and MMAs and exits.
+#include <algorithm>
+
 #include "rlk_device.cuh"
 #include "rlk_internal.h"
 #include "rlk_sm100.cuh"
@@ -57,6 +59,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ int g_status_fwd;
 
+// Pairs split into single-tile CTAs beyond those of the partial last wave.
+// At the 1024^2 CFG pair (816 pairs on 152 SMs) splitting the last wave's 56
+// pairs gave 450 -> 442 us; 40 more changed nothing, 96 more cost 492 us.
+constexpr int kFwdSplitExtra = 0;
+
 struct FwdArgs {
     CUtensorMap map_q;   // qh [B*H*S, 128] bf16, box 64 x 128
     CUtensorMap map_k;   // kh [B*H*S, 128]
@@ -71,6 +78,10 @@ struct FwdArgs {
     // last, which writes out and lse instead). State per query row: m (log2
     // units) and l fp32 [B, H, S], O fp32 [B, H, S, 128] (not yet divided by l).
     int blk_begin, blk_end;
+    // units of the 1-D grid: the pairs of query tiles, in the order pair,
+    // head, sample; pairs below n_keep run as pairs, each later one as two
+    // CTAs of one tile (filling what would be the last, partly empty wave)
+    int npairs, n_keep;
     const float* st_in_m;
     const float* st_in_l;
     const float* st_in_o;
@@ -111,14 +122,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
     __shared__ volatile int abort_flag;
 
     const Geom& g = a.g;
-    const int pt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int u = blockIdx.x;
+    const int pair = u < a.n_keep ? u : a.n_keep + ((u - a.n_keep) >> 1);
+    const int part = u < a.n_keep ? -1 : ((u - a.n_keep) & 1);  // -1: both tiles, else tile 0 or 1 alone
+    const int pt = pair % a.npairs, h = (pair / a.npairs) % g.H, b = pair / (a.npairs * g.H);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // the CTA's pair of query tiles, inside one segment
+    // the CTA's pair of query tiles (or one of them), inside one segment
     const int np_txt = (g.ntq_txt + 1) / 2;
     const bool q_txt = pt < np_txt;
-    const int first = q_txt ? 2 * pt : 2 * (pt - np_txt);          // tile index inside the segment
+    const int first = (q_txt ? 2 * pt : 2 * (pt - np_txt)) + (part == 1 ? 1 : 0);  // tile index inside the segment
     const int seg_tiles = q_txt ? g.ntq_txt : g.ntq_img;
-    const bool has_b = first + 1 < seg_tiles;
+    if (first >= seg_tiles) return;  // the second tile of a pair that has only one
+    const bool has_b = part < 0 && first + 1 < seg_tiles;
     const int seg0 = q_txt ? 0 : g.T_txt;
     const int q_end = q_txt ? g.T_txt : g.S;
     const int q0[2] = {seg0 + first * kBM, seg0 + (first + 1) * kBM};
@@ -517,10 +532,18 @@ cudaError_t launch_attn_fwd(const Geom& g, const ValidLen& vl, const uint16_t* q
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int npairs = (g.ntq_txt + 1) / 2 + (g.ntq_img + 1) / 2;
-    dim3 grid(npairs, g.H, g.B);
+    local.npairs = (g.ntq_txt + 1) / 2 + (g.ntq_img + 1) / 2;
+    const int total = local.npairs * g.H * g.B;
+    // one CTA per SM: the pairs past the last full wave run as single tiles
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int rem = total % sms;
+    const int split = rem == 0 ? 0 : std::min(total, rem + kFwdSplitExtra);
+    local.n_keep = total - split;
     timing_begin(kKAttnFwd, s);
-    attn_fwd_tc_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(local);
+    attn_fwd_tc_kernel<false><<<(unsigned)(local.n_keep + 2 * split), kThreads, kSmemBytes, s>>>(local);
     timing_end(kKAttnFwd, s);
     return cudaGetLastError();
 }
@@ -555,10 +578,10 @@ cudaError_t launch_attn_fwd_shard(const Geom& g, const ValidLen& vl, const uint1
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int npairs = (g.ntq_txt + 1) / 2 + (g.ntq_img + 1) / 2;
-    dim3 grid(npairs, g.H, g.B);
+    local.npairs = (g.ntq_txt + 1) / 2 + (g.ntq_img + 1) / 2;
+    local.n_keep = local.npairs * g.H * g.B;  // every unit a pair
     timing_begin(kKAttnFwdShard, s);
-    attn_fwd_tc_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(local);
+    attn_fwd_tc_kernel<true><<<(unsigned)local.n_keep, kThreads, kSmemBytes, s>>>(local);
     timing_end(kKAttnFwdShard, s);
     return cudaGetLastError();
 }
