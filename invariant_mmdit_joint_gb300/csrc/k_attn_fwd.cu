@@ -18,6 +18,10 @@
 //              PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) -- while one group runs
 //              its softmax the tensor core works for the other.
 // TMEM: S_A [0,128), O_A [128,256), S_B [256,384), O_B [384,512).
+// A CTA runs tile A alone (group B idle) for a segment's odd last tile, and
+// for the pairs past the grid's last full wave, which run as two single-tile
+// CTAs so that the partial wave spreads over twice the SMs; a tile's bytes
+// never depend on its partner.
 // Query tiles are segment aligned (text from token 0, image from token
 // T_txt); key tiles of 128 are visited in one fixed order (text tiles that
 // hold a valid key, then image tiles), so a row's bytes never depend on B,
