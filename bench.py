@@ -18,11 +18,13 @@ Timed regions, each of K steps after W warm-up steps, inputs resident in HBM
 and larger than L2:
   value, ms_per_step        the API calls as a caller makes them
   kernels, roofline         the same with a CUDA event pair around every
-                            launch (ms_per_step_instrumented)
+                            launch (ms_per_step_instrumented); phases splits
+                            it into forward and backward
   graph                     the step captured once into a CUDA graph, replayed
   e2e (e2e_serial)          with each step's inputs copied from pinned host
                             memory and its results read back, pipelined over
                             three streams (serial on one stream)
+dense_convention restates value with every key counted, masked or not.
 """
 
 from __future__ import annotations
@@ -549,6 +551,21 @@ def run_ours(args):
     bf16_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     bf16_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
 
+    # forward and backward apart (sums of the instrumented per-kernel
+    # averages), and the step under the dense convention that counts every
+    # key, masked or not, as FlashAttention-style reports do
+    fwd_names = ("rope_table", "prologue", "attn_fwd")
+    bwd_names = ("bwd_pre", "bwd_dkdv", "bwd_dq", "norm_rope_bwd_k", "dg_fold")
+    dense_gemm = 2.0 * W.HEAD_DIM * w.S * w.S * w.H * w.B
+    phases = {"source": "instrumented region: CUDA events around each launch"}
+    for ph, names, fl in (("fwd", fwd_names, flops["fwd"]), ("bwd", bwd_names, flops["bwd"])):
+        ms = sum(per_kernel[n]["avg_ms"] for n in names if n in per_kernel)
+        phases[ph] = {"ms": round(ms, 4), "credited_gflop": round(fl / 1e9, 2),
+                      "tflops": round(fl / (ms * 1e-3) / 1e12, 1) if ms > 0 else None}
+    dense = {"fwd_gflop": round(2 * dense_gemm / 1e9, 2), "fwd_bwd_gflop": round(7 * dense_gemm / 1e9, 2),
+             "value": round(job_throughput(7 * dense_gemm, world, ms_step), 2), "unit": "TFLOP/s",
+             "what": "every key counted (masked text keys included), same timed step as value"}
+
     clocks = clk.summary()
     unfused = None
     if not args.no_unfused:
@@ -577,7 +594,8 @@ def run_ours(args):
                    "credited_gflop_per_step": round(flops["fwd_bwd"] / 1e9, 2),
                    "l2": "inputs larger than L2: q,k,v,dO, ctx and workspace total "
                          f"{(4 * w.B * w.S * w.H * 128 * 2) / 1e6:.0f} MB + scratch > 129 MB L2"},
-        "roofline": roofline, "kernels": per_kernel, "unfused_forward": unfused, "qkv_producer": qkv,
+        "roofline": roofline, "kernels": per_kernel, "phases": phases, "dense_convention": dense,
+        "unfused_forward": unfused, "qkv_producer": qkv,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
