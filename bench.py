@@ -638,9 +638,45 @@ def _oracle_sample(w, batch, rows_per_sample, n_samples, seed=0):
     return done_flops, t_total
 
 
+def cpu_model() -> str:
+    """The host CPU's model name as lscpu prints it, else the machine type."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
+def oracle_one_thread(w, timeout_s: float = 180.0):
+    """One full (sample, head) pair of w through the oracle with BLAS held to
+    one thread. It runs in a child process, since a BLAS library fixes its
+    thread count when numpy loads it."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-one-thread", "--workload", w.name]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=timeout_s)
+        res = json.loads(r.stdout.strip().splitlines()[-1])
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"value": None, "error": type(e).__name__}
+    res.update(unit="TFLOP/s", cores=1,
+               sample=f"one full (sample, head) pair of {w.name}, forward+backward, BLAS on one thread")
+    return res
+
+
+def _one_thread_child(w):
+    batch = W.make_batch(w, seed=0, rows=[0], valid_len=[w.valid_len[0]])  # sample 0 only
+    fl, t = _oracle_sample(w, batch, w.S, 1)
+    print(json.dumps({"value": round(fl / t / 1e12, 6), "seconds": round(t, 3)}))
+
+
 def cpu_baseline(w, batch, budget_s=20.0):
     """The oracle as it stands, on the host cores: full (sample, head) pairs of
-    the workload until about ``budget_s`` seconds of work are done."""
+    the workload until about ``budget_s`` seconds of work are done; then one
+    pair on one thread."""
     fl, t = _oracle_sample(w, batch, w.S, 1)
     n = 1
     while t < budget_s and n < 2 * w.B * w.H:
@@ -649,9 +685,10 @@ def cpu_baseline(w, batch, budget_s=20.0):
         t += t2
         n += 1
     return {"value": round(fl / t / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
-            "kind": "oracle",
+            "kind": "oracle", "cpu_model": cpu_model(),
             "sample": f"{n} full (sample, head) pairs of {w.name}, forward+backward, float64 numpy "
-                      f"(BLAS threads = host cores); credited flops of the sample / wall time"}
+                      f"(BLAS threads = host cores); credited flops of the sample / wall time",
+            "one_thread": oracle_one_thread(w)}
 
 
 def run_reference(args):
@@ -698,7 +735,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true",
                     help="skip timing the standalone operators and the QKV producer")
+    ap.add_argument("--oracle-one-thread", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_one_thread:
+        _one_thread_child(W.WORKLOADS[args.workload])
+        return
     if args.impl == "ours":
         args.warmup = max(3, args.warmup)
     if args.impl == "reference":

@@ -93,10 +93,14 @@ def sweep_lengths(seed: int, n_rows: int = 8, T_txt: int = 256) -> np.ndarray:
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 to bfloat16 (nearest, ties to even); return uint16 bits."""
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    bias = np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))
-    return ((u + bias) >> np.uint64(16)).astype(np.uint16)
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    # u + 0x7FFF + lsb, in place in 32 bits: a sum that wraps (only the
+    # largest NaN payloads) loses 2^32, which the 16-bit result drops anyway
+    r = (u >> np.uint32(16)) & np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += u
+    r >>= np.uint32(16)
+    return r.astype(np.uint16)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:

@@ -33,3 +33,15 @@ def test_reference_arm_line_has_the_contract_keys():
     e2e = d["e2e"]
     assert (e2e["value"], e2e["unit"]) == (d["value"], d["unit"])
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_reports_cores_model_and_one_thread_run():
+    sys.path.insert(0, ROOT)
+    import bench
+    from invariant_mmdit_joint_gb300 import workloads as W
+    w = W.WORKLOADS["tiny"]
+    cb = bench.cpu_baseline(w, W.make_batch(w, seed=0), budget_s=0.0)
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] == os.cpu_count()
+    assert isinstance(cb["cpu_model"], str) and cb["cpu_model"]
+    one = cb["one_thread"]
+    assert one["cores"] == 1 and one["value"] > 0 and one["unit"] == "TFLOP/s", one
