@@ -245,8 +245,12 @@ def _stream_handle(stream) -> int | None:
     return stream.cuda_stream
 
 
-def _lengths(valid_len: Sequence[int]):
+def _lengths(valid_len: Sequence[int], shape: Shape):
+    """The host array of valid text lengths the C ABI reads: exactly B of
+    them (the library reads B entries, so a shorter list is refused here)."""
     vals = [int(x) for x in valid_len]
+    if len(vals) != shape.B:
+        raise ValueError(f"expected {shape.B} valid text lengths (one per sample), got {len(vals)}")
     return (ctypes.c_int32 * max(1, len(vals)))(*vals)
 
 
@@ -263,7 +267,7 @@ def rlk_joint_attn_fwd(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_v
     """Enqueue the forward; tensors or raw device pointers (ints)."""
     rc = lib().rlk_joint_attn_fwd(
         ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_q_txt), _ptr(g_k_txt),
-        _ptr(g_q_img), _ptr(g_k_img), _lengths(txt_valid_len), _ptr(out), _ptr(lse), _ptr(ctx),
+        _ptr(g_q_img), _ptr(g_k_img), _lengths(txt_valid_len, shape), _ptr(out), _ptr(lse), _ptr(ctx),
         _stream_handle(stream))
     _check(rc, "rlk_joint_attn_fwd")
 
@@ -274,7 +278,7 @@ def rlk_joint_attn_fwd_noalloc(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_im
     callers that cannot allocate); forward-only, calls must not overlap."""
     rc = lib().rlk_joint_attn_fwd_noalloc(
         ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_q_txt), _ptr(g_k_txt),
-        _ptr(g_q_img), _ptr(g_k_img), _lengths(txt_valid_len), _ptr(out), _ptr(lse),
+        _ptr(g_q_img), _ptr(g_k_img), _lengths(txt_valid_len, shape), _ptr(out), _ptr(lse),
         _stream_handle(stream))
     _check(rc, "rlk_joint_attn_fwd_noalloc")
 
@@ -287,7 +291,7 @@ def rlk_joint_attn_bwd(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_v
         workspace_bytes = workspace.numel() * workspace.element_size()
     rc = lib().rlk_joint_attn_bwd(
         ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_q_txt), _ptr(g_k_txt),
-        _ptr(g_q_img), _ptr(g_k_img), _lengths(txt_valid_len), _ptr(out), _ptr(dout), _ptr(lse),
+        _ptr(g_q_img), _ptr(g_k_img), _lengths(txt_valid_len, shape), _ptr(out), _ptr(dout), _ptr(lse),
         _ptr(ctx), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg_partial), _ptr(dg), _ptr(workspace),
         int(workspace_bytes), _stream_handle(stream))
     _check(rc, "rlk_joint_attn_bwd")
@@ -306,20 +310,20 @@ def rlk_qk_norm_rope(shape, q, k, g_q_txt, g_k_txt, g_q_img, g_k_img, ctx, strea
 
 
 def rlk_joint_attn_qk_gemm(shape, ctx, txt_valid_len, scores, stream=None) -> None:
-    rc = lib().rlk_joint_attn_qk_gemm(ctypes.byref(shape), _ptr(ctx), _lengths(txt_valid_len), _ptr(scores),
+    rc = lib().rlk_joint_attn_qk_gemm(ctypes.byref(shape), _ptr(ctx), _lengths(txt_valid_len, shape), _ptr(scores),
                                       _stream_handle(stream))
     _check(rc, "rlk_joint_attn_qk_gemm")
 
 
 def rlk_joint_attn_softmax(shape, scores, txt_valid_len, p, alpha, l, lse, stream=None) -> None:
-    rc = lib().rlk_joint_attn_softmax(ctypes.byref(shape), _ptr(scores), _lengths(txt_valid_len), _ptr(p),
+    rc = lib().rlk_joint_attn_softmax(ctypes.byref(shape), _ptr(scores), _lengths(txt_valid_len, shape), _ptr(p),
                                       _ptr(alpha), _ptr(l), _ptr(lse), _stream_handle(stream))
     _check(rc, "rlk_joint_attn_softmax")
 
 
 def rlk_joint_attn_av_gemm(shape, p, alpha, l, v, txt_valid_len, out, stream=None) -> None:
     rc = lib().rlk_joint_attn_av_gemm(ctypes.byref(shape), _ptr(p), _ptr(alpha), _ptr(l), _ptr(v),
-                                      _lengths(txt_valid_len), _ptr(out), _stream_handle(stream))
+                                      _lengths(txt_valid_len, shape), _ptr(out), _stream_handle(stream))
     _check(rc, "rlk_joint_attn_av_gemm")
 
 
@@ -331,7 +335,7 @@ def rlk_joint_attn_fwd_shard(shape, ctx, v, txt_valid_len, blk_begin, blk_end, s
                              stream=None) -> None:
     """Enqueue the forward over key column blocks [blk_begin, blk_end),
     handing the online-softmax state on (see the header)."""
-    rc = lib().rlk_joint_attn_fwd_shard(ctypes.byref(shape), _ptr(ctx), _ptr(v), _lengths(txt_valid_len),
+    rc = lib().rlk_joint_attn_fwd_shard(ctypes.byref(shape), _ptr(ctx), _ptr(v), _lengths(txt_valid_len, shape),
                                         int(blk_begin), int(blk_end), _ptr(state_in), _ptr(state_out), _ptr(out),
                                         _ptr(lse), _stream_handle(stream))
     _check(rc, "rlk_joint_attn_fwd_shard")
@@ -344,7 +348,7 @@ def rlk_joint_attn_fwd_streams(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_im
     args = [_ptr(x) for pair in (q, k, v) for x in pair]
     rc = lib().rlk_joint_attn_fwd_streams(
         ctypes.byref(shape), *args, _ptr(g_q_txt), _ptr(g_k_txt), _ptr(g_q_img), _ptr(g_k_img),
-        _lengths(txt_valid_len), _ptr(out[0]), _ptr(out[1]), _ptr(lse), _ptr(ctx), _stream_handle(stream))
+        _lengths(txt_valid_len, shape), _ptr(out[0]), _ptr(out[1]), _ptr(lse), _ptr(ctx), _stream_handle(stream))
     _check(rc, "rlk_joint_attn_fwd_streams")
 
 
@@ -356,7 +360,7 @@ def rlk_joint_attn_bwd_streams(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_im
     ins = [_ptr(x) for pair in (q, k, v) for x in pair]
     rc = lib().rlk_joint_attn_bwd_streams(
         ctypes.byref(shape), *ins, _ptr(g_q_txt), _ptr(g_k_txt), _ptr(g_q_img), _ptr(g_k_img),
-        _lengths(txt_valid_len), _ptr(out[0]), _ptr(out[1]), _ptr(dout[0]), _ptr(dout[1]), _ptr(lse), _ptr(ctx),
+        _lengths(txt_valid_len, shape), _ptr(out[0]), _ptr(out[1]), _ptr(dout[0]), _ptr(dout[1]), _ptr(lse), _ptr(ctx),
         _ptr(dq[0]), _ptr(dq[1]), _ptr(dk[0]), _ptr(dk[1]), _ptr(dv[0]), _ptr(dv[1]), _ptr(dg_partial), _ptr(dg),
         _ptr(workspace), int(workspace_bytes), _stream_handle(stream))
     _check(rc, "rlk_joint_attn_bwd_streams")
@@ -377,7 +381,7 @@ def rlk_qkv_bias_gemm(shape, x, w, b, gains, ctx, q, k, v, stream=None) -> None:
 def rlk_joint_attn_fwd_ctx(shape, ctx, v, txt_valid_len, out, lse, stream=None) -> None:
     """Attention from a prepared context; v and out are (text, image) pairs."""
     rc = lib().rlk_joint_attn_fwd_ctx(ctypes.byref(shape), _ptr(ctx), _ptr(v[0]), _ptr(v[1]),
-                                      _lengths(txt_valid_len), _ptr(out[0]), _ptr(out[1]), _ptr(lse),
+                                      _lengths(txt_valid_len, shape), _ptr(out[0]), _ptr(out[1]), _ptr(lse),
                                       _stream_handle(stream))
     _check(rc, "rlk_joint_attn_fwd_ctx")
 
@@ -485,6 +489,13 @@ class JointAttention:
                 raise ValueError(f"expected contiguous bf16 {want} on {self.device}, got {t.dtype} "
                                  f"{tuple(t.shape)} on {t.device}")
 
+    def _check_f32(self, t, want, name):
+        import torch
+        if t.dtype != torch.float32 or tuple(t.shape) != tuple(want) or not t.is_contiguous() \
+                or t.device != self.device:
+            raise ValueError(f"{name} must be a contiguous float32 {tuple(want)} tensor on {self.device}, got "
+                             f"{t.dtype} {tuple(t.shape)} on {t.device}")
+
     def _check_gains(self, gains):
         import torch
         if gains.dtype != torch.float32 or tuple(gains.shape) != (4, HEAD_DIM) or not gains.is_contiguous() \
@@ -497,9 +508,15 @@ class JointAttention:
         self._check_gains(gains)
         if len(valid_len) != self.shape.B:
             raise ValueError("one valid length per sample")
-        out = torch.empty_like(q) if out is None else out
+        sh = self.shape
+        if out is None:
+            out = torch.empty_like(q)
+        else:
+            self._check_inputs(out)
         if lse is None and want_lse:
-            lse = torch.empty((self.shape.B, self.shape.H, self.shape.S), dtype=torch.float32, device=self.device)
+            lse = torch.empty((sh.B, sh.H, sh.S), dtype=torch.float32, device=self.device)
+        elif lse is not None:
+            self._check_f32(lse, (sh.B, sh.H, sh.S), "lse")
         rlk_joint_attn_fwd(self.shape, q, k, v, gains[0], gains[1], gains[2], gains[3], valid_len,
                            out, lse, self.ctx, stream)
         return out, lse
@@ -510,13 +527,17 @@ class JointAttention:
         self._check_inputs(q, k, v, out, dout)
         self._check_gains(gains)
         sh = self.shape
+        self._check_f32(lse, (sh.B, sh.H, sh.S), "lse")
         dq = torch.empty_like(q) if dq is None else dq
         dk = torch.empty_like(k) if dk is None else dk
         dv = torch.empty_like(v) if dv is None else dv
+        self._check_inputs(dq, dk, dv)
         if dg_partial is None:
             dg_partial = torch.empty((sh.B, sh.H, 4, HEAD_DIM), dtype=torch.float32, device=self.device)
         if dg is None:
             dg = torch.empty((4, HEAD_DIM), dtype=torch.float32, device=self.device)
+        self._check_f32(dg_partial, (sh.B, sh.H, 4, HEAD_DIM), "dg_partial")
+        self._check_f32(dg, (4, HEAD_DIM), "dg")
         rlk_joint_attn_bwd(sh, q, k, v, gains[0], gains[1], gains[2], gains[3], valid_len, out, dout,
                            lse, self.ctx, dq, dk, dv, dg_partial, dg, self.workspace, stream=stream)
         return dq, dk, dv, dg_partial, dg

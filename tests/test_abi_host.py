@@ -364,3 +364,33 @@ def test_output_projection_fails_closed(L):
     import torch
     if not torch.cuda.is_available():
         assert L.rlk_attn_out_bias_gemm(ctypes.byref(no_text), None, p, None, p, None, p, None, p, None) == 5
+
+
+def test_binding_refuses_a_wrong_number_of_valid_lengths(L):
+    shape = pkg.Shape.make(2, 16, 8, 8, 2)
+    for bad in ([3], [3, 4, 5], []):
+        with pytest.raises(ValueError):
+            pkg._lengths(bad, shape)
+    assert list(pkg._lengths([3, 4], shape)) == [3, 4]
+
+
+def test_joint_attention_checks_caller_supplied_buffers(L):
+    """Wrongly shaped outputs are refused in Python, before the library is
+    called (CPU tensors: nothing reaches a device)."""
+    torch = pytest.importorskip("torch")
+    ja = pkg.JointAttention(1, 16, 8, 8, 2, device="cpu")
+    x = torch.zeros((1, 80, 2, 128), dtype=torch.bfloat16)
+    gains = torch.ones((4, 128), dtype=torch.float32)
+    with pytest.raises(ValueError):
+        ja.forward(x, x, x, gains, [11], out=torch.zeros((1, 80, 2, 127), dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        ja.forward(x, x, x, gains, [11], lse=torch.zeros((1, 2, 79)))
+    lse = torch.zeros((1, 2, 80))
+    with pytest.raises(ValueError):
+        ja.backward(x, x, x, gains, [11], x, x, lse, dq=torch.zeros((1, 80, 2, 128)))
+    with pytest.raises(ValueError):
+        ja.backward(x, x, x, gains, [11], x, x, lse, dg_partial=torch.zeros((1, 2, 4, 127)))
+    with pytest.raises(ValueError):
+        ja.backward(x, x, x, gains, [11], x, x, lse, dg=torch.zeros((4, 127)))
+    with pytest.raises(ValueError):
+        ja.backward(x, x, x, gains, [11], x, x, torch.zeros((1, 2, 80), dtype=torch.float64))
