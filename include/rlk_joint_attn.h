@@ -201,8 +201,8 @@ rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape,
  * qk_rmsnorm, multi_axis_rope, joint_attn_qk_gemm, joint_attn_softmax and
  * joint_attn_av_gemm as separate rows and requires joint_attention_fused to
  * be a byte-equal fusion of the three attention operators; the WS1
- * Single-GPU Kernel List says the fusion "must match their composition byte
- * for byte". The four calls below, chained as
+ * Single-GPU Kernel List asks the same of the fused kernel. The four calls
+ * below, chained as
  *     rlk_qk_norm_rope -> rlk_joint_attn_qk_gemm -> rlk_joint_attn_softmax
  *                      -> rlk_joint_attn_av_gemm
  * produce `out` and `lse` bytes identical to rlk_joint_attn_fwd() on the same
@@ -302,8 +302,8 @@ rlk_status rlk_joint_attn_bwd_streams(const rlk_ja_shape* shape,
 
 /* ---------------------------------------------------------------------------
  * The attention's adjacent producer: row qkv_bias_gemm of the RFC's WS1
- * table ("per-stream packed QKV + bias"; the WS1 kernel list: 3072 ->
- * 3 x 3072 + bias, one weight set per stream), with qk_rmsnorm and
+ * table (each stream's Q, K and V projections packed in one GEMM with a
+ * bias; the WS1 kernel list: 3072 -> 3 x 3072, one weight set per stream), with qk_rmsnorm and
  * multi_axis_rope fused into its epilogue.
  *   x_txt, x_img   bf16 [B, T_txt, C] and [B, grid_h*grid_w, C], C = H * 128
  *   w_txt, w_img   bf16 [3C, C]: output feature rows (the nn.Linear layout),
@@ -395,8 +395,8 @@ rlk_status rlk_joint_attn_trace(rlk_ja_trace* out);
 
 /* ---------------------------------------------------------------------------
  * The fused forward over one key shard, for ring-ordered sequence
- * parallelism. The RFC's WS2 table asks sp_attention_ring for a "fixed
- * global block and partial-state merge order", and its numerical
+ * parallelism. The RFC's WS2 table asks sp_attention_ring to fix both the
+ * order of the global blocks and the order of merging partial states, and its numerical
  * requirements ask strict replay and topology invariance to keep byte
  * equality. Here the global blocks are the forward's own key tiles (column
  * block t = key tile t: text tiles from token 0, then image tiles from token

@@ -1,10 +1,9 @@
 // The three attention operators of the RFC #386 WS1 table on their own --
 // joint_attn_qk_gemm, joint_attn_softmax and joint_attn_av_gemm -- whose
 // composition reproduces the fused forward (joint_attention_fused,
-// k_attn_fwd.cu) byte for byte, as the table's joint_attention_fused row
-// ("byte-equal fusion of the three attention operators") and the WS1
-// Single-GPU Kernel List ("must match their composition byte for byte")
-// require.
+// k_attn_fwd.cu) byte for byte: the table's joint_attention_fused row and
+// the WS1 Single-GPU Kernel List both define the fused kernel as one whose
+// bytes equal those of the three operators run one after another.
 //
 // Byte equality holds because each operator performs the fused kernel's
 // arithmetic in the fused kernel's order:

@@ -9,7 +9,7 @@
 // Sources: RFC #386 "WS1/WS2 kernel roadmap", Model contract table (Q/K
 // preprocessing and RoPE rows) and WS1 table (qk_rmsnorm, multi_axis_rope);
 // "WS1 Single-GPU Kernel List", Kernel table (fwd + bwd for both rows) and
-// Acceptance ("multi-path gradient sums use a fixed order").
+// Acceptance (gradients summed over several paths in one fixed order).
 #include <cmath>
 
 #include "rlk_device.cuh"

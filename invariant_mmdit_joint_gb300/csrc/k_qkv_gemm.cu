@@ -1,6 +1,6 @@
-// Row qkv_bias_gemm of the RFC #386 WS1 table ("per-stream packed QKV +
-// bias"; the WS1 Single-GPU Kernel List: 3072 -> 3 x 3072 + bias, one weight
-// set per stream) on the tcgen05 tensor cores, with rows qk_rmsnorm and
+// Row qkv_bias_gemm of the RFC #386 WS1 table (each stream's Q, K and V
+// projections in one GEMM with a bias; the WS1 Single-GPU Kernel List:
+// 3072 -> 3 x 3072, one weight set per stream) on the tcgen05 tensor cores, with rows qk_rmsnorm and
 // multi_axis_rope fused into its epilogue, so the normed, rotated q^ and k^
 // go straight into the attention's context (the "adjacent producer" of the
 // fused attention).

@@ -238,7 +238,7 @@ def joint_attn_backward(Q, K, V, g, dO, T_txt, grid_h, grid_w, valid_len,
     Returns dQ, dK, dV [B, S, H, D], the per-(sample, head) gain-gradient
     partials dg_partial [B, H, 4, D] (slots q_txt, k_txt, q_img, k_img, each
     summed over that stream's tokens) and dg [4, D] = their sum over b and h.
-    [KL] "All differentiable ... operators require forward and backward".
+    [RFC] Work items: every differentiable WS1 operator needs a backward too.
     """
     B, S, H, D = Q.shape
     heads = list(range(H)) if heads is None else list(heads)
@@ -267,8 +267,8 @@ def joint_attn_backward(Q, K, V, g, dO, T_txt, grid_h, grid_w, valid_len,
 
 
 def qkv_projection(X, W, b):
-    """[RFC] WS1 row qkv_bias_gemm ("per-stream packed QKV + bias"; [KL]
-    3072 -> 3 x 3072 + bias, one weight set per stream) for one stream, in
+    """[RFC] WS1 row qkv_bias_gemm (each stream's Q, K and V projections in
+    one GEMM with a bias; [KL] 3072 -> 3 x 3072, one weight set per stream) for one stream, in
     float64: Y = X W^T + b.
 
     X [B, T, C] with C = H * 128; W [3C, C], rows are output features in the
@@ -283,8 +283,8 @@ def qkv_projection(X, W, b):
 
 
 def attn_out_projection(O_s, W, b):
-    """[RFC] WS1 row attn_out_bias_gemm ("per-stream attention output
-    projection"; [KL] 3072 -> 3072 + bias) for one stream, in float64:
+    """[RFC] WS1 row attn_out_bias_gemm (the attention output's projection,
+    one per stream; [KL] 3072 -> 3072 with a bias) for one stream, in float64:
     Y = O W^T + b with O [B, T, H, 128] read as [B, T, C], W [C, C] (output
     feature rows), b [C]. Returns Y [B, T, C]."""
     B, T, H, D = O_s.shape
