@@ -25,6 +25,10 @@ and larger than L2:
                             memory and its results read back, pipelined over
                             three streams (serial on one stream)
 dense_convention restates value with every key counted, masked or not.
+Outside those regions: the standalone operators (unfused_forward), the QKV
+producer and output projection (qkv_producer), and the key-shard forward and
+separate-stream step (shards_and_streams), each byte-compared with the fused
+calls.
 """
 
 from __future__ import annotations
@@ -233,6 +237,69 @@ def measure_unfused(pkg, ja, w, q, k, v, gains, vl, fused_out, fused_ms, peaks, 
     return {"ms_per_forward": round(ms, 4), "fused_forward_ms": round(fused_ms, 4),
             "byte_equal_to_fused": byte_equal, "steps": n_steps, "operators": ops,
             "peak": f"hbm_gbs {hbm}"}
+
+
+def _time_ms(fn, n_steps):
+    import torch
+    stream = torch.cuda.current_stream()
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n_steps
+
+
+def measure_shards_streams(ja, w, q, k, v, do, gains, vl, flops, n_steps):
+    """The key-shard forward (ring order: the softmax state handed from shard
+    to shard) with the key blocks split into 2 and 4 equal shards, and the
+    forward + backward on separately allocated text and image buffers; each
+    timed per call with CUDA events and compared byte for byte with the
+    fused calls on the concatenated buffers."""
+    import torch
+
+    def eq(a, b):
+        return bool(torch.equal(a.contiguous().view(torch.int16), b.contiguous().view(torch.int16)))
+
+    out_f, lse_f = ja.forward(q, k, v, gains, vl)
+    res_f = ja.backward(q, k, v, gains, vl, out_f, do, lse_f)
+    fwd_ms = _time_ms(lambda: ja.forward(q, k, v, gains, vl), n_steps)
+    nb = ja.n_key_blocks()
+    shards = {}
+    for n in (2, 4):
+        bounds = [round(i * nb / n) for i in range(1, n)]
+        out_s, lse_s = ja.forward_sharded(q, k, v, gains, vl, bounds)
+        ms = _time_ms(lambda: ja.forward_sharded(q, k, v, gains, vl, bounds), n_steps)
+        shards[str(n)] = {"bounds": bounds, "ms": round(ms, 4),
+                          "tflops": round(flops["fwd"] / (ms * 1e-3) / 1e12, 1),
+                          "bytes_equal_to_fused": eq(out_s, out_f) and bool(torch.equal(lse_s, lse_f))}
+    T = w.T_txt
+    split = lambda t: (t[:, :T].contiguous() if T > 0 else None, t[:, T:].contiguous())  # noqa: E731
+    qs, ks, vs, dos = split(q), split(k), split(v), split(do)
+
+    def step_streams():
+        o, l = ja.forward_streams(qs, ks, vs, gains, vl)
+        return o, l, ja.backward_streams(qs, ks, vs, gains, vl, o, dos, l)
+
+    o_s, l_s, r_s = step_streams()
+    cat = lambda pair: torch.cat([x for x in pair if x is not None], dim=1)  # noqa: E731
+    same = eq(cat(o_s), out_f) and bool(torch.equal(l_s, lse_f))
+    for a, b in zip(r_s[:3], res_f[:3]):
+        same = same and eq(cat(a), b)
+    same = same and bool(torch.equal(r_s[3], res_f[3])) and bool(torch.equal(r_s[4], res_f[4]))
+    ms_streams = _time_ms(step_streams, n_steps)
+    def step_cat():
+        o, l = ja.forward(q, k, v, gains, vl)
+        return ja.backward(q, k, v, gains, vl, o, do, l)
+
+    ms_cat = _time_ms(step_cat, n_steps)
+    return {"fused_forward_ms": round(fwd_ms, 4), "key_shards": shards, "steps": n_steps,
+            "separate_streams": {"ms_per_step": round(ms_streams, 4), "concatenated_ms_per_step": round(ms_cat, 4),
+                                 "tflops": round(flops["fwd_bwd"] / (ms_streams * 1e-3) / 1e12, 1),
+                                 "bytes_equal_to_concatenated": same}}
 
 
 def measure_qkv(pkg, w, peaks, n_steps):
@@ -571,9 +638,10 @@ def run_ours(args):
     if not args.no_unfused:
         fwd_ms = sum(per_kernel[n]["avg_ms"] for n in ("rope_table", "prologue", "attn_fwd") if n in per_kernel)
         unfused = measure_unfused(pkg, ja, w, q, k, v, gains, vl, out, fwd_ms, peaks, max(3, min(args.steps, 10)))
-    qkv = None
+    qkv = rows23 = None
     if not args.no_unfused:
         qkv = measure_qkv(pkg, w, peaks, max(3, min(args.steps, 20)))
+        rows23 = measure_shards_streams(ja, w, q, k, v, do, gains, vl, flops, max(3, min(args.steps, 20)))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -595,7 +663,7 @@ def run_ours(args):
                    "l2": "inputs larger than L2: q,k,v,dO, ctx and workspace total "
                          f"{(4 * w.B * w.S * w.H * 128 * 2) / 1e6:.0f} MB + scratch > 129 MB L2"},
         "roofline": roofline, "kernels": per_kernel, "phases": phases, "dense_convention": dense,
-        "unfused_forward": unfused, "qkv_producer": qkv,
+        "unfused_forward": unfused, "qkv_producer": qkv, "shards_and_streams": rows23,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
