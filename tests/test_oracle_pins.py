@@ -495,3 +495,168 @@ def test_attn_out_projection_matches_brute_force_and_identity():
     P = np.eye(C)[perm]
     Y = O.attn_out_projection(O_s, P, np.zeros(C))
     assert np.array_equal(Y, O_s.reshape(B, T, C)[..., perm])
+
+
+# ---------------------------------------------------------------- widening, row path, gain attribution
+def bf16_by_definition(bits: int) -> float:
+    """A bfloat16 bit pattern decoded from the format's definition: sign bit
+    15, an 8-bit biased exponent (bias 127) in bits 14..7 and 7 fraction bits;
+    exponent 0 is subnormal (0.f x 2^-126), exponent 255 is inf / NaN."""
+    import math
+    s = -1.0 if bits & 0x8000 else 1.0
+    e = (bits >> 7) & 0xFF
+    f = bits & 0x7F
+    if e == 0xFF:
+        return s * math.inf if f == 0 else math.nan
+    if e == 0:
+        return s * math.ldexp(f, -126 - 7)
+    return s * math.ldexp(128 + f, e - 127 - 7)
+
+
+def widen_mismatches(widen_bf16=O.widen_bf16) -> int:
+    """Bit patterns (of all 65,536) that ``widen_bf16`` decodes differently
+    from the definition; NaNs must stay NaN. The count, so a plant shows."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):  # signalling-NaN patterns warn when widened
+        got = widen_bf16(bits)
+    bad = 0
+    for b in range(1 << 16):
+        ref = bf16_by_definition(b)
+        g = float(got[b])
+        if np.isnan(ref):
+            bad += int(not np.isnan(g))
+        elif g != ref or np.signbit(g) != np.signbit(ref):
+            bad += 1
+    return bad
+
+
+def test_widen_bf16_is_exact_over_every_bit_pattern():
+    assert widen_mismatches() == 0
+    torch = pytest.importorskip("torch")
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    with np.errstate(invalid="ignore"):
+        got = O.widen_bf16(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+RAGGED_ROWS = dict(B=2, H=2, T_txt=20, grid_h=3, grid_w=5, valid_len=(7, 20))
+
+
+def forward_rows_error(forward_rows=O.forward_rows) -> float:
+    """``forward_rows`` (one query row at a time, used for the full-size spot
+    checks) against the selected rows of ``joint_attn_forward``, with and
+    without the bf16 storage rounding, on the tiny case and a ragged one."""
+    worst = 0.0
+    w2 = W.Workload("ragged_rows", **RAGGED_ROWS)
+    for w, seed in ((W.TINY, 0), (w2, 3)):
+        d = W.make_batch(w, seed)
+        Q, K, V = (O.widen_bf16(d[n]) for n in ("q", "k", "v"))
+        g, vl = d["gains"].astype(np.float64), d["valid_len"]
+        for store in (False, True):
+            o, lse = O.joint_attn_forward(Q, K, V, g, w.T_txt, w.grid_h, w.grid_w, vl, store_bf16=store)
+            for b in range(w.B):
+                for h in range(w.H):
+                    rows = list(range(w.S)) if w is W.TINY else [0, 1, w.T_txt - 1, w.T_txt, w.S - 1, 9]
+                    ro, rl = forward_rows(Q, K, V, g, w.T_txt, w.grid_h, w.grid_w, vl[b], b, h, rows,
+                                          store_bf16=store)
+                    worst = max(worst, np.max(np.abs(ro - o[b, rows, h])), np.max(np.abs(rl - lse[b, h, rows])))
+    return worst
+
+
+def test_forward_rows_equals_the_full_forward():
+    assert forward_rows_error() <= 1e-12
+
+
+def dg_attribution_error(backward=O.joint_attn_backward, h=1e-6) -> float:
+    """Each per-(sample, head) gain-gradient slot against a central difference
+    of sum(O[b, :, h] * dO[b, :, h]) -- dO zeroed outside that (sample, head)
+    -- in the gain of that slot, along a random direction and elementwise at
+    a few dims. B = 2 and H = 2 with different valid lengths, so a partial
+    credited to the wrong sample, head or slot fails."""
+    rng = np.random.default_rng(21)
+    T, gh, gw, vl = 3, 2, 3, np.array([2, 1])
+    B, H, D = 2, 2, 128
+    S = T + gh * gw
+    Q, K, V, dO = (rng.standard_normal((B, S, H, D)) for _ in range(4))
+    g = rng.uniform(0.5, 1.5, (4, D))
+    _, _, _, dgp, _ = backward(Q, K, V, g, dO, T, gh, gw, vl)
+    worst = 0.0
+    for b in range(B):
+        for hh in range(H):
+            dOm = np.zeros_like(dO)
+            dOm[b, :, hh] = dO[b, :, hh]
+
+            def loss(gg):
+                o, _ = O.joint_attn_forward(Q, K, V, gg, T, gh, gw, vl)
+                return float(np.sum(o * dOm))
+            for slot in range(4):
+                d = rng.standard_normal(D)
+                gp, gm = g.copy(), g.copy()
+                gp[slot] += h * d
+                gm[slot] -= h * d
+                fd = (loss(gp) - loss(gm)) / (2 * h)
+                an = float(np.dot(dgp[b, hh, slot], d))
+                worst = max(worst, abs(fd - an) / max(abs(an), 1e-3))
+                for j in rng.choice(D, 3, replace=False):
+                    gp, gm = g.copy(), g.copy()
+                    gp[slot, j] += h
+                    gm[slot, j] -= h
+                    fd = (loss(gp) - loss(gm)) / (2 * h)
+                    worst = max(worst, abs(fd - dgp[b, hh, slot, j]) / max(1.0, abs(dgp[b, hh, slot, j])))
+    return worst
+
+
+def test_gain_gradient_partials_are_attributed_to_their_sample_head_and_slot():
+    assert dg_attribution_error() <= 1e-6
+
+
+def test_planted_mistakes_in_the_helpers_are_caught():
+    """Widening, the row path and the per-(sample, head) gain partials each
+    fail their pin with one plausible mistake planted."""
+    # widening: a shift by 15 instead of 16
+    def widen_shift(bits):
+        u = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(15)
+        with np.errstate(invalid="ignore"):
+            return u.view(np.float32).astype(np.float64)
+    assert widen_mismatches(widen_shift) > 1000
+
+    # widening: the sign bit dropped
+    def widen_unsigned(bits):
+        with np.errstate(invalid="ignore"):
+            return np.abs(O.widen_bf16(bits))
+    assert widen_mismatches(widen_unsigned) > 1000
+
+    # row path: every selected row rotated by the first token's angles
+    def rows_first_angle(Q, K, V, g, T_txt, grid_h, grid_w, L, b, h, rows, store_bf16=False, **kw):
+        S = Q.shape[1]
+        ang = O.rope_angles(O.rope_positions(T_txt, grid_h, grid_w))
+        gq, gk = O.token_gains(g, T_txt, S, "q"), O.token_gains(g, T_txt, S, "k")
+        kh = O.rope_rotate(O.rmsnorm(K[b, :, h], gk)[0], ang)
+        kh = O.round_bf16(kh) if store_bf16 else kh
+        outs, lses = [], []
+        for i in rows:
+            qh = O.rope_rotate(O.rmsnorm(Q[b, i:i + 1, h], gq[i:i + 1])[0], ang[0:1])
+            qh = O.round_bf16(qh) if store_bf16 else qh
+            o, lse, _ = O.attention_forward(qh, kh, V[b, :, h], O.key_valid(T_txt, S, int(L)))
+            outs.append(o[0])
+            lses.append(lse[0])
+        return np.array(outs), np.array(lses)
+    assert forward_rows_error(rows_first_angle) > 1e-3
+
+    # gain partials: the image Q and K slots swapped, and the (b, h) slots
+    # transposed; both keep dgp.sum(axis=(0, 1)) equal to the true dg sum
+    # of the swapped slots, so only the attribution pin sees them
+    def bwd_slots_swapped(*a, **k):
+        dQ, dK, dV, dgp, dg = O.joint_attn_backward(*a, **k)
+        dgp = dgp[:, :, [0, 1, 3, 2]]
+        return dQ, dK, dV, dgp, dgp.sum(axis=(0, 1))
+    assert dg_attribution_error(bwd_slots_swapped) > 1e-3
+
+    def bwd_bh_transposed(*a, **k):
+        dQ, dK, dV, dgp, dg = O.joint_attn_backward(*a, **k)
+        return dQ, dK, dV, dgp.transpose(1, 0, 2, 3).copy(), dg
+    assert dg_attribution_error(bwd_bh_transposed) > 1e-3
