@@ -2,10 +2,22 @@
 path through the C ABI, and compare with the oracle at the declared
 tolerances: forward max abs <= 1e-2 and mean abs <= 1e-3 for N(0,1) inputs
 (inputs drawn as sigma * N(0,1) scale both by sigma, since O is linear in
-V), lse <= 1e-4 relative, gradients relative L2 <= 1e-2. The oracle is run
-with the declared bf16 storage rounding of the normed, rotated q and k; the
-exact-float64 oracle is also checked, at the looser lse bound that rounding
-implies (PURE_LSE_ABS)."""
+V), lse <= 1e-4 relative, gradients relative L2 <= 1e-2.
+
+These bounds are applied against the oracle run with the declared bf16
+storage of the normed, rotated q and k (``store_bf16=True``): the prologue
+is its own kernel whose output is stored as bf16, and the tensor cores take
+no fp32 operand. Against the exact float64 oracle the bound is derived, not
+chosen (``assert_forward_close_exact``): by the triangle inequality
+
+    |gpu - exact| <= |gpu - stored| + |stored - exact|,
+
+where the first term is held to the declared bounds and the second is the
+change the storage rounding itself makes, which the oracle computes exactly,
+element by element. The declared 1e-4 lse bound therefore holds against the
+storage-rounded oracle; against exact float64 the lse differs by the
+storage term as well (a few 1e-4 relative).
+"""
 
 from __future__ import annotations
 
@@ -17,10 +29,6 @@ FWD_MAX_ABS = 1e-2
 FWD_MEAN_ABS = 1e-3
 LSE_REL = 1e-4
 GRAD_REL_L2 = 1e-2
-# bf16 storage of q and k alone moves lse against exact float64 by up to
-# ~1.5e-3 absolute at S = 80 and ~1.6e-3 at S = 4352 (measured with the
-# oracle); little averaging over keys (S = 6) gives ~2.5e-3.
-PURE_LSE_ABS = 5e-3
 
 
 def to_dev(bits: np.ndarray, dev):
@@ -55,20 +63,48 @@ def oracle_inputs(batch: dict):
     return Q, K, V, dO, batch["gains"].astype(np.float64)
 
 
-def assert_forward_close(out, lse, ref_o, ref_lse, where="", scale=1.0, lse_abs=None):
+def assert_forward_close(out, lse, ref_o, ref_lse, where="", scale=1.0):
+    """The declared bounds against the storage-rounded oracle."""
     err = np.abs(out - ref_o)
-    if lse_abs is not None:
-        # against exact float64 the bf16 rounding of the stored q and k adds
-        # to the output rounding; with few keys |O| is large and the bf16
-        # output rounding alone reaches ~1e-3 mean: the bound doubles
-        scale = 2.0 * scale
     assert err.max() <= FWD_MAX_ABS * scale, (where, "O max abs", err.max())
     assert err.mean() <= FWD_MEAN_ABS * scale, (where, "O mean abs", err.mean())
-    if lse_abs is None:
-        rel = np.abs(lse - ref_lse) / np.abs(ref_lse)
-        assert rel.max() <= LSE_REL, (where, "lse rel", rel.max())
-    else:
-        assert np.max(np.abs(lse - ref_lse)) <= lse_abs, (where, "lse abs", np.max(np.abs(lse - ref_lse)))
+    rel = np.abs(lse - ref_lse) / np.abs(ref_lse)
+    assert rel.max() <= LSE_REL, (where, "lse rel", rel.max())
+
+
+def assert_forward_close_exact(out, lse, stored, exact, where="", scale=1.0):
+    """Against the exact float64 oracle, at the bound the storage reading
+    implies: per element, the declared bound plus the oracle's own change
+    under bf16 storage of q and k (``stored`` = (O, lse) with storage
+    rounding, ``exact`` = (O, lse) without). Records the measured errors
+    when RLK_PARITY_REPORT names a file."""
+    so, sl = stored
+    eo, el = exact
+    store_o = np.abs(so - eo)
+    store_l = np.abs(sl - el)
+    err = np.abs(out - eo)
+    lerr = np.abs(lse - el)
+    assert np.all(err <= FWD_MAX_ABS * scale + store_o), (where, "O abs vs exact", float(np.max(err - store_o)))
+    assert err.mean() <= FWD_MEAN_ABS * scale + store_o.mean(), (where, "O mean abs vs exact", err.mean(),
+                                                                 store_o.mean())
+    assert np.all(lerr <= LSE_REL * np.abs(sl) + store_l), (where, "lse vs exact",
+                                                          float(np.max(lerr - store_l)))
+    report(where, {"o_max_abs": float(err.max()), "o_mean_abs": float(err.mean()),
+                   "lse_max_rel": float(np.max(lerr / np.abs(el))),
+                   "storage_o_max_abs": float(store_o.max()), "storage_o_mean_abs": float(store_o.mean()),
+                   "storage_lse_max_rel": float(np.max(store_l / np.abs(el))),
+                   "gpu_vs_stored_lse_max_rel": float(np.max(np.abs(lse - sl) / np.abs(sl))),
+                   "n": int(err.size)})
+
+
+def report(where, values: dict):
+    """Append one JSON line to the file RLK_PARITY_REPORT names, if any."""
+    import json
+    import os
+    path = os.environ.get("RLK_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": where, **values}) + "\n")
 
 
 def rel_l2(a, b) -> float:

@@ -42,7 +42,7 @@ def _full_compare(w, batch, res, heads=None, where="", pure=True):
     Hh.assert_forward_close(out, lse, ro, rl, where, scale=w.scale)
     if pure:
         po, pl = O.joint_attn_forward(Q, K, V, g, w.T_txt, w.grid_h, w.grid_w, vl)
-        Hh.assert_forward_close(out, lse, po, pl, where + " (exact f64)", scale=w.scale, lse_abs=Hh.PURE_LSE_ABS)
+        Hh.assert_forward_close_exact(out, lse, (ro, rl), (po, pl), where + " (exact f64)", scale=w.scale)
     if "dq" not in res:
         return
     rdq, rdk, rdv, rdgp, rdg = O.joint_attn_backward(Q, K, V, g, dO, w.T_txt, w.grid_h, w.grid_w, vl,
@@ -144,8 +144,8 @@ def test_full_size_workloads_match_oracle_on_head_subset(dev, name):
         lse = Hh.f64(res["lse"][b, h, rows])
         Hh.assert_forward_close(out, lse, ro, rl, f"{name} rows b={b} h={h}", scale=w.scale)
         po, pl = O.forward_rows(Q, K, V, g, w.T_txt, w.grid_h, w.grid_w, L, 0, 0, rows)
-        Hh.assert_forward_close(out, lse, po, pl, f"{name} rows b={b} h={h} (exact f64)", scale=w.scale,
-                                lse_abs=Hh.PURE_LSE_ABS)
+        Hh.assert_forward_close_exact(out, lse, (ro, rl), (po, pl), f"{name} rows b={b} h={h} (exact f64)",
+                                      scale=w.scale)
 
 
 def test_masked_keys_have_no_effect_on_gpu(dev):

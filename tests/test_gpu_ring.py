@@ -1,11 +1,17 @@
 """The forward run as key shards handing the online-softmax state on in the
 fixed global block order (the RFC's WS2 row sp_attention_ring, emulated on
 one GPU): every split of the key blocks into consecutive shards must give
-the fused forward's out and lse bytes (topology invariance)."""
+the fused forward's out and lse bytes (topology invariance), and each split's
+out and lse are also compared with the CPU oracle at the declared bounds, so
+the hand-off itself (the rescale at a shard's first block, a shard with no
+valid key passing its state through, the last shard's O / l) is checked
+against the mathematics, not only against the fused kernel."""
 
 import random
 
 import pytest
+
+from oracle import joint_attn as O
 
 import invariant_mmdit_joint_gb300 as pkg
 from invariant_mmdit_joint_gb300 import workloads as W
@@ -60,10 +66,19 @@ def test_every_shard_split_gives_the_fused_bytes(w, dev):
     out_f, lse_f = ja.forward(q, k, v, gains, vl)
     torch.cuda.synchronize()
     n_txt = -(-w.T_txt // 128)
+    # the oracle on the same inputs (every head of the small cases; heads 0
+    # and H - 1 of the full-size one)
+    heads = list(range(w.H)) if w.S <= 1024 else [0, w.H - 1]
+    sub = {n: batch[n][:, :, heads] for n in ("q", "k", "v")}
+    sub["gains"] = batch["gains"]
+    Q, K, V, _, g = Hh.oracle_inputs(sub)
+    ro, rl = O.joint_attn_forward(Q, K, V, g, w.T_txt, w.grid_h, w.grid_w, batch["valid_len"], store_bf16=True)
     for bounds in _splits(ja.n_key_blocks(), n_txt, 7):
         out, lse = ja.forward_sharded(q, k, v, gains, vl, bounds)
         torch.cuda.synchronize()
         pkg.rlk_joint_attn_check_status()
+        Hh.assert_forward_close(Hh.f64(out[:, :, heads]), Hh.f64(lse[:, heads]), ro, rl,
+                                f"{w.name} shards {bounds}", scale=w.scale)
         assert Hh.bits_equal(out, out_f), (w.name, bounds)
         assert Hh.bits_equal(lse, lse_f), (w.name, bounds)
 
