@@ -156,10 +156,15 @@ rlk_status rlk_joint_attn_fwd(const rlk_ja_shape* shape,
  * `ctx`: the forward context lives in a file-scope device array of
  * RLK_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
  * the process exits. Nothing is allocated or freed.
+ *   - Arguments are checked exactly as rlk_joint_attn_fwd() checks them,
+ *     in the same order and with the same status codes (ctx aside).
  *   - Shapes whose rlk_joint_attn_ctx_bytes() exceeds RLK_NOALLOC_SCRATCH_BYTES
  *     return RLK_ERR_WORKSPACE before anything is launched.
- *   - The first call on a device looks up the array's device address on that
- *     (current) device; make that first call before any stream capture.
+ *   - Every call looks the array's device address up on the current device
+ *     (nothing is cached, so a reset device context leaves no stale
+ *     address); the first lookup on a device also loads the library's
+ *     device code there, so make the first call on each device before any
+ *     stream capture.
  *   - All calls share the one array and keep the last call's contents, so
  *     calls whose kernels overlap on the GPU (other streams, other host
  *     threads) race: serialise them. The context is not kept for a backward:
@@ -354,6 +359,25 @@ rlk_status rlk_attn_out_bias_gemm(const rlk_ja_shape* shape,
  * that bounded waits in the kernels set when they give up. Returns RLK_OK,
  * RLK_ERR_DEVICE_TIMEOUT, or RLK_ERR_CUDA if the stream reported an error. */
 rlk_status rlk_joint_attn_check_status(void* stream);
+
+/* Schedule of the fused forward's query tiles. It changes launch shape and
+ * time only, never a byte of the results. The forward runs one CTA per SM
+ * on pairs of 128-row query tiles of one (sample, head); by default the pairs
+ * past the last full wave of CTAs run as two single-tile CTAs each, which
+ * spreads the partial wave over twice the SMs.
+ *   RLK_FWD_TILES_AUTO    (0)  that default
+ *   RLK_FWD_TILES_PAIRS   (1)  every pair as one CTA
+ *   RLK_FWD_TILES_SINGLE  (2)  every query tile as its own CTA
+ * A query tile's arithmetic never depends on the tile it shares a CTA with,
+ * so all three give identical bytes; the setting exists so that this can be
+ * shown on any GPU, whatever its SM count. It is process-wide and applies to
+ * later calls of every entry point that runs the fused forward (the
+ * key-shard forward always runs pairs). Returns the previous policy, or -1
+ * (nothing changed) for an unknown one. */
+#define RLK_FWD_TILES_AUTO 0
+#define RLK_FWD_TILES_PAIRS 1
+#define RLK_FWD_TILES_SINGLE 2
+int32_t rlk_fwd_tile_schedule(int32_t policy);
 
 /* Self-test of the failure path: enqueues on `stream` one warp that waits,
  * through the same bounded mbarrier wait the kernels use, on a barrier that

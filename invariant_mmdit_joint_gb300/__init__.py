@@ -28,7 +28,7 @@ __all__ = [
     "rlk_op_trace_enable", "rlk_op_trace_count", "rlk_op_trace_read", "op_trace", "OP_TRACE_CAP",
     "rlk_joint_attn_state_bytes", "rlk_joint_attn_fwd_shard", "rlk_joint_attn_fwd_streams",
     "rlk_joint_attn_bwd_streams", "rlk_qkv_bias_gemm", "rlk_joint_attn_fwd_ctx",
-    "rlk_attn_out_bias_gemm", "rlk_selftest_wait_timeout",
+    "rlk_attn_out_bias_gemm", "rlk_selftest_wait_timeout", "rlk_fwd_tile_schedule", "FWD_TILES",
     "EXPORTED_SYMBOLS", "KERNEL_IDS",
 ]
 
@@ -62,6 +62,7 @@ EXPORTED_SYMBOLS = (
     "rlk_joint_attn_state_bytes", "rlk_joint_attn_fwd_shard",
     "rlk_joint_attn_fwd_streams", "rlk_joint_attn_bwd_streams", "rlk_qkv_bias_gemm",
     "rlk_joint_attn_fwd_ctx", "rlk_attn_out_bias_gemm", "rlk_selftest_wait_timeout",
+    "rlk_fwd_tile_schedule",
 )
 OP_TRACE_CAP = 256
 OP_TRACE_MAX_KERNELS = 8
@@ -164,6 +165,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     L.rlk_strict_math_compiled.restype = i32
     L.rlk_selftest_wait_timeout.argtypes = [i32, vp]
     L.rlk_selftest_wait_timeout.restype = i32
+    L.rlk_fwd_tile_schedule.argtypes = [i32]
+    L.rlk_fwd_tile_schedule.restype = i32
     L.rlk_joint_attn_trace.argtypes = [ctypes.POINTER(Trace)]
     L.rlk_joint_attn_trace.restype = i32
     L.rlk_strerror.argtypes = [i32]
@@ -446,6 +449,20 @@ def rlk_joint_attn_trace() -> dict:
     _check(lib().rlk_joint_attn_trace(ctypes.byref(t)), "rlk_joint_attn_trace")
     return {f: (getattr(t, f).decode() if isinstance(getattr(t, f), bytes) else getattr(t, f))
             for f, _ in Trace._fields_}
+
+
+FWD_TILES = {"auto": 0, "pairs": 1, "single": 2}
+
+
+def rlk_fwd_tile_schedule(policy: str) -> str:
+    """Set the fused forward's query-tile schedule ("auto", "pairs" or
+    "single"; time only, never bytes); returns the previous one."""
+    if policy not in FWD_TILES:
+        raise ValueError(f"unknown tile schedule {policy!r}")
+    prev = lib().rlk_fwd_tile_schedule(FWD_TILES[policy])
+    if prev < 0:
+        raise RuntimeError("rlk_fwd_tile_schedule refused the policy")
+    return {v: k for k, v in FWD_TILES.items()}[prev]
 
 
 def rlk_strerror(code: int) -> str:

@@ -29,6 +29,7 @@
 // Every wait is bounded; a wait that gives up records RLK_ERR_DEVICE_TIMEOUT
 // in the status word and the CTA drains its copies and MMAs and exits.
 #include <algorithm>
+#include <atomic>
 
 #include "rlk_device.cuh"
 #include "rlk_internal.h"
@@ -67,6 +68,9 @@ __device__ int g_status_fwd;
 // At the 1024^2 CFG pair (816 pairs on 152 SMs) splitting the last wave's 56
 // pairs gave 450 -> 442 us; 40 more changed nothing, 96 more cost 492 us.
 constexpr int kFwdSplitExtra = 0;
+
+// rlk_fwd_tile_schedule(): RLK_FWD_TILES_AUTO, _PAIRS or _SINGLE.
+std::atomic<int> g_tile_policy{RLK_FWD_TILES_AUTO};
 
 struct FwdArgs {
     CUtensorMap map_q;   // qh [B*H*S, 128] bf16, box 64 x 128
@@ -544,7 +548,10 @@ cudaError_t launch_attn_fwd(const Geom& g, const ValidLen& vl, const uint16_t* q
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const int rem = total % sms;
-    const int split = rem == 0 ? 0 : std::min(total, rem + kFwdSplitExtra);
+    int split = rem == 0 ? 0 : std::min(total, rem + kFwdSplitExtra);
+    const int policy = g_tile_policy.load();
+    if (policy == RLK_FWD_TILES_PAIRS) split = 0;
+    if (policy == RLK_FWD_TILES_SINGLE) split = total;
     local.n_keep = total - split;
     timing_begin(kKAttnFwd, s);
     attn_fwd_tc_kernel<false><<<(unsigned)(local.n_keep + 2 * split), kThreads, kSmemBytes, s>>>(local);
@@ -601,3 +608,8 @@ int read_and_clear_status_fwd(cudaStream_t s) {
 }
 
 }  // namespace rlk
+
+extern "C" int32_t rlk_fwd_tile_schedule(int32_t policy) {
+    if (policy != RLK_FWD_TILES_AUTO && policy != RLK_FWD_TILES_PAIRS && policy != RLK_FWD_TILES_SINGLE) return -1;
+    return rlk::g_tile_policy.exchange(policy);
+}

@@ -436,6 +436,38 @@ rlk_status bwd_core(const Geom& g, const ValidLen& vl, const SegBf16& q, const S
 }  // namespace
 }  // namespace rlk
 
+namespace rlk {
+
+rlk_status fwd_validate(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
+                        const float* g_q_txt, const float* g_k_txt, const float* g_q_img, const float* g_k_img,
+                        const int32_t* txt_valid_len, const void* out, const float* lse, const void* ctx,
+                        bool ctx_required, Geom* g, ValidLen* vl) {
+    rlk_status st = common_checks(shape, txt_valid_len, g, vl);
+    if (st != RLK_OK) return st;
+    // without a ctx argument the slot repeats q, which changes no outcome
+    const void* ptrs[] = {q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, out, ctx_required ? ctx : q};
+    for (const void* p : ptrs)
+        if (p == nullptr) return RLK_ERR_INVALID_ARG;
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return RLK_ERR_ALIGNMENT;
+    if (lse != nullptr && !aligned16(lse)) return RLK_ERR_ALIGNMENT;
+    return RLK_OK;
+}
+
+rlk_status device_check(void* stream) { return device_ok(stream); }
+
+rlk_status fwd_run(const Geom& g, const ValidLen& vl, const void* q, const void* k, const void* v,
+                   const float* g_q_txt, const float* g_k_txt, const float* g_q_img, const float* g_k_img,
+                   void* out, float* lse, void* ctx, void* stream) {
+    const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
+    return fwd_core(g, vl, seg_concat(q, g), seg_concat(k, g), seg_concat(v, g), gains, seg_concat(out, g), lse, ctx,
+                    static_cast<cudaStream_t>(stream));
+}
+
+size_t ctx_bytes_of(const Geom& g) { return ctx_layout(g).total; }
+
+}  // namespace rlk
+
 using namespace rlk;
 
 extern "C" {
@@ -458,20 +490,12 @@ static rlk_status rlk_joint_attn_fwd_impl(const rlk_ja_shape* shape, const void*
                               void* ctx, void* stream) {
     Geom g;
     ValidLen vl;
-    rlk_status st = common_checks(shape, txt_valid_len, &g, &vl);
+    rlk_status st = fwd_validate(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_valid_len, out, lse, ctx,
+                                 true, &g, &vl);
     if (st != RLK_OK) return st;
-    const void* ptrs[] = {q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, out, ctx};
-    for (const void* p : ptrs)
-        if (p == nullptr) return RLK_ERR_INVALID_ARG;
-    for (const void* p : ptrs)
-        if (!aligned16(p)) return RLK_ERR_ALIGNMENT;
-    if (lse != nullptr && !aligned16(lse)) return RLK_ERR_ALIGNMENT;
     st = device_ok(stream);
     if (st != RLK_OK) return st;
-
-    const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
-    return fwd_core(g, vl, seg_concat(q, g), seg_concat(k, g), seg_concat(v, g), gains, seg_concat(out, g), lse, ctx,
-                    static_cast<cudaStream_t>(stream));
+    return fwd_run(g, vl, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, out, lse, ctx, stream);
 }
 
 rlk_status rlk_joint_attn_fwd(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,

@@ -117,6 +117,26 @@ class OpScope {
     bool done_ = false;
 };
 
+// Forward entry-point steps (rlk_host.cu), shared by the regular and the
+// allocation-free forward so both refuse the same arguments with the same
+// status, in the same order:
+//   fwd_validate  shape, valid lengths, null and 16-byte alignment of every
+//                 pointer (ctx too when ctx_required; lse may be null);
+//                 touches no device
+//   device_check  the per-device check (sm_103, strict math); its first run
+//                 on a device launches probes and refuses a capturing stream
+//   fwd_run       the launches, on checked arguments
+rlk_status fwd_validate(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
+                        const float* g_q_txt, const float* g_k_txt, const float* g_q_img, const float* g_k_img,
+                        const int32_t* txt_valid_len, const void* out, const float* lse, const void* ctx,
+                        bool ctx_required, Geom* g, ValidLen* vl);
+rlk_status device_check(void* stream);
+rlk_status fwd_run(const Geom& g, const ValidLen& vl, const void* q, const void* k, const void* v,
+                   const float* g_q_txt, const float* g_k_txt, const float* g_q_img, const float* g_k_img,
+                   void* out, float* lse, void* ctx, void* stream);
+// Bytes of the forward context of a checked geometry.
+size_t ctx_bytes_of(const Geom& g);
+
 // ---- launchers (each returns the cudaGetLastError() of its launch) ----
 // k_prologue.cu
 cudaError_t launch_rope_table(const Geom& g, float2* tab, cudaStream_t s);

@@ -394,3 +394,61 @@ def test_joint_attention_checks_caller_supplied_buffers(L):
         ja.backward(x, x, x, gains, [11], x, x, lse, dg=torch.zeros((4, 127)))
     with pytest.raises(ValueError):
         ja.backward(x, x, x, gains, [11], x, x, torch.zeros((1, 2, 80), dtype=torch.float64))
+
+
+def _noalloc(L, s, vl, ptr=1 << 20, lse=1 << 20, **over):
+    p = dict(q=ptr, k=ptr, v=ptr, a=ptr, b=ptr, c=ptr, d=ptr, out=ptr)
+    p.update(over)
+    arr = (ctypes.c_int32 * len(vl))(*vl) if vl is not None else None
+    return L.rlk_joint_attn_fwd_noalloc(ctypes.byref(s) if s is not None else None, p["q"], p["k"], p["v"],
+                                        p["a"], p["b"], p["c"], p["d"], arr, p["out"], lse, None)
+
+
+def test_noalloc_refuses_what_the_regular_forward_refuses(L):
+    """The allocation-free forward runs the regular forward's checks first:
+    every refusal gives the same status on both entry points, before any
+    device work (the scratch address is looked up only after them)."""
+    s = pkg.Shape.make(2, 16, 8, 8, 2)
+    cases = [
+        (dict(), [3, 17]), (dict(), [-1, 3]),
+        (dict(q=None), [3, 3]), (dict(v=None), [3, 3]), (dict(d=None), [3, 3]), (dict(out=None), [3, 3]),
+        (dict(k=(1 << 20) + 8), [3, 3]), (dict(out=(1 << 20) + 2), [3, 3]), (dict(lse=(1 << 20) + 4), [3, 3]),
+        (dict(q=None, k=(1 << 20) + 8), [3, 3]),
+    ]
+    for over, vl in cases:
+        lse = over.pop("lse", 1 << 20)
+        a = _fwd(L, s, vl, lse=lse, **over)
+        b = _noalloc(L, s, vl, lse=lse, **over)
+        assert a == b and a != 0, (over, vl, a, b)
+    for mutate in (dict(D=64), dict(B=0), dict(grid_h=0), dict(eps=0.0), dict(axes=(16, 48, 64))):
+        base = dict(B=1, T_txt=16, grid_h=8, grid_w=8, H=2)
+        sh = pkg.Shape.make(**{**base, **{k: v for k, v in mutate.items() if k in base}},
+                            **{k: v for k, v in mutate.items() if k not in base})
+        assert _fwd(L, sh, [0]) == _noalloc(L, sh, [0]) != 0, mutate
+    assert L.rlk_joint_attn_fwd_noalloc(None, 0, 0, 0, 0, 0, 0, 0, None, 0, 0, None) == 1
+    assert _noalloc(L, s, None) == 1
+    # a shape beyond the fixed scratch is refused before the device check
+    big = pkg.Shape.make(2, 256, 64, 64, 24)
+    assert pkg.rlk_joint_attn_ctx_bytes(big) > (64 << 20)
+    assert _noalloc(L, big, [87, 193]) == 4
+    import torch
+    if not torch.cuda.is_available():
+        # a well-formed call reaches the device check on both entry points
+        assert _fwd(L, s, [3, 3]) == _noalloc(L, s, [3, 3]) == 5
+
+
+def test_forward_tile_schedule_setting(L):
+    """Three schedules are accepted and the previous one returned; an
+    unknown one changes nothing."""
+    prev = L.rlk_fwd_tile_schedule(1)
+    try:
+        assert L.rlk_fwd_tile_schedule(2) == 1
+        assert L.rlk_fwd_tile_schedule(7) == -1
+        assert L.rlk_fwd_tile_schedule(-1) == -1
+        assert L.rlk_fwd_tile_schedule(0) == 2
+        assert pkg.rlk_fwd_tile_schedule("pairs") == "auto"
+        assert pkg.rlk_fwd_tile_schedule("auto") == "pairs"
+        with pytest.raises(ValueError):
+            pkg.rlk_fwd_tile_schedule("halves")
+    finally:
+        L.rlk_fwd_tile_schedule(prev)

@@ -126,3 +126,36 @@ def test_head_composition_invariance(dev):
         for key in ("out", "dq", "dk", "dv"):
             assert Hh.bits_equal(r1[key][:, 0], res[key][:, h]), (h, key)
         assert Hh.bits_equal(r1["lse"][0], res["lse"][h]) and Hh.bits_equal(r1["dgp"][0], res["dgp"][h])
+
+
+@pytest.mark.parametrize("geom", [
+    dict(name="cfg1024_h5", B=2, H=5, T_txt=256, gh=64, gw=64, vl=(87, 193)),
+    dict(name="odd_tiles", B=3, H=2, T_txt=200, gh=13, gw=21, vl=(0, 130, 200)),
+], ids=lambda g: g["name"])
+def test_query_tile_schedule_never_changes_bytes(dev, geom):
+    """Every pair of query tiles as one CTA, every tile alone, and the default
+    mix give the same output bytes: a tile's arithmetic does not depend on
+    the tile it shares a CTA with, whatever the SM count."""
+    import torch
+
+    import invariant_mmdit_joint_gb300 as pkg
+    w = Hh.workload(geom["name"], geom["B"], geom["H"], geom["T_txt"], geom["gh"], geom["gw"], geom["vl"])
+    batch = W.make_batch(w, seed=6, with_dout=False)
+    q, k, v = (Hh.to_dev(batch[n], dev) for n in ("q", "k", "v"))
+    gains = torch.from_numpy(batch["gains"]).to(dev)
+    vl = [int(x) for x in batch["valid_len"]]
+    ja = pkg.JointAttention(w.B, w.T_txt, w.grid_h, w.grid_w, w.H, device=dev)
+    res = {}
+    prev = pkg.rlk_fwd_tile_schedule("auto")
+    try:
+        for policy in ("auto", "pairs", "single"):
+            pkg.rlk_fwd_tile_schedule(policy)
+            out, lse = ja.forward(q, k, v, gains, vl)
+            torch.cuda.synchronize()
+            res[policy] = (out.clone(), lse.clone())
+    finally:
+        pkg.rlk_fwd_tile_schedule(prev)
+    pkg.rlk_joint_attn_check_status()
+    for policy in ("pairs", "single"):
+        assert Hh.bits_equal(res[policy][0], res["auto"][0]), policy
+        assert Hh.bits_equal(res[policy][1], res["auto"][1]), policy
