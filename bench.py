@@ -386,6 +386,16 @@ def load_traffic(source_hash: str):
 
 
 # ---------------------------------------------------------------- our arm
+def selected_workload(args) -> W.Workload:
+    """The named workload; with --heads, the same shape on fewer heads (a
+    reduced case for profiler section captures, reported as such)."""
+    w = W.WORKLOADS[args.workload]
+    if getattr(args, "heads", None):
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}_h{args.heads}", H=int(args.heads))
+    return w
+
+
 def run_ours(args):
     import torch
 
@@ -398,7 +408,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = W.WORKLOADS[args.workload]
+    w = selected_workload(args)
     batch = W.make_batch(w, seed=0)
     flops = W.credited_flops(w)
 
@@ -803,7 +813,7 @@ def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
         return
-    w = W.WORKLOADS[args.workload]
+    w = selected_workload(args)
     batch = W.make_batch(w, seed=0)
     # size each step so the whole run stays within about two minutes
     per_step_budget = 120.0 / max(1, args.steps + args.warmup)
@@ -840,6 +850,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default="cfg1024")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="run the workload's shape on this many heads (a reduced profiling case)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true",

@@ -4,15 +4,16 @@
 //
 //   dkdv: one CTA = (key tile of 128, head, sample). Walks every query tile
 //         of 128 in one fixed ascending order (text tiles from token 0, then
-//         image tiles from token T_txt). Per query tile (dS^T is formed
-//         while dV computes, the next tile's P^T while dK computes):
+//         image tiles from token T_txt). Per query tile i:
 //           S^T  = K Q^T, dP^T = V dO^T            (tcgen05, A and B in smem)
 //           P^T  = exp2(S^T * c - lse2), dS^T = P^T * (dP^T - Delta)
 //                                                  (8 warps: key row = TMEM
 //                                                   lane, 64 queries each;
 //                                                   bf16 results into TMEM)
 //           dV  += P^T dO,  dK += dS^T Q           (tcgen05, A from TMEM)
-//         and stores the bf16 dS^T tile in the tensor cores' operand layout.
+//         in two alternating TMEM regions, so tile i + 1's scores and dP^T
+//         run while tile i's products finish; stores the bf16 dS^T tile in
+//         the tensor cores' operand layout.
 //   dq:   persistent; one unit = (query tile of 128, head, sample):
 //         dQ += dS K over the key tiles in the forward's order, reading the
 //         dS^T tiles back, so S and dP are computed once, not twice.
@@ -36,14 +37,11 @@ namespace {
 
 using namespace sm100;
 
-// warps 0-7: elementwise (warp w owns TMEM lane quarter w % 4 and the
-// column half w / 4 of each row; kEwWarps below); warp 8: TMA producer;
-// warps 9 and 10: MMA issuers of two independent chains (warp 9 owns TMEM).
-constexpr int kEwWarps = 8;                       // elementwise warps (16 measured 3% slower)
+// dK/dV warps 0-7: elementwise (warp w owns TMEM lane quarter w % 4 and the
+// column half w / 4 of each row); warp 8: TMA producer; warps 9 and 10: MMA
+// issuers of chains X and Y (warp 9 owns the TMEM allocation).
+constexpr int kEwWarps = 8;                       // elementwise warps
 constexpr int kEwThreads = 32 * kEwWarps;
-constexpr int kThreads = kEwThreads + 96;         // + TMA producer + two MMA issuers
-constexpr int kWarpTma = kEwWarps, kWarpMma = kEwWarps + 1;
-constexpr int kGroupCols = 128 / (kEwWarps / 4);  // query columns per elementwise warp
 constexpr int kBoxBytes = 128 * 128;       // 128 rows x 64 bf16
 constexpr int kTileBytes = 2 * kBoxBytes;  // 128 rows x 128 bf16
 constexpr uint32_t kTmemCols = 512;
@@ -97,19 +95,36 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
     return sdesc_sw128(tile + kk * 2048, kBoxBytes, 1024);
 }
 
-// TMEM column of the bf16 A operand (P or dS) for k-step kk: the column
-// half h = kk / 4 of the 128 fp32 columns is rewritten in place as 32 packed
-// columns at the start of that half, so the two warps sharing a lane
-// quarter never overwrite each other's unread scores.
-__device__ __forceinline__ uint32_t a_col(int kk) {
-    return (16 * kk / kGroupCols) * kGroupCols + (16 * kk % kGroupCols) / 2;
+// Two fp32 lanes at once (fma / sub / mul .rn.f32x2): each lane rounds
+// exactly as the scalar instruction does, in half the issue slots.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
 }
-// A warp's packed bf16 pairs of its columns, kGroupCols / 2 TMEM columns.
-__device__ __forceinline__ void tmem_st_packed(uint32_t taddr, const uint32_t (&r)[kGroupCols / 2]) {
-    if constexpr (kGroupCols == 64)
-        tmem_st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(&r[0]));
-    else
-        tmem_st16(taddr, *reinterpret_cast<const uint32_t(*)[16]>(&r[0]));
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    lo = __uint_as_float((uint32_t)v);
+    hi = __uint_as_float((uint32_t)(v >> 32));
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// 16-byte store of dS^T image data that skips L1 (the dQ kernel reads it
+// back through L2).
+__device__ __forceinline__ void st_image(uint8_t* p, uint4 v) {
+    asm volatile("st.global.L1::no_allocate.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
 }
 
 // dS^T tile image (128 keys x 128 queries, bf16, 32 KB): the non-swizzled
@@ -141,16 +156,47 @@ __device__ __forceinline__ void q_tile(const Geom& g, int i, int& q0, int& q_end
 }
 
 // ====================================================================== dK, dV
-constexpr int kKvSmemK = 0, kKvSmemV = kTileBytes, kKvSmemStage = 2 * kTileBytes;
-constexpr int kKvStageBytes = 2 * kTileBytes + 1024;  // Q, dO, lse2[128], delta[128]
-constexpr int kKvSmemBytes = kKvSmemStage + 2 * kKvStageBytes + 1024;
-constexpr uint32_t kColDV = 0, kColDK = 128, kColST = 256, kColDPT = 384;
+// TMEM: dV [0, 128), dK [128, 256) and two 128-column regions R_0, R_1 at 256
+// and 384, used by query tiles alternately (tile i in R_{i & 1}). In its
+// region a tile's S^T lands first; once the elementwise warps have read it,
+// dP^T is computed into the same columns; the warps then write the bf16 P^T
+// and dS^T there (each warp into the columns its own dP^T came from), and
+// dV and dK take them as their A operands. Two issuing threads on different
+// SMSPs (so neither SMSP's elementwise warps carry all the issue work):
+//   chain Y: S^T_0, S^T_1, dP^T_0; per tile i: dP^T_{i+1} (once the warps
+//            have read S^T_{i+1}), then S^T_{i+2} into R_{i & 1} (once
+//            chain X reports dV_i and dK_i complete there);
+//   chain X: per tile i: dV_i and dK_i (once P^T_i and dS^T_i are written),
+//            then a commit that frees R_{i & 1}.
+// So the next tile's scores are ready before its warps need them, and the
+// warps form P^T_{i+1} while dV_i, dK_i and dP^T_{i+1} run.
+// Shared memory: K, V, three Q slots (Q_i is still read by dK_i when
+// S^T_{i+2} needs Q_{i+2}) and two dO slots, each with its tile's lse2 and
+// Delta; no static shared memory (the barriers sit in the alignment slack
+// or after the tiles). A slot frees on chain X's commit: every product
+// reading it has been issued by then, the S^T and dP^T ones completed
+// before the warps formed that tile's P^T and dS^T.
+constexpr int kKvWarps = kEwWarps + 3;                // + TMA producer + two MMA issuers
+constexpr int kKvThreads = 32 * kKvWarps;
+constexpr int kKvWarpTma = kEwWarps, kKvWarpMma = kEwWarps + 1, kKvWarpMma2 = kEwWarps + 2;
+constexpr int kKvQSlots = 3, kKvOSlots = 2;
+constexpr int kKvSmemK = 0, kKvSmemV = kTileBytes, kKvSmemQ = 2 * kTileBytes;
+constexpr int kKvSmemO = kKvSmemQ + kKvQSlots * kTileBytes;
+constexpr int kKvSmemL = kKvSmemO + kKvOSlots * kTileBytes;   // lse2[128], delta[128] per dO slot
+constexpr int kKvSmemBar = kKvSmemL + kKvOSlots * 1024;
+constexpr int kKvBarBytes = 256;
+constexpr int kKvSmemBytes = kKvSmemBar + 1024;  // + alignment slack (holds the barriers when it can)
+static_assert(kKvSmemBytes <= 232448, "dK/dV shared memory exceeds the per-block limit");
+constexpr uint32_t kColDV = 0, kColDK = 128, kColR = 256;
+constexpr int kEwCols = 128 / (kEwWarps / 4);  // query / output columns per elementwise warp
+// bf16 A operand of k-step kk (queries 16 kk .. 16 kk + 15) in a region:
+// warp group g = kk / 4 owns fp32 columns [64 g, 64 g + 64) and rewrites
+// them as 32 packed P^T columns, then 32 packed dS^T columns
+__device__ __forceinline__ uint32_t p_col(int kk) { return 64u * (kk >> 2) + 8u * (kk & 3); }
+__device__ __forceinline__ uint32_t ds_col(int kk) { return 64u * (kk >> 2) + 32u + 8u * (kk & 3); }
 
-__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[12];  // bars[9]: second issuer's drain
-    __shared__ uint32_t tmem_slot;
-    __shared__ volatile int abort_flag;
 
     const Geom& g = a.g;
     const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -168,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
 
     if (k0 >= kvalid_end) {  // every key of the tile is masked: exact zeros
         const int rows = min(128, seg_end - k0);
-        for (int i = tid; i < rows * 16; i += kThreads) {
+        for (int i = tid; i < rows * 16; i += kKvThreads) {
             const int r = i >> 4, c = i & 15;
             *reinterpret_cast<uint4*>(seg_row(a.dv, g, b, k0 + r, h) + c * 8) = make_uint4(0, 0, 0, 0);
             float4* dst = reinterpret_cast<float4*>(dkh + (size_t)(k0 + r) * kHeadDim + c * 8);
@@ -178,48 +224,67 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
         return;
     }
 
-    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sraw = smem_u32(smem_raw);
+    const uint32_t sbase = (sraw + 1023u) & ~1023u;
+    // barriers: in the slack below the tiles when it is large enough, else
+    // after the lse2 / Delta slots (the request covers either case)
+    const uint32_t sbar = (sbase - sraw >= (uint32_t)kKvBarBytes) ? sraw : sbase + kKvSmemBar;
+    uint8_t* const bar_gen = smem_raw + (sbar - sraw);
+    volatile int& abort_flag = *reinterpret_cast<volatile int*>(bar_gen + 240);
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bar_gen + 244);
     const uint32_t sK = sbase + kKvSmemK, sV = sbase + kKvSmemV;
-    auto stage_q = [&](int s) { return sbase + kKvSmemStage + s * kKvStageBytes; };
-    auto stage_o = [&](int s) { return stage_q(s) + kTileBytes; };
-    auto stage_l = [&](int s) { return stage_q(s) + 2 * kTileBytes; };
-    const uint32_t bar_kv = smem_u32(&bars[0]);
-    const uint32_t bar_full = smem_u32(&bars[1]);   // [2]
-    const uint32_t bar_empty = smem_u32(&bars[3]);  // [2]
-    const uint32_t bar_st = smem_u32(&bars[5]);   // S^T_i computed
-    const uint32_t bar_dpt = smem_u32(&bars[6]);  // dP^T_i computed
-    const uint32_t bar_p = smem_u32(&bars[10]);   // P^T_i written (bf16)
-    const uint32_t bar_ds = smem_u32(&bars[11]);  // dS^T_i written (bf16)
-    const uint32_t bar_done = smem_u32(&bars[7]);
-    const uint32_t bar_drain = smem_u32(&bars[8]);
+    auto slot_q = [&](int i) { return sbase + kKvSmemQ + (uint32_t)(i % kKvQSlots) * kTileBytes; };
+    auto slot_o = [&](int i) { return sbase + kKvSmemO + (uint32_t)(i & 1) * kTileBytes; };
+    auto slot_l = [&](int i) { return sbase + kKvSmemL + (uint32_t)(i & 1) * 1024u; };
+    const uint32_t bar_kv = sbar;
+    const uint32_t bar_qf = sbar + 8;        // [3] Q slot landed
+    const uint32_t bar_qe = sbar + 32;       // [3] Q slot read by every product
+    const uint32_t bar_of = sbar + 56;       // [2] dO slot (+ lse2, Delta) landed
+    const uint32_t bar_oe = sbar + 72;       // [2] dO slot free
+    const uint32_t bar_st = sbar + 88;       // [2] S^T of the region's tile computed
+    const uint32_t bar_sr = sbar + 104;      // [2] S^T read by the warps (kEwThreads arrivals)
+    const uint32_t bar_dp = sbar + 120;      // [2] dP^T computed
+    const uint32_t bar_pds = sbar + 136;     // [2] P^T and dS^T written (kEwThreads arrivals)
+    const uint32_t bar_done = sbar + 152;
+    const uint32_t bar_drain = sbar + 160;   // [2]
+    const uint32_t bar_rf = sbar + 176;      // [2] region consumed by dV and dK
 
     if (tid == 0) {
         abort_flag = 0;
         mbar_init(bar_kv, 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 2);  // one commit per issuer
+        for (int j = 0; j < kKvQSlots; ++j) {
+            mbar_init(bar_qf + 8 * j, 1);
+            mbar_init(bar_qe + 8 * j, 1);
         }
-        mbar_init(bar_st, 1);
-        mbar_init(bar_dpt, 1);
-        mbar_init(bar_p, kEwThreads);
-        mbar_init(bar_ds, kEwThreads);
-        mbar_init(bar_done, 2);
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(bar_of + 8 * j, 1);
+            mbar_init(bar_oe + 8 * j, 1);
+            mbar_init(bar_st + 8 * j, 1);
+            mbar_init(bar_sr + 8 * j, kEwThreads);
+            mbar_init(bar_dp + 8 * j, 1);
+            mbar_init(bar_pds + 8 * j, kEwThreads);
+        }
+        mbar_init(bar_done, 1);
         mbar_init(bar_drain, 1);
-        mbar_init(smem_u32(&bars[9]), 1);
+        mbar_init(bar_drain + 8, 1);
+        mbar_init(bar_rf, 1);
+        mbar_init(bar_rf + 8, 1);
         fence_barrier_init();
     }
-    if (warp == kWarpMma) {
-        tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+    if (warp == kKvWarpMma) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = tmem_slot;
+    const uint32_t tmem = *tmem_slot;
 
-    if (warp == kWarpTma) {
+    if (warp == kKvWarpTma) {
         // ------------------------------------------------ TMA producer
+        // In order: K, V; then per query tile i its Q slot (free once dK_{i-3}
+        // has run) and its dO slot with lse2 and Delta (free once dV_{i-2}
+        // has run, which follows the warps' last read of that tile).
         if (lane == 0) {
             prefetch_tensormap(&a.map_q);
             prefetch_tensormap(&a.map_k);
@@ -236,209 +301,242 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
             tma_load_4d(sV + kBoxBytes, &a.map_v[vseg], bar_kv, 64, h, vrow, b);
             int issued = 0;
             for (int i = 0; i < nq && !abort_flag; ++i) {
-                const int s = i & 1;
-                if (i >= 2 && !mbar_wait(bar_empty + 8 * s, ((i >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                const int jq = i % kKvQSlots, jo = i & 1;
+                int q0, q_end;
+                q_tile(g, i, q0, q_end);
+                if (i >= kKvQSlots && !mbar_wait(bar_qe + 8 * jq, ((i / kKvQSlots) + 1) & 1, &abort_flag, kWaitLimitNs)) {
                     fail(&abort_flag);
                     break;
                 }
-                int q0, q_end;
-                q_tile(g, i, q0, q_end);
-                const uint32_t bf = bar_full + 8 * s;
-                mbar_expect_tx(bf, 2 * kTileBytes + 1024);
-                tma_load_2d(stage_q(s), &a.map_q, bf, 0, row_base + q0);
-                tma_load_2d(stage_q(s) + kBoxBytes, &a.map_q, bf, 64, row_base + q0);
+                const uint32_t bq = bar_qf + 8 * jq;
+                mbar_expect_tx(bq, kTileBytes);
+                tma_load_2d(slot_q(i), &a.map_q, bq, 0, row_base + q0);
+                tma_load_2d(slot_q(i) + kBoxBytes, &a.map_q, bq, 64, row_base + q0);
+                if (i >= 2 && !mbar_wait(bar_oe + 8 * jo, ((i >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                    fail(&abort_flag);
+                    break;
+                }
+                const uint32_t bo = bar_of + 8 * jo;
+                mbar_expect_tx(bo, kTileBytes + 1024);
                 const int oseg = i < g.ntq_txt ? 0 : 1, orow = oseg ? q0 - g.T_txt : q0;
-                tma_load_4d(stage_o(s), &a.map_do[oseg], bf, 0, h, orow, b);
-                tma_load_4d(stage_o(s) + kBoxBytes, &a.map_do[oseg], bf, 64, h, orow, b);
+                tma_load_4d(slot_o(i), &a.map_do[oseg], bo, 0, h, orow, b);
+                tma_load_4d(slot_o(i) + kBoxBytes, &a.map_do[oseg], bo, 64, h, orow, b);
                 const size_t slot = bh * g.nq_pad + (size_t)i * 128;
-                bulk_load(stage_l(s), a.lse2_p + slot, 512, bf);
-                bulk_load(stage_l(s) + 512, a.delta_p + slot, 512, bf);
+                bulk_load(slot_l(i), a.lse2_p + slot, 512, bo);
+                bulk_load(slot_l(i) + 512, a.delta_p + slot, 512, bo);
                 issued = i + 1;
             }
+            // leave no copy in flight
             const volatile int no_abort = 0;
             mbar_wait(bar_kv, 0, &no_abort, kWaitLimitNs);
+            for (int i = issued - kKvQSlots < 0 ? 0 : issued - kKvQSlots; i < issued; ++i)
+                mbar_wait(bar_qf + 8 * (i % kKvQSlots), (i / kKvQSlots) & 1, &no_abort, kWaitLimitNs);
             for (int i = issued - 2 < 0 ? 0 : issued - 2; i < issued; ++i)
-                mbar_wait(bar_full + 8 * (i & 1), (i >> 1) & 1, &no_abort, kWaitLimitNs);
+                mbar_wait(bar_of + 8 * (i & 1), (i >> 1) & 1, &no_abort, kWaitLimitNs);
         }
-    } else if (warp == kWarpMma || warp == kWarpMma + 1) {
-        // ------------------------------------------------ MMA issuers
-        // Two independent chains, one issuing thread each, so that one keeps
-        // the tensor pipe fed while the other waits on a barrier:
-        //   warp 9:  S^T_0; per query tile i: dV_i (after P^T_i), then
-        //            S^T_{i+1} (after stage i+1 lands). S^T_{i+1} overwrites
-        //            the columns holding P^T_i, which dV_i, issued before it
-        //            on the same thread, has consumed.
-        //   warp 10: per query tile i: dP^T_i, then dK_i (after dS^T_i).
-        //            dP^T_{i+1} overwrites dS^T_i after dK_i, likewise.
-        // The two write disjoint TMEM columns; a stage frees when both have
-        // issued their last product reading it.
+    } else if (warp == kKvWarpMma || warp == kKvWarpMma2) {
+        // ------------------------------------------------ MMA issuers (chains X, Y)
         if (lane == 0) {
-            const bool chain_p = warp == kWarpMma;
-            const uint32_t bar_my_drain = chain_p ? bar_drain : smem_u32(&bars[9]);
-            auto issue_st = [&](int i) {
+            const bool chain_y = warp == kKvWarpMma2;
+            auto issue_scores = [&](int i, bool dp) {
+                const uint32_t at = dp ? sV : sK, bt = dp ? slot_o(i) : slot_q(i);
+                const uint32_t d = tmem + kColR + 128u * (uint32_t)(i & 1);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kColST, desc_kmajor(sK, kk), desc_kmajor(stage_q(i & 1), kk), kIdescKK, kk > 0);
-                mma_commit(bar_st);
+                    mma_ss(d, desc_kmajor(at, kk), desc_kmajor(bt, kk), kIdescKK, kk > 0);
+                mma_commit((dp ? bar_dp : bar_st) + 8 * (i & 1));
             };
             bool ok = mbar_wait(bar_kv, 0, &abort_flag, kWaitLimitNs);
-            if (chain_p) {
-                ok = ok && mbar_wait(bar_full, 0, &abort_flag, kWaitLimitNs);
+            if (chain_y) {
+                ok = ok && mbar_wait(bar_qf, 0, &abort_flag, kWaitLimitNs);
                 if (ok) {
                     tc_fence_after();
-                    issue_st(0);
+                    issue_scores(0, false);
+                }
+                if (ok && nq > 1) {
+                    ok = mbar_wait(bar_qf + 8, 0, &abort_flag, kWaitLimitNs);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_scores(1, false);
+                    }
+                }
+                ok = ok && mbar_wait(bar_sr, 0, &abort_flag, kWaitLimitNs) && mbar_wait(bar_of, 0, &abort_flag, kWaitLimitNs);
+                if (ok) {
+                    tc_fence_after();
+                    issue_scores(0, true);
                 }
                 for (int i = 0; ok && i < nq; ++i) {
-                    const int s = i & 1;
-                    if (!mbar_wait(bar_p, i & 1, &abort_flag, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tmem + kColDV, tmem + kColST + a_col(kk), desc_mnmajor(stage_o(s), kk), kIdescKM,
-                               (i > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(bar_empty + 8 * s);
+                    const int r = i & 1;
                     if (i + 1 < nq) {
-                        if (!mbar_wait(bar_full + 8 * (s ^ 1), ((i + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                        if (!mbar_wait(bar_sr + 8 * (r ^ 1), ((i + 1) >> 1) & 1, &abort_flag, kWaitLimitNs) ||
+                            !mbar_wait(bar_of + 8 * ((i + 1) & 1), ((i + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        issue_st(i + 1);
+                        issue_scores(i + 1, true);
+                    }
+                    if (i + 2 < nq) {
+                        if (!mbar_wait(bar_rf + 8 * r, (i >> 1) & 1, &abort_flag, kWaitLimitNs) ||
+                            !mbar_wait(bar_qf + 8 * ((i + 2) % kKvQSlots), ((i + 2) / kKvQSlots) & 1, &abort_flag,
+                                       kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_scores(i + 2, false);
                     }
                 }
             } else {
                 for (int i = 0; ok && i < nq; ++i) {
-                    const int s = i & 1;
-                    if (!mbar_wait(bar_full + 8 * s, (i >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                    const int r = i & 1;
+                    const uint32_t reg = tmem + kColR + 128u * (uint32_t)r;
+                    if (!mbar_wait(bar_pds + 8 * r, (i >> 1) & 1, &abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tmem + kColDPT, desc_kmajor(sV, kk), desc_kmajor(stage_o(s), kk), kIdescKK, kk > 0);
-                    mma_commit(bar_dpt);
-                    if (!mbar_wait(bar_ds, i & 1, &abort_flag, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tmem + kColDK, tmem + kColDPT + a_col(kk), desc_mnmajor(stage_q(s), kk), kIdescKM,
+                        mma_ts(tmem + kColDV, reg + p_col(kk), desc_mnmajor(slot_o(i), kk), kIdescKM,
                                (i > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(bar_empty + 8 * s);
+                    mma_commit(bar_oe + 8 * (i & 1));
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tmem + kColDK, reg + ds_col(kk), desc_mnmajor(slot_q(i), kk), kIdescKM,
+                               (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar_qe + 8 * (i % kKvQSlots));
+                    mma_commit(bar_rf + 8 * r);
                 }
+                if (ok) mma_commit(bar_done);
             }
-            if (ok)
-                mma_commit(bar_done);
-            else
-                fail(&abort_flag);
-            mma_commit(bar_my_drain);
+            if (!ok) fail(&abort_flag);
+            const uint32_t my_drain = bar_drain + (chain_y ? 8 : 0);
+            mma_commit(my_drain);
             const volatile int no_abort = 0;
-            mbar_wait(bar_my_drain, 0, &no_abort, kWaitLimitNs);
+            mbar_wait(my_drain, 0, &no_abort, kWaitLimitNs);
         }
     } else {
         // ------------------------------------------------ elementwise warps
         // warp w: key rows 32 * (w % 4) + lane, query columns
-        // [kGroupCols * grp, kGroupCols * (grp + 1)), grp = w / 4. No row
+        // [kEwCols * grp, kEwCols * (grp + 1)), grp = w / 4. No row
         // reduction: every element of P^T and dS^T is the thread's own.
         const int lq = warp & 3, grp = warp >> 2;
         const uint32_t lane_addr = (uint32_t)(lq * 32) << 16;
         const int kr = lq * 32 + lane;
-        const int c0 = kGroupCols * grp;
+        const int c0 = kEwCols * grp;
         const bool kvalid = k0 + kr < kvalid_end;
         bool ok = true;
+        uint32_t pkd[kEwCols / 2];  // dS^T of the previous tile, packed, for its image
+        uint8_t* ds_prev = nullptr;
         for (int i = 0; i < nq; ++i) {
-            const int s = i & 1;
-            if (!warp_wait(bar_full + 8 * s, (i >> 1) & 1, &abort_flag) || !warp_wait(bar_st, i & 1, &abort_flag)) {
+            const int r = i & 1;
+            const uint32_t reg = tmem + lane_addr + kColR + 128u * (uint32_t)r + c0;
+            if (!warp_wait(bar_st + 8 * r, (i >> 1) & 1, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float4* l2v =
-                reinterpret_cast<const float4*>(smem_raw + (stage_l(s) - smem_u32(smem_raw))) + c0 / 4;
+            uint32_t rs[kEwCols];
+#pragma unroll
+            for (int c = 0; c < kEwCols; c += 32)
+                tmem_ld32(reg + c, *reinterpret_cast<uint32_t(*)[32]>(&rs[c]));
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(bar_sr + 8 * r);
+            if (!warp_wait(bar_of + 8 * (i & 1), (i >> 1) & 1, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            const float4* l2v = reinterpret_cast<const float4*>(smem_raw + (slot_l(i) - sraw)) + c0 / 4;
             const float4* dlv = l2v + 32;
             // P^T = exp2(S^T * c - lse2[query]) (masked keys: 0), kept in fp32 for dS
-            uint32_t rs[kGroupCols];
-#pragma unroll
-            for (int c = 0; c < kGroupCols; c += 32)
-                tmem_ld32(tmem + lane_addr + kColST + c0 + c, *reinterpret_cast<uint32_t(*)[32]>(&rs[c]));
-            tmem_ld_wait();
-            float pf[kGroupCols];
-            uint32_t pk[kGroupCols / 2];
+            float pf[kEwCols];
             if (kvalid) {  // the row's key is valid for the whole CTA: no per-element select
 #pragma unroll
-                for (int e4 = 0; e4 < kGroupCols / 4; ++e4) {
+                for (int e4 = 0; e4 < kEwCols / 4; ++e4) {
                     const float4 l4 = l2v[e4];
                     const float lq4[4] = {l4.x, l4.y, l4.z, l4.w};
+                    float x[4];
+                    f2_unpack(fma_f2(f2_pack(__uint_as_float(rs[4 * e4]), __uint_as_float(rs[4 * e4 + 1])),
+                                     f2_pack(kC, kC), f2_pack(-lq4[0], -lq4[1])), x[0], x[1]);
+                    f2_unpack(fma_f2(f2_pack(__uint_as_float(rs[4 * e4 + 2]), __uint_as_float(rs[4 * e4 + 3])),
+                                     f2_pack(kC, kC), f2_pack(-lq4[2], -lq4[3])), x[2], x[3]);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        pf[4 * e4 + u] = exp2_num(fmaf(__uint_as_float(rs[4 * e4 + u]), kC, -lq4[u]));
-                    pk[2 * e4] = pack_bf16(pf[4 * e4], pf[4 * e4 + 1]);
-                    pk[2 * e4 + 1] = pack_bf16(pf[4 * e4 + 2], pf[4 * e4 + 3]);
+                    for (int u = 0; u < 4; ++u) pf[4 * e4 + u] = exp2_num(x[u]);
                 }
             } else {  // a masked key: P = 0
 #pragma unroll
-                for (int e = 0; e < kGroupCols; ++e) pf[e] = 0.0f;
-#pragma unroll
-                for (int e = 0; e < kGroupCols / 2; ++e) pk[e] = 0u;
+                for (int e = 0; e < kEwCols; ++e) pf[e] = 0.0f;
             }
-            tmem_st_packed(tmem + lane_addr + kColST + c0, pk);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar_p);
+            // the previous tile's bf16 dS^T into its (query tile, key tile kt)
+            // image for the dQ product (see ds_image_offset), while dP^T_i
+            // computes: a warp's store of one query chunk covers 512
+            // contiguous bytes
+            if (ds_prev != nullptr) {
+#pragma unroll
+                for (int c = 0; c < kEwCols / 8; ++c)
+                    st_image(ds_prev + c * kDsChunkBytes, make_uint4(pkd[4 * c], pkd[4 * c + 1], pkd[4 * c + 2], pkd[4 * c + 3]));
+            }
             // dS^T = P^T * (dP^T - Delta[query])
-            if (!warp_wait(bar_dpt, i & 1, &abort_flag)) {
+            if (!warp_wait(bar_dp + 8 * r, (i >> 1) & 1, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t rd[kGroupCols];
+            // two chunks of 32 columns; once a chunk's dP^T is in registers its
+            // columns take the packed P^T (chunk 0) or dS^T (chunk 1)
 #pragma unroll
-            for (int c = 0; c < kGroupCols; c += 32)
-                tmem_ld32(tmem + lane_addr + kColDPT + c0 + c, *reinterpret_cast<uint32_t(*)[32]>(&rd[c]));
-            tmem_ld_wait();
+            for (int c = 0; c < kEwCols; c += 32) {
+                uint32_t rd[32];
+                tmem_ld32(reg + c, rd);
+                tmem_ld_wait();
+                if (c == 0) {
+                    uint32_t pkp[kEwCols / 2];
 #pragma unroll
-            for (int e4 = 0; e4 < kGroupCols / 4; ++e4) {
-                const float4 d4 = dlv[e4];
-                const float dq4[4] = {d4.x, d4.y, d4.z, d4.w};
-                float ds[4];
+                    for (int e = 0; e < kEwCols / 2; ++e) pkp[e] = pack_bf16(pf[2 * e], pf[2 * e + 1]);
+                    tmem_st32(reg, *reinterpret_cast<const uint32_t(*)[32]>(&pkp[0]));
+                }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) ds[u] = pf[4 * e4 + u] * (__uint_as_float(rd[4 * e4 + u]) - dq4[u]);
-                pk[2 * e4] = pack_bf16(ds[0], ds[1]);
-                pk[2 * e4 + 1] = pack_bf16(ds[2], ds[3]);
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const float4 d4 = dlv[c / 4 + e4];
+                    const float dq4[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float ds[4];
+#pragma unroll
+                    for (int u = 0; u < 4; u += 2)
+                        f2_unpack(mul_f2(f2_pack(pf[c + 4 * e4 + u], pf[c + 4 * e4 + u + 1]),
+                                         sub_f2(f2_pack(__uint_as_float(rd[4 * e4 + u]), __uint_as_float(rd[4 * e4 + u + 1])),
+                                                f2_pack(dq4[u], dq4[u + 1]))),
+                                  ds[u], ds[u + 1]);
+                    pkd[c / 2 + 2 * e4] = pack_bf16(ds[0], ds[1]);
+                    pkd[c / 2 + 2 * e4 + 1] = pack_bf16(ds[2], ds[3]);
+                }
             }
-            tmem_st_packed(tmem + lane_addr + kColDPT + c0, pk);
+            tmem_st32(reg + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pkd[0]));
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar_ds);
-            // the same bf16 dS^T row into the (query tile i, key tile kt)
-            // image for the dQ product (see ds_image_offset): a warp's
-            // store of one query chunk covers 512 contiguous bytes
-            uint8_t* ds_img = a.ds_tiles + ((bh * nq + i) * nq + kt) * (size_t)kTileBytes + ds_image_offset(c0, kr);
+            mbar_arrive(bar_pds + 8 * r);
+            ds_prev = a.ds_tiles + ((bh * nq + i) * nq + kt) * (size_t)kTileBytes + ds_image_offset(c0, kr);
+        }
+        if (ok && ds_prev != nullptr) {
 #pragma unroll
-            for (int c = 0; c < kGroupCols / 8; ++c)
-                *reinterpret_cast<uint4*>(ds_img + c * kDsChunkBytes) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            for (int c = 0; c < kEwCols / 8; ++c)
+                st_image(ds_prev + c * kDsChunkBytes, make_uint4(pkd[4 * c], pkd[4 * c + 1], pkd[4 * c + 2], pkd[4 * c + 3]));
         }
         if (ok && warp_wait(bar_done, 0, &abort_flag)) {
             tc_fence_after();
             // Stage dV (bf16) and dK (fp32, times 1/sqrt(D)) in the K, V and
-            // first Q buffers (every product has finished) as six 128-row x
+            // first Q slots (every product has finished) as six 128-row x
             // 128-byte boxes in the 128-byte-swizzled layout of the output
             // maps: dV boxes 0-1 (64 columns each), dK boxes 2-5 (32 columns
             // each). One thread then stores the tile with TMA; the segment
             // maps clip rows past the key's segment. Masked keys get zeros.
-            uint8_t* stg = smem_raw + (sbase - smem_u32(smem_raw));
+            uint8_t* stg = smem_raw + (sbase - sraw);
             const int sw = kr & 7;
 #pragma unroll 1
-            for (int c = 0; c < kGroupCols; c += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_addr + kColDV + c0 + c, r);
+            for (int c = 0; c < kEwCols; c += 32) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + lane_addr + kColDV + c0 + c, rr);
                 tmem_ld_wait();
                 // dV box (c0 + c) / 64, 16-byte chunks from ((c0 + c) % 64) / 8
                 uint8_t* dvrow = stg + ((c0 + c) >> 6) * kBoxBytes + kr * 128;
@@ -447,21 +545,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        w[e] = kvalid ? pack_bf16(__uint_as_float(r[8 * q + 2 * e]), __uint_as_float(r[8 * q + 2 * e + 1]))
+                        w[e] = kvalid ? pack_bf16(__uint_as_float(rr[8 * q + 2 * e]), __uint_as_float(rr[8 * q + 2 * e + 1]))
                                       : 0u;
                     *reinterpret_cast<uint4*>(dvrow + (((((c0 + c) & 63) >> 3) + q) ^ sw) * 16) =
                         make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                tmem_ld32(tmem + lane_addr + kColDK + c0 + c, r);
+                tmem_ld32(tmem + lane_addr + kColDK + c0 + c, rr);
                 tmem_ld_wait();
                 uint8_t* dkrow = stg + (2 + ((c0 + c) >> 5)) * kBoxBytes + kr * 128;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     float4 f;
-                    f.x = kvalid ? __uint_as_float(r[4 * q]) * kScale : 0.0f;
-                    f.y = kvalid ? __uint_as_float(r[4 * q + 1]) * kScale : 0.0f;
-                    f.z = kvalid ? __uint_as_float(r[4 * q + 2]) * kScale : 0.0f;
-                    f.w = kvalid ? __uint_as_float(r[4 * q + 3]) * kScale : 0.0f;
+                    f.x = kvalid ? __uint_as_float(rr[4 * q]) * kScale : 0.0f;
+                    f.y = kvalid ? __uint_as_float(rr[4 * q + 1]) * kScale : 0.0f;
+                    f.z = kvalid ? __uint_as_float(rr[4 * q + 2]) * kScale : 0.0f;
+                    f.w = kvalid ? __uint_as_float(rr[4 * q + 3]) * kScale : 0.0f;
                     *reinterpret_cast<float4*>(dkrow + ((q ^ sw) << 4)) = f;
                 }
             }
@@ -484,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_tc_kernel(const __g
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == kKvWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -724,7 +822,7 @@ cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16
     if (e != cudaSuccess) return e;
     dim3 grid(g.ntq_txt + g.ntq_img, g.H, g.B);
     timing_begin(kKBwdDkDv, s);
-    attn_bwd_dkdv_tc_kernel<<<grid, kThreads, kKvSmemBytes, s>>>(args);
+    attn_bwd_dkdv_tc_kernel<<<grid, kKvThreads, kKvSmemBytes, s>>>(args);
     timing_end(kKBwdDkDv, s);
     return cudaGetLastError();
 }
