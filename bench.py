@@ -50,7 +50,9 @@ from invariant_mmdit_joint_gb300 import workloads as W  # noqa: E402
 
 METRIC = "joint-attn fwd+bwd TFLOP/s and % of BF16 tensor peak at 1024² (4096 img+256 txt)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-LAUNCHES_PER_STEP = 9  # fwd: table, prologue, attention; bwd: pre, dkdv, dq, key norm/rope, 2 folds
+# fwd: table, prologue, attention; bwd: pre, key norm/rope, 2 folds, and a
+# dK/dV + dQ pair per workspace group (one group with the full workspace)
+LAUNCHES_FIXED, LAUNCHES_PER_GROUP = 7, 2
 THROTTLE_BITS = {
     0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
     0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
@@ -421,7 +423,15 @@ def run_ours(args):
     q, k, v, do = (t.to(dev) for t in (h_q, h_k, h_v, h_do))
     gains = h_g.to(dev)
     vl = [int(x) for x in batch["valid_len"]]
-    ja = pkg.JointAttention(w.B, w.T_txt, w.grid_h, w.grid_w, w.H, device=dev)
+    budget = None if args.ws_budget_gb is None else int(args.ws_budget_gb * 1e9)
+    ja = pkg.JointAttention(w.B, w.T_txt, w.grid_h, w.grid_w, w.H, device=dev, ws_budget_bytes=budget)
+    ws_full = pkg.rlk_joint_attn_bwd_workspace_bytes(ja.shape)
+    ws_min = pkg.rlk_joint_attn_bwd_workspace_min_bytes(ja.shape)
+    per_pair = (ws_full - ws_min) // max(1, w.B * w.H - 1) if w.B * w.H > 1 else 0
+    ws_bytes = ja.workspace.numel()
+    pairs_per_group = w.B * w.H if ws_bytes >= ws_full else 1 + (ws_bytes - ws_min) // per_pair
+    workspace = {"bytes": ws_bytes, "full_bytes": ws_full, "min_bytes": ws_min, "pairs_per_group": pairs_per_group,
+                 "groups": -(-(w.B * w.H) // pairs_per_group)}
     out = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -678,6 +688,7 @@ def run_ours(args):
         "l2": "inputs larger than L2 (no flush): q,k,v,dO total "
               f"{(4 * w.B * w.S * w.H * 128 * 2) / 1e6:.0f} MB, plus ctx and workspace, against 129 MB of L2",
         "roofline": roofline, "kernels": per_kernel, "phases": phases, "dense_convention": dense,
+        "workspace": workspace,
         "unfused_forward": unfused, "qkv_producer": qkv, "shards_and_streams": rows23,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 4),
@@ -690,7 +701,7 @@ def run_ours(args):
         "graph": {"value": round(job_throughput(flops["fwd_bwd"], world, ms_graph), 2), "unit": "TFLOP/s",
                   "ms_per_step": round(ms_graph, 4), "bytes_equal_to_eager": graph_bytes_equal,
                   "what": "the forward+backward step captured once into a CUDA graph and replayed"},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": (LAUNCHES_FIXED + LAUNCHES_PER_GROUP * workspace["groups"]) * args.steps,
         "clocks": clocks,
         "backend": trace["backend"], "fingerprint": trace["fingerprint"],
     }
@@ -852,6 +863,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default="cfg1024")
     ap.add_argument("--heads", type=int, default=None,
                     help="run the workload's shape on this many heads (a reduced profiling case)")
+    ap.add_argument("--ws-budget-gb", type=float, default=None,
+                    help="cap the backward workspace (the backward then runs its (sample, head) pairs in groups)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true",

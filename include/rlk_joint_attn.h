@@ -83,7 +83,7 @@ typedef enum rlk_status {
     RLK_ERR_INVALID_ARG = 1,   /* null pointer, bad size, L_b outside [0, T_txt] */
     RLK_ERR_UNSUPPORTED = 2,   /* D != 128, axes != {16,56,56}, not sm_103, fast-math build */
     RLK_ERR_ALIGNMENT = 3,     /* a device pointer not 16-byte aligned */
-    RLK_ERR_WORKSPACE = 4,     /* workspace smaller than rlk_joint_attn_bwd_workspace_bytes() */
+    RLK_ERR_WORKSPACE = 4,     /* workspace below rlk_joint_attn_bwd_workspace_min_bytes() */
     RLK_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
     RLK_ERR_DEVICE_TIMEOUT = 6 /* a bounded device-side wait gave up (see check_status) */
 } rlk_status;
@@ -121,6 +121,17 @@ size_t rlk_joint_attn_ctx_bytes(const rlk_ja_shape* shape);
  * ceil(grid_h * grid_w / 128); 1.8 GB for B = 2, H = 24 at 1024 x 1024).
  * Returns 0 for an invalid shape. */
 size_t rlk_joint_attn_bwd_workspace_bytes(const rlk_ja_shape* shape);
+
+/* The smallest backward workspace: everything above but the dS tiles of a
+ * single (sample, head) pair (n_tiles^2 * 32 KiB; 37.9 MB at 1024 x 1024,
+ * 52.4 MB at 1328 x 1328). A backward given less than
+ * rlk_joint_attn_bwd_workspace_bytes() but at least this runs its dK/dV and
+ * dQ kernels over consecutive groups of (sample, head) pairs, in b * H + h
+ * order, each group as large as the dS tiles the workspace holds, reusing
+ * the one region; the results are byte-identical to the single-group run (a
+ * pair's arithmetic never depends on its group), only the launch count and
+ * the time change. Returns 0 for an invalid shape. */
+size_t rlk_joint_attn_bwd_workspace_min_bytes(const rlk_ja_shape* shape);
 
 /* Forward: rows qk_rmsnorm, multi_axis_rope, joint_attn_qk_gemm,
  * joint_attn_softmax and joint_attn_av_gemm of the RFC's WS1 table, fused.
@@ -186,7 +197,10 @@ rlk_status rlk_joint_attn_fwd_noalloc(const rlk_ja_shape* shape,
  *                   a fixed order; these are batch invariant
  *   dg              device fp32 [4, D], written: dg_partial summed over h
  *                   ascending, then over b ascending
- *   workspace       device scratch of >= rlk_joint_attn_bwd_workspace_bytes()
+ *   workspace       device scratch of >= rlk_joint_attn_bwd_workspace_min_bytes()
+ *                   (rlk_joint_attn_bwd_workspace_bytes() runs every pair in
+ *                   one group; less runs the pairs in groups, same bytes);
+ *                   below the minimum: RLK_ERR_WORKSPACE, nothing launched
  * Note: a padded text query row with nonzero dout feeds the key and value
  * gradients of the valid keys, as the mathematics says. */
 rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape,

@@ -19,7 +19,7 @@ from typing import Sequence
 
 __all__ = [
     "Shape", "RlkError", "lib", "library_path", "load_library",
-    "rlk_joint_attn_ctx_bytes", "rlk_joint_attn_bwd_workspace_bytes",
+    "rlk_joint_attn_ctx_bytes", "rlk_joint_attn_bwd_workspace_bytes", "rlk_joint_attn_bwd_workspace_min_bytes",
     "rlk_joint_attn_fwd", "rlk_joint_attn_bwd", "rlk_joint_attn_check_status",
     "rlk_strict_math_compiled", "rlk_joint_attn_trace", "rlk_strerror",
     "rlk_kernel_timing", "rlk_kernel_timing_read", "rlk_joint_attn_fwd_noalloc",
@@ -52,7 +52,7 @@ KERNEL_IDS = {
 UNFUSED = {"scores": 0, "p": 1, "alpha": 2, "rows": 3}
 # Every symbol include/rlk_joint_attn.h declares.
 EXPORTED_SYMBOLS = (
-    "rlk_joint_attn_ctx_bytes", "rlk_joint_attn_bwd_workspace_bytes",
+    "rlk_joint_attn_ctx_bytes", "rlk_joint_attn_bwd_workspace_bytes", "rlk_joint_attn_bwd_workspace_min_bytes",
     "rlk_joint_attn_fwd", "rlk_joint_attn_bwd", "rlk_joint_attn_check_status",
     "rlk_strict_math_compiled", "rlk_joint_attn_trace", "rlk_strerror",
     "rlk_kernel_timing", "rlk_kernel_timing_read", "rlk_joint_attn_fwd_noalloc",
@@ -153,6 +153,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     L.rlk_joint_attn_ctx_bytes.restype = sz
     L.rlk_joint_attn_bwd_workspace_bytes.argtypes = [shp]
     L.rlk_joint_attn_bwd_workspace_bytes.restype = sz
+    L.rlk_joint_attn_bwd_workspace_min_bytes.argtypes = [shp]
+    L.rlk_joint_attn_bwd_workspace_min_bytes.restype = sz
     L.rlk_joint_attn_fwd.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_int32),
                                      vp, vp, vp, vp]
     L.rlk_joint_attn_fwd.restype = i32
@@ -263,6 +265,10 @@ def rlk_joint_attn_ctx_bytes(shape: Shape) -> int:
 
 def rlk_joint_attn_bwd_workspace_bytes(shape: Shape) -> int:
     return int(lib().rlk_joint_attn_bwd_workspace_bytes(ctypes.byref(shape)))
+
+
+def rlk_joint_attn_bwd_workspace_min_bytes(shape: Shape) -> int:
+    return int(lib().rlk_joint_attn_bwd_workspace_min_bytes(ctypes.byref(shape)))
 
 
 def rlk_joint_attn_fwd(shape, q, k, v, g_q_txt, g_k_txt, g_q_img, g_k_img, txt_valid_len,
@@ -486,7 +492,10 @@ class JointAttention:
     CUDA tensors; gains a float32 [4, 128] tensor (q_txt, k_txt, q_img, k_img)."""
 
     def __init__(self, B: int, T_txt: int, grid_h: int, grid_w: int, H: int, device="cuda",
-                 eps: float = 1e-6, theta: float = 10000.0):
+                 eps: float = 1e-6, theta: float = 10000.0, ws_budget_bytes: int | None = None):
+        """ws_budget_bytes caps the backward workspace: with less than the
+        full size the backward runs its (sample, head) pairs in groups (same
+        bytes, more launches); below the minimum it raises."""
         import torch
         self.shape = Shape.make(B, T_txt, grid_h, grid_w, H, eps=eps, theta=theta)
         self.device = torch.device(device)
@@ -494,6 +503,11 @@ class JointAttention:
         n_ws = rlk_joint_attn_bwd_workspace_bytes(self.shape)
         if n_ctx == 0 or n_ws == 0:
             raise RlkError(1, "JointAttention: invalid shape")
+        if ws_budget_bytes is not None:
+            n_min = rlk_joint_attn_bwd_workspace_min_bytes(self.shape)
+            if ws_budget_bytes < n_min:
+                raise RlkError(4, f"JointAttention: workspace budget {ws_budget_bytes} below the minimum {n_min}")
+            n_ws = min(n_ws, int(ws_budget_bytes))
         self.ctx = torch.empty(n_ctx, dtype=torch.uint8, device=self.device)
         self.workspace = torch.empty(n_ws, dtype=torch.uint8, device=self.device)
 

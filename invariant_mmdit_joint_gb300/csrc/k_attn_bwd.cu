@@ -63,7 +63,10 @@ struct BwdArgs {
     const float* lse2_p;  // [B, H, nq_pad]
     const float* delta_p; // [B, H, nq_pad]
     SegBf16 dv;           // [B, S, H, 128] (text rows, image rows)
-    uint8_t* ds_tiles;    // [B, H, nq, nq] images of 32 KB (query tile major)
+    uint8_t* ds_tiles;    // [n_pairs, nq, nq] images of 32 KB (query tile major)
+    // the (sample, head) pairs of this launch: bh0 .. bh0 + n_pairs - 1 in
+    // b * H + h order; the images are indexed from bh0
+    int bh0, n_pairs;
     // output maps per segment (0 text, 1 image) so a tile's rows past its
     // segment are clipped: dV [B, S, H, 128] bf16, dk^ [B*H, S, 128] fp32
     CUtensorMap map_dv[2];
@@ -199,7 +202,8 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc_kernel(const _
     extern __shared__ uint8_t smem_raw[];
 
     const Geom& g = a.g;
-    const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int kt = blockIdx.x, pair = blockIdx.y;  // pair: within this launch's range
+    const int h = (a.bh0 + pair) % g.H, b = (a.bh0 + pair) / g.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool k_txt = kt < g.ntq_txt;
     const int k0 = k_txt ? kt * 128 : g.T_txt + (kt - g.ntq_txt) * 128;
@@ -516,7 +520,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc_kernel(const _
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_pds + 8 * r);
-            ds_prev = a.ds_tiles + ((bh * nq + i) * nq + kt) * (size_t)kTileBytes + ds_image_offset(c0, kr);
+            ds_prev = a.ds_tiles + (((size_t)pair * nq + i) * nq + kt) * (size_t)kTileBytes + ds_image_offset(c0, kr);
         }
         if (ok && ds_prev != nullptr) {
 #pragma unroll
@@ -605,16 +609,18 @@ constexpr uint32_t kDqTmemCols = 256;
 constexpr uint32_t kIdescMM = idesc_bf16(128, 128, true, true);
 
 struct DqUnit {
-    int qt, h, b;
+    int qt, h, b, pair;  // pair: within the launch's range (indexes the images)
 };
-// Units run from the last (sample, head) down: the dK/dV kernel's last CTAs
-// wrote those dS^T images, some still in L2 (317.0 -> 313.6 us measured).
-__device__ __forceinline__ DqUnit dq_unit(const Geom& g, int nq, int u) {
+// Units run from the last (sample, head) of the range down: the dK/dV
+// kernel's last CTAs wrote those dS^T images, some still in L2 (317.0 ->
+// 313.6 us measured).
+__device__ __forceinline__ DqUnit dq_unit(const BwdArgs& a, int nq, int u) {
     DqUnit r;
-    u = nq * g.H * g.B - 1 - u;
+    u = nq * a.n_pairs - 1 - u;
     r.qt = u % nq;
-    r.h = (u / nq) % g.H;
-    r.b = u / (nq * g.H);
+    r.pair = u / nq;
+    r.h = (a.bh0 + r.pair) % a.g.H;
+    r.b = (a.bh0 + r.pair) / a.g.H;
     return r;
 }
 
@@ -627,7 +633,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc_kernel(const __g
     const Geom& g = a.g;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nq = g.ntq_txt + g.ntq_img;
-    const int n_units = nq * g.H * g.B;
+    const int n_units = nq * a.n_pairs;
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     auto stage = [&](int s) { return sbase + s * kDqStageBytes; };
     const uint32_t bar_full = smem_u32(&bars[0]);                   // [3] stage loaded
@@ -665,13 +671,13 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc_kernel(const __g
             int t = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < n_units && !abort_flag; u += gridDim.x) {
-                const DqUnit w = dq_unit(g, nq, u);
+                const DqUnit w = dq_unit(a, nq, u);
                 const int L = a.vl.L[w.b];
                 const int nkt_txt = (L + 127) / 128;
                 const int nkt = nkt_txt + g.ntq_img;
                 const size_t bh = (size_t)w.b * g.H + w.h;
                 const int row_base = (int)(bh * g.S);
-                const uint8_t* tiles = a.ds_tiles + (bh * nq + w.qt) * nq * (size_t)kTileBytes;
+                const uint8_t* tiles = a.ds_tiles + ((size_t)w.pair * nq + w.qt) * nq * (size_t)kTileBytes;
                 for (int j = 0; j < nkt; ++j, ++t) {
                     const int s = t % kDqStages;
                     if (t >= kDqStages &&
@@ -699,7 +705,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc_kernel(const __g
             int t = 0, n = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++n) {
-                const DqUnit w = dq_unit(g, nq, u);
+                const DqUnit w = dq_unit(a, nq, u);
                 const int nkt = (a.vl.L[w.b] + 127) / 128 + g.ntq_img;
                 const int buf = n & 1;
                 if (n >= 2 && !mbar_wait(bar_free + 8 * buf, ((n >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
@@ -738,7 +744,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc_kernel(const __g
         int n = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++n) {
-            const DqUnit w = dq_unit(g, nq, u);
+            const DqUnit w = dq_unit(a, nq, u);
             const int buf = n & 1;
             if (!warp_wait(bar_acc + 8 * buf, (n >> 1) & 1, &abort_flag)) {
                 ok = false;
@@ -808,9 +814,13 @@ void set_norm_rope_io(BwdArgs* a, const NormRopeBwdIo& nr) {
 
 cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh,
                                  const SegBf16& v, const SegBf16& dout, const float* lse2_p, const float* delta_p,
-                                 const SegBf16& dv, float* dkh, uint8_t* ds_tiles, cudaStream_t s) {
+                                 const SegBf16& dv, float* dkh, uint8_t* ds_tiles, int bh0, int n_pairs,
+                                 cudaStream_t s) {
     BwdArgs args;
     if (!make_args(&args, g, vl, qh, kh, v, dout, lse2_p, delta_p)) return cudaErrorInvalidValue;
+    if (bh0 < 0 || n_pairs < 1 || bh0 + n_pairs > g.B * g.H) return cudaErrorInvalidValue;
+    args.bh0 = bh0;
+    args.n_pairs = n_pairs;
     args.dv = dv;
     args.dkh = dkh;
     args.ds_tiles = ds_tiles;
@@ -820,7 +830,7 @@ cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16
     cudaError_t e =
         cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(g.ntq_txt + g.ntq_img, g.H, g.B);
+    dim3 grid(g.ntq_txt + g.ntq_img, n_pairs);
     timing_begin(kKBwdDkDv, s);
     attn_bwd_dkdv_tc_kernel<<<grid, kKvThreads, kKvSmemBytes, s>>>(args);
     timing_end(kKBwdDkDv, s);
@@ -828,9 +838,12 @@ cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16
 }
 
 cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t* kh, const uint8_t* ds_tiles,
-                               const NormRopeBwdIo& nr, cudaStream_t s) {
+                               const NormRopeBwdIo& nr, int bh0, int n_pairs, cudaStream_t s) {
     BwdArgs args;
     if (!tmap::rows_bf16(&args.map_k, kh, (uint64_t)g.B * g.H * g.S)) return cudaErrorInvalidValue;
+    if (bh0 < 0 || n_pairs < 1 || bh0 + n_pairs > g.B * g.H) return cudaErrorInvalidValue;
+    args.bh0 = bh0;
+    args.n_pairs = n_pairs;
     args.g = g;
     args.vl = vl;
     args.ds_tiles = const_cast<uint8_t*>(ds_tiles);
@@ -841,7 +854,7 @@ cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmemBytes);
     if (e != cudaSuccess) return e;
-    const int n_units = (g.ntq_txt + g.ntq_img) * g.H * g.B;
+    const int n_units = (g.ntq_txt + g.ntq_img) * n_pairs;
     const int grid = n_units < sms ? n_units : sms;
     timing_begin(kKBwdDq, s);
     attn_bwd_dq_tc_kernel<<<grid, kDqThreads, kDqSmemBytes, s>>>(args);

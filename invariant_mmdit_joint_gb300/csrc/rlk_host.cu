@@ -102,8 +102,11 @@ CtxLayout ctx_layout(const Geom& g) {
 
 struct WsLayout {
     size_t lse2, delta, dkh, dgt, dgp, dst, total;
+    size_t image_pair;  // bytes of one (sample, head) pair's dS^T images
 };
-WsLayout ws_layout(const Geom& g) {
+// The workspace with room for the dS^T images of image_pairs (sample, head)
+// pairs (all B * H by default: one dK/dV and one dQ launch).
+WsLayout ws_layout(const Geom& g, long long image_pairs = -1) {
     const size_t rows = (size_t)g.B * g.H * g.S;
     const size_t slots = (size_t)g.B * g.H * g.nq_pad;
     const size_t ntiles = (size_t)g.ntq_txt + g.ntq_img;
@@ -117,7 +120,9 @@ WsLayout ws_layout(const Geom& g) {
     l.dgp = align_up(l.dgt + (size_t)g.B * g.H * 2 * ntiles * 4 * kHeadDim * 4);
     // bf16 dS^T tile images, one 32 KB image per (query tile, key tile)
     l.dst = align_up(l.dgp + (size_t)g.B * g.H * 4 * kHeadDim * 4);
-    l.total = align_up(l.dst + (size_t)g.B * g.H * ntiles * ntiles * 32768);
+    l.image_pair = ntiles * ntiles * 32768;
+    const size_t pairs = image_pairs < 0 ? (size_t)g.B * g.H : (size_t)image_pairs;
+    l.total = align_up(l.dst + pairs * l.image_pair);
     return l;
 }
 
@@ -211,7 +216,7 @@ rlk_status fwd_core(const Geom& g, const ValidLen& vl, const SegBf16& q, const S
 rlk_status bwd_core(const Geom& g, const ValidLen& vl, const SegBf16& q, const SegBf16& k, const SegBf16& v,
                     const float* const gains[4], const SegBf16& out, const SegBf16& dout, const float* lse,
                     const void* ctx, const SegBf16& dq, const SegBf16& dk, const SegBf16& dv, float* dg_partial,
-                    float* dg, void* workspace, cudaStream_t s);
+                    float* dg, void* workspace, size_t workspace_bytes, cudaStream_t s);
 
 // Sizes of the standalone operators' intermediates.// Sizes of the standalone operators' intermediates.
 size_t unfused_bytes(const Geom& g, int which) {
@@ -407,7 +412,7 @@ namespace {
 rlk_status bwd_core(const Geom& g, const ValidLen& vl, const SegBf16& q, const SegBf16& k, const SegBf16& v,
                     const float* const gains[4], const SegBf16& out, const SegBf16& dout, const float* lse,
                     const void* ctx, const SegBf16& dq, const SegBf16& dk, const SegBf16& dv, float* dg_partial,
-                    float* dg, void* workspace, cudaStream_t s) {
+                    float* dg, void* workspace, size_t workspace_bytes, cudaStream_t s) {
     const CtxLayout l = ctx_layout(g);
     const WsLayout w = ws_layout(g);
     const uint8_t* c = static_cast<const uint8_t*>(ctx);
@@ -425,9 +430,18 @@ rlk_status bwd_core(const Geom& g, const ValidLen& vl, const SegBf16& q, const S
     uint8_t* ds_tiles = ws + w.dst;
     const NormRopeBwdIo nr{q, dq, rq, {gains[0], gains[1], gains[2], gains[3]}, tab, dgt};
     if (launch_bwd_pre(g, out, dout, lse, lse2_p, delta_p, s) != cudaSuccess) return RLK_ERR_CUDA;
-    if (launch_attn_bwd_dkdv(g, vl, qh, kh, v, dout, lse2_p, delta_p, dv, dkh, ds_tiles, s) != cudaSuccess)
-        return RLK_ERR_CUDA;
-    if (launch_attn_bwd_dq(g, vl, kh, ds_tiles, nr, s) != cudaSuccess) return RLK_ERR_CUDA;
+    // dK/dV then dQ over consecutive groups of (sample, head) pairs, as many
+    // per group as the workspace holds images for (every pair at once when
+    // it holds them all); a pair's arithmetic never depends on its group
+    const int n_pairs = g.B * g.H;
+    const int group = (int)std::min<size_t>((size_t)n_pairs, (workspace_bytes - w.dst) / w.image_pair);
+    for (int bh0 = 0; bh0 < n_pairs; bh0 += group) {
+        const int n = std::min(group, n_pairs - bh0);
+        if (launch_attn_bwd_dkdv(g, vl, qh, kh, v, dout, lse2_p, delta_p, dv, dkh, ds_tiles, bh0, n, s) !=
+            cudaSuccess)
+            return RLK_ERR_CUDA;
+        if (launch_attn_bwd_dq(g, vl, kh, ds_tiles, nr, bh0, n, s) != cudaSuccess) return RLK_ERR_CUDA;
+    }
     if (launch_norm_rope_bwd_k(g, k, gains[1], gains[3], tab, rk, dkh, dk, dgt, s) != cudaSuccess)
         return RLK_ERR_CUDA;
     if (launch_dg_fold(g, dgt, dgp, dg, s) != cudaSuccess) return RLK_ERR_CUDA;
@@ -484,6 +498,12 @@ size_t rlk_joint_attn_bwd_workspace_bytes(const rlk_ja_shape* shape) {
     return ws_layout(make_geom(shape)).total;
 }
 
+size_t rlk_joint_attn_bwd_workspace_min_bytes(const rlk_ja_shape* shape) {
+    rlk_status why;
+    if (!shape_ok(shape, &why)) return 0;
+    return ws_layout(make_geom(shape), 1).total;
+}
+
 static rlk_status rlk_joint_attn_fwd_impl(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
                               const float* g_q_txt, const float* g_k_txt, const float* g_q_img,
                               const float* g_k_img, const int32_t* txt_valid_len, void* out, float* lse,
@@ -524,15 +544,14 @@ static rlk_status rlk_joint_attn_bwd_impl(const rlk_ja_shape* shape, const void*
     for (const void* p : ptrs)
         if (!aligned16(p)) return RLK_ERR_ALIGNMENT;
     if (dg_partial != nullptr && !aligned16(dg_partial)) return RLK_ERR_ALIGNMENT;
-    const WsLayout w = ws_layout(g);
-    if (workspace_bytes < w.total) return RLK_ERR_WORKSPACE;
+    if (workspace_bytes < ws_layout(g, 1).total) return RLK_ERR_WORKSPACE;
     st = device_ok(stream);
     if (st != RLK_OK) return st;
 
     const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
     return bwd_core(g, vl, seg_concat(q, g), seg_concat(k, g), seg_concat(v, g), gains, seg_concat(out, g),
                     seg_concat(dout, g), lse, ctx, seg_concat(dq, g), seg_concat(dk, g), seg_concat(dv, g), dg_partial,
-                    dg, workspace, static_cast<cudaStream_t>(stream));
+                    dg, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape, const void* q, const void* k, const void* v,
@@ -605,14 +624,14 @@ static rlk_status rlk_joint_attn_bwd_streams_impl(
     if (st != RLK_OK) return st;
     st = check_ptrs({g_q_txt, g_k_txt, g_q_img, g_k_img, lse, ctx, dg, workspace}, {dg_partial});
     if (st != RLK_OK) return st;
-    if (workspace_bytes < ws_layout(g).total) return RLK_ERR_WORKSPACE;
+    if (workspace_bytes < ws_layout(g, 1).total) return RLK_ERR_WORKSPACE;
     st = device_ok(stream);
     if (st != RLK_OK) return st;
     const float* gains[4] = {g_q_txt, g_k_txt, g_q_img, g_k_img};
     return bwd_core(g, vl, seg_split(q_txt, q_img, g), seg_split(k_txt, k_img, g), seg_split(v_txt, v_img, g), gains,
                     seg_split(out_txt, out_img, g), seg_split(dout_txt, dout_img, g), lse, ctx,
                     seg_split(dq_txt, dq_img, g), seg_split(dk_txt, dk_img, g), seg_split(dv_txt, dv_img, g),
-                    dg_partial, dg, workspace, static_cast<cudaStream_t>(stream));
+                    dg_partial, dg, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 rlk_status rlk_joint_attn_bwd_streams(const rlk_ja_shape* shape, const void* q_txt, const void* q_img,

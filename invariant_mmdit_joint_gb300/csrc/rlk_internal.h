@@ -188,13 +188,16 @@ struct NormRopeBwdIo {
 };
 // dkh: dk^ (the gradient of the rotated, normalised keys, times 1/sqrt(128)),
 // fp32 [B, H, S, 128], written by dkdv and read by norm_rope_bwd_k.
+// Both run over the (sample, head) pairs bh0 .. bh0 + n_pairs - 1 (b * H + h
+// order); ds_tiles holds the n_pairs x nq x nq dS^T images of that range.
 cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16_t* qh,
                                  const uint16_t* kh, const SegBf16& v,
                                  const SegBf16& dout, const float* lse2_p,
                                  const float* delta_p, const SegBf16& dv, float* dkh,
-                                 uint8_t* ds_tiles, cudaStream_t s);
+                                 uint8_t* ds_tiles, int bh0, int n_pairs, cudaStream_t s);
 cudaError_t launch_attn_bwd_dq(const Geom& g, const ValidLen& vl, const uint16_t* kh,
-                               const uint8_t* ds_tiles, const NormRopeBwdIo& nr, cudaStream_t s);
+                               const uint8_t* ds_tiles, const NormRopeBwdIo& nr, int bh0, int n_pairs,
+                               cudaStream_t s);
 int probe_bwd_tu(void);
 int read_and_clear_status_bwd(cudaStream_t s);
 

@@ -111,15 +111,31 @@ def test_argument_checks_fail_closed_without_a_gpu(L):
 
 
 def test_backward_checks_workspace_size(L):
-    s = pkg.Shape.make(1, 16, 8, 8, 2)
-    need = pkg.rlk_joint_attn_bwd_workspace_bytes(s)
+    """Below the minimum (one (sample, head) pair's dS tiles) the backward
+    refuses before any launch; from the minimum up it reaches the device
+    check (on this machine: no GPU)."""
+    s = pkg.Shape.make(2, 16, 8, 8, 3)
+    full = pkg.rlk_joint_attn_bwd_workspace_bytes(s)
+    least = pkg.rlk_joint_attn_bwd_workspace_min_bytes(s)
+    nt = 1 + 1
+    assert full - least == (2 * 3 - 1) * nt * nt * 32768
     p = 1 << 20
-    vl = (ctypes.c_int32 * 1)(4)
-    rc = L.rlk_joint_attn_bwd(ctypes.byref(s), p, p, p, p, p, p, p, vl, p, p, p, p, p, p, p, None, p, p,
-                              need - 1, None)
-    assert rc == 4
+    vl = (ctypes.c_int32 * 2)(4, 9)
+
+    def bwd(n):
+        return L.rlk_joint_attn_bwd(ctypes.byref(s), p, p, p, p, p, p, p, vl, p, p, p, p, p, p, p, None, p, p,
+                                    n, None)
+    assert bwd(least - 1) == 4
+    import torch
+    if not torch.cuda.is_available():
+        assert bwd(least) == 5 and bwd(full) == 5
+    assert pkg.rlk_joint_attn_bwd_workspace_min_bytes(pkg.Shape.make(1, 16, 8, 8, 2, D=64)) == 0
+    # 1024^2: one pair's 34 x 34 tiles of 32 KiB above the fixed part
+    big = pkg.Shape.make(2, 256, 64, 64, 24)
+    assert (pkg.rlk_joint_attn_bwd_workspace_bytes(big) - pkg.rlk_joint_attn_bwd_workspace_min_bytes(big)
+            == 47 * 34 * 34 * 32768)
     rc = L.rlk_joint_attn_bwd(ctypes.byref(s), p, p, p, p, p, p, p, vl, p, p, None, p, p, p, p, None, p, p,
-                              need, None)
+                              full, None)
     assert rc == 1  # lse is required by the backward
 
 
@@ -321,11 +337,12 @@ def test_stream_pair_calls_fail_closed(L):
     no_text = pkg.Shape.make(2, 0, 8, 8, 2)
     zero = (ctypes.c_int32 * 2)(0, 0)
     ws = pkg.rlk_joint_attn_bwd_workspace_bytes(s)
+    least = pkg.rlk_joint_attn_bwd_workspace_min_bytes(s)
 
     def bwd(wsb=ws, dvt=p):
         return L.rlk_joint_attn_bwd_streams(ctypes.byref(s), p, p, p, p, p, p, p, p, p, p, vl, p, p, p, p, p, p,
                                             p, p, p, p, dvt, p, None, p, p, wsb, None)
-    assert bwd(wsb=ws - 1) == 4
+    assert bwd(wsb=least - 1) == 4
     assert bwd(dvt=None) == 1
     import torch
     if not torch.cuda.is_available():
