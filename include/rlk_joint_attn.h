@@ -251,6 +251,12 @@ rlk_status rlk_joint_attn_bwd(const rlk_ja_shape* shape,
 #define RLK_UNFUSED_P 1
 #define RLK_UNFUSED_ALPHA 2
 #define RLK_UNFUSED_ROWS 3 /* one of l or lse */
+/* the standalone backward's intermediates (see rlk_joint_attn_softmax_bwd()) */
+#define RLK_UNFUSED_DP 4         /* dP, fp32, the layout of `scores` */
+#define RLK_UNFUSED_DS 5         /* P or dS, bf16, the layout of P */
+#define RLK_UNFUSED_STATS 6      /* lse2 and Delta, fp32 [2][B, H, n_tiles * 128] */
+#define RLK_UNFUSED_DHAT 7       /* dq^ or dk^, fp32 [B, H, S, D] */
+#define RLK_UNFUSED_GAIN_TILES 8 /* gain-gradient partials, fp32 [B, H, 2, n_tiles, 4, D] */
 
 /* Bytes of one intermediate (`which` = RLK_UNFUSED_*); 0 for an invalid
  * shape or `which`. 3.6 GB of scores for B = 2, H = 24 at 1024 x 1024. */
@@ -283,6 +289,69 @@ rlk_status rlk_joint_attn_av_gemm(const rlk_ja_shape* shape, const void* p,
                                   const float* alpha, const float* l, const void* v,
                                   const int32_t* txt_valid_len, void* out,
                                   void* stream);
+
+/* ---------------------------------------------------------------------------
+ * The backward of the same operators, one call per row, byte-equal in
+ * composition to rlk_joint_attn_bwd(): the RFC #386 WS1 table marks every
+ * attention row "fwd + bwd", and the fused backward's bytes are those of
+ *     rlk_joint_attn_bwd_stats -> rlk_joint_attn_softmax_bwd (P)
+ *       -> rlk_joint_attn_av_gemm_bwd (dV, dP)
+ *       -> rlk_joint_attn_softmax_bwd (dS)
+ *       -> rlk_joint_attn_qk_gemm_bwd (dq^, dk^)
+ *       -> rlk_qk_norm_rope_bwd (dQ, dK, gain gradients)
+ * run after the forward operators above (or the fused forward) on the same
+ * inputs: dq, dk, dv, dg_partial and dg are identical to the fused call's.
+ * Each step repeats the fused backward's arithmetic in its order (tiles of
+ * 128, k-steps of 16, the same roundings); the products are taken with the
+ * query index first where the fused kernel takes the key index first, which
+ * gives the same bits on the tensor cores.
+ * Intermediates (sizes from rlk_joint_attn_unfused_bytes()):
+ *   stats  fp32: lse2 = lse * log2(e) [B, H, n_tiles * 128] (one 128-slot
+ *          block per query tile, +inf past a segment), then Delta =
+ *          rowsum(dO * O) in the same layout (0 past a segment)
+ *   P, dS  bf16, the layout of the forward's P (visited key blocks only):
+ *          P = exp2(s * log2(e) / sqrt(128) - lse2), the normalised
+ *          probability (not the forward's lazily rescaled one); dS =
+ *          P * (dP - Delta) with P in fp32; masked keys: P = 0
+ *   dP     fp32, the layout of `scores`: dO V^T, every key of a visited
+ *          block (masked ones too)
+ *   dq^, dk^  fp32 [B, H, S, D]: dS k^ / sqrt(128) and dS^T q^ / sqrt(128)
+ *          (masked keys: 0)
+ * Pointer rules, errors and streams are those of the fused calls. */
+
+/* lse2 and Delta into `stats` (the fused backward's preprocess). */
+rlk_status rlk_joint_attn_bwd_stats(const rlk_ja_shape* shape, const void* out, const void* dout,
+                                    const float* lse, float* stats, void* stream);
+
+/* Row joint_attn_softmax, backward. With dp NULL: P from `scores` and
+ * `stats` into p (required). With dp given: dS into ds (required), and P
+ * into p if p is not NULL. */
+rlk_status rlk_joint_attn_softmax_bwd(const rlk_ja_shape* shape, const float* scores, const float* stats,
+                                      const float* dp, const int32_t* txt_valid_len, void* p, void* ds,
+                                      void* stream);
+
+/* Row joint_attn_av_gemm, backward: dP = dO V^T into dp and dV = P^T dO
+ * (bf16 [B, S, H, D], masked keys 0) into dv; either may be NULL (not
+ * both); p (from rlk_joint_attn_softmax_bwd) is required with dv. */
+rlk_status rlk_joint_attn_av_gemm_bwd(const rlk_ja_shape* shape, const void* p, const void* v,
+                                      const void* dout, const int32_t* txt_valid_len, void* dv,
+                                      float* dp, void* stream);
+
+/* Row joint_attn_qk_gemm, backward: dq^ and dk^ (fp32 [B, H, S, D]) from dS
+ * and the q^, k^ in `ctx`. */
+rlk_status rlk_joint_attn_qk_gemm_bwd(const rlk_ja_shape* shape, const void* ds, const void* ctx,
+                                      const int32_t* txt_valid_len, float* dqh, float* dkh, void* stream);
+
+/* Rows multi_axis_rope and qk_rmsnorm, backward: dQ, dK (bf16 [B, S, H, D])
+ * from dq^, dk^, the inputs q, k, the gains and the RMSNorm factors and
+ * cos/sin table in `ctx`; gain gradients as rlk_joint_attn_bwd() gives
+ * them. gain_tiles: scratch of rlk_joint_attn_unfused_bytes(
+ * RLK_UNFUSED_GAIN_TILES) bytes. */
+rlk_status rlk_qk_norm_rope_bwd(const rlk_ja_shape* shape, const void* q, const void* k,
+                                const float* g_q_txt, const float* g_k_txt,
+                                const float* g_q_img, const float* g_k_img, const void* ctx,
+                                const float* dqh, const float* dkh, void* dq, void* dk,
+                                float* dg_partial, float* dg, float* gain_tiles, void* stream);
 
 /* ---------------------------------------------------------------------------
  * The same forward and backward with the text and image streams in separate

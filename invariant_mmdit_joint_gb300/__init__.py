@@ -29,6 +29,8 @@ __all__ = [
     "rlk_joint_attn_state_bytes", "rlk_joint_attn_fwd_shard", "rlk_joint_attn_fwd_streams",
     "rlk_joint_attn_bwd_streams", "rlk_qkv_bias_gemm", "rlk_joint_attn_fwd_ctx",
     "rlk_attn_out_bias_gemm", "rlk_selftest_wait_timeout", "rlk_fwd_tile_schedule", "FWD_TILES",
+    "rlk_joint_attn_bwd_stats", "rlk_joint_attn_softmax_bwd", "rlk_joint_attn_av_gemm_bwd",
+    "rlk_joint_attn_qk_gemm_bwd", "rlk_qk_norm_rope_bwd",
     "EXPORTED_SYMBOLS", "KERNEL_IDS",
 ]
 
@@ -47,9 +49,10 @@ KERNEL_IDS = {
     "rope_table": 0, "prologue": 1, "attn_fwd": 2, "bwd_pre": 3,
     "bwd_dkdv": 4, "bwd_dq": 5, "norm_rope_bwd_k": 6, "dg_fold": 7,
     "qk_gemm": 8, "softmax": 9, "av_gemm": 10, "attn_fwd_shard": 11, "qkv_gemm": 12, "out_gemm": 13,
+    "dp_gemm": 14, "softmax_bwd": 15, "key_gemm": 16, "query_gemm": 17, "norm_rope_bwd_q": 18,
 }
 # which intermediate rlk_joint_attn_unfused_bytes() sizes
-UNFUSED = {"scores": 0, "p": 1, "alpha": 2, "rows": 3}
+UNFUSED = {"scores": 0, "p": 1, "alpha": 2, "rows": 3, "dp": 4, "ds": 5, "stats": 6, "dhat": 7, "gain_tiles": 8}
 # Every symbol include/rlk_joint_attn.h declares.
 EXPORTED_SYMBOLS = (
     "rlk_joint_attn_ctx_bytes", "rlk_joint_attn_bwd_workspace_bytes", "rlk_joint_attn_bwd_workspace_min_bytes",
@@ -63,6 +66,8 @@ EXPORTED_SYMBOLS = (
     "rlk_joint_attn_fwd_streams", "rlk_joint_attn_bwd_streams", "rlk_qkv_bias_gemm",
     "rlk_joint_attn_fwd_ctx", "rlk_attn_out_bias_gemm", "rlk_selftest_wait_timeout",
     "rlk_fwd_tile_schedule",
+    "rlk_joint_attn_bwd_stats", "rlk_joint_attn_softmax_bwd", "rlk_joint_attn_av_gemm_bwd",
+    "rlk_joint_attn_qk_gemm_bwd", "rlk_qk_norm_rope_bwd",
 )
 OP_TRACE_CAP = 256
 OP_TRACE_MAX_KERNELS = 8
@@ -191,6 +196,16 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     L.rlk_joint_attn_softmax.restype = i32
     L.rlk_joint_attn_av_gemm.argtypes = [shp, vp, vp, vp, vp, i32p, vp, vp]
     L.rlk_joint_attn_av_gemm.restype = i32
+    L.rlk_joint_attn_bwd_stats.argtypes = [shp, vp, vp, vp, vp, vp]
+    L.rlk_joint_attn_bwd_stats.restype = i32
+    L.rlk_joint_attn_softmax_bwd.argtypes = [shp, vp, vp, vp, i32p, vp, vp, vp]
+    L.rlk_joint_attn_softmax_bwd.restype = i32
+    L.rlk_joint_attn_av_gemm_bwd.argtypes = [shp, vp, vp, vp, i32p, vp, vp, vp]
+    L.rlk_joint_attn_av_gemm_bwd.restype = i32
+    L.rlk_joint_attn_qk_gemm_bwd.argtypes = [shp, vp, vp, i32p, vp, vp, vp]
+    L.rlk_joint_attn_qk_gemm_bwd.restype = i32
+    L.rlk_qk_norm_rope_bwd.argtypes = [shp] + [vp] * 15
+    L.rlk_qk_norm_rope_bwd.restype = i32
     L.rlk_joint_attn_state_bytes.argtypes = [shp]
     L.rlk_joint_attn_state_bytes.restype = sz
     L.rlk_joint_attn_fwd_shard.argtypes = [shp, vp, vp, i32p, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp, vp]
@@ -334,6 +349,37 @@ def rlk_joint_attn_av_gemm(shape, p, alpha, l, v, txt_valid_len, out, stream=Non
     rc = lib().rlk_joint_attn_av_gemm(ctypes.byref(shape), _ptr(p), _ptr(alpha), _ptr(l), _ptr(v),
                                       _lengths(txt_valid_len, shape), _ptr(out), _stream_handle(stream))
     _check(rc, "rlk_joint_attn_av_gemm")
+
+
+def rlk_joint_attn_bwd_stats(shape, out, dout, lse, stats, stream=None) -> None:
+    _check(lib().rlk_joint_attn_bwd_stats(ctypes.byref(shape), _ptr(out), _ptr(dout), _ptr(lse), _ptr(stats),
+                                          _stream_handle(stream)), "rlk_joint_attn_bwd_stats")
+
+
+def rlk_joint_attn_softmax_bwd(shape, scores, stats, dp, txt_valid_len, p, ds, stream=None) -> None:
+    _check(lib().rlk_joint_attn_softmax_bwd(ctypes.byref(shape), _ptr(scores), _ptr(stats), _ptr(dp),
+                                            _lengths(txt_valid_len, shape), _ptr(p), _ptr(ds),
+                                            _stream_handle(stream)), "rlk_joint_attn_softmax_bwd")
+
+
+def rlk_joint_attn_av_gemm_bwd(shape, p, v, dout, txt_valid_len, dv, dp, stream=None) -> None:
+    _check(lib().rlk_joint_attn_av_gemm_bwd(ctypes.byref(shape), _ptr(p), _ptr(v), _ptr(dout),
+                                            _lengths(txt_valid_len, shape), _ptr(dv), _ptr(dp),
+                                            _stream_handle(stream)), "rlk_joint_attn_av_gemm_bwd")
+
+
+def rlk_joint_attn_qk_gemm_bwd(shape, ds, ctx, txt_valid_len, dqh, dkh, stream=None) -> None:
+    _check(lib().rlk_joint_attn_qk_gemm_bwd(ctypes.byref(shape), _ptr(ds), _ptr(ctx),
+                                            _lengths(txt_valid_len, shape), _ptr(dqh), _ptr(dkh),
+                                            _stream_handle(stream)), "rlk_joint_attn_qk_gemm_bwd")
+
+
+def rlk_qk_norm_rope_bwd(shape, q, k, g_q_txt, g_k_txt, g_q_img, g_k_img, ctx, dqh, dkh, dq, dk, dg_partial, dg,
+                         gain_tiles, stream=None) -> None:
+    _check(lib().rlk_qk_norm_rope_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(g_q_txt), _ptr(g_k_txt),
+                                      _ptr(g_q_img), _ptr(g_k_img), _ptr(ctx), _ptr(dqh), _ptr(dkh), _ptr(dq),
+                                      _ptr(dk), _ptr(dg_partial), _ptr(dg), _ptr(gain_tiles),
+                                      _stream_handle(stream)), "rlk_qk_norm_rope_bwd")
 
 
 def rlk_joint_attn_state_bytes(shape: Shape) -> int:
@@ -598,6 +644,41 @@ class JointAttention:
         rlk_joint_attn_softmax(sh, scores, valid_len, p, alpha, l, lse, stream)
         rlk_joint_attn_av_gemm(sh, p, alpha, l, v, valid_len, out, stream)
         return {"out": out, "lse": lse, "l": l, "scores": scores, "p": p, "alpha": alpha}
+
+    def backward_unfused(self, q, k, v, gains, valid_len, out, dout, lse, scores, stream=None):
+        """The backward as the standalone operators' backward calls, after a
+        forward (fused or standalone) on the same inputs left its context in
+        this object; scores from rlk_joint_attn_qk_gemm. Returns a dict with
+        dq, dk, dv, dgp, dg (bytes equal to backward()) and the intermediates
+        stats, p, dp, ds, dqh, dkh."""
+        import torch
+        self._check_inputs(q, k, v, out, dout)
+        self._check_gains(gains)
+        if len(valid_len) != self.shape.B:
+            raise ValueError("one valid length per sample")
+        sh = self.shape
+        n_tiles = -(-sh.T_txt // 128) + -(-(sh.grid_h * sh.grid_w) // 128)
+        dev = self.device
+        stats = torch.empty((2, sh.B, sh.H, n_tiles * 128), dtype=torch.float32, device=dev)
+        p = torch.empty((sh.B, sh.H, sh.S, n_tiles * 128), dtype=torch.bfloat16, device=dev)
+        ds = torch.empty_like(p)
+        dp = torch.empty((sh.B, sh.H, sh.S, n_tiles * 128), dtype=torch.float32, device=dev)
+        dqh = torch.empty((sh.B, sh.H, sh.S, HEAD_DIM), dtype=torch.float32, device=dev)
+        dkh = torch.empty_like(dqh)
+        gain_tiles = torch.empty(rlk_joint_attn_unfused_bytes(sh, UNFUSED["gain_tiles"]) // 4, dtype=torch.float32,
+                                 device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dgp = torch.empty((sh.B, sh.H, 4, HEAD_DIM), dtype=torch.float32, device=dev)
+        dg = torch.empty((4, HEAD_DIM), dtype=torch.float32, device=dev)
+        rlk_joint_attn_bwd_stats(sh, out, dout, lse, stats, stream)
+        rlk_joint_attn_softmax_bwd(sh, scores, stats, None, valid_len, p, None, stream)
+        rlk_joint_attn_av_gemm_bwd(sh, p, v, dout, valid_len, dv, dp, stream)
+        rlk_joint_attn_softmax_bwd(sh, scores, stats, dp, valid_len, None, ds, stream)
+        rlk_joint_attn_qk_gemm_bwd(sh, ds, self.ctx, valid_len, dqh, dkh, stream)
+        rlk_qk_norm_rope_bwd(sh, q, k, gains[0], gains[1], gains[2], gains[3], self.ctx, dqh, dkh, dq, dk, dgp, dg,
+                             gain_tiles, stream)
+        return {"dq": dq, "dk": dk, "dv": dv, "dgp": dgp, "dg": dg, "stats": stats, "p": p, "dp": dp, "ds": ds,
+                "dqh": dqh, "dkh": dkh}
 
     def forward_streams(self, q, k, v, gains, valid_len, stream=None):
         """Forward on separate text/image tensors: q, k, v are (txt, img)

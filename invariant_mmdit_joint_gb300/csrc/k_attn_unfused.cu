@@ -106,6 +106,10 @@ __device__ __forceinline__ void query_tile(const Geom& g, int qt, int& q0, int& 
 struct QkArgs {
     CUtensorMap map_q;  // qh [B*H*S, 128] bf16
     CUtensorMap map_k;  // kh [B*H*S, 128] bf16
+    // the dP form (joint_attn_av_gemm's backward, dP = dO V^T): dO as the A
+    // rows and V as the B rows, per segment (rows past a segment read zeros)
+    CUtensorMap map_a_seg[2];
+    CUtensorMap map_b_seg[2];
     Geom g;
     ValidLen vl;
     float* scores;      // [B, H, S, ncols]
@@ -118,6 +122,10 @@ struct QkArgs {
 constexpr int kQkStageBytes = 4 * 4 * 4096;
 constexpr int kQkSmemBytes = 3 * kTileBytes + kQkStageBytes + 1024;
 
+// kDp: the backward's dP = dO V^T in the same tiling -- the A rows come from
+// dO and the B rows from V (per-segment maps), and no key is masked (dP of a
+// masked key is finite; its P is 0).
+template <bool kDp>
 __global__ void __launch_bounds__(kThreads, 1) qk_gemm_kernel(const __grid_constant__ QkArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[10];
@@ -169,8 +177,14 @@ __global__ void __launch_bounds__(kThreads, 1) qk_gemm_kernel(const __grid_const
             prefetch_tensormap(&a.map_q);
             prefetch_tensormap(&a.map_k);
             mbar_expect_tx(bar_q, kTileBytes);
-            tma_load_2d(sQ, &a.map_q, bar_q, 0, row_base + q0);
-            tma_load_2d(sQ + kBoxBytes, &a.map_q, bar_q, 64, row_base + q0);
+            if (kDp) {
+                const int aseg = q0 < g.T_txt ? 0 : 1, arow = aseg ? q0 - g.T_txt : q0;
+                tma_load_4d(sQ, &a.map_a_seg[aseg], bar_q, 0, h, arow, b);
+                tma_load_4d(sQ + kBoxBytes, &a.map_a_seg[aseg], bar_q, 64, h, arow, b);
+            } else {
+                tma_load_2d(sQ, &a.map_q, bar_q, 0, row_base + q0);
+                tma_load_2d(sQ + kBoxBytes, &a.map_q, bar_q, 64, row_base + q0);
+            }
             int issued = 0;
             for (int j = 0; j < nkt && !abort_flag; ++j) {
                 const int s = j & 1;
@@ -180,8 +194,14 @@ __global__ void __launch_bounds__(kThreads, 1) qk_gemm_kernel(const __grid_const
                 }
                 const KeyTile kt = key_tile(g, L, j);
                 mbar_expect_tx(bar_kf + 8 * s, kTileBytes);
-                tma_load_2d(sK + s * kTileBytes, &a.map_k, bar_kf + 8 * s, 0, row_base + kt.k0);
-                tma_load_2d(sK + s * kTileBytes + kBoxBytes, &a.map_k, bar_kf + 8 * s, 64, row_base + kt.k0);
+                if (kDp) {
+                    const int bseg = kt.k0 < g.T_txt ? 0 : 1, brow = bseg ? kt.k0 - g.T_txt : kt.k0;
+                    tma_load_4d(sK + s * kTileBytes, &a.map_b_seg[bseg], bar_kf + 8 * s, 0, h, brow, b);
+                    tma_load_4d(sK + s * kTileBytes + kBoxBytes, &a.map_b_seg[bseg], bar_kf + 8 * s, 64, h, brow, b);
+                } else {
+                    tma_load_2d(sK + s * kTileBytes, &a.map_k, bar_kf + 8 * s, 0, row_base + kt.k0);
+                    tma_load_2d(sK + s * kTileBytes + kBoxBytes, &a.map_k, bar_kf + 8 * s, 64, row_base + kt.k0);
+                }
                 issued = j + 1;
             }
             const volatile int no_abort = 0;
@@ -244,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) qk_gemm_kernel(const __grid_const
             mbar_arrive(bar_se + 8 * s);
             const KeyTile kt = key_tile(g, L, j);
             const int nvalid = kt.kend - kt.k0;  // masked keys (and keys past the segment) score -inf
-            if (nvalid < 128) {
+            if (!kDp && nvalid < 128) {
 #pragma unroll
                 for (int i = 0; i < 128; ++i) r[i] = i < nvalid ? r[i] : 0xff800000u;
             }
@@ -647,12 +667,37 @@ cudaError_t launch_qk_gemm(const Geom& g, const ValidLen& vl, const uint16_t* qh
     a.ncols = 128 * (g.ntq_txt + g.ntq_img);
     for (int seg = 0; seg < 2; ++seg)
         if (!tmap::scores_f32_segment(&a.map_s[seg], scores, g, a.ncols, seg)) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(qk_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkSmemBytes);
+    cudaError_t e =
+        cudaFuncSetAttribute(qk_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkSmemBytes);
     if (e != cudaSuccess) return e;
     const dim3 grid(g.ntq_txt + g.ntq_img, g.H, g.B);
     timing_begin(kKQkGemm, s);
-    qk_gemm_kernel<<<grid, kThreads, kQkSmemBytes, s>>>(a);
+    qk_gemm_kernel<false><<<grid, kThreads, kQkSmemBytes, s>>>(a);
     timing_end(kKQkGemm, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dp_gemm(const Geom& g, const ValidLen& vl, const SegBf16& dout, const SegBf16& v, float* dp,
+                           cudaStream_t s) {
+    QkArgs a;
+    memset(&a.map_q, 0, sizeof(a.map_q));
+    memset(&a.map_k, 0, sizeof(a.map_k));
+    for (int seg = 0; seg < 2; ++seg)
+        if (!tmap::seg_bf16(&a.map_a_seg[seg], dout, g, seg) || !tmap::seg_bf16(&a.map_b_seg[seg], v, g, seg))
+            return cudaErrorInvalidValue;
+    a.g = g;
+    a.vl = vl;
+    a.scores = dp;
+    a.ncols = 128 * (g.ntq_txt + g.ntq_img);
+    for (int seg = 0; seg < 2; ++seg)
+        if (!tmap::scores_f32_segment(&a.map_s[seg], dp, g, a.ncols, seg)) return cudaErrorInvalidValue;
+    cudaError_t e =
+        cudaFuncSetAttribute(qk_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkSmemBytes);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(g.ntq_txt + g.ntq_img, g.H, g.B);
+    timing_begin(kKDpGemm, s);
+    qk_gemm_kernel<true><<<grid, kThreads, kQkSmemBytes, s>>>(a);
+    timing_end(kKDpGemm, s);
     return cudaGetLastError();
 }
 

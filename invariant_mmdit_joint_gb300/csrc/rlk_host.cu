@@ -133,8 +133,8 @@ std::mutex g_dev_mu;
 int g_dev_state[kMaxDevices];  // 0 unknown, 1 ok, 2 wrong arch, 3 fast math, 4 cuda error
 
 int strict_all_units() {
-    const int r[6] = {probe_host_tu(), probe_prologue_tu(), probe_fwd_tu(), probe_bwd_tu(), probe_unfused_tu(),
-                      probe_qkv_tu()};
+    const int r[7] = {probe_host_tu(), probe_prologue_tu(), probe_fwd_tu(), probe_bwd_tu(), probe_unfused_tu(),
+                      probe_qkv_tu(), probe_unfused_bwd_tu()};
     for (int v : r)
         if (v < 0) return -1;
     for (int v : r)
@@ -227,6 +227,11 @@ size_t unfused_bytes(const Geom& g, int which) {
         case RLK_UNFUSED_P: return rows * nblk * 128 * 2;
         case RLK_UNFUSED_ALPHA: return rows * nblk * 4;
         case RLK_UNFUSED_ROWS: return rows * 4;
+        case RLK_UNFUSED_DP: return rows * nblk * 128 * 4;
+        case RLK_UNFUSED_DS: return rows * nblk * 128 * 2;
+        case RLK_UNFUSED_STATS: return (size_t)2 * g.B * g.H * g.nq_pad * 4;
+        case RLK_UNFUSED_DHAT: return rows * kHeadDim * 4;
+        case RLK_UNFUSED_GAIN_TILES: return (size_t)g.B * g.H * 2 * nblk * 4 * kHeadDim * 4;
         default: return 0;
     }
 }
@@ -302,12 +307,29 @@ const OpInfo kOps[] = {
     {"attn_out_bias_gemm", "rlk_attn_out_bias_gemm",
      "bf16 O W operands, fp32 TMEM accumulators, + bf16 bias, one bf16 rounding of the output",
      "K in ascending steps of 64 (16 per MMA); no split-K"},
+    {"joint_attn_softmax backward preprocess", "rlk_joint_attn_bwd_stats",
+     "fp32 lse * log2(e) and rowsum(dO * O), tile-padded", "row sums: 16 partials of 8 products, then xor 8,4,2,1"},
+    {"joint_attn_softmax backward", "rlk_joint_attn_softmax_bwd",
+     "P = exp2f(fmaf(s, log2(e)/sqrt(128), -lse2)) fp32, one bf16 rounding; dS = P * (dP - Delta), one bf16 "
+     "rounding; no fast math",
+     "elementwise"},
+    {"joint_attn_av_gemm backward", "rlk_joint_attn_av_gemm_bwd",
+     "bf16 dO V P operands, fp32 TMEM accumulators; dP fp32, dV one bf16 rounding",
+     "dP: k-steps of 16 dims in order; dV: query tiles ascending, k-steps of 16 queries"},
+    {"joint_attn_qk_gemm backward", "rlk_joint_attn_qk_gemm_bwd",
+     "bf16 dS q^ k^ operands, fp32 TMEM accumulators, times 1/sqrt(128); dq^ dk^ fp32",
+     "dk^: query tiles ascending; dq^: key tiles in the forward order; k-steps of 16"},
+    {"qk_rmsnorm+multi_axis_rope backward", "rlk_qk_norm_rope_bwd",
+     "fp32 inverse rotation and RMSNorm backward, one bf16 cast of dQ dK",
+     "row dot products: 4 products per lane then xor 16..1; gain partials per 32-row quarter, then tiles, h, b "
+     "ascending"},
 };
 const char* const kKernelNames[kNumKernelIds] = {
     "rope_table_kernel", "prologue_kernel", "attn_fwd_tc_kernel", "bwd_pre_kernel",
     "attn_bwd_dkdv_tc_kernel", "attn_bwd_dq_tc_kernel", "norm_rope_bwd_k_kernel", "dg_fold_kernels",
     "qk_gemm_kernel", "softmax_kernel", "av_gemm_kernel", "attn_fwd_tc_kernel<shard>", "qkv_gemm_kernel",
-    "qkv_gemm_kernel<out_proj>"};
+    "qkv_gemm_kernel<out_proj>", "qk_gemm_kernel<dp>", "softmax_bwd_kernel", "acc_gemm_kernel<key>",
+    "acc_gemm_kernel<query>", "norm_rope_bwd_q_kernel"};
 
 struct OpLog {
     std::mutex mu;
@@ -861,6 +883,146 @@ rlk_status rlk_joint_attn_av_gemm(const rlk_ja_shape* shape, const void* p, cons
     return sc.finish(rlk_joint_attn_av_gemm_impl(shape, p, alpha, l, v, txt_valid_len, out, stream));
 }
 
+// ---- the standalone backward operators (k_attn_unfused_bwd.cu) ----
+static rlk_status bwd_stats_impl(const rlk_ja_shape* shape, const void* out, const void* dout, const float* lse,
+                                 float* stats, void* stream) {
+    rlk_status why = RLK_OK;
+    if (!shape_ok(shape, &why)) return why;
+    const Geom g = make_geom(shape);
+    rlk_status st = check_ptrs({out, dout, lse, stats}, {});
+    if (st != RLK_OK) return st;
+    st = device_ok(stream);
+    if (st != RLK_OK) return st;
+    const size_t half = (size_t)g.B * g.H * g.nq_pad;
+    if (launch_bwd_pre(g, seg_concat(out, g), seg_concat(dout, g), lse, stats, stats + half,
+                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status rlk_joint_attn_bwd_stats(const rlk_ja_shape* shape, const void* out, const void* dout, const float* lse,
+                                    float* stats, void* stream) {
+    OpScope sc(kOpBwdStats, shape);
+    return sc.finish(bwd_stats_impl(shape, out, dout, lse, stats, stream));
+}
+
+static rlk_status softmax_bwd_impl(const rlk_ja_shape* shape, const float* scores, const float* stats,
+                                   const float* dp, const int32_t* txt_valid_len, void* p, void* ds, void* stream) {
+    Geom g;
+    ValidLen vl;
+    rlk_status st = common_checks(shape, txt_valid_len, &g, &vl);
+    if (st != RLK_OK) return st;
+    // P alone (dp NULL), or dS (dp and ds given; P optional)
+    if ((dp == nullptr) != (ds == nullptr) || (dp == nullptr && p == nullptr)) return RLK_ERR_INVALID_ARG;
+    st = check_ptrs({scores, stats}, {dp, p, ds});
+    if (st != RLK_OK) return st;
+    st = device_ok(stream);
+    if (st != RLK_OK) return st;
+    const size_t half = (size_t)g.B * g.H * g.nq_pad;
+    if (launch_softmax_bwd(g, vl, scores, stats, stats + half, dp, static_cast<uint16_t*>(p),
+                           static_cast<uint16_t*>(ds), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status rlk_joint_attn_softmax_bwd(const rlk_ja_shape* shape, const float* scores, const float* stats,
+                                      const float* dp, const int32_t* txt_valid_len, void* p, void* ds,
+                                      void* stream) {
+    OpScope sc(kOpSoftmaxBwd, shape);
+    return sc.finish(softmax_bwd_impl(shape, scores, stats, dp, txt_valid_len, p, ds, stream));
+}
+
+static rlk_status av_gemm_bwd_impl(const rlk_ja_shape* shape, const void* p, const void* v, const void* dout,
+                                   const int32_t* txt_valid_len, void* dv, float* dp, void* stream) {
+    Geom g;
+    ValidLen vl;
+    rlk_status st = common_checks(shape, txt_valid_len, &g, &vl);
+    if (st != RLK_OK) return st;
+    if (dv == nullptr && dp == nullptr) return RLK_ERR_INVALID_ARG;
+    if (dv != nullptr && p == nullptr) return RLK_ERR_INVALID_ARG;
+    st = check_ptrs({v, dout}, {p, dv, dp});
+    if (st != RLK_OK) return st;
+    st = device_ok(stream);
+    if (st != RLK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dp != nullptr && launch_dp_gemm(g, vl, seg_concat(dout, g), seg_concat(v, g), dp, s) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    if (dv != nullptr &&
+        launch_dv_gemm(g, vl, static_cast<const uint16_t*>(p), seg_concat(dout, g), seg_concat(dv, g), s) !=
+            cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status rlk_joint_attn_av_gemm_bwd(const rlk_ja_shape* shape, const void* p, const void* v, const void* dout,
+                                      const int32_t* txt_valid_len, void* dv, float* dp, void* stream) {
+    OpScope sc(kOpAvGemmBwd, shape);
+    return sc.finish(av_gemm_bwd_impl(shape, p, v, dout, txt_valid_len, dv, dp, stream));
+}
+
+static rlk_status qk_gemm_bwd_impl(const rlk_ja_shape* shape, const void* ds, const void* ctx,
+                                   const int32_t* txt_valid_len, float* dqh, float* dkh, void* stream) {
+    Geom g;
+    ValidLen vl;
+    rlk_status st = common_checks(shape, txt_valid_len, &g, &vl);
+    if (st != RLK_OK) return st;
+    st = check_ptrs({ds, ctx, dqh, dkh}, {});
+    if (st != RLK_OK) return st;
+    st = device_ok(stream);
+    if (st != RLK_OK) return st;
+    const CtxLayout l = ctx_layout(g);
+    const uint8_t* c = static_cast<const uint8_t*>(ctx);
+    if (launch_dhat_gemms(g, vl, static_cast<const uint16_t*>(ds), reinterpret_cast<const uint16_t*>(c + l.qh),
+                          reinterpret_cast<const uint16_t*>(c + l.kh), dqh, dkh,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status rlk_joint_attn_qk_gemm_bwd(const rlk_ja_shape* shape, const void* ds, const void* ctx,
+                                      const int32_t* txt_valid_len, float* dqh, float* dkh, void* stream) {
+    OpScope sc(kOpQkGemmBwd, shape);
+    return sc.finish(qk_gemm_bwd_impl(shape, ds, ctx, txt_valid_len, dqh, dkh, stream));
+}
+
+static rlk_status norm_rope_bwd_impl(const rlk_ja_shape* shape, const void* q, const void* k, const float* g_q_txt,
+                                     const float* g_k_txt, const float* g_q_img, const float* g_k_img,
+                                     const void* ctx, const float* dqh, const float* dkh, void* dq, void* dk,
+                                     float* dg_partial, float* dg, float* gain_tiles, void* stream) {
+    rlk_status why = RLK_OK;
+    if (!shape_ok(shape, &why)) return why;
+    const Geom g = make_geom(shape);
+    rlk_status st = check_ptrs({q, k, g_q_txt, g_k_txt, g_q_img, g_k_img, ctx, dqh, dkh, dq, dk, dg_partial, dg,
+                                gain_tiles},
+                               {});
+    if (st != RLK_OK) return st;
+    st = device_ok(stream);
+    if (st != RLK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const CtxLayout l = ctx_layout(g);
+    const uint8_t* c = static_cast<const uint8_t*>(ctx);
+    const float* rq = reinterpret_cast<const float*>(c + l.rq);
+    const float* rk = reinterpret_cast<const float*>(c + l.rk);
+    const float2* tab = reinterpret_cast<const float2*>(c + l.tab);
+    if (launch_norm_rope_bwd_q(g, seg_concat(q, g), g_q_txt, g_q_img, tab, rq, dqh, seg_concat(dq, g), gain_tiles,
+                               s) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    if (launch_norm_rope_bwd_k(g, seg_concat(k, g), g_k_txt, g_k_img, tab, rk, dkh, seg_concat(dk, g), gain_tiles,
+                               s) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    if (launch_dg_fold(g, gain_tiles, dg_partial, dg, s) != cudaSuccess) return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
+rlk_status rlk_qk_norm_rope_bwd(const rlk_ja_shape* shape, const void* q, const void* k, const float* g_q_txt,
+                                const float* g_k_txt, const float* g_q_img, const float* g_k_img, const void* ctx,
+                                const float* dqh, const float* dkh, void* dq, void* dk, float* dg_partial,
+                                float* dg, float* gain_tiles, void* stream) {
+    OpScope sc(kOpNormRopeBwd, shape);
+    return sc.finish(norm_rope_bwd_impl(shape, q, k, g_q_txt, g_k_txt, g_q_img, g_k_img, ctx, dqh, dkh, dq, dk,
+                                        dg_partial, dg, gain_tiles, stream));
+}
+
 size_t rlk_joint_attn_state_bytes(const rlk_ja_shape* shape) {
     rlk_status why;
     if (!shape_ok(shape, &why)) return 0;
@@ -915,8 +1077,9 @@ rlk_status rlk_joint_attn_check_status(void* stream) {
     const int c = read_and_clear_status_unfused(s);
     const int d = read_and_clear_status_qkv(s);
     const int e = read_and_clear_status_prologue(s);
-    if (a < 0 || b < 0 || c < 0 || d < 0 || e < 0) return RLK_ERR_CUDA;
-    if (a != 0 || b != 0 || c != 0 || d != 0 || e != 0) return RLK_ERR_DEVICE_TIMEOUT;
+    const int f = read_and_clear_status_unfused_bwd(s);
+    if (a < 0 || b < 0 || c < 0 || d < 0 || e < 0 || f < 0) return RLK_ERR_CUDA;
+    if (a != 0 || b != 0 || c != 0 || d != 0 || e != 0 || f != 0) return RLK_ERR_DEVICE_TIMEOUT;
     return RLK_OK;
 }
 

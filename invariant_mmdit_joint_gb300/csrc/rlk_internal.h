@@ -91,7 +91,8 @@ __host__ __device__ inline int pair_axis(int k) {
 enum KernelId {
     kKRopeTable = 0, kKPrologue = 1, kKAttnFwd = 2, kKBwdPre = 3,
     kKBwdDkDv = 4, kKBwdDq = 5, kKNormRopeBwd = 6, kKDgFold = 7,
-    kKQkGemm = 8, kKSoftmax = 9, kKAvGemm = 10, kKAttnFwdShard = 11, kKQkvGemm = 12, kKOutGemm = 13, kNumKernelIds = 14
+    kKQkGemm = 8, kKSoftmax = 9, kKAvGemm = 10, kKAttnFwdShard = 11, kKQkvGemm = 12, kKOutGemm = 13,
+    kKDpGemm = 14, kKSoftmaxBwd = 15, kKKeyGemm = 16, kKQueryGemm = 17, kKNormRopeBwdQ = 18, kNumKernelIds = 19
 };
 
 // Launch timing hooks (rlk_host.cu): bracket one launch with events.
@@ -104,7 +105,8 @@ void timing_end(int kernel_id, cudaStream_t s);
 // launches inside it fill and finish() appends to the log.
 enum OpKind {
     kOpFwd = 0, kOpBwd, kOpFwdNoalloc, kOpNormRope, kOpQkGemm, kOpSoftmax, kOpAvGemm, kOpFwdShard,
-    kOpFwdStreams, kOpBwdStreams, kOpQkvGemm, kOpFwdCtx, kOpOutGemm
+    kOpFwdStreams, kOpBwdStreams, kOpQkvGemm, kOpFwdCtx, kOpOutGemm,
+    kOpBwdStats, kOpSoftmaxBwd, kOpAvGemmBwd, kOpQkGemmBwd, kOpNormRopeBwd
 };
 class OpScope {
    public:
@@ -209,8 +211,26 @@ cudaError_t launch_softmax(const Geom& g, const ValidLen& vl, const float* score
                            float* alpha, float* l, float* lse, cudaStream_t s);
 cudaError_t launch_av_gemm(const Geom& g, const ValidLen& vl, const uint16_t* p, const float* alpha,
                            const float* l, const SegBf16& v, const SegBf16& out, cudaStream_t s);
+// dP = dO V^T in the qk_gemm tiling, fp32 [B, H, S, n_tiles * 128] (the
+// backward of joint_attn_av_gemm, first half)
+cudaError_t launch_dp_gemm(const Geom& g, const ValidLen& vl, const SegBf16& dout, const SegBf16& v, float* dp,
+                           cudaStream_t s);
 int probe_unfused_tu(void);
 int read_and_clear_status_unfused(cudaStream_t s);
+
+// k_attn_unfused_bwd.cu: the standalone backward operators (layouts in that
+// file's header). lse2 / delta: the tile-padded arrays of launch_bwd_pre.
+cudaError_t launch_softmax_bwd(const Geom& g, const ValidLen& vl, const float* scores, const float* lse2,
+                               const float* delta, const float* dp, uint16_t* p, uint16_t* ds, cudaStream_t s);
+cudaError_t launch_dv_gemm(const Geom& g, const ValidLen& vl, const uint16_t* p, const SegBf16& dout,
+                           const SegBf16& dv, cudaStream_t s);
+cudaError_t launch_dhat_gemms(const Geom& g, const ValidLen& vl, const uint16_t* ds, const uint16_t* qh,
+                              const uint16_t* kh, float* dqh, float* dkh, cudaStream_t s);
+cudaError_t launch_norm_rope_bwd_q(const Geom& g, const SegBf16& q, const float* gq_txt, const float* gq_img,
+                                   const float2* tab, const float* rq, const float* dqh, const SegBf16& dq,
+                                   float* dgt, cudaStream_t s);
+int probe_unfused_bwd_tu(void);
+int read_and_clear_status_unfused_bwd(cudaStream_t s);
 
 // k_qkv_gemm.cu: per-stream projection Y = X W^T + b (both streams in one
 // launch), stored as bf16. QKV (out_proj false): W is [3C, C]; with

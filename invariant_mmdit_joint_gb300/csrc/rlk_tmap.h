@@ -124,8 +124,8 @@ inline bool mat_f32(CUtensorMap* m, const float* base, long long rows, int cols,
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box);
 }
 
-// bf16 P [B*H, S, ncols] per segment (as scores_f32_segment), box 64 x 32 x 1
-inline bool p_bf16_segment(CUtensorMap* m, const void* base, const Geom& g, int ncols, int seg) {
+// bf16 P [B*H, S, ncols] per segment (as scores_f32_segment), box 64 x box_rows x 1
+inline bool p_bf16_segment(CUtensorMap* m, const void* base, const Geom& g, int ncols, int seg, int box_rows = 32) {
     const int rows = seg == 0 ? g.T_txt : g.T_img;
     if (rows == 0) {
         memset(m, 0, sizeof(*m));
@@ -134,7 +134,7 @@ inline bool p_bf16_segment(CUtensorMap* m, const void* base, const Geom& g, int 
     const uint16_t* p = static_cast<const uint16_t*>(base) + (seg == 0 ? 0 : (size_t)g.T_txt * ncols);
     const cuuint64_t dims[3] = {(cuuint64_t)ncols, (cuuint64_t)rows, (cuuint64_t)g.B * g.H};
     const cuuint64_t strides[2] = {(cuuint64_t)ncols * 2, (cuuint64_t)g.S * ncols * 2};
-    const cuuint32_t box[3] = {64, 32, 1};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p, dims, strides, box);
 }
 

@@ -171,7 +171,14 @@ def test_unfused_intermediate_sizes(L):
     assert pkg.rlk_joint_attn_unfused_bytes(s, "p") == rows * n_tiles * 128 * 2
     assert pkg.rlk_joint_attn_unfused_bytes(s, "alpha") == rows * n_tiles * 4
     assert pkg.rlk_joint_attn_unfused_bytes(s, "rows") == rows * 4
-    assert L.rlk_joint_attn_unfused_bytes(ctypes.byref(s), 7) == 0
+    # the standalone backward's intermediates
+    assert pkg.rlk_joint_attn_unfused_bytes(s, "dp") == rows * n_tiles * 128 * 4
+    assert pkg.rlk_joint_attn_unfused_bytes(s, "ds") == rows * n_tiles * 128 * 2
+    assert pkg.rlk_joint_attn_unfused_bytes(s, "stats") == 2 * 2 * 24 * n_tiles * 128 * 4
+    assert pkg.rlk_joint_attn_unfused_bytes(s, "dhat") == rows * 128 * 4
+    assert pkg.rlk_joint_attn_unfused_bytes(s, "gain_tiles") == 2 * 24 * 2 * n_tiles * 4 * 128 * 4
+    assert L.rlk_joint_attn_unfused_bytes(ctypes.byref(s), 9) == 0
+    assert L.rlk_joint_attn_unfused_bytes(ctypes.byref(s), -1) == 0
     # a ragged image side: ceil(83 * 83 / 128) = 54 image tiles, 2 text tiles
     s2 = pkg.Shape.make(4, 256, 83, 83, 24)
     assert pkg.rlk_joint_attn_unfused_bytes(s2, "alpha") == 4 * 24 * (256 + 83 * 83) * 56 * 4
@@ -469,3 +476,38 @@ def test_forward_tile_schedule_setting(L):
             pkg.rlk_fwd_tile_schedule("halves")
     finally:
         L.rlk_fwd_tile_schedule(prev)
+
+
+def test_backward_operators_fail_closed_without_a_gpu(L):
+    """The standalone backward calls refuse bad arguments before any launch
+    and otherwise reach the device check."""
+    s = pkg.Shape.make(2, 16, 8, 8, 2)
+    p = 1 << 20
+    vl = (ctypes.c_int32 * 2)(3, 5)
+    bad_vl = (ctypes.c_int32 * 2)(3, 17)
+    sb = ctypes.byref(s)
+    # stats
+    assert L.rlk_joint_attn_bwd_stats(sb, p, p, p, None, None) == 1
+    assert L.rlk_joint_attn_bwd_stats(sb, p, p + 8, p, p, None) == 3
+    # softmax_bwd: P alone needs p; dS needs dp and ds together
+    assert L.rlk_joint_attn_softmax_bwd(sb, p, p, None, vl, None, None, None) == 1
+    assert L.rlk_joint_attn_softmax_bwd(sb, p, p, p, vl, p, None, None) == 1
+    assert L.rlk_joint_attn_softmax_bwd(sb, p, p, None, vl, p, p, None) == 1
+    assert L.rlk_joint_attn_softmax_bwd(sb, p, p, None, bad_vl, p, None, None) == 1
+    assert L.rlk_joint_attn_softmax_bwd(sb, p, p, p, vl, None, p + 2, None) == 3
+    # av_gemm_bwd: at least one output; dV needs P
+    assert L.rlk_joint_attn_av_gemm_bwd(sb, p, p, p, vl, None, None, None) == 1
+    assert L.rlk_joint_attn_av_gemm_bwd(sb, None, p, p, vl, p, None, None) == 1
+    assert L.rlk_joint_attn_av_gemm_bwd(sb, p, p, p, vl, p, p + 4, None) == 3
+    # qk_gemm_bwd and the norm/rope backward
+    assert L.rlk_joint_attn_qk_gemm_bwd(sb, p, None, vl, p, p, None) == 1
+    assert L.rlk_qk_norm_rope_bwd(sb, p, p, p, p, p, p, p, p, p, p, p, p, p, None, None) == 1
+    bad = pkg.Shape.make(2, 16, 8, 8, 2, D=64)
+    assert L.rlk_joint_attn_qk_gemm_bwd(ctypes.byref(bad), p, p, vl, p, p, None) == 2
+    import torch
+    if not torch.cuda.is_available():
+        assert L.rlk_joint_attn_bwd_stats(sb, p, p, p, p, None) == 5
+        assert L.rlk_joint_attn_softmax_bwd(sb, p, p, None, vl, p, None, None) == 5
+        assert L.rlk_joint_attn_av_gemm_bwd(sb, p, p, p, vl, p, p, None) == 5
+        assert L.rlk_joint_attn_qk_gemm_bwd(sb, p, p, vl, p, p, None) == 5
+        assert L.rlk_qk_norm_rope_bwd(sb, p, p, p, p, p, p, p, p, p, p, p, p, p, p, None) == 5
