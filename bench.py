@@ -246,6 +246,71 @@ def measure_unfused(pkg, ja, w, q, k, v, gains, vl, fused_out, fused_ms, peaks, 
             "peak": f"hbm_gbs {hbm}"}
 
 
+def unfused_bwd_work(w: W.Workload):
+    """Algorithmic HBM bytes per step of the standalone backward's kernels
+    (each reads its inputs once and writes its outputs once; the [query,
+    key] intermediates cover the key tiles each sample visits)."""
+    rows = w.B * w.H * w.S
+    D = W.HEAD_DIM
+    ntq_img = -(-w.T_img // 128)
+    blocks = sum(w.H * w.S * (-(-L // 128) + ntq_img) for L in w.valid_len)
+    f32, b16 = blocks * 128 * 4, blocks * 128 * 2
+    slots = w.B * w.H * 128 * (-(-w.T_txt // 128) + ntq_img)
+    return {
+        # P pass: scores, lse2 in; P out. dS pass: scores, dP, lse2, Delta in; dS out
+        "softmax_bwd": (f32 + b16 + slots * 4) + (2 * f32 + b16 + 2 * slots * 4),
+        # dO and V in, dP out
+        "dp_gemm": 2 * rows * D * 2 + f32,
+        # dV: P, dO in, dV out (bf16); dk^: dS, q^ in, dk^ out (fp32)
+        "key_gemm": (b16 + rows * D * 2 + rows * D * 2) + (b16 + rows * D * 2 + rows * D * 4),
+        # dq^: dS, k^ in, dq^ out (fp32)
+        "query_gemm": b16 + rows * D * 2 + rows * D * 4,
+    }
+
+
+def measure_unfused_bwd(pkg, ja, w, q, k, v, do, gains, vl, fused, fused_ms, peaks, n_steps):
+    """The backward as the standalone operators' backward calls (stats,
+    softmax_bwd for P, av_gemm_bwd, softmax_bwd for dS, qk_gemm_bwd,
+    qk_norm_rope_bwd) after a standalone forward: time per backward, byte
+    equality with the fused backward on the same inputs (fused = its dq, dk,
+    dv, dg_partial, dg) and the HBM rate of the materialising kernels."""
+    import torch
+    stream = torch.cuda.current_stream()
+    u = ja.forward_unfused(q, k, v, gains, vl)
+    ub = ja.backward_unfused(q, k, v, gains, vl, u["out"], do, u["lse"], u["scores"])  # warm-up
+    torch.cuda.synchronize()
+    byte_equal = all(bool(torch.equal(ub[n].view(torch.int32 if ub[n].dtype == torch.float32 else torch.int16),
+                                      f.view(torch.int32 if f.dtype == torch.float32 else torch.int16)))
+                     for n, f in zip(("dq", "dk", "dv", "dgp", "dg"), fused))
+    del ub
+    pkg.rlk_kernel_timing(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n_steps):
+        ja.backward_unfused(q, k, v, gains, vl, u["out"], do, u["lse"], u["scores"])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n_steps
+    work = unfused_bwd_work(w)
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    ops = {}
+    for name in ("softmax_bwd", "dp_gemm", "key_gemm", "query_gemm", "norm_rope_bwd_q"):
+        tot, n = pkg.rlk_kernel_timing_read(name)
+        if n:
+            per_step = tot / n_steps
+            entry = {"ms_per_step": round(per_step, 4), "launches_per_step": n // n_steps}
+            if name in work:
+                gbs = work[name] / (per_step * 1e-3) / 1e9
+                entry.update(algorithmic_bytes=work[name], achieved=round(gbs, 1), unit="GB/s",
+                             frac=round(gbs / hbm, 4))
+            ops[name] = entry
+    pkg.rlk_kernel_timing(False)
+    del u
+    return {"ms_per_backward": round(ms, 4), "fused_backward_ms": round(fused_ms, 4),
+            "byte_equal_to_fused": byte_equal, "steps": n_steps, "operators": ops, "peak": f"hbm_gbs {hbm}"}
+
+
 def _time_ms(fn, n_steps):
     import torch
     stream = torch.cuda.current_stream()
@@ -659,10 +724,13 @@ def run_ours(args):
              "what": "every key counted (masked text keys included), same timed step as value"}
 
     clocks = clk.summary()
-    unfused = None
+    unfused = unfused_bwd = None
     if not args.no_unfused:
         fwd_ms = sum(per_kernel[n]["avg_ms"] for n in ("rope_table", "prologue", "attn_fwd") if n in per_kernel)
         unfused = measure_unfused(pkg, ja, w, q, k, v, gains, vl, out, fwd_ms, peaks, max(3, min(args.steps, 10)))
+        bwd_ms = sum(per_kernel[n]["avg_ms"] for n in bwd_names if n in per_kernel)
+        unfused_bwd = measure_unfused_bwd(pkg, ja, w, q, k, v, do, gains, vl, eager_result[2:], bwd_ms, peaks,
+                                          max(3, min(args.steps, 10)))
     qkv = rows23 = None
     if not args.no_unfused:
         qkv = measure_qkv(pkg, w, peaks, max(3, min(args.steps, 20)))
@@ -689,7 +757,8 @@ def run_ours(args):
               f"{(4 * w.B * w.S * w.H * 128 * 2) / 1e6:.0f} MB, plus ctx and workspace, against 129 MB of L2",
         "roofline": roofline, "kernels": per_kernel, "phases": phases, "dense_convention": dense,
         "workspace": workspace,
-        "unfused_forward": unfused, "qkv_producer": qkv, "shards_and_streams": rows23,
+        "unfused_forward": unfused, "unfused_backward": unfused_bwd, "qkv_producer": qkv,
+        "shards_and_streams": rows23,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
