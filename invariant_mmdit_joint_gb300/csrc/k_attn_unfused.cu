@@ -659,6 +659,8 @@ __global__ void __launch_bounds__(kThreads, 1) av_gemm_kernel(const __grid_const
 cudaError_t launch_qk_gemm(const Geom& g, const ValidLen& vl, const uint16_t* qh, const uint16_t* kh, float* scores,
                            cudaStream_t s) {
     QkArgs a;
+    memset(a.map_a_seg, 0, sizeof(a.map_a_seg));  // the dP form's maps: unused here
+    memset(a.map_b_seg, 0, sizeof(a.map_b_seg));
     const uint64_t rows = (uint64_t)g.B * g.H * g.S;
     if (!tmap::rows_bf16(&a.map_q, qh, rows) || !tmap::rows_bf16(&a.map_k, kh, rows)) return cudaErrorInvalidValue;
     a.g = g;
