@@ -188,6 +188,7 @@ constexpr int kKvSmemO = kKvSmemQ + kKvQSlots * kTileBytes;
 constexpr int kKvSmemL = kKvSmemO + kKvOSlots * kTileBytes;   // lse2[128], delta[128] per dO slot
 constexpr int kKvSmemBar = kKvSmemL + kKvOSlots * 1024;
 constexpr int kKvBarBytes = 256;
+constexpr uint32_t kProducerSleepNs = 512;
 constexpr int kKvSmemBytes = kKvSmemBar + 1024;  // + alignment slack (holds the barriers when it can)
 static_assert(kKvSmemBytes <= 232448, "dK/dV shared memory exceeds the per-block limit");
 constexpr uint32_t kColDV = 0, kColDK = 128, kColR = 256;
@@ -308,7 +309,11 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc_kernel(const _
                 const int jq = i % kKvQSlots, jo = i & 1;
                 int q0, q_end;
                 q_tile(g, i, q0, q_end);
-                if (i >= kKvQSlots && !mbar_wait(bar_qe + 8 * jq, ((i / kKvQSlots) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                // the copies run ahead of the products: their waits back off
+                // (512 ns per failed poll) to leave SMSP 0's issue slots to
+                // the elementwise warps there (708.5 against 711 us)
+                if (i >= kKvQSlots && !mbar_wait_backoff(bar_qe + 8 * jq, ((i / kKvQSlots) + 1) & 1, &abort_flag,
+                                                         kWaitLimitNs, kProducerSleepNs)) {
                     fail(&abort_flag);
                     break;
                 }
@@ -316,7 +321,8 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc_kernel(const _
                 mbar_expect_tx(bq, kTileBytes);
                 tma_load_2d(slot_q(i), &a.map_q, bq, 0, row_base + q0);
                 tma_load_2d(slot_q(i) + kBoxBytes, &a.map_q, bq, 64, row_base + q0);
-                if (i >= 2 && !mbar_wait(bar_oe + 8 * jo, ((i >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                if (i >= 2 && !mbar_wait_backoff(bar_oe + 8 * jo, ((i >> 1) + 1) & 1, &abort_flag, kWaitLimitNs,
+                                                 kProducerSleepNs)) {
                     fail(&abort_flag);
                     break;
                 }

@@ -73,6 +73,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
     }
 }
 
+// Like mbar_wait, but a failed poll sleeps about sleep_ns before the next,
+// so a warp whose wait is not on the critical path leaves its SMSP's issue
+// slots to the others (same time limit and abort rule).
+__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                                  uint64_t limit_ns, uint32_t sleep_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        asm volatile("nanosleep.u32 %0;" ::"r"(sleep_ns));
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 15) == 0) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
     asm volatile(
