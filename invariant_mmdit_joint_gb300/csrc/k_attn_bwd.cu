@@ -98,30 +98,6 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
     return sdesc_sw128(tile + kk * 2048, kBoxBytes, 1024);
 }
 
-// Two fp32 lanes at once (fma / sub / mul .rn.f32x2): each lane rounds
-// exactly as the scalar instruction does, in half the issue slots.
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-    return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-    lo = __uint_as_float((uint32_t)v);
-    hi = __uint_as_float((uint32_t)(v >> 32));
-}
-__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t sub_f2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 // 16-byte store of dS^T image data that skips L1 (the dQ kernel reads it
 // back through L2).
 __device__ __forceinline__ void st_image(uint8_t* p, uint4 v) {

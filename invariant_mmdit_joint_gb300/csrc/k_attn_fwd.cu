@@ -4,17 +4,21 @@
 // softmax over key tiles.
 //
 // One CTA = two query tiles A and B of 128 rows (the same head, sample and
-// stream segment) sharing every K/V tile; 10 warps:
-//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread t of a
-//              group owns query row t = TMEM lane t. Per key tile it reads
-//              the row of S from TMEM into registers, keeps a reference max m
-//              and the sum l (FP32, log2 units), writes P = exp2(s - m) as
-//              bf16 back over S and rescales O in TMEM when m moves (only
-//              when the row max has grown by more than 2^8). Epilogue: O / l, one bf16 cast, and lse.
-//   warp 8     TMA producer: Q tiles once, then K and V tiles (two slots
+// stream segment) sharing every K/V tile; 18 warps:
+//   warps 0-15 softmax, two threads per query row: warp w serves tile
+//              (w >> 2) & 1, TMEM lane quarter w & 3 (rows 32 (w & 3) + lane)
+//              and key half w >> 3 (S columns [64 (w >> 3), + 64)). Per key
+//              tile a thread reads its half row of S from TMEM, the two
+//              threads of a row trade their halves' maxima (and the previous
+//              tile's half sums) through shared memory, keep a reference max
+//              m and the sum l (FP32, log2 units), write P = exp2(s - m) as
+//              bf16 back over S and rescale their half of O in TMEM when m
+//              moves (only when the row max has grown by more than 2^8).
+//              Epilogue: O / l, one bf16 cast, and lse.
+//   warp 16    TMA producer: Q tiles once, then K and V tiles (two slots
 //              each; a K slot frees when its S products are done, a V slot
 //              when its PV products are done).
-//   warp 9     MMA issuer (one thread) and TMEM owner, per key tile j:
+//   warp 17    MMA issuer (one thread) and TMEM owner, per key tile j:
 //              PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) -- while one group runs
 //              its softmax the tensor core works for the other.
 // TMEM: S_A [0,128), O_A [128,256), S_B [256,384), O_B [384,512).
@@ -49,8 +53,11 @@ namespace {
 using namespace sm100;
 
 constexpr int kBM = 128, kBN = 128;
-constexpr int kThreads = 320;
-constexpr int kWarpTma = 8, kWarpMma = 9;
+// warps 0-15 softmax (tile t = (w >> 2) & 1, key half (w >> 3), TMEM lane
+// quarter w & 3: two threads per query row), 16 TMA, 17 MMA
+constexpr int kSoftmaxWarps = 16;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+constexpr int kWarpTma = kSoftmaxWarps, kWarpMma = kSoftmaxWarps + 1;
 constexpr int kBoxBytes = 128 * 128;          // 128 rows x 64 bf16
 constexpr int kTileBytes = 2 * kBoxBytes;     // 128 rows x 128 bf16
 constexpr int kSmemQ = 0;                     // Q_A, Q_B
@@ -125,7 +132,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 template <bool kShard>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ FwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[16];
+    __shared__ __align__(8) uint64_t bars[32];
+    // the two threads of a query row trade their half's partial row max of
+    // this key tile and their half's row sum of the previous one, through
+    // slot j & 1 of (tile, half, row)
+    __shared__ float2 xch[2][2][2][kBM];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
@@ -144,7 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
     const bool has_b = part < 0 && first + 1 < seg_tiles;
     const int seg0 = q_txt ? 0 : g.T_txt;
     const int q_end = q_txt ? g.T_txt : g.S;
-    const int q0[2] = {seg0 + first * kBM, seg0 + (first + 1) * kBM};
+    // first rows of the two query tiles (scalars, selected by tile: an
+    // array indexed at run time would live on the stack)
+    const int q0a = seg0 + first * kBM, q0b = q0a + kBM;
     const int L = a.vl.L[b];
     const int nkt_txt = (L + kBN - 1) / kBN;
     const int nkt_all = nkt_txt + g.ntq_img;
@@ -163,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
         // passes through unchanged (or starts empty)
         const size_t bh = (size_t)b * g.H + h;
         for (int i = threadIdx.x; i < 2 * kBM; i += kThreads) {
-            const int n = q0[i >> 7] + (i & 127);
+            const int n = ((i >> 7) ? q0b : q0a) + (i & 127);
             if (!(i < kBM || has_b) || n >= q_end) continue;
             const size_t rowi = bh * g.S + n;
             const bool have = a.st_in_m != nullptr && j0 > 0;
@@ -186,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
     const uint32_t bar_p = smem_u32(&bars[11]);   // [2] per Q tile: P written
     const uint32_t bar_o = smem_u32(&bars[13]);   // [2] per Q tile: PV done
     const uint32_t bar_drain = smem_u32(&bars[15]);
+    const uint32_t bar_x = smem_u32(&bars[16]);   // [tile][quarter][slot]: both halves' values written
 
     if (tid == 0) {
         abort_flag = 0;
@@ -196,10 +210,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             mbar_init(bar_ke + 8 * s, 1);
             mbar_init(bar_ve + 8 * s, 1);
             mbar_init(bar_s + 8 * s, 1);
-            mbar_init(bar_p + 8 * s, 128);
+            mbar_init(bar_p + 8 * s, 256);
             mbar_init(bar_o + 8 * s, 1);
         }
         mbar_init(bar_drain, 1);
+        for (int x = 0; x < 16; ++x) mbar_init(bar_x + 8 * x, 64);
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
@@ -219,9 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             prefetch_tensormap(&a.map_v[0]);
             prefetch_tensormap(&a.map_v[1]);
             mbar_expect_tx(bar_q, (has_b ? 2 : 1) * kTileBytes);
-            for (int t = 0; t < (has_b ? 2 : 1); ++t) {
-                tma_load_2d(sQ + t * kTileBytes, &a.map_q, bar_q, 0, row_base + q0[t]);
-                tma_load_2d(sQ + t * kTileBytes + kBoxBytes, &a.map_q, bar_q, 64, row_base + q0[t]);
+            tma_load_2d(sQ, &a.map_q, bar_q, 0, row_base + q0a);
+            tma_load_2d(sQ + kBoxBytes, &a.map_q, bar_q, 64, row_base + q0a);
+            if (has_b) {
+                tma_load_2d(sQ + kTileBytes, &a.map_q, bar_q, 0, row_base + q0b);
+                tma_load_2d(sQ + kTileBytes + kBoxBytes, &a.map_q, bar_q, 64, row_base + q0b);
             }
             int k_issued = 0, v_issued = 0;
             for (int j = 0; j < nkt && !abort_flag; ++j) {
@@ -250,12 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                 v_issued = j + 1;
             }
             // drain: the copies of Q and of the last (up to) two K and V tiles have landed
-            const volatile int no_abort = 0;
-            mbar_wait(bar_q, 0, &no_abort, kWaitLimitNs);
+            mbar_wait_drain(bar_q, 0, kWaitLimitNs);
             for (int j = k_issued - 2 < 0 ? 0 : k_issued - 2; j < k_issued; ++j)
-                mbar_wait(bar_kf + 8 * (j & 1), (j >> 1) & 1, &no_abort, kWaitLimitNs);
+                mbar_wait_drain(bar_kf + 8 * (j & 1), (j >> 1) & 1, kWaitLimitNs);
             for (int j = v_issued - 2 < 0 ? 0 : v_issued - 2; j < v_issued; ++j)
-                mbar_wait(bar_vf + 8 * (j & 1), (j >> 1) & 1, &no_abort, kWaitLimitNs);
+                mbar_wait_drain(bar_vf + 8 * (j & 1), (j >> 1) & 1, kWaitLimitNs);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------ MMA issuer
@@ -330,27 +346,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             if (!ok) fail(&abort_flag);
             // drain every MMA this thread issued before TMEM is released
             mma_commit(bar_drain);
-            const volatile int no_abort = 0;
-            mbar_wait(bar_drain, 0, &no_abort, kWaitLimitNs);
+            mbar_wait_drain(bar_drain, 0, kWaitLimitNs);
         }
-    } else if (warp < 4 || has_b) {
-        // ------------------------------------------------ softmax warps (tile t = warp / 4)
+    } else if (warp < kSoftmaxWarps && (((warp >> 2) & 1) == 0 || has_b)) {
+        // ------------------------------------------------ softmax warps
+        // Tile t = (warp >> 2) & 1; this thread takes key columns
+        // [64 hc, 64 hc + 64) of its query row and O columns [64 hc, + 64).
         // Barrier phases are consumed strictly in order (S_j, then PV_{j-1}
         // once per tile), so no waiter ever falls two phases behind.
-        const int t = warp >> 2;
-        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+        const int t = (warp >> 2) & 1, hc = warp >> 3, q4 = warp & 3;
+        const int q0t = t ? q0b : q0a;
+        const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
         const uint32_t s_tmem = tmem + lane_addr + 256 * t;
-        const uint32_t o_tmem = s_tmem + 128;
-        const int row = (warp & 3) * 32 + lane;
+        const uint32_t o_half = s_tmem + 128 + 64 * hc;
+        const int row = q4 * 32 + lane;
+        const uint32_t xbar = bar_x + 8 * (2 * (4 * t + q4));
         float m = -INFINITY, l = 0.0f;
         // this row's slot in a shard state (rows past the segment read a
         // valid row and write nothing)
-        const size_t rowi = ((size_t)b * g.H + h) * g.S + min(q0[t] + row, q_end - 1);
+        const size_t rowi = ((size_t)b * g.H + h) * g.S + min(q0t + row, q_end - 1);
         if (kShard && j0 > 0) {
             m = a.st_in_m[rowi];
             l = a.st_in_l[rowi];
         }
+        // the row sum of tile j is (half 0's sum) + (half 1's sum), folded
+        // into l as l = fmaf(l, alpha_j, rs_j) at the next exchange
+        float rs_prev = 0.0f, alpha_prev = 1.0f;
         bool ok = true;
+        auto exchange = [&](int j, float mine_max, float mine_sum, float2& other) {
+            xch[j & 1][t][hc][row] = make_float2(mine_max, mine_sum);
+            mbar_arrive(xbar + 8 * (j & 1));
+            if (!mbar_wait(xbar + 8 * (j & 1), (j >> 1) & 1, &abort_flag, kWaitLimitNs)) return false;
+            other = xch[j & 1][t][hc ^ 1][row];
+            return true;
+        };
         for (int j = 0; j < nkt; ++j) {
             if (!warp_wait(bar_s + 8 * t, j & 1, &abort_flag)) {
                 ok = false;
@@ -358,28 +387,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             }
             tc_fence_after();
             const TileInfo ti = kv_tile(g, L, nkt_txt, j0 + j);
-            const int nvalid = ti.kend - ti.k0;  // keys k0 + c with c < nvalid are valid
-            // the row's 128 scores in one register array, loaded at once;
-            // the packed P later reuses its first 64 entries in place
-            uint32_t r[128];
-            tmem_ld32(s_tmem, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-            tmem_ld32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-            tmem_ld32(s_tmem + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
-            tmem_ld32(s_tmem + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+            const int nvalid = ti.kend - ti.k0 - 64 * hc;  // keys of this half with c < nvalid are valid
+            // the half row's 64 scores; the packed P later reuses the first 32 entries
+            uint32_t r[64];
+            tmem_ld32(s_tmem + 64 * hc, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+            tmem_ld32(s_tmem + 64 * hc + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
             tmem_ld_wait();
-            if (nvalid < 128) {
+            if (nvalid < 64) {
 #pragma unroll
-                for (int i = 0; i < 128; ++i) r[i] = i < nvalid ? r[i] : 0xff800000u;  // -inf
+                for (int i = 0; i < 64; ++i) r[i] = i < nvalid ? r[i] : 0xff800000u;  // -inf
             }
-            // row max of the raw scores: eight interleaved partial maxima,
-            // then a fixed tree (max is exact in any order)
+            // max of the half row: eight interleaved partial maxima, then a
+            // fixed tree; the row max is the larger of the two halves' (max
+            // is exact in any order)
             float mp[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mp[i] = __uint_as_float(r[i]);
+            for (int e = 0; e < 8; ++e)
+                mp[e] = fmax3(__uint_as_float(r[e]), __uint_as_float(r[8 + e]), __uint_as_float(r[16 + e]));
 #pragma unroll
-            for (int i = 8; i < 128; ++i) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(r[i]));
-            const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+            for (int e = 0; e < 8; ++e) mp[e] = fmax3(mp[e], __uint_as_float(r[24 + e]), __uint_as_float(r[32 + e]));
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mp[e] = fmax3(mp[e], __uint_as_float(r[40 + e]), __uint_as_float(r[48 + e]));
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mp[e] = fmaxf(mp[e], __uint_as_float(r[56 + e]));
+            const float pm = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                    fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+            float2 other;
+            if (!exchange(j, pm, rs_prev, other)) {
+                ok = false;
+                break;
+            }
+            if (j > 0) l = fmaf(l, alpha_prev, rs_prev + other.y);  // (a + b == b + a exactly)
+            const float mx = fmaxf(pm, other.x);
             // Lazy rescaling: a row moves its reference max m only when the
             // new max exceeds it by more than 8 (a factor 256), so rows
             // rarely touch O; until then p = exp2(s c - m) <= 256, exact in
@@ -389,23 +428,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             const bool move = m_cand > m + 8.0f;      // always true on the first tile
             const float m_new = move ? m_cand : m;
             const float alpha = move ? exp2f(m - m_new) : 1.0f;
-            // p = exp2(s * c - m), packed to bf16 into r[0..63] (pair i lands
-            // on an entry already read); the row sum adds column i into
-            // partial i % 8, partials in a fixed tree
-            float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            // p = exp2(s * c - m), packed to bf16 into r[0..31] (pair i lands
+            // on an entry already read); the half row's sum adds its column
+            // i into partial i % 8, partials in a fixed tree (the argument
+            // and the partial sums two lanes at a time: each lane rounds as
+            // the scalar fmaf / add would)
+            uint64_t sp2[4] = {0ull, 0ull, 0ull, 0ull};
+            const uint64_t c2 = f2_pack(kC, kC), nm2 = f2_pack(-m_new, -m_new);
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const float p0 = exp2_num(fmaf(__uint_as_float(r[2 * i]), kC, -m_new));
-                const float p1 = exp2_num(fmaf(__uint_as_float(r[2 * i + 1]), kC, -m_new));
-                sp[(2 * i) & 7] += p0;
-                sp[(2 * i + 1) & 7] += p1;
+            for (int i = 0; i < 32; ++i) {
+                float x0, x1;
+                f2_unpack(fma_f2(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c2, nm2), x0, x1);
+                const float p0 = exp2_num(x0), p1 = exp2_num(x1);
+                sp2[i & 3] = add_f2(sp2[i & 3], f2_pack(p0, p1));
                 r[i] = pack_bf16(p0, p1);
             }
-            const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-            l = fmaf(l, alpha, rs);  // one rounding, as the standalone softmax operator
+            float sp[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f2_unpack(sp2[e], sp[2 * e], sp[2 * e + 1]);
+            rs_prev = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+            alpha_prev = alpha;
             m = m_new;
-            tmem_st32(s_tmem, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-            tmem_st32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+            // P of keys [64 hc, + 64) as bf16 pairs over S columns [32 hc, + 32)
+            // (both halves have read their scores: the exchange came after)
+            tmem_st32(s_tmem + 32 * hc, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
             if (j > 0) {
                 // PV_{j-1} has finished writing O
                 if (!warp_wait(bar_o + 8 * t, (j - 1) & 1, &abort_flag)) {
@@ -413,27 +459,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                     break;
                 }
                 tc_fence_after();
-                // rescale O in the rows that moved their max; the decision is
-                // warp-wide and the other rows scale by exactly 1
+                // rescale this half of O in the rows that moved their max; the
+                // decision is warp-wide and the other rows scale by exactly 1
                 if (__any_sync(0xffffffffu, move)) {
-                    uint32_t (&o32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[64]);
+                    uint32_t o32[32];
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        tmem_ld32(o_tmem + 32 * c, o32);
+                    for (int c = 0; c < 2; ++c) {
+                        tmem_ld32(o_half + 32 * c, o32);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
-                        tmem_st32(o_tmem + 32 * c, o32);
+                        tmem_st32(o_half + 32 * c, o32);
                     }
                 }
             } else if (kShard && j0 > 0) {
                 // first tile of a later shard: O is the previous shard's,
                 // scaled by alpha as above (alpha is exactly 1 in rows whose
                 // reference max stays, so those keep their bits)
-                uint32_t (&o32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[64]);
-                const float4* oin = reinterpret_cast<const float4*>(a.st_in_o + rowi * kHeadDim);
+                uint32_t o32[32];
+                const float4* oin = reinterpret_cast<const float4*>(a.st_in_o + rowi * kHeadDim + 64 * hc);
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const float4 x = oin[8 * c + i];
@@ -442,26 +488,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                         o32[4 * i + 2] = __float_as_uint(x.z * alpha);
                         o32[4 * i + 3] = __float_as_uint(x.w * alpha);
                     }
-                    tmem_st32(o_tmem + 32 * c, o32);
+                    tmem_st32(o_half + 32 * c, o32);
                 }
             }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_p + 8 * t);
         }
+        // the last tile's row sum
+        if (ok && nkt > 0) {
+            float2 other;
+            if (exchange(nkt, 0.0f, rs_prev, other))
+                l = fmaf(l, alpha_prev, rs_prev + other.y);
+            else
+                ok = false;
+        }
         if (ok && !last_shard && warp_wait(bar_o + 8 * t, (nkt - 1) & 1, &abort_flag)) {
             tc_fence_after();
             // hand the state on: m, l and O (not divided by l), fp32
-            const bool mine = q0[t] + row < q_end;
-            if (mine) {
+            const bool mine = q0t + row < q_end;
+            if (mine && hc == 0) {
                 a.st_out_m[rowi] = m;
                 a.st_out_l[rowi] = l;
             }
-            float4* oout = reinterpret_cast<float4*>(a.st_out_o + rowi * kHeadDim);
+            float4* oout = reinterpret_cast<float4*>(a.st_out_o + rowi * kHeadDim + 64 * hc);
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t r[32];
-                tmem_ld32(o_tmem + 32 * c, r);
+                tmem_ld32(o_half + 32 * c, r);
                 tmem_ld_wait();
                 if (mine) {
 #pragma unroll
@@ -474,39 +528,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             tc_fence_after();
             // O / l as bf16 into this tile's Q buffer (its last S product has
             // finished) as two 128-row x 128-byte boxes in the 128-byte
-            // swizzle; one thread of the group then stores the tile with
-            // TMA, the segment map clipping rows past the segment.
+            // swizzle, box hc from this thread; one thread of the tile then
+            // stores it with TMA, the segment map clipping rows past the
+            // segment.
             const float inv = 1.0f / l;
-            const int n = q0[t] + row;
+            const int n = q0t + row;
             const uint32_t stg_u32 = sQ + t * kTileBytes;
             uint8_t* stg = smem_raw + (stg_u32 - smem_u32(smem_raw));
             const int sw = row & 7;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t r[32];
-                tmem_ld32(o_tmem + 32 * c, r);
+                tmem_ld32(o_half + 32 * c, r);
                 tmem_ld_wait();
-                uint8_t* orow = stg + (c >> 1) * kBoxBytes + row * 128;
+                uint8_t* orow = stg + hc * kBoxBytes + row * 128;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         w[e] = pack_bf16(__uint_as_float(r[8 * q + 2 * e]) * inv, __uint_as_float(r[8 * q + 2 * e + 1]) * inv);
-                    *reinterpret_cast<uint4*>(orow + ((((c & 1) * 4 + q) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(orow + (((c * 4 + q) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             fence_proxy_async_smem();
-            named_barrier_sync(1 + t, 128);
-            if ((warp & 3) == 0 && lane == 0) {
+            named_barrier_sync(1 + t, 256);
+            if (warp == 4 * t && lane == 0) {
                 const int seg = q_txt ? 0 : 1;
-                const int srow = q0[t] - seg0;
+                const int srow = q0t - seg0;
                 tma_store_4d(&a.map_o[seg], stg_u32, 0, h, srow, b);
                 tma_store_4d(&a.map_o[seg], stg_u32 + kBoxBytes, 64, h, srow, b);
                 bulk_commit_group();
                 bulk_wait_read_all();
             }
-            if (n < q_end && a.lse != nullptr) a.lse[((size_t)b * g.H + h) * g.S + n] = (m + log2f(l)) * kLn2;
+            if (hc == 0 && n < q_end && a.lse != nullptr) a.lse[((size_t)b * g.H + h) * g.S + n] = (m + log2f(l)) * kLn2;
         } else {
             fail(&abort_flag);
         }

@@ -18,7 +18,8 @@
 //   softmax   per query row, key tiles in the fused order (text tiles that
 //             hold a valid key, then image tiles): the same masking, lazy
 //             reference max (moves only past a 2^8 growth), exp2f
-//             numerators, eight-way partial row sums and fixed sum tree; it
+//             numerators, eight-way partial sums and a fixed tree per 64-key
+//             half, the two halves' sums added; it
 //             writes P (bf16, relative to the row's reference max at that
 //             tile), the rescale factor alpha of every tile, the final row
 //             sum l and lse.
@@ -420,16 +421,24 @@ __global__ void __launch_bounds__(32) softmax_kernel(const __grid_constant__ SmA
         const bool move = m_cand > m + 8.0f;
         const float m_new = move ? m_cand : m;
         const float alpha = move ? exp2f(m - m_new) : 1.0f;
-        float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // the row sum as the fused kernel's two threads of a row form it:
+        // per 64-key half, column i into partial i % 8, partials in a fixed
+        // tree; then half 0 + half 1
+        float rs_half[2];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            const float p0 = exp2_num(fmaf(__uint_as_float(r[2 * i]), kC, -m_new));
-            const float p1 = exp2_num(fmaf(__uint_as_float(r[2 * i + 1]), kC, -m_new));
-            sp[(2 * i) & 7] += p0;
-            sp[(2 * i + 1) & 7] += p1;
-            r[i] = pack_bf16(p0, p1);
+        for (int hc = 0; hc < 2; ++hc) {
+            float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 32 * hc; i < 32 * hc + 32; ++i) {
+                const float p0 = exp2_num(fmaf(__uint_as_float(r[2 * i]), kC, -m_new));
+                const float p1 = exp2_num(fmaf(__uint_as_float(r[2 * i + 1]), kC, -m_new));
+                sp[(2 * i) & 7] += p0;
+                sp[(2 * i + 1) & 7] += p1;
+                r[i] = pack_bf16(p0, p1);
+            }
+            rs_half[hc] = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
         }
-        const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+        const float rs = rs_half[0] + rs_half[1];
         l = fmaf(l, alpha, rs);
         m = m_new;
         // P: the previous tile's stores have read the staging

@@ -73,6 +73,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
     }
 }
 
+// A wait with the time limit alone, for draining copies and products
+// already in flight after a failure (no abort flag to read).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // Like mbar_wait, but a failed poll sleeps about sleep_ns before the next,
 // so a warp whose wait is not on the critical path leaves its SMSP's issue
 // slots to the others (same time limit and abort rule).
@@ -256,6 +267,42 @@ __device__ __forceinline__ uint64_t sdesc_noswizzle(uint32_t saddr, uint32_t lbo
     d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
     d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;  // descriptor version of this architecture; layout 0: no swizzle
+    return d;
+}
+
+// Two fp32 lanes at once (fma / add / sub / mul .rn.f32x2): each lane rounds
+// exactly as the scalar instruction does, in half the issue slots.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    lo = __uint_as_float((uint32_t)v);
+    hi = __uint_as_float((uint32_t)(v >> 32));
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// max(a, b, c) in one instruction (exact, like two fmaxf)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
 }
 
