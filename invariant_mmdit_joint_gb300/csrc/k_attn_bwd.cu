@@ -155,8 +155,14 @@ __device__ __forceinline__ void q_tile(const Geom& g, int i, int& q0, int& q_end
 // or after the tiles). A slot frees on chain X's commit: every product
 // reading it has been issued by then, the S^T and dP^T ones completed
 // before the warps formed that tile's P^T and dS^T.
-constexpr int kKvWarps = kEwWarps + 3;                // + TMA producer + two MMA issuers
+// Warps 0-7 (elementwise) and 8-11 (TMA producer, the two issuers, one idle
+// warp) are three warpgroups launched at 168 registers a thread; the helper
+// warpgroup drops to 56 and the elementwise ones rise to 224 (setmaxnreg), so
+// the warps on the critical path run without spills (705 -> 660 us).
+constexpr int kKvWarps = kEwWarps + 4;  // + TMA producer, two MMA issuers, one idle warp (a full warpgroup)
 constexpr int kKvThreads = 32 * kKvWarps;
+// registers per thread at launch, and after the split (helper warpgroup, elementwise warpgroups)
+constexpr int kKvRegs = 168, kKvRegsHelper = 56, kKvRegsEw = 224;
 constexpr int kKvWarpTma = kEwWarps, kKvWarpMma = kEwWarps + 1, kKvWarpMma2 = kEwWarps + 2;
 constexpr int kKvQSlots = 3, kKvOSlots = 2;
 constexpr int kKvSmemK = 0, kKvSmemV = kTileBytes, kKvSmemQ = 2 * kTileBytes;
@@ -260,149 +266,157 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc_kernel(const _
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    if (warp == kKvWarpTma) {
-        // ------------------------------------------------ TMA producer
-        // In order: K, V; then per query tile i its Q slot (free once dK_{i-3}
-        // has run) and its dO slot with lse2 and Delta (free once dV_{i-2}
-        // has run, which follows the warps' last read of that tile).
-        if (lane == 0) {
-            prefetch_tensormap(&a.map_q);
-            prefetch_tensormap(&a.map_k);
-            prefetch_tensormap(&a.map_v[0]);
-            prefetch_tensormap(&a.map_v[1]);
-            prefetch_tensormap(&a.map_do[0]);
-            prefetch_tensormap(&a.map_do[1]);
-            mbar_expect_tx(bar_kv, 2 * kTileBytes);
-            tma_load_2d(sK, &a.map_k, bar_kv, 0, row_base + k0);
-            tma_load_2d(sK + kBoxBytes, &a.map_k, bar_kv, 64, row_base + k0);
-            // tiles never straddle the streams: rows counted from the segment start
-            const int vseg = k_txt ? 0 : 1, vrow = k_txt ? k0 : k0 - g.T_txt;
-            tma_load_4d(sV, &a.map_v[vseg], bar_kv, 0, h, vrow, b);
-            tma_load_4d(sV + kBoxBytes, &a.map_v[vseg], bar_kv, 64, h, vrow, b);
-            int issued = 0;
-            for (int i = 0; i < nq && !abort_flag; ++i) {
-                const int jq = i % kKvQSlots, jo = i & 1;
-                int q0, q_end;
-                q_tile(g, i, q0, q_end);
-                // the copies run ahead of the products: their waits back off
-                // (512 ns per failed poll) to leave SMSP 0's issue slots to
-                // the elementwise warps there (708.5 against 711 us)
-                if (i >= kKvQSlots && !mbar_wait_backoff(bar_qe + 8 * jq, ((i / kKvQSlots) + 1) & 1, &abort_flag,
-                                                         kWaitLimitNs, kProducerSleepNs)) {
-                    fail(&abort_flag);
-                    break;
-                }
-                const uint32_t bq = bar_qf + 8 * jq;
-                mbar_expect_tx(bq, kTileBytes);
-                tma_load_2d(slot_q(i), &a.map_q, bq, 0, row_base + q0);
-                tma_load_2d(slot_q(i) + kBoxBytes, &a.map_q, bq, 64, row_base + q0);
-                if (i >= 2 && !mbar_wait_backoff(bar_oe + 8 * jo, ((i >> 1) + 1) & 1, &abort_flag, kWaitLimitNs,
-                                                 kProducerSleepNs)) {
-                    fail(&abort_flag);
-                    break;
-                }
-                const uint32_t bo = bar_of + 8 * jo;
-                mbar_expect_tx(bo, kTileBytes + 1024);
-                const int oseg = i < g.ntq_txt ? 0 : 1, orow = oseg ? q0 - g.T_txt : q0;
-                tma_load_4d(slot_o(i), &a.map_do[oseg], bo, 0, h, orow, b);
-                tma_load_4d(slot_o(i) + kBoxBytes, &a.map_do[oseg], bo, 64, h, orow, b);
-                const size_t slot = bh * g.nq_pad + (size_t)i * 128;
-                bulk_load(slot_l(i), a.lse2_p + slot, 512, bo);
-                bulk_load(slot_l(i) + 512, a.delta_p + slot, 512, bo);
-                issued = i + 1;
-            }
-            // leave no copy in flight
-            const volatile int no_abort = 0;
-            mbar_wait(bar_kv, 0, &no_abort, kWaitLimitNs);
-            for (int i = issued - kKvQSlots < 0 ? 0 : issued - kKvQSlots; i < issued; ++i)
-                mbar_wait(bar_qf + 8 * (i % kKvQSlots), (i / kKvQSlots) & 1, &no_abort, kWaitLimitNs);
-            for (int i = issued - 2 < 0 ? 0 : issued - 2; i < issued; ++i)
-                mbar_wait(bar_of + 8 * (i & 1), (i >> 1) & 1, &no_abort, kWaitLimitNs);
-        }
-    } else if (warp == kKvWarpMma || warp == kKvWarpMma2) {
-        // ------------------------------------------------ MMA issuers (chains X, Y)
-        if (lane == 0) {
-            const bool chain_y = warp == kKvWarpMma2;
-            auto issue_scores = [&](int i, bool dp) {
-                const uint32_t at = dp ? sV : sK, bt = dp ? slot_o(i) : slot_q(i);
-                const uint32_t d = tmem + kColR + 128u * (uint32_t)(i & 1);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(d, desc_kmajor(at, kk), desc_kmajor(bt, kk), kIdescKK, kk > 0);
-                mma_commit((dp ? bar_dp : bar_st) + 8 * (i & 1));
-            };
-            bool ok = mbar_wait(bar_kv, 0, &abort_flag, kWaitLimitNs);
-            if (chain_y) {
-                ok = ok && mbar_wait(bar_qf, 0, &abort_flag, kWaitLimitNs);
-                if (ok) {
-                    tc_fence_after();
-                    issue_scores(0, false);
-                }
-                if (ok && nq > 1) {
-                    ok = mbar_wait(bar_qf + 8, 0, &abort_flag, kWaitLimitNs);
-                    if (ok) {
-                        tc_fence_after();
-                        issue_scores(1, false);
-                    }
-                }
-                ok = ok && mbar_wait(bar_sr, 0, &abort_flag, kWaitLimitNs) && mbar_wait(bar_of, 0, &abort_flag, kWaitLimitNs);
-                if (ok) {
-                    tc_fence_after();
-                    issue_scores(0, true);
-                }
-                for (int i = 0; ok && i < nq; ++i) {
-                    const int r = i & 1;
-                    if (i + 1 < nq) {
-                        if (!mbar_wait(bar_sr + 8 * (r ^ 1), ((i + 1) >> 1) & 1, &abort_flag, kWaitLimitNs) ||
-                            !mbar_wait(bar_of + 8 * ((i + 1) & 1), ((i + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        issue_scores(i + 1, true);
-                    }
-                    if (i + 2 < nq) {
-                        if (!mbar_wait(bar_rf + 8 * r, (i >> 1) & 1, &abort_flag, kWaitLimitNs) ||
-                            !mbar_wait(bar_qf + 8 * ((i + 2) % kKvQSlots), ((i + 2) / kKvQSlots) & 1, &abort_flag,
-                                       kWaitLimitNs)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        issue_scores(i + 2, false);
-                    }
-                }
-            } else {
-                for (int i = 0; ok && i < nq; ++i) {
-                    const int r = i & 1;
-                    const uint32_t reg = tmem + kColR + 128u * (uint32_t)r;
-                    if (!mbar_wait(bar_pds + 8 * r, (i >> 1) & 1, &abort_flag, kWaitLimitNs)) {
-                        ok = false;
+    // Register split: the helper warpgroup gives registers up and the two
+    // elementwise warpgroups take them, from the launch's own allotment
+    // (the host launches only when the kernel was built at kKvRegs).
+    static_assert(32 * (kKvWarps - kEwWarps) * kKvRegsHelper + 32 * kEwWarps * kKvRegsEw == kKvThreads * kKvRegs,
+                  "register split must equal the launch allotment");
+    if (warp >= kEwWarps) {
+        setmaxnreg_dec<kKvRegsHelper>();
+        if (warp == kKvWarpTma) {
+            // ------------------------------------------------ TMA producer
+            // In order: K, V; then per query tile i its Q slot (free once dK_{i-3}
+            // has run) and its dO slot with lse2 and Delta (free once dV_{i-2}
+            // has run, which follows the warps' last read of that tile).
+            if (lane == 0) {
+                prefetch_tensormap(&a.map_q);
+                prefetch_tensormap(&a.map_k);
+                prefetch_tensormap(&a.map_v[0]);
+                prefetch_tensormap(&a.map_v[1]);
+                prefetch_tensormap(&a.map_do[0]);
+                prefetch_tensormap(&a.map_do[1]);
+                mbar_expect_tx(bar_kv, 2 * kTileBytes);
+                tma_load_2d(sK, &a.map_k, bar_kv, 0, row_base + k0);
+                tma_load_2d(sK + kBoxBytes, &a.map_k, bar_kv, 64, row_base + k0);
+                // tiles never straddle the streams: rows counted from the segment start
+                const int vseg = k_txt ? 0 : 1, vrow = k_txt ? k0 : k0 - g.T_txt;
+                tma_load_4d(sV, &a.map_v[vseg], bar_kv, 0, h, vrow, b);
+                tma_load_4d(sV + kBoxBytes, &a.map_v[vseg], bar_kv, 64, h, vrow, b);
+                int issued = 0;
+                for (int i = 0; i < nq && !abort_flag; ++i) {
+                    const int jq = i % kKvQSlots, jo = i & 1;
+                    int q0, q_end;
+                    q_tile(g, i, q0, q_end);
+                    // the copies run ahead of the products: their waits back off
+                    // (512 ns per failed poll) to leave SMSP 0's issue slots to
+                    // the elementwise warps there (708.5 against 711 us)
+                    if (i >= kKvQSlots && !mbar_wait_backoff(bar_qe + 8 * jq, ((i / kKvQSlots) + 1) & 1, &abort_flag,
+                                                             kWaitLimitNs, kProducerSleepNs)) {
+                        fail(&abort_flag);
                         break;
                     }
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tmem + kColDV, reg + p_col(kk), desc_mnmajor(slot_o(i), kk), kIdescKM,
-                               (i > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(bar_oe + 8 * (i & 1));
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tmem + kColDK, reg + ds_col(kk), desc_mnmajor(slot_q(i), kk), kIdescKM,
-                               (i > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(bar_qe + 8 * (i % kKvQSlots));
-                    mma_commit(bar_rf + 8 * r);
+                    const uint32_t bq = bar_qf + 8 * jq;
+                    mbar_expect_tx(bq, kTileBytes);
+                    tma_load_2d(slot_q(i), &a.map_q, bq, 0, row_base + q0);
+                    tma_load_2d(slot_q(i) + kBoxBytes, &a.map_q, bq, 64, row_base + q0);
+                    if (i >= 2 && !mbar_wait_backoff(bar_oe + 8 * jo, ((i >> 1) + 1) & 1, &abort_flag, kWaitLimitNs,
+                                                     kProducerSleepNs)) {
+                        fail(&abort_flag);
+                        break;
+                    }
+                    const uint32_t bo = bar_of + 8 * jo;
+                    mbar_expect_tx(bo, kTileBytes + 1024);
+                    const int oseg = i < g.ntq_txt ? 0 : 1, orow = oseg ? q0 - g.T_txt : q0;
+                    tma_load_4d(slot_o(i), &a.map_do[oseg], bo, 0, h, orow, b);
+                    tma_load_4d(slot_o(i) + kBoxBytes, &a.map_do[oseg], bo, 64, h, orow, b);
+                    const size_t slot = bh * g.nq_pad + (size_t)i * 128;
+                    bulk_load(slot_l(i), a.lse2_p + slot, 512, bo);
+                    bulk_load(slot_l(i) + 512, a.delta_p + slot, 512, bo);
+                    issued = i + 1;
                 }
-                if (ok) mma_commit(bar_done);
+                // leave no copy in flight
+                const volatile int no_abort = 0;
+                mbar_wait(bar_kv, 0, &no_abort, kWaitLimitNs);
+                for (int i = issued - kKvQSlots < 0 ? 0 : issued - kKvQSlots; i < issued; ++i)
+                    mbar_wait(bar_qf + 8 * (i % kKvQSlots), (i / kKvQSlots) & 1, &no_abort, kWaitLimitNs);
+                for (int i = issued - 2 < 0 ? 0 : issued - 2; i < issued; ++i)
+                    mbar_wait(bar_of + 8 * (i & 1), (i >> 1) & 1, &no_abort, kWaitLimitNs);
             }
-            if (!ok) fail(&abort_flag);
-            const uint32_t my_drain = bar_drain + (chain_y ? 8 : 0);
-            mma_commit(my_drain);
-            const volatile int no_abort = 0;
-            mbar_wait(my_drain, 0, &no_abort, kWaitLimitNs);
+        } else if (warp == kKvWarpMma || warp == kKvWarpMma2) {
+            // ------------------------------------------------ MMA issuers (chains X, Y)
+            if (lane == 0) {
+                const bool chain_y = warp == kKvWarpMma2;
+                auto issue_scores = [&](int i, bool dp) {
+                    const uint32_t at = dp ? sV : sK, bt = dp ? slot_o(i) : slot_q(i);
+                    const uint32_t d = tmem + kColR + 128u * (uint32_t)(i & 1);
+    #pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(d, desc_kmajor(at, kk), desc_kmajor(bt, kk), kIdescKK, kk > 0);
+                    mma_commit((dp ? bar_dp : bar_st) + 8 * (i & 1));
+                };
+                bool ok = mbar_wait(bar_kv, 0, &abort_flag, kWaitLimitNs);
+                if (chain_y) {
+                    ok = ok && mbar_wait(bar_qf, 0, &abort_flag, kWaitLimitNs);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_scores(0, false);
+                    }
+                    if (ok && nq > 1) {
+                        ok = mbar_wait(bar_qf + 8, 0, &abort_flag, kWaitLimitNs);
+                        if (ok) {
+                            tc_fence_after();
+                            issue_scores(1, false);
+                        }
+                    }
+                    ok = ok && mbar_wait(bar_sr, 0, &abort_flag, kWaitLimitNs) &&
+                         mbar_wait(bar_of, 0, &abort_flag, kWaitLimitNs);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_scores(0, true);
+                    }
+                    for (int i = 0; ok && i < nq; ++i) {
+                        const int r = i & 1;
+                        if (i + 1 < nq) {
+                            if (!mbar_wait(bar_sr + 8 * (r ^ 1), ((i + 1) >> 1) & 1, &abort_flag, kWaitLimitNs) ||
+                                !mbar_wait(bar_of + 8 * ((i + 1) & 1), ((i + 1) >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_scores(i + 1, true);
+                        }
+                        if (i + 2 < nq) {
+                            if (!mbar_wait(bar_rf + 8 * r, (i >> 1) & 1, &abort_flag, kWaitLimitNs) ||
+                                !mbar_wait(bar_qf + 8 * ((i + 2) % kKvQSlots), ((i + 2) / kKvQSlots) & 1, &abort_flag,
+                                           kWaitLimitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_scores(i + 2, false);
+                        }
+                    }
+                } else {
+                    for (int i = 0; ok && i < nq; ++i) {
+                        const int r = i & 1;
+                        const uint32_t reg = tmem + kColR + 128u * (uint32_t)r;
+                        if (!mbar_wait(bar_pds + 8 * r, (i >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+    #pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ts(tmem + kColDV, reg + p_col(kk), desc_mnmajor(slot_o(i), kk), kIdescKM,
+                                   (i > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(bar_oe + 8 * (i & 1));
+    #pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ts(tmem + kColDK, reg + ds_col(kk), desc_mnmajor(slot_q(i), kk), kIdescKM,
+                                   (i > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(bar_qe + 8 * (i % kKvQSlots));
+                        mma_commit(bar_rf + 8 * r);
+                    }
+                    if (ok) mma_commit(bar_done);
+                }
+                if (!ok) fail(&abort_flag);
+                const uint32_t my_drain = bar_drain + (chain_y ? 8 : 0);
+                mma_commit(my_drain);
+                mbar_wait_drain(my_drain, 0, kWaitLimitNs);
+            }
         }
     } else {
+        setmaxnreg_inc<kKvRegsEw>();
         // ------------------------------------------------ elementwise warps
         // warp w: key rows 32 * (w % 4) + lane, query columns
         // [kEwCols * grp, kEwCols * (grp + 1)), grp = w / 4. No row
@@ -812,6 +826,13 @@ cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16
     cudaError_t e =
         cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmemBytes);
     if (e != cudaSuccess) return e;
+    // the warpgroups' register split adds up to kKvRegs per launched thread:
+    // a build at any other count would leave the elementwise warps waiting
+    // for registers that are not there, so it is not launched
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, attn_bwd_dkdv_tc_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kKvRegs) return cudaErrorInvalidConfiguration;
     dim3 grid(g.ntq_txt + g.ntq_img, n_pairs);
     timing_begin(kKBwdDkDv, s);
     attn_bwd_dkdv_tc_kernel<<<grid, kKvThreads, kKvSmemBytes, s>>>(args);

@@ -73,6 +73,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
     }
 }
 
+// Move registers between warpgroups (every warp of a warpgroup runs the same
+// one): the pool is what the block was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+
 // A wait with the time limit alone, for draining copies and products
 // already in flight after a failure (no abort flag to read).
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
