@@ -132,7 +132,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 template <bool kShard>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ FwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[32];
+    __shared__ __align__(8) uint64_t bars[34];
     // the two threads of a query row trade their half's partial row max of
     // this key tile and their half's row sum of the previous one, through
     // slot j & 1 of (tile, half, row)
@@ -196,7 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
     const uint32_t bar_ke = smem_u32(&bars[5]);   // [2] K slot free (S_A, S_B done)
     const uint32_t bar_ve = smem_u32(&bars[7]);   // [2] V slot free (PV_A, PV_B done)
     const uint32_t bar_s = smem_u32(&bars[9]);    // [2] per Q tile: S ready
-    const uint32_t bar_p = smem_u32(&bars[11]);   // [2] per Q tile: P written
+    const uint32_t bar_p = smem_u32(&bars[11]);   // [2] per Q tile: P of key chunk 0 written
+    const uint32_t bar_p1 = smem_u32(&bars[32]);  // [2] per Q tile: P of key chunk 1 written
     const uint32_t bar_o = smem_u32(&bars[13]);   // [2] per Q tile: PV done
     const uint32_t bar_drain = smem_u32(&bars[15]);
     const uint32_t bar_x = smem_u32(&bars[16]);   // [tile][quarter][slot]: both halves' values written
@@ -211,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             mbar_init(bar_ve + 8 * s, 1);
             mbar_init(bar_s + 8 * s, 1);
             mbar_init(bar_p + 8 * s, 256);
+            mbar_init(bar_p1 + 8 * s, 256);
             mbar_init(bar_o + 8 * s, 1);
         }
         mbar_init(bar_drain, 1);
@@ -290,14 +292,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                 }
                 mma_commit(bar_s + 8 * t);
             };
-            // O_t += P_t V_j, P_t read from TMEM over S_t
-            auto issue_pv = [&](int t, int j) {
+            // O_t += P_t V_j, P_t read from TMEM over S_t, in two parts: key
+            // chunk 0 (k-steps 0, 1, 4, 5: keys 0-31 and 64-95, the first
+            // P each softmax thread writes) once its P is written, then key
+            // chunk 1 (k-steps 2, 3, 6, 7); that k-step order is the
+            // accumulation order of O
+            auto issue_pv = [&](int t, int j, int part) {
                 const uint32_t dv = sV + (j & 1) * kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
+                for (int i = 0; i < 4; ++i) {
+                    const int kk = 2 * part + (i & 1) + 4 * (i >> 1);
                     mma_ts(tmem + 256 * t + 128, tmem + 256 * t + kk * 8, sdesc_sw128(dv + kk * 2048, kBoxBytes, 1024),
                            idesc_o, (j0 + j > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar_o + 8 * t);
+                }
+                if (part == 1) mma_commit(bar_o + 8 * t);
+            };
+            auto wait_p = [&](uint32_t bar, int j) {
+                return mbar_test(bar, j & 1) || mbar_wait(bar, j & 1, &abort_flag, kWaitLimitNs);
             };
             bool ok = mbar_wait(bar_q, 0, &abort_flag, kWaitLimitNs) &&
                       mbar_wait(bar_kf, 0, &abort_flag, kWaitLimitNs);
@@ -326,16 +337,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                     break;
                 }
                 tc_fence_after();
-                issue_pv(0, j);
+                issue_pv(0, j, 0);
+                if (!wait_p(bar_p1, j)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                issue_pv(0, j, 1);
                 if (more) issue_s(0, j + 1);
                 if (has_b) {
                     // PV_B(j) needs P_B(j); S_B(j+1) reads the K(j+1) checked above
-                    if (!mbar_test(bar_p + 8, j & 1) && !mbar_wait(bar_p + 8, j & 1, &abort_flag, kWaitLimitNs)) {
+                    if (!wait_p(bar_p + 8, j)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    issue_pv(1, j);
+                    issue_pv(1, j, 0);
+                    if (!wait_p(bar_p1 + 8, j)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv(1, j, 1);
                 }
                 mma_commit(bar_ve + 8 * s);
                 if (more) {
@@ -435,23 +458,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             // the scalar fmaf / add would)
             uint64_t sp2[4] = {0ull, 0ull, 0ull, 0ull};
             const uint64_t c2 = f2_pack(kC, kC), nm2 = f2_pack(-m_new, -m_new);
+            auto numerators = [&](int i0) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                float x0, x1;
-                f2_unpack(fma_f2(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c2, nm2), x0, x1);
-                const float p0 = exp2_num(x0), p1 = exp2_num(x1);
-                sp2[i & 3] = add_f2(sp2[i & 3], f2_pack(p0, p1));
-                r[i] = pack_bf16(p0, p1);
-            }
-            float sp[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) f2_unpack(sp2[e], sp[2 * e], sp[2 * e + 1]);
-            rs_prev = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-            alpha_prev = alpha;
-            m = m_new;
-            // P of keys [64 hc, + 64) as bf16 pairs over S columns [32 hc, + 32)
-            // (both halves have read their scores: the exchange came after)
-            tmem_st32(s_tmem + 32 * hc, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                for (int i = i0; i < i0 + 16; ++i) {
+                    float x0, x1;
+                    f2_unpack(fma_f2(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c2, nm2), x0,
+                              x1);
+                    const float p0 = exp2_num(x0), p1 = exp2_num(x1);
+                    sp2[i & 3] = add_f2(sp2[i & 3], f2_pack(p0, p1));
+                    r[i] = pack_bf16(p0, p1);
+                }
+            };
+            // key chunk 0 (this half's first 32 keys): P over S columns
+            // [32 hc, + 16) (all halves have read their scores: the exchange
+            // came after), then O rescaled, then the chunk handed to the MMA
+            numerators(0);
+            tmem_st16(s_tmem + 32 * hc, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
             if (j > 0) {
                 // PV_{j-1} has finished writing O
                 if (!warp_wait(bar_o + 8 * t, (j - 1) & 1, &abort_flag)) {
@@ -494,6 +516,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_p + 8 * t);
+            // key chunk 1 (the half's last 32 keys): P over S columns [32 hc + 16, + 16)
+            numerators(16);
+            tmem_st16(s_tmem + 32 * hc + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar_p1 + 8 * t);
+            float sp[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f2_unpack(sp2[e], sp[2 * e], sp[2 * e + 1]);
+            rs_prev = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+            alpha_prev = alpha;
+            m = m_new;
         }
         // the last tile's row sum
         if (ok && nkt > 0) {

@@ -23,8 +23,9 @@
 //             writes P (bf16, relative to the row's reference max at that
 //             tile), the rescale factor alpha of every tile, the final row
 //             sum l and lse.
-//   av_gemm   the same tcgen05 TS products O += P V (P in TMEM as the A
-//             operand, V tiles MN-major in shared memory), O rescaled in
+//   av_gemm   the same tcgen05 products O += P V (k-steps of 16 keys in the
+//             fused kernel's order 0, 1, 4, 5, 2, 3, 6, 7; V tiles MN-major
+//             in shared memory), O rescaled in
 //             TMEM by alpha before each tile's product, then O * (1 / l)
 //             rounded once to bf16.
 // The intermediates are materialised in caller-owned buffers:
@@ -585,9 +586,12 @@ __global__ void __launch_bounds__(kThreads, 1) av_gemm_kernel(const __grid_const
                 // shared memory), B = V MN-major, k-steps in the same order
                 const uint32_t dv = stage_v(s), dp = stage_p(s);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
+                for (int i = 0; i < 8; ++i) {
+                    // the fused kernel's k-step order: 0, 1, 4, 5, then 2, 3, 6, 7
+                    const int kk = 2 * (i >> 2) + (i & 1) + 4 * ((i >> 1) & 1);
                     mma_ss(tmem, sdesc_sw128(dp + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
                            sdesc_sw128(dv + kk * 2048, kBoxBytes, 1024), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
                 mma_commit(bar_o);
                 mma_commit(bar_empty + 8 * s);
             }
