@@ -145,8 +145,9 @@ __device__ __forceinline__ void q_tile(const Geom& g, int i, int& q0, int& q_end
 //   chain Y: S^T_0, S^T_1, dP^T_0; per tile i: dP^T_{i+1} (once the warps
 //            have read S^T_{i+1}), then S^T_{i+2} into R_{i & 1} (once
 //            chain X reports dV_i and dK_i complete there);
-//   chain X: per tile i: dV_i and dK_i (once P^T_i and dS^T_i are written),
-//            then a commit that frees R_{i & 1}.
+//   chain X: per tile i: dV_i once the warps have written P^T_i (before they
+//            form dS^T_i), dK_i once dS^T_i is written, then a commit that
+//            frees R_{i & 1}.
 // So the next tile's scores are ready before its warps need them, and the
 // warps form P^T_{i+1} while dV_i, dK_i and dP^T_{i+1} run.
 // Shared memory: K, V, three Q slots (Q_i is still read by dK_i when
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc_kernel(const _
     const uint32_t bar_done = sbar + 152;
     const uint32_t bar_drain = sbar + 160;   // [2]
     const uint32_t bar_rf = sbar + 176;      // [2] region consumed by dV and dK
+    const uint32_t bar_pt = sbar + 192;      // [2] P^T written (kEwThreads arrivals)
 
     if (tid == 0) {
         abort_flag = 0;
@@ -250,6 +252,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc_kernel(const _
             mbar_init(bar_sr + 8 * j, kEwThreads);
             mbar_init(bar_dp + 8 * j, 1);
             mbar_init(bar_pds + 8 * j, kEwThreads);
+            mbar_init(bar_pt + 8 * j, kEwThreads);
         }
         mbar_init(bar_done, 1);
         mbar_init(bar_drain, 1);
@@ -339,7 +342,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc_kernel(const _
                 auto issue_scores = [&](int i, bool dp) {
                     const uint32_t at = dp ? sV : sK, bt = dp ? slot_o(i) : slot_q(i);
                     const uint32_t d = tmem + kColR + 128u * (uint32_t)(i & 1);
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ss(d, desc_kmajor(at, kk), desc_kmajor(bt, kk), kIdescKK, kk > 0);
                     mma_commit((dp ? bar_dp : bar_st) + 8 * (i & 1));
@@ -390,17 +393,23 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc_kernel(const _
                     for (int i = 0; ok && i < nq; ++i) {
                         const int r = i & 1;
                         const uint32_t reg = tmem + kColR + 128u * (uint32_t)r;
+                        // dV_i once P^T_i is written, dK_i once dS^T_i is
+                        if (!mbar_wait(bar_pt + 8 * r, (i >> 1) & 1, &abort_flag, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ts(tmem + kColDV, reg + p_col(kk), desc_mnmajor(slot_o(i), kk), kIdescKM,
+                                   (i > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(bar_oe + 8 * (i & 1));
                         if (!mbar_wait(bar_pds + 8 * r, (i >> 1) & 1, &abort_flag, kWaitLimitNs)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-    #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            mma_ts(tmem + kColDV, reg + p_col(kk), desc_mnmajor(slot_o(i), kk), kIdescKM,
-                                   (i > 0 || kk > 0) ? 1u : 0u);
-                        mma_commit(bar_oe + 8 * (i & 1));
-    #pragma unroll
+#pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
                             mma_ts(tmem + kColDK, reg + ds_col(kk), desc_mnmajor(slot_q(i), kk), kIdescKM,
                                    (i > 0 || kk > 0) ? 1u : 0u);
@@ -496,6 +505,9 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc_kernel(const _
 #pragma unroll
                     for (int e = 0; e < kEwCols / 2; ++e) pkp[e] = pack_bf16(pf[2 * e], pf[2 * e + 1]);
                     tmem_st32(reg, *reinterpret_cast<const uint32_t(*)[32]>(&pkp[0]));
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(bar_pt + 8 * r);
                 }
 #pragma unroll
                 for (int e4 = 0; e4 < 8; ++e4) {
