@@ -66,6 +66,9 @@ constexpr int kSmemV = 4 * kTileBytes;        // 2 slots
 constexpr int kSmemBytes = 6 * kTileBytes + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// the producer's slot waits sleep this long per failed poll, leaving its
+// SMSP's issue slots to the softmax warps (424.1 -> 422.7 us)
+constexpr uint32_t kProducerSleepNs = 512;
 constexpr float kC = (float)(1.4426950408889634 * 0.08838834764831845);  // log2(e) / sqrt(128)
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -245,7 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             int k_issued = 0, v_issued = 0;
             for (int j = 0; j < nkt && !abort_flag; ++j) {
                 const int s = j & 1;
-                if (j >= 2 && !mbar_wait(bar_ke + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                if (j >= 2 &&
+                    !mbar_wait_backoff(bar_ke + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs, kProducerSleepNs)) {
                     fail(&abort_flag);
                     break;
                 }
@@ -255,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                 tma_load_2d(dk, &a.map_k, bar_kf + 8 * s, 0, row_base + ti.k0);
                 tma_load_2d(dk + kBoxBytes, &a.map_k, bar_kf + 8 * s, 64, row_base + ti.k0);
                 k_issued = j + 1;
-                if (j >= 2 && !mbar_wait(bar_ve + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs)) {
+                if (j >= 2 &&
+                    !mbar_wait_backoff(bar_ve + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs, kProducerSleepNs)) {
                     fail(&abort_flag);
                     break;
                 }
