@@ -249,7 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
             for (int j = 0; j < nkt && !abort_flag; ++j) {
                 const int s = j & 1;
                 if (j >= 2 &&
-                    !mbar_wait_backoff(bar_ke + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs, kProducerSleepNs)) {
+                    !mbar_wait_backoff(bar_ke + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs,
+                                       kProducerSleepNs)) {
                     fail(&abort_flag);
                     break;
                 }
@@ -260,7 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
                 tma_load_2d(dk + kBoxBytes, &a.map_k, bar_kf + 8 * s, 64, row_base + ti.k0);
                 k_issued = j + 1;
                 if (j >= 2 &&
-                    !mbar_wait_backoff(bar_ve + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs, kProducerSleepNs)) {
+                    !mbar_wait_backoff(bar_ve + 8 * s, ((j >> 1) + 1) & 1, &abort_flag, kWaitLimitNs,
+                                       kProducerSleepNs)) {
                     fail(&abort_flag);
                     break;
                 }
