@@ -12,15 +12,19 @@
 //              threads of a row trade their halves' maxima (and the previous
 //              tile's half sums) through shared memory, keep a reference max
 //              m and the sum l (FP32, log2 units), write P = exp2(s - m) as
-//              bf16 back over S and rescale their half of O in TMEM when m
-//              moves (only when the row max has grown by more than 2^8).
+//              bf16 back over S in two chunks (the half's first 32 keys,
+//              then its last 32), each handed to the MMA once written, and
+//              rescale their half of O in TMEM when m moves (only when the
+//              row max has grown by more than 2^8) before the first chunk.
 //              Epilogue: O / l, one bf16 cast, and lse.
 //   warp 16    TMA producer: Q tiles once, then K and V tiles (two slots
 //              each; a K slot frees when its S products are done, a V slot
 //              when its PV products are done).
 //   warp 17    MMA issuer (one thread) and TMEM owner, per key tile j:
-//              PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) -- while one group runs
-//              its softmax the tensor core works for the other.
+//              PV_A(j) over key chunk 0 (k-steps 0, 1, 4, 5), then over key
+//              chunk 1 (2, 3, 6, 7), S_A(j+1), and the same for tile B --
+//              while one group runs its softmax the tensor core works for
+//              the other.
 // TMEM: S_A [0,128), O_A [128,256), S_B [256,384), O_B [384,512).
 // A CTA runs tile A alone (group B idle) for a segment's odd last tile, and
 // for the pairs past the grid's last full wave, which run as two single-tile
