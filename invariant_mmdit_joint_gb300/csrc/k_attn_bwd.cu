@@ -23,6 +23,8 @@
 // backward preprocess in a tile-padded layout (one 128-slot block per query
 // tile; slots past a segment hold lse2 = +inf and Delta = 0, so their P is
 // exactly 0). Every wait is bounded (RLK_ERR_DEVICE_TIMEOUT on give-up).
+#include <atomic>
+
 #include "rlk_device.cuh"
 #include "rlk_internal.h"
 #include "rlk_normrope_bwd.cuh"
@@ -841,10 +843,17 @@ cudaError_t launch_attn_bwd_dkdv(const Geom& g, const ValidLen& vl, const uint16
     // the warpgroups' register split adds up to kKvRegs per launched thread:
     // a build at any other count would leave the elementwise warps waiting
     // for registers that are not there, so it is not launched
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_bwd_dkdv_tc_kernel);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != kKvRegs) return cudaErrorInvalidConfiguration;
+    // (a successful lookup is kept: every device runs the same build)
+    static std::atomic<int> regs_at_launch{0};
+    int regs = regs_at_launch.load(std::memory_order_relaxed);
+    if (regs == 0) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, attn_bwd_dkdv_tc_kernel);
+        if (e != cudaSuccess) return e;
+        regs = fa.numRegs;
+        regs_at_launch.store(regs, std::memory_order_relaxed);
+    }
+    if (regs != kKvRegs) return cudaErrorInvalidConfiguration;
     dim3 grid(g.ntq_txt + g.ntq_img, n_pairs);
     timing_begin(kKBwdDkDv, s);
     attn_bwd_dkdv_tc_kernel<<<grid, kKvThreads, kKvSmemBytes, s>>>(args);
