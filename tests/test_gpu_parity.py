@@ -114,6 +114,11 @@ EDGE = [
     Hh.workload("exact", 2, 2, 64, 16, 16, (64, 1)),
     # inputs scaled by 3
     Hh.workload("scaled", 1, 2, 24, 10, 10, (9,), scale=3.0),
+    # the valid text length ending at and around every edge the kernels
+    # split a 128-key tile at (the softmax threads' 64-key halves, their
+    # 32-key P chunks, the 16-key k-steps), in two text tiles
+    Hh.workload("mask_edges", 16, 2, 256, 8, 9,
+                (0, 1, 15, 16, 31, 32, 33, 63, 64, 65, 95, 96, 97, 127, 128, 129)),
 ]
 
 

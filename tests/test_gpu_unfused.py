@@ -58,6 +58,8 @@ SMALL = [
     # two text tiles (the second partly padded), a ragged 13 x 21 image,
     # a sample with no valid text key and one whose last text tile holds 2
     Hh.workload("ragged", 3, 2, 200, 13, 21, (0, 130, 200)),
+    # the valid text length at and around the tile's half, chunk and k-step edges
+    Hh.workload("mask_edges", 14, 1, 256, 8, 9, (1, 15, 16, 31, 32, 33, 63, 64, 65, 95, 96, 97, 127, 129)),
 ]
 
 
